@@ -1,0 +1,453 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged-attention engine step on GB300.
+
+A step is one pass of the whole hot path over one batch: for each of the 28
+layers of a Qwen2.5-1.5B-shaped decode step (64 requests, context 512, Hq=12,
+Hkv=2, D=128, 16-token blocks, each layer its own 1.25x pool with shuffled
+blocks), append this step's K/V through the slot mapping, then run paged
+attention.  The 56 launches are captured once in a CUDA graph and replayed.
+
+Prints one JSON line (rank 0).  ``value`` is algorithmic HBM bytes (KV read +
+q read + out write + append traffic) per second over all ranks; the pools of
+one step (1.2 GB) exceed L2, so every step streams from HBM.
+
+``--impl reference`` times the fp64 CPU oracle on bounded samples of the same
+workload on the host cores instead (the reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from paged_kv_cache_195_gb300 import roofline as rl  # noqa: E402
+from paged_kv_cache_195_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "paged-attention step: KV GB/s and % of GB300 HBM peak; attended tokens/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+DECODE_SRC = os.path.join(ROOT, "paged_kv_cache_195_gb300", "csrc", "pkv_decode.cu")
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def committed_traffic():
+    """Per-launch DRAM bytes of the decode kernel from the committed ncu
+    summary, if it was taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "decode_kernel_qwen_decode.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    src_sha = hashlib.sha256(open(DECODE_SRC, "rb").read()).hexdigest()[:16]
+    m_sha = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+    if m_sha and m_tr and m_sha.group(1) == src_sha:
+        return int(m_tr.group(1))
+    return None
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+
+def nvsmi_id(local_rank: int) -> str:
+    """nvidia-smi --id for this process's GPU (honours CUDA_VISIBLE_DEVICES)."""
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "").strip()
+    if vis:
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        if local_rank < len(ids):
+            return ids[local_rank]
+    return str(local_rank)
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.strip()]
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+                for name, v in zip(names, r[5:9]):
+                    if v.strip().lower() == "active":
+                        reasons.add(name)
+            except (ValueError, IndexError):
+                continue
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# raw CUDA events recorded as graph nodes (cudaEventRecordExternal)
+# ---------------------------------------------------------------------------
+
+class GraphEvents:
+    def __init__(self, n):
+        self.rt = ctypes.CDLL("libcudart.so.13")
+        self.rt.cudaEventCreate.argtypes = [ctypes.POINTER(ctypes.c_void_p)]
+        self.rt.cudaEventRecordWithFlags.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint]
+        self.rt.cudaEventElapsedTime.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_void_p,
+                                                 ctypes.c_void_p]
+        self.ev = []
+        for _ in range(n):
+            e = ctypes.c_void_p()
+            assert self.rt.cudaEventCreate(ctypes.byref(e)) == 0
+            self.ev.append(e)
+
+    def record(self, i, stream):
+        assert self.rt.cudaEventRecordWithFlags(self.ev[i], ctypes.c_void_p(stream.cuda_stream), 1) == 0
+
+    def elapsed_ms(self, a, b):
+        ms = ctypes.c_float()
+        assert self.rt.cudaEventElapsedTime(ctypes.byref(ms), self.ev[a], self.ev[b]) == 0
+        return ms.value
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def build_layers(shape, device, rank):
+    layers = []
+    for layer in range(shape.layers):
+        inp = wl.make_step(shape, device=device, layer=layer + 1000 * rank)
+        layers.append(inp)
+    return layers
+
+
+def run_ours(args):
+    import paged_kv_cache_195_gb300 as pkv
+    from paged_kv_cache_195_gb300 import build as pkv_build
+
+    ws_n, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if ws_n > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    if rank == 0 or ws_n == 1:
+        pkv_build.build()
+    if ws_n > 1:
+        torch.distributed.barrier()
+        pkv_build.build()
+    pkv.load_library()
+
+    shape = wl.CONFIGS[args.config]()
+    layers = build_layers(shape, device, rank)
+    L0 = layers[0]
+    dims = pkv.make_dims(tuple(L0.q.shape), tuple(L0.k_pool.shape), shape.num_reqs,
+                         shape.max_blocks_per_req)
+    ws = pkv.Workspace(dims, device=device)
+    pkv.pkv_workspace_init(ws, dims)
+    outs = [torch.empty_like(x.q) for x in layers]
+
+    att = rl.attention_bytes(shape.seq_lens, shape.q_lens, shape.num_q_heads, shape.num_kv_heads)
+    app = rl.append_bytes(shape.num_q_tokens, shape.num_kv_heads)
+    bytes_per_layer = att["total"] + app
+    bytes_per_step = bytes_per_layer * shape.layers
+    tokens_per_step = rl.attended_tokens(shape.seq_lens, shape.q_lens) * shape.layers
+
+    stream = torch.cuda.Stream(device)
+    gev = GraphEvents(2 * shape.layers)
+
+    def step(events=False):
+        s = torch.cuda.current_stream(device)
+        for li, x in enumerate(layers):
+            pkv.pkv_append(x.k_new, x.v_new, x.slot_mapping, x.k_pool, x.v_pool)
+            if events:
+                gev.record(2 * li, s)
+            pkv.pkv_attention(x.q, x.k_pool, x.v_pool, x.block_tables, x.seq_lens,
+                              x.query_start_loc, x.scale, out=outs[li], workspace=ws)
+            if events:
+                gev.record(2 * li + 1, s)
+
+    # eager warm-up (module load, attribute set-up), then capture
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize(device)
+    assert pkv.pkv_get_device_error() == 0, pkv.pkv_last_error()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    graph_ev = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_ev, stream=stream):
+        step(events=True)
+
+    # e2e: pinned host inputs -> device, the step, result -> pinned host
+    host_in = []
+    for x in layers:
+        host_in.append({k: getattr(x, k).cpu().pin_memory() for k in
+                        ("q", "k_new", "v_new", "slot_mapping", "block_tables", "seq_lens",
+                         "query_start_loc")})
+    host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    h2d = sum(t.numel() * t.element_size() for d in host_in for t in d.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    graph_e2e = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_e2e, stream=stream):
+        for x, hin in zip(layers, host_in):
+            for k, t in hin.items():
+                getattr(x, k).copy_(t, non_blocking=True)
+        step()
+        for o, ho in zip(outs, host_out):
+            ho.copy_(o, non_blocking=True)
+
+    def barrier():
+        if ws_n > 1:
+            torch.distributed.barrier()
+
+    def timed(g, k):
+        for _ in range(args.warmup):
+            g.replay()
+        torch.cuda.synchronize(device)
+        barrier()
+        torch.cuda.synchronize(device)
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(k):
+                g.replay()
+        t1.record(stream)
+        torch.cuda.synchronize(device)
+        barrier()
+        ms = t0.elapsed_time(t1)
+        if ws_n > 1:
+            tt = torch.tensor([ms], device=device)
+            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+            ms = float(tt.item())
+        return ms
+
+    clocks = ClockSampler(nvsmi_id(local))
+    clocks.start()
+    ms_total = timed(graph, args.steps)
+    clock_info = clocks.stop()
+    ms_step = ms_total / args.steps
+
+    # roofline pass: the same graph with event nodes around every attention
+    # kernel; per-launch durations averaged over the replays
+    durs = []
+    n_rep = max(3, min(args.steps, 200))
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph_ev.replay()
+        for _ in range(n_rep):
+            graph_ev.replay()
+            stream.synchronize()
+            durs.extend(gev.elapsed_ms(2 * li, 2 * li + 1) for li in range(shape.layers))
+    kernel_ms = statistics.mean(durs)
+
+    e2e_ms = timed(graph_e2e, max(1, args.steps // 4)) / max(1, args.steps // 4)
+    assert pkv.pkv_get_device_error() == 0, pkv.pkv_last_error()
+
+    peak, peak_src = measured_peak()
+    value = bytes_per_step * ws_n / (ms_step * 1e-3) / 1e9
+    achieved = att["total"] / (kernel_ms * 1e-3) / 1e9
+    traffic = committed_traffic()
+    cpu = cpu_baseline(shape, layers, args) if (rank == 0 and ws_n == 1 and not args.no_cpu) else None
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws_n,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 K/V/q, shuffled block placement; no weights)",
+        "config": {
+            "workload": f"{shape.name} x{shape.layers} layers",
+            "num_reqs": shape.num_reqs, "context": int(shape.seq_lens[0]),
+            "q_tokens_per_req": int(shape.q_lens[0]), "layers": shape.layers,
+            "num_q_heads": shape.num_q_heads, "num_kv_heads": shape.num_kv_heads,
+            "head_dim": shape.head_dim, "block_size": shape.block_size,
+            "pool_blocks_per_layer": shape.num_blocks, "parallelism": f"replicas x{ws_n}",
+            "l2": f"inputs exceed L2: {shape.layers} distinct pools, "
+                  f"{2 * shape.layers * shape.num_blocks * shape.num_kv_heads * 4096 / 1e9:.2f} GB per step",
+            "launch": "CUDA graph of 28 x (append + attention)",
+        },
+        "attended_tokens_per_s": round(tokens_per_step * ws_n / (ms_step * 1e-3), 1),
+        "us_per_layer": round(ms_step * 1e3 / shape.layers, 3),
+        "frac_of_nominal_8tbs": round(value / ws_n / NOMINAL_HBM_GBS, 4),
+        "roofline": {
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": traffic,
+            "kernel": "pkv::decode_kernel<6>", "algorithmic_bytes_per_launch": att["total"],
+            "avg_launch_us": round(kernel_ms * 1e3, 3), "peak_source": peak_src,
+            "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
+        },
+        "e2e": {"value": round(bytes_per_step * ws_n / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 2 * shape.layers * args.steps,
+        "clocks": clock_info,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws_n > 1:
+        torch.distributed.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline / reference arm: the fp64 oracle on bounded samples
+# ---------------------------------------------------------------------------
+
+def _oracle_sample(shape, inp_host, n_reqs):
+    """Oracle attention for the first n_reqs requests of one layer."""
+    import oracle
+    qsl = inp_host["qsl"]
+    sub_qsl = qsl[:n_reqs + 1]
+    t = int(sub_qsl[-1])
+    return oracle.paged_attention(inp_host["q"][:t], inp_host["k_pool"], inp_host["v_pool"],
+                                  inp_host["block_tables"][:n_reqs], inp_host["seq_lens"][:n_reqs],
+                                  sub_qsl, inp_host["scale"])
+
+
+def _host_layer(inp):
+    return dict(q=wl.bf16_bits(inp.q), k_pool=wl.bf16_bits(inp.k_pool),
+                v_pool=wl.bf16_bits(inp.v_pool), block_tables=inp.block_tables.cpu().numpy(),
+                seq_lens=inp.seq_lens.cpu().numpy(), qsl=inp.query_start_loc.cpu().numpy(),
+                scale=inp.scale)
+
+
+def cpu_baseline(shape, layers, args, budget_s=10.0):
+    import oracle
+    oracle.build()
+    host = [_host_layer(x) for x in layers[:4]]
+    done_bytes, t_total, n_calls = 0, 0.0, 0
+    per_req = rl.attention_bytes(shape.seq_lens[:1], shape.q_lens[:1], shape.num_q_heads,
+                                 shape.num_kv_heads)["total"]
+    t0 = time.perf_counter()
+    while t_total < budget_s:
+        h = host[n_calls % len(host)]
+        t1 = time.perf_counter()
+        _oracle_sample(shape, h, shape.num_reqs)
+        t_total += time.perf_counter() - t1
+        done_bytes += per_req * shape.num_reqs
+        n_calls += 1
+    return {"value": round(done_bytes / t_total / 1e9, 4), "unit": "GB/s",
+            "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"{n_calls} full layers ({shape.num_reqs} requests each) of {shape.name}, "
+                      f"fp64 C oracle, OpenMP, {t_total:.1f} s wall",
+            "wall_s": round(time.perf_counter() - t0, 2)}
+
+
+def run_reference(args):
+    ws_n, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    shape = wl.CONFIGS[args.config]()
+    # inputs generated on the host (same seeded recipe as the GPU arm)
+    n_layers = min(shape.layers, 2)
+    host = [_host_layer(wl.make_step(shape, device="cpu", layer=li)) for li in range(n_layers)]
+    per_req = rl.attention_bytes(shape.seq_lens[:1], shape.q_lens[:1], shape.num_q_heads,
+                                 shape.num_kv_heads)["total"]
+    # size each step so that warm-up + timed steps fit in about a minute
+    t1 = time.perf_counter()
+    _oracle_sample(shape, host[0], 1)
+    one = max(1e-4, time.perf_counter() - t1)
+    budget = 60.0 / max(1, args.steps + args.warmup)
+    n_reqs = int(max(1, min(shape.num_reqs, budget / one)))
+    for i in range(args.warmup):
+        _oracle_sample(shape, host[i % n_layers], n_reqs)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        _oracle_sample(shape, host[i % n_layers], n_reqs)
+    dt = time.perf_counter() - t0
+    value = per_req * n_reqs * args.steps / dt / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": ws_n, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3 / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{shape.name} x{shape.layers} layers", "num_reqs": shape.num_reqs,
+                   "context": int(shape.seq_lens[0]), "layers": shape.layers},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.max_threads(),
+                         "kind": "oracle",
+                         "sample": f"each step: attention of {n_reqs} of {shape.num_reqs} "
+                                   f"requests of one layer, fp64 C oracle"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="qwen_decode", choices=sorted(wl.CONFIGS))
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,153 @@
+/*
+ * pagedkv.h -- C ABI of libpagedkv.so: one engine step of attention over a
+ * paged (block-tabled) KV cache, for NVIDIA GB300 (sm_103a).
+ *
+ * The problem these calls solve is the one of a continuously batched serving
+ * step.  The running requests form a ragged batch: each contributes one query
+ * token (decode) or a chunk of query tokens (chunked prefill), flattened into
+ * one [tokens, heads, head_dim] tensor with per-request offsets
+ * (query_start_loc), the interface a variable-length attention kernel offers
+ * (The Serving Playbook, "Continuous batching").  Each request's keys and
+ * values live in fixed-size blocks of one shared pool, found through the
+ * request's block table (The Serving Playbook, "Paged KV cache"; LLM 7 -
+ * Efficient LLM Serving, sec. 3 "Paging the Cache").  A serving step first
+ * writes this step's K/V into the cache through a slot mapping, then attends
+ * (The Serving Playbook, "CUDA graphs and the CPU you forgot about", which
+ * lists block tables and slot mappings among the preallocated step buffers).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Element type: bf16 for q, K/V rows, pools and out.  head_dim = 128 and
+ *   block_size = 16 are the supported shapes; num_q_heads must be a multiple
+ *   of num_kv_heads with a group size g = num_q_heads / num_kv_heads of 1..8.
+ * - Layouts (row-major, contiguous):
+ *     q, out        [num_q_tokens, num_q_heads, head_dim]
+ *     k_new, v_new  [num_new_tokens, num_kv_heads, head_dim]
+ *     k_pool,v_pool [num_blocks, num_kv_heads, block_size, head_dim]
+ *                   -- one (block, KV head) pair is one contiguous 4 KiB tile
+ *     block_tables  [num_reqs, max_blocks_per_req] int32
+ *     seq_lens      [num_reqs] int32: L_r, INCLUDING this step's tokens
+ *     query_start_loc [num_reqs + 1] int32: query rows of request r are
+ *                   query_start_loc[r] .. query_start_loc[r+1]-1
+ *     slot_mapping  [num_new_tokens] int64: block * block_size + offset
+ * - Query head h reads KV head h / g.  Query i of request r (q_r queries)
+ *   sits at position L_r - q_r + i and attends to keys 0 .. L_r - q_r + i.
+ * - Ownership: every pointer is device memory owned by the caller; the
+ *   library never frees or keeps it.  All calls are asynchronous on the given
+ *   stream and never synchronise it (except pkv_get_device_error).
+ * - All device pointers must be 16-byte aligned.
+ * - Return codes: PKV_OK or a negative PKV_ERR_*; pkv_last_error() gives a
+ *   message (thread-local).  Device-side violations (a block id outside the
+ *   pool, inconsistent lengths) are skipped by the kernels and recorded in a
+ *   per-device error word that pkv_get_device_error() reads and clears.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PKV_OK 0
+#define PKV_ERR_INVALID (-1)      /* null pointer, bad dims, misalignment */
+#define PKV_ERR_UNSUPPORTED (-2)  /* head_dim, block_size, group size, too many requests */
+#define PKV_ERR_WORKSPACE (-3)    /* workspace smaller than pkv_attention_workspace_size */
+#define PKV_ERR_CUDA (-4)         /* a CUDA runtime call or launch failed */
+#define PKV_ERR_DEVICE_BOUNDS (-5) /* reported later: block id or lengths out of range */
+#define PKV_ERR_TIMEOUT (-6)      /* reported later: a bounded device wait ran out */
+
+/* Upper bound on num_reqs for pkv_attention (its per-request plan lives in
+ * shared memory). */
+#define PKV_MAX_REQS 4096
+
+typedef struct pkv_dims {
+    int32_t num_reqs;           /* R */
+    int32_t num_q_tokens;       /* Tq = query_start_loc[R] */
+    int32_t num_q_heads;        /* Hq */
+    int32_t num_kv_heads;       /* Hkv */
+    int32_t head_dim;           /* D, must be 128 */
+    int32_t block_size;         /* bs, must be 16 */
+    int32_t num_blocks;         /* physical blocks in each pool */
+    int32_t max_blocks_per_req; /* columns of block_tables */
+} pkv_dims;
+
+/*
+ * KV append (the step's cache write).  For each new token t with
+ * slot_mapping[t] >= 0, copies k_new[t, :, :] into k_pool[slot / bs, :,
+ * slot % bs, :] and v_new likewise, bit for bit.  Negative slots are padding
+ * and are skipped.  A slot >= num_blocks * bs is skipped and recorded as
+ * PKV_ERR_DEVICE_BOUNDS.  Duplicate slots are a caller error (the last writer
+ * is unspecified).  Only dims->num_kv_heads, head_dim, block_size and
+ * num_blocks are read.
+ * Source: LLM 7 - Efficient LLM Serving, sec. 3 "What the Cache Stores" (the
+ * new token's K and V join the cache each step); The Serving Playbook, "CUDA
+ * graphs and the CPU you forgot about" (slot mappings as a step buffer).
+ */
+int pkv_append(const void *k_new, const void *v_new, const int64_t *slot_mapping,
+               void *k_pool, void *v_pool, int32_t num_new_tokens,
+               const pkv_dims *dims, cudaStream_t stream);
+
+/*
+ * Bytes of workspace pkv_attention needs for these dims (split-context
+ * partial outputs, their log-sum-exp statistics and per-row merge counters).
+ * Depends only on dims and the device's SM count, not on the lengths, so one
+ * buffer serves every step of a captured CUDA graph.
+ */
+size_t pkv_attention_workspace_size(const pkv_dims *dims);
+
+/*
+ * Zeroes the merge counters at the head of a workspace (a stream-ordered
+ * memset).  Call once after allocating a workspace; pkv_attention leaves the
+ * counters at zero when it finishes, so later calls need no re-initialisation.
+ */
+int pkv_workspace_init(void *workspace, size_t workspace_bytes,
+                       const pkv_dims *dims, cudaStream_t stream);
+
+/*
+ * Attention for one engine step.  For every request r and query i < q_r
+ * (row t = query_start_loc[r] + i) and query head h:
+ *     out[t, h, :] = sum_j softmax_j(scale * <q[t,h,:], K_r[j, h/g, :]>) V_r[j, h/g, :]
+ * over keys j = 0 .. L_r - q_r + i, where K_r[j] = k_pool[block_tables[r,
+ * j/bs], :, j%bs, :].  Computed with fp32 accumulation and an online softmax;
+ * long contexts are split across CTAs and merged by log-sum-exp (Flash-
+ * Decoding); prefill chunks run on tcgen05 tensor cores.  out is written as
+ * bf16 (round to nearest even).  Requests with q_r = 0 produce nothing.
+ * Preconditions: query_start_loc[0] = 0, non-decreasing, last entry =
+ * num_q_tokens; 0 <= q_r <= L_r <= max_blocks_per_req * bs; table entries
+ * b < ceil(L_r / bs) are in [0, num_blocks).  Violations found on the device
+ * skip the affected work and are reported by pkv_get_device_error.
+ * workspace: at least pkv_attention_workspace_size(dims) bytes, initialised
+ * once with pkv_workspace_init; NULL makes the library use an internal
+ * per-device buffer (allocated on first use: not capturable in a CUDA graph,
+ * and not safe for concurrent calls on different streams).
+ * Source: The Serving Playbook, "The block table lives in the hottest kernel
+ * in the system" (gather through the table, partial softmax per piece of the
+ * cache, rescaling pass), "Kernel fusion, briefly" (Flash-Decoding splits the
+ * KV axis), "Chunked prefill" (causal chunk over earlier chunks' KV); LLM 7,
+ * sec. 2 "Online Softmax Makes Tiling Possible".
+ */
+int pkv_attention(const void *q, const void *k_pool, const void *v_pool,
+                  const int32_t *block_tables, const int32_t *seq_lens,
+                  const int32_t *query_start_loc, float scale, void *out,
+                  const pkv_dims *dims, void *workspace, size_t workspace_bytes,
+                  cudaStream_t stream);
+
+/* Message of the last failing call on this thread ("" if none). */
+const char *pkv_last_error(void);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's error
+ * word.  Returns PKV_OK, PKV_ERR_DEVICE_BOUNDS, PKV_ERR_TIMEOUT (a timeout
+ * takes precedence) or PKV_ERR_CUDA.
+ */
+int pkv_get_device_error(cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

@@ -1,0 +1,195 @@
+"""ctypes binding of libpagedkv.so -- argument marshalling only.
+
+Every function here checks the tensors it is given (device, dtype, shape,
+contiguity), turns them into raw pointers and calls the C ABI declared in
+``include/pagedkv.h``.  All computation runs in the library's CUDA kernels;
+there is no fallback of any kind: if the library is missing, calls raise.
+PyTorch supplies device memory and streams, nothing else.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libpagedkv.so")
+
+PKV_OK = 0
+PKV_ERR_INVALID = -1
+PKV_ERR_UNSUPPORTED = -2
+PKV_ERR_WORKSPACE = -3
+PKV_ERR_CUDA = -4
+PKV_ERR_DEVICE_BOUNDS = -5
+PKV_ERR_TIMEOUT = -6
+
+EXPORTED = ("pkv_append", "pkv_attention", "pkv_attention_workspace_size",
+            "pkv_workspace_init", "pkv_last_error", "pkv_get_device_error")
+
+
+class PagedKVError(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"libpagedkv error {code}: {message}")
+        self.code = code
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("num_reqs", ctypes.c_int32), ("num_q_tokens", ctypes.c_int32),
+                ("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("num_blocks", ctypes.c_int32), ("max_blocks_per_req", ctypes.c_int32)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libpagedkv.so and declare its signatures (raises if absent)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is not built: run paged_kv_cache_195_gb300.build.build() "
+                "(the CUDA library is required; there is no fallback)")
+        lib = ctypes.CDLL(path)
+        vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+        dp = ctypes.POINTER(Dims)
+        lib.pkv_append.argtypes = [vp, vp, vp, vp, vp, i32, dp, vp]
+        lib.pkv_append.restype = ctypes.c_int
+        lib.pkv_attention.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, dp, vp, sz, vp]
+        lib.pkv_attention.restype = ctypes.c_int
+        lib.pkv_attention_workspace_size.argtypes = [dp]
+        lib.pkv_attention_workspace_size.restype = sz
+        lib.pkv_workspace_init.argtypes = [vp, sz, dp, vp]
+        lib.pkv_workspace_init.restype = ctypes.c_int
+        lib.pkv_last_error.argtypes = []
+        lib.pkv_last_error.restype = ctypes.c_char_p
+        lib.pkv_get_device_error.argtypes = [vp]
+        lib.pkv_get_device_error.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def pkv_last_error() -> str:
+    return load_library().pkv_last_error().decode()
+
+
+def _check(rc: int):
+    if rc != PKV_OK:
+        raise PagedKVError(rc, pkv_last_error())
+
+
+def _stream(stream, device) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype, ndim: int):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got shape {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def make_dims(q_shape, pool_shape, num_reqs: int, max_blocks_per_req: int) -> Dims:
+    Tq, Hq, D = q_shape
+    nb, Hkv, bs, D2 = pool_shape
+    return Dims(num_reqs, Tq, Hq, Hkv, D, bs, nb, max_blocks_per_req)
+
+
+def pkv_attention_workspace_size(dims: Dims) -> int:
+    return int(load_library().pkv_attention_workspace_size(ctypes.byref(dims)))
+
+
+class Workspace:
+    """A zero-initialised device workspace for pkv_attention (reusable)."""
+
+    def __init__(self, dims: Dims, device="cuda"):
+        self.nbytes = pkv_attention_workspace_size(dims)
+        if self.nbytes == 0:
+            raise PagedKVError(PKV_ERR_INVALID, pkv_last_error() or "bad dims")
+        self.buf = torch.zeros(self.nbytes + 256, dtype=torch.uint8, device=device)
+        off = (-self.buf.data_ptr()) % 256
+        self.ptr = self.buf.data_ptr() + off
+
+
+def pkv_workspace_init(ws: Workspace, dims: Dims, stream=None):
+    _check(load_library().pkv_workspace_init(ctypes.c_void_p(ws.ptr), ws.nbytes,
+                                             ctypes.byref(dims),
+                                             ctypes.c_void_p(_stream(stream, ws.buf.device))))
+
+
+def pkv_append(k_new, v_new, slot_mapping, k_pool, v_pool, stream=None):
+    """Write k_new/v_new [T, Hkv, D] bf16 into the pools at slot_mapping [T] int64."""
+    _need(k_new, "k_new", torch.bfloat16, 3)
+    _need(v_new, "v_new", torch.bfloat16, 3)
+    _need(slot_mapping, "slot_mapping", torch.int64, 1)
+    _need(k_pool, "k_pool", torch.bfloat16, 4)
+    _need(v_pool, "v_pool", torch.bfloat16, 4)
+    T = k_new.shape[0]
+    if v_new.shape != k_new.shape or slot_mapping.shape[0] != T:
+        raise ValueError("k_new, v_new and slot_mapping disagree on the token count")
+    if v_pool.shape != k_pool.shape or k_pool.shape[1] != k_new.shape[1] or \
+            k_pool.shape[3] != k_new.shape[2]:
+        raise ValueError("pool shape does not match the new rows")
+    nb, Hkv, bs, D = k_pool.shape
+    dims = Dims(0, 0, Hkv, Hkv, D, bs, nb, 0)
+    _check(load_library().pkv_append(
+        ctypes.c_void_p(k_new.data_ptr()), ctypes.c_void_p(v_new.data_ptr()),
+        ctypes.c_void_p(slot_mapping.data_ptr()), ctypes.c_void_p(k_pool.data_ptr()),
+        ctypes.c_void_p(v_pool.data_ptr()), T, ctypes.byref(dims),
+        ctypes.c_void_p(_stream(stream, k_pool.device))))
+
+
+def pkv_attention(q, k_pool, v_pool, block_tables, seq_lens, query_start_loc, scale,
+                  out=None, workspace: Workspace | None = None, stream=None):
+    """One step of paged attention; returns out [Tq, Hq, D] bf16."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_pool, "k_pool", torch.bfloat16, 4)
+    _need(v_pool, "v_pool", torch.bfloat16, 4)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    _need(query_start_loc, "query_start_loc", torch.int32, 1)
+    R = seq_lens.shape[0]
+    if query_start_loc.shape[0] != R + 1 or block_tables.shape[0] != R:
+        raise ValueError("seq_lens, query_start_loc and block_tables disagree on num_reqs")
+    if v_pool.shape != k_pool.shape or k_pool.shape[3] != q.shape[2]:
+        raise ValueError("pool / q shape mismatch")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need(out, "out", torch.bfloat16, 3)
+        if out.shape != q.shape:
+            raise ValueError("out must have q's shape")
+    dims = make_dims(tuple(q.shape), tuple(k_pool.shape), R, block_tables.shape[1])
+    ws_ptr, ws_bytes = (None, 0) if workspace is None else (workspace.ptr, workspace.nbytes)
+    _check(load_library().pkv_attention(
+        ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k_pool.data_ptr()),
+        ctypes.c_void_p(v_pool.data_ptr()), ctypes.c_void_p(block_tables.data_ptr()),
+        ctypes.c_void_p(seq_lens.data_ptr()), ctypes.c_void_p(query_start_loc.data_ptr()),
+        ctypes.c_float(scale), ctypes.c_void_p(out.data_ptr()), ctypes.byref(dims),
+        ctypes.c_void_p(ws_ptr), ws_bytes, ctypes.c_void_p(_stream(stream, q.device))))
+    return out
+
+
+def pkv_get_device_error(stream=None) -> int:
+    """Synchronise the stream; return (and clear) the device error code."""
+    dev = torch.cuda.current_device()
+    return int(load_library().pkv_get_device_error(ctypes.c_void_p(_stream(stream, dev))))
+
+
+# The names the step's calls go by in the serving literature.
+paged_kv_append = pkv_append
+paged_attention = pkv_attention

@@ -1,0 +1,262 @@
+// pkv_api.cu -- the C ABI of libpagedkv.so (declared in include/pagedkv.h):
+// argument validation, per-device state, workspace carve-up and launches.
+// No call allocates on the hot path (the NULL-workspace convenience path
+// allocates once per device), none synchronises, so a whole step can be
+// captured in a CUDA graph.
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/pagedkv.h"
+#include "pkv_internal.h"
+
+static_assert(PKV_MAX_REQS == pkv::kMaxReqs, "request limit mismatch");
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(PKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// The device error word lives in this translation unit; kernels get its
+// address as an argument.
+__device__ int g_device_error;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool ready = false;
+  int sm_count = 0;
+  int* err = nullptr;          // device address of g_device_error
+  void* own_ws = nullptr;      // the NULL-workspace convenience buffer
+  size_t own_ws_bytes = 0;
+};
+
+std::mutex g_mutex;
+DeviceState g_devices[kMaxDevices];
+
+// Per-device set-up with that device current: SM count and the address of
+// the error word.  Returns nullptr (and sets the message) on failure.
+DeviceState* device_state() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    cuda_fail(e, "cudaGetDevice");
+    return nullptr;
+  }
+  if (dev < 0 || dev >= kMaxDevices) {
+    fail(PKV_ERR_UNSUPPORTED, "device ordinal %d beyond %d", dev, kMaxDevices);
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState& st = g_devices[dev];
+  if (!st.ready) {
+    e = cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) {
+      cuda_fail(e, "cudaDeviceGetAttribute");
+      return nullptr;
+    }
+    e = cudaGetSymbolAddress(reinterpret_cast<void**>(&st.err), g_device_error);
+    if (e != cudaSuccess) {
+      cuda_fail(e, "cudaGetSymbolAddress(error word)");
+      return nullptr;
+    }
+    st.ready = true;
+  }
+  return &st;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+int check_dims(const pkv_dims* d, bool for_attention) {
+  if (d == nullptr) return fail(PKV_ERR_INVALID, "dims is NULL");
+  if (d->head_dim != pkv::kHeadDim)
+    return fail(PKV_ERR_UNSUPPORTED, "head_dim %d unsupported (only 128)", d->head_dim);
+  if (d->block_size != pkv::kBlockSize)
+    return fail(PKV_ERR_UNSUPPORTED, "block_size %d unsupported (only 16)", d->block_size);
+  if (d->num_kv_heads <= 0 || d->num_blocks < 0)
+    return fail(PKV_ERR_INVALID, "num_kv_heads %d / num_blocks %d invalid", d->num_kv_heads,
+                d->num_blocks);
+  if ((long long)d->num_blocks * d->num_kv_heads * pkv::kBlockSize > (1ll << 40))
+    return fail(PKV_ERR_INVALID, "pool too large");
+  if (!for_attention) return PKV_OK;
+  if (d->num_reqs < 0 || d->num_q_tokens < 0 || d->num_q_heads <= 0 ||
+      d->max_blocks_per_req < 0)
+    return fail(PKV_ERR_INVALID, "negative dims");
+  if (d->num_q_heads % d->num_kv_heads != 0)
+    return fail(PKV_ERR_INVALID, "num_q_heads %d not a multiple of num_kv_heads %d",
+                d->num_q_heads, d->num_kv_heads);
+  const int g = d->num_q_heads / d->num_kv_heads;
+  if (g < 1 || g > 8) return fail(PKV_ERR_UNSUPPORTED, "group size %d unsupported (1..8)", g);
+  if (d->num_reqs > pkv::kMaxReqs)
+    return fail(PKV_ERR_UNSUPPORTED, "num_reqs %d beyond %d", d->num_reqs, pkv::kMaxReqs);
+  if ((long long)d->max_blocks_per_req * pkv::kBlockSize > (1ll << 30))
+    return fail(PKV_ERR_UNSUPPORTED, "max_blocks_per_req too large");
+  return PKV_OK;
+}
+
+pkv::WorkspaceLayout layout_for(const pkv_dims* d, int sm_count) {
+  return pkv::decode_workspace_layout(d->num_q_tokens, d->num_kv_heads,
+                                      d->num_q_heads / d->num_kv_heads,
+                                      pkv::decode_target_units(sm_count));
+}
+
+int env_int(const char* name, int dflt) {
+  const char* v = getenv(name);
+  return (v && *v) ? atoi(v) : dflt;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pkv_last_error(void) { return g_last_error; }
+
+int pkv_append(const void* k_new, const void* v_new, const int64_t* slot_mapping, void* k_pool,
+               void* v_pool, int32_t num_new_tokens, const pkv_dims* dims, cudaStream_t stream) {
+  g_last_error[0] = '\0';
+  int rc = check_dims(dims, false);
+  if (rc != PKV_OK) return rc;
+  if (num_new_tokens < 0) return fail(PKV_ERR_INVALID, "num_new_tokens < 0");
+  if (num_new_tokens == 0) return PKV_OK;
+  if (!k_new || !v_new || !slot_mapping || !k_pool || !v_pool)
+    return fail(PKV_ERR_INVALID, "NULL pointer argument");
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pool) || !aligned16(v_pool))
+    return fail(PKV_ERR_INVALID, "bf16 buffers must be 16-byte aligned");
+  DeviceState* st = device_state();
+  if (!st) return PKV_ERR_CUDA;
+  pkv::AppendParams p;
+  p.k_new = static_cast<const __nv_bfloat16*>(k_new);
+  p.v_new = static_cast<const __nv_bfloat16*>(v_new);
+  p.slot_mapping = slot_mapping;
+  p.k_pool = static_cast<__nv_bfloat16*>(k_pool);
+  p.v_pool = static_cast<__nv_bfloat16*>(v_pool);
+  p.err = st->err;
+  p.num_tokens = num_new_tokens;
+  p.num_kv_heads = dims->num_kv_heads;
+  p.num_blocks = dims->num_blocks;
+  cudaError_t e = pkv::launch_append(p, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "append launch");
+  return PKV_OK;
+}
+
+size_t pkv_attention_workspace_size(const pkv_dims* dims) {
+  if (check_dims(dims, true) != PKV_OK) return 0;
+  DeviceState* st = device_state();
+  if (!st) return 0;
+  return layout_for(dims, st->sm_count).total;
+}
+
+int pkv_workspace_init(void* workspace, size_t workspace_bytes, const pkv_dims* dims,
+                       cudaStream_t stream) {
+  g_last_error[0] = '\0';
+  int rc = check_dims(dims, true);
+  if (rc != PKV_OK) return rc;
+  DeviceState* st = device_state();
+  if (!st) return PKV_ERR_CUDA;
+  const pkv::WorkspaceLayout w = layout_for(dims, st->sm_count);
+  if (workspace == nullptr || workspace_bytes < w.total)
+    return fail(PKV_ERR_WORKSPACE, "workspace %zu bytes, need %zu", workspace_bytes, w.total);
+  cudaError_t e = cudaMemsetAsync(workspace, 0, w.ml_off, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(workspace counters)");
+  return PKV_OK;
+}
+
+int pkv_attention(const void* q, const void* k_pool, const void* v_pool,
+                  const int32_t* block_tables, const int32_t* seq_lens,
+                  const int32_t* query_start_loc, float scale, void* out, const pkv_dims* dims,
+                  void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  g_last_error[0] = '\0';
+  int rc = check_dims(dims, true);
+  if (rc != PKV_OK) return rc;
+  if (dims->num_reqs == 0 || dims->num_q_tokens == 0) return PKV_OK;
+  if (!q || !k_pool || !v_pool || !block_tables || !seq_lens || !query_start_loc || !out)
+    return fail(PKV_ERR_INVALID, "NULL pointer argument");
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
+    return fail(PKV_ERR_INVALID, "bf16 buffers must be 16-byte aligned");
+  if (!(scale == scale) || scale == 0.f) return fail(PKV_ERR_INVALID, "scale must be finite, non-zero");
+  DeviceState* st = device_state();
+  if (!st) return PKV_ERR_CUDA;
+  const pkv::WorkspaceLayout w = layout_for(dims, st->sm_count);
+  if (workspace == nullptr) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (st->own_ws_bytes < w.total) {
+      if (st->own_ws) cudaFree(st->own_ws);
+      st->own_ws = nullptr;
+      st->own_ws_bytes = 0;
+      cudaError_t e = cudaMalloc(&st->own_ws, w.total);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(workspace)");
+      e = cudaMemset(st->own_ws, 0, w.total);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(workspace)");
+      st->own_ws_bytes = w.total;
+    }
+    workspace = st->own_ws;
+    workspace_bytes = st->own_ws_bytes;
+  }
+  if (workspace_bytes < w.total)
+    return fail(PKV_ERR_WORKSPACE, "workspace %zu bytes, need %zu", workspace_bytes, w.total);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
+    return fail(PKV_ERR_INVALID, "workspace must be 256-byte aligned");
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  pkv::DecodeParams p;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k_pool = static_cast<const __nv_bfloat16*>(k_pool);
+  p.v_pool = static_cast<const __nv_bfloat16*>(v_pool);
+  p.block_tables = block_tables;
+  p.seq_lens = seq_lens;
+  p.qsl = query_start_loc;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.ws_cnt = reinterpret_cast<int*>(ws + w.cnt_off);
+  p.ws_ml = reinterpret_cast<float*>(ws + w.ml_off);
+  p.ws_o = reinterpret_cast<float*>(ws + w.o_off);
+  p.err = st->err;
+  p.num_reqs = dims->num_reqs;
+  p.num_q_tokens = dims->num_q_tokens;
+  p.num_q_heads = dims->num_q_heads;
+  p.num_kv_heads = dims->num_kv_heads;
+  p.num_blocks = dims->num_blocks;
+  p.max_blocks = dims->max_blocks_per_req;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.prefill_min_q = 0x7fffffff;
+  p.target_units = pkv::decode_target_units(st->sm_count);
+  p.max_units = w.max_units;
+  p.min_chunk = env_int("PKV_MIN_CHUNK", 4);
+  if (p.min_chunk < 1) p.min_chunk = 1;
+  cudaError_t e = pkv::launch_decode(p, dims->num_q_heads / dims->num_kv_heads, st->sm_count,
+                                     stream);
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  return PKV_OK;
+}
+
+int pkv_get_device_error(cudaStream_t stream) {
+  g_last_error[0] = '\0';
+  DeviceState* st = device_state();
+  if (!st) return PKV_ERR_CUDA;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int word = 0;
+  e = cudaMemcpy(&word, st->err, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "read device error word");
+  const int zero = 0;
+  e = cudaMemcpy(st->err, &zero, sizeof(int), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(e, "clear device error word");
+  if (word & pkv::kErrTimeout) return fail(PKV_ERR_TIMEOUT, "a device wait timed out (flags %d)", word);
+  if (word & (pkv::kErrBounds | pkv::kErrCapacity))
+    return fail(PKV_ERR_DEVICE_BOUNDS, "device bounds violation (flags %d)", word);
+  return PKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,268 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Small cases are compared element by element on every output; the full-size
+workloads (in the launch configuration the benchmark times) on sampled rows
+the oracle computes one by one, plus properties that hold at any size.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_195_gb300 as pkv
+from paged_kv_cache_195_gb300 import build as pkv_build
+from paged_kv_cache_195_gb300 import workloads as wl
+
+from pkv_testutil import (assert_close, gpu_step, host_copy, oracle_full,
+                          oracle_pools_after_append, sampled_rows_oracle, to_f64)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    pkv_build.build()
+    pkv.load_library()
+    yield
+    assert pkv.pkv_get_device_error() == 0, pkv.pkv_last_error()
+
+
+def _full_parity(shape, poison=False, append=True):
+    inp = wl.make_step(shape, device="cuda", poison=poison)
+    h = host_copy(inp)
+    kp, vp = oracle_pools_after_append(h) if append else (h["k_pool"], h["v_pool"])
+    out = gpu_step(inp, append=append)
+    torch.cuda.synchronize()
+    if append:
+        assert np.array_equal(wl.bf16_bits(inp.k_pool), kp)
+        assert np.array_equal(wl.bf16_bits(inp.v_pool), vp)
+    want = oracle_full(h, kp, vp)
+    return assert_close(to_f64(out), want, shape.name), inp, out
+
+
+# ---------------------------------------------------------------------------
+# KV append: bit-exact
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("factory", [wl.tiny_decode, lambda: wl.qwen_decode(layers=1),
+                                     lambda: wl.llama_mixed(num_decode=40, num_prefill=3)])
+def test_append_bit_exact(factory):
+    inp = wl.make_step(factory(), device="cuda")
+    h = host_copy(inp)
+    slots = inp.slot_mapping.clone()
+    slots[::7] = -1                                   # padding tokens are skipped
+    h["slot_mapping"] = slots.cpu().numpy()
+    kp, vp = oracle_pools_after_append(h)
+    pkv.pkv_append(inp.k_new, inp.v_new, slots, inp.k_pool, inp.v_pool)
+    torch.cuda.synchronize()
+    assert np.array_equal(wl.bf16_bits(inp.k_pool), kp)
+    assert np.array_equal(wl.bf16_bits(inp.v_pool), vp)
+
+
+def test_append_out_of_range_slot_is_reported_not_written():
+    inp = wl.make_step(wl.tiny_decode(), device="cuda")
+    before = wl.bf16_bits(inp.k_pool).copy()
+    bad = torch.full_like(inp.slot_mapping, 64 * 16 + 5)
+    pkv.pkv_append(inp.k_new, inp.v_new, bad, inp.k_pool, inp.v_pool)
+    assert pkv.pkv_get_device_error() == pkv._binding.PKV_ERR_DEVICE_BOUNDS
+    assert np.array_equal(wl.bf16_bits(inp.k_pool), before)
+    assert pkv.pkv_get_device_error() == 0        # the read cleared it
+
+
+# ---------------------------------------------------------------------------
+# Attention: every element on small cases
+# ---------------------------------------------------------------------------
+
+def test_tiny_decode_step():
+    _full_parity(wl.tiny_decode())
+
+
+def test_tiny_decode_step_poisoned_free_slots():
+    (mx, mean), inp, out = _full_parity(wl.tiny_decode(), poison=True)
+    assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_ragged_steps(seed):
+    rng = np.random.default_rng(500 + seed)
+    Hkv = int(rng.choice([1, 2, 4, 8]))
+    g = int(rng.integers(1, 9))
+    shape = wl.random_small_shape(rng, max_reqs=9, max_len=300, Hq=Hkv * g, Hkv=Hkv,
+                                  max_q=int(rng.choice([1, 4, 40])))
+    _full_parity(shape, poison=bool(seed % 2))
+
+
+@pytest.mark.parametrize("g", [1, 2, 3, 4, 5, 6, 7, 8])
+def test_every_group_size(g):
+    shape = wl.StepShape(f"g{g}", [1, 15, 16, 17, 200, 777], [1, 1, 2, 17, 1, 5], 2 * g, 2,
+                         seed=90 + g)
+    _full_parity(shape, poison=True)
+
+
+def test_edge_lengths():
+    """L = 1, exact block multiples, a fresh prefill (q = L), q_r = 0 rows."""
+    shape = wl.StepShape("edges", [1, 16, 32, 48, 33, 20, 5], [1, 1, 16, 0, 33, 0, 1], 12, 2,
+                         seed=77)
+    _full_parity(shape, poison=True)
+
+
+def test_empty_step():
+    shape = wl.StepShape("empty", [5, 9], [0, 0], 4, 2, seed=1)
+    inp = wl.make_step(shape, device="cuda")
+    out = gpu_step(inp, append=False)
+    assert out.shape == (0, 4, 128)
+
+
+def test_block_relabelling_is_bit_identical():
+    shape = wl.random_small_shape(np.random.default_rng(8), max_reqs=6, max_len=400, Hq=12, Hkv=2)
+    inp = wl.make_step(shape, device="cuda")
+    out1 = gpu_step(inp, append=False).clone()
+    perm = torch.randperm(shape.num_blocks, generator=torch.Generator().manual_seed(3)).cuda()
+    kp2 = torch.empty_like(inp.k_pool)
+    vp2 = torch.empty_like(inp.v_pool)
+    kp2[perm] = inp.k_pool
+    vp2[perm] = inp.v_pool
+    bt2 = torch.where(inp.block_tables >= 0, perm[inp.block_tables.clamp(min=0).long()].int(),
+                      inp.block_tables)
+    out2 = pkv.pkv_attention(inp.q, kp2, vp2, bt2.contiguous(), inp.seq_lens,
+                             inp.query_start_loc, inp.scale)
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+
+
+def test_split_count_does_not_change_the_answer(monkeypatch):
+    """Online-softmax merging is exact: any split count gives the same result
+    up to fp32 rounding (at most one bf16 ulp of the output)."""
+    shape = wl.StepShape("splits", [3000, 1200, 17], [1, 3, 1], 32, 8, seed=5)
+    inp = wl.make_step(shape, device="cuda")
+    outs = []
+    for chunk in ("1", "3", "4096"):
+        monkeypatch.setenv("PKV_MIN_CHUNK", chunk)
+        outs.append(gpu_step(inp, append=False).float().clone())
+    ref = oracle_full(host_copy(inp))
+    for o in outs:
+        assert_close(to_f64(o.bfloat16()), ref, "split")
+        ulp = torch.finfo(torch.bfloat16).eps * outs[-1].abs().clamp(min=2.0**-8)
+        assert ((o - outs[-1]).abs() <= ulp + 1e-6).all()
+
+
+def test_two_chunks_equal_one_chunk():
+    """A prefill chunk in one call equals two calls with the cache appended in
+    between (chunk k attends to what chunks 0..k-1 wrote)."""
+    prefix, q1, q2 = 37, 20, 45
+    one = wl.StepShape("c", [prefix + q1 + q2], [q1 + q2], 16, 4, seed=21)
+    inp = wl.make_step(one, device="cuda")
+    full = gpu_step(inp).clone()
+    outs = []
+    for lo, hi, L in ((0, q1, prefix + q1), (q1, q1 + q2, prefix + q1 + q2)):
+        o = pkv.pkv_attention(inp.q[lo:hi].contiguous(), inp.k_pool, inp.v_pool,
+                              inp.block_tables, torch.tensor([L], dtype=torch.int32, device="cuda"),
+                              torch.tensor([0, hi - lo], dtype=torch.int32, device="cuda"),
+                              inp.scale)
+        outs.append(o)
+    two = torch.cat(outs)
+    want = oracle_full(host_copy(inp))
+    assert_close(to_f64(two), want, "two chunks")
+    assert_close(to_f64(full), want, "one chunk")
+
+
+def test_constant_v_returns_the_constant():
+    shape = wl.random_small_shape(np.random.default_rng(31), max_reqs=5, max_len=500, Hq=32, Hkv=8)
+    inp = wl.make_step(shape, device="cuda")
+    inp.v_pool.fill_(0.71875)                              # exact in bf16
+    inp.v_new.fill_(0.71875)
+    out = gpu_step(inp)
+    assert torch.equal(out, torch.full_like(out, 0.71875))
+
+
+def test_explicit_workspace_reused_across_calls():
+    shape = wl.StepShape("ws", [2000, 700, 64], [1, 1, 1], 12, 2, seed=4)
+    inp = wl.make_step(shape, device="cuda")
+    dims = pkv.make_dims(tuple(inp.q.shape), tuple(inp.k_pool.shape), shape.num_reqs,
+                         shape.max_blocks_per_req)
+    ws = pkv.Workspace(dims)
+    pkv.pkv_workspace_init(ws, dims)
+    a = gpu_step(inp, workspace=ws).clone()
+    b = gpu_step(inp, append=False, workspace=ws).clone()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert_close(to_f64(a), oracle_full(host_copy(inp)), "workspace")
+
+
+def test_bad_block_id_is_reported():
+    shape = wl.StepShape("bad", [40, 40], [1, 1], 4, 2, seed=2)
+    inp = wl.make_step(shape, device="cuda")
+    inp.block_tables[1, 1] = shape.num_blocks + 3
+    gpu_step(inp, append=False)
+    assert pkv.pkv_get_device_error() == pkv._binding.PKV_ERR_DEVICE_BOUNDS
+
+
+def test_inconsistent_lengths_are_reported():
+    shape = wl.StepShape("badlen", [40, 40], [1, 1], 4, 2, seed=2)
+    inp = wl.make_step(shape, device="cuda")
+    inp.seq_lens[0] = 10_000                       # beyond the block table
+    gpu_step(inp, append=False)
+    assert pkv.pkv_get_device_error() == pkv._binding.PKV_ERR_DEVICE_BOUNDS
+
+
+# ---------------------------------------------------------------------------
+# Full-size workloads: sampled rows against the oracle + size-free properties
+# ---------------------------------------------------------------------------
+
+def _sampled(shape, n_rows, seed, layer=0):
+    inp = wl.make_step(shape, device="cuda", layer=layer)
+    out = gpu_step(inp)
+    again = gpu_step(inp, append=False)
+    assert torch.equal(out.view(torch.int16), again.view(torch.int16)), "non-deterministic"
+    assert torch.isfinite(out.float()).all()
+    rng = np.random.default_rng(seed)
+    rows = []
+    for r in rng.choice(shape.num_reqs, size=min(n_rows, shape.num_reqs), replace=False):
+        qr = int(shape.q_lens[r])
+        if qr:
+            rows.append((int(r), int(rng.integers(0, qr))))
+    # always include the longest request and the last query of any prefill
+    rows.append((int(np.argmax(shape.seq_lens)), int(shape.q_lens[np.argmax(shape.seq_lens)]) - 1))
+    qrows, want = sampled_rows_oracle(inp, rows)
+    got = to_f64(out[torch.tensor(qrows, device="cuda")])
+    return assert_close(got, want, shape.name)
+
+
+def test_qwen_decode_full_size_layers():
+    shape = wl.qwen_decode()
+    for layer in (0, 27):
+        _sampled(shape, 24, 10 + layer, layer=layer)
+
+
+def test_qwen_long_batch_full_size():
+    _sampled(wl.qwen_long_batch(), 24, 11)
+
+
+def test_llama_mixed_full_size():
+    shape = wl.llama_mixed()
+    _sampled(shape, 20, 12)
+    # every prefill request: first, middle and last query rows
+    inp = wl.make_step(shape, device="cuda")
+    out = gpu_step(inp)
+    rows = [(r, i) for r in range(248, 256) for i in (0, 255, 511)]
+    qrows, want = sampled_rows_oracle(inp, rows)
+    assert_close(to_f64(out[torch.tensor(qrows, device="cuda")]), want, "prefill rows")
+
+
+def test_llama_long_context_full_size():
+    _sampled(wl.llama_long_context(), 8, 13)
+
+
+def test_maximum_request_count():
+    R = 4096
+    rng = np.random.default_rng(14)
+    shape = wl.StepShape("r4096", rng.integers(1, 200, size=R), np.ones(R, np.int32), 8, 2, seed=14)
+    _sampled(shape, 30, 15)
+
+
+def test_very_long_context():
+    shape = wl.StepShape("L131072", [131072, 5], [1, 1], 8, 1, seed=16)
+    _sampled(shape, 2, 17)
