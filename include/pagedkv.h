@@ -60,9 +60,9 @@ extern "C" {
 #define PKV_ERR_DEVICE_BOUNDS (-5) /* reported later: block id or lengths out of range */
 #define PKV_ERR_TIMEOUT (-6)      /* reported later: a bounded device wait ran out */
 
-/* Upper bound on num_reqs for pkv_attention (its per-request plan lives in
- * shared memory). */
-#define PKV_MAX_REQS 4096
+/* Upper bound on num_reqs for pkv_attention (every CTA scans the per-request
+ * lengths to plan its share of the step). */
+#define PKV_MAX_REQS 65536
 
 typedef struct pkv_dims {
     int32_t num_reqs;           /* R */
@@ -101,8 +101,11 @@ size_t pkv_attention_workspace_size(const pkv_dims *dims);
 
 /*
  * Zeroes the merge counters at the head of a workspace (a stream-ordered
- * memset).  Call once after allocating a workspace; pkv_attention leaves the
- * counters at zero when it finishes, so later calls need no re-initialisation.
+ * memset).  Call once after allocating a workspace, and again whenever the
+ * workspace is reused with different num_q_tokens or num_kv_heads (the
+ * counter region grows with them).  pkv_attention leaves the counters at zero
+ * when it finishes, so calls with unchanged dims need no re-initialisation.
+ * After a PKV_ERR_TIMEOUT report, initialise it again.
  */
 int pkv_workspace_init(void *workspace, size_t workspace_bytes,
                        const pkv_dims *dims, cudaStream_t stream);

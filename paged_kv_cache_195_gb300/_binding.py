@@ -114,7 +114,10 @@ def pkv_attention_workspace_size(dims: Dims) -> int:
 
 
 class Workspace:
-    """A zero-initialised device workspace for pkv_attention (reusable)."""
+    """A zero-initialised device workspace for pkv_attention (reusable).
+
+    It remembers the (num_q_tokens, num_kv_heads) its counters were zeroed
+    for; pkv_attention re-initialises it when a call's dims differ."""
 
     def __init__(self, dims: Dims, device="cuda"):
         self.nbytes = pkv_attention_workspace_size(dims)
@@ -123,12 +126,14 @@ class Workspace:
         self.buf = torch.zeros(self.nbytes + 256, dtype=torch.uint8, device=device)
         off = (-self.buf.data_ptr()) % 256
         self.ptr = self.buf.data_ptr() + off
+        self.counter_dims = (dims.num_q_tokens, dims.num_kv_heads)
 
 
 def pkv_workspace_init(ws: Workspace, dims: Dims, stream=None):
     _check(load_library().pkv_workspace_init(ctypes.c_void_p(ws.ptr), ws.nbytes,
                                              ctypes.byref(dims),
                                              ctypes.c_void_p(_stream(stream, ws.buf.device))))
+    ws.counter_dims = (dims.num_q_tokens, dims.num_kv_heads)
 
 
 def pkv_append(k_new, v_new, slot_mapping, k_pool, v_pool, stream=None):
@@ -174,6 +179,8 @@ def pkv_attention(q, k_pool, v_pool, block_tables, seq_lens, query_start_loc, sc
         if out.shape != q.shape:
             raise ValueError("out must have q's shape")
     dims = make_dims(tuple(q.shape), tuple(k_pool.shape), R, block_tables.shape[1])
+    if workspace is not None and workspace.counter_dims != (dims.num_q_tokens, dims.num_kv_heads):
+        pkv_workspace_init(workspace, dims, stream)
     ws_ptr, ws_bytes = (None, 0) if workspace is None else (workspace.ptr, workspace.nbytes)
     _check(load_library().pkv_attention(
         ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k_pool.data_ptr()),

@@ -21,6 +21,8 @@ LIB = os.path.join(BUILD, "libpagedkv.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
           "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]
+# Extra nvcc flags (e.g. -D switches of a kernel variant) for experiments.
+EXTRA = os.environ.get("PKV_EXTRA_NVCC", "").split()
 
 
 def _nvcc() -> str:
@@ -49,11 +51,16 @@ def build(verbose: bool = False, force: bool = False) -> str:
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     headers = _headers()
     objs, jobs = [], []
+    stamp = os.path.join(BUILD, "flags.txt")
+    if (open(stamp).read() if os.path.exists(stamp) else "") != " ".join(EXTRA):
+        force = True
+        with open(stamp, "w") as f:
+            f.write(" ".join(EXTRA))
     for src in srcs:
         obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         if force or _stale(obj, [src] + headers):
-            jobs.append([nvcc, *ARCH, *CFLAGS, "-c", src, "-o", obj])
+            jobs.append([nvcc, *ARCH, *CFLAGS, *EXTRA, "-c", src, "-o", obj])
 
     def run(cmd):
         r = subprocess.run(cmd, capture_output=True, text=True)

@@ -42,6 +42,7 @@ struct DeviceState {
   int* err = nullptr;          // device address of g_device_error
   void* own_ws = nullptr;      // the NULL-workspace convenience buffer
   size_t own_ws_bytes = 0;
+  size_t own_ws_cnt_bytes = 0; // counter bytes its last user needed zeroed
 };
 
 std::mutex g_mutex;
@@ -109,13 +110,66 @@ int check_dims(const pkv_dims* d, bool for_attention) {
 
 pkv::WorkspaceLayout layout_for(const pkv_dims* d, int sm_count) {
   return pkv::decode_workspace_layout(d->num_q_tokens, d->num_kv_heads,
-                                      d->num_q_heads / d->num_kv_heads,
-                                      pkv::decode_target_units(sm_count));
+                                      d->num_q_heads / d->num_kv_heads, sm_count);
 }
 
 int env_int(const char* name, int dflt) {
   const char* v = getenv(name);
   return (v && *v) ? atoi(v) : dflt;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against libcuda).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// 2-D map of a pool as [num_blocks * Hkv * 16 rows][128] bf16, 64 x 16 boxes.
+int encode_pool_map(CUtensorMap* m, const void* pool, const pkv_dims* d) {
+  EncodeTiledFn enc = encode_tiled();
+  if (!enc) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  const cuuint64_t dims[2] = {(cuuint64_t)pkv::kHeadDim,
+                              (cuuint64_t)d->num_blocks * d->num_kv_heads * pkv::kBlockSize};
+  const cuuint64_t strides[1] = {(cuuint64_t)pkv::kHeadDim * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)pkv::kBlockSize};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "encode pool tensor map: CUresult %d", (int)r);
+  return PKV_OK;
+}
+
+// 3-D map of q as [Tq][Hq][128] bf16, boxes of (64 dims, g heads, 128/g tokens).
+int encode_q_map(CUtensorMap* m, const void* q, const pkv_dims* d, int group) {
+  EncodeTiledFn enc = encode_tiled();
+  if (!enc) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  const cuuint64_t dims[3] = {(cuuint64_t)pkv::kHeadDim, (cuuint64_t)d->num_q_heads,
+                              (cuuint64_t)d->num_q_tokens};
+  const cuuint64_t strides[2] = {(cuuint64_t)pkv::kHeadDim * 2,
+                                 (cuuint64_t)d->num_q_heads * pkv::kHeadDim * 2};
+  const cuuint32_t box[3] = {64, (cuuint32_t)group, (cuuint32_t)pkv::prefill_tokens_per_tile(group)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "encode q tensor map: CUresult %d", (int)r);
+  return PKV_OK;
 }
 
 }  // namespace
@@ -147,6 +201,7 @@ int pkv_append(const void* k_new, const void* v_new, const int64_t* slot_mapping
   p.num_tokens = num_new_tokens;
   p.num_kv_heads = dims->num_kv_heads;
   p.num_blocks = dims->num_blocks;
+  p.pdl = env_int("PKV_PDL", 1) != 0;
   cudaError_t e = pkv::launch_append(p, stream);
   if (e != cudaSuccess) return cuda_fail(e, "append launch");
   return PKV_OK;
@@ -201,6 +256,12 @@ int pkv_attention(const void* q, const void* k_pool, const void* v_pool,
       e = cudaMemset(st->own_ws, 0, w.total);
       if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(workspace)");
       st->own_ws_bytes = w.total;
+      st->own_ws_cnt_bytes = w.ml_off;
+    } else if (st->own_ws_cnt_bytes != w.ml_off) {
+      // The counter region moved with the dims: zero it again.
+      cudaError_t e = cudaMemsetAsync(st->own_ws, 0, w.ml_off, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(workspace)");
+      st->own_ws_cnt_bytes = w.ml_off;
     }
     workspace = st->own_ws;
     workspace_bytes = st->own_ws_bytes;
@@ -230,14 +291,46 @@ int pkv_attention(const void* q, const void* k_pool, const void* v_pool,
   p.num_blocks = dims->num_blocks;
   p.max_blocks = dims->max_blocks_per_req;
   p.scale_log2 = scale * 1.4426950408889634f;
-  p.prefill_min_q = 0x7fffffff;
-  p.target_units = pkv::decode_target_units(st->sm_count);
-  p.max_units = w.max_units;
+  // Requests with at least this many query tokens go to the tensor-core
+  // prefill kernel (when the step has that many query tokens at all).
+  int prefill_min_q = env_int("PKV_PREFILL_MIN_Q", 16);
+  if (prefill_min_q < 1) prefill_min_q = 0x7fffffff;
+  const bool run_prefill = dims->num_q_tokens >= prefill_min_q;
+  p.prefill_min_q = run_prefill ? prefill_min_q : 0x7fffffff;
+  p.num_slots = w.num_slots;
+  p.pdl = env_int("PKV_PDL", 1) != 0;
   p.min_chunk = env_int("PKV_MIN_CHUNK", 4);
   if (p.min_chunk < 1) p.min_chunk = 1;
-  cudaError_t e = pkv::launch_decode(p, dims->num_q_heads / dims->num_kv_heads, st->sm_count,
-                                     stream);
+  const int group = dims->num_q_heads / dims->num_kv_heads;
+  int grid = pkv::decode_grid(st->sm_count, group);
+  const int grid_env = env_int("PKV_DECODE_GRID", 0);  // tuning override, bounded by the slots
+  if (grid_env > 0 && 2 * grid_env <= w.num_slots) grid = grid_env;
+  cudaError_t e = pkv::launch_decode(p, group, grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  if (run_prefill) {
+    pkv::PrefillLaunch L;
+    rc = encode_q_map(&L.qmap, q, dims, group);
+    if (rc == PKV_OK) rc = encode_pool_map(&L.kmap, k_pool, dims);
+    if (rc == PKV_OK) rc = encode_pool_map(&L.vmap, v_pool, dims);
+    if (rc != PKV_OK) return rc;
+    L.p.block_tables = block_tables;
+    L.p.seq_lens = seq_lens;
+    L.p.qsl = query_start_loc;
+    L.p.out = p.out;
+    L.p.err = st->err;
+    L.p.num_reqs = dims->num_reqs;
+    L.p.num_q_tokens = dims->num_q_tokens;
+    L.p.num_q_heads = dims->num_q_heads;
+    L.p.num_kv_heads = dims->num_kv_heads;
+    L.p.num_blocks = dims->num_blocks;
+    L.p.max_blocks = dims->max_blocks_per_req;
+    L.p.scale_log2 = p.scale_log2;
+    L.p.prefill_min_q = prefill_min_q;
+    L.p.pdl = p.pdl;
+    L.grid = st->sm_count;
+    e = pkv::launch_prefill(L, group, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+  }
   return PKV_OK;
 }
 

@@ -11,6 +11,8 @@
 namespace pkv {
 
 __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
+  grid_dependency_wait();  // inputs and pool may belong to the previous kernel
+  allow_dependent_launch();
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= p.num_tokens * p.num_kv_heads) return;
@@ -38,7 +40,17 @@ cudaError_t launch_append(const AppendParams& p, cudaStream_t stream) {
   if (warps == 0) return cudaSuccess;
   const int threads = 256;
   const long long blocks = (warps * 32 + threads - 1) / threads;
-  append_kernel<<<(unsigned)blocks, threads, 0, stream>>>(p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(threads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = p.pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, append_kernel, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

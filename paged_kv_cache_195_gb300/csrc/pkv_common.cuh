@@ -13,8 +13,8 @@ constexpr int kHeadDim = 128;
 constexpr int kBlockSize = 16;
 // One (block, KV head) tile of the pool: 16 tokens x 128 dims x 2 bytes.
 constexpr int kTileBytes = kBlockSize * kHeadDim * 2;
-// Largest num_reqs pkv_attention accepts (its plan lives in shared memory).
-constexpr int kMaxReqs = 4096;
+// Largest num_reqs pkv_attention accepts.
+constexpr int kMaxReqs = 65536;
 
 // Device error word bits (see pkv_get_device_error).
 constexpr int kErrBounds = 1;   // block id / slot / lengths out of range
@@ -59,14 +59,18 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
+// One potentially blocking probe: the warp sleeps until the phase completes
+// or about kSuspendHintNs pass, whichever is first.
+constexpr uint32_t kSuspendHintNs = 100000;
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
       : "memory");
   return ok != 0;
 }
@@ -118,6 +122,17 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
       "[%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
+}
+
+// Programmatic dependent launch: wait until the preceding kernel in the
+// stream has completed and its writes are visible (a no-op when the launch
+// had no programmatic dependency), and allow the next kernel to be scheduled.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void allow_dependent_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // Named barrier over `threads` threads (a multiple of 32).

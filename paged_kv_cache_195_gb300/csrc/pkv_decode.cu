@@ -11,27 +11,31 @@
 //  * One CTA serves all g query heads of a KV head, so each (block, KV head)
 //    tile -- 4 KiB of K and 4 KiB of V, contiguous in the pool -- leaves HBM
 //    once per row.
-//  * Parallelism comes from the KV axis: each row's blocks are cut into
-//    splits ("units") sized by a device-side plan from the step's lengths
-//    (Flash-Decoding: The Serving Playbook, "Kernel fusion, briefly").  Each
-//    CTA keeps an online-softmax state per split (running max, normaliser,
-//    rescaled output: LLM 7 - Efficient LLM Serving, sec. 2 "Online Softmax
-//    Makes Tiling Possible").  The last CTA to finish a row merges the splits
-//    by log-sum-exp (the "second pass rescales the partials" step), found with
-//    one atomic counter per row: no extra launch, deterministic merge order.
-//  * A producer warp walks the CTA's units and issues cp.async.bulk copies of
-//    whole tiles into an 8-stage shared-memory ring (mbarrier-tracked);
-//    four consumer warps take ring stages round-robin.  The 16 KiB per tile
-//    pair in flight per stage keeps ~128 KiB of loads outstanding per SM.
+//  * Parallelism comes from the KV axis (Flash-Decoding: The Serving
+//    Playbook, "Kernel fusion, briefly").  The step's work is the sequence of
+//    (row, KV head) row-groups, each a run of 16-token blocks; a persistent
+//    grid cuts that sequence into equal contiguous ranges, one per CTA, so
+//    every CTA streams the same number of tiles whatever the length mix.  A
+//    row-group cut by a range boundary is computed in pieces; each piece
+//    keeps an online-softmax state (running max, normaliser, rescaled output:
+//    LLM 7 - Efficient LLM Serving, sec. 2 "Online Softmax Makes Tiling
+//    Possible"), and the last CTA to finish a row-group merges its pieces by
+//    log-sum-exp, found with one atomic counter per row-group: no extra
+//    launch, merge in piece order (deterministic).
+//  * The plan -- the block count of every request, their prefix sum and this
+//    CTA's range -- is computed by the producer warp of every CTA from
+//    seq_lens / query_start_loc in device memory, so the launch shape depends
+//    only on bounds and the call is CUDA-graph capturable.
+//  * The producer warp walks the CTA's range and issues cp.async.bulk copies of
+//    whole tiles into an 8-stage shared-memory ring (mbarrier-tracked), running
+//    ahead across piece boundaries; four consumer warps take stages
+//    round-robin.  Two CTAs per SM keep ~128 KiB of loads in flight per SM.
 //  * Consumers: lane = (token half, 16-byte chunk of d).  q for all g heads of
 //    the lane's chunk stays in registers; QK partial sums over the lane's 8
 //    dims are reduced across the 16 lanes of a half-warp by a reduce-scatter
 //    whose register order is permuted per lane so that no selects are needed;
 //    softmax in fp32 (exp2 with scale*log2(e) folded into q); PV accumulates
 //    in packed fp32 (fma.rn.f32x2).
-//  * The plan (per-request unit counts and their prefix sum) is recomputed by
-//    every CTA from seq_lens / query_start_loc in device memory, so the
-//    launch shape depends only on bounds: the call is CUDA-graph capturable.
 #include <climits>
 
 #include "pkv_internal.h"
@@ -41,67 +45,61 @@ namespace {
 
 constexpr int kConsumerWarps = 4;
 constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;
-constexpr int kStages = 8;
+// Ring depth: two CTAs per SM for g <= 6 (10 stages each), one for g >= 7
+// (registers), which then takes a 20-stage ring.
+template <int G>
+constexpr int stages_for() { return G <= 6 ? 10 : 20; }
 constexpr int kStageBytes = 2 * kTileBytes;  // K tile then V tile
 constexpr float kNegBig = -1.0e30f;          // "no key seen yet" running max
+constexpr int kEndRow = -2;                  // piece marker: the CTA's range is done
 
-struct UnitInfo {
-  int row;    // global query row
-  int k;      // KV head
-  int b0;     // first logical block
-  int nblk;   // blocks in this unit (may be 0)
-  int limit;  // keys visible to this row: positions < limit
-  int S;      // splits of this (row, KV head)
-  int unit;   // global unit id (workspace slot of this split)
-  int base;   // workspace slot of split 0 of this row
+// One piece of a row-group: the blocks [b0, b0 + nblk) of row `row`, KV head k.
+struct Piece {
+  int row;     // global query row, or kEndRow
+  int k;       // KV head
+  int b0;      // first logical block of the piece
+  int nblk;    // blocks in the piece (>= 1)
+  int limit;   // keys visible to this row: positions < limit
+  int slot;    // workspace slot of this piece's partial state (partial pieces)
+  int c0;      // first CTA whose range touches the row-group
+  int S;       // pieces of the row-group (1: complete in this CTA)
+  int odd0;    // piece 0 of the row-group uses slot 2*c0+1 (else 2*c0)
 };
+
+#ifndef PKV_P_DUP
+#define PKV_P_DUP 1
+#endif
 
 template <int G>
 struct __align__(128) DecodeSmem {
-  static constexpr int kPStride = (G + 3) & ~3;
+  static constexpr int kStages = stages_for<G>();
+  // Probabilities of one block, stored twice ({p, p}) so that the PV loop
+  // feeds packed fp32 FMAs straight from 16-byte loads.
+#if PKV_P_DUP
+  static constexpr int kPStride = (G + 1) & ~1;  // float2 entries per token
+#else
+  static constexpr int kPStride = ((G + 3) & ~3) / 2;  // float2 slots = 2 floats each
+#endif
   uint8_t ring[kStages][kStageBytes];
   __nv_bfloat16 qbuf[2][G * kHeadDim];
-  float pbuf[kConsumerWarps][kBlockSize][kPStride];
+  float2 pbuf[kConsumerWarps][kBlockSize][kPStride];
   float comb[kConsumerWarps][G][kHeadDim];
   float comb_m[kConsumerWarps][G];
   float comb_l[kConsumerWarps][G];
-  UnitInfo uinfo[2];
+  Piece pinfo[2];
   int stage_valid[kStages];
   uint64_t full[kStages];
   uint64_t empty[kStages];
   uint64_t qfull[2];
   uint64_t qempty[2];
-  long long red[kDecodeThreads / 32];
-  int total_units;
   int abort_flag;
-  int stop;
   int is_last;
   int wait_ok[kConsumerWarps];
+  int end_flag[kConsumerWarps];
 };
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
-
-// Inclusive block-wide scan of one value per thread (all threads call).
-template <typename T>
-__device__ T block_inclusive_scan(T v, T* red, T* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    T n = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v += n;
-  }
-  if (lane == 31) red[warp] = v;
-  __syncthreads();
-  T before = 0, all = 0;
-  #pragma unroll
-  for (int w = 0; w < kDecodeThreads / 32; ++w) {
-    if (w < warp) before += red[w];
-    all += red[w];
-  }
-  __syncthreads();
-  *total = all;
-  return v + before;
-}
+__device__ __forceinline__ long long ceil_div_ll(long long a, long long b) { return (a + b - 1) / b; }
 
 // ---------------------------------------------------------------------------
 // Consumer: one 16-token block for one warp.
@@ -125,7 +123,7 @@ struct BlockMath {
   __device__ static __forceinline__ void run(const uint8_t* stage, int nvalid, int lane,
                                              const float2 (&qf)[G][4], float (&m)[G],
                                              float (&lsum)[F], float2 (&acc)[G][4],
-                                             float (*pbuf)[kPStride]) {
+                                             float2 (*pbuf)[kPStride]) {
     const int half = lane >> 4;
     const int c = lane & 15;
     const int x = (lane >> 1) & 7;
@@ -226,7 +224,11 @@ struct BlockMath {
       }
       const float pj = fast_exp2(sc[j] - mh);
       lsum[j] = lsum[j] * ah + pj;
-      if (kEven || b0 == 0) pbuf[tl][h] = pj;
+#if PKV_P_DUP
+      if (kEven || b0 == 0) pbuf[tl][h] = make_float2(pj, pj);
+#else
+      if (kEven || b0 == 0) reinterpret_cast<float*>(pbuf[tl])[h] = pj;
+#endif
     }
     __syncwarp();
     if (__any_sync(0xffffffffu, changed)) {
@@ -245,15 +247,29 @@ struct BlockMath {
         const uint4 w = lds128(Vt + tok * (kHeadDim * 2) + c * 16);
         const float2 v0 = bf16x2_to_float2(w.x), v1 = bf16x2_to_float2(w.y);
         const float2 v2 = bf16x2_to_float2(w.z), v3 = bf16x2_to_float2(w.w);
-        float pr[kPStride];
+#if PKV_P_DUP
+        float2 pr[kPStride];
         #pragma unroll
-        for (int i = 0; i < kPStride; i += 4) {
+        for (int i = 0; i < kPStride; i += 2) {
           const float4 t4 = *reinterpret_cast<const float4*>(&pbuf[tok][i]);
-          pr[i] = t4.x; pr[i + 1] = t4.y; pr[i + 2] = t4.z; pr[i + 3] = t4.w;
+          pr[i] = make_float2(t4.x, t4.y);
+          pr[i + 1] = make_float2(t4.z, t4.w);
         }
+#else
+        float prs[2 * kPStride];
+        #pragma unroll
+        for (int i = 0; i < 2 * kPStride; i += 4) {
+          const float4 t4 = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(pbuf[tok]) + i);
+          prs[i] = t4.x; prs[i + 1] = t4.y; prs[i + 2] = t4.z; prs[i + 3] = t4.w;
+        }
+#endif
         #pragma unroll
         for (int h = 0; h < G; ++h) {
-          const float2 p2 = make_float2(pr[h], pr[h]);
+#if PKV_P_DUP
+          const float2 p2 = pr[h];
+#else
+          const float2 p2 = make_float2(prs[h], prs[h]);
+#endif
           acc[h][0] = ffma2(p2, v0, acc[h][0]);
           acc[h][1] = ffma2(p2, v1, acc[h][1]);
           acc[h][2] = ffma2(p2, v2, acc[h][2]);
@@ -265,154 +281,239 @@ struct BlockMath {
 };
 
 // ---------------------------------------------------------------------------
+// The plan.
+// ---------------------------------------------------------------------------
+// Sum over x = 1..n of ceil(x / 16): with n = 16m + t, 8m(m+1) + t(m+1).
+__device__ __forceinline__ long long ceil16_prefix(long long n) {
+  if (n <= 0) return 0;
+  const long long m = n / kBlockSize, t = n % kBlockSize;
+  return 8 * m * (m + 1) + t * (m + 1);
+}
+
+struct ReqInfo {
+  int q0, qr, L;
+  bool decode;  // has rows this kernel serves
+};
+
+__device__ __forceinline__ ReqInfo load_request(const DecodeParams& p, int r) {
+  ReqInfo ri;
+  ri.q0 = __ldg(p.qsl + r);
+  const int q1 = __ldg(p.qsl + r + 1);
+  ri.L = __ldg(p.seq_lens + r);
+  ri.qr = q1 - ri.q0;
+  const bool ok = ri.q0 >= 0 && ri.qr >= 0 && q1 <= p.num_q_tokens && ri.qr <= ri.L &&
+                  ri.L <= p.max_blocks * kBlockSize;
+  ri.decode = ok && ri.qr > 0 && ri.qr < p.prefill_min_q;
+  return ri;
+}
+
+// Blocks of rows 0..i-1 of a request (one KV head): row i sees L - qr + i + 1
+// keys, i.e. ceil((L - qr + 1 + i) / 16) blocks.
+__device__ __forceinline__ long long rows_blocks(const ReqInfo& ri, int i) {
+  const long long a = (long long)ri.L - ri.qr + 1;
+  return ceil16_prefix(a + i - 1) - ceil16_prefix(a - 1);
+}
+
+// ---------------------------------------------------------------------------
 // The kernel.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ bool request_ok(const DecodeParams& p, int q0, int q1, int L) {
-  const int qr = q1 - q0;
-  return q0 >= 0 && qr >= 0 && q1 <= p.num_q_tokens && qr <= L &&
-         L <= p.max_blocks * kBlockSize;
-}
-
-// Work units of request r: its decode rows x KV heads x splits.
-__device__ __forceinline__ long long request_units(const DecodeParams& p, int r, int chunk,
-                                                   long long* work) {
-  const int q0 = p.qsl[r], q1 = p.qsl[r + 1], L = p.seq_lens[r];
-  const int qr = q1 - q0;
-  if (!request_ok(p, q0, q1, L) || qr == 0 || qr >= p.prefill_min_q) {
-    *work = 0;
-    return 0;
-  }
-  const int nb = ceil_div(L, kBlockSize);
-  *work = (long long)qr * nb;
-  return chunk > 0 ? (long long)qr * p.num_kv_heads * ceil_div(nb, chunk) : 0;
-}
-
 template <int G>
 __global__ void __launch_bounds__(kDecodeThreads, (G <= 6 ? 2 : 1))
     decode_kernel(const DecodeParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   DecodeSmem<G>& sm = *reinterpret_cast<DecodeSmem<G>*>(smem_raw);
-  int* prefix = reinterpret_cast<int*>(smem_raw + sizeof(DecodeSmem<G>));  // [R+1]
   volatile int* abort_flag = &sm.abort_flag;
+  constexpr int kRing = DecodeSmem<G>::kStages;
+  const int kStages = (p.stages >= 2 && p.stages <= kRing) ? p.stages : kRing;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int R = p.num_reqs, Hkv = p.num_kv_heads;
 
   if (tid == 0) {
     #pragma unroll
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kRing; ++s) {
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.qfull[b], 1);
       mbar_init(&sm.qempty[b], kConsumerWarps);
-      sm.uinfo[b].row = -1;  // "no unit": fails the consumers' range checks
     }
     sm.abort_flag = 0;
-    sm.stop = 0;
     fence_barrier_init();
   }
-
-  // ---- device plan, pass 1: total work of the decode-class rows ----------
-  const int per = ceil_div(R, kDecodeThreads);
-  const int r_lo = min(R, tid * per), r_hi = min(R, r_lo + per);
-  long long work = 0;
-  for (int r = r_lo; r < r_hi; ++r) {
-    long long w;
-    request_units(p, r, 0, &w);
-    work += w;
-    if (blockIdx.x == 0 && !request_ok(p, p.qsl[r], p.qsl[r + 1], p.seq_lens[r]))
-      record_error(p.err, kErrBounds);
-  }
-  long long total_work;
-  block_inclusive_scan<long long>(work, sm.red, &total_work);
-  total_work *= Hkv;
-  const int chunk = (int)max((long long)p.min_chunk,
-                             (total_work + p.target_units - 1) / max(1, p.target_units));
-
-  // ---- pass 2: units per request and their exclusive prefix sum ----------
-  long long units = 0;
-  for (int r = r_lo; r < r_hi; ++r) {
-    long long w;
-    units += request_units(p, r, chunk, &w);
-  }
-  long long total_units;
-  const long long incl = block_inclusive_scan<long long>(units, sm.red, &total_units);
-  {
-    long long run = incl - units;
-    for (int r = r_lo; r < r_hi; ++r) {
-      prefix[r] = (int)run;
-      long long w;
-      run += request_units(p, r, chunk, &w);
-    }
-  }
-  if (tid == 0) {
-    if (total_units > p.max_units) {
-      if (blockIdx.x == 0) record_error(p.err, kErrCapacity);
-      total_units = 0;
-    }
-    prefix[R] = (int)total_units;
-    sm.total_units = (int)total_units;
-  }
   __syncthreads();
-  const int T = sm.total_units;
+  // Everything above overlaps the previous kernel's tail; every input may be
+  // that kernel's output, so all reads come after this point.
+  grid_dependency_wait();
+  allow_dependent_launch();
 
   if (warp == kConsumerWarps) {
     // ======================= producer warp =================================
-    const uint64_t pol = l2_policy_evict_first();
-    int r = 0;
-    uint32_t n = 0;  // CTA-wide block sequence number
-    int j = 0;       // CTA-local unit index
-    for (int u = blockIdx.x; u < T && !*abort_flag; u += gridDim.x, ++j) {
-      while (r < R - 1 && prefix[r + 1] <= u) ++r;
-      const int q0 = __ldg(p.qsl + r), qr = __ldg(p.qsl + r + 1) - q0;
-      const int L = __ldg(p.seq_lens + r);
-      const int nb = ceil_div(L, kBlockSize);
-      const int S = ceil_div(nb, chunk);
-      const int local = u - prefix[r];
-      const int s = local % S;
-      const int rest = local / S;
-      const int k = rest % Hkv;
-      const int i = rest / Hkv;
-      const int limit = L - qr + i + 1;
-      const int b0 = s * chunk;
-      const int nblk = max(0, min(b0 + chunk, ceil_div(limit, kBlockSize)) - b0);
-      const int ub = j & 1;
-      if (j >= 2 && !mbar_wait(&sm.qempty[ub], ((j >> 1) - 1) & 1, p.err, abort_flag)) break;
-      if (lane == 0) {
-        UnitInfo ui;
-        ui.row = q0 + i; ui.k = k; ui.b0 = b0; ui.nblk = nblk; ui.limit = limit;
-        ui.S = S; ui.unit = u; ui.base = u - s;
-        sm.uinfo[ub] = ui;
-        mbar_arrive_expect_tx(&sm.qfull[ub], G * kHeadDim * 2);
-        bulk_copy_g2s(sm.qbuf[ub],
-                      p.q + ((long long)(q0 + i) * p.num_q_heads + (long long)k * G) * kHeadDim,
-                      G * kHeadDim * 2, &sm.qfull[ub]);
+    // Warm L2 with the part of the block table this CTA will probably read
+    // (its share of the step if every row were full), while the plan loads.
+    {
+      const long long entries = (long long)R * p.max_blocks;
+      const long long est = entries * blockIdx.x / gridDim.x;
+      const long long line0 = (est * 4) / 128 - 2;
+      const long long lines = (entries * 4 + 127) / 128;
+      const long long line = line0 + lane;
+      if (line >= 0 && line < lines)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(p.block_tables) +
+                                                     line * 128));
+    }
+    // ---- plan, pass 1: total blocks W of the decode rows (all KV heads) ----
+    long long mine = 0;
+    int nb_min = INT_MAX, nb_max = 0;
+    for (int r = lane; r < R; r += 32) {
+      const ReqInfo ri = load_request(p, r);
+      if (ri.decode) {
+        mine += rows_blocks(ri, ri.qr) * Hkv;
+        nb_min = min(nb_min, ceil_div(ri.L - ri.qr + 1, kBlockSize));
+        nb_max = max(nb_max, ceil_div(ri.L, kBlockSize));
+      } else if (blockIdx.x == 0 && ri.qr != 0 && ri.qr < p.prefill_min_q) {
+        record_error(p.err, kErrBounds);  // inconsistent lengths: request skipped
       }
-      const int32_t* bt = p.block_tables + (long long)r * p.max_blocks + b0;
-      for (int bb = 0; bb < nblk && !*abort_flag; bb += 32) {
-        const int cnt = min(32, nblk - bb);
-        const int ent = lane < cnt ? __ldg(bt + bb + lane) : 0;
-        for (int xb = 0; xb < cnt; ++xb, ++n) {
-          int phys = __shfl_sync(0xffffffffu, ent, xb);
-          const int st = n % kStages;
-          if (n >= kStages && !mbar_wait(&sm.empty[st], ((n / kStages) - 1) & 1, p.err, abort_flag))
-            break;
-          if (lane == 0) {
-            const bool valid = (unsigned)phys < (unsigned)p.num_blocks;
-            if (!valid) {
-              record_error(p.err, kErrBounds);
-              phys = 0;
-            }
-            sm.stage_valid[st] = valid;
-            const long long tile = ((long long)phys * Hkv + k) * (kTileBytes / 2);
-            mbar_arrive_expect_tx(&sm.full[st], kStageBytes);
-            bulk_copy_g2s(sm.ring[st], p.k_pool + tile, kTileBytes, &sm.full[st], pol);
-            bulk_copy_g2s(sm.ring[st] + kTileBytes, p.v_pool + tile, kTileBytes, &sm.full[st], pol);
-          }
-          __syncwarp();
+    }
+    #pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      mine += __shfl_xor_sync(0xffffffffu, mine, o);
+      nb_min = min(nb_min, __shfl_xor_sync(0xffffffffu, nb_min, o));
+      nb_max = max(nb_max, __shfl_xor_sync(0xffffffffu, nb_max, o));
+    }
+    const long long W = mine;
+    long long chunk = max((long long)p.min_chunk, ceil_div_ll(W, gridDim.x));
+    if (p.align && nb_min == nb_max && W > 0) {
+      // Uniform row-groups: cut each into equal pieces, or keep whole groups
+      // together, so that piece boundaries coincide with CTA boundaries.
+      const long long nb = nb_max;
+      chunk = chunk < nb ? ceil_div_ll(nb, nb / chunk) : ceil_div_ll(chunk, nb) * nb;
+    }
+    const long long lo = (long long)blockIdx.x * chunk;
+    const long long hi = min(W, lo + chunk);
+
+    const uint64_t pol = l2_policy_evict_first();
+    uint32_t n = 0;  // CTA-wide block sequence number
+    int j = 0;       // CTA-local piece index
+    if (lo < hi) {
+      // ---- pass 2: the request holding block lo, and where it starts -------
+      int r = -1;
+      long long pos = 0, base = 0;
+      for (int b = 0; b < R; b += 32) {
+        const int rr = b + lane;
+        long long w = 0;
+        if (rr < R) {
+          const ReqInfo ri = load_request(p, rr);
+          if (ri.decode) w = rows_blocks(ri, ri.qr) * Hkv;
         }
+        long long incl = w;
+        #pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const long long t = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += t;
+        }
+        const long long excl = incl - w;
+        const unsigned own = __ballot_sync(0xffffffffu, w > 0 && base + excl <= lo && lo < base + incl);
+        if (own) {
+          const int src = __ffs(own) - 1;
+          r = b + src;
+          pos = base + __shfl_sync(0xffffffffu, excl, src);
+          break;
+        }
+        base += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      // Walk the row-groups that intersect [lo, hi).
+      if (r < 0) {
+        record_error(p.err, kErrBounds);  // unreachable when the lengths are stable
+        r = R;
+      }
+      ReqInfo ri = load_request(p, r < R ? r : 0);
+      int i = 0;
+      {  // first row of request r whose groups reach lo (binary search)
+        int a = 0, b = ri.qr - 1;
+        while (a < b) {
+          const int mid = (a + b + 1) / 2;
+          if (pos + rows_blocks(ri, mid) * Hkv <= lo) a = mid; else b = mid - 1;
+        }
+        i = a;
+      }
+      long long g = r < R ? pos + rows_blocks(ri, i) * Hkv : hi;  // start of row i, head 0
+      int nb = ceil_div(ri.L - ri.qr + i + 1, kBlockSize);
+      int k = (int)((lo - g) / nb);
+      g += (long long)k * nb;
+      while (g < hi && !*abort_flag) {
+        // ---- one piece: row-group (r, i, k) = global blocks [g, g + nb) ----
+        const long long s0 = max(g, lo), s1 = min(g + nb, hi);
+        const long long c0 = g / chunk, c1 = (g + nb - 1) / chunk;
+        Piece pc;
+        pc.row = ri.q0 + i;
+        pc.k = k;
+        pc.b0 = (int)(s0 - g);
+        pc.nblk = (int)(s1 - s0);
+        pc.limit = ri.L - ri.qr + i + 1;
+        pc.S = (int)(c1 - c0 + 1);
+        pc.c0 = (int)c0;
+        pc.odd0 = g != c0 * chunk;
+        pc.slot = 2 * (int)blockIdx.x + (s0 == lo ? 0 : 1);
+        const int ub = j & 1;
+        if (j >= 2 && !mbar_wait(&sm.qempty[ub], ((j >> 1) - 1) & 1, p.err, abort_flag)) break;
+        if (lane == 0) {
+          sm.pinfo[ub] = pc;
+          mbar_arrive_expect_tx(&sm.qfull[ub], G * kHeadDim * 2);
+          bulk_copy_g2s(sm.qbuf[ub],
+                        p.q + ((long long)pc.row * p.num_q_heads + (long long)k * G) * kHeadDim,
+                        G * kHeadDim * 2, &sm.qfull[ub]);
+        }
+        const int32_t* bt = p.block_tables + (long long)r * p.max_blocks + pc.b0;
+        for (int bb = 0; bb < pc.nblk && !*abort_flag; bb += 32) {
+          const int cnt = min(32, pc.nblk - bb);
+          const int ent = lane < cnt ? __ldg(bt + bb + lane) : 0;
+          for (int xb = 0; xb < cnt; ++xb, ++n) {
+            int phys = __shfl_sync(0xffffffffu, ent, xb);
+            const int st = n % kStages;
+            if (n >= kStages &&
+                !mbar_wait(&sm.empty[st], ((n / kStages) - 1) & 1, p.err, abort_flag))
+              break;
+            if (lane == 0) {
+              const bool valid = (unsigned)phys < (unsigned)p.num_blocks;
+              if (!valid) {
+                record_error(p.err, kErrBounds);
+                phys = 0;
+              }
+              sm.stage_valid[st] = valid;
+              const long long tile = ((long long)phys * Hkv + k) * (kTileBytes / 2);
+              mbar_arrive_expect_tx(&sm.full[st], kStageBytes);
+              bulk_copy_g2s(sm.ring[st], p.k_pool + tile, kTileBytes, &sm.full[st], pol);
+              bulk_copy_g2s(sm.ring[st] + kTileBytes, p.v_pool + tile, kTileBytes, &sm.full[st],
+                            pol);
+            }
+            __syncwarp();
+          }
+        }
+        ++j;
+        // ---- advance to the next row-group ---------------------------------
+        g += nb;
+        if (++k == Hkv) {
+          k = 0;
+          if (++i == ri.qr) {
+            i = 0;
+            do {
+              ++r;
+              if (r >= R) break;
+              ri = load_request(p, r);
+            } while (!ri.decode);
+            if (r >= R) break;
+          }
+          nb = ceil_div(ri.L - ri.qr + i + 1, kBlockSize);
+        }
+      }
+    }
+    // End marker: no more pieces for this CTA.
+    const int ub = j & 1;
+    if (j < 2 || mbar_wait(&sm.qempty[ub], ((j >> 1) - 1) & 1, p.err, abort_flag)) {
+      if (lane == 0) {
+        sm.pinfo[ub].row = kEndRow;
+        mbar_arrive(&sm.qfull[ub]);
       }
     }
     return;
@@ -423,21 +524,22 @@ __global__ void __launch_bounds__(kDecodeThreads, (G <= 6 ? 2 : 1))
   constexpr int F = BM::F;
   constexpr int kConsumerThreads = kConsumerWarps * 32;
   const int cw = warp;
-  const int ct = tid;  // 0..127: the output dim this thread writes
+  const int ct = tid;  // 0..127: the output dim this thread writes in the epilogue
   const int c = lane & 15;
   const int b0bit = lane & 1;
   uint32_t n_base = 0;
-  int j = 0;
-  for (int u = blockIdx.x; u < T; u += gridDim.x, ++j) {
+  for (int j = 0;; ++j) {
     const int ub = j & 1;
     const bool have_q = mbar_wait(&sm.qfull[ub], (j >> 1) & 1, p.err, abort_flag);
-    UnitInfo ui = sm.uinfo[ub];
+    Piece pc = sm.pinfo[ub];
+    const bool is_end = !have_q || pc.row == kEndRow;
     // Range checks make every later index safe even after an abort.
-    const bool in_range = ui.row >= 0 && ui.row < p.num_q_tokens && ui.k >= 0 &&
-                          ui.k < Hkv && ui.nblk >= 0 && ui.nblk <= p.max_blocks && ui.S >= 1 &&
-                          ui.base >= 0 && ui.base + ui.S <= p.max_units && ui.unit >= ui.base &&
-                          ui.unit < ui.base + ui.S;
-    if (!(have_q && in_range)) ui.nblk = 0;
+    const bool in_range = !is_end && pc.row >= 0 && pc.row < p.num_q_tokens && pc.k >= 0 &&
+                          pc.k < Hkv && pc.nblk >= 1 && pc.nblk <= p.max_blocks &&
+                          pc.b0 >= 0 && pc.S >= 1 && pc.c0 >= 0 &&
+                          2 * (pc.c0 + pc.S) <= p.num_slots && pc.slot >= 0 &&
+                          pc.slot < p.num_slots;
+    if (!in_range) pc.nblk = 0;
     float2 qf[G][4];
     #pragma unroll
     for (int hs = 0; hs < G; ++hs) {
@@ -450,7 +552,7 @@ __global__ void __launch_bounds__(kDecodeThreads, (G <= 6 ? 2 : 1))
       qf[hs][3] = fmul2(bf16x2_to_float2(w.w), s2);
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.qempty[ub]);
+    if (lane == 0 && !is_end) mbar_arrive(&sm.qempty[ub]);
 
     float m[G], lsum[F];
     float2 acc[G][4];
@@ -463,17 +565,17 @@ __global__ void __launch_bounds__(kDecodeThreads, (G <= 6 ? 2 : 1))
     #pragma unroll
     for (int jj = 0; jj < F; ++jj) lsum[jj] = 0.f;
 
-    for (int bi = (int)((cw - n_base) & (kConsumerWarps - 1)); bi < ui.nblk; bi += kConsumerWarps) {
+    for (int bi = (int)((cw - n_base) & (kConsumerWarps - 1)); bi < pc.nblk; bi += kConsumerWarps) {
       const uint32_t n = n_base + bi;
       const int st = n % kStages;
       const bool arrived = mbar_wait(&sm.full[st], (n / kStages) & 1, p.err, abort_flag);
-      const int first = (ui.b0 + bi) * kBlockSize;
-      const int nvalid = (arrived && sm.stage_valid[st]) ? min(kBlockSize, ui.limit - first) : 0;
+      const int first = (pc.b0 + bi) * kBlockSize;
+      const int nvalid = (arrived && sm.stage_valid[st]) ? min(kBlockSize, pc.limit - first) : 0;
       BM::run(sm.ring[st], nvalid, lane, qf, m, lsum, acc, sm.pbuf[cw]);
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.empty[st]);
     }
-    n_base += ui.nblk;
+    n_base += pc.nblk;
 
     // ---- combine the four warps' states -----------------------------------
     float lall[G];
@@ -519,18 +621,23 @@ __global__ void __launch_bounds__(kDecodeThreads, (G <= 6 ? 2 : 1))
         sm.comb_m[cw][h] = m[h];
         sm.comb_l[cw][h] = lall[h];
       }
-      sm.wait_ok[cw] = have_q && in_range;
+      sm.wait_ok[cw] = in_range;
+      sm.end_flag[cw] = is_end;
     }
     named_barrier(1, kConsumerThreads);
 
-    // When every warp's wait succeeded, all four hold the same unit info (it
-    // cannot change before all four have released the q buffer), so `ok` is
-    // uniform across the consumer warps and so are the barriers below.
-    bool ok = true;
+    // When every warp's wait succeeded, all four hold the same piece (it
+    // cannot change before all four have released the q buffer), so `ok` and
+    // `end` are uniform across the consumer warps and so are the barriers.
+    bool ok = true, end = false;
     #pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) ok = ok && sm.wait_ok[w];
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      ok = ok && sm.wait_ok[w];
+      end = end || sm.end_flag[w];
+    }
+    ok = ok && !end;
     const int d = ct;
-    const long long out_row = ((long long)ui.row * p.num_q_heads + (long long)ui.k * G) * kHeadDim;
+    const long long out_row = ((long long)pc.row * p.num_q_heads + (long long)pc.k * G) * kHeadDim;
     float res[G];
     #pragma unroll
     for (int h = 0; h < G; ++h) {
@@ -545,62 +652,64 @@ __global__ void __launch_bounds__(kDecodeThreads, (G <= 6 ? 2 : 1))
         den += e * sm.comb_l[w][h];
       }
       res[h] = den > 0.f ? num / den : 0.f;
-      if (ok && ui.S > 1) {
-        const long long slot = (long long)ui.unit * G + h;
+      if (ok && pc.S > 1) {
+        const long long slot = (long long)pc.slot * G + h;
         p.ws_o[slot * kHeadDim + d] = res[h];
-        if (d == 0) {
-          p.ws_ml[slot * 2] = M;
-          p.ws_ml[slot * 2 + 1] = den;
-        }
+        if (d == 0) *reinterpret_cast<float2*>(p.ws_ml + slot * 2) = make_float2(M, den);
       }
     }
-    if (ok && ui.S == 1) {
+    if (ok && pc.S == 1) {
       #pragma unroll
       for (int h = 0; h < G; ++h) p.out[out_row + h * kHeadDim + d] = __float2bfloat16_rn(res[h]);
     }
-    if (ok && ui.S > 1) {
+    if (ok && pc.S > 1) {
       __threadfence();
       named_barrier(1, kConsumerThreads);
       if (ct == 0) {
-        int* cnt = p.ws_cnt + (long long)ui.row * Hkv + ui.k;
+        int* cnt = p.ws_cnt + (long long)pc.row * Hkv + pc.k;
         const int old = atomicAdd(cnt, 1);
-        const int last = (old == ui.S - 1);
-        if (last) *cnt = 0;  // every split has arrived: leave the counter at zero
+        const int last = (old == pc.S - 1);
+        if (last) *cnt = 0;  // every piece has arrived: leave the counter at zero
         sm.is_last = last;
       }
       named_barrier(1, kConsumerThreads);
       if (sm.is_last) {
-        // Log-sum-exp merge of the row's splits, in split order.
+        // Log-sum-exp merge of the row-group's pieces, in piece order, one
+        // pass with a running maximum; loads of four pieces are in flight at
+        // once.
         __threadfence();
-        #pragma unroll 1
-        for (int h = 0; h < G; ++h) {
-          float M = kNegBig;
-          for (int s = 0; s < ui.S; ++s)
-            M = fmaxf(M, __ldcg(p.ws_ml + ((long long)(ui.base + s) * G + h) * 2));
-          float num = 0.f, den = 0.f;
-          for (int s = 0; s < ui.S; ++s) {
-            const long long slot = (long long)(ui.base + s) * G + h;
-            const float w = fast_exp2(__ldcg(p.ws_ml + slot * 2) - M) * __ldcg(p.ws_ml + slot * 2 + 1);
-            num += w * __ldcg(p.ws_o + slot * kHeadDim + d);
-            den += w;
+        float M[G], num[G], den[G];
+        #pragma unroll
+        for (int h = 0; h < G; ++h) { M[h] = kNegBig; num[h] = 0.f; den[h] = 0.f; }
+        #pragma unroll 4
+        for (int s = 0; s < pc.S; ++s) {
+          const int slot = 2 * (pc.c0 + s) + ((s == 0 && pc.odd0) ? 1 : 0);
+          #pragma unroll
+          for (int h = 0; h < G; ++h) {
+            const long long sl = (long long)slot * G + h;
+            const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.ws_ml + sl * 2));
+            const float o = __ldcg(p.ws_o + sl * kHeadDim + d);
+            const float Mn = fmaxf(M[h], ml.x);
+            const float a = fast_exp2(M[h] - Mn), w = fast_exp2(ml.x - Mn) * ml.y;
+            num[h] = num[h] * a + w * o;
+            den[h] = den[h] * a + w;
+            M[h] = Mn;
           }
-          p.out[out_row + h * kHeadDim + d] = __float2bfloat16_rn(num / den);
         }
+        #pragma unroll
+        for (int h = 0; h < G; ++h)
+          p.out[out_row + h * kHeadDim + d] = __float2bfloat16_rn(num[h] / den[h]);
       }
     }
-    // End of unit: agree on whether to stop (abort is set asynchronously, so
-    // one thread samples it and the barrier publishes the sample).
-    if (ct == 0) sm.stop = *abort_flag;
+    // Close the piece: nobody rewrites comb/is_last before everyone is done.
     named_barrier(1, kConsumerThreads);
-    if (sm.stop) break;
+    if (end) break;
   }
 }
 
 template <int G>
-cudaError_t launch_decode_g(const DecodeParams& p, int sm_count, cudaStream_t stream) {
-  const size_t smem = sizeof(DecodeSmem<G>) + (size_t)(p.num_reqs + 1) * sizeof(int);
-  // The opt-in shared-memory limit is set once per device for the largest
-  // plan (kMaxReqs requests).
+cudaError_t launch_decode_g(const DecodeParams& p, int grid, cudaStream_t stream) {
+  const size_t smem = sizeof(DecodeSmem<G>);
   static unsigned long long configured = 0;  // bit per device ordinal
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -608,45 +717,53 @@ cudaError_t launch_decode_g(const DecodeParams& p, int sm_count, cudaStream_t st
   const unsigned long long bit = 1ull << (dev & 63);
   if (!(__atomic_load_n(&configured, __ATOMIC_ACQUIRE) & bit)) {
     e = cudaFuncSetAttribute(decode_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)(sizeof(DecodeSmem<G>) + (kMaxReqs + 1) * sizeof(int)));
+                             (int)smem);
     if (e != cudaSuccess) return e;
     __atomic_fetch_or(&configured, bit, __ATOMIC_RELEASE);
   }
-  int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<G>, kDecodeThreads, smem);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kDecodeThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = p.pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, decode_kernel<G>, p);
   if (e != cudaSuccess) return e;
-  per_sm = max(1, per_sm);
-  const int grid = max(1, min(p.max_units, sm_count * per_sm));
-  decode_kernel<G><<<grid, kDecodeThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-int decode_target_units(int sm_count) { return sm_count * 4; }
+int decode_ctas_per_sm(int group) { return group <= 6 ? 2 : 1; }
+
+int decode_grid(int sm_count, int group) { return sm_count * decode_ctas_per_sm(group); }
 
 WorkspaceLayout decode_workspace_layout(int num_q_tokens, int num_kv_heads, int group,
-                                        int target_units) {
+                                        int sm_count) {
   WorkspaceLayout w;
   auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
-  w.max_units = target_units + num_q_tokens * num_kv_heads;
+  w.num_slots = 2 * sm_count * 2;  // two partial pieces per CTA, up to two CTAs per SM
   w.cnt_off = 0;
   w.ml_off = up((size_t)num_q_tokens * num_kv_heads * sizeof(int));
-  w.o_off = w.ml_off + up((size_t)w.max_units * group * 2 * sizeof(float));
-  w.total = w.o_off + up((size_t)w.max_units * group * kHeadDim * sizeof(float));
+  w.o_off = w.ml_off + up((size_t)w.num_slots * group * 2 * sizeof(float));
+  w.total = w.o_off + up((size_t)w.num_slots * group * kHeadDim * sizeof(float));
   return w;
 }
 
-cudaError_t launch_decode(const DecodeParams& p, int group, int sm_count, cudaStream_t stream) {
+cudaError_t launch_decode(const DecodeParams& p, int group, int grid, cudaStream_t stream) {
   switch (group) {
-    case 1: return launch_decode_g<1>(p, sm_count, stream);
-    case 2: return launch_decode_g<2>(p, sm_count, stream);
-    case 3: return launch_decode_g<3>(p, sm_count, stream);
-    case 4: return launch_decode_g<4>(p, sm_count, stream);
-    case 5: return launch_decode_g<5>(p, sm_count, stream);
-    case 6: return launch_decode_g<6>(p, sm_count, stream);
-    case 7: return launch_decode_g<7>(p, sm_count, stream);
-    case 8: return launch_decode_g<8>(p, sm_count, stream);
+    case 1: return launch_decode_g<1>(p, grid, stream);
+    case 2: return launch_decode_g<2>(p, grid, stream);
+    case 3: return launch_decode_g<3>(p, grid, stream);
+    case 4: return launch_decode_g<4>(p, grid, stream);
+    case 5: return launch_decode_g<5>(p, grid, stream);
+    case 6: return launch_decode_g<6>(p, grid, stream);
+    case 7: return launch_decode_g<7>(p, grid, stream);
+    case 8: return launch_decode_g<8>(p, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -21,6 +22,7 @@ struct AppendParams {
   int num_tokens;
   int num_kv_heads;
   int num_blocks;
+  int pdl;  // launch with programmatic stream serialization
 };
 
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
@@ -36,8 +38,8 @@ struct DecodeParams {
   const int32_t* qsl;
   __nv_bfloat16* out;
   int* ws_cnt;    // [num_q_tokens * num_kv_heads] merge counters, zero between calls
-  float* ws_ml;   // [max_units, g, 2] (max, normaliser) of each split, log2 domain
-  float* ws_o;    // [max_units, g, 128] normalised partial output of each split
+  float* ws_ml;   // [num_slots, g, 2] (max, normaliser) of each partial piece, log2 domain
+  float* ws_o;    // [num_slots, g, 128] normalised partial output of each piece
   int* err;
   int num_reqs;
   int num_q_tokens;
@@ -47,24 +49,55 @@ struct DecodeParams {
   int max_blocks;
   float scale_log2;   // scale * log2(e)
   int prefill_min_q;  // requests with q_r >= this are left to the prefill kernel
-  int target_units;   // split policy: aim for about this many work units
-  int max_units;      // workspace capacity in units
-  int min_chunk;      // smallest split, in blocks
+  int num_slots;      // partial-piece slots in the workspace (>= 2 * grid)
+  int min_chunk;      // smallest per-CTA range, in blocks
+  int align;          // snap ranges to row-group boundaries when lengths are uniform
+  int stages;         // ring stages in use (<= the compiled ring; 0 = all)
+  int pdl;            // launch with programmatic stream serialization
 };
 
 // Workspace carve-up shared by the host code that sizes it and the launcher.
 struct WorkspaceLayout {
   size_t cnt_off, ml_off, o_off, total;
-  int max_units;
+  int num_slots;
 };
 
 WorkspaceLayout decode_workspace_layout(int num_q_tokens, int num_kv_heads, int group,
-                                        int target_units);
+                                        int sm_count);
 
-// Returns the grid the decode launch will use (for workspace sizing).
-int decode_target_units(int sm_count);
+int decode_grid(int sm_count, int group);
 
-cudaError_t launch_decode(const DecodeParams& p, int group, int sm_count,
-                          cudaStream_t stream);
+cudaError_t launch_decode(const DecodeParams& p, int group, int grid, cudaStream_t stream);
+
+// Chunked-prefill attention on tcgen05 tensor cores (requests with
+// q_r >= prefill_min_q).
+struct PrefillParams {
+  const int32_t* block_tables;
+  const int32_t* seq_lens;
+  const int32_t* qsl;
+  __nv_bfloat16* out;
+  int* err;
+  int num_reqs;
+  int num_q_tokens;
+  int num_q_heads;
+  int num_kv_heads;
+  int num_blocks;
+  int max_blocks;
+  float scale_log2;
+  int prefill_min_q;
+  int pdl;
+};
+
+struct PrefillLaunch {
+  CUtensorMap qmap;  // q as [tokens][Hq][128], box (64, g, 128/g)
+  CUtensorMap kmap;  // k_pool as [blocks*Hkv*16][128], box (64, 16), 128-byte swizzle
+  CUtensorMap vmap;  // v_pool, same
+  PrefillParams p;
+  int grid;
+};
+
+int prefill_tokens_per_tile(int group);
+
+cudaError_t launch_prefill(const PrefillLaunch& L, int group, cudaStream_t stream);
 
 }  // namespace pkv

@@ -1,0 +1,461 @@
+// pkv_prefill.cu -- ragged chunked-prefill attention on tcgen05 tensor cores.
+//
+// A prefill chunk of q_r query tokens attends causally to the keys earlier
+// chunks wrote plus its own (The Serving Playbook, "Chunked prefill"); with
+// many query rows per request the step is a real dense contraction, so QK^T
+// and PV run on the 5th-generation tensor cores with fp32 accumulators in
+// TMEM, FlashAttention-style: Q, K and V tiles are staged in shared memory,
+// the score matrix never leaves the chip, and an online softmax carries the
+// running maximum and normaliser across key tiles (LLM 7 - Efficient LLM
+// Serving, sec. 2).
+//
+// Tiling.  A work item is (request, KV head, q-tile).  Its 128 MMA rows are
+// (query token, head of the group) pairs -- T_q = floor(128 / g) tokens times
+// the g query heads that share the KV head -- so every K/V tile loaded for
+// the item serves all g heads.  Key tiles are 128 keys = 8 pool blocks; each
+// 16-row block tile is fetched through the block table with a 2-D TMA copy
+// of the pool viewed as [blocks * Hkv * 16 rows, 128] (128-byte swizzle);
+// blocks past the request's end are fetched at an out-of-range row, which TMA
+// fills with zeros.  Q comes in with one 3-D TMA copy per half (d, head,
+// token).
+//
+// Roles (192 threads): warps 0-3 own one TMEM lane / MMA row each and run the
+// softmax and the epilogue; warp 4 issues TMA copies; one thread of warp 5
+// issues tcgen05.mma and commits.  Per key tile: S = Q K^T (8 MMAs of K=16)
+// into TMEM, softmax reads S, writes P (bf16, swizzled) to shared memory,
+// then O += P V (8 MMAs) accumulates in TMEM.  O is rescaled in TMEM only
+// when a row's maximum grows by more than 2^8 (the result is exact either
+// way: O and the normaliser always share the same reference maximum).
+#include <climits>
+
+#include "pkv_internal.h"
+#include "pkv_tc.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kPfThreads = 192;
+constexpr int kTileRows = 128;               // MMA M
+constexpr int kKeyTile = 128;                // MMA N for S, K for PV
+constexpr int kHalfBytes = kTileRows * 128;  // one 64-column half of a 128-row tile
+constexpr uint32_t kTmemCols = 256;          // S: cols 0..127, O: cols 128..255
+constexpr float kRescaleLog2 = 8.0f;
+constexpr float kNegBig = -1.0e30f;
+
+struct Item {
+  int r, k;
+  int row0;   // first query row of the tile
+  int nt;     // valid tokens in the tile
+  int pos0;   // position of its first token
+  int L;      // request length (keys)
+  int nj;     // key tiles
+  int end;    // no more items
+};
+
+struct __align__(1024) PfSmem {
+  uint8_t q[2][kHalfBytes];      // Q: d 0..63 | d 64..127
+  uint8_t k[2][2][kHalfBytes];   // [stage][d half]
+  uint8_t v[2][2][kHalfBytes];   // [stage][d half]
+  uint8_t p[2][kHalfBytes];      // P: keys 0..63 | keys 64..127
+  uint64_t q_full, q_empty;
+  uint64_t k_full[2], v_full[2], kv_empty[2];
+  uint64_t s_full, p_full, o_full, o_empty;
+  Item items[2];
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+__device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+struct PfReq {
+  int q0, qr, L, ntiles;
+  bool ok;
+};
+
+__device__ __forceinline__ PfReq load_pf_request(const PrefillParams& p, int r, int tq) {
+  PfReq a;
+  a.q0 = __ldg(p.qsl + r);
+  const int q1 = __ldg(p.qsl + r + 1);
+  a.L = __ldg(p.seq_lens + r);
+  a.qr = q1 - a.q0;
+  a.ok = a.q0 >= 0 && a.qr >= p.prefill_min_q && q1 <= p.num_q_tokens && a.qr <= a.L &&
+         a.L <= p.max_blocks * kBlockSize;
+  a.ntiles = a.ok ? ceil_div(a.qr, tq) : 0;
+  return a;
+}
+
+template <int G>
+__global__ void __launch_bounds__(kPfThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+                   const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
+  constexpr int TQ = kTileRows / G;   // query tokens per item
+  constexpr int ROWS = TQ * G;        // MMA rows in use
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 128-byte swizzled tiles need 1024-byte aligned shared addresses.
+  const uint32_t raw = smem_u32(smem_raw);
+  PfSmem& sm = *reinterpret_cast<PfSmem*>(smem_raw + (((raw + 1023u) & ~1023u) - raw));
+  volatile int* abort_flag = &sm.abort_flag;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int Hkv = p.num_kv_heads;
+
+  if (tid == 0) {
+    mbar_init(&sm.q_full, 1);
+    mbar_init(&sm.q_empty, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&sm.k_full[s], 1);
+      mbar_init(&sm.v_full[s], 1);
+      mbar_init(&sm.kv_empty[s], 1);
+    }
+    mbar_init(&sm.s_full, 1);
+    mbar_init(&sm.p_full, 4);
+    mbar_init(&sm.o_full, 1);
+    mbar_init(&sm.o_empty, 4);
+    sm.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 4 && lane == 0) {
+    prefetch_tensormap(&qmap);
+    prefetch_tensormap(&kmap);
+    prefetch_tensormap(&vmap);
+  }
+  // Q rows no item writes stay zero (their S and O rows are never read).
+  if constexpr (ROWS < kTileRows) {
+    constexpr int kPad = (kTileRows - ROWS) * 8;  // 16-byte chunks per half
+    for (int i = tid; i < 2 * kPad; i += kPfThreads) {
+      const int half = i / kPad;
+      const int rest = i % kPad;
+      const int row = ROWS + rest / 8, chunk = rest % 8;
+      *reinterpret_cast<uint4*>(sm.q[half] + (row / 8) * 1024 + (row % 8) * 128 + chunk * 16) =
+          make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async_smem();
+  }
+  if (warp == 5) {
+    tmem_alloc(&sm.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  grid_dependency_wait();
+  allow_dependent_launch();
+
+  if (warp == 4) {
+    // ========================= TMA producer ===============================
+    int n_item = 0, tile_ctr = 0;
+    long long item = blockIdx.x;  // global item index handled next
+    long long base = 0;           // items before the current request batch
+    const int oob_row = p.num_blocks * Hkv * kBlockSize;
+    for (int b = 0; b < p.num_reqs && !*abort_flag; b += 32) {
+      const int rr = b + lane;
+      PfReq rq = {0, 0, 0, 0, false};
+      if (rr < p.num_reqs) rq = load_pf_request(p, rr, TQ);
+      const long long cnt = (long long)rq.ntiles * Hkv;
+      long long incl = cnt;
+      #pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      const long long excl = incl - cnt;
+      const long long total = __shfl_sync(0xffffffffu, incl, 31);
+      while (item < base + total && !*abort_flag) {
+        const long long rel = item - base;
+        const unsigned own = __ballot_sync(0xffffffffu, cnt > 0 && excl <= rel && rel < incl);
+        const int src = __ffs(own) - 1;
+        const long long local = rel - __shfl_sync(0xffffffffu, excl, src);
+        const int r = b + src;
+        const int q0 = __shfl_sync(0xffffffffu, rq.q0, src);
+        const int qr = __shfl_sync(0xffffffffu, rq.qr, src);
+        const int L = __shfl_sync(0xffffffffu, rq.L, src);
+        const int ntiles = __shfl_sync(0xffffffffu, rq.ntiles, src);
+        // heavier (later) q-tiles first
+        const int qt = ntiles - 1 - (int)(local / Hkv);
+        const int k = (int)(local % Hkv);
+        Item it;
+        it.r = r; it.k = k;
+        it.row0 = q0 + qt * TQ;
+        it.nt = min(TQ, qr - qt * TQ);
+        it.pos0 = L - qr + qt * TQ;
+        it.L = L;
+        it.nj = (it.pos0 + it.nt - 1) / kKeyTile + 1;
+        it.end = 0;
+        if (n_item >= 1 && !mbar_wait(&sm.q_empty, (n_item - 1) & 1, p.err, abort_flag)) break;
+        if (lane == 0) {
+          sm.items[n_item & 1] = it;
+          mbar_arrive_expect_tx(&sm.q_full, 2u * 64u * ROWS * 2u);
+          tma_load_3d(sm.q[0], &qmap, 0, k * G, it.row0, &sm.q_full);
+          tma_load_3d(sm.q[1], &qmap, 64, k * G, it.row0, &sm.q_full);
+        }
+        const int nbl = ceil_div(L, kBlockSize);
+        const int32_t* bt = p.block_tables + (long long)r * p.max_blocks;
+        for (int j = 0; j < it.nj; ++j, ++tile_ctr) {
+          const int st = tile_ctr & 1;
+          if (tile_ctr >= 2 &&
+              !mbar_wait(&sm.kv_empty[st], ((tile_ctr >> 1) - 1) & 1, p.err, abort_flag))
+            break;
+          const int blk = j * 8 + (lane & 7);
+          int rowc = oob_row;  // zero-filled by TMA
+          if (lane < 8 && blk < nbl) {
+            const int phys = __ldg(bt + blk);
+            if ((unsigned)phys < (unsigned)p.num_blocks) rowc = (phys * Hkv + k) * kBlockSize;
+            else record_error(p.err, kErrBounds);
+          }
+          int rows[8];
+          #pragma unroll
+          for (int x = 0; x < 8; ++x) rows[x] = __shfl_sync(0xffffffffu, rowc, x);
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&sm.k_full[st], 2u * kHalfBytes);
+            #pragma unroll
+            for (int x = 0; x < 8; ++x) {
+              tma_load_2d(sm.k[st][0] + x * 2048, &kmap, 0, rows[x], &sm.k_full[st]);
+              tma_load_2d(sm.k[st][1] + x * 2048, &kmap, 64, rows[x], &sm.k_full[st]);
+            }
+            mbar_arrive_expect_tx(&sm.v_full[st], 2u * kHalfBytes);
+            #pragma unroll
+            for (int x = 0; x < 8; ++x) {
+              tma_load_2d(sm.v[st][0] + x * 2048, &vmap, 0, rows[x], &sm.v_full[st]);
+              tma_load_2d(sm.v[st][1] + x * 2048, &vmap, 64, rows[x], &sm.v_full[st]);
+            }
+          }
+          __syncwarp();
+        }
+        ++n_item;
+        item += gridDim.x;
+      }
+      base += total;
+    }
+    // end marker
+    if (n_item == 0 || mbar_wait(&sm.q_empty, (n_item - 1) & 1, p.err, abort_flag)) {
+      if (lane == 0) {
+        sm.items[n_item & 1].end = 1;
+        mbar_arrive(&sm.q_full);
+      }
+    }
+  } else if (warp == 5) {
+    // ========================= MMA issuer =================================
+    if (lane == 0) {
+      constexpr uint32_t kIdescS = idesc_bf16_f32(kTileRows, kKeyTile, 0, 0);
+      constexpr uint32_t kIdescO = idesc_bf16_f32(kTileRows, kHeadDim, 0, 1);
+      const uint32_t tS = tmem, tO = tmem + kKeyTile;
+      int tile_ctr = 0;
+      for (int n_item = 0;; ++n_item) {
+        if (!mbar_wait(&sm.q_full, n_item & 1, p.err, abort_flag)) break;
+        const Item it = sm.items[n_item & 1];
+        if (it.end) break;
+        tc_fence_after();
+        bool ok = true;
+        for (int j = 0; j < it.nj && ok; ++j, ++tile_ctr) {
+          const int st = tile_ctr & 1;
+          ok = mbar_wait(&sm.k_full[st], (tile_ctr >> 1) & 1, p.err, abort_flag);
+          tc_fence_after();
+          #pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t a = smem_desc_sw128(smem_u32(sm.q[kk >> 2]) + (kk & 3) * 32, 16, 1024);
+            const uint64_t b = smem_desc_sw128(smem_u32(sm.k[st][kk >> 2]) + (kk & 3) * 32, 16, 1024);
+            tc_mma_f16_ss(tS, a, b, kIdescS, kk > 0);
+          }
+          tc_commit(&sm.s_full);
+          ok = ok && mbar_wait(&sm.p_full, tile_ctr & 1, p.err, abort_flag);
+          ok = ok && mbar_wait(&sm.v_full[st], (tile_ctr >> 1) & 1, p.err, abort_flag);
+          if (j == 0 && n_item > 0)
+            ok = ok && mbar_wait(&sm.o_empty, (n_item - 1) & 1, p.err, abort_flag);
+          tc_fence_after();
+          #pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t a = smem_desc_sw128(smem_u32(sm.p[kk >> 2]) + (kk & 3) * 32, 16, 1024);
+            // V is MN-major (d contiguous): atoms of 64 d x 8 keys; the two d
+            // halves are kHalfBytes apart, 8-key groups 1024 bytes apart.
+            const uint64_t b = smem_desc_sw128(smem_u32(sm.v[st][0]) + kk * 2048, kHalfBytes, 1024);
+            tc_mma_f16_ss(tO, a, b, kIdescO, j > 0 || kk > 0);
+          }
+          tc_commit(&sm.kv_empty[st]);
+        }
+        tc_commit(&sm.o_full);
+        tc_commit(&sm.q_empty);
+        if (!ok) break;
+      }
+    }
+    __syncwarp();
+  } else {
+    // ===================== softmax + epilogue (warps 0-3) ==================
+    const int row = tid;  // MMA row == TMEM lane
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t tS = tmem + lane_off, tO = tmem + lane_off + kKeyTile;
+    const int t_local = row / G, h = row % G;
+    int tile_ctr = 0;
+    for (int n_item = 0;; ++n_item) {
+      const bool have = mbar_wait(&sm.q_full, n_item & 1, p.err, abort_flag);
+      const Item it = sm.items[n_item & 1];
+      if (!have || it.end) break;
+      const bool valid = row < ROWS && t_local < it.nt;
+      const int prow = valid ? it.pos0 + t_local : -1;  // this row's position
+      float m = kNegBig, l = 0.f;
+      bool ok = true;
+      for (int j = 0; j < it.nj; ++j, ++tile_ctr) {
+        ok = ok && mbar_wait(&sm.s_full, tile_ctr & 1, p.err, abort_flag);
+        tc_fence_after();
+        float s[kKeyTile];
+        #pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, *reinterpret_cast<float(*)[32]>(&s[c * 32]));
+        tc_wait_ld();
+        const int kbase = j * kKeyTile;
+        float mx = -INFINITY;
+        #pragma unroll
+        for (int c = 0; c < kKeyTile; ++c) {
+          s[c] = (kbase + c <= prow) ? s[c] * p.scale_log2 : -INFINITY;
+          mx = fmaxf(mx, s[c]);
+        }
+        float m_use = m;
+        const bool grow = j == 0 ? true : (mx > m + kRescaleLog2);
+        if (j == 0) {
+          m_use = fmaxf(m, mx);
+        } else if (__any_sync(0xffffffffu, grow)) {
+          // O (and l) move to the new reference maximum; rows that do not
+          // grow scale by 1.
+          const float m_new = grow ? fmaxf(m, mx) : m;
+          const float alpha = fast_exp2(m - m_new);
+          #pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            float o[32];
+            tmem_ld32(tO + c * 32, o);
+            tc_wait_ld();
+            #pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+            tmem_st32(tO + c * 32, o);
+          }
+          tc_wait_st();
+          l *= alpha;
+          m_use = m_new;
+        }
+        m = m_use;
+        // P = exp2(s - m) in bf16, row-major keys, 128-byte swizzle; the
+        // normaliser sums the rounded values the MMA will use.
+        float sum = 0.f;
+        uint8_t* prow_base = nullptr;
+        #pragma unroll
+        for (int c = 0; c < 16; ++c) {  // 16-byte chunk c = keys 8c .. 8c+7
+          uint32_t w[4];
+          #pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float p0 = fast_exp2(s[c * 8 + 2 * e] - m);
+            const float p1 = fast_exp2(s[c * 8 + 2 * e + 1] - m);
+            w[e] = pack_bf16x2(p0, p1);
+            const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&w[e]);
+            sum += __low2float(b2) + __high2float(b2);
+          }
+          const int half = c >> 3, cc = c & 7;
+          prow_base = sm.p[half] + (row >> 3) * 1024 + (row & 7) * 128;
+          *reinterpret_cast<uint4*>(prow_base + ((cc ^ (row & 7)) * 16)) =
+              make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        l += sum;
+        // Keys past the request's end inside its last block may hold anything
+        // (even NaN); zero those V rows so that 0 * V stays 0 in the MMA.
+        const int st = tile_ctr & 1;
+        const int tail0 = it.L - kbase;                      // first key >= L in this tile
+        const int tail1 = min(kKeyTile, ceil_div(it.L, kBlockSize) * kBlockSize - kbase);
+        if (warp == 0 && tail0 < tail1 && tail0 >= 0) {
+          ok = ok && mbar_wait(&sm.v_full[st], (tile_ctr >> 1) & 1, p.err, abort_flag);
+          const int nrows = tail1 - tail0;
+          for (int i = lane; i < nrows * 16; i += 32) {
+            const int rr = tail0 + i / 16, half = (i / 8) & 1, chunk = i & 7;
+            *reinterpret_cast<uint4*>(sm.v[st][half] + (rr >> 3) * 1024 + (rr & 7) * 128 +
+                                      chunk * 16) = make_uint4(0, 0, 0, 0);
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.p_full);
+      }
+      // ---- epilogue: O / l -> bf16 -> out ---------------------------------
+      ok = ok && mbar_wait(&sm.o_full, n_item & 1, p.err, abort_flag);
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      __nv_bfloat16* dst = p.out + ((long long)(it.row0 + t_local) * p.num_q_heads +
+                                    (long long)it.k * G + h) * kHeadDim;
+      #pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float o[32];
+        tmem_ld32(tO + c * 32, o);
+        tc_wait_ld();
+        if (valid && ok) {
+          #pragma unroll
+          for (int i = 0; i < 32; i += 8) {
+            uint4 v;
+            v.x = pack_bf16x2(o[i] * inv, o[i + 1] * inv);
+            v.y = pack_bf16x2(o[i + 2] * inv, o[i + 3] * inv);
+            v.z = pack_bf16x2(o[i + 4] * inv, o[i + 5] * inv);
+            v.w = pack_bf16x2(o[i + 6] * inv, o[i + 7] * inv);
+            *reinterpret_cast<uint4*>(dst + c * 32 + i) = v;
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.o_empty);
+      if (!ok) break;
+    }
+  }
+  // Every warp reaches this point (aborts only shorten the loops), so the
+  // allocating warp can always free TMEM.
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 5) tmem_dealloc(tmem, kTmemCols);
+}
+
+template <int G>
+cudaError_t launch_prefill_g(const PrefillLaunch& L, cudaStream_t stream) {
+  const size_t smem = sizeof(PfSmem) + 1024;  // + alignment slack
+  static unsigned long long configured = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (!(__atomic_load_n(&configured, __ATOMIC_ACQUIRE) & bit)) {
+    e = cudaFuncSetAttribute(prefill_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    __atomic_fetch_or(&configured, bit, __ATOMIC_RELEASE);
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(L.grid);
+  cfg.blockDim = dim3(kPfThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = L.p.pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, prefill_kernel<G>, L.qmap, L.kmap, L.vmap, L.p);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int prefill_tokens_per_tile(int group) { return kTileRows / group; }
+
+cudaError_t launch_prefill(const PrefillLaunch& L, int group, cudaStream_t stream) {
+  switch (group) {
+    case 1: return launch_prefill_g<1>(L, stream);
+    case 2: return launch_prefill_g<2>(L, stream);
+    case 3: return launch_prefill_g<3>(L, stream);
+    case 4: return launch_prefill_g<4>(L, stream);
+    case 5: return launch_prefill_g<5>(L, stream);
+    case 6: return launch_prefill_g<6>(L, stream);
+    case 7: return launch_prefill_g<7>(L, stream);
+    case 8: return launch_prefill_g<8>(L, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace pkv

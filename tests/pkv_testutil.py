@@ -63,13 +63,15 @@ def assert_close(got: np.ndarray, want: np.ndarray, what: str = ""):
     return mx, mean
 
 
-def sampled_rows_oracle(inp: wl.StepInputs, rows: list[tuple[int, int]]):
-    """Oracle outputs for sampled (request, query index) rows, computed on a
-    relabelled sub-problem: row i of request r (q_r queries, length L) is the
-    single query of a request of length L - q_r + i + 1 with the same table,
-    and only the blocks those rows read are copied to the host (gathered into
-    a compact pool -- physical placement does not change the result).
-    Uses the device pools as they are (call after the GPU append)."""
+def snapshot_rows(inp: wl.StepInputs, rows: list[tuple[int, int]]) -> dict:
+    """Host copy of everything the oracle needs for sampled (request, query
+    index) rows, taken BEFORE the GPU step runs: the rows' q, the pool blocks
+    they read (pre-append contents) and this step's new K/V with their slots.
+
+    Row i of request r (q_r queries, length L) is the single query of a
+    request of length L - q_r + i + 1 with the same table; only the blocks
+    those rows read are copied, gathered into a compact pool (physical
+    placement does not change the result)."""
     bs = inp.shape.block_size
     qsl = inp.query_start_loc.cpu().numpy()
     sl = inp.seq_lens.cpu().numpy()
@@ -84,13 +86,27 @@ def sampled_rows_oracle(inp: wl.StepInputs, rows: list[tuple[int, int]]):
     uniq = np.unique(np.concatenate(phys_lists)).astype(np.int64)
     remap = {int(b): n for n, b in enumerate(uniq)}
     idx = torch.from_numpy(uniq).to(inp.k_pool.device)
-    kp = wl.bf16_bits(inp.k_pool.index_select(0, idx))
-    vp = wl.bf16_bits(inp.v_pool.index_select(0, idx))
     maxb = max(len(p) for p in phys_lists)
     sub_bt = np.full((len(rows), maxb), -1, np.int32)
     for n, pl in enumerate(phys_lists):
         sub_bt[n, :len(pl)] = [remap[int(b)] for b in pl]
-    q = wl.bf16_bits(inp.q[torch.tensor(qrows, device=inp.q.device)])
-    want = oracle.paged_attention(q, kp, vp, sub_bt, np.array(lens, np.int32),
-                                  np.arange(len(rows) + 1, dtype=np.int32), inp.scale)
-    return qrows, want
+    slots = inp.slot_mapping.cpu().numpy()
+    sub_slots = np.array([remap[int(s) // bs] * bs + int(s) % bs
+                          if s >= 0 and int(s) // bs in remap else -1 for s in slots], np.int64)
+    return dict(qrows=qrows, lens=np.array(lens, np.int32), bt=sub_bt,
+                q=wl.bf16_bits(inp.q[torch.tensor(qrows, device=inp.q.device)]),
+                k_pool=wl.bf16_bits(inp.k_pool.index_select(0, idx)),
+                v_pool=wl.bf16_bits(inp.v_pool.index_select(0, idx)),
+                k_new=wl.bf16_bits(inp.k_new), v_new=wl.bf16_bits(inp.v_new),
+                slots=sub_slots, scale=inp.scale)
+
+
+def snapshot_oracle(snap: dict, appended: bool = True):
+    """Oracle outputs (fp64) of the snapshotted rows, after the oracle's own
+    append of this step's new K/V when the GPU step appended too."""
+    kp, vp = snap["k_pool"], snap["v_pool"]
+    if appended:
+        kp, vp = oracle.append(snap["k_new"], snap["v_new"], snap["slots"], kp, vp)
+    n = len(snap["qrows"])
+    return oracle.paged_attention(snap["q"], kp, vp, snap["bt"], snap["lens"],
+                                  np.arange(n + 1, dtype=np.int32), snap["scale"])

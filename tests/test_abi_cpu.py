@@ -64,7 +64,7 @@ def _attn(lib, dims, null_q=False):
     (dict(block_size=32), b.PKV_ERR_UNSUPPORTED),
     (dict(num_q_heads=13), b.PKV_ERR_INVALID),
     (dict(num_q_heads=18), b.PKV_ERR_UNSUPPORTED),      # group of 9
-    (dict(num_reqs=5000), b.PKV_ERR_UNSUPPORTED),
+    (dict(num_reqs=70000), b.PKV_ERR_UNSUPPORTED),
     (dict(num_kv_heads=0), b.PKV_ERR_INVALID),
     (dict(num_q_tokens=-1), b.PKV_ERR_INVALID),
 ])

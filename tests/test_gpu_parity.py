@@ -17,7 +17,7 @@ from paged_kv_cache_195_gb300 import build as pkv_build
 from paged_kv_cache_195_gb300 import workloads as wl
 
 from pkv_testutil import (assert_close, gpu_step, host_copy, oracle_full,
-                          oracle_pools_after_append, sampled_rows_oracle, to_f64)
+                          oracle_pools_after_append, snapshot_oracle, snapshot_rows, to_f64)
 
 pytestmark = pytest.mark.gpu
 
@@ -156,6 +156,8 @@ def test_two_chunks_equal_one_chunk():
     prefix, q1, q2 = 37, 20, 45
     one = wl.StepShape("c", [prefix + q1 + q2], [q1 + q2], 16, 4, seed=21)
     inp = wl.make_step(one, device="cuda")
+    h = host_copy(inp)
+    kp, vp = oracle_pools_after_append(h)
     full = gpu_step(inp).clone()
     outs = []
     for lo, hi, L in ((0, q1, prefix + q1), (q1, q1 + q2, prefix + q1 + q2)):
@@ -165,7 +167,7 @@ def test_two_chunks_equal_one_chunk():
                               inp.scale)
         outs.append(o)
     two = torch.cat(outs)
-    want = oracle_full(host_copy(inp))
+    want = oracle_full(h, kp, vp)
     assert_close(to_f64(two), want, "two chunks")
     assert_close(to_f64(full), want, "one chunk")
 
@@ -186,10 +188,12 @@ def test_explicit_workspace_reused_across_calls():
                          shape.max_blocks_per_req)
     ws = pkv.Workspace(dims)
     pkv.pkv_workspace_init(ws, dims)
+    h = host_copy(inp)
+    kp, vp = oracle_pools_after_append(h)
     a = gpu_step(inp, workspace=ws).clone()
     b = gpu_step(inp, append=False, workspace=ws).clone()
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
-    assert_close(to_f64(a), oracle_full(host_copy(inp)), "workspace")
+    assert_close(to_f64(a), oracle_full(h, kp, vp), "workspace")
 
 
 def test_bad_block_id_is_reported():
@@ -212,22 +216,29 @@ def test_inconsistent_lengths_are_reported():
 # Full-size workloads: sampled rows against the oracle + size-free properties
 # ---------------------------------------------------------------------------
 
-def _sampled(shape, n_rows, seed, layer=0):
-    inp = wl.make_step(shape, device="cuda", layer=layer)
-    out = gpu_step(inp)
-    again = gpu_step(inp, append=False)
-    assert torch.equal(out.view(torch.int16), again.view(torch.int16)), "non-deterministic"
-    assert torch.isfinite(out.float()).all()
+def _sample_rows(shape, n_rows, seed):
     rng = np.random.default_rng(seed)
     rows = []
     for r in rng.choice(shape.num_reqs, size=min(n_rows, shape.num_reqs), replace=False):
         qr = int(shape.q_lens[r])
         if qr:
             rows.append((int(r), int(rng.integers(0, qr))))
-    # always include the longest request and the last query of any prefill
-    rows.append((int(np.argmax(shape.seq_lens)), int(shape.q_lens[np.argmax(shape.seq_lens)]) - 1))
-    qrows, want = sampled_rows_oracle(inp, rows)
-    got = to_f64(out[torch.tensor(qrows, device="cuda")])
+    # always include the longest request's last query row
+    rl = int(np.argmax(shape.seq_lens))
+    rows.append((rl, int(shape.q_lens[rl]) - 1))
+    return rows
+
+
+def _sampled(shape, n_rows, seed, layer=0, extra_rows=()):
+    inp = wl.make_step(shape, device="cuda", layer=layer)
+    rows = _sample_rows(shape, n_rows, seed) + list(extra_rows)
+    snap = snapshot_rows(inp, rows)
+    out = gpu_step(inp)
+    again = gpu_step(inp, append=False)
+    assert torch.equal(out.view(torch.int16), again.view(torch.int16)), "non-deterministic"
+    assert torch.isfinite(out.float()).all()
+    want = snapshot_oracle(snap)
+    got = to_f64(out[torch.tensor(snap["qrows"], device="cuda")])
     return assert_close(got, want, shape.name)
 
 
@@ -242,14 +253,9 @@ def test_qwen_long_batch_full_size():
 
 
 def test_llama_mixed_full_size():
-    shape = wl.llama_mixed()
-    _sampled(shape, 20, 12)
-    # every prefill request: first, middle and last query rows
-    inp = wl.make_step(shape, device="cuda")
-    out = gpu_step(inp)
+    # sampled decode rows plus the first, middle and last rows of every prefill
     rows = [(r, i) for r in range(248, 256) for i in (0, 255, 511)]
-    qrows, want = sampled_rows_oracle(inp, rows)
-    assert_close(to_f64(out[torch.tensor(qrows, device="cuda")]), want, "prefill rows")
+    _sampled(wl.llama_mixed(), 20, 12, extra_rows=rows)
 
 
 def test_llama_long_context_full_size():
@@ -266,3 +272,44 @@ def test_maximum_request_count():
 def test_very_long_context():
     shape = wl.StepShape("L131072", [131072, 5], [1, 1], 8, 1, seed=16)
     _sampled(shape, 2, 17)
+
+
+# ---------------------------------------------------------------------------
+# Path routing: requests with q_r >= PKV_PREFILL_MIN_Q (default 16) run on the
+# tcgen05 prefill kernel, the rest on the decode kernel; both must agree with
+# the oracle whichever way a request is routed.
+# ---------------------------------------------------------------------------
+
+def _prefill_shape(g, seed, Hkv=2):
+    rng = np.random.default_rng(seed)
+    R = int(rng.integers(1, 5))
+    q = rng.integers(16, 300, size=R)
+    prefix = rng.integers(0, 400, size=R)
+    q[0] = 16 + int(rng.integers(0, 3))         # a short chunk
+    prefix[-1] = 0                               # a fresh prompt
+    seq = (q + prefix).astype(np.int32)
+    return wl.StepShape(f"prefill_g{g}_{seed}", seq, q.astype(np.int32), g * Hkv, Hkv, seed=seed)
+
+
+@pytest.mark.parametrize("g", [1, 2, 3, 4, 5, 6, 7, 8])
+def test_prefill_tensor_core_path(g, monkeypatch):
+    monkeypatch.setenv("PKV_PREFILL_MIN_Q", "16")
+    _full_parity(_prefill_shape(g, 700 + g), poison=True)
+
+
+@pytest.mark.parametrize("route", ["decode_only", "prefill_from_2"])
+def test_both_routes_agree_with_oracle(route, monkeypatch):
+    monkeypatch.setenv("PKV_PREFILL_MIN_Q", "0" if route == "decode_only" else "2")
+    shape = wl.StepShape("mix", [300, 40, 517, 129, 16], [1, 40, 200, 3, 16], 32, 8, seed=41)
+    _full_parity(shape, poison=True)
+
+
+def test_prefill_long_prefix_many_key_tiles(monkeypatch):
+    monkeypatch.setenv("PKV_PREFILL_MIN_Q", "16")
+    shape = wl.StepShape("longprefix", [4096 + 512, 1000 + 64], [512, 64], 32, 8, seed=42)
+    rows = [(0, i) for i in (0, 1, 31, 32, 255, 511)] + [(1, i) for i in (0, 63)]
+    inp = wl.make_step(shape, device="cuda", poison=True)
+    snap = snapshot_rows(inp, rows)
+    out = gpu_step(inp)
+    want = snapshot_oracle(snap)
+    assert_close(to_f64(out[torch.tensor(snap["qrows"], device="cuda")]), want, "long prefix")
