@@ -139,6 +139,34 @@ int pkv_attention(const void *q, const void *k_pool, const void *v_pool,
                   const pkv_dims *dims, void *workspace, size_t workspace_bytes,
                   cudaStream_t stream);
 
+/* Size of the static scratch array behind pkv_attention_noalloc (4 MiB). */
+#define PKV_NOALLOC_SCRATCH_BYTES (4 * 1024 * 1024)
+
+/*
+ * pkv_attention without a workspace and without any allocation.  The paper
+ * has no counterpart: this is a convenience of the library.
+ *
+ * For callers that cannot allocate device memory -- code running while a
+ * CUDA graph is captured in global mode, plugins whose host framework owns
+ * all device memory, serving loops that forbid allocation after start-up --
+ * and so cannot pass pkv_attention a workspace.  Same arguments, results and
+ * error codes as pkv_attention; the split-context scratch comes from a
+ * PKV_NOALLOC_SCRATCH_BYTES array compiled into the library, which every GPU
+ * that loads the library holds until the process exits.  Dims needing more
+ * scratch than that (pkv_attention_workspace_size) return PKV_ERR_WORKSPACE.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  Each call clears the merge counters at the head of the array
+ * (stream-ordered memset) and leaves other contents from earlier calls in
+ * place.  All calls share the one array: calls that overlap on the GPU (two
+ * streams, two host threads) race and must be serialised by the caller.
+ * Never calls cudaMalloc, cudaFree or any allocating routine.
+ */
+int pkv_attention_noalloc(const void *q, const void *k_pool, const void *v_pool,
+                          const int32_t *block_tables, const int32_t *seq_lens,
+                          const int32_t *query_start_loc, float scale, void *out,
+                          const pkv_dims *dims, cudaStream_t stream);
+
 /* Message of the last failing call on this thread ("" if none). */
 const char *pkv_last_error(void);
 

@@ -26,7 +26,8 @@ PKV_ERR_DEVICE_BOUNDS = -5
 PKV_ERR_TIMEOUT = -6
 
 EXPORTED = ("pkv_append", "pkv_attention", "pkv_attention_workspace_size",
-            "pkv_workspace_init", "pkv_last_error", "pkv_get_device_error")
+            "pkv_workspace_init", "pkv_last_error", "pkv_get_device_error",
+            "pkv_attention_noalloc")
 
 
 class PagedKVError(RuntimeError):
@@ -71,6 +72,8 @@ def load_library(path: str = LIB_PATH):
         lib.pkv_last_error.restype = ctypes.c_char_p
         lib.pkv_get_device_error.argtypes = [vp]
         lib.pkv_get_device_error.restype = ctypes.c_int
+        lib.pkv_attention_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, dp, vp]
+        lib.pkv_attention_noalloc.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -188,6 +191,31 @@ def pkv_attention(q, k_pool, v_pool, block_tables, seq_lens, query_start_loc, sc
         ctypes.c_void_p(seq_lens.data_ptr()), ctypes.c_void_p(query_start_loc.data_ptr()),
         ctypes.c_float(scale), ctypes.c_void_p(out.data_ptr()), ctypes.byref(dims),
         ctypes.c_void_p(ws_ptr), ws_bytes, ctypes.c_void_p(_stream(stream, q.device))))
+    return out
+
+
+def pkv_attention_noalloc(q, k_pool, v_pool, block_tables, seq_lens, query_start_loc, scale,
+                          out, stream=None):
+    """pkv_attention for callers that cannot allocate: the library's static
+    scratch array replaces the workspace and `out` must be given (nothing is
+    allocated here either).  Calls sharing the scratch must not overlap."""
+    for t, name, dt, nd in ((q, "q", torch.bfloat16, 3), (k_pool, "k_pool", torch.bfloat16, 4),
+                            (v_pool, "v_pool", torch.bfloat16, 4),
+                            (block_tables, "block_tables", torch.int32, 2),
+                            (seq_lens, "seq_lens", torch.int32, 1),
+                            (query_start_loc, "query_start_loc", torch.int32, 1),
+                            (out, "out", torch.bfloat16, 3)):
+        _need(t, name, dt, nd)
+    R = seq_lens.shape[0]
+    if query_start_loc.shape[0] != R + 1 or block_tables.shape[0] != R or out.shape != q.shape:
+        raise ValueError("inconsistent shapes")
+    dims = make_dims(tuple(q.shape), tuple(k_pool.shape), R, block_tables.shape[1])
+    _check(load_library().pkv_attention_noalloc(
+        ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k_pool.data_ptr()),
+        ctypes.c_void_p(v_pool.data_ptr()), ctypes.c_void_p(block_tables.data_ptr()),
+        ctypes.c_void_p(seq_lens.data_ptr()), ctypes.c_void_p(query_start_loc.data_ptr()),
+        ctypes.c_float(scale), ctypes.c_void_p(out.data_ptr()), ctypes.byref(dims),
+        ctypes.c_void_p(_stream(stream, q.device))))
     return out
 
 

@@ -174,6 +174,10 @@ int encode_q_map(CUtensorMap* m, const void* q, const pkv_dims* d, int group) {
 
 }  // namespace
 
+namespace pkv {
+void set_error_message(const char* msg) { snprintf(g_last_error, sizeof g_last_error, "%s", msg); }
+}  // namespace pkv
+
 extern "C" {
 
 const char* pkv_last_error(void) { return g_last_error; }

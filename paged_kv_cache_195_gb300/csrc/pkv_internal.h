@@ -98,6 +98,9 @@ struct PrefillLaunch {
 
 int prefill_tokens_per_tile(int group);
 
+// Sets the thread's pkv_last_error() message.
+void set_error_message(const char* msg);
+
 cudaError_t launch_prefill(const PrefillLaunch& L, int group, cudaStream_t stream);
 
 }  // namespace pkv
