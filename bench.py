@@ -170,6 +170,34 @@ class GraphEvents:
 # our arm
 # ---------------------------------------------------------------------------
 
+def workload_config(shape, ws_n):
+    """The `config` object of the JSON line (both arms)."""
+    return {
+        "workload": f"{shape.name} x{shape.layers} layers",
+        "num_reqs": shape.num_reqs, "context": int(shape.seq_lens[0]),
+        "q_tokens_per_req": int(shape.q_lens[0]), "layers": shape.layers,
+        "num_q_heads": shape.num_q_heads, "num_kv_heads": shape.num_kv_heads,
+        "head_dim": shape.head_dim, "block_size": shape.block_size,
+        "pool_blocks_per_layer": shape.num_blocks, "parallelism": f"replicas x{ws_n}",
+        "l2": f"inputs exceed L2: {shape.layers} distinct pools, "
+              f"{2 * shape.layers * shape.num_blocks * shape.num_kv_heads * 4096 / 1e9:.2f} GB per step",
+        "launch": f"CUDA graph of {shape.layers} x (append + attention)",
+    }
+
+
+def aggregate_over_ranks(ms_local: float, units_local: float, device=None):
+    """Max of the timed region and sum of the work over all ranks (identity
+    without an initialised process group)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return ms_local, units_local
+    t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+    u = torch.tensor([units_local], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
 def build_layers(shape, device, rank):
     layers = []
     for layer in range(shape.layers):
@@ -273,11 +301,7 @@ def run_ours(args):
         t1.record(stream)
         torch.cuda.synchronize(device)
         barrier()
-        ms = t0.elapsed_time(t1)
-        if ws_n > 1:
-            tt = torch.tensor([ms], device=device)
-            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-            ms = float(tt.item())
+        ms, _ = aggregate_over_ranks(t0.elapsed_time(t1), 0.0, device)
         return ms
 
     clocks = ClockSampler(nvsmi_id(local))
@@ -312,17 +336,7 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16 K/V/q, shuffled block placement; no weights)",
-        "config": {
-            "workload": f"{shape.name} x{shape.layers} layers",
-            "num_reqs": shape.num_reqs, "context": int(shape.seq_lens[0]),
-            "q_tokens_per_req": int(shape.q_lens[0]), "layers": shape.layers,
-            "num_q_heads": shape.num_q_heads, "num_kv_heads": shape.num_kv_heads,
-            "head_dim": shape.head_dim, "block_size": shape.block_size,
-            "pool_blocks_per_layer": shape.num_blocks, "parallelism": f"replicas x{ws_n}",
-            "l2": f"inputs exceed L2: {shape.layers} distinct pools, "
-                  f"{2 * shape.layers * shape.num_blocks * shape.num_kv_heads * 4096 / 1e9:.2f} GB per step",
-            "launch": "CUDA graph of 28 x (append + attention)",
-        },
+        "config": workload_config(shape, ws_n),
         "attended_tokens_per_s": round(tokens_per_step * ws_n / (ms_step * 1e-3), 1),
         "us_per_layer": round(ms_step * 1e3 / shape.layers, 3),
         "frac_of_nominal_8tbs": round(value / ws_n / NOMINAL_HBM_GBS, 4),
@@ -420,8 +434,7 @@ def run_reference(args):
         "n_gpus": ws_n, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt * 1e3 / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{shape.name} x{shape.layers} layers", "num_reqs": shape.num_reqs,
-                   "context": int(shape.seq_lens[0]), "layers": shape.layers},
+        "config": workload_config(shape, ws_n),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.max_threads(),
                          "kind": "oracle",
                          "sample": f"each step: attention of {n_reqs} of {shape.num_reqs} "

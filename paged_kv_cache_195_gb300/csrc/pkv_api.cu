@@ -356,4 +356,11 @@ int pkv_get_device_error(cudaStream_t stream) {
   return PKV_OK;
 }
 
+#if PKV_TRACE
+// Debug builds only: copies the decode kernel's per-CTA phase stamps.
+int pkv_debug_trace(void* host, size_t bytes) {
+  return pkv::decode_trace(host, bytes) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+#endif
+
 }  // extern "C"

@@ -59,12 +59,17 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
-// One potentially blocking probe: the warp sleeps until the phase completes
-// or about kSuspendHintNs pass, whichever is first.
+// One potentially blocking probe of an mbarrier phase.  With
+// PKV_WAIT_HINT the warp may sleep until the phase completes or about
+// kSuspendHintNs pass; without it the probe returns at once.
+#ifndef PKV_WAIT_HINT
+#define PKV_WAIT_HINT 0
+#endif
 constexpr uint32_t kSuspendHintNs = 100000;
 
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
+#if PKV_WAIT_HINT
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
@@ -72,6 +77,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "=r"(ok)
       : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
       : "memory");
+#else
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+#endif
   return ok != 0;
 }
 

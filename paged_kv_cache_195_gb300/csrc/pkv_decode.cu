@@ -37,18 +37,27 @@
 //    softmax in fp32 (exp2 with scale*log2(e) folded into q); PV accumulates
 //    in packed fp32 (fma.rn.f32x2).
 #include <climits>
+#include <cstdio>
+#include <cstdlib>
 
 #include "pkv_internal.h"
 
 namespace pkv {
 namespace {
 
-constexpr int kConsumerWarps = 4;
+#ifndef PKV_CWARPS
+#define PKV_CWARPS 4
+#endif
+constexpr int kConsumerWarps = PKV_CWARPS;
+static_assert(kConsumerWarps % 4 == 0, "consumer warps come in groups of four");
 constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;
-// Ring depth: two CTAs per SM for g <= 6 (10 stages each), one for g >= 7
+// Ring depth: two CTAs per SM for g <= 6 (8 stages each), one for g >= 7
 // (registers), which then takes a 20-stage ring.
+#ifndef PKV_RING
+#define PKV_RING 8
+#endif
 template <int G>
-constexpr int stages_for() { return G <= 6 ? 10 : 20; }
+constexpr int stages_for() { return G <= 6 ? PKV_RING : 20; }
 constexpr int kStageBytes = 2 * kTileBytes;  // K tile then V tile
 constexpr float kNegBig = -1.0e30f;          // "no key seen yet" running max
 constexpr int kEndRow = -2;                  // piece marker: the CTA's range is done
@@ -67,7 +76,7 @@ struct Piece {
 };
 
 #ifndef PKV_P_DUP
-#define PKV_P_DUP 1
+#define PKV_P_DUP 0
 #endif
 
 template <int G>
@@ -97,6 +106,19 @@ struct __align__(128) DecodeSmem {
   int wait_ok[kConsumerWarps];
   int end_flag[kConsumerWarps];
 };
+
+// Debug-only phase trace (build with -DPKV_TRACE=1): %globaltimer stamps of
+// each CTA's phases, read back with pkv_debug_trace().
+#ifndef PKV_TRACE
+#define PKV_TRACE 0
+#endif
+#if PKV_TRACE
+constexpr int kTraceCtas = 1024, kTraceEvents = 8;
+__device__ unsigned long long g_trace[kTraceCtas][kTraceEvents];
+#define TRACE(ev) do { if (blockIdx.x < kTraceCtas) g_trace[blockIdx.x][ev] = global_timer_ns(); } while (0)
+#else
+#define TRACE(ev) do { } while (0)
+#endif
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 __device__ __forceinline__ long long ceil_div_ll(long long a, long long b) { return (a + b - 1) / b; }
@@ -318,20 +340,23 @@ __device__ __forceinline__ long long rows_blocks(const ReqInfo& ri, int i) {
 // The kernel.
 // ---------------------------------------------------------------------------
 template <int G>
-__global__ void __launch_bounds__(kDecodeThreads, (G <= 6 ? 2 : 1))
+#ifndef PKV_MIN_CTAS
+#define PKV_MIN_CTAS(G) ((G) <= 6 && kConsumerWarps == 4 ? 2 : 1)
+#endif
+__global__ void __launch_bounds__(kDecodeThreads, PKV_MIN_CTAS(G))
     decode_kernel(const DecodeParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   DecodeSmem<G>& sm = *reinterpret_cast<DecodeSmem<G>*>(smem_raw);
   volatile int* abort_flag = &sm.abort_flag;
-  constexpr int kRing = DecodeSmem<G>::kStages;
-  const int kStages = (p.stages >= 2 && p.stages <= kRing) ? p.stages : kRing;
+  constexpr int kStages = DecodeSmem<G>::kStages;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int R = p.num_reqs, Hkv = p.num_kv_heads;
 
+  if (tid == 0) TRACE(0);
   if (tid == 0) {
     #pragma unroll
-    for (int s = 0; s < kRing; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], 1);
     }
@@ -347,12 +372,13 @@ __global__ void __launch_bounds__(kDecodeThreads, (G <= 6 ? 2 : 1))
   // that kernel's output, so all reads come after this point.
   grid_dependency_wait();
   allow_dependent_launch();
+  if (tid == 0) TRACE(1);
 
   if (warp == kConsumerWarps) {
     // ======================= producer warp =================================
     // Warm L2 with the part of the block table this CTA will probably read
     // (its share of the step if every row were full), while the plan loads.
-    {
+    if (p.prefetch) {
       const long long entries = (long long)R * p.max_blocks;
       const long long est = entries * blockIdx.x / gridDim.x;
       const long long line0 = (est * 4) / 128 - 2;
@@ -391,6 +417,7 @@ __global__ void __launch_bounds__(kDecodeThreads, (G <= 6 ? 2 : 1))
     }
     const long long lo = (long long)blockIdx.x * chunk;
     const long long hi = min(W, lo + chunk);
+    if (lane == 0) TRACE(2);
 
     const uint64_t pol = l2_policy_evict_first();
     uint32_t n = 0;  // CTA-wide block sequence number
@@ -565,10 +592,12 @@ __global__ void __launch_bounds__(kDecodeThreads, (G <= 6 ? 2 : 1))
     #pragma unroll
     for (int jj = 0; jj < F; ++jj) lsum[jj] = 0.f;
 
-    for (int bi = (int)((cw - n_base) & (kConsumerWarps - 1)); bi < pc.nblk; bi += kConsumerWarps) {
+    for (int bi = (int)((cw + kConsumerWarps - n_base % kConsumerWarps) % kConsumerWarps);
+         bi < pc.nblk; bi += kConsumerWarps) {
       const uint32_t n = n_base + bi;
       const int st = n % kStages;
       const bool arrived = mbar_wait(&sm.full[st], (n / kStages) & 1, p.err, abort_flag);
+      if (n == 0 && lane == 0) TRACE(4);
       const int first = (pc.b0 + bi) * kBlockSize;
       const int nvalid = (arrived && sm.stage_valid[st]) ? min(kBlockSize, pc.limit - first) : 0;
       BM::run(sm.ring[st], nvalid, lane, qf, m, lsum, acc, sm.pbuf[cw]);
@@ -576,6 +605,7 @@ __global__ void __launch_bounds__(kDecodeThreads, (G <= 6 ? 2 : 1))
       if (lane == 0) mbar_arrive(&sm.empty[st]);
     }
     n_base += pc.nblk;
+    if (ct == 0 && !is_end) TRACE(5);
 
     // ---- combine the four warps' states -----------------------------------
     float lall[G];
@@ -636,11 +666,13 @@ __global__ void __launch_bounds__(kDecodeThreads, (G <= 6 ? 2 : 1))
       end = end || sm.end_flag[w];
     }
     ok = ok && !end;
-    const int d = ct;
+    // Epilogue: thread ct owns output dim d = ct % 128 of heads h0, h0 + hstep, ...
+    constexpr int kHStep = kConsumerThreads / kHeadDim;
+    const int d = ct % kHeadDim;
+    const int h0 = ct / kHeadDim;
     const long long out_row = ((long long)pc.row * p.num_q_heads + (long long)pc.k * G) * kHeadDim;
-    float res[G];
-    #pragma unroll
-    for (int h = 0; h < G; ++h) {
+    #pragma unroll 1
+    for (int h = h0; h < G; h += kHStep) {
       float M = sm.comb_m[0][h];
       #pragma unroll
       for (int w = 1; w < kConsumerWarps; ++w) M = fmaxf(M, sm.comb_m[w][h]);
@@ -651,16 +683,14 @@ __global__ void __launch_bounds__(kDecodeThreads, (G <= 6 ? 2 : 1))
         num += e * sm.comb[w][h][d];
         den += e * sm.comb_l[w][h];
       }
-      res[h] = den > 0.f ? num / den : 0.f;
+      const float res = den > 0.f ? num / den : 0.f;
       if (ok && pc.S > 1) {
         const long long slot = (long long)pc.slot * G + h;
-        p.ws_o[slot * kHeadDim + d] = res[h];
+        p.ws_o[slot * kHeadDim + d] = res;
         if (d == 0) *reinterpret_cast<float2*>(p.ws_ml + slot * 2) = make_float2(M, den);
+      } else if (ok) {
+        p.out[out_row + h * kHeadDim + d] = __float2bfloat16_rn(res);
       }
-    }
-    if (ok && pc.S == 1) {
-      #pragma unroll
-      for (int h = 0; h < G; ++h) p.out[out_row + h * kHeadDim + d] = __float2bfloat16_rn(res[h]);
     }
     if (ok && pc.S > 1) {
       __threadfence();
@@ -678,37 +708,42 @@ __global__ void __launch_bounds__(kDecodeThreads, (G <= 6 ? 2 : 1))
         // pass with a running maximum; loads of four pieces are in flight at
         // once.
         __threadfence();
-        float M[G], num[G], den[G];
-        #pragma unroll
-        for (int h = 0; h < G; ++h) { M[h] = kNegBig; num[h] = 0.f; den[h] = 0.f; }
-        #pragma unroll 4
-        for (int s = 0; s < pc.S; ++s) {
-          const int slot = 2 * (pc.c0 + s) + ((s == 0 && pc.odd0) ? 1 : 0);
-          #pragma unroll
-          for (int h = 0; h < G; ++h) {
+        #pragma unroll 1
+        for (int h = h0; h < G; h += kHStep) {
+          float M = kNegBig, num = 0.f, den = 0.f;
+          #pragma unroll 4
+          for (int s = 0; s < pc.S; ++s) {
+            const int slot = 2 * (pc.c0 + s) + ((s == 0 && pc.odd0) ? 1 : 0);
             const long long sl = (long long)slot * G + h;
             const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.ws_ml + sl * 2));
             const float o = __ldcg(p.ws_o + sl * kHeadDim + d);
-            const float Mn = fmaxf(M[h], ml.x);
-            const float a = fast_exp2(M[h] - Mn), w = fast_exp2(ml.x - Mn) * ml.y;
-            num[h] = num[h] * a + w * o;
-            den[h] = den[h] * a + w;
-            M[h] = Mn;
+            const float Mn = fmaxf(M, ml.x);
+            const float a = fast_exp2(M - Mn), w = fast_exp2(ml.x - Mn) * ml.y;
+            num = num * a + w * o;
+            den = den * a + w;
+            M = Mn;
           }
+          p.out[out_row + h * kHeadDim + d] = __float2bfloat16_rn(num / den);
         }
-        #pragma unroll
-        for (int h = 0; h < G; ++h)
-          p.out[out_row + h * kHeadDim + d] = __float2bfloat16_rn(num[h] / den[h]);
       }
     }
     // Close the piece: nobody rewrites comb/is_last before everyone is done.
     named_barrier(1, kConsumerThreads);
+    if (ct == 0 && !end) TRACE(6);
     if (end) break;
   }
+  if (ct == 0) TRACE(7);
 }
 
 template <int G>
 cudaError_t launch_decode_g(const DecodeParams& p, int grid, cudaStream_t stream) {
+  if (getenv("PKV_DEBUG")) {
+    int occ = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_kernel<G>, kDecodeThreads,
+                                                  sizeof(DecodeSmem<G>));
+    fprintf(stderr, "decode_kernel<%d>: smem %zu B, %d CTAs/SM resident, grid %d\n", G,
+            sizeof(DecodeSmem<G>), occ, grid);
+  }
   const size_t smem = sizeof(DecodeSmem<G>);
   static unsigned long long configured = 0;  // bit per device ordinal
   int dev = 0;
@@ -718,6 +753,9 @@ cudaError_t launch_decode_g(const DecodeParams& p, int grid, cudaStream_t stream
   if (!(__atomic_load_n(&configured, __ATOMIC_ACQUIRE) & bit)) {
     e = cudaFuncSetAttribute(decode_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
+    if (e != cudaSuccess) return e;
+    // Two CTAs per SM need the largest shared-memory carveout.
+    e = cudaFuncSetAttribute(decode_kernel<G>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
     __atomic_fetch_or(&configured, bit, __ATOMIC_RELEASE);
   }
@@ -738,7 +776,13 @@ cudaError_t launch_decode_g(const DecodeParams& p, int grid, cudaStream_t stream
 
 }  // namespace
 
-int decode_ctas_per_sm(int group) { return group <= 6 ? 2 : 1; }
+#if PKV_TRACE
+cudaError_t decode_trace(void* host, size_t bytes) {
+  return cudaMemcpyFromSymbol(host, g_trace, bytes < sizeof(g_trace) ? bytes : sizeof(g_trace));
+}
+#endif
+
+int decode_ctas_per_sm(int group) { return group <= 6 && kConsumerWarps == 4 ? 2 : 1; }
 
 int decode_grid(int sm_count, int group) { return sm_count * decode_ctas_per_sm(group); }
 

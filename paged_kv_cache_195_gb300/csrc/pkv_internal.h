@@ -52,7 +52,7 @@ struct DecodeParams {
   int num_slots;      // partial-piece slots in the workspace (>= 2 * grid)
   int min_chunk;      // smallest per-CTA range, in blocks
   int align;          // snap ranges to row-group boundaries when lengths are uniform
-  int stages;         // ring stages in use (<= the compiled ring; 0 = all)
+  int prefetch;       // warm L2 with the block-table rows this CTA will likely read
   int pdl;            // launch with programmatic stream serialization
 };
 
@@ -97,6 +97,13 @@ struct PrefillLaunch {
 };
 
 int prefill_tokens_per_tile(int group);
+
+#ifndef PKV_TRACE
+#define PKV_TRACE 0
+#endif
+#if PKV_TRACE
+cudaError_t decode_trace(void* host, size_t bytes);
+#endif
 
 // Sets the thread's pkv_last_error() message.
 void set_error_message(const char* msg);

@@ -103,6 +103,34 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hkv = p.num_kv_heads;
 
+  // Ordering.  The decode kernel launched just before this one in the same
+  // call lets it start early; everything read here (lengths, tables, q, the
+  // pools) was complete before the decode kernel signalled, and the decode
+  // kernel writes only decode rows of `out`, which this kernel never touches.
+  // So the work below needs no wait; the wait at the end makes this grid
+  // finish after the decode grid, so that successors of the call see both.
+  //
+  // Before any set-up: does this CTA have an item at all?  Pure-decode steps
+  // (no request with q_r >= prefill_min_q) leave every CTA idle.
+  if (warp == 0) {
+    long long total = 0;
+    for (int b = 0; b < p.num_reqs; b += 32) {
+      const int rr = b + lane;
+      long long cnt = 0;
+      if (rr < p.num_reqs) cnt = (long long)load_pf_request(p, rr, TQ).ntiles * Hkv;
+      #pragma unroll
+      for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+      total += cnt;
+    }
+    if (lane == 0) sm.abort_flag = (long long)blockIdx.x >= total;  // reused as "idle"
+  }
+  __syncthreads();
+  if (sm.abort_flag) {
+    grid_dependency_wait();
+    return;
+  }
+  __syncthreads();
+
   if (tid == 0) {
     mbar_init(&sm.q_full, 1);
     mbar_init(&sm.q_empty, 1);
@@ -143,7 +171,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
-  grid_dependency_wait();
   allow_dependent_launch();
 
   if (warp == 4) {
@@ -410,6 +437,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 5) tmem_dealloc(tmem, kTmemCols);
+  grid_dependency_wait();
 }
 
 template <int G>
