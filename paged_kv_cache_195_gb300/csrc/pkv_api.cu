@@ -299,7 +299,11 @@ int pkv_attention(const void* q, const void* k_pool, const void* v_pool,
   // prefill kernel (when the step has that many query tokens at all).
   int prefill_min_q = env_int("PKV_PREFILL_MIN_Q", 16);
   if (prefill_min_q < 1) prefill_min_q = 0x7fffffff;
-  const bool run_prefill = dims->num_q_tokens >= prefill_min_q;
+  // Launch it only when the step can hold such a request next to one query
+  // for every other request; otherwise the decode kernel serves every row
+  // (it is correct for any q_r, the prefill kernel is only faster).
+  const bool run_prefill =
+      (long long)dims->num_q_tokens - dims->num_reqs + 1 >= (long long)prefill_min_q;
   p.prefill_min_q = run_prefill ? prefill_min_q : 0x7fffffff;
   p.num_slots = w.num_slots;
   p.pdl = env_int("PKV_PDL", 1) != 0;

@@ -45,19 +45,38 @@
 namespace pkv {
 namespace {
 
-#ifndef PKV_CWARPS
-#define PKV_CWARPS 4
+// Warp layout.  Blocks are consumed by four warp groups in turn; with an
+// even group size g the g query heads are split across the two warps of a
+// group (each warp owns g/2 heads: half the registers, twice the warps per
+// SM to hide latency), otherwise one warp holds all g heads.
+#ifndef PKV_HSPLIT
+#define PKV_HSPLIT 0
 #endif
-constexpr int kConsumerWarps = PKV_CWARPS;
-static_assert(kConsumerWarps % 4 == 0, "consumer warps come in groups of four");
-constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;
-// Ring depth: two CTAs per SM for g <= 6 (8 stages each), one for g >= 7
-// (registers), which then takes a 20-stage ring.
+#ifndef PKV_GROUPS_SPLIT
+#define PKV_GROUPS_SPLIT 3
+#endif
+template <int G>
+struct DecodeCfg {
+  static constexpr int kHS = (PKV_HSPLIT && G % 2 == 0) ? 2 : 1;  // warps per group
+  static constexpr int kGH = G / kHS;                             // heads per warp
+  static constexpr int kGroups = kHS == 2 ? PKV_GROUPS_SPLIT : 4;  // blocks in flight per round
+  static constexpr int kCW = kGroups * kHS;                       // consumer warps
+  static constexpr int kThreads = (kCW + 1) * 32;                 // + producer warp
+  static constexpr int kMinCtas = (kGH <= 6) ? 2 : 1;
+  // Registers per thread that still let kMinCtas CTAs share an SM (the
+  // register file is handed out as if a CTA's warp count were even).
+  static constexpr int kWarpsAlloc = (kCW + 2) / 2 * 2;
+  static constexpr int kMaxRegs =
+      kMinCtas == 1 ? 255 : (65536 / (kMinCtas * kWarpsAlloc * 32)) / 8 * 8;
+};
+
+// Ring depth: 8 stages per CTA when two CTAs share an SM (shared memory),
+// 20 when one CTA has the SM to itself.
 #ifndef PKV_RING
 #define PKV_RING 8
 #endif
 template <int G>
-constexpr int stages_for() { return G <= 6 ? PKV_RING : 20; }
+constexpr int stages_for() { return DecodeCfg<G>::kMinCtas == 2 ? PKV_RING : 20; }
 constexpr int kStageBytes = 2 * kTileBytes;  // K tile then V tile
 constexpr float kNegBig = -1.0e30f;          // "no key seen yet" running max
 constexpr int kEndRow = -2;                  // piece marker: the CTA's range is done
@@ -81,20 +100,21 @@ struct Piece {
 
 template <int G>
 struct __align__(128) DecodeSmem {
+  using Cfg = DecodeCfg<G>;
   static constexpr int kStages = stages_for<G>();
   // Probabilities of one block, stored twice ({p, p}) so that the PV loop
   // feeds packed fp32 FMAs straight from 16-byte loads.
 #if PKV_P_DUP
-  static constexpr int kPStride = (G + 1) & ~1;  // float2 entries per token
+  static constexpr int kPStride = (Cfg::kGH + 1) & ~1;  // float2 entries per token
 #else
-  static constexpr int kPStride = ((G + 3) & ~3) / 2;  // float2 slots = 2 floats each
+  static constexpr int kPStride = ((Cfg::kGH + 3) & ~3) / 2;  // float2 slots = 2 floats each
 #endif
   uint8_t ring[kStages][kStageBytes];
   __nv_bfloat16 qbuf[2][G * kHeadDim];
-  float2 pbuf[kConsumerWarps][kBlockSize][kPStride];
-  float comb[kConsumerWarps][G][kHeadDim];
-  float comb_m[kConsumerWarps][G];
-  float comb_l[kConsumerWarps][G];
+  float2 pbuf[Cfg::kCW][kBlockSize][kPStride];
+  float comb[Cfg::kGroups][G][kHeadDim];
+  float comb_m[Cfg::kGroups][G];
+  float comb_l[Cfg::kGroups][G];
   Piece pinfo[2];
   int stage_valid[kStages];
   uint64_t full[kStages];
@@ -103,8 +123,8 @@ struct __align__(128) DecodeSmem {
   uint64_t qempty[2];
   int abort_flag;
   int is_last;
-  int wait_ok[kConsumerWarps];
-  int end_flag[kConsumerWarps];
+  int wait_ok[Cfg::kCW];
+  int end_flag[Cfg::kCW];
 };
 
 // Debug-only phase trace (build with -DPKV_TRACE=1): %globaltimer stamps of
@@ -113,11 +133,15 @@ struct __align__(128) DecodeSmem {
 #define PKV_TRACE 0
 #endif
 #if PKV_TRACE
-constexpr int kTraceCtas = 1024, kTraceEvents = 8;
+constexpr int kTraceCtas = 1024, kTraceEvents = 12;
 __device__ unsigned long long g_trace[kTraceCtas][kTraceEvents];
 #define TRACE(ev) do { if (blockIdx.x < kTraceCtas) g_trace[blockIdx.x][ev] = global_timer_ns(); } while (0)
+#define TRACE_ADD(ev, v) do { if (blockIdx.x < kTraceCtas) g_trace[blockIdx.x][ev] += (v); } while (0)
+#define TRACE_NOW() global_timer_ns()
 #else
 #define TRACE(ev) do { } while (0)
+#define TRACE_ADD(ev, v) do { } while (0)
+#define TRACE_NOW() 0ull
 #endif
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
@@ -126,11 +150,10 @@ __device__ __forceinline__ long long ceil_div_ll(long long a, long long b) { ret
 // ---------------------------------------------------------------------------
 // Consumer: one 16-token block for one warp.
 // ---------------------------------------------------------------------------
-template <int G>
-struct BlockMath {
+template <int G, int kPStride>
+struct BlockMath {  // G = query heads this warp holds
   static constexpr bool kEven = (G % 2) == 0;
   static constexpr int F = kEven ? G / 2 : G;  // scores a lane owns after the scatter
-  static constexpr int kPStride = DecodeSmem<G>::kPStride;
 
   // Logical head held in register slot hs of a lane (see the reduce-scatter).
   __device__ static __forceinline__ int head_of_slot(int hs, int b0) {
@@ -340,10 +363,7 @@ __device__ __forceinline__ long long rows_blocks(const ReqInfo& ri, int i) {
 // The kernel.
 // ---------------------------------------------------------------------------
 template <int G>
-#ifndef PKV_MIN_CTAS
-#define PKV_MIN_CTAS(G) ((G) <= 6 && kConsumerWarps == 4 ? 2 : 1)
-#endif
-__global__ void __launch_bounds__(kDecodeThreads, PKV_MIN_CTAS(G))
+__global__ void __launch_bounds__(DecodeCfg<G>::kThreads) __maxnreg__(DecodeCfg<G>::kMaxRegs)
     decode_kernel(const DecodeParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   DecodeSmem<G>& sm = *reinterpret_cast<DecodeSmem<G>*>(smem_raw);
@@ -358,11 +378,11 @@ __global__ void __launch_bounds__(kDecodeThreads, PKV_MIN_CTAS(G))
     #pragma unroll
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.full[s], 1);
-      mbar_init(&sm.empty[s], 1);
+      mbar_init(&sm.empty[s], DecodeCfg<G>::kHS);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.qfull[b], 1);
-      mbar_init(&sm.qempty[b], kConsumerWarps);
+      mbar_init(&sm.qempty[b], DecodeCfg<G>::kCW);
     }
     sm.abort_flag = 0;
     fence_barrier_init();
@@ -374,7 +394,7 @@ __global__ void __launch_bounds__(kDecodeThreads, PKV_MIN_CTAS(G))
   allow_dependent_launch();
   if (tid == 0) TRACE(1);
 
-  if (warp == kConsumerWarps) {
+  if (warp == DecodeCfg<G>::kCW) {
     // ======================= producer warp =================================
     // Warm L2 with the part of the block table this CTA will probably read
     // (its share of the step if every row were full), while the plan loads.
@@ -498,9 +518,11 @@ __global__ void __launch_bounds__(kDecodeThreads, PKV_MIN_CTAS(G))
           for (int xb = 0; xb < cnt; ++xb, ++n) {
             int phys = __shfl_sync(0xffffffffu, ent, xb);
             const int st = n % kStages;
+            [[maybe_unused]] const unsigned long long tw0 = TRACE_NOW();
             if (n >= kStages &&
                 !mbar_wait(&sm.empty[st], ((n / kStages) - 1) & 1, p.err, abort_flag))
               break;
+            if (lane == 0) TRACE_ADD(8, TRACE_NOW() - tw0);
             if (lane == 0) {
               const bool valid = (unsigned)phys < (unsigned)p.num_blocks;
               if (!valid) {
@@ -547,10 +569,15 @@ __global__ void __launch_bounds__(kDecodeThreads, PKV_MIN_CTAS(G))
   }
 
   // ========================= consumer warps ================================
-  using BM = BlockMath<G>;
+  using Cfg = DecodeCfg<G>;
+  constexpr int GH = Cfg::kGH;  // heads of this warp: ho .. ho + GH - 1
+  using BM = BlockMath<GH, DecodeSmem<G>::kPStride>;
   constexpr int F = BM::F;
-  constexpr int kConsumerThreads = kConsumerWarps * 32;
+  constexpr int kConsumerThreads = Cfg::kCW * 32;
   const int cw = warp;
+  constexpr int kGroups = Cfg::kGroups;
+  const int grp = cw / Cfg::kHS;       // the warp group that takes a block
+  const int ho = (cw % Cfg::kHS) * GH;  // first head of this warp
   const int ct = tid;  // 0..127: the output dim this thread writes in the epilogue
   const int c = lane & 15;
   const int b0bit = lane & 1;
@@ -567,10 +594,10 @@ __global__ void __launch_bounds__(kDecodeThreads, PKV_MIN_CTAS(G))
                           2 * (pc.c0 + pc.S) <= p.num_slots && pc.slot >= 0 &&
                           pc.slot < p.num_slots;
     if (!in_range) pc.nblk = 0;
-    float2 qf[G][4];
+    float2 qf[GH][4];
     #pragma unroll
-    for (int hs = 0; hs < G; ++hs) {
-      const int hl = BM::head_of_slot(hs, b0bit);
+    for (int hs = 0; hs < GH; ++hs) {
+      const int hl = ho + BM::head_of_slot(hs, b0bit);
       const uint4 w = lds128(&sm.qbuf[ub][hl * kHeadDim + c * 8]);
       const float2 s2 = make_float2(p.scale_log2, p.scale_log2);
       qf[hs][0] = fmul2(bf16x2_to_float2(w.x), s2);
@@ -581,10 +608,10 @@ __global__ void __launch_bounds__(kDecodeThreads, PKV_MIN_CTAS(G))
     __syncwarp();
     if (lane == 0 && !is_end) mbar_arrive(&sm.qempty[ub]);
 
-    float m[G], lsum[F];
-    float2 acc[G][4];
+    float m[GH], lsum[F];
+    float2 acc[GH][4];
     #pragma unroll
-    for (int h = 0; h < G; ++h) {
+    for (int h = 0; h < GH; ++h) {
       m[h] = kNegBig;
       #pragma unroll
       for (int i = 0; i < 4; ++i) acc[h][i] = make_float2(0.f, 0.f);
@@ -592,23 +619,39 @@ __global__ void __launch_bounds__(kDecodeThreads, PKV_MIN_CTAS(G))
     #pragma unroll
     for (int jj = 0; jj < F; ++jj) lsum[jj] = 0.f;
 
-    for (int bi = (int)((cw + kConsumerWarps - n_base % kConsumerWarps) % kConsumerWarps);
-         bi < pc.nblk; bi += kConsumerWarps) {
+    for (int bi = (int)((grp + kGroups - n_base % kGroups) % kGroups); bi < pc.nblk;
+         bi += kGroups) {
       const uint32_t n = n_base + bi;
       const int st = n % kStages;
+      [[maybe_unused]] const unsigned long long tw0 = TRACE_NOW();
       const bool arrived = mbar_wait(&sm.full[st], (n / kStages) & 1, p.err, abort_flag);
+      [[maybe_unused]] const unsigned long long tw1 = TRACE_NOW();
       if (n == 0 && lane == 0) TRACE(4);
+      if (cw == 0 && lane == 0) TRACE_ADD(9, tw1 - tw0);
       const int first = (pc.b0 + bi) * kBlockSize;
       const int nvalid = (arrived && sm.stage_valid[st]) ? min(kBlockSize, pc.limit - first) : 0;
       BM::run(sm.ring[st], nvalid, lane, qf, m, lsum, acc, sm.pbuf[cw]);
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.empty[st]);
+      if (cw == 0 && lane == 0) {
+        TRACE_ADD(10, TRACE_NOW() - tw1);
+        TRACE_ADD(11, 1);
+      }
     }
     n_base += pc.nblk;
     if (ct == 0 && !is_end) TRACE(5);
 
-    // ---- combine the four warps' states -----------------------------------
-    float lall[G];
+    // ---- combine the four warp groups' states -----------------------------
+    if (is_end) {
+      // The end marker carries no work: only agree on it, then leave.
+      if (lane == 0) {
+        sm.wait_ok[cw] = 0;
+        sm.end_flag[cw] = 1;
+      }
+      named_barrier(1, kConsumerThreads);
+      break;
+    }
+    float lall[GH];
     {
       float l2[F];
       #pragma unroll
@@ -627,11 +670,11 @@ __global__ void __launch_bounds__(kDecodeThreads, PKV_MIN_CTAS(G))
         }
       } else {
         #pragma unroll
-        for (int jj = 0; jj < G; ++jj) lall[jj] = l2[jj];
+        for (int jj = 0; jj < GH; ++jj) lall[jj] = l2[jj];
       }
     }
     #pragma unroll
-    for (int h = 0; h < G; ++h)
+    for (int h = 0; h < GH; ++h)
       #pragma unroll
       for (int i = 0; i < 4; ++i) {
         acc[h][i].x += __shfl_xor_sync(0xffffffffu, acc[h][i].x, 16);
@@ -639,17 +682,17 @@ __global__ void __launch_bounds__(kDecodeThreads, PKV_MIN_CTAS(G))
       }
     if (lane < 16) {
       #pragma unroll
-      for (int h = 0; h < G; ++h) {
-        float4* dst = reinterpret_cast<float4*>(&sm.comb[cw][h][c * 8]);
+      for (int h = 0; h < GH; ++h) {
+        float4* dst = reinterpret_cast<float4*>(&sm.comb[grp][ho + h][c * 8]);
         dst[0] = make_float4(acc[h][0].x, acc[h][0].y, acc[h][1].x, acc[h][1].y);
         dst[1] = make_float4(acc[h][2].x, acc[h][2].y, acc[h][3].x, acc[h][3].y);
       }
     }
     if (lane == 0) {
       #pragma unroll
-      for (int h = 0; h < G; ++h) {
-        sm.comb_m[cw][h] = m[h];
-        sm.comb_l[cw][h] = lall[h];
+      for (int h = 0; h < GH; ++h) {
+        sm.comb_m[grp][ho + h] = m[h];
+        sm.comb_l[grp][ho + h] = lall[h];
       }
       sm.wait_ok[cw] = in_range;
       sm.end_flag[cw] = is_end;
@@ -661,24 +704,22 @@ __global__ void __launch_bounds__(kDecodeThreads, PKV_MIN_CTAS(G))
     // `end` are uniform across the consumer warps and so are the barriers.
     bool ok = true, end = false;
     #pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) {
+    for (int w = 0; w < Cfg::kCW; ++w) {
       ok = ok && sm.wait_ok[w];
       end = end || sm.end_flag[w];
     }
-    ok = ok && !end;
-    // Epilogue: thread ct owns output dim d = ct % 128 of heads h0, h0 + hstep, ...
-    constexpr int kHStep = kConsumerThreads / kHeadDim;
-    const int d = ct % kHeadDim;
-    const int h0 = ct / kHeadDim;
+    if (end) break;  // another warp saw the end marker (only after an abort)
+    // Epilogue: the consumer threads stride over the g x 128 outputs.
     const long long out_row = ((long long)pc.row * p.num_q_heads + (long long)pc.k * G) * kHeadDim;
     #pragma unroll 1
-    for (int h = h0; h < G; h += kHStep) {
+    for (int idx = ct; idx < G * kHeadDim; idx += kConsumerThreads) {
+      const int h = idx / kHeadDim, d = idx % kHeadDim;
       float M = sm.comb_m[0][h];
       #pragma unroll
-      for (int w = 1; w < kConsumerWarps; ++w) M = fmaxf(M, sm.comb_m[w][h]);
+      for (int w = 1; w < kGroups; ++w) M = fmaxf(M, sm.comb_m[w][h]);
       float num = 0.f, den = 0.f;
       #pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) {
+      for (int w = 0; w < kGroups; ++w) {
         const float e = fast_exp2(sm.comb_m[w][h] - M);
         num += e * sm.comb[w][h][d];
         den += e * sm.comb_l[w][h];
@@ -693,13 +734,19 @@ __global__ void __launch_bounds__(kDecodeThreads, PKV_MIN_CTAS(G))
       }
     }
     if (ok && pc.S > 1) {
-      __threadfence();
+      // Ticket: the barrier orders every thread's partial stores before
+      // thread 0's fence, whose release is cumulative, then the atomic.  The
+      // piece that draws the last ticket fences again (acquire) and merges.
       named_barrier(1, kConsumerThreads);
       if (ct == 0) {
+        __threadfence();
         int* cnt = p.ws_cnt + (long long)pc.row * Hkv + pc.k;
         const int old = atomicAdd(cnt, 1);
         const int last = (old == pc.S - 1);
-        if (last) *cnt = 0;  // every piece has arrived: leave the counter at zero
+        if (last) {
+          *cnt = 0;  // every piece has arrived: leave the counter at zero
+          __threadfence();
+        }
         sm.is_last = last;
       }
       named_barrier(1, kConsumerThreads);
@@ -707,9 +754,9 @@ __global__ void __launch_bounds__(kDecodeThreads, PKV_MIN_CTAS(G))
         // Log-sum-exp merge of the row-group's pieces, in piece order, one
         // pass with a running maximum; loads of four pieces are in flight at
         // once.
-        __threadfence();
         #pragma unroll 1
-        for (int h = h0; h < G; h += kHStep) {
+        for (int idx = ct; idx < G * kHeadDim; idx += kConsumerThreads) {
+          const int h = idx / kHeadDim, d = idx % kHeadDim;
           float M = kNegBig, num = 0.f, den = 0.f;
           #pragma unroll 4
           for (int s = 0; s < pc.S; ++s) {
@@ -739,7 +786,7 @@ template <int G>
 cudaError_t launch_decode_g(const DecodeParams& p, int grid, cudaStream_t stream) {
   if (getenv("PKV_DEBUG")) {
     int occ = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_kernel<G>, kDecodeThreads,
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_kernel<G>, DecodeCfg<G>::kThreads,
                                                   sizeof(DecodeSmem<G>));
     fprintf(stderr, "decode_kernel<%d>: smem %zu B, %d CTAs/SM resident, grid %d\n", G,
             sizeof(DecodeSmem<G>), occ, grid);
@@ -761,7 +808,7 @@ cudaError_t launch_decode_g(const DecodeParams& p, int grid, cudaStream_t stream
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kDecodeThreads);
+  cfg.blockDim = dim3(DecodeCfg<G>::kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -782,7 +829,18 @@ cudaError_t decode_trace(void* host, size_t bytes) {
 }
 #endif
 
-int decode_ctas_per_sm(int group) { return group <= 6 && kConsumerWarps == 4 ? 2 : 1; }
+int decode_ctas_per_sm(int group) {
+  switch (group) {
+    case 1: return DecodeCfg<1>::kMinCtas;
+    case 2: return DecodeCfg<2>::kMinCtas;
+    case 3: return DecodeCfg<3>::kMinCtas;
+    case 4: return DecodeCfg<4>::kMinCtas;
+    case 5: return DecodeCfg<5>::kMinCtas;
+    case 6: return DecodeCfg<6>::kMinCtas;
+    case 7: return DecodeCfg<7>::kMinCtas;
+    default: return DecodeCfg<8>::kMinCtas;
+  }
+}
 
 int decode_grid(int sm_count, int group) { return sm_count * decode_ctas_per_sm(group); }
 

@@ -126,6 +126,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   }
   __syncthreads();
   if (sm.abort_flag) {
+    allow_dependent_launch();
     grid_dependency_wait();
     return;
   }
