@@ -92,6 +92,25 @@ int pkv_append(const void *k_new, const void *v_new, const int64_t *slot_mapping
                const pkv_dims *dims, cudaStream_t stream);
 
 /*
+ * Whole-block copies between two pools of the same layout: for each pair i,
+ * block pairs[2i] of (k_src, v_src) -- every KV head, K and V -- is copied to
+ * block pairs[2i+1] of (k_dst, v_dst).  Source and destination may be the same
+ * pool (copy-on-write of a shared block) or different pools; either side may
+ * be pinned host memory that the device can address (swap out / swap in).
+ * pairs: [num_pairs, 2] int64 in device-accessible memory.  Pairs naming a
+ * block outside [0, src_num_blocks) / [0, dst_num_blocks) are skipped and
+ * reported as PKV_ERR_DEVICE_BOUNDS; pairs must not overlap (no block is both
+ * a source and a destination).  Only dims->num_kv_heads, head_dim and
+ * block_size are read.
+ * Source: LLM 7 - Efficient LLM Serving, sec. 3 "Sharing and Preemption"
+ * (copy-on-write, swapping blocks to CPU memory); The Serving Playbook,
+ * "Sharing is a reference count", "Preemption, where the folklore is wrong".
+ */
+int pkv_copy_blocks(const void *k_src, const void *v_src, void *k_dst, void *v_dst,
+                    const int64_t *pairs, int32_t num_pairs, int32_t src_num_blocks,
+                    int32_t dst_num_blocks, const pkv_dims *dims, cudaStream_t stream);
+
+/*
  * Bytes of workspace pkv_attention needs for these dims (split-context
  * partial outputs, their log-sum-exp statistics and per-row merge counters).
  * Depends only on dims and the device's SM count, not on the lengths, so one

@@ -54,6 +54,8 @@ def _load():
                 p, p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32,
                 ctypes.c_double, p]
             lib.oracle_paged_attention.restype = ctypes.c_int
+            lib.oracle_copy_blocks.argtypes = [p, p, p, p, p, i64, i64, i64, i64, i64, i64]
+            lib.oracle_copy_blocks.restype = ctypes.c_int
             lib.oracle_set_threads.argtypes = [ctypes.c_int]
             lib.oracle_set_threads.restype = None
             lib.oracle_max_threads.argtypes = []
@@ -117,6 +119,21 @@ def paged_attention(q, k_pool, v_pool, block_tables, seq_lens,
     if rc != 0:
         raise ValueError(f"oracle_paged_attention: inconsistent inputs (rc={rc})")
     return out
+
+
+def copy_blocks(k_src, v_src, k_dst, v_dst, pairs):
+    """Copies of the destination pools after moving whole blocks: block
+    pairs[i, 0] of the source pools to block pairs[i, 1] of the destination."""
+    ks, vs = _c(k_src, np.uint16), _c(v_src, np.uint16)
+    kd, vd = _c(k_dst, np.uint16).copy(), _c(v_dst, np.uint16).copy()
+    pr = _c(pairs, np.int64).reshape(-1, 2)
+    nb_s, Hkv, bs, D = ks.shape
+    assert kd.shape[1:] == (Hkv, bs, D) and vs.shape == ks.shape and vd.shape == kd.shape
+    rc = _load().oracle_copy_blocks(_ptr(ks), _ptr(vs), _ptr(kd), _ptr(vd), _ptr(pr), pr.shape[0],
+                                    nb_s, kd.shape[0], Hkv, bs, D)
+    if rc != 0:
+        raise ValueError("oracle_copy_blocks: block outside its pool")
+    return kd, vd
 
 
 def set_threads(n: int) -> None:

@@ -116,6 +116,35 @@ int oracle_append(const uint16_t *k_new, const uint16_t *v_new,
 }
 
 /*
+ * Whole-block copy between pools of layout [blocks, Hkv, bs, D]: for each
+ * pair i, block pairs[2i] of the source pools goes to block pairs[2i+1] of the
+ * destination pools (copy-on-write of a shared block; swapping blocks out to
+ * CPU memory and back: LLM 7 - Efficient LLM Serving, sec. 3 "Sharing and
+ * Preemption").  Returns -1 (copying nothing for that pair) if a block lies
+ * outside its pool.
+ */
+int oracle_copy_blocks(const uint16_t *k_src, const uint16_t *v_src, uint16_t *k_dst,
+                       uint16_t *v_dst, const int64_t *pairs, int64_t num_pairs,
+                       int64_t src_blocks, int64_t dst_blocks, int64_t Hkv, int64_t bs,
+                       int64_t D)
+{
+    int status = 0;
+    const int64_t per_block = Hkv * bs * D;
+    for (int64_t i = 0; i < num_pairs; ++i) {
+        int64_t src = pairs[2 * i], dst = pairs[2 * i + 1];
+        if (src < 0 || src >= src_blocks || dst < 0 || dst >= dst_blocks) {
+            status = -1;
+            continue;
+        }
+        for (int64_t e = 0; e < per_block; ++e) {
+            k_dst[dst * per_block + e] = k_src[src * per_block + e];
+            v_dst[dst * per_block + e] = v_src[src * per_block + e];
+        }
+    }
+    return status;
+}
+
+/*
  * q        [Tq, Hq, D]   bf16 bits, Tq = query_start_loc[R]
  * k_pool   [num_blocks, Hkv, bs, D] bf16 bits (v_pool the same)
  * block_tables [R, max_blocks] int32; seq_lens [R] int32 (L_r, this step's

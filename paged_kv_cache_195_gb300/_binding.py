@@ -27,7 +27,7 @@ PKV_ERR_TIMEOUT = -6
 
 EXPORTED = ("pkv_append", "pkv_attention", "pkv_attention_workspace_size",
             "pkv_workspace_init", "pkv_last_error", "pkv_get_device_error",
-            "pkv_attention_noalloc")
+            "pkv_attention_noalloc", "pkv_copy_blocks")
 
 
 class PagedKVError(RuntimeError):
@@ -74,6 +74,8 @@ def load_library(path: str = LIB_PATH):
         lib.pkv_get_device_error.restype = ctypes.c_int
         lib.pkv_attention_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, dp, vp]
         lib.pkv_attention_noalloc.restype = ctypes.c_int
+        lib.pkv_copy_blocks.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, dp, vp]
+        lib.pkv_copy_blocks.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -217,6 +219,30 @@ def pkv_attention_noalloc(q, k_pool, v_pool, block_tables, seq_lens, query_start
         ctypes.c_float(scale), ctypes.c_void_p(out.data_ptr()), ctypes.byref(dims),
         ctypes.c_void_p(_stream(stream, q.device))))
     return out
+
+
+def pkv_copy_blocks(k_src, v_src, k_dst, v_dst, pairs, stream=None):
+    """Copy whole blocks (all KV heads, K and V): block pairs[i, 0] of the
+    source pools to block pairs[i, 1] of the destination pools.  The pools may
+    be CUDA tensors or pinned host tensors (swap out / in); pairs is an int64
+    CUDA tensor [n, 2]."""
+    for t, name in ((k_src, "k_src"), (v_src, "v_src"), (k_dst, "k_dst"), (v_dst, "v_dst")):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or t.dim() != 4 \
+                or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 [blocks, Hkv, 16, 128] tensor")
+        if not (t.is_cuda or t.is_pinned()):
+            raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
+    _need(pairs, "pairs", torch.int64, 2)
+    if k_src.shape[1:] != k_dst.shape[1:] or v_src.shape != k_src.shape or v_dst.shape != k_dst.shape:
+        raise ValueError("pool shapes disagree")
+    nb, Hkv, bs, D = k_src.shape
+    dims = Dims(0, 0, Hkv, Hkv, D, bs, nb, 0)
+    dev = pairs.device
+    _check(load_library().pkv_copy_blocks(
+        ctypes.c_void_p(k_src.data_ptr()), ctypes.c_void_p(v_src.data_ptr()),
+        ctypes.c_void_p(k_dst.data_ptr()), ctypes.c_void_p(v_dst.data_ptr()),
+        ctypes.c_void_p(pairs.data_ptr()), pairs.shape[0], k_src.shape[0], k_dst.shape[0],
+        ctypes.byref(dims), ctypes.c_void_p(_stream(stream, dev))))
 
 
 def pkv_get_device_error(stream=None) -> int:

@@ -211,6 +211,38 @@ int pkv_append(const void* k_new, const void* v_new, const int64_t* slot_mapping
   return PKV_OK;
 }
 
+int pkv_copy_blocks(const void* k_src, const void* v_src, void* k_dst, void* v_dst,
+                    const int64_t* pairs, int32_t num_pairs, int32_t src_num_blocks,
+                    int32_t dst_num_blocks, const pkv_dims* dims, cudaStream_t stream) {
+  g_last_error[0] = '\0';
+  int rc = check_dims(dims, false);
+  if (rc != PKV_OK) return rc;
+  if (num_pairs < 0 || src_num_blocks < 0 || dst_num_blocks < 0)
+    return fail(PKV_ERR_INVALID, "negative count");
+  if (num_pairs == 0) return PKV_OK;
+  if (!k_src || !v_src || !k_dst || !v_dst || !pairs)
+    return fail(PKV_ERR_INVALID, "NULL pointer argument");
+  if (!aligned16(k_src) || !aligned16(v_src) || !aligned16(k_dst) || !aligned16(v_dst))
+    return fail(PKV_ERR_INVALID, "pools must be 16-byte aligned");
+  DeviceState* st = device_state();
+  if (!st) return PKV_ERR_CUDA;
+  pkv::CopyParams p;
+  p.k_src = static_cast<const __nv_bfloat16*>(k_src);
+  p.v_src = static_cast<const __nv_bfloat16*>(v_src);
+  p.k_dst = static_cast<__nv_bfloat16*>(k_dst);
+  p.v_dst = static_cast<__nv_bfloat16*>(v_dst);
+  p.pairs = pairs;
+  p.err = st->err;
+  p.num_pairs = num_pairs;
+  p.num_kv_heads = dims->num_kv_heads;
+  p.src_blocks = src_num_blocks;
+  p.dst_blocks = dst_num_blocks;
+  p.pdl = env_int("PKV_PDL", 1) != 0;
+  cudaError_t e = pkv::launch_copy_blocks(p, st->sm_count, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "copy_blocks launch");
+  return PKV_OK;
+}
+
 size_t pkv_attention_workspace_size(const pkv_dims* dims) {
   if (check_dims(dims, true) != PKV_OK) return 0;
   DeviceState* st = device_state();

@@ -161,7 +161,19 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// Packed fp32: d = a * b + c on both lanes of a float2 (one instruction).
+// Packed fp32: d = a * b + c on both lanes of a float2 (one instruction;
+// PKV_SCALAR_FMA=1 builds two scalar FMAs instead, for comparison).
+#ifndef PKV_SCALAR_FMA
+#define PKV_SCALAR_FMA 0
+#endif
+#if PKV_SCALAR_FMA
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  return make_float2(fmaf(a.x, b.x, c.x), fmaf(a.y, b.y, c.y));
+}
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  return make_float2(a.x * b.x, a.y * b.y);
+}
+#else
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
   float2 d;
   asm("fma.rn.f32x2 %0, %1, %2, %3;"
@@ -180,6 +192,7 @@ __device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
         "l"(reinterpret_cast<unsigned long long&>(b)));
   return d;
 }
+#endif
 
 // Two packed bf16 -> two fp32 (exact: a bf16 is the top half of an fp32).
 __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {

@@ -27,6 +27,23 @@ struct AppendParams {
 
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
 
+// Whole-block copies between two pools (device or mapped host memory).
+struct CopyParams {
+  const __nv_bfloat16* k_src;
+  const __nv_bfloat16* v_src;
+  __nv_bfloat16* k_dst;
+  __nv_bfloat16* v_dst;
+  const int64_t* pairs;  // [num_pairs, 2]: (source block, destination block)
+  int* err;
+  int num_pairs;
+  int num_kv_heads;
+  long long src_blocks;
+  long long dst_blocks;
+  int pdl;
+};
+
+cudaError_t launch_copy_blocks(const CopyParams& p, int sm_count, cudaStream_t stream);
+
 // Split-context decode: the device plan, the paged gather, the online
 // softmax, and the log-sum-exp merge, in one launch.
 struct DecodeParams {

@@ -313,3 +313,86 @@ def test_prefill_long_prefix_many_key_tiles(monkeypatch):
     out = gpu_step(inp)
     want = snapshot_oracle(snap)
     assert_close(to_f64(out[torch.tensor(snap["qrows"], device="cuda")]), want, "long prefix")
+
+
+def test_captured_graph_follows_new_lengths():
+    """One captured step serves later steps whose lengths differ: the plan is
+    made on the device from seq_lens / query_start_loc (The Serving Playbook,
+    "CUDA graphs and the CPU you forgot about": step buffers are fixed, their
+    contents change)."""
+    R, max_blocks, Hq, Hkv = 16, 40, 12, 2
+    shape_a = wl.StepShape("ga", np.full(R, 300), np.ones(R), Hq, Hkv, num_blocks=R * max_blocks,
+                           seed=51)
+    inp = wl.make_step(shape_a, device="cuda")
+    bt = torch.full((R, max_blocks), -1, dtype=torch.int32, device="cuda")
+    perm = torch.randperm(R * max_blocks, generator=torch.Generator().manual_seed(9)).int().cuda()
+    bt[:] = perm.view(R, max_blocks)
+    seq = torch.full((R,), 300, dtype=torch.int32, device="cuda")
+    qsl = torch.arange(R + 1, dtype=torch.int32, device="cuda")
+    out = torch.empty_like(inp.q)
+    dims = pkv.make_dims(tuple(inp.q.shape), tuple(inp.k_pool.shape), R, max_blocks)
+    ws = pkv.Workspace(dims)
+    pkv.pkv_workspace_init(ws, dims)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        pkv.pkv_attention(inp.q, inp.k_pool, inp.v_pool, bt, seq, qsl, inp.scale, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        pkv.pkv_attention(inp.q, inp.k_pool, inp.v_pool, bt, seq, qsl, inp.scale, out=out, workspace=ws)
+    rng = np.random.default_rng(52)
+    h = host_copy(inp)
+    for trial in range(3):
+        lens = rng.integers(1, max_blocks * 16 + 1, size=R).astype(np.int32)
+        seq.copy_(torch.from_numpy(lens))
+        g.replay()
+        torch.cuda.synchronize()
+        want = oracle.paged_attention(h["q"], h["k_pool"], h["v_pool"], bt.cpu().numpy(), lens,
+                                      np.arange(R + 1, dtype=np.int32), inp.scale)
+        assert_close(to_f64(out), want, f"graph replay {trial}")
+
+
+# ---------------------------------------------------------------------------
+# Block copies: copy-on-write and swap to / from pinned host memory
+# ---------------------------------------------------------------------------
+
+def test_copy_blocks_copy_on_write_bit_exact():
+    shape = wl.StepShape("cow", [200, 90], [1, 1], 32, 8, num_blocks=40, seed=33)
+    inp = wl.make_step(shape, device="cuda")
+    kp0, vp0 = wl.bf16_bits(inp.k_pool), wl.bf16_bits(inp.v_pool)
+    pairs = torch.tensor([[3, 30], [17, 31], [0, 39]], dtype=torch.int64, device="cuda")
+    pkv.pkv_copy_blocks(inp.k_pool, inp.v_pool, inp.k_pool, inp.v_pool, pairs)
+    torch.cuda.synchronize()
+    ek, ev = oracle.copy_blocks(kp0, vp0, kp0, vp0, pairs.cpu().numpy())
+    assert np.array_equal(wl.bf16_bits(inp.k_pool), ek)
+    assert np.array_equal(wl.bf16_bits(inp.v_pool), ev)
+
+
+def test_swap_out_and_back_through_pinned_host_memory():
+    shape = wl.StepShape("swap", [500, 33], [1, 1], 12, 2, num_blocks=60, seed=34)
+    inp = wl.make_step(shape, device="cuda")
+    host_k = torch.zeros((8,) + tuple(inp.k_pool.shape[1:]), dtype=torch.bfloat16).pin_memory()
+    host_v = torch.zeros_like(host_k).pin_memory()
+    out_pairs = torch.tensor([[i * 5, i] for i in range(8)], dtype=torch.int64, device="cuda")
+    kp0, vp0 = wl.bf16_bits(inp.k_pool), wl.bf16_bits(inp.v_pool)
+    pkv.pkv_copy_blocks(inp.k_pool, inp.v_pool, host_k, host_v, out_pairs)   # swap out
+    torch.cuda.synchronize()
+    ek, ev = oracle.copy_blocks(kp0, vp0, np.zeros_like(wl.bf16_bits(host_k)),
+                                np.zeros_like(wl.bf16_bits(host_v)), out_pairs.cpu().numpy())
+    assert np.array_equal(wl.bf16_bits(host_k), ek) and np.array_equal(wl.bf16_bits(host_v), ev)
+    in_pairs = torch.tensor([[i, 52 + i] for i in range(8)], dtype=torch.int64, device="cuda")
+    pkv.pkv_copy_blocks(host_k, host_v, inp.k_pool, inp.v_pool, in_pairs)    # swap back in
+    torch.cuda.synchronize()
+    ek2, ev2 = oracle.copy_blocks(ek, ev, kp0, vp0, in_pairs.cpu().numpy())
+    assert np.array_equal(wl.bf16_bits(inp.k_pool), ek2)
+    assert np.array_equal(wl.bf16_bits(inp.v_pool), ev2)
+
+
+def test_copy_blocks_out_of_range_is_reported():
+    shape = wl.StepShape("cowbad", [40], [1], 4, 2, num_blocks=8, seed=35)
+    inp = wl.make_step(shape, device="cuda")
+    before = wl.bf16_bits(inp.k_pool).copy()
+    pairs = torch.tensor([[2, 8]], dtype=torch.int64, device="cuda")
+    pkv.pkv_copy_blocks(inp.k_pool, inp.v_pool, inp.k_pool, inp.v_pool, pairs)
+    assert pkv.pkv_get_device_error() == pkv._binding.PKV_ERR_DEVICE_BOUNDS
+    assert np.array_equal(wl.bf16_bits(inp.k_pool), before)

@@ -343,3 +343,19 @@ def test_rejects_inconsistent_lengths():
     with pytest.raises(ValueError):   # block id beyond the pool
         oracle.paged_attention(q, pool, pool, bt + 7, np.array([5], np.int32),
                                np.array([0, 3], np.int32), 1.0)
+
+
+def test_copy_blocks_matches_numpy_and_touches_nothing_else():
+    rng = np.random.default_rng(21)
+    src = rng.integers(0, 2**16, size=(10, 3, 16, 8), dtype=np.uint16)
+    vsrc = rng.integers(0, 2**16, size=(10, 3, 16, 8), dtype=np.uint16)
+    dst = rng.integers(0, 2**16, size=(6, 3, 16, 8), dtype=np.uint16)
+    vdst = rng.integers(0, 2**16, size=(6, 3, 16, 8), dtype=np.uint16)
+    pairs = np.array([[7, 0], [2, 5], [9, 3]], np.int64)
+    kd, vd = oracle.copy_blocks(src, vsrc, dst, vdst, pairs)
+    ek, ev = dst.copy(), vdst.copy()
+    ek[pairs[:, 1]] = src[pairs[:, 0]]
+    ev[pairs[:, 1]] = vsrc[pairs[:, 0]]
+    assert np.array_equal(kd, ek) and np.array_equal(vd, ev)
+    with pytest.raises(ValueError):
+        oracle.copy_blocks(src, vsrc, dst, vdst, np.array([[10, 0]], np.int64))
