@@ -38,7 +38,7 @@ constexpr int kPfThreads = 192;
 constexpr int kTileRows = 128;               // MMA M
 constexpr int kKeyTile = 128;                // MMA N for S, K for PV
 constexpr int kHalfBytes = kTileRows * 128;  // one 64-column half of a 128-row tile
-constexpr uint32_t kTmemCols = 256;          // S: cols 0..127, O: cols 128..255
+constexpr uint32_t kTmemCols = 512;          // S0: cols 0..127, S1: 128..255, O: 256..383
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kNegBig = -1.0e30f;
 
@@ -56,10 +56,11 @@ struct __align__(1024) PfSmem {
   uint8_t q[2][kHalfBytes];      // Q: d 0..63 | d 64..127
   uint8_t k[2][2][kHalfBytes];   // [stage][d half]
   uint8_t v[2][2][kHalfBytes];   // [stage][d half]
-  uint8_t p[2][kHalfBytes];      // P: keys 0..63 | keys 64..127
+  uint8_t p[2][2][kHalfBytes];   // [buffer][keys 0..63 | keys 64..127]
   uint64_t q_full, q_empty;
   uint64_t k_full[2], v_full[2], kv_empty[2];
-  uint64_t s_full, p_full, o_full, o_empty;
+  uint64_t s_full[2], s_free[2], p_full[2], p_free[2];
+  uint64_t o_full, o_empty;
   Item items[2];
   uint32_t tmem_base;
   int abort_flag;
@@ -140,8 +141,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       mbar_init(&sm.v_full[s], 1);
       mbar_init(&sm.kv_empty[s], 1);
     }
-    mbar_init(&sm.s_full, 1);
-    mbar_init(&sm.p_full, 4);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.s_full[b], 1);   // tcgen05.commit after S = QK^T into buffer b
+      mbar_init(&sm.s_free[b], 4);   // the four softmax warps have read S buffer b
+      mbar_init(&sm.p_full[b], 4);   // P buffer b written (and O rescaled) by all four
+      mbar_init(&sm.p_free[b], 1);   // tcgen05.commit after the PV that read P buffer b
+    }
     mbar_init(&sm.o_full, 1);
     mbar_init(&sm.o_empty, 4);
     sm.abort_flag = 0;
@@ -214,13 +219,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         it.L = L;
         it.nj = (it.pos0 + it.nt - 1) / kKeyTile + 1;
         it.end = 0;
-        if (n_item >= 1 && !mbar_wait(&sm.q_empty, (n_item - 1) & 1, p.err, abort_flag)) break;
-        if (lane == 0) {
-          sm.items[n_item & 1] = it;
-          mbar_arrive_expect_tx(&sm.q_full, 2u * 64u * ROWS * 2u);
-          tma_load_3d(sm.q[0], &qmap, 0, k * G, it.row0, &sm.q_full);
-          tma_load_3d(sm.q[1], &qmap, 64, k * G, it.row0, &sm.q_full);
-        }
         const int nbl = ceil_div(L, kBlockSize);
         const int32_t* bt = p.block_tables + (long long)r * p.max_blocks;
         for (int j = 0; j < it.nj; ++j, ++tile_ctr) {
@@ -253,6 +251,19 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             }
           }
           __syncwarp();
+          if (j == 0) {
+            // Q of this item, once the previous item's MMAs are done with Q
+            // (its first K/V tile is already on its way).
+            if (n_item >= 1 && !mbar_wait(&sm.q_empty, (n_item - 1) & 1, p.err, abort_flag))
+              break;
+            if (lane == 0) {
+              sm.items[n_item & 1] = it;
+              mbar_arrive_expect_tx(&sm.q_full, 2u * 64u * ROWS * 2u);
+              tma_load_3d(sm.q[0], &qmap, 0, k * G, it.row0, &sm.q_full);
+              tma_load_3d(sm.q[1], &qmap, 64, k * G, it.row0, &sm.q_full);
+            }
+            __syncwarp();
+          }
         }
         ++n_item;
         item += gridDim.x;
@@ -268,46 +279,56 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
   } else if (warp == 5) {
     // ========================= MMA issuer =================================
+    // Tile t: S(t) = Q K(t)^T into S buffer t&1, then O += P(t-1) V(t-1).  S
+    // of the next tile therefore runs on the tensor core while the softmax
+    // warps work on the current one.
     if (lane == 0) {
       constexpr uint32_t kIdescS = idesc_bf16_f32(kTileRows, kKeyTile, 0, 0);
       constexpr uint32_t kIdescO = idesc_bf16_f32(kTileRows, kHeadDim, 0, 1);
-      const uint32_t tS = tmem, tO = tmem + kKeyTile;
-      int tile_ctr = 0;
-      for (int n_item = 0;; ++n_item) {
+      const uint32_t tO = tmem + 2 * kKeyTile;
+      int t = 0;  // tile counter, shared sequence with the producer and softmax
+      bool ok = true;
+      auto pv = [&](int tt, bool first, int n_item) {
+        const int b = tt & 1;
+        ok = ok && mbar_wait(&sm.p_full[b], (tt >> 1) & 1, p.err, abort_flag);
+        ok = ok && mbar_wait(&sm.v_full[b], (tt >> 1) & 1, p.err, abort_flag);
+        if (first && n_item > 0)
+          ok = ok && mbar_wait(&sm.o_empty, (n_item - 1) & 1, p.err, abort_flag);
+        tc_fence_after();
+        #pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t da = smem_desc_sw128(smem_u32(sm.p[b][kk >> 2]) + (kk & 3) * 32, 16, 1024);
+          // V is MN-major (d contiguous): atoms of 64 d x 8 keys; the two d
+          // halves are kHalfBytes apart, 8-key groups 1024 bytes apart.
+          const uint64_t db = smem_desc_sw128(smem_u32(sm.v[b][0]) + kk * 2048, kHalfBytes, 1024);
+          tc_mma_f16_ss(tO, da, db, kIdescO, !first || kk > 0);
+        }
+        tc_commit(&sm.kv_empty[b]);
+        tc_commit(&sm.p_free[b]);
+      };
+      for (int n_item = 0; ok; ++n_item) {
         if (!mbar_wait(&sm.q_full, n_item & 1, p.err, abort_flag)) break;
         const Item it = sm.items[n_item & 1];
         if (it.end) break;
         tc_fence_after();
-        bool ok = true;
-        for (int j = 0; j < it.nj && ok; ++j, ++tile_ctr) {
-          const int st = tile_ctr & 1;
-          ok = mbar_wait(&sm.k_full[st], (tile_ctr >> 1) & 1, p.err, abort_flag);
+        for (int j = 0; j < it.nj && ok; ++j, ++t) {
+          const int b = t & 1;
+          ok = mbar_wait(&sm.k_full[b], (t >> 1) & 1, p.err, abort_flag);
+          if (t >= 2) ok = ok && mbar_wait(&sm.s_free[b], ((t >> 1) - 1) & 1, p.err, abort_flag);
           tc_fence_after();
+          const uint32_t tS = tmem + b * kKeyTile;
           #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t a = smem_desc_sw128(smem_u32(sm.q[kk >> 2]) + (kk & 3) * 32, 16, 1024);
-            const uint64_t b = smem_desc_sw128(smem_u32(sm.k[st][kk >> 2]) + (kk & 3) * 32, 16, 1024);
-            tc_mma_f16_ss(tS, a, b, kIdescS, kk > 0);
+            const uint64_t da = smem_desc_sw128(smem_u32(sm.q[kk >> 2]) + (kk & 3) * 32, 16, 1024);
+            const uint64_t db = smem_desc_sw128(smem_u32(sm.k[b][kk >> 2]) + (kk & 3) * 32, 16, 1024);
+            tc_mma_f16_ss(tS, da, db, kIdescS, kk > 0);
           }
-          tc_commit(&sm.s_full);
-          ok = ok && mbar_wait(&sm.p_full, tile_ctr & 1, p.err, abort_flag);
-          ok = ok && mbar_wait(&sm.v_full[st], (tile_ctr >> 1) & 1, p.err, abort_flag);
-          if (j == 0 && n_item > 0)
-            ok = ok && mbar_wait(&sm.o_empty, (n_item - 1) & 1, p.err, abort_flag);
-          tc_fence_after();
-          #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t a = smem_desc_sw128(smem_u32(sm.p[kk >> 2]) + (kk & 3) * 32, 16, 1024);
-            // V is MN-major (d contiguous): atoms of 64 d x 8 keys; the two d
-            // halves are kHalfBytes apart, 8-key groups 1024 bytes apart.
-            const uint64_t b = smem_desc_sw128(smem_u32(sm.v[st][0]) + kk * 2048, kHalfBytes, 1024);
-            tc_mma_f16_ss(tO, a, b, kIdescO, j > 0 || kk > 0);
-          }
-          tc_commit(&sm.kv_empty[st]);
+          tc_commit(&sm.s_full[b]);
+          if (j >= 1) pv(t - 1, j == 1, n_item);
         }
+        if (ok) pv(t - 1, it.nj == 1, n_item);  // the item's last tile
         tc_commit(&sm.o_full);
         tc_commit(&sm.q_empty);
-        if (!ok) break;
       }
     }
     __syncwarp();
@@ -315,7 +336,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     // ===================== softmax + epilogue (warps 0-3) ==================
     const int row = tid;  // MMA row == TMEM lane
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    const uint32_t tS = tmem + lane_off, tO = tmem + lane_off + kKeyTile;
+    const uint32_t tO = tmem + lane_off + 2 * kKeyTile;
     const int t_local = row / G, h = row % G;
     int tile_ctr = 0;
     for (int n_item = 0;; ++n_item) {
@@ -327,29 +348,48 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       float m = kNegBig, l = 0.f;
       bool ok = true;
       for (int j = 0; j < it.nj; ++j, ++tile_ctr) {
-        ok = ok && mbar_wait(&sm.s_full, tile_ctr & 1, p.err, abort_flag);
+        const int sb = tile_ctr & 1;  // S / P / K / V buffer of this tile
+        const uint32_t tS = tmem + lane_off + sb * kKeyTile;
+        ok = ok && mbar_wait(&sm.s_full[sb], (tile_ctr >> 1) & 1, p.err, abort_flag);
         tc_fence_after();
-        float s[kKeyTile];
-        #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, *reinterpret_cast<float(*)[32]>(&s[c * 32]));
-        tc_wait_ld();
+        // Pass 1: the row maximum of this tile (masked keys excluded).  S
+        // stays in TMEM and is read in 32-column chunks, twice, so that the
+        // loop bodies stay small.
         const int kbase = j * kKeyTile;
-        float mx = -INFINITY;
+        const bool full_tile = kbase + kKeyTile - 1 <= prow;  // no key of this tile masked
+        float mxp[8];
         #pragma unroll
-        for (int c = 0; c < kKeyTile; ++c) {
-          s[c] = (kbase + c <= prow) ? s[c] * p.scale_log2 : -INFINITY;
-          mx = fmaxf(mx, s[c]);
+        for (int i = 0; i < 8; ++i) mxp[i] = -INFINITY;
+        #pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          float v[32];
+          tmem_ld32(tS + c * 32, v);
+          tc_wait_ld();
+          if (full_tile) {
+            #pragma unroll
+            for (int i = 0; i < 32; ++i) mxp[i & 7] = fmaxf(mxp[i & 7], v[i]);
+          } else {
+            #pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (kbase + c * 32 + i <= prow) mxp[i & 7] = fmaxf(mxp[i & 7], v[i]);
+          }
         }
+        float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
+                         fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
+        mx = mx * p.scale_log2;  // scale > 0 keeps the arg max
         float m_use = m;
         const bool grow = j == 0 ? true : (mx > m + kRescaleLog2);
         if (j == 0) {
           m_use = fmaxf(m, mx);
         } else if (__any_sync(0xffffffffu, grow)) {
           // O (and l) move to the new reference maximum; rows that do not
-          // grow scale by 1.
+          // grow scale by 1.  O must first hold the previous tile's PV.
+          ok = ok && mbar_wait(&sm.p_free[(tile_ctr - 1) & 1], ((tile_ctr - 1) >> 1) & 1, p.err,
+                               abort_flag);
+          tc_fence_after();
           const float m_new = grow ? fmaxf(m, mx) : m;
           const float alpha = fast_exp2(m - m_new);
-          #pragma unroll
+          #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
             float o[32];
             tmem_ld32(tO + c * 32, o);
@@ -363,30 +403,50 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           m_use = m_new;
         }
         m = m_use;
-        // P = exp2(s - m) in bf16, row-major keys, 128-byte swizzle; the
-        // normaliser sums the rounded values the MMA will use.
-        float sum = 0.f;
-        uint8_t* prow_base = nullptr;
-        #pragma unroll
-        for (int c = 0; c < 16; ++c) {  // 16-byte chunk c = keys 8c .. 8c+7
-          uint32_t w[4];
+        // P buffer sb was last read by the PV of tile - 2.
+        if (tile_ctr >= 2)
+          ok = ok && mbar_wait(&sm.p_free[sb], ((tile_ctr >> 1) - 1) & 1, p.err, abort_flag);
+        // Pass 2: P = exp2(s * scale_log2 - m) in bf16, keys contiguous per
+        // row, 128-byte swizzle; the normaliser sums the rounded values the
+        // MMA will use.
+        float sump[4] = {0.f, 0.f, 0.f, 0.f};
+        const float neg_m = -m;
+        #pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          float v[32];
+          tmem_ld32(tS + c * 32, v);
+          tc_wait_ld();
           #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float p0 = fast_exp2(s[c * 8 + 2 * e] - m);
-            const float p1 = fast_exp2(s[c * 8 + 2 * e + 1] - m);
-            w[e] = pack_bf16x2(p0, p1);
-            const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&w[e]);
-            sum += __low2float(b2) + __high2float(b2);
+          for (int q4 = 0; q4 < 4; ++q4) {  // 16-byte chunk: keys c*32 + q4*8 .. +8
+            uint32_t w[4];
+            #pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int i0 = q4 * 8 + 2 * e;
+              float p0 = fast_exp2(fmaf(v[i0], p.scale_log2, neg_m));
+              float p1 = fast_exp2(fmaf(v[i0 + 1], p.scale_log2, neg_m));
+              if (!full_tile) {
+                if (kbase + c * 32 + i0 > prow) p0 = 0.f;
+                if (kbase + c * 32 + i0 + 1 > prow) p1 = 0.f;
+              }
+              w[e] = pack_bf16x2(p0, p1);
+              const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&w[e]);
+              sump[e] += __low2float(b2) + __high2float(b2);
+            }
+            const int chunk = c * 4 + q4, half = chunk >> 3, cc = chunk & 7;
+            uint8_t* rowp = sm.p[sb][half] + (row >> 3) * 1024 + (row & 7) * 128;
+            *reinterpret_cast<uint4*>(rowp + ((cc ^ (row & 7)) * 16)) =
+                make_uint4(w[0], w[1], w[2], w[3]);
           }
-          const int half = c >> 3, cc = c & 7;
-          prow_base = sm.p[half] + (row >> 3) * 1024 + (row & 7) * 128;
-          *reinterpret_cast<uint4*>(prow_base + ((cc ^ (row & 7)) * 16)) =
-              make_uint4(w[0], w[1], w[2], w[3]);
         }
+        // S is no longer needed: the MMA may overwrite this buffer (tile + 2).
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.s_free[sb]);
+        const float sum = (sump[0] + sump[1]) + (sump[2] + sump[3]);
         l += sum;
         // Keys past the request's end inside its last block may hold anything
         // (even NaN); zero those V rows so that 0 * V stays 0 in the MMA.
-        const int st = tile_ctr & 1;
+        const int st = sb;
         const int tail0 = it.L - kbase;                      // first key >= L in this tile
         const int tail1 = min(kKeyTile, ceil_div(it.L, kBlockSize) * kBlockSize - kbase);
         if (warp == 0 && tail0 < tail1 && tail0 >= 0) {
@@ -401,7 +461,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.p_full);
+        if (lane == 0) mbar_arrive(&sm.p_full[sb]);
       }
       // ---- epilogue: O / l -> bf16 -> out ---------------------------------
       ok = ok && mbar_wait(&sm.o_full, n_item & 1, p.err, abort_flag);
