@@ -54,6 +54,16 @@ def _load():
                 p, p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32,
                 ctypes.c_double, p]
             lib.oracle_paged_attention.restype = ctypes.c_int
+            u8 = ctypes.c_uint8
+            lib.oracle_e4m3_decode.argtypes = [u8]
+            lib.oracle_e4m3_decode.restype = ctypes.c_double
+            lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+            lib.oracle_e4m3_encode.restype = u8
+            lib.oracle_append_fp8.argtypes = [p, p, p, i64, i64, i64, i64, i64, p, p, p, p]
+            lib.oracle_append_fp8.restype = ctypes.c_int
+            lib.oracle_paged_attention_fp8.argtypes = [
+                p, p, p, p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32, ctypes.c_double, p]
+            lib.oracle_paged_attention_fp8.restype = ctypes.c_int
             lib.oracle_copy_blocks.argtypes = [p, p, p, p, p, i64, i64, i64, i64, i64, i64]
             lib.oracle_copy_blocks.restype = ctypes.c_int
             lib.oracle_set_threads.argtypes = [ctypes.c_int]
@@ -118,6 +128,53 @@ def paged_attention(q, k_pool, v_pool, block_tables, seq_lens,
         D, bs, nb, bt.shape[1], float(scale), _ptr(out))
     if rc != 0:
         raise ValueError(f"oracle_paged_attention: inconsistent inputs (rc={rc})")
+    return out
+
+
+def e4m3_decode(code: int) -> float:
+    """Value of an e4m3 code (NaN for the NaN patterns)."""
+    return float(_load().oracle_e4m3_decode(int(code) & 0xFF))
+
+
+def e4m3_encode(x: float) -> int:
+    """Nearest e4m3 code to the fp32 value x (ties to even, saturating)."""
+    return int(_load().oracle_e4m3_encode(float(np.float32(x))))
+
+
+def append_fp8(k_new, v_new, slot_mapping, k_pool, v_pool, k_scale, v_scale):
+    """Quantise new rows (bf16 bits) into copies of uint8 e4m3 pools:
+    code = encode(fp32(x) / fp32(scale[h]))."""
+    k_new, v_new = _c(k_new, np.uint16), _c(v_new, np.uint16)
+    slots = _c(slot_mapping, np.int64)
+    kp, vp = _c(k_pool, np.uint8).copy(), _c(v_pool, np.uint8).copy()
+    ks, vs = _c(k_scale, np.float32), _c(v_scale, np.float32)
+    T, Hkv, D = k_new.shape
+    nb, _, bs, _ = kp.shape
+    rc = _load().oracle_append_fp8(_ptr(k_new), _ptr(v_new), _ptr(slots), T, Hkv, D, bs, nb,
+                                   _ptr(ks), _ptr(vs), _ptr(kp), _ptr(vp))
+    if rc != 0:
+        raise ValueError("oracle_append_fp8: slot outside the pool")
+    return kp, vp
+
+
+def paged_attention_fp8(q, k_pool, v_pool, k_scale, v_scale, block_tables, seq_lens,
+                        query_start_loc, scale):
+    """paged_attention over uint8 e4m3 pools dequantised by per-KV-head scales."""
+    q = _c(q, np.uint16)
+    kp, vp = _c(k_pool, np.uint8), _c(v_pool, np.uint8)
+    ks, vs = _c(k_scale, np.float32), _c(v_scale, np.float32)
+    bt = _c(block_tables, np.int32)
+    sl = _c(seq_lens, np.int32)
+    qsl = _c(query_start_loc, np.int32)
+    Tq, Hq, D = q.shape
+    nb, Hkv, bs, _ = kp.shape
+    R = sl.shape[0]
+    out = np.zeros((Tq, Hq, D), dtype=np.float64)
+    rc = _load().oracle_paged_attention_fp8(
+        _ptr(q), _ptr(kp), _ptr(vp), _ptr(ks), _ptr(vs), _ptr(bt), _ptr(sl), _ptr(qsl), R, Hq,
+        Hkv, D, bs, nb, bt.shape[1], float(scale), _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_paged_attention_fp8: inconsistent inputs")
     return out
 
 

@@ -115,6 +115,89 @@ int oracle_append(const uint16_t *k_new, const uint16_t *v_new,
     return status;
 }
 
+/* ------------------------------------------------------------------------
+ * FP8 (e4m3) KV cache.  Eight-bit KV halves the bytes a decode step reads
+ * (What Actually Runs the Model, "The KV cache"; The Serving Playbook,
+ * "Quantized serving").  The format is the 8-bit float with 1 sign bit, 4
+ * exponent bits (bias 7) and 3 mantissa bits, no infinities, one NaN pattern
+ * per sign (exponent and mantissa all ones), largest finite magnitude 448.
+ * [READING] A stored code is round-to-nearest-even of x / scale computed in
+ * fp32, saturated to +-448; the value it stands for is decode(code) * scale.
+ * ------------------------------------------------------------------------ */
+
+double oracle_e4m3_decode(uint8_t c)
+{
+    const int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)m, -9);               /* subnormal: m/8 * 2^(1-7) */
+    else
+        v = ldexp(1.0 + m / 8.0, e - 7);
+    return s ? -v : v;
+}
+
+/* Nearest finite code by exhaustive search; ties go to the even code. */
+uint8_t oracle_e4m3_encode(float x)
+{
+    if (x != x)
+        return 0x7F;
+    const double a = fabs((double)x);
+    int best = 0;
+    double best_err = INFINITY;
+    for (int c = 0; c <= 0x7E; ++c) {           /* non-negative finite codes */
+        const double err = fabs(oracle_e4m3_decode((uint8_t)c) - a);
+        if (err < best_err || (err == best_err && (c & 1) == 0 && (best & 1) == 1)) {
+            best_err = err;
+            best = c;
+        }
+    }
+    if (a >= 448.0)
+        best = 0x7E;                            /* saturate */
+    return (uint8_t)(signbit(x) ? (best | 0x80) : best);  /* -0 keeps its sign */
+}
+
+static float bf16_bits_to_float(uint16_t bits)
+{
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/*
+ * Append into fp8 pools: code = encode(fp32(x) / fp32(scale[h])).
+ * k_scale / v_scale: [Hkv] floats.  Returns -1 if a slot lies beyond the pool.
+ */
+int oracle_append_fp8(const uint16_t *k_new, const uint16_t *v_new,
+                      const int64_t *slot_mapping, int64_t num_new_tokens, int64_t Hkv,
+                      int64_t D, int64_t bs, int64_t num_blocks, const float *k_scale,
+                      const float *v_scale, uint8_t *k_pool, uint8_t *v_pool)
+{
+    int status = 0;
+    for (int64_t t = 0; t < num_new_tokens; ++t) {
+        const int64_t slot = slot_mapping[t];
+        if (slot < 0)
+            continue;
+        if (slot >= num_blocks * bs) {
+            status = -1;
+            continue;
+        }
+        const int64_t blk = slot / bs, off = slot % bs;
+        for (int64_t h = 0; h < Hkv; ++h)
+            for (int64_t d = 0; d < D; ++d) {
+                const int64_t src = (t * Hkv + h) * D + d;
+                const int64_t dst = pool_index(blk, h, off, d, Hkv, bs, D);
+                const float kq = bf16_bits_to_float(k_new[src]) / k_scale[h];
+                const float vq = bf16_bits_to_float(v_new[src]) / v_scale[h];
+                k_pool[dst] = oracle_e4m3_encode(kq);
+                v_pool[dst] = oracle_e4m3_encode(vq);
+            }
+    }
+    return status;
+}
+
 /*
  * Whole-block copy between pools of layout [blocks, Hkv, bs, D]: for each
  * pair i, block pairs[2i] of the source pools goes to block pairs[2i+1] of the
@@ -154,13 +237,15 @@ int oracle_copy_blocks(const uint16_t *k_src, const uint16_t *v_src, uint16_t *k
  * Returns 0, -1 for inconsistent arguments (q_r > L_r, a table entry outside
  * the pool, L_r beyond the table), -2 if memory for a score row is exhausted.
  */
-int oracle_paged_attention(const uint16_t *q, const uint16_t *k_pool,
-                           const uint16_t *v_pool, const int32_t *block_tables,
-                           const int32_t *seq_lens,
-                           const int32_t *query_start_loc, int32_t R,
-                           int32_t Hq, int32_t Hkv, int32_t D, int32_t bs,
-                           int32_t num_blocks, int32_t max_blocks, double scale,
-                           double *out)
+static int paged_attention_impl(const uint16_t *q, const uint16_t *k_pool,
+                                const uint16_t *v_pool, const uint8_t *k8, const uint8_t *v8,
+                                const float *k_scale, const float *v_scale,
+                                const int32_t *block_tables,
+                                const int32_t *seq_lens,
+                                const int32_t *query_start_loc, int32_t R,
+                                int32_t Hq, int32_t Hkv, int32_t D, int32_t bs,
+                                int32_t num_blocks, int32_t max_blocks, double scale,
+                                double *out)
 {
     if (Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || bs <= 0)
         return -1;
@@ -206,10 +291,12 @@ int oracle_paged_attention(const uint16_t *q, const uint16_t *k_pool,
             int32_t blk = block_tables[(int64_t)r * max_blocks + j / bs];
             int32_t off = j % bs;
             double dot = 0.0;
-            for (int32_t d = 0; d < D; ++d)
-                dot += bf16_bits_to_double(q[((int64_t)t * Hq + h) * D + d]) *
-                       bf16_bits_to_double(
-                           k_pool[pool_index(blk, kh, off, d, Hkv, bs, D)]);
+            for (int32_t d = 0; d < D; ++d) {
+                const int64_t e = pool_index(blk, kh, off, d, Hkv, bs, D);
+                const double kv = k8 ? oracle_e4m3_decode(k8[e]) * (double)k_scale[kh]
+                                     : bf16_bits_to_double(k_pool[e]);
+                dot += bf16_bits_to_double(q[((int64_t)t * Hq + h) * D + d]) * kv;
+            }
             s[j] = scale * dot;
             if (s[j] > m)
                 m = s[j];
@@ -226,11 +313,38 @@ int oracle_paged_attention(const uint16_t *q, const uint16_t *k_pool,
             int32_t blk = block_tables[(int64_t)r * max_blocks + j / bs];
             int32_t off = j % bs;
             double w = s[j] / z;
-            for (int32_t d = 0; d < D; ++d)
-                o[d] += w * bf16_bits_to_double(
-                                v_pool[pool_index(blk, kh, off, d, Hkv, bs, D)]);
+            for (int32_t d = 0; d < D; ++d) {
+                const int64_t e = pool_index(blk, kh, off, d, Hkv, bs, D);
+                const double vv = v8 ? oracle_e4m3_decode(v8[e]) * (double)v_scale[kh]
+                                     : bf16_bits_to_double(v_pool[e]);
+                o[d] += w * vv;
+            }
         }
         free(s);
     }
     return status;
+}
+
+int oracle_paged_attention(const uint16_t *q, const uint16_t *k_pool, const uint16_t *v_pool,
+                           const int32_t *block_tables, const int32_t *seq_lens,
+                           const int32_t *query_start_loc, int32_t R, int32_t Hq,
+                           int32_t Hkv, int32_t D, int32_t bs, int32_t num_blocks,
+                           int32_t max_blocks, double scale, double *out)
+{
+    return paged_attention_impl(q, k_pool, v_pool, NULL, NULL, NULL, NULL, block_tables,
+                                seq_lens, query_start_loc, R, Hq, Hkv, D, bs, num_blocks,
+                                max_blocks, scale, out);
+}
+
+/* The same attention over fp8 pools: K = decode(code) * k_scale[h], V alike. */
+int oracle_paged_attention_fp8(const uint16_t *q, const uint8_t *k_pool, const uint8_t *v_pool,
+                               const float *k_scale, const float *v_scale,
+                               const int32_t *block_tables, const int32_t *seq_lens,
+                               const int32_t *query_start_loc, int32_t R, int32_t Hq,
+                               int32_t Hkv, int32_t D, int32_t bs, int32_t num_blocks,
+                               int32_t max_blocks, double scale, double *out)
+{
+    return paged_attention_impl(q, NULL, NULL, k_pool, v_pool, k_scale, v_scale, block_tables,
+                                seq_lens, query_start_loc, R, Hq, Hkv, D, bs, num_blocks,
+                                max_blocks, scale, out);
 }

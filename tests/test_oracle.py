@@ -359,3 +359,91 @@ def test_copy_blocks_matches_numpy_and_touches_nothing_else():
     assert np.array_equal(kd, ek) and np.array_equal(vd, ev)
     with pytest.raises(ValueError):
         oracle.copy_blocks(src, vsrc, dst, vdst, np.array([[10, 0]], np.int64))
+
+
+# ---------------------------------------------------------------------------
+# FP8 (e4m3) KV: the codec against the format's definition, and fp8 attention
+# against bf16-free dequantised attention
+# ---------------------------------------------------------------------------
+
+def test_e4m3_known_codes():
+    assert oracle.e4m3_decode(0x38) == 1.0          # exponent 7 = bias, mantissa 0
+    assert oracle.e4m3_decode(0xB8) == -1.0
+    assert oracle.e4m3_decode(0x7E) == 448.0        # largest finite
+    assert oracle.e4m3_decode(0x08) == 2.0 ** -6    # smallest normal
+    assert oracle.e4m3_decode(0x01) == 2.0 ** -9    # smallest subnormal
+    assert oracle.e4m3_decode(0x07) == 7 * 2.0 ** -9
+    assert oracle.e4m3_decode(0x3C) == 1.5
+    assert math.isnan(oracle.e4m3_decode(0x7F)) and math.isnan(oracle.e4m3_decode(0xFF))
+
+
+def test_e4m3_encode_inverts_decode_and_rounds_to_even():
+    for c in range(256):
+        v = oracle.e4m3_decode(c)
+        if math.isnan(v):
+            continue
+        assert oracle.e4m3_encode(v) == c, hex(c)
+    # midpoints go to the even code: 1.0 (0x38) .. 1.125 (0x39) -> 0x38;
+    # 1.125 .. 1.25 (0x3A) -> 0x3A
+    assert oracle.e4m3_encode(1.0625) == 0x38
+    assert oracle.e4m3_encode(1.1875) == 0x3A
+    assert oracle.e4m3_encode(1.07) == 0x39
+    assert oracle.e4m3_encode(1000.0) == 0x7E and oracle.e4m3_encode(-1e30) == 0xFE  # saturate
+    assert oracle.e4m3_encode(2.0 ** -11) == 0x00                                    # tie to 0
+    assert oracle.e4m3_encode(-0.0) == 0x80
+
+
+def test_fp8_attention_equals_attention_on_dequantised_values():
+    """Dequantised fp8 pools, fed to the (pinned) fp64 attention as exact
+    values, give the same answer as the fp8 path."""
+    rng = np.random.default_rng(77)
+    shape = wl.random_small_shape(rng, max_reqs=4, max_len=60, Hq=8, Hkv=2)
+    nb, Hkv, bs, D = shape.num_blocks, 2, shape.block_size, shape.head_dim
+    k8 = rng.integers(0, 256, size=(nb, Hkv, bs, D), dtype=np.uint8)
+    v8 = rng.integers(0, 256, size=(nb, Hkv, bs, D), dtype=np.uint8)
+    k8[(k8 & 0x7F) == 0x7F] = 0x30                        # no NaN codes
+    v8[(v8 & 0x7F) == 0x7F] = 0x30
+    ks = np.array([0.05, 0.02], np.float32)
+    vs = np.array([0.01, 0.04], np.float32)
+    q = _bits(rng.standard_normal((shape.num_q_tokens, 8, D)).astype(np.float32))
+    bt = wl.block_placement(shape, 5)
+    got = oracle.paged_attention_fp8(q, k8, v8, ks, vs, bt, shape.seq_lens,
+                                     shape.query_start_loc, 0.09)
+    lut = np.array([oracle.e4m3_decode(c) for c in range(256)])
+    kd = lut[k8] * ks.astype(np.float64)[None, :, None, None]
+    vd = lut[v8] * vs.astype(np.float64)[None, :, None, None]
+    lk = [np.stack([kd[bt[r, j // bs], :, j % bs] for j in range(L)]) for r, L in enumerate(shape.seq_lens)]
+    lv = [np.stack([vd[bt[r, j // bs], :, j % bs] for j in range(L)]) for r, L in enumerate(shape.seq_lens)]
+    want = _dense_reference(_vals(q), lk, lv, shape.seq_lens, shape.query_start_loc, 0.09, 8)
+    np.testing.assert_allclose(got, want, rtol=0, atol=1e-12)
+
+
+def test_fp8_append_codes():
+    rng = np.random.default_rng(78)
+    kn = _bits(rng.standard_normal((5, 2, 8)).astype(np.float32) * 3)
+    vn = _bits(rng.standard_normal((5, 2, 8)).astype(np.float32))
+    ks, vs = np.array([0.5, 0.01], np.float32), np.array([2.0, 0.125], np.float32)
+    pool = np.zeros((4, 2, 4, 8), np.uint8)
+    slots = np.array([0, 5, -1, 14, 9], np.int64)
+    kp, vp = oracle.append_fp8(kn, vn, slots, pool, pool, ks, vs)
+    kv, vv = _vals(kn).astype(np.float32), _vals(vn).astype(np.float32)
+    for t, s in enumerate(slots):
+        if s < 0:
+            continue
+        for h in range(2):
+            for d in range(8):
+                assert kp[s // 4, h, s % 4, d] == oracle.e4m3_encode(np.float32(kv[t, h, d]) / ks[h])
+                assert vp[s // 4, h, s % 4, d] == oracle.e4m3_encode(np.float32(vv[t, h, d]) / vs[h])
+    assert kp[0, :, 2].sum() == 0    # untouched slots stay zero
+
+
+def test_e4m3_encode_matches_torch_in_range():
+    """Within +-448 the encoder agrees with torch's float8_e4m3fn cast (an
+    independent round-to-nearest-even implementation)."""
+    rng = np.random.default_rng(79)
+    x = np.concatenate([rng.standard_normal(4000).astype(np.float32) * 50,
+                        np.linspace(-448, 448, 2001, dtype=np.float32),
+                        (np.arange(256) * 2.0 ** -12).astype(np.float32)])
+    t = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    o = np.array([oracle.e4m3_encode(v) for v in x], np.uint8)
+    assert np.array_equal(t, o)
