@@ -42,7 +42,8 @@ from paged_kv_cache_195_gb300 import workloads as wl  # noqa: E402
 METRIC = "paged-attention step: KV GB/s and % of GB300 HBM peak; attended tokens/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-DECODE_SRC = os.path.join(ROOT, "paged_kv_cache_195_gb300", "csrc", "pkv_decode.cu")
+DECODE_SRCS = [os.path.join(ROOT, "paged_kv_cache_195_gb300", "csrc", f)
+               for f in ("pkv_decode_kernel.cuh", "pkv_decode.cu")]
 
 
 def dist_env():
@@ -61,15 +62,24 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def committed_traffic():
+def decode_source_sha() -> str:
+    h = hashlib.sha256()
+    for path in DECODE_SRCS:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(config: str, kv: str):
     """Per-launch DRAM bytes of the decode kernel from the committed ncu
-    summary, if it was taken on the current kernel source (else None)."""
-    path = os.path.join(ROOT, "profiles", "decode_kernel_qwen_decode.md")
+    summary of this workload, if it was taken on the current kernel source
+    (else None)."""
+    path = os.path.join(ROOT, "profiles", f"decode_kernel_{config}_{kv}.md")
     try:
         text = open(path).read()
     except OSError:
         return None
-    src_sha = hashlib.sha256(open(DECODE_SRC, "rb").read()).hexdigest()[:16]
+    src_sha = decode_source_sha()
     m_sha = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
     m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
     if m_sha and m_tr and m_sha.group(1) == src_sha:
@@ -170,8 +180,9 @@ class GraphEvents:
 # our arm
 # ---------------------------------------------------------------------------
 
-def workload_config(shape, ws_n):
+def workload_config(shape, ws_n, kv="bf16"):
     """The `config` object of the JSON line (both arms)."""
+    kvb = 1 if kv == "fp8" else 2
     return {
         "workload": f"{shape.name} x{shape.layers} layers",
         "num_reqs": shape.num_reqs, "context": int(shape.seq_lens[0]),
@@ -179,8 +190,10 @@ def workload_config(shape, ws_n):
         "num_q_heads": shape.num_q_heads, "num_kv_heads": shape.num_kv_heads,
         "head_dim": shape.head_dim, "block_size": shape.block_size,
         "pool_blocks_per_layer": shape.num_blocks, "parallelism": f"replicas x{ws_n}",
+        "kv_cache_dtype": "e4m3 (per-KV-head scales)" if kv == "fp8" else "bf16",
         "l2": f"inputs exceed L2: {shape.layers} distinct pools, "
-              f"{2 * shape.layers * shape.num_blocks * shape.num_kv_heads * 4096 / 1e9:.2f} GB per step",
+              f"{2 * shape.layers * shape.num_blocks * shape.num_kv_heads * 2048 * kvb / 1e9:.2f}"
+              " GB per step",
         "launch": f"CUDA graph of {shape.layers} x (append + attention)",
     }
 
@@ -198,12 +211,9 @@ def aggregate_over_ranks(ms_local: float, units_local: float, device=None):
     return float(t.item()), float(u.item())
 
 
-def build_layers(shape, device, rank):
-    layers = []
-    for layer in range(shape.layers):
-        inp = wl.make_step(shape, device=device, layer=layer + 1000 * rank)
-        layers.append(inp)
-    return layers
+def build_layers(shape, device, rank, kv="bf16"):
+    make = wl.make_fp8_step if kv == "fp8" else wl.make_step
+    return [make(shape, device=device, layer=layer + 1000 * rank) for layer in range(shape.layers)]
 
 
 def run_ours(args):
@@ -224,7 +234,9 @@ def run_ours(args):
     pkv.load_library()
 
     shape = wl.CONFIGS[args.config]()
-    layers = build_layers(shape, device, rank)
+    fp8 = args.kv == "fp8"
+    kvb = 1 if fp8 else 2
+    layers = build_layers(shape, device, rank, args.kv)
     L0 = layers[0]
     dims = pkv.make_dims(tuple(L0.q.shape), tuple(L0.k_pool.shape), shape.num_reqs,
                          shape.max_blocks_per_req)
@@ -232,8 +244,9 @@ def run_ours(args):
     pkv.pkv_workspace_init(ws, dims)
     outs = [torch.empty_like(x.q) for x in layers]
 
-    att = rl.attention_bytes(shape.seq_lens, shape.q_lens, shape.num_q_heads, shape.num_kv_heads)
-    app = rl.append_bytes(shape.num_q_tokens, shape.num_kv_heads)
+    att = rl.attention_bytes(shape.seq_lens, shape.q_lens, shape.num_q_heads, shape.num_kv_heads,
+                             kv_dtype_bytes=kvb)
+    app = rl.append_bytes(shape.num_q_tokens, shape.num_kv_heads, kv_dtype_bytes=kvb)
     bytes_per_layer = att["total"] + app
     bytes_per_step = bytes_per_layer * shape.layers
     tokens_per_step = rl.attended_tokens(shape.seq_lens, shape.q_lens) * shape.layers
@@ -244,11 +257,20 @@ def run_ours(args):
     def step(events=False):
         s = torch.cuda.current_stream(device)
         for li, x in enumerate(layers):
-            pkv.pkv_append(x.k_new, x.v_new, x.slot_mapping, x.k_pool, x.v_pool)
+            if fp8:
+                pkv.pkv_append_fp8(x.k_new, x.v_new, x.slot_mapping, x.k_pool, x.v_pool,
+                                   x.k_scale, x.v_scale)
+            else:
+                pkv.pkv_append(x.k_new, x.v_new, x.slot_mapping, x.k_pool, x.v_pool)
             if events:
                 gev.record(2 * li, s)
-            pkv.pkv_attention(x.q, x.k_pool, x.v_pool, x.block_tables, x.seq_lens,
-                              x.query_start_loc, x.scale, out=outs[li], workspace=ws)
+            if fp8:
+                pkv.pkv_attention_fp8kv(x.q, x.k_pool, x.v_pool, x.k_scale, x.v_scale,
+                                        x.block_tables, x.seq_lens, x.query_start_loc, x.scale,
+                                        out=outs[li], workspace=ws)
+            else:
+                pkv.pkv_attention(x.q, x.k_pool, x.v_pool, x.block_tables, x.seq_lens,
+                                  x.query_start_loc, x.scale, out=outs[li], workspace=ws)
             if events:
                 gev.record(2 * li + 1, s)
 
@@ -329,21 +351,26 @@ def run_ours(args):
     peak, peak_src = measured_peak()
     value = bytes_per_step * ws_n / (ms_step * 1e-3) / 1e9
     achieved = att["total"] / (kernel_ms * 1e-3) / 1e9
-    traffic = committed_traffic()
+    traffic = committed_traffic(args.config, args.kv)
     cpu = cpu_baseline(shape, layers, args) if (rank == 0 and ws_n == 1 and not args.no_cpu) else None
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws_n,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded N(0,1) bf16 K/V/q, shuffled block placement; no weights)",
-        "config": workload_config(shape, ws_n),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 KV, bf16 q/out, f32 math" if fp8 else "bf16",
+        "data": ("synthetic (seeded uniform e4m3 codes, N(0,1) bf16 q/new K/V, shuffled block "
+                 "placement; no weights)" if fp8 else
+                 "synthetic (seeded N(0,1) bf16 K/V/q, shuffled block placement; no weights)"),
+        "config": workload_config(shape, ws_n, args.kv),
         "attended_tokens_per_s": round(tokens_per_step * ws_n / (ms_step * 1e-3), 1),
         "us_per_layer": round(ms_step * 1e3 / shape.layers, 3),
         "frac_of_nominal_8tbs": round(value / ws_n / NOMINAL_HBM_GBS, 4),
         "roofline": {
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "traffic": traffic,
-            "kernel": "pkv::decode_kernel<6>", "algorithmic_bytes_per_launch": att["total"],
+            "kernel": f"pkv::decode_kernel<{shape.num_q_heads // shape.num_kv_heads}, "
+                      f"{'KvE4m3' if fp8 else 'KvBf16'}>",
+            "algorithmic_bytes_per_launch": att["total"],
             "avg_launch_us": round(kernel_ms * 1e3, 3), "peak_source": peak_src,
             "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
         },
@@ -370,16 +397,26 @@ def _oracle_sample(shape, inp_host, n_reqs):
     qsl = inp_host["qsl"]
     sub_qsl = qsl[:n_reqs + 1]
     t = int(sub_qsl[-1])
-    return oracle.paged_attention(inp_host["q"][:t], inp_host["k_pool"], inp_host["v_pool"],
-                                  inp_host["block_tables"][:n_reqs], inp_host["seq_lens"][:n_reqs],
-                                  sub_qsl, inp_host["scale"])
+    h = inp_host
+    if "k_scale" in h:
+        return oracle.paged_attention_fp8(h["q"][:t], h["k_pool"], h["v_pool"], h["k_scale"],
+                                          h["v_scale"], h["block_tables"][:n_reqs],
+                                          h["seq_lens"][:n_reqs], sub_qsl, h["scale"])
+    return oracle.paged_attention(h["q"][:t], h["k_pool"], h["v_pool"],
+                                  h["block_tables"][:n_reqs], h["seq_lens"][:n_reqs],
+                                  sub_qsl, h["scale"])
 
 
 def _host_layer(inp):
-    return dict(q=wl.bf16_bits(inp.q), k_pool=wl.bf16_bits(inp.k_pool),
-                v_pool=wl.bf16_bits(inp.v_pool), block_tables=inp.block_tables.cpu().numpy(),
-                seq_lens=inp.seq_lens.cpu().numpy(), qsl=inp.query_start_loc.cpu().numpy(),
-                scale=inp.scale)
+    fp8 = inp.k_pool.dtype == torch.uint8
+    pool = (lambda t: t.cpu().numpy()) if fp8 else wl.bf16_bits
+    h = dict(q=wl.bf16_bits(inp.q), k_pool=pool(inp.k_pool), v_pool=pool(inp.v_pool),
+             block_tables=inp.block_tables.cpu().numpy(), seq_lens=inp.seq_lens.cpu().numpy(),
+             qsl=inp.query_start_loc.cpu().numpy(), scale=inp.scale)
+    if fp8:
+        h["k_scale"] = inp.k_scale.cpu().numpy()
+        h["v_scale"] = inp.v_scale.cpu().numpy()
+    return h
 
 
 def cpu_baseline(shape, layers, args, budget_s=10.0):
@@ -388,7 +425,8 @@ def cpu_baseline(shape, layers, args, budget_s=10.0):
     host = [_host_layer(x) for x in layers[:4]]
     done_bytes, t_total, n_calls = 0, 0.0, 0
     per_req = rl.attention_bytes(shape.seq_lens[:1], shape.q_lens[:1], shape.num_q_heads,
-                                 shape.num_kv_heads)["total"]
+                                 shape.num_kv_heads,
+                                 kv_dtype_bytes=1 if args.kv == "fp8" else 2)["total"]
     t0 = time.perf_counter()
     while t_total < budget_s:
         h = host[n_calls % len(host)]
@@ -413,9 +451,11 @@ def run_reference(args):
     shape = wl.CONFIGS[args.config]()
     # inputs generated on the host (same seeded recipe as the GPU arm)
     n_layers = min(shape.layers, 2)
-    host = [_host_layer(wl.make_step(shape, device="cpu", layer=li)) for li in range(n_layers)]
+    make = wl.make_fp8_step if args.kv == "fp8" else wl.make_step
+    host = [_host_layer(make(shape, device="cpu", layer=li)) for li in range(n_layers)]
     per_req = rl.attention_bytes(shape.seq_lens[:1], shape.q_lens[:1], shape.num_q_heads,
-                                 shape.num_kv_heads)["total"]
+                                 shape.num_kv_heads,
+                                 kv_dtype_bytes=1 if args.kv == "fp8" else 2)["total"]
     # size each step so that warm-up + timed steps fit in about a minute
     t1 = time.perf_counter()
     _oracle_sample(shape, host[0], 1)
@@ -434,7 +474,7 @@ def run_reference(args):
         "n_gpus": ws_n, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt * 1e3 / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(shape, ws_n),
+        "config": workload_config(shape, ws_n, args.kv),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.max_threads(),
                          "kind": "oracle",
                          "sample": f"each step: attention of {n_reqs} of {shape.num_reqs} "
@@ -452,6 +492,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="qwen_decode", choices=sorted(wl.CONFIGS))
+    ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
+                    help="KV-cache element type (fp8: e4m3 with per-KV-head scales)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -146,6 +146,14 @@ int pkv_workspace_init(void *workspace, size_t workspace_bytes,
  * once with pkv_workspace_init; NULL makes the library use an internal
  * per-device buffer (allocated on first use: not capturable in a CUDA graph,
  * and not safe for concurrent calls on different streams).
+ * Launch overlap: unless the environment sets PKV_PDL=0, the kernels are
+ * launched with programmatic dependent launch and may start while the
+ * kernel before them on the stream is still running.  They wait for it
+ * before touching q, the pools, block_tables, out or the workspace, but read
+ * seq_lens and query_start_loc before that wait (PKV_EARLY_PLAN=0 moves
+ * those reads after it).  So the kernel issued immediately before this call
+ * must not write seq_lens or query_start_loc; pkv_append, which writes only
+ * pool slots, and host-to-device copies may.
  * Source: The Serving Playbook, "The block table lives in the hottest kernel
  * in the system" (gather through the table, partial softmax per piece of the
  * cache, rescaling pass), "Kernel fusion, briefly" (Flash-Decoding splits the
@@ -157,6 +165,38 @@ int pkv_attention(const void *q, const void *k_pool, const void *v_pool,
                   const int32_t *query_start_loc, float scale, void *out,
                   const pkv_dims *dims, void *workspace, size_t workspace_bytes,
                   cudaStream_t stream);
+
+/*
+ * KV append into e4m3 pools (8-bit float: 1 sign, 4 exponent bits with bias
+ * 7, 3 mantissa bits, largest finite magnitude 448).  Same slots, padding and
+ * bounds rules as pkv_append; k_pool / v_pool are [num_blocks, Hkv, bs, 128]
+ * bytes.  Element x of head h becomes the code nearest to x / k_scale[h]
+ * (v_scale[h] for V), the quotient taken in fp32 with round to nearest even,
+ * ties to the even code, magnitudes beyond 448 saturated to +-448.  k_scale /
+ * v_scale: [num_kv_heads] positive finite fp32 in device memory (per layer:
+ * pass that layer's scales).  k_new / v_new are bf16 as in pkv_append.
+ * Source: The Serving Playbook, "Quantized serving" (an fp8 KV cache halves
+ * the bytes decode reads); What Actually Runs the Model, "The KV cache".
+ */
+int pkv_append_fp8(const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                   void *k_pool, void *v_pool, const float *k_scale, const float *v_scale,
+                   int32_t num_new_tokens, const pkv_dims *dims, cudaStream_t stream);
+
+/*
+ * pkv_attention over e4m3 pools written by pkv_append_fp8: the key of
+ * position j, KV head kh, is decode(code) * k_scale[kh], the value
+ * decode(code) * v_scale[kh]; everything else (q, out, lengths, tables,
+ * workspace, errors) as in pkv_attention.  All rows, prefill chunks
+ * included, run in the split-context decode kernel (the tensor-core prefill
+ * kernel takes bf16 pools only).
+ * Source: as pkv_attention; The Serving Playbook, "Quantized serving".
+ */
+int pkv_attention_fp8kv(const void *q, const void *k_pool, const void *v_pool,
+                        const float *k_scale, const float *v_scale,
+                        const int32_t *block_tables, const int32_t *seq_lens,
+                        const int32_t *query_start_loc, float scale, void *out,
+                        const pkv_dims *dims, void *workspace, size_t workspace_bytes,
+                        cudaStream_t stream);
 
 /* Size of the static scratch array behind pkv_attention_noalloc (4 MiB). */
 #define PKV_NOALLOC_SCRATCH_BYTES (4 * 1024 * 1024)

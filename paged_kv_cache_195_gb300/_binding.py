@@ -27,7 +27,8 @@ PKV_ERR_TIMEOUT = -6
 
 EXPORTED = ("pkv_append", "pkv_attention", "pkv_attention_workspace_size",
             "pkv_workspace_init", "pkv_last_error", "pkv_get_device_error",
-            "pkv_attention_noalloc", "pkv_copy_blocks")
+            "pkv_attention_noalloc", "pkv_copy_blocks", "pkv_append_fp8",
+            "pkv_attention_fp8kv")
 
 
 class PagedKVError(RuntimeError):
@@ -76,6 +77,11 @@ def load_library(path: str = LIB_PATH):
         lib.pkv_attention_noalloc.restype = ctypes.c_int
         lib.pkv_copy_blocks.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, dp, vp]
         lib.pkv_copy_blocks.restype = ctypes.c_int
+        lib.pkv_append_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, dp, vp]
+        lib.pkv_append_fp8.restype = ctypes.c_int
+        lib.pkv_attention_fp8kv.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, dp,
+                                            vp, sz, vp]
+        lib.pkv_attention_fp8kv.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -190,6 +196,76 @@ def pkv_attention(q, k_pool, v_pool, block_tables, seq_lens, query_start_loc, sc
     _check(load_library().pkv_attention(
         ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k_pool.data_ptr()),
         ctypes.c_void_p(v_pool.data_ptr()), ctypes.c_void_p(block_tables.data_ptr()),
+        ctypes.c_void_p(seq_lens.data_ptr()), ctypes.c_void_p(query_start_loc.data_ptr()),
+        ctypes.c_float(scale), ctypes.c_void_p(out.data_ptr()), ctypes.byref(dims),
+        ctypes.c_void_p(ws_ptr), ws_bytes, ctypes.c_void_p(_stream(stream, q.device))))
+    return out
+
+
+def _need_scales(k_scale, v_scale, Hkv: int):
+    for t, name in ((k_scale, "k_scale"), (v_scale, "v_scale")):
+        _need(t, name, torch.float32, 1)
+        if t.shape[0] != Hkv:
+            raise ValueError(f"{name} must have num_kv_heads = {Hkv} entries")
+
+
+def pkv_append_fp8(k_new, v_new, slot_mapping, k_pool, v_pool, k_scale, v_scale, stream=None):
+    """Quantise k_new/v_new [T, Hkv, D] bf16 into e4m3 pools (uint8
+    [blocks, Hkv, 16, D]) at slot_mapping [T] int64, with the per-KV-head
+    scales k_scale / v_scale [Hkv] fp32: code = e4m3(x / scale)."""
+    _need(k_new, "k_new", torch.bfloat16, 3)
+    _need(v_new, "v_new", torch.bfloat16, 3)
+    _need(slot_mapping, "slot_mapping", torch.int64, 1)
+    _need(k_pool, "k_pool", torch.uint8, 4)
+    _need(v_pool, "v_pool", torch.uint8, 4)
+    T = k_new.shape[0]
+    if v_new.shape != k_new.shape or slot_mapping.shape[0] != T:
+        raise ValueError("k_new, v_new and slot_mapping disagree on the token count")
+    if v_pool.shape != k_pool.shape or k_pool.shape[1] != k_new.shape[1] or \
+            k_pool.shape[3] != k_new.shape[2]:
+        raise ValueError("pool shape does not match the new rows")
+    nb, Hkv, bs, D = k_pool.shape
+    _need_scales(k_scale, v_scale, Hkv)
+    dims = Dims(0, 0, Hkv, Hkv, D, bs, nb, 0)
+    _check(load_library().pkv_append_fp8(
+        ctypes.c_void_p(k_new.data_ptr()), ctypes.c_void_p(v_new.data_ptr()),
+        ctypes.c_void_p(slot_mapping.data_ptr()), ctypes.c_void_p(k_pool.data_ptr()),
+        ctypes.c_void_p(v_pool.data_ptr()), ctypes.c_void_p(k_scale.data_ptr()),
+        ctypes.c_void_p(v_scale.data_ptr()), T, ctypes.byref(dims),
+        ctypes.c_void_p(_stream(stream, k_pool.device))))
+
+
+def pkv_attention_fp8kv(q, k_pool, v_pool, k_scale, v_scale, block_tables, seq_lens,
+                        query_start_loc, scale, out=None, workspace: Workspace | None = None,
+                        stream=None):
+    """pkv_attention over e4m3 pools (uint8) dequantised by the per-KV-head
+    scales k_scale / v_scale [Hkv] fp32; returns out [Tq, Hq, D] bf16."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_pool, "k_pool", torch.uint8, 4)
+    _need(v_pool, "v_pool", torch.uint8, 4)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    _need(query_start_loc, "query_start_loc", torch.int32, 1)
+    R = seq_lens.shape[0]
+    if query_start_loc.shape[0] != R + 1 or block_tables.shape[0] != R:
+        raise ValueError("seq_lens, query_start_loc and block_tables disagree on num_reqs")
+    if v_pool.shape != k_pool.shape or k_pool.shape[3] != q.shape[2]:
+        raise ValueError("pool / q shape mismatch")
+    _need_scales(k_scale, v_scale, k_pool.shape[1])
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need(out, "out", torch.bfloat16, 3)
+        if out.shape != q.shape:
+            raise ValueError("out must have q's shape")
+    dims = make_dims(tuple(q.shape), tuple(k_pool.shape), R, block_tables.shape[1])
+    if workspace is not None and workspace.counter_dims != (dims.num_q_tokens, dims.num_kv_heads):
+        pkv_workspace_init(workspace, dims, stream)
+    ws_ptr, ws_bytes = (None, 0) if workspace is None else (workspace.ptr, workspace.nbytes)
+    _check(load_library().pkv_attention_fp8kv(
+        ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k_pool.data_ptr()),
+        ctypes.c_void_p(v_pool.data_ptr()), ctypes.c_void_p(k_scale.data_ptr()),
+        ctypes.c_void_p(v_scale.data_ptr()), ctypes.c_void_p(block_tables.data_ptr()),
         ctypes.c_void_p(seq_lens.data_ptr()), ctypes.c_void_p(query_start_loc.data_ptr()),
         ctypes.c_float(scale), ctypes.c_void_p(out.data_ptr()), ctypes.byref(dims),
         ctypes.c_void_p(ws_ptr), ws_bytes, ctypes.c_void_p(_stream(stream, q.device))))

@@ -195,7 +195,7 @@ int pkv_append(const void* k_new, const void* v_new, const int64_t* slot_mapping
     return fail(PKV_ERR_INVALID, "bf16 buffers must be 16-byte aligned");
   DeviceState* st = device_state();
   if (!st) return PKV_ERR_CUDA;
-  pkv::AppendParams p;
+  pkv::AppendParams p{};
   p.k_new = static_cast<const __nv_bfloat16*>(k_new);
   p.v_new = static_cast<const __nv_bfloat16*>(v_new);
   p.slot_mapping = slot_mapping;
@@ -208,6 +208,38 @@ int pkv_append(const void* k_new, const void* v_new, const int64_t* slot_mapping
   p.pdl = env_int("PKV_PDL", 1) != 0;
   cudaError_t e = pkv::launch_append(p, stream);
   if (e != cudaSuccess) return cuda_fail(e, "append launch");
+  return PKV_OK;
+}
+
+int pkv_append_fp8(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                   void* k_pool, void* v_pool, const float* k_scale, const float* v_scale,
+                   int32_t num_new_tokens, const pkv_dims* dims, cudaStream_t stream) {
+  g_last_error[0] = '\0';
+  int rc = check_dims(dims, false);
+  if (rc != PKV_OK) return rc;
+  if (num_new_tokens < 0) return fail(PKV_ERR_INVALID, "num_new_tokens < 0");
+  if (num_new_tokens == 0) return PKV_OK;
+  if (!k_new || !v_new || !slot_mapping || !k_pool || !v_pool || !k_scale || !v_scale)
+    return fail(PKV_ERR_INVALID, "NULL pointer argument");
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pool) || !aligned16(v_pool))
+    return fail(PKV_ERR_INVALID, "k/v buffers and pools must be 16-byte aligned");
+  DeviceState* st = device_state();
+  if (!st) return PKV_ERR_CUDA;
+  pkv::AppendFp8Params p{};
+  p.k_new = static_cast<const __nv_bfloat16*>(k_new);
+  p.v_new = static_cast<const __nv_bfloat16*>(v_new);
+  p.slot_mapping = slot_mapping;
+  p.k_pool = static_cast<uint8_t*>(k_pool);
+  p.v_pool = static_cast<uint8_t*>(v_pool);
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.err = st->err;
+  p.num_tokens = num_new_tokens;
+  p.num_kv_heads = dims->num_kv_heads;
+  p.num_blocks = dims->num_blocks;
+  p.pdl = env_int("PKV_PDL", 1) != 0;
+  cudaError_t e = pkv::launch_append_fp8(p, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "append_fp8 launch");
   return PKV_OK;
 }
 
@@ -226,7 +258,7 @@ int pkv_copy_blocks(const void* k_src, const void* v_src, void* k_dst, void* v_d
     return fail(PKV_ERR_INVALID, "pools must be 16-byte aligned");
   DeviceState* st = device_state();
   if (!st) return PKV_ERR_CUDA;
-  pkv::CopyParams p;
+  pkv::CopyParams p{};
   p.k_src = static_cast<const __nv_bfloat16*>(k_src);
   p.v_src = static_cast<const __nv_bfloat16*>(v_src);
   p.k_dst = static_cast<__nv_bfloat16*>(k_dst);
@@ -265,18 +297,24 @@ int pkv_workspace_init(void* workspace, size_t workspace_bytes, const pkv_dims* 
   return PKV_OK;
 }
 
-int pkv_attention(const void* q, const void* k_pool, const void* v_pool,
-                  const int32_t* block_tables, const int32_t* seq_lens,
-                  const int32_t* query_start_loc, float scale, void* out, const pkv_dims* dims,
-                  void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Both attention entry points: bf16 pools (k_scale == nullptr) or e4m3 pools.
+int attention_impl(const void* q, const void* k_pool, const void* v_pool, const float* k_scale,
+                   const float* v_scale, const int32_t* block_tables, const int32_t* seq_lens,
+                   const int32_t* query_start_loc, float scale, void* out, const pkv_dims* dims,
+                   void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   g_last_error[0] = '\0';
+  const bool fp8 = k_scale != nullptr;
   int rc = check_dims(dims, true);
   if (rc != PKV_OK) return rc;
   if (dims->num_reqs == 0 || dims->num_q_tokens == 0) return PKV_OK;
   if (!q || !k_pool || !v_pool || !block_tables || !seq_lens || !query_start_loc || !out)
     return fail(PKV_ERR_INVALID, "NULL pointer argument");
   if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
-    return fail(PKV_ERR_INVALID, "bf16 buffers must be 16-byte aligned");
+    return fail(PKV_ERR_INVALID, "q, out and the pools must be 16-byte aligned");
   if (!(scale == scale) || scale == 0.f) return fail(PKV_ERR_INVALID, "scale must be finite, non-zero");
   DeviceState* st = device_state();
   if (!st) return PKV_ERR_CUDA;
@@ -308,10 +346,13 @@ int pkv_attention(const void* q, const void* k_pool, const void* v_pool,
     return fail(PKV_ERR_INVALID, "workspace must be 256-byte aligned");
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  pkv::DecodeParams p;
+  pkv::DecodeParams p{};
   p.q = static_cast<const __nv_bfloat16*>(q);
-  p.k_pool = static_cast<const __nv_bfloat16*>(k_pool);
-  p.v_pool = static_cast<const __nv_bfloat16*>(v_pool);
+  p.k_pool = static_cast<const uint8_t*>(k_pool);
+  p.v_pool = static_cast<const uint8_t*>(v_pool);
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.kv_fp8 = fp8 ? 1 : 0;
   p.block_tables = block_tables;
   p.seq_lens = seq_lens;
   p.qsl = query_start_loc;
@@ -334,13 +375,18 @@ int pkv_attention(const void* q, const void* k_pool, const void* v_pool,
   // Launch it only when the step can hold such a request next to one query
   // for every other request; otherwise the decode kernel serves every row
   // (it is correct for any q_r, the prefill kernel is only faster).
+  // e4m3 pools: every row runs in the decode kernel.
   const bool run_prefill =
-      (long long)dims->num_q_tokens - dims->num_reqs + 1 >= (long long)prefill_min_q;
+      !fp8 && (long long)dims->num_q_tokens - dims->num_reqs + 1 >= (long long)prefill_min_q;
   p.prefill_min_q = run_prefill ? prefill_min_q : 0x7fffffff;
   p.num_slots = w.num_slots;
   p.pdl = env_int("PKV_PDL", 1) != 0;
   p.min_chunk = env_int("PKV_MIN_CHUNK", 4);
   if (p.min_chunk < 1) p.min_chunk = 1;
+  p.align = env_int("PKV_ALIGN", 1) != 0;
+  p.align_slack = env_int("PKV_ALIGN_SLACK", 32);
+  p.prefetch = env_int("PKV_PREFETCH", 1) != 0;
+  p.early_plan = p.pdl && env_int("PKV_EARLY_PLAN", 1) != 0;
   const int group = dims->num_q_heads / dims->num_kv_heads;
   int grid = pkv::decode_grid(st->sm_count, group);
   const int grid_env = env_int("PKV_DECODE_GRID", 0);  // tuning override, bounded by the slots
@@ -348,7 +394,7 @@ int pkv_attention(const void* q, const void* k_pool, const void* v_pool,
   cudaError_t e = pkv::launch_decode(p, group, grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   if (run_prefill) {
-    pkv::PrefillLaunch L;
+    pkv::PrefillLaunch L{};
     rc = encode_q_map(&L.qmap, q, dims, group);
     if (rc == PKV_OK) rc = encode_pool_map(&L.kmap, k_pool, dims);
     if (rc == PKV_OK) rc = encode_pool_map(&L.vmap, v_pool, dims);
@@ -372,6 +418,31 @@ int pkv_attention(const void* q, const void* k_pool, const void* v_pool,
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   }
   return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pkv_attention(const void* q, const void* k_pool, const void* v_pool,
+                  const int32_t* block_tables, const int32_t* seq_lens,
+                  const int32_t* query_start_loc, float scale, void* out, const pkv_dims* dims,
+                  void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return attention_impl(q, k_pool, v_pool, nullptr, nullptr, block_tables, seq_lens,
+                        query_start_loc, scale, out, dims, workspace, workspace_bytes, stream);
+}
+
+int pkv_attention_fp8kv(const void* q, const void* k_pool, const void* v_pool,
+                        const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                        const int32_t* seq_lens, const int32_t* query_start_loc, float scale,
+                        void* out, const pkv_dims* dims, void* workspace, size_t workspace_bytes,
+                        cudaStream_t stream) {
+  if (!k_scale || !v_scale) {
+    g_last_error[0] = '\0';
+    return fail(PKV_ERR_INVALID, "k_scale / v_scale is NULL");
+  }
+  return attention_impl(q, k_pool, v_pool, k_scale, v_scale, block_tables, seq_lens,
+                        query_start_loc, scale, out, dims, workspace, workspace_bytes, stream);
 }
 
 int pkv_get_device_error(cudaStream_t stream) {

@@ -35,6 +35,64 @@ __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
   *dst = __ldg(src);
 }
 
+// Quantising append into e4m3 pools (The Serving Playbook, "Quantized
+// serving"): each element becomes the code nearest to x / scale[KV head]
+// (round to nearest even on the fp32 quotient, saturated to +-448).  Same
+// warp layout as the bf16 append; a lane reads 16 bytes and writes 8.
+__global__ void __launch_bounds__(256) append_fp8_kernel(AppendFp8Params p) {
+  grid_dependency_wait();
+  allow_dependent_launch();
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp >= p.num_tokens * p.num_kv_heads) return;
+  const int t = warp / p.num_kv_heads;
+  const int h = warp - t * p.num_kv_heads;
+  const long long slot = p.slot_mapping[t];
+  if (slot < 0) return;  // padding token
+  if (slot >= (long long)p.num_blocks * kBlockSize) {
+    if (lane == 0) record_error(p.err, kErrBounds);
+    return;
+  }
+  const long long blk = slot / kBlockSize;
+  const int off = (int)(slot - blk * kBlockSize);
+  const int half = lane >> 4;  // 0: K, 1: V
+  const int c = lane & 15;     // 8 elements of the 128-element row
+  const float sc = __ldg((half ? p.v_scale : p.k_scale) + h);
+  const uint4 w = __ldg(reinterpret_cast<const uint4*>(half ? p.v_new : p.k_new) +
+                        ((long long)t * p.num_kv_heads + h) * (kHeadDim / 8) + c);
+  const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+  uint32_t code[2] = {0u, 0u};
+  #pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 x = bf16x2_to_float2(in[i]);
+    const float2 y = make_float2(__fdiv_rn(x.x, sc), __fdiv_rn(x.y, sc));
+    const uint32_t two = __nv_cvt_float2_to_fp8x2(y, __NV_SATFINITE, __NV_E4M3);
+    code[i >> 1] |= two << (16 * (i & 1));
+  }
+  uint2* dst = reinterpret_cast<uint2*>(half ? p.v_pool : p.k_pool) +
+               ((blk * p.num_kv_heads + h) * kBlockSize + off) * (kHeadDim / 8) + c;
+  *dst = make_uint2(code[0], code[1]);
+}
+
+cudaError_t launch_append_fp8(const AppendFp8Params& p, cudaStream_t stream) {
+  const long long warps = (long long)p.num_tokens * p.num_kv_heads;
+  if (warps == 0) return cudaSuccess;
+  const int threads = 256;
+  const long long blocks = (warps * 32 + threads - 1) / threads;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(threads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = p.pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, append_fp8_kernel, p);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream) {
   const long long warps = (long long)p.num_tokens * p.num_kv_heads;
   if (warps == 0) return cudaSuccess;

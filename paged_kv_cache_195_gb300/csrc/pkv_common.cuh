@@ -5,6 +5,8 @@
 
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 namespace pkv {
@@ -200,6 +202,14 @@ __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
   r.x = __uint_as_float(w << 16);
   r.y = __uint_as_float(w & 0xffff0000u);
   return r;
+}
+
+// Two e4m3 codes (low byte first) to fp32, exactly: the hardware
+// e4m3x2 -> f16x2 conversion (every e4m3 value is an f16 value), then f16 -> f32.
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two_codes) {
+  const __half2_raw h =
+      __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two_codes, __NV_E4M3);
+  return __half22float2(__half2(h));
 }
 
 // 16-byte shared-memory load (a plain access, so the compiler orders it

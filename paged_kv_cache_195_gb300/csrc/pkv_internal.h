@@ -48,8 +48,11 @@ cudaError_t launch_copy_blocks(const CopyParams& p, int sm_count, cudaStream_t s
 // softmax, and the log-sum-exp merge, in one launch.
 struct DecodeParams {
   const __nv_bfloat16* q;
-  const __nv_bfloat16* k_pool;
-  const __nv_bfloat16* v_pool;
+  const uint8_t* k_pool;   // bf16 or e4m3 elements, [num_blocks, Hkv, 16, 128]
+  const uint8_t* v_pool;
+  const float* k_scale;    // e4m3 pools: [Hkv] dequantisation scales (else unused)
+  const float* v_scale;
+  int kv_fp8;              // 1: the pools hold e4m3 codes
   const int32_t* block_tables;
   const int32_t* seq_lens;
   const int32_t* qsl;
@@ -69,7 +72,9 @@ struct DecodeParams {
   int num_slots;      // partial-piece slots in the workspace (>= 2 * grid)
   int min_chunk;      // smallest per-CTA range, in blocks
   int align;          // snap ranges to row-group boundaries when lengths are uniform
+  int align_slack;    // ... if that lengthens the per-CTA range by at most this many blocks
   int prefetch;       // warm L2 with the block-table rows this CTA will likely read
+  int early_plan;     // plan from seq_lens / query_start_loc before the PDL wait
   int pdl;            // launch with programmatic stream serialization
 };
 
@@ -85,6 +90,25 @@ WorkspaceLayout decode_workspace_layout(int num_q_tokens, int num_kv_heads, int 
 int decode_grid(int sm_count, int group);
 
 cudaError_t launch_decode(const DecodeParams& p, int group, int grid, cudaStream_t stream);
+cudaError_t launch_decode_e4m3(const DecodeParams& p, int group, int grid, cudaStream_t stream);
+
+// Quantising KV append into e4m3 pools.
+struct AppendFp8Params {
+  const __nv_bfloat16* k_new;
+  const __nv_bfloat16* v_new;
+  const int64_t* slot_mapping;
+  uint8_t* k_pool;
+  uint8_t* v_pool;
+  const float* k_scale;  // [Hkv]
+  const float* v_scale;
+  int* err;
+  int num_tokens;
+  int num_kv_heads;
+  int num_blocks;
+  int pdl;
+};
+
+cudaError_t launch_append_fp8(const AppendFp8Params& p, cudaStream_t stream);
 
 // Chunked-prefill attention on tcgen05 tensor cores (requests with
 // q_r >= prefill_min_q).

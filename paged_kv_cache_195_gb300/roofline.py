@@ -5,7 +5,9 @@ The step reads every cached K and V row a query row may see exactly once per
 it reads q and writes out once.  KV bytes per token and layer are
 2 (K and V) x Hkv x D x 2 bytes -- the per-token, per-layer term of the
 KV-cache size formula (What Actually Runs the Model, "The KV cache").  Block
-tables and lengths are not counted (4 bytes per 16 tokens).
+tables and lengths are not counted (4 bytes per 16 tokens).  An e4m3 pool
+stores one byte per element (The Serving Playbook, "Quantized serving"); q,
+out and the appended rows stay bf16.
 """
 from __future__ import annotations
 
@@ -22,7 +24,8 @@ def kv_cache_bytes(layers, kv_heads, head_dim, dtype_bytes, seq_len, batch) -> i
     return 2 * layers * kv_heads * head_dim * dtype_bytes * seq_len * batch
 
 
-def attention_bytes(seq_lens, q_lens, num_q_heads, num_kv_heads, head_dim=128) -> dict:
+def attention_bytes(seq_lens, q_lens, num_q_heads, num_kv_heads, head_dim=128,
+                    kv_dtype_bytes: int = BF16) -> dict:
     """Algorithmic HBM bytes of one attention call.
 
     Decode rows (q_r = 1) read their L_r keys; a prefill chunk reads its L_r
@@ -31,14 +34,14 @@ def attention_bytes(seq_lens, q_lens, num_q_heads, num_kv_heads, head_dim=128) -
     seq_lens = np.asarray(seq_lens, np.int64)
     q_lens = np.asarray(q_lens, np.int64)
     active = q_lens > 0
-    kv = int(seq_lens[active].sum()) * kv_bytes_per_token(num_kv_heads, head_dim)
+    kv = int(seq_lens[active].sum()) * kv_bytes_per_token(num_kv_heads, head_dim, kv_dtype_bytes)
     qo = int(q_lens.sum()) * num_q_heads * head_dim * BF16 * 2
     return {"kv": kv, "q_out": qo, "total": kv + qo}
 
 
-def append_bytes(num_tokens, num_kv_heads, head_dim=128) -> int:
-    """Read k_new/v_new and write them into the pool."""
-    return 2 * 2 * num_tokens * num_kv_heads * head_dim * BF16
+def append_bytes(num_tokens, num_kv_heads, head_dim=128, kv_dtype_bytes: int = BF16) -> int:
+    """Read k_new/v_new (bf16) and write them into the pool (bf16 or e4m3)."""
+    return 2 * num_tokens * num_kv_heads * head_dim * (BF16 + kv_dtype_bytes)
 
 
 def attention_flops(seq_lens, q_lens, num_q_heads, head_dim=128) -> int:

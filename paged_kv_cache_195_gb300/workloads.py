@@ -231,6 +231,72 @@ def make_step(shape: StepShape, device="cpu", layer: int = 0,
         scale=1.0 / math.sqrt(D))
 
 
+@dataclasses.dataclass
+class Fp8StepInputs:
+    """A step over e4m3 pools: the bf16 fields of ``StepInputs`` except the
+    pools, which hold uint8 codes, plus the per-KV-head scales."""
+    shape: StepShape
+    q: torch.Tensor
+    k_new: torch.Tensor
+    v_new: torch.Tensor
+    slot_mapping: torch.Tensor
+    k_pool: torch.Tensor   # uint8 [num_blocks, Hkv, bs, D]
+    v_pool: torch.Tensor
+    k_scale: torch.Tensor  # float32 [Hkv]
+    v_scale: torch.Tensor
+    block_tables: torch.Tensor
+    seq_lens: torch.Tensor
+    query_start_loc: torch.Tensor
+    scale: float
+
+
+E4M3_NAN = 0x7F  # the positive NaN code (exponent and mantissa all ones)
+
+
+def make_fp8_step(shape: StepShape, device="cpu", layer: int = 0,
+                  poison: bool = False) -> Fp8StepInputs:
+    """Seeded inputs of one layer of one step with e4m3 pools.
+
+    Pool codes are drawn uniformly from the 254 non-NaN codes (they are
+    inputs: nothing here encodes a value); per-KV-head scales are drawn from
+    [0.003, 0.0045], so a stored value is at most 448 * 0.0045 ~ 2 in
+    magnitude.  ``poison`` puts the NaN code at slots no request owns."""
+    device = torch.device(device)
+    seed = shape.seed + layer
+    bt = block_placement(shape, seed)
+    slots = new_token_slots(shape, bt)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    Hq, Hkv, D, bs = shape.num_q_heads, shape.num_kv_heads, shape.head_dim, shape.block_size
+    T = shape.num_q_tokens
+    pool_shape = (shape.num_blocks, Hkv, bs, D)
+
+    def codes():
+        r = torch.randint(0, 254, pool_shape, generator=gen, device=device, dtype=torch.int32)
+        return (r + (r >= E4M3_NAN).to(torch.int32)).to(torch.uint8)  # skip 0x7F and 0xFF
+
+    k_pool, v_pool = codes(), codes()
+    q = _randn_bf16((T, Hq, D), gen, device)
+    k_new = _randn_bf16((T, Hkv, D), gen, device)
+    v_new = _randn_bf16((T, Hkv, D), gen, device)
+    sc = torch.rand((2, Hkv), generator=gen, device=device, dtype=torch.float32)
+    k_scale = (0.003 + 0.0015 * sc[0]).contiguous()
+    v_scale = (0.003 + 0.0015 * sc[1]).contiguous()
+    if poison:
+        owned = torch.from_numpy(owned_slot_mask(shape, bt)).to(device)
+        free = (~owned)[:, None, :, None].expand(pool_shape)
+        k_pool = k_pool.masked_fill(free, E4M3_NAN)
+        v_pool = v_pool.masked_fill(free, E4M3_NAN)
+    return Fp8StepInputs(
+        shape=shape, q=q, k_new=k_new, v_new=v_new,
+        slot_mapping=torch.from_numpy(slots).to(device),
+        k_pool=k_pool, v_pool=v_pool, k_scale=k_scale, v_scale=v_scale,
+        block_tables=torch.from_numpy(bt).to(device),
+        seq_lens=torch.from_numpy(shape.seq_lens.copy()).to(device),
+        query_start_loc=torch.from_numpy(shape.query_start_loc).to(device),
+        scale=1.0 / math.sqrt(D))
+
+
 def bf16_bits(t: torch.Tensor) -> np.ndarray:
     """uint16 bit patterns of a bf16 tensor, on the host."""
     assert t.dtype == torch.bfloat16

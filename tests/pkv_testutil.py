@@ -63,7 +63,12 @@ def assert_close(got: np.ndarray, want: np.ndarray, what: str = ""):
     return mx, mean
 
 
-def snapshot_rows(inp: wl.StepInputs, rows: list[tuple[int, int]]) -> dict:
+def pool_host(t: torch.Tensor) -> np.ndarray:
+    """Host copy of a pool: bf16 bit patterns (uint16) or e4m3 codes (uint8)."""
+    return wl.bf16_bits(t) if t.dtype == torch.bfloat16 else t.detach().contiguous().cpu().numpy()
+
+
+def snapshot_rows(inp, rows: list[tuple[int, int]]) -> dict:
     """Host copy of everything the oracle needs for sampled (request, query
     index) rows, taken BEFORE the GPU step runs: the rows' q, the pool blocks
     they read (pre-append contents) and this step's new K/V with their slots.
@@ -93,20 +98,31 @@ def snapshot_rows(inp: wl.StepInputs, rows: list[tuple[int, int]]) -> dict:
     slots = inp.slot_mapping.cpu().numpy()
     sub_slots = np.array([remap[int(s) // bs] * bs + int(s) % bs
                           if s >= 0 and int(s) // bs in remap else -1 for s in slots], np.int64)
-    return dict(qrows=qrows, lens=np.array(lens, np.int32), bt=sub_bt,
+    snap = dict(qrows=qrows, lens=np.array(lens, np.int32), bt=sub_bt,
                 q=wl.bf16_bits(inp.q[torch.tensor(qrows, device=inp.q.device)]),
-                k_pool=wl.bf16_bits(inp.k_pool.index_select(0, idx)),
-                v_pool=wl.bf16_bits(inp.v_pool.index_select(0, idx)),
+                k_pool=pool_host(inp.k_pool.index_select(0, idx)),
+                v_pool=pool_host(inp.v_pool.index_select(0, idx)),
                 k_new=wl.bf16_bits(inp.k_new), v_new=wl.bf16_bits(inp.v_new),
                 slots=sub_slots, scale=inp.scale)
+    if hasattr(inp, "k_scale"):  # e4m3 pools
+        snap["k_scale"] = inp.k_scale.cpu().numpy()
+        snap["v_scale"] = inp.v_scale.cpu().numpy()
+    return snap
 
 
 def snapshot_oracle(snap: dict, appended: bool = True):
     """Oracle outputs (fp64) of the snapshotted rows, after the oracle's own
     append of this step's new K/V when the GPU step appended too."""
     kp, vp = snap["k_pool"], snap["v_pool"]
+    n = len(snap["qrows"])
+    qsl = np.arange(n + 1, dtype=np.int32)
+    if "k_scale" in snap:
+        ks, vs = snap["k_scale"], snap["v_scale"]
+        if appended:
+            kp, vp = oracle.append_fp8(snap["k_new"], snap["v_new"], snap["slots"], kp, vp, ks, vs)
+        return oracle.paged_attention_fp8(snap["q"], kp, vp, ks, vs, snap["bt"], snap["lens"],
+                                          qsl, snap["scale"])
     if appended:
         kp, vp = oracle.append(snap["k_new"], snap["v_new"], snap["slots"], kp, vp)
-    n = len(snap["qrows"])
-    return oracle.paged_attention(snap["q"], kp, vp, snap["bt"], snap["lens"],
-                                  np.arange(n + 1, dtype=np.int32), snap["scale"])
+    return oracle.paged_attention(snap["q"], kp, vp, snap["bt"], snap["lens"], qsl,
+                                  snap["scale"])
