@@ -43,7 +43,16 @@ METRIC = "paged-attention step: KV GB/s and % of GB300 HBM peak; attended tokens
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 DECODE_SRCS = [os.path.join(ROOT, "paged_kv_cache_195_gb300", "csrc", f)
-               for f in ("pkv_decode_kernel.cuh", "pkv_decode.cu")]
+               for f in ("pkv_decode_kernel.cuh", "pkv_decode.cu", "pkv_decode_tc.cu",
+                         "pkv_plan.cuh")]
+
+
+def decode_kernel_name(group: int, fp8: bool) -> str:
+    """The decode kernel the library routes this step to (bf16 pools with 4 or
+    more query heads per KV head run on the tensor cores)."""
+    if not fp8 and group >= 4 and os.environ.get("PKV_DECODE_TC", "1") != "0":
+        return f"pkv::decode_tc_kernel<{group}>"
+    return f"pkv::decode_kernel<{group}, {'KvE4m3' if fp8 else 'KvBf16'}>"
 
 
 def dist_env():
@@ -72,9 +81,9 @@ def decode_source_sha() -> str:
 
 def committed_traffic(config: str, kv: str):
     """Per-launch DRAM bytes of the decode kernel from the committed ncu
-    summary of this workload, if it was taken on the current kernel source
+    summary of this workload, if it was taken on the current decode sources
     (else None)."""
-    path = os.path.join(ROOT, "profiles", f"decode_kernel_{config}_{kv}.md")
+    path = os.path.join(ROOT, "profiles", f"decode_{config}_{kv}.md")
     try:
         text = open(path).read()
     except OSError:
@@ -368,8 +377,7 @@ def run_ours(args):
         "roofline": {
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "traffic": traffic,
-            "kernel": f"pkv::decode_kernel<{shape.num_q_heads // shape.num_kv_heads}, "
-                      f"{'KvE4m3' if fp8 else 'KvBf16'}>",
+            "kernel": decode_kernel_name(shape.num_q_heads // shape.num_kv_heads, fp8),
             "algorithmic_bytes_per_launch": att["total"],
             "avg_launch_us": round(kernel_ms * 1e3, 3), "peak_source": peak_src,
             "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),

@@ -155,15 +155,15 @@ int encode_pool_map(CUtensorMap* m, const void* pool, const pkv_dims* d) {
   return PKV_OK;
 }
 
-// 3-D map of q as [Tq][Hq][128] bf16, boxes of (64 dims, g heads, 128/g tokens).
-int encode_q_map(CUtensorMap* m, const void* q, const pkv_dims* d, int group) {
+// 3-D map of q as [Tq][Hq][128] bf16, boxes of (64 dims, g heads, `tokens` tokens).
+int encode_q_map(CUtensorMap* m, const void* q, const pkv_dims* d, int group, int tokens) {
   EncodeTiledFn enc = encode_tiled();
   if (!enc) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
   const cuuint64_t dims[3] = {(cuuint64_t)pkv::kHeadDim, (cuuint64_t)d->num_q_heads,
                               (cuuint64_t)d->num_q_tokens};
   const cuuint64_t strides[2] = {(cuuint64_t)pkv::kHeadDim * 2,
                                  (cuuint64_t)d->num_q_heads * pkv::kHeadDim * 2};
-  const cuuint32_t box[3] = {64, (cuuint32_t)group, (cuuint32_t)pkv::prefill_tokens_per_tile(group)};
+  const cuuint32_t box[3] = {64, (cuuint32_t)group, (cuuint32_t)tokens};
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -384,18 +384,33 @@ int attention_impl(const void* q, const void* k_pool, const void* v_pool, const 
   p.min_chunk = env_int("PKV_MIN_CHUNK", 4);
   if (p.min_chunk < 1) p.min_chunk = 1;
   p.align = env_int("PKV_ALIGN", 1) != 0;
-  p.align_slack = env_int("PKV_ALIGN_SLACK", 32);
+  p.align_slack = env_int("PKV_ALIGN_SLACK", 64);
   p.prefetch = env_int("PKV_PREFETCH", 1) != 0;
   p.early_plan = p.pdl && env_int("PKV_EARLY_PLAN", 1) != 0;
   const int group = dims->num_q_heads / dims->num_kv_heads;
   int grid = pkv::decode_grid(st->sm_count, group);
   const int grid_env = env_int("PKV_DECODE_GRID", 0);  // tuning override, bounded by the slots
   if (grid_env > 0 && 2 * grid_env <= w.num_slots) grid = grid_env;
-  cudaError_t e = pkv::launch_decode(p, group, grid, stream);
+  // Groups of 4 or more query heads per KV head make the decode's FP32 FMA
+  // work comparable to its HBM time; those run on the tensor cores.
+  const bool use_tc = !fp8 && group >= 4 && env_int("PKV_DECODE_TC", 1) != 0;
+  cudaError_t e;
+  if (use_tc) {
+    pkv::DecodeTcLaunch T{};
+    rc = encode_q_map(&T.qmap, q, dims, group, 1);
+    if (rc == PKV_OK) rc = encode_pool_map(&T.kmap, k_pool, dims);
+    if (rc == PKV_OK) rc = encode_pool_map(&T.vmap, v_pool, dims);
+    if (rc != PKV_OK) return rc;
+    T.p = p;
+    T.grid = st->sm_count;
+    e = pkv::launch_decode_tc(T, group, stream);
+  } else {
+    e = pkv::launch_decode(p, group, grid, stream);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   if (run_prefill) {
     pkv::PrefillLaunch L{};
-    rc = encode_q_map(&L.qmap, q, dims, group);
+    rc = encode_q_map(&L.qmap, q, dims, group, pkv::prefill_tokens_per_tile(group));
     if (rc == PKV_OK) rc = encode_pool_map(&L.kmap, k_pool, dims);
     if (rc == PKV_OK) rc = encode_pool_map(&L.vmap, v_pool, dims);
     if (rc != PKV_OK) return rc;
@@ -462,6 +477,13 @@ int pkv_get_device_error(cudaStream_t stream) {
     return fail(PKV_ERR_DEVICE_BOUNDS, "device bounds violation (flags %d)", word);
   return PKV_OK;
 }
+
+#if PKV_TC_TRACE
+// Debug builds only: copies the tensor-core decode's per-tile timeline.
+int pkv_debug_tc_trace(void* host, size_t bytes) {
+  return pkv::decode_tc_trace(host, bytes) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+#endif
 
 #if PKV_TRACE
 // Debug builds only: copies the decode kernel's per-CTA phase stamps.

@@ -157,6 +157,21 @@ __device__ __forceinline__ void named_barrier(int id, int threads) {
 }
 
 // ------------------------------------------------------------- arithmetic
+// OR of `v` over the `threads` threads (a multiple of 32) that meet at named
+// barrier `id`; also a barrier for them.
+__device__ __forceinline__ bool barrier_or(int id, int threads, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(v ? 1u : 0u), "r"(id), "r"(threads)
+      : "memory");
+  return r != 0;
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

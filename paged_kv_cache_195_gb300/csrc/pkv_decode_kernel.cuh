@@ -51,6 +51,7 @@
 #include <cuda_fp8.h>
 
 #include "pkv_internal.h"
+#include "pkv_plan.cuh"
 
 namespace pkv {
 namespace {
@@ -141,20 +142,8 @@ constexpr float kNegBig = -1.0e30f;          // "no key seen yet" running max
 #endif
 constexpr bool kLazyMax = PKV_LAZY_MAX != 0;  // raise the running max only when needed
 constexpr float kLazyMargin = 8.f;           // log2 of the largest probability allowed
-constexpr int kEndRow = -2;                  // piece marker: the CTA's range is done
-
-// One piece of a row-group: the blocks [b0, b0 + nblk) of row `row`, KV head k.
-struct Piece {
-  int row;     // global query row, or kEndRow
-  int k;       // KV head
-  int b0;      // first logical block of the piece
-  int nblk;    // blocks in the piece (>= 1)
-  int limit;   // keys visible to this row: positions < limit
-  int slot;    // workspace slot of this piece's partial state (partial pieces)
-  int c0;      // first CTA whose range touches the row-group
-  int S;       // pieces of the row-group (1: complete in this CTA)
-  int odd0;    // piece 0 of the row-group uses slot 2*c0+1 (else 2*c0)
-};
+using plan::Piece;
+using plan::kEndRow;
 
 #ifndef PKV_P_DUP
 #define PKV_P_DUP 0
@@ -416,40 +405,6 @@ struct BlockMath {  // G = query heads this warp holds
 };
 
 // ---------------------------------------------------------------------------
-// The plan.
-// ---------------------------------------------------------------------------
-// Sum over x = 1..n of ceil(x / 16): with n = 16m + t, 8m(m+1) + t(m+1).
-__device__ __forceinline__ long long ceil16_prefix(long long n) {
-  if (n <= 0) return 0;
-  const long long m = n / kBlockSize, t = n % kBlockSize;
-  return 8 * m * (m + 1) + t * (m + 1);
-}
-
-struct ReqInfo {
-  int q0, qr, L;
-  bool decode;  // has rows this kernel serves
-};
-
-__device__ __forceinline__ ReqInfo load_request(const DecodeParams& p, int r) {
-  ReqInfo ri;
-  ri.q0 = __ldg(p.qsl + r);
-  const int q1 = __ldg(p.qsl + r + 1);
-  ri.L = __ldg(p.seq_lens + r);
-  ri.qr = q1 - ri.q0;
-  const bool ok = ri.q0 >= 0 && ri.qr >= 0 && q1 <= p.num_q_tokens && ri.qr <= ri.L &&
-                  ri.L <= p.max_blocks * kBlockSize;
-  ri.decode = ok && ri.qr > 0 && ri.qr < p.prefill_min_q;
-  return ri;
-}
-
-// Blocks of rows 0..i-1 of a request (one KV head): row i sees L - qr + i + 1
-// keys, i.e. ceil((L - qr + 1 + i) / 16) blocks.
-__device__ __forceinline__ long long rows_blocks(const ReqInfo& ri, int i) {
-  const long long a = (long long)ri.L - ri.qr + 1;
-  return ceil16_prefix(a + i - 1) - ceil16_prefix(a - 1);
-}
-
-// ---------------------------------------------------------------------------
 // The kernel.
 // ---------------------------------------------------------------------------
 template <int G, class KV>
@@ -464,7 +419,7 @@ __global__ void __launch_bounds__(DecodeCfg<G>::kThreads) __maxnreg__(DecodeCfg<
   constexpr int kTile = KV::kTileBytes;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int R = p.num_reqs, Hkv = p.num_kv_heads;
+  const int Hkv = p.num_kv_heads;
 
   if (tid == 0) TRACE(0);
   if (tid == 0) {
@@ -496,51 +451,8 @@ __global__ void __launch_bounds__(DecodeCfg<G>::kThreads) __maxnreg__(DecodeCfg<
 
   if (warp == DecodeCfg<G>::kCW) {
     // ======================= producer warp =================================
-    // Warm L2 with the part of the block table this CTA will probably read
-    // (its share of the step if every row were full), while the plan loads.
-    if (p.prefetch) {
-      const long long entries = (long long)R * p.max_blocks;
-      const long long est = entries * blockIdx.x / gridDim.x;
-      const long long line0 = (est * 4) / 128 - 2;
-      const long long lines = (entries * 4 + 127) / 128;
-      const long long line = line0 + lane;
-      if (line >= 0 && line < lines)
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(p.block_tables) +
-                                                     line * 128));
-    }
-    // ---- plan, pass 1: total blocks W of the decode rows (all KV heads) ----
-    long long mine = 0;
-    int nb_min = INT_MAX, nb_max = 0;
-    for (int r = lane; r < R; r += 32) {
-      const ReqInfo ri = load_request(p, r);
-      if (ri.decode) {
-        mine += rows_blocks(ri, ri.qr) * Hkv;
-        nb_min = min(nb_min, ceil_div(ri.L - ri.qr + 1, kBlockSize));
-        nb_max = max(nb_max, ceil_div(ri.L, kBlockSize));
-      } else if (blockIdx.x == 0 && ri.qr != 0 && ri.qr < p.prefill_min_q) {
-        record_error(p.err, kErrBounds);  // inconsistent lengths: request skipped
-      }
-    }
-    #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      mine += __shfl_xor_sync(0xffffffffu, mine, o);
-      nb_min = min(nb_min, __shfl_xor_sync(0xffffffffu, nb_min, o));
-      nb_max = max(nb_max, __shfl_xor_sync(0xffffffffu, nb_max, o));
-    }
-    const long long W = mine;
-    long long chunk = max((long long)p.min_chunk, ceil_div_ll(W, gridDim.x));
-    if (p.align && nb_min == nb_max && W > 0) {
-      // Uniform row-groups: cut each into equal pieces, or keep whole groups
-      // together, so that piece boundaries coincide with CTA boundaries --
-      // unless that lengthens every CTA's range by more than align_slack
-      // blocks (then idle CTAs cost more than the extra pieces save).
-      const long long nb = nb_max;
-      const long long snapped =
-          chunk < nb ? ceil_div_ll(nb, nb / chunk) : ceil_div_ll(chunk, nb) * nb;
-      if (snapped - chunk <= p.align_slack) chunk = snapped;
-    }
-    const long long lo = (long long)blockIdx.x * chunk;
-    const long long hi = min(W, lo + chunk);
+    if (p.prefetch) plan::prefetch_block_table(p, lane);
+    const plan::Range rg = plan::cta_range(p, lane);
     if (lane == 0) TRACE(2);
 
     const uint64_t pol = l2_policy_evict_first();
@@ -550,119 +462,49 @@ __global__ void __launch_bounds__(DecodeCfg<G>::kThreads) __maxnreg__(DecodeCfg<
       grid_dependency_wait();
       allow_dependent_launch();
     }
-    if (lo < hi) {
-      // ---- pass 2: the request holding block lo, and where it starts -------
-      int r = -1;
-      long long pos = 0, base = 0;
-      for (int b = 0; b < R; b += 32) {
-        const int rr = b + lane;
-        long long w = 0;
-        if (rr < R) {
-          const ReqInfo ri = load_request(p, rr);
-          if (ri.decode) w = rows_blocks(ri, ri.qr) * Hkv;
-        }
-        long long incl = w;
-        #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const long long t = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += t;
-        }
-        const long long excl = incl - w;
-        const unsigned own = __ballot_sync(0xffffffffu, w > 0 && base + excl <= lo && lo < base + incl);
-        if (own) {
-          const int src = __ffs(own) - 1;
-          r = b + src;
-          pos = base + __shfl_sync(0xffffffffu, excl, src);
-          break;
-        }
-        base += __shfl_sync(0xffffffffu, incl, 31);
+    plan::Walker wk;
+    wk.start(p, rg, lane);
+    Piece pc;
+    while (!*abort_flag && wk.next(p, pc)) {
+      // ---- one piece: blocks [b0, b0 + nblk) of row-group (row, k) --------
+      const int k = pc.k;
+      const int ub = j & 1;
+      if (j >= 2 && !mbar_wait(&sm.qempty[ub], ((j >> 1) - 1) & 1, p.err, abort_flag)) break;
+      if (lane == 0) {
+        sm.pinfo[ub] = pc;
+        mbar_arrive_expect_tx(&sm.qfull[ub], G * kHeadDim * 2);
+        bulk_copy_g2s(sm.qbuf[ub],
+                      p.q + ((long long)pc.row * p.num_q_heads + (long long)k * G) * kHeadDim,
+                      G * kHeadDim * 2, &sm.qfull[ub]);
       }
-      // Walk the row-groups that intersect [lo, hi).
-      if (r < 0) {
-        record_error(p.err, kErrBounds);  // unreachable when the lengths are stable
-        r = R;
-      }
-      ReqInfo ri = load_request(p, r < R ? r : 0);
-      int i = 0;
-      {  // first row of request r whose groups reach lo (binary search)
-        int a = 0, b = ri.qr - 1;
-        while (a < b) {
-          const int mid = (a + b + 1) / 2;
-          if (pos + rows_blocks(ri, mid) * Hkv <= lo) a = mid; else b = mid - 1;
-        }
-        i = a;
-      }
-      long long g = r < R ? pos + rows_blocks(ri, i) * Hkv : hi;  // start of row i, head 0
-      int nb = ceil_div(ri.L - ri.qr + i + 1, kBlockSize);
-      int k = (int)((lo - g) / nb);
-      g += (long long)k * nb;
-      while (g < hi && !*abort_flag) {
-        // ---- one piece: row-group (r, i, k) = global blocks [g, g + nb) ----
-        const long long s0 = max(g, lo), s1 = min(g + nb, hi);
-        const long long c0 = g / chunk, c1 = (g + nb - 1) / chunk;
-        Piece pc;
-        pc.row = ri.q0 + i;
-        pc.k = k;
-        pc.b0 = (int)(s0 - g);
-        pc.nblk = (int)(s1 - s0);
-        pc.limit = ri.L - ri.qr + i + 1;
-        pc.S = (int)(c1 - c0 + 1);
-        pc.c0 = (int)c0;
-        pc.odd0 = g != c0 * chunk;
-        pc.slot = 2 * (int)blockIdx.x + (s0 == lo ? 0 : 1);
-        const int ub = j & 1;
-        if (j >= 2 && !mbar_wait(&sm.qempty[ub], ((j >> 1) - 1) & 1, p.err, abort_flag)) break;
-        if (lane == 0) {
-          sm.pinfo[ub] = pc;
-          mbar_arrive_expect_tx(&sm.qfull[ub], G * kHeadDim * 2);
-          bulk_copy_g2s(sm.qbuf[ub],
-                        p.q + ((long long)pc.row * p.num_q_heads + (long long)k * G) * kHeadDim,
-                        G * kHeadDim * 2, &sm.qfull[ub]);
-        }
-        const int32_t* bt = p.block_tables + (long long)r * p.max_blocks + pc.b0;
-        for (int bb = 0; bb < pc.nblk && !*abort_flag; bb += 32) {
-          const int cnt = min(32, pc.nblk - bb);
-          const int ent = lane < cnt ? __ldg(bt + bb + lane) : 0;
-          for (int xb = 0; xb < cnt; ++xb, ++n) {
-            int phys = __shfl_sync(0xffffffffu, ent, xb);
-            const int st = n % kStages;
-            [[maybe_unused]] const unsigned long long tw0 = TRACE_NOW();
-            if (n >= kStages &&
-                !mbar_wait(&sm.empty[st], ((n / kStages) - 1) & 1, p.err, abort_flag))
-              break;
-            if (lane == 0) TRACE_ADD(8, TRACE_NOW() - tw0);
-            if (lane == 0) {
-              const bool valid = (unsigned)phys < (unsigned)p.num_blocks;
-              if (!valid) {
-                record_error(p.err, kErrBounds);
-                phys = 0;
-              }
-              sm.stage_valid[st] = valid;
-              const long long tile = ((long long)phys * Hkv + k) * kTile;
-              mbar_arrive_expect_tx(&sm.full[st], kStageBytes);
-              bulk_copy_g2s(sm.ring[st], p.k_pool + tile, kTile, &sm.full[st], pol);
-              bulk_copy_g2s(sm.ring[st] + kTile, p.v_pool + tile, kTile, &sm.full[st], pol);
+      const int32_t* bt = p.block_tables + (long long)pc.r * p.max_blocks + pc.b0;
+      for (int bb = 0; bb < pc.nblk && !*abort_flag; bb += 32) {
+        const int cnt = min(32, pc.nblk - bb);
+        const int ent = lane < cnt ? __ldg(bt + bb + lane) : 0;
+        for (int xb = 0; xb < cnt; ++xb, ++n) {
+          int phys = __shfl_sync(0xffffffffu, ent, xb);
+          const int st = n % kStages;
+          [[maybe_unused]] const unsigned long long tw0 = TRACE_NOW();
+          if (n >= kStages &&
+              !mbar_wait(&sm.empty[st], ((n / kStages) - 1) & 1, p.err, abort_flag))
+            break;
+          if (lane == 0) TRACE_ADD(8, TRACE_NOW() - tw0);
+          if (lane == 0) {
+            const bool valid = (unsigned)phys < (unsigned)p.num_blocks;
+            if (!valid) {
+              record_error(p.err, kErrBounds);
+              phys = 0;
             }
-            __syncwarp();
+            sm.stage_valid[st] = valid;
+            const long long tile = ((long long)phys * Hkv + k) * kTile;
+            mbar_arrive_expect_tx(&sm.full[st], kStageBytes);
+            bulk_copy_g2s(sm.ring[st], p.k_pool + tile, kTile, &sm.full[st], pol);
+            bulk_copy_g2s(sm.ring[st] + kTile, p.v_pool + tile, kTile, &sm.full[st], pol);
           }
-        }
-        ++j;
-        // ---- advance to the next row-group ---------------------------------
-        g += nb;
-        if (++k == Hkv) {
-          k = 0;
-          if (++i == ri.qr) {
-            i = 0;
-            do {
-              ++r;
-              if (r >= R) break;
-              ri = load_request(p, r);
-            } while (!ri.decode);
-            if (r >= R) break;
-          }
-          nb = ceil_div(ri.L - ri.qr + i + 1, kBlockSize);
+          __syncwarp();
         }
       }
+      ++j;
     }
     // End marker: no more pieces for this CTA.
     const int ub = j & 1;

@@ -1,0 +1,568 @@
+// pkv_decode_tc.cu -- paged decode attention on tcgen05 tensor cores, for
+// GQA groups of g >= 4 query heads per KV head.
+//
+// What it computes is the decode kernel's (pkv_decode_kernel.cuh): for every
+// query row served by the decode path and every KV head, the softmax-weighted
+// sum of V over the row's visible keys, gathered through the block table (The
+// Serving Playbook, "The block table lives in the hottest kernel in the
+// system"), with an fp32 online softmax (LLM 7 - Efficient LLM Serving,
+// sec. 2 "Online Softmax Makes Tiling Possible") and a log-sum-exp merge of
+// the pieces a row is split into (The Serving Playbook, "Kernel fusion,
+// briefly").  The work plan -- equal contiguous ranges of the step's block
+// sequence, one per CTA -- is the same (pkv_plan.cuh), and so is the
+// workspace format of partial pieces.
+//
+// Why tensor cores.  With g heads sharing a KV head, each K or V element
+// feeds g multiply-adds per query row: 2g FMAs per 2-byte element.  GB300's
+// FP32 pipe peaks near 128 FMA/clk/SM, so at g = 6 the FMA work of a block
+// is half its HBM time at the copy peak, and an e4m3 cache would need all of
+// it.  The group's QK^T and PV are small dense contractions; run them on the
+// tensor core instead and the SIMT work left per key is one exp2 per head.
+//
+// Shape.  A tile is 128 consecutive keys of a piece = 8 pool blocks, each
+// (block, KV head) 16-row slab fetched through the block table by a 2-D TMA
+// copy (128-byte swizzle; blocks past the piece are fetched at an
+// out-of-range row, which TMA fills with zeros).  With the keys as the MMA's
+// M dimension and the group's heads as N (padded to 16):
+//     S^T[128 keys x 16] = K[128 x 128 d] . Q^T                 (K-major A, B)
+//     O^T[128 d x 16]   += V^T[128 d x 128 keys] . P^T[128 x 16] (MN-major A)
+// both accumulating in fp32 in TMEM.  Thread t of the four softmax warps owns
+// TMEM lane t: key t of S^T, dim t of O^T.
+//
+// Roles (192 threads): warps 0-3 softmax and epilogue, warp 4 plan and TMA
+// producer, one thread of warp 5 issues the MMAs.  S and P are double
+// buffered, so the QK^T of tile n+1 runs while the softmax works on tile n.
+// The running maximum is raised only when a score exceeds it by more than
+// 2^8 (a CTA-wide vote), so the common tile needs no cross-thread reduction;
+// O^T is rescaled in TMEM on the rare raise.
+#include "pkv_internal.h"
+#include "pkv_plan.cuh"
+#include "pkv_tc.cuh"
+
+namespace pkv {
+namespace {
+
+using plan::Piece;
+using plan::kEndRow;
+
+constexpr int kTcThreads = 192;
+constexpr int kTile = 128;                 // keys per tile (MMA M of S^T, K of PV)
+constexpr int kBlkPerTile = kTile / kBlockSize;
+constexpr int kN = 16;                     // MMA N: the group's heads, padded
+constexpr int kHalf = kTile * 128;         // one 64-dim half of a 128-key bf16 tile
+constexpr int kOpHalf = kN * 128;          // one 64-element half of a 16-row operand
+#ifndef PKV_TC_STAGES
+#define PKV_TC_STAGES 3
+#endif
+constexpr int kStages = PKV_TC_STAGES;     // K/V tile stages (64 KiB each)
+#ifndef PKV_TC_PV_FIRST
+#define PKV_TC_PV_FIRST 1
+#endif
+constexpr uint32_t kTmemCols = 64;         // S0: 0..15, S1: 16..31, O: 32..47
+constexpr uint32_t kColO = 32;
+constexpr float kNegBig = -1.0e30f;
+constexpr float kLazyMargin = 8.f;         // log2 of the largest probability allowed
+constexpr int kBarSoftmax = 1;             // named barrier of the four softmax warps
+
+// Debug-only per-tile timeline of CTA 0 (build with -DPKV_TC_TRACE=1):
+// %globaltimer at load issue, keys seen by the MMA warp, scores seen by the
+// softmax, PV issue, and stage release seen by the producer.
+#ifndef PKV_TC_TRACE
+#define PKV_TC_TRACE 0
+#endif
+#if PKV_TC_TRACE
+constexpr int kTrTiles = 64;
+__device__ unsigned long long g_tc_trace[7][kTrTiles];
+#define TC_TR(ev, tile) do { if (blockIdx.x == 0 && (tile) < kTrTiles) g_tc_trace[ev][tile] = global_timer_ns(); } while (0)
+#else
+#define TC_TR(ev, tile) do { } while (0)
+#endif
+
+struct __align__(1024) TcSmem {
+  uint8_t k[kStages][2][kHalf];   // [stage][d half]: 128 keys x 64 d, swizzled
+  uint8_t v[kStages][2][kHalf];
+  uint8_t q[2][2][kOpHalf];       // [piece buffer][d half]: Q rows (heads), rows >= g zero
+  uint8_t pt[2][2][kOpHalf];      // [buffer][key half]: P^T as 16 rows (heads) x 64 keys
+  float red[4][kN];               // per-warp partial maxima / sums
+  Piece pinfo[2];
+  uint64_t q_full[2], q_empty[2];
+  uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
+  uint64_t s_full[2], s_free[2], p_full[2], p_free[2];
+  uint64_t o_full, o_empty;
+  uint32_t tmem_base;
+  int abort_flag;
+  int is_last;
+};
+
+__device__ __forceinline__ float warp_max(float v) {
+  #pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+  #pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+template <int G>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap qmap,
+                     const __grid_constant__ CUtensorMap kmap,
+                     const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
+  static_assert(G >= 1 && G <= 8, "group size");
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 128-byte swizzled operands need 1024-byte aligned shared addresses.
+  const uint32_t raw = smem_u32(smem_raw);
+  TcSmem& sm = *reinterpret_cast<TcSmem*>(smem_raw + (((raw + 1023u) & ~1023u) - raw));
+  volatile int* abort_flag = &sm.abort_flag;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int Hkv = p.num_kv_heads;
+
+  if (tid == 0) {
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.q_full[b], 1);
+      mbar_init(&sm.q_empty[b], 1);   // tcgen05.commit after the piece's last MMA
+      mbar_init(&sm.s_full[b], 1);    // tcgen05.commit after S^T = K Q^T into buffer b
+      mbar_init(&sm.s_free[b], 4);    // the softmax warps have read S buffer b
+      mbar_init(&sm.p_full[b], 4);    // P^T buffer b written by the softmax warps
+      mbar_init(&sm.p_free[b], 1);    // tcgen05.commit after the PV that read P^T buffer b
+    }
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sm.k_full[s], 1);
+      mbar_init(&sm.v_full[s], 1);
+      mbar_init(&sm.kv_empty[s], 1);
+    }
+    mbar_init(&sm.o_full, 1);
+    mbar_init(&sm.o_empty, 4);
+    sm.abort_flag = 0;
+    fence_barrier_init();
+  }
+  // Operand rows g..15 (padding heads) stay zero for the whole kernel.
+  for (int i = tid; i < (int)(sizeof(sm.q) + sizeof(sm.pt)) / 16; i += kTcThreads) {
+    uint8_t* base = i < (int)sizeof(sm.q) / 16 ? &sm.q[0][0][0] + i * 16
+                                               : &sm.pt[0][0][0] + (i - (int)sizeof(sm.q) / 16) * 16;
+    *reinterpret_cast<uint4*>(base) = make_uint4(0, 0, 0, 0);
+  }
+  fence_proxy_async_smem();
+  if (warp == 4 && lane == 0) {
+    prefetch_tensormap(&qmap);
+    prefetch_tensormap(&kmap);
+    prefetch_tensormap(&vmap);
+  }
+  if (warp == 5) {
+    tmem_alloc(&sm.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  // Consumers wait for the previous kernel on the stream here; the producer
+  // builds its plan first (it reads only seq_lens / query_start_loc, which
+  // with early_plan set the previous kernel does not write).  Each thread
+  // lets the next kernel launch only after its own wait.
+  if (warp != 4 || !p.early_plan) {
+    grid_dependency_wait();
+    allow_dependent_launch();
+  }
+
+  if (warp == 4) {
+    // ========================= plan + TMA producer ========================
+    if (p.prefetch) plan::prefetch_block_table(p, lane);
+    const plan::Range rg = plan::cta_range(p, lane);
+    if (p.early_plan) {
+      grid_dependency_wait();
+      allow_dependent_launch();
+    }
+    const int oob_row = p.num_blocks * Hkv * kBlockSize;  // zero-filled by TMA
+    plan::Walker wk;
+    wk.start(p, rg, lane);
+    Piece pc;
+    int j = 0, t = 0;  // piece and tile counters
+    bool ok = true;
+    while (ok && !*abort_flag && wk.next(p, pc)) {
+      const int k = pc.k;
+      const int ntile = plan::cdiv(pc.nblk, kBlkPerTile);
+      const int32_t* bt = p.block_tables + (long long)pc.r * p.max_blocks + pc.b0;
+      // Pool rows of the piece's blocks, 32 blocks (four tiles) per load, the
+      // next group fetched while the current one is being issued.
+      auto rows_of = [&](int x0) {
+        int rowc = oob_row;
+        const int x = x0 + lane;
+        if (x < pc.nblk) {
+          const int phys = __ldg(bt + x);
+          if ((unsigned)phys < (unsigned)p.num_blocks) rowc = (phys * Hkv + k) * kBlockSize;
+          else record_error(p.err, kErrBounds);
+        }
+        return rowc;
+      };
+      int rows_cur = rows_of(0);
+      int rows_nxt = ntile > 4 ? rows_of(32) : oob_row;
+      for (int tt = 0; tt < ntile; ++tt, ++t) {
+        if (tt > 0 && (tt & 3) == 0) {
+          rows_cur = rows_nxt;
+          if (tt + 4 < ntile) rows_nxt = rows_of((tt + 4) * kBlkPerTile);
+        }
+        const int st = t % kStages;
+        if (t >= kStages &&
+            !mbar_wait(&sm.kv_empty[st], ((t / kStages) - 1) & 1, p.err, abort_flag)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0 && t >= kStages) TC_TR(4, t - kStages);
+        if (lane == 0) TC_TR(0, t);
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&sm.k_full[st], 2u * kHalf);
+          mbar_arrive_expect_tx(&sm.v_full[st], 2u * kHalf);
+        }
+        __syncwarp();
+        // Lanes 0..15 each copy one (block, d half) of K and of V.
+        const int bsel = lane & 7, hsel = (lane >> 3) & 1;
+        const int row = __shfl_sync(0xffffffffu, rows_cur, (tt & 3) * kBlkPerTile + bsel);
+        if (lane < 16) {
+          tma_load_2d(sm.k[st][hsel] + bsel * 2048, &kmap, hsel * 64, row, &sm.k_full[st]);
+          tma_load_2d(sm.v[st][hsel] + bsel * 2048, &vmap, hsel * 64, row, &sm.v_full[st]);
+        }
+        __syncwarp();
+        if (tt == 0) {
+          // Q of this piece, once the MMAs of piece j-2 are done with its
+          // buffer (the piece's first K/V tile is already on its way).
+          const int ub = j & 1;
+          if (j >= 2 && !mbar_wait(&sm.q_empty[ub], ((j >> 1) - 1) & 1, p.err, abort_flag)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) {
+            sm.pinfo[ub] = pc;
+            mbar_arrive_expect_tx(&sm.q_full[ub], 2u * 64u * G * 2u);
+            tma_load_3d(sm.q[ub][0], &qmap, 0, k * G, pc.row, &sm.q_full[ub]);
+            tma_load_3d(sm.q[ub][1], &qmap, 64, k * G, pc.row, &sm.q_full[ub]);
+          }
+          __syncwarp();
+        }
+      }
+      ++j;
+    }
+    // End marker: no more pieces for this CTA.
+    const int ub = j & 1;
+    if (j < 2 || mbar_wait(&sm.q_empty[ub], ((j >> 1) - 1) & 1, p.err, abort_flag)) {
+      if (lane == 0) {
+        sm.pinfo[ub].row = kEndRow;
+        mbar_arrive(&sm.q_full[ub]);
+      }
+    }
+  } else if (warp == 5) {
+    // ============================ MMA issuer ==============================
+    // Tile n: S^T(n) = K(n) Q^T into S buffer n&1, then O^T += V^T(n-1)
+    // P^T(n-1), so the QK^T of a tile overlaps the softmax of the previous.
+    if (lane == 0) {
+      constexpr uint32_t kIdescS = idesc_bf16_f32(kTile, kN, 0, 0);
+      constexpr uint32_t kIdescO = idesc_bf16_f32(kHeadDim, kN, 1, 0);
+      const uint32_t tO = tmem + kColO;
+      int t = 0;
+      bool ok = true;
+      auto pv = [&](int tt, bool first, int j) {
+        const int b = tt & 1, st = tt % kStages;
+        ok = ok && mbar_wait(&sm.p_full[b], (tt >> 1) & 1, p.err, abort_flag);
+        ok = ok && mbar_wait(&sm.v_full[st], (tt / kStages) & 1, p.err, abort_flag);
+        if (first && j > 0) ok = ok && mbar_wait(&sm.o_empty, (j - 1) & 1, p.err, abort_flag);
+        if (!ok) return;
+        TC_TR(3, tt);
+        tc_fence_after();
+        #pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          // V^T is MN-major (d contiguous): atoms of 64 d x 8 keys, the two d
+          // halves kHalf apart, 8-key groups 1024 bytes apart.
+          const uint64_t da = smem_desc_sw128(smem_u32(sm.v[st][0]) + kk * 2048, kHalf, 1024);
+          const uint64_t db =
+              smem_desc_sw128(smem_u32(sm.pt[b][kk >> 2]) + (kk & 3) * 32, 16, 1024);
+          tc_mma_f16_ss(tO, da, db, kIdescO, !first || kk > 0);
+        }
+        tc_commit(&sm.kv_empty[st]);
+        tc_commit(&sm.p_free[b]);
+#if PKV_TC_TRACE >= 2
+        mbar_wait(&sm.p_free[b], (tt >> 1) & 1, p.err, abort_flag);  // PV completion
+        TC_TR(6, tt);
+#endif
+      };
+      for (int j = 0; ok; ++j) {
+        const int ub = j & 1;
+        if (!mbar_wait(&sm.q_full[ub], (j >> 1) & 1, p.err, abort_flag)) break;
+        const Piece pc = sm.pinfo[ub];
+        if (pc.row == kEndRow) break;
+        const int ntile = plan::cdiv(pc.nblk, kBlkPerTile);
+        tc_fence_after();
+        for (int tt = 0; tt < ntile && ok; ++tt, ++t) {
+          const int b = t & 1, st = t % kStages;
+          // The previous tile's PV first: its stage is released as soon as
+          // its probabilities are ready, not after this tile's keys arrive.
+          if (PKV_TC_PV_FIRST && tt >= 1) pv(t - 1, tt == 1, j);
+          ok = ok && mbar_wait(&sm.k_full[st], (t / kStages) & 1, p.err, abort_flag);
+          TC_TR(1, t);
+          if (t >= 2) ok = ok && mbar_wait(&sm.s_free[b], ((t >> 1) - 1) & 1, p.err, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t tS = tmem + b * kN;
+          #pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t da =
+                smem_desc_sw128(smem_u32(sm.k[st][kk >> 2]) + (kk & 3) * 32, 16, 1024);
+            const uint64_t db =
+                smem_desc_sw128(smem_u32(sm.q[ub][kk >> 2]) + (kk & 3) * 32, 16, 1024);
+            tc_mma_f16_ss(tS, da, db, kIdescS, kk > 0);
+          }
+          tc_commit(&sm.s_full[b]);
+#if PKV_TC_TRACE >= 2
+          mbar_wait(&sm.s_full[b], (t >> 1) & 1, p.err, abort_flag);  // QK completion
+          TC_TR(5, t);
+#endif
+          if (!PKV_TC_PV_FIRST && tt >= 1) pv(t - 1, tt == 1, j);
+        }
+        if (ok) pv(t - 1, ntile == 1, j);  // the piece's last tile
+        tc_commit(&sm.o_full);
+        tc_commit(&sm.q_empty[ub]);
+      }
+    }
+    __syncwarp();
+  } else {
+    // =================== softmax + epilogue (warps 0-3) ===================
+    const int row = tid;  // TMEM lane: key `row` of a tile, dim `row` of O^T
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t tO = tmem + lane_off + kColO;
+    constexpr int kSoftThreads = 128;
+    int t = 0;
+    bool ok = true;
+    for (int j = 0; ok; ++j) {
+      const int ub = j & 1;
+      ok = mbar_wait(&sm.q_full[ub], (j >> 1) & 1, p.err, abort_flag);
+      const Piece pc = sm.pinfo[ub];
+      if (!ok || pc.row == kEndRow) break;
+      const bool in_range = pc.row >= 0 && pc.row < p.num_q_tokens && pc.k >= 0 &&
+                            pc.k < Hkv && pc.nblk >= 1 && pc.S >= 1 && pc.c0 >= 0 &&
+                            2 * (pc.c0 + pc.S) <= p.num_slots && pc.slot >= 0 &&
+                            pc.slot < p.num_slots;
+      const int ntile = plan::cdiv(pc.nblk, kBlkPerTile);
+      float m[G], l[G];
+      #pragma unroll
+      for (int h = 0; h < G; ++h) {
+        m[h] = kNegBig;
+        l[h] = 0.f;
+      }
+      for (int tt = 0; tt < ntile; ++tt, ++t) {
+        const int b = t & 1, st = t % kStages;
+        ok = ok && mbar_wait(&sm.s_full[b], (t >> 1) & 1, p.err, abort_flag);
+        if (row == 0) TC_TR(2, t);
+        tc_fence_after();
+        float s[8];
+        tmem_ld8(tmem + lane_off + b * kN, s);
+        tc_wait_ld();
+        // Key `row` of this tile: block x of the tile, offset row % 16.
+        const int x = tt * kBlkPerTile + (row >> 4);
+        const int pos = (pc.b0 + x) * kBlockSize + (row & 15);
+        const bool valid = ok && x < pc.nblk && pos < pc.limit;
+        bool over = false;
+        #pragma unroll
+        for (int h = 0; h < G; ++h) {
+          s[h] = valid ? s[h] * p.scale_log2 : -INFINITY;
+          over |= s[h] > m[h] + kLazyMargin;
+        }
+        // S buffer b has been read: the MMA may overwrite it (tile t + 2).
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.s_free[b]);
+        if (barrier_or(kBarSoftmax, kSoftThreads, over)) {
+          // Raise the running maxima to this tile's; O^T and l move with them.
+          #pragma unroll
+          for (int h = 0; h < G; ++h) {
+            const float mx = warp_max(s[h]);
+            if (lane == 0) sm.red[warp][h] = mx;
+          }
+          named_barrier(kBarSoftmax, kSoftThreads);
+          float alpha[8];
+          bool grow = false;
+          #pragma unroll
+          for (int h = 0; h < G; ++h) {
+            const float mx = fmaxf(fmaxf(sm.red[0][h], sm.red[1][h]),
+                                   fmaxf(sm.red[2][h], sm.red[3][h]));
+            const float mn = fmaxf(m[h], mx);
+            alpha[h] = fast_exp2(m[h] - mn);
+            grow |= mn != m[h];
+            m[h] = mn;
+            l[h] *= alpha[h];
+          }
+          if (tt > 0 && grow) {
+            // O^T must hold the previous tile's PV before it is rescaled.
+            ok = ok && mbar_wait(&sm.p_free[(t - 1) & 1], ((t - 1) >> 1) & 1, p.err, abort_flag);
+            tc_fence_after();
+            float o[8];
+            tmem_ld8(tO, o);
+            tc_wait_ld();
+            #pragma unroll
+            for (int h = 0; h < G; ++h) o[h] *= alpha[h];
+            tmem_st8(tO, o);
+            tc_wait_st();
+          }
+          // sm.red is read by every softmax thread before its next write.
+          named_barrier(kBarSoftmax, kSoftThreads);
+        }
+        // P^T buffer b was last read by the PV of tile t - 2.
+        if (t >= 2) ok = ok && mbar_wait(&sm.p_free[b], ((t >> 1) - 1) & 1, p.err, abort_flag);
+        // p = exp2(s - m) in bf16; P^T row h holds head h, keys contiguous,
+        // 128-byte swizzle.  The normaliser sums the rounded values the MMA
+        // will use.
+        uint8_t* prow = sm.pt[b][row >> 6];
+        const int kc = (row & 63) >> 3;
+        #pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const __nv_bfloat16 pb = __float2bfloat16_rn(fast_exp2(s[h] - m[h]));
+          l[h] += __bfloat162float(pb);
+          *reinterpret_cast<__nv_bfloat16*>(prow + (h >> 3) * 1024 + (h & 7) * 128 +
+                                            ((kc ^ (h & 7)) * 16) + (row & 7) * 2) = pb;
+        }
+        // Keys past the request's end inside its last block may hold anything
+        // (even NaN): zero those V rows so that 0 * V stays 0 in the MMA.
+        if (x < pc.nblk && pos >= pc.L) {
+          ok = ok && mbar_wait(&sm.v_full[st], (t / kStages) & 1, p.err, abort_flag);
+          #pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            uint4* vr = reinterpret_cast<uint4*>(sm.v[st][hf] + (row >> 3) * 1024 + (row & 7) * 128);
+            #pragma unroll
+            for (int c = 0; c < 8; ++c) vr[c] = make_uint4(0, 0, 0, 0);
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.p_full[b]);
+      }
+      // ---- epilogue: O^T / l -> out, or a partial piece ------------------
+      ok = ok && mbar_wait(&sm.o_full, j & 1, p.err, abort_flag);
+      tc_fence_after();
+      float o[8];
+      tmem_ld8(tO, o);
+      tc_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.o_empty);
+      float lt[8];
+      #pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float sw = warp_sum(l[h]);
+        if (lane == 0) sm.red[warp][h] = sw;
+      }
+      named_barrier(kBarSoftmax, kSoftThreads);
+      #pragma unroll
+      for (int h = 0; h < G; ++h)
+        lt[h] = (sm.red[0][h] + sm.red[1][h]) + (sm.red[2][h] + sm.red[3][h]);
+      named_barrier(kBarSoftmax, kSoftThreads);  // sm.red is free again
+      const bool write = ok && in_range;
+      const int d = row;
+      const long long out_row = ((long long)pc.row * p.num_q_heads + (long long)pc.k * G) * kHeadDim;
+      if (write && pc.S == 1) {
+        #pragma unroll
+        for (int h = 0; h < G; ++h)
+          p.out[out_row + h * kHeadDim + d] = __float2bfloat16_rn(lt[h] > 0.f ? o[h] / lt[h] : 0.f);
+      } else if (write) {
+        // Partial piece: normalised output and (max, normaliser), then the
+        // last piece of the row-group to arrive merges all of them.
+        #pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const long long slot = (long long)pc.slot * G + h;
+          p.ws_o[slot * kHeadDim + d] = lt[h] > 0.f ? o[h] / lt[h] : 0.f;
+          if (d == 0) *reinterpret_cast<float2*>(p.ws_ml + slot * 2) = make_float2(m[h], lt[h]);
+        }
+        named_barrier(kBarSoftmax, kSoftThreads);
+        if (row == 0) {
+          __threadfence();
+          int* cnt = p.ws_cnt + (long long)pc.row * Hkv + pc.k;
+          const int old = atomicAdd(cnt, 1);
+          const int last = (old == pc.S - 1);
+          if (last) {
+            *cnt = 0;  // every piece has arrived: leave the counter at zero
+            __threadfence();
+          }
+          sm.is_last = last;
+        }
+        named_barrier(kBarSoftmax, kSoftThreads);
+        if (sm.is_last) {
+          #pragma unroll
+          for (int h = 0; h < G; ++h) {
+            float M = kNegBig, num = 0.f, den = 0.f;
+            #pragma unroll 4
+            for (int s2 = 0; s2 < pc.S; ++s2) {
+              const int slot = 2 * (pc.c0 + s2) + ((s2 == 0 && pc.odd0) ? 1 : 0);
+              const long long sl = (long long)slot * G + h;
+              const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.ws_ml + sl * 2));
+              const float ov = __ldcg(p.ws_o + sl * kHeadDim + d);
+              const float Mn = fmaxf(M, ml.x);
+              const float a = fast_exp2(M - Mn), w = fast_exp2(ml.x - Mn) * ml.y;
+              num = num * a + w * ov;
+              den = den * a + w;
+              M = Mn;
+            }
+            p.out[out_row + h * kHeadDim + d] = __float2bfloat16_rn(den > 0.f ? num / den : 0.f);
+          }
+        }
+        named_barrier(kBarSoftmax, kSoftThreads);  // sm.is_last is free again
+      }
+    }
+  }
+  // Every warp reaches this point (aborts only shorten the loops), so the
+  // allocating warp can always free TMEM.
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 5) tmem_dealloc(tmem, kTmemCols);
+}
+
+template <int G>
+cudaError_t launch_decode_tc_g(const DecodeTcLaunch& L, cudaStream_t stream) {
+  const size_t smem = sizeof(TcSmem) + 1024;  // + alignment slack
+  static unsigned long long configured = 0;   // bit per device ordinal
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (!(__atomic_load_n(&configured, __ATOMIC_ACQUIRE) & bit)) {
+    e = cudaFuncSetAttribute(decode_tc_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+    if (e != cudaSuccess) return e;
+    __atomic_fetch_or(&configured, bit, __ATOMIC_RELEASE);
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(L.grid);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = L.p.pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, decode_tc_kernel<G>, L.qmap, L.kmap, L.vmap, L.p);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+#if PKV_TC_TRACE
+cudaError_t decode_tc_trace(void* host, size_t bytes) {
+  return cudaMemcpyFromSymbol(host, g_tc_trace, bytes < sizeof(g_tc_trace) ? bytes : sizeof(g_tc_trace));
+}
+#endif
+
+cudaError_t launch_decode_tc(const DecodeTcLaunch& L, int group, cudaStream_t stream) {
+  switch (group) {
+    case 4: return launch_decode_tc_g<4>(L, stream);
+    case 5: return launch_decode_tc_g<5>(L, stream);
+    case 6: return launch_decode_tc_g<6>(L, stream);
+    case 7: return launch_decode_tc_g<7>(L, stream);
+    case 8: return launch_decode_tc_g<8>(L, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace pkv

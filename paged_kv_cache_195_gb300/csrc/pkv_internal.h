@@ -92,6 +92,17 @@ int decode_grid(int sm_count, int group);
 cudaError_t launch_decode(const DecodeParams& p, int group, int grid, cudaStream_t stream);
 cudaError_t launch_decode_e4m3(const DecodeParams& p, int group, int grid, cudaStream_t stream);
 
+// The same decode on tcgen05 tensor cores (bf16 pools, groups of 4..8).
+struct DecodeTcLaunch {
+  CUtensorMap qmap;  // q as [tokens][Hq][128], box (64, g, 1)
+  CUtensorMap kmap;  // k_pool as [blocks*Hkv*16][128], box (64, 16), 128-byte swizzle
+  CUtensorMap vmap;  // v_pool, same
+  DecodeParams p;
+  int grid;
+};
+
+cudaError_t launch_decode_tc(const DecodeTcLaunch& L, int group, cudaStream_t stream);
+
 // Quantising KV append into e4m3 pools.
 struct AppendFp8Params {
   const __nv_bfloat16* k_new;
@@ -144,6 +155,12 @@ int prefill_tokens_per_tile(int group);
 #endif
 #if PKV_TRACE
 cudaError_t decode_trace(void* host, size_t bytes);
+#endif
+#ifndef PKV_TC_TRACE
+#define PKV_TC_TRACE 0
+#endif
+#if PKV_TC_TRACE
+cudaError_t decode_tc_trace(void* host, size_t bytes);
 #endif
 
 // Sets the thread's pkv_last_error() message.

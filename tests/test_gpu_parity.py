@@ -136,7 +136,9 @@ def test_block_relabelling_is_bit_identical():
 
 def test_split_count_does_not_change_the_answer(monkeypatch):
     """Online-softmax merging is exact: any split count gives the same result
-    up to fp32 rounding (at most one bf16 ulp of the output)."""
+    up to fp32 rounding (at most one bf16 ulp of the output).  This holds for
+    the SIMT decode, whose probabilities stay in fp32."""
+    monkeypatch.setenv("PKV_DECODE_TC", "0")
     shape = wl.StepShape("splits", [3000, 1200, 17], [1, 3, 1], 32, 8, seed=5)
     inp = wl.make_step(shape, device="cuda")
     outs = []
@@ -148,6 +150,29 @@ def test_split_count_does_not_change_the_answer(monkeypatch):
         assert_close(to_f64(o.bfloat16()), ref, "split")
         ulp = torch.finfo(torch.bfloat16).eps * outs[-1].abs().clamp(min=2.0**-8)
         assert ((o - outs[-1]).abs() <= ulp + 1e-6).all()
+
+
+def test_split_count_tensor_core_decode(monkeypatch):
+    """The tensor-core decode feeds P to the MMA in bf16 (relative error at
+    most 2^-9 per weight), and where a piece starts decides which 128-key
+    tiles form; the merge itself is exact.  A softmax-weighted mean with every
+    weight perturbed by at most 2^-9 moves by at most 2 * 2^-9 * max_j |v_j - o|,
+    so two splits differ by at most twice that plus the output rounding."""
+    monkeypatch.setenv("PKV_DECODE_TC", "1")
+    shape = wl.StepShape("splits_tc", [3000, 1200, 17], [1, 3, 1], 32, 8, seed=5)
+    inp = wl.make_step(shape, device="cuda")
+    outs = []
+    for chunk in ("1", "3", "4096"):
+        monkeypatch.setenv("PKV_MIN_CHUNK", chunk)
+        outs.append(gpu_step(inp, append=False).float().clone())
+    h = host_copy(inp)
+    ref = oracle_full(h)
+    vmax = float(inp.v_pool.float().abs().max())
+    bound = 4 * 2.0 ** -9 * 2 * vmax
+    for o in outs:
+        assert_close(to_f64(o.bfloat16()), ref, "split")
+        ulp = torch.finfo(torch.bfloat16).eps * outs[-1].abs().clamp(min=2.0**-8)
+        assert ((o - outs[-1]).abs() <= 2 * ulp + bound).all()
 
 
 def test_two_chunks_equal_one_chunk():
