@@ -29,12 +29,16 @@
 // both accumulating in fp32 in TMEM.  Thread t of the four softmax warps owns
 // TMEM lane t: key t of S^T, dim t of O^T.
 //
-// Roles (192 threads): warps 0-3 softmax and epilogue, warp 4 plan and TMA
-// producer, one thread of warp 5 issues the MMAs.  S and P are double
-// buffered, so the QK^T of tile n+1 runs while the softmax works on tile n.
+// Roles (320 threads): warps 0-3 softmax, warp 4 plan and TMA producer, one
+// thread of warp 5 issues the MMAs, warps 6-9 the epilogue (normalise, write
+// the output or a partial piece, merge).  S, P and O^T are double buffered:
+// the softmax moves on to the next piece while the epilogue finishes the
+// previous one, so piece boundaries do not stall the K/V stream.
 // The running maximum is raised only when a score exceeds it by more than
 // 2^8 (a CTA-wide vote), so the common tile needs no cross-thread reduction;
 // O^T is rescaled in TMEM on the rare raise.
+#include <climits>
+
 #include "pkv_internal.h"
 #include "pkv_plan.cuh"
 #include "pkv_tc.cuh"
@@ -45,7 +49,7 @@ namespace {
 using plan::Piece;
 using plan::kEndRow;
 
-constexpr int kTcThreads = 192;
+constexpr int kTcThreads = 320;
 constexpr int kTile = 128;                 // keys per tile (MMA M of S^T, K of PV)
 constexpr int kBlkPerTile = kTile / kBlockSize;
 constexpr int kN = 16;                     // MMA N: the group's heads, padded
@@ -58,11 +62,13 @@ constexpr int kStages = PKV_TC_STAGES;     // K/V tile stages (64 KiB each)
 #ifndef PKV_TC_PV_FIRST
 #define PKV_TC_PV_FIRST 1
 #endif
-constexpr uint32_t kTmemCols = 64;         // S0: 0..15, S1: 16..31, O: 32..47
-constexpr uint32_t kColO = 32;
+constexpr uint32_t kTmemCols = 64;         // S0: 0..15, S1: 16..31, O0: 32..47, O1: 48..63
+constexpr uint32_t kColO = 32;             // O^T of piece j in columns kColO + (j & 1) * kN
 constexpr float kNegBig = -1.0e30f;
 constexpr float kLazyMargin = 8.f;         // log2 of the largest probability allowed
 constexpr int kBarSoftmax = 1;             // named barrier of the four softmax warps
+constexpr int kBarEpi = 2;                 // named barrier of the four epilogue warps
+constexpr int kPastPiece = INT_MIN;        // block-table slot past the piece (not read)
 
 // Debug-only per-tile timeline of CTA 0 (build with -DPKV_TC_TRACE=1):
 // %globaltimer at load issue, keys seen by the MMA warp, scores seen by the
@@ -83,12 +89,16 @@ struct __align__(1024) TcSmem {
   uint8_t v[kStages][2][kHalf];
   uint8_t q[2][2][kOpHalf];       // [piece buffer][d half]: Q rows (heads), rows >= g zero
   uint8_t pt[2][2][kOpHalf];      // [buffer][key half]: P^T as 16 rows (heads) x 64 keys
-  float red[4][kN];               // per-warp partial maxima / sums
+  float red[4][kN];               // per-warp partial maxima (softmax warps)
+  float st_l[2][4][kN];           // [piece buffer][softmax warp]: normaliser partial sums
+  float st_m[2][kN];              // [piece buffer]: running maxima (log2 domain)
+  Piece st_pc[2];                 // [piece buffer]: the piece, for the epilogue
   Piece pinfo[2];
   uint64_t q_full[2], q_empty[2];
   uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
   uint64_t s_full[2], s_free[2], p_full[2], p_free[2];
-  uint64_t o_full, o_empty;
+  uint64_t o_full[2], o_empty[2];  // O^T buffer complete / read by the epilogue
+  uint64_t st_full[2], st_empty[2];  // piece statistics published / consumed
   uint32_t tmem_base;
   int abort_flag;
   int is_last;
@@ -134,8 +144,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&sm.v_full[s], 1);
       mbar_init(&sm.kv_empty[s], 1);
     }
-    mbar_init(&sm.o_full, 1);
-    mbar_init(&sm.o_empty, 4);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.o_full[b], 1);    // tcgen05.commit after the piece's last PV
+      mbar_init(&sm.o_empty[b], 4);   // the epilogue warps have read O^T buffer b
+      mbar_init(&sm.st_full[b], 4);   // the softmax warps have published the statistics
+      mbar_init(&sm.st_empty[b], 4);  // the epilogue warps have read them
+    }
     sm.abort_flag = 0;
     fence_barrier_init();
   }
@@ -179,31 +193,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int oob_row = p.num_blocks * Hkv * kBlockSize;  // zero-filled by TMA
     plan::Walker wk;
     wk.start(p, rg, lane);
-    Piece pc;
+    // Block-table entries are loaded 32 blocks (four tiles) at a time and
+    // well before use -- the next group while a group is issued, the next
+    // piece's first group while a piece is issued -- and checked only when
+    // used, so the producer never waits on the table.
+    auto raw_entries = [&](const Piece& q, int x0) {
+      const int x = x0 + lane;
+      return x < q.nblk ? __ldg(p.block_tables + (long long)q.r * p.max_blocks + q.b0 + x)
+                        : kPastPiece;
+    };
+    Piece pc, pn;
+    bool have = wk.next(p, pc);
+    bool have_n = have && wk.next(p, pn);
+    int ent_first = have ? raw_entries(pc, 0) : kPastPiece;
+    int ent_first_n = have_n ? raw_entries(pn, 0) : kPastPiece;
     int j = 0, t = 0;  // piece and tile counters
     bool ok = true;
-    while (ok && !*abort_flag && wk.next(p, pc)) {
+    while (ok && have && !*abort_flag) {
       const int k = pc.k;
       const int ntile = plan::cdiv(pc.nblk, kBlkPerTile);
-      const int32_t* bt = p.block_tables + (long long)pc.r * p.max_blocks + pc.b0;
-      // Pool rows of the piece's blocks, 32 blocks (four tiles) per load, the
-      // next group fetched while the current one is being issued.
-      auto rows_of = [&](int x0) {
-        int rowc = oob_row;
-        const int x = x0 + lane;
-        if (x < pc.nblk) {
-          const int phys = __ldg(bt + x);
-          if ((unsigned)phys < (unsigned)p.num_blocks) rowc = (phys * Hkv + k) * kBlockSize;
-          else record_error(p.err, kErrBounds);
-        }
-        return rowc;
-      };
-      int rows_cur = rows_of(0);
-      int rows_nxt = ntile > 4 ? rows_of(32) : oob_row;
+      int ent_cur = ent_first;
+      int ent_nxt = ntile > 4 ? raw_entries(pc, 32) : kPastPiece;
       for (int tt = 0; tt < ntile; ++tt, ++t) {
         if (tt > 0 && (tt & 3) == 0) {
-          rows_cur = rows_nxt;
-          if (tt + 4 < ntile) rows_nxt = rows_of((tt + 4) * kBlkPerTile);
+          ent_cur = ent_nxt;
+          if (tt + 4 < ntile) ent_nxt = raw_entries(pc, (tt + 4) * kBlkPerTile);
         }
         const int st = t % kStages;
         if (t >= kStages &&
@@ -218,10 +232,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           mbar_arrive_expect_tx(&sm.v_full[st], 2u * kHalf);
         }
         __syncwarp();
-        // Lanes 0..15 each copy one (block, d half) of K and of V.
+        // Lanes 0..15 each copy one (block, d half) of K and of V; blocks
+        // past the piece are read at an out-of-range row (zero fill).
         const int bsel = lane & 7, hsel = (lane >> 3) & 1;
-        const int row = __shfl_sync(0xffffffffu, rows_cur, (tt & 3) * kBlkPerTile + bsel);
+        const int phys = __shfl_sync(0xffffffffu, ent_cur, (tt & 3) * kBlkPerTile + bsel);
         if (lane < 16) {
+          int row = oob_row;
+          if ((unsigned)phys < (unsigned)p.num_blocks) row = (phys * Hkv + k) * kBlockSize;
+          else if (phys != kPastPiece && hsel == 0) record_error(p.err, kErrBounds);
           tma_load_2d(sm.k[st][hsel] + bsel * 2048, &kmap, hsel * 64, row, &sm.k_full[st]);
           tma_load_2d(sm.v[st][hsel] + bsel * 2048, &vmap, hsel * 64, row, &sm.v_full[st]);
         }
@@ -244,6 +262,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
       ++j;
+      pc = pn;
+      have = have_n;
+      ent_first = ent_first_n;
+      have_n = have && wk.next(p, pn);
+      ent_first_n = have_n ? raw_entries(pn, 0) : kPastPiece;
     }
     // End marker: no more pieces for this CTA.
     const int ub = j & 1;
@@ -260,14 +283,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdescS = idesc_bf16_f32(kTile, kN, 0, 0);
       constexpr uint32_t kIdescO = idesc_bf16_f32(kHeadDim, kN, 1, 0);
-      const uint32_t tO = tmem + kColO;
       int t = 0;
       bool ok = true;
       auto pv = [&](int tt, bool first, int j) {
-        const int b = tt & 1, st = tt % kStages;
+        const int b = tt & 1, st = tt % kStages, ob = j & 1;
+        const uint32_t tO = tmem + kColO + ob * kN;
         ok = ok && mbar_wait(&sm.p_full[b], (tt >> 1) & 1, p.err, abort_flag);
         ok = ok && mbar_wait(&sm.v_full[st], (tt / kStages) & 1, p.err, abort_flag);
-        if (first && j > 0) ok = ok && mbar_wait(&sm.o_empty, (j - 1) & 1, p.err, abort_flag);
+        // O^T buffer ob was last read by the epilogue of piece j - 2.
+        if (first && j >= 2)
+          ok = ok && mbar_wait(&sm.o_empty[ob], ((j >> 1) - 1) & 1, p.err, abort_flag);
         if (!ok) return;
         TC_TR(3, tt);
         tc_fence_after();
@@ -321,191 +346,231 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (!PKV_TC_PV_FIRST && tt >= 1) pv(t - 1, tt == 1, j);
         }
         if (ok) pv(t - 1, ntile == 1, j);  // the piece's last tile
-        tc_commit(&sm.o_full);
+        tc_commit(&sm.o_full[ub]);
         tc_commit(&sm.q_empty[ub]);
       }
     }
     __syncwarp();
   } else {
-    // =================== softmax + epilogue (warps 0-3) ===================
-    const int row = tid;  // TMEM lane: key `row` of a tile, dim `row` of O^T
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    const uint32_t tO = tmem + lane_off + kColO;
-    constexpr int kSoftThreads = 128;
-    int t = 0;
-    bool ok = true;
-    for (int j = 0; ok; ++j) {
-      const int ub = j & 1;
-      ok = mbar_wait(&sm.q_full[ub], (j >> 1) & 1, p.err, abort_flag);
-      const Piece pc = sm.pinfo[ub];
-      if (!ok || pc.row == kEndRow) break;
-      const bool in_range = pc.row >= 0 && pc.row < p.num_q_tokens && pc.k >= 0 &&
-                            pc.k < Hkv && pc.nblk >= 1 && pc.S >= 1 && pc.c0 >= 0 &&
-                            2 * (pc.c0 + pc.S) <= p.num_slots && pc.slot >= 0 &&
-                            pc.slot < p.num_slots;
-      const int ntile = plan::cdiv(pc.nblk, kBlkPerTile);
-      float m[G], l[G];
-      #pragma unroll
-      for (int h = 0; h < G; ++h) {
-        m[h] = kNegBig;
-        l[h] = 0.f;
-      }
-      for (int tt = 0; tt < ntile; ++tt, ++t) {
-        const int b = t & 1, st = t % kStages;
-        ok = ok && mbar_wait(&sm.s_full[b], (t >> 1) & 1, p.err, abort_flag);
-        if (row == 0) TC_TR(2, t);
-        tc_fence_after();
-        float s[8];
-        tmem_ld8(tmem + lane_off + b * kN, s);
-        tc_wait_ld();
-        // Key `row` of this tile: block x of the tile, offset row % 16.
-        const int x = tt * kBlkPerTile + (row >> 4);
-        const int pos = (pc.b0 + x) * kBlockSize + (row & 15);
-        const bool valid = ok && x < pc.nblk && pos < pc.limit;
-        bool over = false;
+    if (warp < 4) {
+      // ========================= softmax (warps 0-3) ========================
+      const int row = tid;  // TMEM lane: key `row` of a tile
+      const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+      constexpr int kSoftThreads = 128;
+      int t = 0;
+      int j = 0;
+      for (;; ++j) {
+        const int ub = j & 1;
+        const bool got = mbar_wait(&sm.q_full[ub], (j >> 1) & 1, p.err, abort_flag);
+        const Piece pc = sm.pinfo[ub];
+        // Agree before any barrier: a wait that gave up (abort) stops everyone.
+        if (barrier_or(kBarSoftmax, kSoftThreads, !got || pc.row == kEndRow)) break;
+        bool ok = true;
+        const uint32_t tO = tmem + lane_off + kColO + ub * kN;
+        const int ntile = plan::cdiv(pc.nblk, kBlkPerTile);
+        float m[G], l[G];
         #pragma unroll
         for (int h = 0; h < G; ++h) {
-          s[h] = valid ? s[h] * p.scale_log2 : -INFINITY;
-          over |= s[h] > m[h] + kLazyMargin;
+          m[h] = kNegBig;
+          l[h] = 0.f;
         }
-        // S buffer b has been read: the MMA may overwrite it (tile t + 2).
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.s_free[b]);
-        if (barrier_or(kBarSoftmax, kSoftThreads, over)) {
-          // Raise the running maxima to this tile's; O^T and l move with them.
+        for (int tt = 0; tt < ntile; ++tt, ++t) {
+          const int b = t & 1, st = t % kStages;
+          ok = ok && mbar_wait(&sm.s_full[b], (t >> 1) & 1, p.err, abort_flag);
+          if (row == 0) TC_TR(2, t);
+          tc_fence_after();
+          float s[8];
+          tmem_ld8(tmem + lane_off + b * kN, s);
+          tc_wait_ld();
+          // Key `row` of this tile: block x of the tile, offset row % 16.
+          const int x = tt * kBlkPerTile + (row >> 4);
+          const int pos = (pc.b0 + x) * kBlockSize + (row & 15);
+          const bool valid = ok && x < pc.nblk && pos < pc.limit;
+          bool over = false;
           #pragma unroll
           for (int h = 0; h < G; ++h) {
-            const float mx = warp_max(s[h]);
-            if (lane == 0) sm.red[warp][h] = mx;
+            s[h] = valid ? s[h] * p.scale_log2 : -INFINITY;
+            over |= s[h] > m[h] + kLazyMargin;
           }
-          named_barrier(kBarSoftmax, kSoftThreads);
-          float alpha[8];
-          bool grow = false;
-          #pragma unroll
-          for (int h = 0; h < G; ++h) {
-            const float mx = fmaxf(fmaxf(sm.red[0][h], sm.red[1][h]),
-                                   fmaxf(sm.red[2][h], sm.red[3][h]));
-            const float mn = fmaxf(m[h], mx);
-            alpha[h] = fast_exp2(m[h] - mn);
-            grow |= mn != m[h];
-            m[h] = mn;
-            l[h] *= alpha[h];
-          }
-          if (tt > 0 && grow) {
-            // O^T must hold the previous tile's PV before it is rescaled.
-            ok = ok && mbar_wait(&sm.p_free[(t - 1) & 1], ((t - 1) >> 1) & 1, p.err, abort_flag);
-            tc_fence_after();
-            float o[8];
-            tmem_ld8(tO, o);
-            tc_wait_ld();
+          // S buffer b has been read: the MMA may overwrite it (tile t + 2).
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.s_free[b]);
+          if (barrier_or(kBarSoftmax, kSoftThreads, over)) {
+            // Raise the running maxima to this tile's; O^T and l move with them.
             #pragma unroll
-            for (int h = 0; h < G; ++h) o[h] *= alpha[h];
-            tmem_st8(tO, o);
-            tc_wait_st();
-          }
-          // sm.red is read by every softmax thread before its next write.
-          named_barrier(kBarSoftmax, kSoftThreads);
-        }
-        // P^T buffer b was last read by the PV of tile t - 2.
-        if (t >= 2) ok = ok && mbar_wait(&sm.p_free[b], ((t >> 1) - 1) & 1, p.err, abort_flag);
-        // p = exp2(s - m) in bf16; P^T row h holds head h, keys contiguous,
-        // 128-byte swizzle.  The normaliser sums the rounded values the MMA
-        // will use.
-        uint8_t* prow = sm.pt[b][row >> 6];
-        const int kc = (row & 63) >> 3;
-        #pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const __nv_bfloat16 pb = __float2bfloat16_rn(fast_exp2(s[h] - m[h]));
-          l[h] += __bfloat162float(pb);
-          *reinterpret_cast<__nv_bfloat16*>(prow + (h >> 3) * 1024 + (h & 7) * 128 +
-                                            ((kc ^ (h & 7)) * 16) + (row & 7) * 2) = pb;
-        }
-        // Keys past the request's end inside its last block may hold anything
-        // (even NaN): zero those V rows so that 0 * V stays 0 in the MMA.
-        if (x < pc.nblk && pos >= pc.L) {
-          ok = ok && mbar_wait(&sm.v_full[st], (t / kStages) & 1, p.err, abort_flag);
-          #pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            uint4* vr = reinterpret_cast<uint4*>(sm.v[st][hf] + (row >> 3) * 1024 + (row & 7) * 128);
-            #pragma unroll
-            for (int c = 0; c < 8; ++c) vr[c] = make_uint4(0, 0, 0, 0);
-          }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.p_full[b]);
-      }
-      // ---- epilogue: O^T / l -> out, or a partial piece ------------------
-      ok = ok && mbar_wait(&sm.o_full, j & 1, p.err, abort_flag);
-      tc_fence_after();
-      float o[8];
-      tmem_ld8(tO, o);
-      tc_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.o_empty);
-      float lt[8];
-      #pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float sw = warp_sum(l[h]);
-        if (lane == 0) sm.red[warp][h] = sw;
-      }
-      named_barrier(kBarSoftmax, kSoftThreads);
-      #pragma unroll
-      for (int h = 0; h < G; ++h)
-        lt[h] = (sm.red[0][h] + sm.red[1][h]) + (sm.red[2][h] + sm.red[3][h]);
-      named_barrier(kBarSoftmax, kSoftThreads);  // sm.red is free again
-      const bool write = ok && in_range;
-      const int d = row;
-      const long long out_row = ((long long)pc.row * p.num_q_heads + (long long)pc.k * G) * kHeadDim;
-      if (write && pc.S == 1) {
-        #pragma unroll
-        for (int h = 0; h < G; ++h)
-          p.out[out_row + h * kHeadDim + d] = __float2bfloat16_rn(lt[h] > 0.f ? o[h] / lt[h] : 0.f);
-      } else if (write) {
-        // Partial piece: normalised output and (max, normaliser), then the
-        // last piece of the row-group to arrive merges all of them.
-        #pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const long long slot = (long long)pc.slot * G + h;
-          p.ws_o[slot * kHeadDim + d] = lt[h] > 0.f ? o[h] / lt[h] : 0.f;
-          if (d == 0) *reinterpret_cast<float2*>(p.ws_ml + slot * 2) = make_float2(m[h], lt[h]);
-        }
-        named_barrier(kBarSoftmax, kSoftThreads);
-        if (row == 0) {
-          __threadfence();
-          int* cnt = p.ws_cnt + (long long)pc.row * Hkv + pc.k;
-          const int old = atomicAdd(cnt, 1);
-          const int last = (old == pc.S - 1);
-          if (last) {
-            *cnt = 0;  // every piece has arrived: leave the counter at zero
-            __threadfence();
-          }
-          sm.is_last = last;
-        }
-        named_barrier(kBarSoftmax, kSoftThreads);
-        if (sm.is_last) {
-          #pragma unroll
-          for (int h = 0; h < G; ++h) {
-            float M = kNegBig, num = 0.f, den = 0.f;
-            #pragma unroll 4
-            for (int s2 = 0; s2 < pc.S; ++s2) {
-              const int slot = 2 * (pc.c0 + s2) + ((s2 == 0 && pc.odd0) ? 1 : 0);
-              const long long sl = (long long)slot * G + h;
-              const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.ws_ml + sl * 2));
-              const float ov = __ldcg(p.ws_o + sl * kHeadDim + d);
-              const float Mn = fmaxf(M, ml.x);
-              const float a = fast_exp2(M - Mn), w = fast_exp2(ml.x - Mn) * ml.y;
-              num = num * a + w * ov;
-              den = den * a + w;
-              M = Mn;
+            for (int h = 0; h < G; ++h) {
+              const float mx = warp_max(s[h]);
+              if (lane == 0) sm.red[warp][h] = mx;
             }
-            p.out[out_row + h * kHeadDim + d] = __float2bfloat16_rn(den > 0.f ? num / den : 0.f);
+            named_barrier(kBarSoftmax, kSoftThreads);
+            float alpha[8];
+            bool grow = false;
+            #pragma unroll
+            for (int h = 0; h < G; ++h) {
+              const float mx = fmaxf(fmaxf(sm.red[0][h], sm.red[1][h]),
+                                     fmaxf(sm.red[2][h], sm.red[3][h]));
+              const float mn = fmaxf(m[h], mx);
+              alpha[h] = fast_exp2(m[h] - mn);
+              grow |= mn != m[h];
+              m[h] = mn;
+              l[h] *= alpha[h];
+            }
+            if (tt > 0 && grow) {
+              // O^T must hold the previous tile's PV before it is rescaled.
+              ok = ok && mbar_wait(&sm.p_free[(t - 1) & 1], ((t - 1) >> 1) & 1, p.err, abort_flag);
+              tc_fence_after();
+              float o[8];
+              tmem_ld8(tO, o);
+              tc_wait_ld();
+              #pragma unroll
+              for (int h = 0; h < G; ++h) o[h] *= alpha[h];
+              tmem_st8(tO, o);
+              tc_wait_st();
+            }
+            // sm.red is read by every softmax thread before its next write.
+            named_barrier(kBarSoftmax, kSoftThreads);
           }
+          // P^T buffer b was last read by the PV of tile t - 2.
+          if (t >= 2) ok = ok && mbar_wait(&sm.p_free[b], ((t >> 1) - 1) & 1, p.err, abort_flag);
+          // p = exp2(s - m) in bf16; P^T row h holds head h, keys contiguous,
+          // 128-byte swizzle.  The normaliser sums the rounded values the MMA
+          // will use.
+          uint8_t* prow = sm.pt[b][row >> 6];
+          const int kc = (row & 63) >> 3;
+          #pragma unroll
+          for (int h = 0; h < G; ++h) {
+            const __nv_bfloat16 pb = __float2bfloat16_rn(fast_exp2(s[h] - m[h]));
+            l[h] += __bfloat162float(pb);
+            *reinterpret_cast<__nv_bfloat16*>(prow + (h >> 3) * 1024 + (h & 7) * 128 +
+                                              ((kc ^ (h & 7)) * 16) + (row & 7) * 2) = pb;
+          }
+          // Keys past the request's end inside its last block may hold anything
+          // (even NaN): zero those V rows so that 0 * V stays 0 in the MMA.
+          if (x < pc.nblk && pos >= pc.L) {
+            ok = ok && mbar_wait(&sm.v_full[st], (t / kStages) & 1, p.err, abort_flag);
+            #pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+              uint4* vr = reinterpret_cast<uint4*>(sm.v[st][hf] + (row >> 3) * 1024 + (row & 7) * 128);
+              #pragma unroll
+              for (int c = 0; c < 8; ++c) vr[c] = make_uint4(0, 0, 0, 0);
+            }
+          }
+          fence_proxy_async_smem();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.p_full[b]);
         }
-        named_barrier(kBarSoftmax, kSoftThreads);  // sm.is_last is free again
+        // ---- hand the piece to the epilogue: maxima, normaliser partials ---
+        if (j >= 2) mbar_wait(&sm.st_empty[ub], ((j >> 1) - 1) & 1, p.err, abort_flag);
+        #pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float sw = warp_sum(l[h]);
+          if (lane == 0) sm.st_l[ub][warp][h] = sw;
+        }
+        if (warp == 0 && lane == 0) {
+          #pragma unroll
+          for (int h = 0; h < G; ++h) sm.st_m[ub][h] = m[h];
+          sm.st_pc[ub] = pc;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.st_full[ub]);
+      }
+      // End marker for the epilogue.
+      {
+        const int ub = j & 1;
+        if (j >= 2) mbar_wait(&sm.st_empty[ub], ((j >> 1) - 1) & 1, p.err, abort_flag);
+        if (warp == 0 && lane == 0) sm.st_pc[ub].row = kEndRow;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.st_full[ub]);
+      }
+    } else {
+      // ======================== epilogue (warps 6-9) ========================
+      // Warp w reaches TMEM lanes 32 (w % 4) .. +31: dims d of O^T.
+      const int d = (warp & 3) * 32 + lane;
+      const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+      constexpr int kEpiThreads = 128;
+      for (int j = 0;; ++j) {
+        const int ob = j & 1;
+        const bool got = mbar_wait(&sm.st_full[ob], (j >> 1) & 1, p.err, abort_flag);
+        const Piece pc = sm.st_pc[ob];
+        if (barrier_or(kBarEpi, kEpiThreads, !got || pc.row == kEndRow)) break;
+        float m[8], lt[8];
+        #pragma unroll
+        for (int h = 0; h < G; ++h) {
+          m[h] = sm.st_m[ob][h];
+          lt[h] = (sm.st_l[ob][0][h] + sm.st_l[ob][1][h]) + (sm.st_l[ob][2][h] + sm.st_l[ob][3][h]);
+        }
+        const bool ok = mbar_wait(&sm.o_full[ob], (j >> 1) & 1, p.err, abort_flag);
+        tc_fence_after();
+        float o[8];
+        tmem_ld8(tmem + lane_off + kColO + ob * kN, o);
+        tc_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&sm.o_empty[ob]);
+          mbar_arrive(&sm.st_empty[ob]);
+        }
+        const bool in_range = pc.row >= 0 && pc.row < p.num_q_tokens && pc.k >= 0 &&
+                              pc.k < Hkv && pc.nblk >= 1 && pc.S >= 1 && pc.c0 >= 0 &&
+                              2 * (pc.c0 + pc.S) <= p.num_slots && pc.slot >= 0 &&
+                              pc.slot < p.num_slots;
+        const long long out_row = ((long long)pc.row * p.num_q_heads + (long long)pc.k * G) * kHeadDim;
+        if (in_range && pc.S == 1) {
+          if (ok) {
+            #pragma unroll
+            for (int h = 0; h < G; ++h)
+              p.out[out_row + h * kHeadDim + d] =
+                  __float2bfloat16_rn(lt[h] > 0.f ? o[h] / lt[h] : 0.f);
+          }
+        } else if (in_range) {
+          // Partial piece: normalised output and (max, normaliser), then the
+          // last piece of the row-group to arrive merges all of them.  Every
+          // epilogue thread takes this branch (pc is shared), so the barriers
+          // below are uniform.
+          if (ok) {
+            #pragma unroll
+            for (int h = 0; h < G; ++h) {
+              const long long slot = (long long)pc.slot * G + h;
+              p.ws_o[slot * kHeadDim + d] = lt[h] > 0.f ? o[h] / lt[h] : 0.f;
+              if (d == 0) *reinterpret_cast<float2*>(p.ws_ml + slot * 2) = make_float2(m[h], lt[h]);
+            }
+          }
+          named_barrier(kBarEpi, kEpiThreads);
+          if (d == 0) {
+            __threadfence();
+            int* cnt = p.ws_cnt + (long long)pc.row * Hkv + pc.k;
+            const int old = atomicAdd(cnt, 1);
+            const int last = (old == pc.S - 1);
+            if (last) {
+              *cnt = 0;  // every piece has arrived: leave the counter at zero
+              __threadfence();
+            }
+            sm.is_last = last;
+          }
+          named_barrier(kBarEpi, kEpiThreads);
+          if (sm.is_last) {
+            #pragma unroll
+            for (int h = 0; h < G; ++h) {
+              float M = kNegBig, num = 0.f, den = 0.f;
+              #pragma unroll 4
+              for (int s2 = 0; s2 < pc.S; ++s2) {
+                const int slot = 2 * (pc.c0 + s2) + ((s2 == 0 && pc.odd0) ? 1 : 0);
+                const long long sl = (long long)slot * G + h;
+                const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.ws_ml + sl * 2));
+                const float ov = __ldcg(p.ws_o + sl * kHeadDim + d);
+                const float Mn = fmaxf(M, ml.x);
+                const float a = fast_exp2(M - Mn), w = fast_exp2(ml.x - Mn) * ml.y;
+                num = num * a + w * ov;
+                den = den * a + w;
+                M = Mn;
+              }
+              p.out[out_row + h * kHeadDim + d] = __float2bfloat16_rn(den > 0.f ? num / den : 0.f);
+            }
+          }
+          named_barrier(kBarEpi, kEpiThreads);  // sm.is_last is free again
+        }
       }
     }
   }
