@@ -198,6 +198,48 @@ int pkv_attention_fp8kv(const void *q, const void *k_pool, const void *v_pool,
                         const pkv_dims *dims, void *workspace, size_t workspace_bytes,
                         cudaStream_t stream);
 
+/*
+ * Bytes of workspace pkv_attention_cascade needs for these dims: the
+ * pkv_attention workspace (same head, initialised the same way with
+ * pkv_workspace_init) plus a partial state per (query token, query head) and
+ * an int per request.
+ */
+size_t pkv_cascade_workspace_size(const pkv_dims *dims);
+
+/*
+ * pkv_attention for a batch whose requests share prompts (shared-prefix,
+ * "cascade" attention).  The result is pkv_attention's; the shared blocks
+ * are read once per batch instead of once per request.
+ * Groups (device arrays, num_groups entries): group g is the requests
+ * group_first_req[g] .. group_first_req[g] + group_num_reqs[g] - 1 (a
+ * contiguous run; groups must not overlap), whose first
+ * group_prefix_blocks[g] block-table entries name the same physical blocks.
+ * Every member must have all of its query tokens after the shared prefix
+ * (L_r - q_r >= 16 * group_prefix_blocks[g]); a member that does not reads
+ * its whole context itself.  Entries naming requests outside [0, num_reqs)
+ * are skipped and reported as PKV_ERR_DEVICE_BOUNDS.
+ * How: one pass attends every member's query rows to the group's shared
+ * blocks at once on the tensor cores (rows = the members' (token, head)
+ * pairs) and keeps a partial state per row; the decode then reads each row's
+ * remaining blocks and merges the two by log-sum-exp.  Every row runs in the
+ * decode path (no separate prefill kernel).  Sharing applies when the step
+ * runs the tensor-core decode (bf16 pools, 4..8 query heads per KV head);
+ * otherwise the call computes the same result without it.
+ * workspace: caller-owned, at least pkv_cascade_workspace_size(dims) bytes.
+ * Source: The Serving Playbook, "The tree changes what the scheduler should
+ * do" (requests batched with a shared prefix read the same KV blocks, which
+ * can then be fetched from HBM once per batch); LLM 7 - Efficient LLM
+ * Serving, sec. 3 "Sharing and Preemption" (many block tables point at one
+ * set of physical prefix blocks); sec. 2 "Online Softmax Makes Tiling
+ * Possible" (merging partial softmax states).
+ */
+int pkv_attention_cascade(const void *q, const void *k_pool, const void *v_pool,
+                          const int32_t *block_tables, const int32_t *seq_lens,
+                          const int32_t *query_start_loc, const int32_t *group_first_req,
+                          const int32_t *group_num_reqs, const int32_t *group_prefix_blocks,
+                          int32_t num_groups, float scale, void *out, const pkv_dims *dims,
+                          void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* Size of the static scratch array behind pkv_attention_noalloc (4 MiB). */
 #define PKV_NOALLOC_SCRATCH_BYTES (4 * 1024 * 1024)
 

@@ -28,7 +28,7 @@ PKV_ERR_TIMEOUT = -6
 EXPORTED = ("pkv_append", "pkv_attention", "pkv_attention_workspace_size",
             "pkv_workspace_init", "pkv_last_error", "pkv_get_device_error",
             "pkv_attention_noalloc", "pkv_copy_blocks", "pkv_append_fp8",
-            "pkv_attention_fp8kv")
+            "pkv_attention_fp8kv", "pkv_cascade_workspace_size", "pkv_attention_cascade")
 
 
 class PagedKVError(RuntimeError):
@@ -82,6 +82,11 @@ def load_library(path: str = LIB_PATH):
         lib.pkv_attention_fp8kv.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, dp,
                                             vp, sz, vp]
         lib.pkv_attention_fp8kv.restype = ctypes.c_int
+        lib.pkv_cascade_workspace_size.argtypes = [dp]
+        lib.pkv_cascade_workspace_size.restype = sz
+        lib.pkv_attention_cascade.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32,
+                                              ctypes.c_float, vp, dp, vp, sz, vp]
+        lib.pkv_attention_cascade.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -269,6 +274,65 @@ def pkv_attention_fp8kv(q, k_pool, v_pool, k_scale, v_scale, block_tables, seq_l
         ctypes.c_void_p(seq_lens.data_ptr()), ctypes.c_void_p(query_start_loc.data_ptr()),
         ctypes.c_float(scale), ctypes.c_void_p(out.data_ptr()), ctypes.byref(dims),
         ctypes.c_void_p(ws_ptr), ws_bytes, ctypes.c_void_p(_stream(stream, q.device))))
+    return out
+
+
+class CascadeWorkspace(Workspace):
+    """A zero-initialised device workspace for pkv_attention_cascade."""
+
+    def __init__(self, dims: Dims, device="cuda"):
+        self.nbytes = int(load_library().pkv_cascade_workspace_size(ctypes.byref(dims)))
+        if self.nbytes == 0:
+            raise PagedKVError(PKV_ERR_INVALID, pkv_last_error() or "bad dims")
+        self.buf = torch.zeros(self.nbytes + 256, dtype=torch.uint8, device=device)
+        off = (-self.buf.data_ptr()) % 256
+        self.ptr = self.buf.data_ptr() + off
+        self.counter_dims = (dims.num_q_tokens, dims.num_kv_heads)
+
+
+def pkv_attention_cascade(q, k_pool, v_pool, block_tables, seq_lens, query_start_loc,
+                          group_first_req, group_num_reqs, group_prefix_blocks, scale,
+                          out=None, workspace: CascadeWorkspace | None = None, stream=None):
+    """pkv_attention for requests that share prompts: group g is the requests
+    group_first_req[g] .. + group_num_reqs[g] - 1, whose first
+    group_prefix_blocks[g] table entries are the same physical blocks (int32
+    CUDA tensors).  The shared blocks are read once per batch."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_pool, "k_pool", torch.bfloat16, 4)
+    _need(v_pool, "v_pool", torch.bfloat16, 4)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    _need(query_start_loc, "query_start_loc", torch.int32, 1)
+    for t, name in ((group_first_req, "group_first_req"), (group_num_reqs, "group_num_reqs"),
+                    (group_prefix_blocks, "group_prefix_blocks")):
+        _need(t, name, torch.int32, 1)
+    G = group_first_req.shape[0]
+    if group_num_reqs.shape[0] != G or group_prefix_blocks.shape[0] != G:
+        raise ValueError("group arrays disagree on the group count")
+    R = seq_lens.shape[0]
+    if query_start_loc.shape[0] != R + 1 or block_tables.shape[0] != R:
+        raise ValueError("seq_lens, query_start_loc and block_tables disagree on num_reqs")
+    if v_pool.shape != k_pool.shape or k_pool.shape[3] != q.shape[2]:
+        raise ValueError("pool / q shape mismatch")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need(out, "out", torch.bfloat16, 3)
+        if out.shape != q.shape:
+            raise ValueError("out must have q's shape")
+    dims = make_dims(tuple(q.shape), tuple(k_pool.shape), R, block_tables.shape[1])
+    if workspace is None:
+        workspace = CascadeWorkspace(dims, device=q.device)
+    if workspace.counter_dims != (dims.num_q_tokens, dims.num_kv_heads):
+        pkv_workspace_init(workspace, dims, stream)
+    _check(load_library().pkv_attention_cascade(
+        ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k_pool.data_ptr()),
+        ctypes.c_void_p(v_pool.data_ptr()), ctypes.c_void_p(block_tables.data_ptr()),
+        ctypes.c_void_p(seq_lens.data_ptr()), ctypes.c_void_p(query_start_loc.data_ptr()),
+        ctypes.c_void_p(group_first_req.data_ptr()), ctypes.c_void_p(group_num_reqs.data_ptr()),
+        ctypes.c_void_p(group_prefix_blocks.data_ptr()), G, ctypes.c_float(scale),
+        ctypes.c_void_p(out.data_ptr()), ctypes.byref(dims), ctypes.c_void_p(workspace.ptr),
+        workspace.nbytes, ctypes.c_void_p(_stream(stream, q.device))))
     return out
 
 

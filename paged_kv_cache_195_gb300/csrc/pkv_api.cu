@@ -301,11 +301,37 @@ int pkv_workspace_init(void* workspace, size_t workspace_bytes, const pkv_dims* 
 
 namespace {
 
-// Both attention entry points: bf16 pools (k_scale == nullptr) or e4m3 pools.
+// Sharing groups of a cascade call (device arrays).
+struct CascadeArgs {
+  const int32_t* grp_first;
+  const int32_t* grp_count;
+  const int32_t* grp_blocks;
+  int num_groups;
+};
+
+// Regions a cascade call adds after the attention workspace.
+struct CascadeLayout {
+  size_t pre_o, pre_ml, first_block, total;
+};
+
+CascadeLayout cascade_layout(const pkv::WorkspaceLayout& w, const pkv_dims* d) {
+  auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  const size_t rows = (size_t)d->num_q_tokens * d->num_q_heads;
+  CascadeLayout c;
+  c.pre_o = up(w.total);
+  c.pre_ml = c.pre_o + up(rows * pkv::kHeadDim * sizeof(float));
+  c.first_block = c.pre_ml + up(rows * 2 * sizeof(float));
+  c.total = c.first_block + up((size_t)d->num_reqs * sizeof(int32_t));
+  return c;
+}
+
+// The attention entry points: bf16 pools (k_scale == nullptr) or e4m3 pools,
+// optionally with shared-prefix groups.
 int attention_impl(const void* q, const void* k_pool, const void* v_pool, const float* k_scale,
                    const float* v_scale, const int32_t* block_tables, const int32_t* seq_lens,
                    const int32_t* query_start_loc, float scale, void* out, const pkv_dims* dims,
-                   void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+                   void* workspace, size_t workspace_bytes, cudaStream_t stream,
+                   const CascadeArgs* cas = nullptr) {
   g_last_error[0] = '\0';
   const bool fp8 = k_scale != nullptr;
   int rc = check_dims(dims, true);
@@ -319,6 +345,15 @@ int attention_impl(const void* q, const void* k_pool, const void* v_pool, const 
   DeviceState* st = device_state();
   if (!st) return PKV_ERR_CUDA;
   const pkv::WorkspaceLayout w = layout_for(dims, st->sm_count);
+  const CascadeLayout cl = cascade_layout(w, dims);
+  if (cas) {
+    if (cas->num_groups < 0) return fail(PKV_ERR_INVALID, "num_groups < 0");
+    if (cas->num_groups > 0 && (!cas->grp_first || !cas->grp_count || !cas->grp_blocks))
+      return fail(PKV_ERR_INVALID, "NULL group array");
+    if (workspace == nullptr || workspace_bytes < cl.total)
+      return fail(PKV_ERR_WORKSPACE, "cascade workspace %zu bytes, need %zu (caller-owned)",
+                  workspace_bytes, cl.total);
+  }
   if (workspace == nullptr) {
     std::lock_guard<std::mutex> lock(g_mutex);
     if (st->own_ws_bytes < w.total) {
@@ -395,6 +430,64 @@ int attention_impl(const void* q, const void* k_pool, const void* v_pool, const 
   // work comparable to its HBM time; those run on the tensor cores.
   const bool use_tc = !fp8 && group >= 4 && env_int("PKV_DECODE_TC", 1) != 0;
   cudaError_t e;
+  // Shared prefixes are read once by the prefix pass when the tensor-core
+  // decode serves the step; otherwise every row reads its whole context (the
+  // same result, without the sharing).
+  const bool cascade = cas && cas->num_groups > 0 && use_tc;
+  if (cascade) {
+    int32_t* first_block = reinterpret_cast<int32_t*>(ws + cl.first_block);
+    e = cudaMemsetAsync(first_block, 0, (size_t)dims->num_reqs * sizeof(int32_t), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(first blocks)");
+    pkv::CascadePrepParams cp{};
+    cp.grp_first = cas->grp_first;
+    cp.grp_count = cas->grp_count;
+    cp.grp_blocks = cas->grp_blocks;
+    cp.first_block = first_block;
+    cp.err = st->err;
+    cp.num_groups = cas->num_groups;
+    cp.num_reqs = dims->num_reqs;
+    cp.max_blocks = dims->max_blocks_per_req;
+    cp.pdl = p.pdl;
+    e = pkv::launch_cascade_prep(cp, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cascade set-up launch");
+    // Prefix pass: every member's rows against the group's shared blocks.
+    pkv::PrefillLaunch L{};
+    rc = encode_q_map(&L.qmap, q, dims, group, pkv::prefill_tokens_per_tile(group));
+    if (rc == PKV_OK) rc = encode_pool_map(&L.kmap, k_pool, dims);
+    if (rc == PKV_OK) rc = encode_pool_map(&L.vmap, v_pool, dims);
+    if (rc != PKV_OK) return rc;
+    L.p.block_tables = block_tables;
+    L.p.seq_lens = seq_lens;
+    L.p.qsl = query_start_loc;
+    L.p.out = p.out;
+    L.p.err = st->err;
+    L.p.num_reqs = dims->num_reqs;
+    L.p.num_q_tokens = dims->num_q_tokens;
+    L.p.num_q_heads = dims->num_q_heads;
+    L.p.num_kv_heads = dims->num_kv_heads;
+    L.p.num_blocks = dims->num_blocks;
+    L.p.max_blocks = dims->max_blocks_per_req;
+    L.p.scale_log2 = p.scale_log2;
+    L.p.prefill_min_q = 1;
+    L.p.pdl = p.pdl;
+    L.p.prefix_mode = 1;
+    L.p.grp_first = cas->grp_first;
+    L.p.grp_count = cas->grp_count;
+    L.p.grp_blocks = cas->grp_blocks;
+    L.p.num_groups = cas->num_groups;
+    L.p.pre_o = reinterpret_cast<float*>(ws + cl.pre_o);
+    L.p.pre_ml = reinterpret_cast<float*>(ws + cl.pre_ml);
+    L.grid = st->sm_count;
+    e = pkv::launch_prefill(L, group, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "prefix pass launch");
+    // Decode of every row from its first unshared block, merging the prefix.
+    p.first_block = first_block;
+    p.pre_o = L.p.pre_o;
+    p.pre_ml = L.p.pre_ml;
+    p.prefill_min_q = 0x7fffffff;
+    p.early_plan = 0;  // first_block comes from the set-up kernel, two launches back
+  }
+  const bool do_prefill = run_prefill && !cascade;
   if (use_tc) {
     pkv::DecodeTcLaunch T{};
     rc = encode_q_map(&T.qmap, q, dims, group, 1);
@@ -408,7 +501,7 @@ int attention_impl(const void* q, const void* k_pool, const void* v_pool, const 
     e = pkv::launch_decode(p, group, grid, stream);
   }
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-  if (run_prefill) {
+  if (do_prefill) {
     pkv::PrefillLaunch L{};
     rc = encode_q_map(&L.qmap, q, dims, group, pkv::prefill_tokens_per_tile(group));
     if (rc == PKV_OK) rc = encode_pool_map(&L.kmap, k_pool, dims);
@@ -445,6 +538,25 @@ int pkv_attention(const void* q, const void* k_pool, const void* v_pool,
                   void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   return attention_impl(q, k_pool, v_pool, nullptr, nullptr, block_tables, seq_lens,
                         query_start_loc, scale, out, dims, workspace, workspace_bytes, stream);
+}
+
+size_t pkv_cascade_workspace_size(const pkv_dims* dims) {
+  if (check_dims(dims, true) != PKV_OK) return 0;
+  DeviceState* st = device_state();
+  if (!st) return 0;
+  return cascade_layout(layout_for(dims, st->sm_count), dims).total;
+}
+
+int pkv_attention_cascade(const void* q, const void* k_pool, const void* v_pool,
+                          const int32_t* block_tables, const int32_t* seq_lens,
+                          const int32_t* query_start_loc, const int32_t* group_first_req,
+                          const int32_t* group_num_reqs, const int32_t* group_prefix_blocks,
+                          int32_t num_groups, float scale, void* out, const pkv_dims* dims,
+                          void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  const CascadeArgs cas{group_first_req, group_num_reqs, group_prefix_blocks, num_groups};
+  return attention_impl(q, k_pool, v_pool, nullptr, nullptr, block_tables, seq_lens,
+                        query_start_loc, scale, out, dims, workspace, workspace_bytes, stream,
+                        &cas);
 }
 
 int pkv_attention_fp8kv(const void* q, const void* k_pool, const void* v_pool,

@@ -517,12 +517,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                               2 * (pc.c0 + pc.S) <= p.num_slots && pc.slot >= 0 &&
                               pc.slot < p.num_slots;
         const long long out_row = ((long long)pc.row * p.num_q_heads + (long long)pc.k * G) * kHeadDim;
+        // Shared-prefix (cascade) rows: fold in the prefix pass's partial
+        // state (max M, normaliser, normalised output) by log-sum-exp.
+        auto fold_prefix = [&](int h, float& M, float& num, float& den) {
+          const long long pr = (long long)pc.row * p.num_q_heads + (long long)pc.k * G + h;
+          const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.pre_ml + pr * 2));
+          const float ov = __ldcg(p.pre_o + pr * kHeadDim + d);
+          const float Mn = fmaxf(M, ml.x);
+          const float a = fast_exp2(M - Mn), w = fast_exp2(ml.x - Mn) * ml.y;
+          num = num * a + w * ov;
+          den = den * a + w;
+          M = Mn;
+        };
         if (in_range && pc.S == 1) {
           if (ok) {
             #pragma unroll
-            for (int h = 0; h < G; ++h)
-              p.out[out_row + h * kHeadDim + d] =
-                  __float2bfloat16_rn(lt[h] > 0.f ? o[h] / lt[h] : 0.f);
+            for (int h = 0; h < G; ++h) {
+              float res = lt[h] > 0.f ? o[h] / lt[h] : 0.f;
+              if (pc.pre) {
+                float M = m[h], num = lt[h] * res, den = lt[h];
+                fold_prefix(h, M, num, den);
+                res = den > 0.f ? num / den : 0.f;
+              }
+              p.out[out_row + h * kHeadDim + d] = __float2bfloat16_rn(res);
+            }
           }
         } else if (in_range) {
           // Partial piece: normalised output and (max, normaliser), then the
@@ -566,6 +584,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 den = den * a + w;
                 M = Mn;
               }
+              if (pc.pre) fold_prefix(h, M, num, den);
               p.out[out_row + h * kHeadDim + d] = __float2bfloat16_rn(den > 0.f ? num / den : 0.f);
             }
           }

@@ -75,6 +75,12 @@ struct DecodeParams {
   int align_slack;    // ... if that lengthens the per-CTA range by at most this many blocks
   int prefetch;       // warm L2 with the block-table rows this CTA will likely read
   int early_plan;     // plan from seq_lens / query_start_loc before the PDL wait
+  // Shared-prefix (cascade) calls: the first table column each request reads
+  // ([R], or null), and the prefix pass's partial states to merge
+  // ([Tq, Hq, 128] normalised outputs and [Tq, Hq] (max, normaliser)).
+  const int32_t* first_block;
+  const float* pre_o;
+  const float* pre_ml;
   int pdl;            // launch with programmatic stream serialization
 };
 
@@ -138,7 +144,33 @@ struct PrefillParams {
   float scale_log2;
   int prefill_min_q;
   int pdl;
+  // Prefix pass of a shared-prefix (cascade) call: the work units are the
+  // sharing groups -- all query tokens of a group's members (contiguous
+  // requests) against the group's leading shared blocks, with no causal
+  // mask -- and the output is each row's partial state, not `out`.
+  int prefix_mode;
+  const int32_t* grp_first;   // [num_groups] first member request
+  const int32_t* grp_count;   // [num_groups] members
+  const int32_t* grp_blocks;  // [num_groups] shared leading blocks
+  int num_groups;
+  float* pre_o;               // [Tq, Hq, 128] normalised partial outputs
+  float* pre_ml;              // [Tq, Hq, 2] (max in log2 units, normaliser)
 };
+
+// Shared-prefix (cascade) set-up: per-request first unshared block.
+struct CascadePrepParams {
+  const int32_t* grp_first;
+  const int32_t* grp_count;
+  const int32_t* grp_blocks;
+  int32_t* first_block;  // [num_reqs], cleared before the launch
+  int* err;
+  int num_groups;
+  int num_reqs;
+  int max_blocks;
+  int pdl;
+};
+
+cudaError_t launch_cascade_prep(const CascadePrepParams& p, cudaStream_t stream);
 
 struct PrefillLaunch {
   CUtensorMap qmap;  // q as [tokens][Hq][128], box (64, g, 128/g)

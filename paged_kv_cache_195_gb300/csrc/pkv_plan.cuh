@@ -35,6 +35,7 @@ __device__ __forceinline__ long long ceil16_prefix(long long n) {
 
 struct ReqInfo {
   int q0, qr, L;
+  int fb;       // first block this call reads (a shared prefix before it is computed elsewhere)
   bool decode;  // has rows the decode kernels serve
 };
 
@@ -47,14 +48,21 @@ __device__ __forceinline__ ReqInfo load_request(const DecodeParams& p, int r) {
   const bool ok = ri.q0 >= 0 && ri.qr >= 0 && q1 <= p.num_q_tokens && ri.qr <= ri.L &&
                   ri.L <= p.max_blocks * kBlockSize;
   ri.decode = ok && ri.qr > 0 && ri.qr < p.prefill_min_q;
+  // A shared prefix (cascade) must end before the request's first query.
+  ri.fb = p.first_block ? __ldg(p.first_block + r) : 0;
+  if (ri.fb < 0 || (long long)ri.fb * kBlockSize > (long long)ri.L - ri.qr) ri.fb = 0;
   return ri;
 }
 
-// Blocks of rows 0..i-1 of a request (one KV head): row i sees L - qr + i + 1
-// keys, i.e. ceil((L - qr + 1 + i) / 16) blocks.
+// Blocks row i reads: positions fb*16 .. L - qr + i (row i sees L - qr + i + 1 keys).
+__device__ __forceinline__ int row_blocks(const ReqInfo& ri, int i) {
+  return cdiv(ri.L - ri.qr + i + 1, kBlockSize) - ri.fb;
+}
+
+// Blocks of rows 0..i-1 of a request (one KV head).
 __device__ __forceinline__ long long rows_blocks(const ReqInfo& ri, int i) {
   const long long a = (long long)ri.L - ri.qr + 1;
-  return ceil16_prefix(a + i - 1) - ceil16_prefix(a - 1);
+  return ceil16_prefix(a + i - 1) - ceil16_prefix(a - 1) - (long long)i * ri.fb;
 }
 
 // This CTA's share [lo, hi) of the step's block sequence, and the range
@@ -71,8 +79,8 @@ __device__ __forceinline__ Range cta_range(const DecodeParams& p, int lane) {
     const ReqInfo ri = load_request(p, r);
     if (ri.decode) {
       mine += rows_blocks(ri, ri.qr) * Hkv;
-      nb_min = min(nb_min, cdiv(ri.L - ri.qr + 1, kBlockSize));
-      nb_max = max(nb_max, cdiv(ri.L, kBlockSize));
+      nb_min = min(nb_min, row_blocks(ri, 0));
+      nb_max = max(nb_max, row_blocks(ri, ri.qr - 1));
     } else if (blockIdx.x == 0 && ri.qr != 0 && ri.qr < p.prefill_min_q) {
       record_error(p.err, kErrBounds);  // inconsistent lengths: request skipped
     }
@@ -106,7 +114,8 @@ struct Piece {
   int row;     // global query row, or kEndRow
   int r;       // request
   int k;       // KV head
-  int b0;      // first logical block of the piece
+  int b0;      // first logical block of the piece (a table column)
+  int pre;     // the row's shared prefix was computed by the prefix pass (merge it)
   int nblk;    // blocks in the piece (>= 1)
   int limit;   // keys visible to this row: positions < limit
   int L;       // request length (positions >= L hold no key)
@@ -173,7 +182,7 @@ struct Walker {
       i = a;
     }
     g = pos + rows_blocks(ri, i) * Hkv;  // start of row i, head 0
-    nb = cdiv(ri.L - ri.qr + i + 1, kBlockSize);
+    nb = row_blocks(ri, i);
     k = (int)((rg.lo - g) / nb);
     g += (long long)k * nb;
     done = g >= rg.hi;
@@ -187,7 +196,8 @@ struct Walker {
     pc.row = ri.q0 + i;
     pc.r = r;
     pc.k = k;
-    pc.b0 = (int)(s0 - g);
+    pc.b0 = ri.fb + (int)(s0 - g);
+    pc.pre = ri.fb > 0;
     pc.nblk = (int)(s1 - s0);
     pc.limit = ri.L - ri.qr + i + 1;
     pc.L = ri.L;
@@ -208,7 +218,7 @@ struct Walker {
         } while (!ri.decode);
         if (r >= p.num_reqs) done = true;
       }
-      if (!done) nb = cdiv(ri.L - ri.qr + i + 1, kBlockSize);
+      if (!done) nb = row_blocks(ri, i);
     }
     if (g >= rg.hi) done = true;
     return true;

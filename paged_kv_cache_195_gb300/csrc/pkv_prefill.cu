@@ -41,14 +41,16 @@ constexpr int kHalfBytes = kTileRows * 128;  // one 64-column half of a 128-row 
 constexpr uint32_t kTmemCols = 512;          // S0: cols 0..127, S1: 128..255, O: 256..383
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kNegBig = -1.0e30f;
+constexpr int kPastEnd = INT_MIN;            // block-table slot past the request (not read)
 
 struct Item {
-  int r, k;
+  int r, k;   // block-table row, KV head
   int row0;   // first query row of the tile
   int nt;     // valid tokens in the tile
   int pos0;   // position of its first token
   int L;      // request length (keys)
   int nj;     // key tiles
+  int causal; // 0: prefix pass (every row sees all L keys)
   int end;    // no more items
 };
 
@@ -73,19 +75,41 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+// A unit of prefill work: a request's query chunk (causal over its keys), or
+// in the prefix pass a sharing group's query tokens against its shared
+// blocks (every key visible).
 struct PfReq {
   int q0, qr, L, ntiles;
+  int tab;     // block-table row
   bool ok;
 };
 
-__device__ __forceinline__ PfReq load_pf_request(const PrefillParams& p, int r, int tq) {
+__device__ __forceinline__ int num_units(const PrefillParams& p) {
+  return p.prefix_mode ? p.num_groups : p.num_reqs;
+}
+
+__device__ __forceinline__ PfReq load_pf_request(const PrefillParams& p, int u, int tq) {
   PfReq a;
-  a.q0 = __ldg(p.qsl + r);
-  const int q1 = __ldg(p.qsl + r + 1);
-  a.L = __ldg(p.seq_lens + r);
-  a.qr = q1 - a.q0;
-  a.ok = a.q0 >= 0 && a.qr >= p.prefill_min_q && q1 <= p.num_q_tokens && a.qr <= a.L &&
-         a.L <= p.max_blocks * kBlockSize;
+  if (p.prefix_mode) {
+    const int first = __ldg(p.grp_first + u), n = __ldg(p.grp_count + u);
+    const int nb = __ldg(p.grp_blocks + u);
+    const bool idx_ok = first >= 0 && n >= 1 && (long long)first + n <= p.num_reqs;
+    a.tab = idx_ok ? first : 0;
+    a.q0 = idx_ok ? __ldg(p.qsl + first) : 0;
+    const int q1 = idx_ok ? __ldg(p.qsl + first + n) : 0;
+    a.qr = q1 - a.q0;
+    a.L = nb * kBlockSize;
+    a.ok = idx_ok && a.q0 >= 0 && a.qr >= 1 && q1 <= p.num_q_tokens && nb >= 1 &&
+           nb <= p.max_blocks;
+  } else {
+    a.tab = u;
+    a.q0 = __ldg(p.qsl + u);
+    const int q1 = __ldg(p.qsl + u + 1);
+    a.L = __ldg(p.seq_lens + u);
+    a.qr = q1 - a.q0;
+    a.ok = a.q0 >= 0 && a.qr >= p.prefill_min_q && q1 <= p.num_q_tokens && a.qr <= a.L &&
+           a.L <= p.max_blocks * kBlockSize;
+  }
   a.ntiles = a.ok ? ceil_div(a.qr, tq) : 0;
   return a;
 }
@@ -115,10 +139,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   // (no request with q_r >= prefill_min_q) leave every CTA idle.
   if (warp == 0) {
     long long total = 0;
-    for (int b = 0; b < p.num_reqs; b += 32) {
+    for (int b = 0; b < num_units(p); b += 32) {
       const int rr = b + lane;
       long long cnt = 0;
-      if (rr < p.num_reqs) cnt = (long long)load_pf_request(p, rr, TQ).ntiles * Hkv;
+      if (rr < num_units(p)) cnt = (long long)load_pf_request(p, rr, TQ).ntiles * Hkv;
       #pragma unroll
       for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
       total += cnt;
@@ -185,10 +209,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     long long item = blockIdx.x;  // global item index handled next
     long long base = 0;           // items before the current request batch
     const int oob_row = p.num_blocks * Hkv * kBlockSize;
-    for (int b = 0; b < p.num_reqs && !*abort_flag; b += 32) {
+    const int nunits = num_units(p);
+    for (int b = 0; b < nunits && !*abort_flag; b += 32) {
       const int rr = b + lane;
-      PfReq rq = {0, 0, 0, 0, false};
-      if (rr < p.num_reqs) rq = load_pf_request(p, rr, TQ);
+      PfReq rq = {0, 0, 0, 0, 0, false};
+      if (rr < nunits) rq = load_pf_request(p, rr, TQ);
       const long long cnt = (long long)rq.ntiles * Hkv;
       long long incl = cnt;
       #pragma unroll
@@ -203,7 +228,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const unsigned own = __ballot_sync(0xffffffffu, cnt > 0 && excl <= rel && rel < incl);
         const int src = __ffs(own) - 1;
         const long long local = rel - __shfl_sync(0xffffffffu, excl, src);
-        const int r = b + src;
+        const int r = __shfl_sync(0xffffffffu, rq.tab, src);
         const int q0 = __shfl_sync(0xffffffffu, rq.q0, src);
         const int qr = __shfl_sync(0xffffffffu, rq.qr, src);
         const int L = __shfl_sync(0xffffffffu, rq.L, src);
@@ -217,38 +242,43 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         it.nt = min(TQ, qr - qt * TQ);
         it.pos0 = L - qr + qt * TQ;
         it.L = L;
-        it.nj = (it.pos0 + it.nt - 1) / kKeyTile + 1;
+        it.causal = !p.prefix_mode;
+        it.nj = it.causal ? (it.pos0 + it.nt - 1) / kKeyTile + 1 : ceil_div(L, kKeyTile);
         it.end = 0;
         const int nbl = ceil_div(L, kBlockSize);
         const int32_t* bt = p.block_tables + (long long)r * p.max_blocks;
+        // Block-table entries 32 blocks (four key tiles) per load, the next
+        // group fetched while the current one is issued, checked at use.
+        auto raw_entries = [&](int x0) {
+          const int x = x0 + lane;
+          return x < nbl ? __ldg(bt + x) : kPastEnd;
+        };
+        int ent_cur = raw_entries(0);
+        int ent_nxt = it.nj > 4 ? raw_entries(32) : kPastEnd;
         for (int j = 0; j < it.nj; ++j, ++tile_ctr) {
+          if (j > 0 && (j & 3) == 0) {
+            ent_cur = ent_nxt;
+            if (j + 4 < it.nj) ent_nxt = raw_entries((j + 4) * 8);
+          }
           const int st = tile_ctr & 1;
           if (tile_ctr >= 2 &&
               !mbar_wait(&sm.kv_empty[st], ((tile_ctr >> 1) - 1) & 1, p.err, abort_flag))
             break;
-          const int blk = j * 8 + (lane & 7);
-          int rowc = oob_row;  // zero-filled by TMA
-          if (lane < 8 && blk < nbl) {
-            const int phys = __ldg(bt + blk);
-            if ((unsigned)phys < (unsigned)p.num_blocks) rowc = (phys * Hkv + k) * kBlockSize;
-            else record_error(p.err, kErrBounds);
-          }
-          int rows[8];
-          #pragma unroll
-          for (int x = 0; x < 8; ++x) rows[x] = __shfl_sync(0xffffffffu, rowc, x);
           if (lane == 0) {
             mbar_arrive_expect_tx(&sm.k_full[st], 2u * kHalfBytes);
-            #pragma unroll
-            for (int x = 0; x < 8; ++x) {
-              tma_load_2d(sm.k[st][0] + x * 2048, &kmap, 0, rows[x], &sm.k_full[st]);
-              tma_load_2d(sm.k[st][1] + x * 2048, &kmap, 64, rows[x], &sm.k_full[st]);
-            }
             mbar_arrive_expect_tx(&sm.v_full[st], 2u * kHalfBytes);
-            #pragma unroll
-            for (int x = 0; x < 8; ++x) {
-              tma_load_2d(sm.v[st][0] + x * 2048, &vmap, 0, rows[x], &sm.v_full[st]);
-              tma_load_2d(sm.v[st][1] + x * 2048, &vmap, 64, rows[x], &sm.v_full[st]);
-            }
+          }
+          __syncwarp();
+          // Lanes 0..15 each copy one (block, d half) of K and of V; blocks
+          // past the request are read at an out-of-range row (zero fill).
+          const int bsel = lane & 7, hsel = (lane >> 3) & 1;
+          const int phys = __shfl_sync(0xffffffffu, ent_cur, (j & 3) * 8 + bsel);
+          if (lane < 16) {
+            int rowc = oob_row;
+            if ((unsigned)phys < (unsigned)p.num_blocks) rowc = (phys * Hkv + k) * kBlockSize;
+            else if (phys != kPastEnd && hsel == 0) record_error(p.err, kErrBounds);
+            tma_load_2d(sm.k[st][hsel] + bsel * 2048, &kmap, hsel * 64, rowc, &sm.k_full[st]);
+            tma_load_2d(sm.v[st][hsel] + bsel * 2048, &vmap, hsel * 64, rowc, &sm.v_full[st]);
           }
           __syncwarp();
           if (j == 0) {
@@ -344,7 +374,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const Item it = sm.items[n_item & 1];
       if (!have || it.end) break;
       const bool valid = row < ROWS && t_local < it.nt;
-      const int prow = valid ? it.pos0 + t_local : -1;  // this row's position
+      // The last key this row sees (all keys in the prefix pass).
+      const int prow = !valid ? -1 : it.causal ? it.pos0 + t_local : it.L - 1;
       float m = kNegBig, l = 0.f;
       bool ok = true;
       for (int j = 0; j < it.nj; ++j, ++tile_ctr) {
@@ -467,14 +498,22 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       ok = ok && mbar_wait(&sm.o_full, n_item & 1, p.err, abort_flag);
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      __nv_bfloat16* dst = p.out + ((long long)(it.row0 + t_local) * p.num_q_heads +
-                                    (long long)it.k * G + h) * kHeadDim;
+      const long long orow = (long long)(it.row0 + t_local) * p.num_q_heads + (long long)it.k * G + h;
+      __nv_bfloat16* dst = p.out + orow * kHeadDim;
+      float* pdst = p.pre_o + orow * kHeadDim;  // prefix pass: partial state
+      if (p.prefix_mode && valid && ok)
+        *reinterpret_cast<float2*>(p.pre_ml + orow * 2) = make_float2(m, l);
       #pragma unroll
       for (int c = 0; c < 4; ++c) {
         float o[32];
         tmem_ld32(tO + c * 32, o);
         tc_wait_ld();
-        if (valid && ok) {
+        if (valid && ok && p.prefix_mode) {
+          #pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4*>(pdst + c * 32 + i) =
+                make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv);
+        } else if (valid && ok) {
           #pragma unroll
           for (int i = 0; i < 32; i += 8) {
             uint4 v;

@@ -47,12 +47,20 @@ class StepShape:
     num_blocks: int | None = None  # default: 1.25 x live blocks
     layers: int = 1
     seed: int = 195
+    # Shared prefixes: (first request, members, blocks).  Requests first ..
+    # first + members - 1 point their first `blocks` table entries at the
+    # same physical blocks (one copy of a common prompt in the pool).
+    prefix_groups: tuple = ()
 
     def __post_init__(self):
         self.seq_lens = np.asarray(self.seq_lens, dtype=np.int32)
         self.q_lens = np.asarray(self.q_lens, dtype=np.int32)
         assert self.seq_lens.shape == self.q_lens.shape
         assert (self.q_lens >= 0).all() and (self.q_lens <= self.seq_lens).all()
+        for first, members, blocks in self.prefix_groups:
+            for r in range(first, first + members):
+                # every member's new tokens come after the shared prefix
+                assert self.seq_lens[r] - self.q_lens[r] >= blocks * self.block_size
         if self.num_blocks is None:
             self.num_blocks = max(1, int(math.ceil(1.25 * self.live_blocks)))
         assert self.num_blocks >= self.live_blocks
@@ -67,7 +75,8 @@ class StepShape:
 
     @property
     def live_blocks(self) -> int:
-        return int(self.blocks_per_req.sum())
+        shared = sum((members - 1) * blocks for _, members, blocks in self.prefix_groups)
+        return int(self.blocks_per_req.sum()) - shared
 
     @property
     def max_blocks_per_req(self) -> int:
@@ -130,12 +139,21 @@ def llama_long_context() -> StepShape:
                      seed=195)
 
 
+def qwen_shared_prefix(layers: int = 28) -> StepShape:
+    """The Qwen decode step (64 x 512) with a shared prompt: four groups of 16
+    requests share their first 384 tokens (24 blocks)."""
+    groups = tuple((16 * i, 16, 24) for i in range(4))
+    return StepShape("qwen2.5-1.5b_decode_r64_L512_shared4x384", [512] * 64, [1] * 64, 12, 2,
+                     layers=layers, seed=195, prefix_groups=groups)
+
+
 CONFIGS = {
     "tiny": tiny_decode,
     "qwen_decode": qwen_decode,
     "qwen_long": qwen_long_batch,
     "llama_mixed": llama_mixed,
     "llama_long": llama_long_context,
+    "qwen_shared": qwen_shared_prefix,
 }
 
 
@@ -159,13 +177,23 @@ class StepInputs:
 
 
 def block_placement(shape: StepShape, seed: int) -> np.ndarray:
-    """[R, max_blocks] int32 physical block ids from a seeded permutation."""
+    """[R, max_blocks] int32 physical block ids from a seeded permutation.
+    Members of a shared-prefix group after the first reuse the first
+    member's leading blocks."""
     perm = np.random.default_rng(seed).permutation(shape.num_blocks).astype(np.int32)
     bt = np.full((shape.num_reqs, shape.max_blocks_per_req), -1, dtype=np.int32)
+    share = {}
+    for first, members, blocks in shape.prefix_groups:
+        for r in range(first + 1, first + members):
+            share[r] = (first, blocks)
     nxt = 0
     for r, nb in enumerate(shape.blocks_per_req):
-        bt[r, :nb] = perm[nxt:nxt + nb]
-        nxt += int(nb)
+        start = 0
+        if r in share:
+            first, start = share[r]
+            bt[r, :start] = bt[first, :start]
+        bt[r, start:nb] = perm[nxt:nxt + nb - start]
+        nxt += int(nb) - start
     return bt
 
 

@@ -447,3 +447,29 @@ def test_e4m3_encode_matches_torch_in_range():
     t = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
     o = np.array([oracle.e4m3_encode(v) for v in x], np.uint8)
     assert np.array_equal(t, o)
+
+
+def test_shared_prefix_tables_equal_private_copies():
+    """Requests whose tables share physical prefix blocks (one copy of a
+    common prompt) get exactly the attention of tables pointing at private
+    copies of those blocks: the oracle follows each table, so a shared-prefix
+    (cascade) call has the plain definition as its reference."""
+    shape = wl.StepShape("shared_pin", [40, 37, 52, 20], [1, 2, 1, 1], 8, 2, head_dim=16,
+                         seed=31, prefix_groups=((0, 3, 2),))
+    inp = wl.make_step(shape)
+    bt = inp.block_tables.numpy().copy()
+    k, v = wl.bf16_bits(inp.k_pool), wl.bf16_bits(inp.v_pool)
+    assert (bt[1, :2] == bt[0, :2]).all() and (bt[2, :2] == bt[0, :2]).all()
+    q = wl.bf16_bits(inp.q)
+    sl, qsl = inp.seq_lens.numpy(), inp.query_start_loc.numpy()
+    shared = oracle.paged_attention(q, k, v, bt, sl, qsl, inp.scale)
+    # give requests 1 and 2 private copies of the two prefix blocks
+    nb = k.shape[0]
+    extra = [bt[0, 0], bt[0, 1], bt[0, 0], bt[0, 1]]
+    k2 = np.concatenate([k, k[extra]])
+    v2 = np.concatenate([v, v[extra]])
+    bt2 = bt.copy()
+    bt2[1, :2] = [nb, nb + 1]
+    bt2[2, :2] = [nb + 2, nb + 3]
+    private = oracle.paged_attention(q, k2, v2, bt2, sl, qsl, inp.scale)
+    assert np.array_equal(shared, private)
