@@ -204,6 +204,9 @@ def workload_config(shape, ws_n, kv="bf16"):
               f"{2 * shape.layers * shape.num_blocks * shape.num_kv_heads * 2048 * kvb / 1e9:.2f}"
               " GB per step",
         "launch": f"CUDA graph of {shape.layers} x (append + attention)",
+        **({"shared_prefix": [{"first_request": int(f), "members": int(m), "blocks": int(b)}
+                              for f, m, b in shape.prefix_groups],
+            "attention_call": "pkv_attention_cascade"} if shape.prefix_groups else {}),
     }
 
 
@@ -249,8 +252,12 @@ def run_ours(args):
     L0 = layers[0]
     dims = pkv.make_dims(tuple(L0.q.shape), tuple(L0.k_pool.shape), shape.num_reqs,
                          shape.max_blocks_per_req)
-    ws = pkv.Workspace(dims, device=device)
+    cascade = bool(shape.prefix_groups) and not fp8
+    ws = (pkv.CascadeWorkspace if cascade else pkv.Workspace)(dims, device=device)
     pkv.pkv_workspace_init(ws, dims)
+    if cascade:
+        grp = np.array(shape.prefix_groups, dtype=np.int32).reshape(-1, 3)
+        grp_t = [torch.from_numpy(np.ascontiguousarray(grp[:, i])).to(device) for i in range(3)]
     outs = [torch.empty_like(x.q) for x in layers]
 
     att = rl.attention_bytes(shape.seq_lens, shape.q_lens, shape.num_q_heads, shape.num_kv_heads,
@@ -277,6 +284,10 @@ def run_ours(args):
                 pkv.pkv_attention_fp8kv(x.q, x.k_pool, x.v_pool, x.k_scale, x.v_scale,
                                         x.block_tables, x.seq_lens, x.query_start_loc, x.scale,
                                         out=outs[li], workspace=ws)
+            elif cascade:
+                pkv.pkv_attention_cascade(x.q, x.k_pool, x.v_pool, x.block_tables, x.seq_lens,
+                                          x.query_start_loc, *grp_t, x.scale, out=outs[li],
+                                          workspace=ws)
             else:
                 pkv.pkv_attention(x.q, x.k_pool, x.v_pool, x.block_tables, x.seq_lens,
                                   x.query_start_loc, x.scale, out=outs[li], workspace=ws)
@@ -359,7 +370,12 @@ def run_ours(args):
 
     peak, peak_src = measured_peak()
     value = bytes_per_step * ws_n / (ms_step * 1e-3) / 1e9
-    achieved = att["total"] / (kernel_ms * 1e-3) / 1e9
+    # The roofline counts the bytes the kernels must read: with shared
+    # prefixes, each group's prefix once.
+    unique = (rl.unique_kv_bytes(shape.seq_lens, shape.q_lens, shape.num_kv_heads,
+                                 shape.prefix_groups, kv_dtype_bytes=kvb) + att["q_out"]
+              if shape.prefix_groups else att["total"])
+    achieved = unique / (kernel_ms * 1e-3) / 1e9
     traffic = committed_traffic(args.config, args.kv)
     cpu = cpu_baseline(shape, layers, args) if (rank == 0 and ws_n == 1 and not args.no_cpu) else None
     line = {
@@ -378,7 +394,7 @@ def run_ours(args):
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "traffic": traffic,
             "kernel": decode_kernel_name(shape.num_q_heads // shape.num_kv_heads, fp8),
-            "algorithmic_bytes_per_launch": att["total"],
+            "algorithmic_bytes_per_launch": unique,
             "avg_launch_us": round(kernel_ms * 1e3, 3), "peak_source": peak_src,
             "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
         },

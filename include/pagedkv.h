@@ -201,8 +201,8 @@ int pkv_attention_fp8kv(const void *q, const void *k_pool, const void *v_pool,
 /*
  * Bytes of workspace pkv_attention_cascade needs for these dims: the
  * pkv_attention workspace (same head, initialised the same way with
- * pkv_workspace_init) plus a partial state per (query token, query head) and
- * an int per request.
+ * pkv_workspace_init), plus partial states for up to 8 chunks of each shared
+ * prefix per (query token, query head), plus an int per request.
  */
 size_t pkv_cascade_workspace_size(const pkv_dims *dims);
 
@@ -220,8 +220,9 @@ size_t pkv_cascade_workspace_size(const pkv_dims *dims);
  * are skipped and reported as PKV_ERR_DEVICE_BOUNDS.
  * How: one pass attends every member's query rows to the group's shared
  * blocks at once on the tensor cores (rows = the members' (token, head)
- * pairs) and keeps a partial state per row; the decode then reads each row's
- * remaining blocks and merges the two by log-sum-exp.  Every row runs in the
+ * pairs; the shared keys split into up to 8 chunks of 128-key tiles, one
+ * work item each) and keeps a partial state per row and chunk; the decode
+ * then reads each row's remaining blocks and merges them by log-sum-exp.  Every row runs in the
  * decode path (no separate prefill kernel).  Sharing applies when the step
  * runs the tensor-core decode (bf16 pools, 4..8 query heads per KV head);
  * otherwise the call computes the same result without it.

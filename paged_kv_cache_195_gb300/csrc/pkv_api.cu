@@ -316,7 +316,7 @@ struct CascadeLayout {
 
 CascadeLayout cascade_layout(const pkv::WorkspaceLayout& w, const pkv_dims* d) {
   auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
-  const size_t rows = (size_t)d->num_q_tokens * d->num_q_heads;
+  const size_t rows = (size_t)pkv::kPrefixSplits * d->num_q_tokens * d->num_q_heads;
   CascadeLayout c;
   c.pre_o = up(w.total);
   c.pre_ml = c.pre_o + up(rows * pkv::kHeadDim * sizeof(float));

@@ -258,6 +258,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tma_load_3d(sm.q[ub][0], &qmap, 0, k * G, pc.row, &sm.q_full[ub]);
             tma_load_3d(sm.q[ub][1], &qmap, 64, k * G, pc.row, &sm.q_full[ub]);
           }
+          if (pc.pre) {
+            // The epilogue will fold the prefix pass's partial states of
+            // this row: bring them into L2 now (G x 512 B of outputs and the
+            // (max, normaliser) pairs per chunk).
+            const long long pr = (long long)pc.row * p.num_q_heads + (long long)k * G;
+            const long long stride = (long long)p.num_q_tokens * p.num_q_heads;
+            const int nch = prefix_chunks(pc.fb * kBlockSize);
+            for (int i = lane; i < nch * (G * 4 + 1); i += 32) {
+              const int c = i / (G * 4 + 1), x = i % (G * 4 + 1);
+              const char* a = x < G * 4
+                  ? reinterpret_cast<const char*>(p.pre_o + ((c * stride + pr) * kHeadDim)) + x * 128
+                  : reinterpret_cast<const char*>(p.pre_ml + (c * stride + pr) * 2);
+              asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+            }
+          }
           __syncwarp();
         }
       }
@@ -519,15 +534,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const long long out_row = ((long long)pc.row * p.num_q_heads + (long long)pc.k * G) * kHeadDim;
         // Shared-prefix (cascade) rows: fold in the prefix pass's partial
         // state (max M, normaliser, normalised output) by log-sum-exp.
+        // The prefix pass left one partial per chunk of the shared keys
+        // (pc.b0 is at least the shared block count, and the row's first
+        // piece starts exactly there).
         auto fold_prefix = [&](int h, float& M, float& num, float& den) {
           const long long pr = (long long)pc.row * p.num_q_heads + (long long)pc.k * G + h;
-          const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.pre_ml + pr * 2));
-          const float ov = __ldcg(p.pre_o + pr * kHeadDim + d);
-          const float Mn = fmaxf(M, ml.x);
-          const float a = fast_exp2(M - Mn), w = fast_exp2(ml.x - Mn) * ml.y;
-          num = num * a + w * ov;
-          den = den * a + w;
-          M = Mn;
+          const long long stride = (long long)p.num_q_tokens * p.num_q_heads;
+          const int nch = prefix_chunks(pc.fb * kBlockSize);
+          // all chunks' loads first (they were prefetched into L2), then fold
+          float2 ml[kPrefixSplits];
+          float ov[kPrefixSplits];
+          #pragma unroll
+          for (int c = 0; c < kPrefixSplits; ++c) {
+            if (c < nch) {
+              const long long sl = c * stride + pr;
+              ml[c] = __ldcg(reinterpret_cast<const float2*>(p.pre_ml + sl * 2));
+              ov[c] = __ldcg(p.pre_o + sl * kHeadDim + d);
+            }
+          }
+          #pragma unroll
+          for (int c = 0; c < kPrefixSplits; ++c) {
+            if (c < nch) {
+              const float Mn = fmaxf(M, ml[c].x);
+              const float a = fast_exp2(M - Mn), w = fast_exp2(ml[c].x - Mn) * ml[c].y;
+              num = num * a + w * ov[c];
+              den = den * a + w;
+              M = Mn;
+            }
+          }
         };
         if (in_range && pc.S == 1) {
           if (ok) {

@@ -157,6 +157,24 @@ struct PrefillParams {
   float* pre_ml;              // [Tq, Hq, 2] (max in log2 units, normaliser)
 };
 
+// Shared-prefix (cascade) prefix pass: a group's shared keys (L of them) are
+// split into at most kPrefixSplits chunks of whole 128-key tiles, one work
+// item each, so that a few groups still spread over many SMs; each chunk
+// leaves its own partial state ([kPrefixSplits, Tq, Hq] slots).
+#ifndef PKV_PREFIX_SPLITS
+#define PKV_PREFIX_SPLITS 8
+#endif
+constexpr int kPrefixSplits = PKV_PREFIX_SPLITS;
+constexpr int kPrefixTile = 128;
+__host__ __device__ inline int prefix_chunk_tiles(int L) {
+  const int tiles = (L + kPrefixTile - 1) / kPrefixTile;
+  return (tiles + kPrefixSplits - 1) / kPrefixSplits;
+}
+__host__ __device__ inline int prefix_chunks(int L) {
+  const int tiles = (L + kPrefixTile - 1) / kPrefixTile;
+  return tiles > 0 ? (tiles + prefix_chunk_tiles(L) - 1) / prefix_chunk_tiles(L) : 1;
+}
+
 // Shared-prefix (cascade) set-up: per-request first unshared block.
 struct CascadePrepParams {
   const int32_t* grp_first;

@@ -116,6 +116,7 @@ struct Piece {
   int k;       // KV head
   int b0;      // first logical block of the piece (a table column)
   int pre;     // the row's shared prefix was computed by the prefix pass (merge it)
+  int fb;      // shared blocks before the row's own (the prefix pass covered them)
   int nblk;    // blocks in the piece (>= 1)
   int limit;   // keys visible to this row: positions < limit
   int L;       // request length (positions >= L hold no key)
@@ -198,6 +199,7 @@ struct Walker {
     pc.k = k;
     pc.b0 = ri.fb + (int)(s0 - g);
     pc.pre = ri.fb > 0;
+    pc.fb = ri.fb;
     pc.nblk = (int)(s1 - s0);
     pc.limit = ri.L - ri.qr + i + 1;
     pc.L = ri.L;

@@ -51,6 +51,8 @@ struct Item {
   int L;      // request length (keys)
   int nj;     // key tiles
   int causal; // 0: prefix pass (every row sees all L keys)
+  int kt0;    // first key tile (a prefix-pass chunk of the keys)
+  int kc;     // prefix-pass chunk index (selects the partial-state slot)
   int end;    // no more items
 };
 
@@ -79,8 +81,9 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // in the prefix pass a sharing group's query tokens against its shared
 // blocks (every key visible).
 struct PfReq {
-  int q0, qr, L, ntiles;
+  int q0, qr, L, ntiles;  // ntiles: items per KV head (q-tiles x key chunks)
   int tab;     // block-table row
+  int nchunk;  // key chunks (prefix pass; 1 otherwise)
   bool ok;
 };
 
@@ -110,7 +113,8 @@ __device__ __forceinline__ PfReq load_pf_request(const PrefillParams& p, int u, 
     a.ok = a.q0 >= 0 && a.qr >= p.prefill_min_q && q1 <= p.num_q_tokens && a.qr <= a.L &&
            a.L <= p.max_blocks * kBlockSize;
   }
-  a.ntiles = a.ok ? ceil_div(a.qr, tq) : 0;
+  a.nchunk = p.prefix_mode ? prefix_chunks(a.L) : 1;
+  a.ntiles = a.ok ? ceil_div(a.qr, tq) * a.nchunk : 0;
   return a;
 }
 
@@ -212,7 +216,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const int nunits = num_units(p);
     for (int b = 0; b < nunits && !*abort_flag; b += 32) {
       const int rr = b + lane;
-      PfReq rq = {0, 0, 0, 0, 0, false};
+      PfReq rq = {0, 0, 0, 0, 0, 1, false};
       if (rr < nunits) rq = load_pf_request(p, rr, TQ);
       const long long cnt = (long long)rq.ntiles * Hkv;
       long long incl = cnt;
@@ -233,8 +237,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const int qr = __shfl_sync(0xffffffffu, rq.qr, src);
         const int L = __shfl_sync(0xffffffffu, rq.L, src);
         const int ntiles = __shfl_sync(0xffffffffu, rq.ntiles, src);
+        const int nchunk = __shfl_sync(0xffffffffu, rq.nchunk, src);
         // heavier (later) q-tiles first
-        const int qt = ntiles - 1 - (int)(local / Hkv);
+        const int qk = ntiles - 1 - (int)(local / Hkv);
+        const int qt = qk / nchunk, kc = qk % nchunk;
         const int k = (int)(local % Hkv);
         Item it;
         it.r = r; it.k = k;
@@ -243,14 +249,17 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         it.pos0 = L - qr + qt * TQ;
         it.L = L;
         it.causal = !p.prefix_mode;
-        it.nj = it.causal ? (it.pos0 + it.nt - 1) / kKeyTile + 1 : ceil_div(L, kKeyTile);
+        it.kc = kc;
+        it.kt0 = it.causal ? 0 : kc * prefix_chunk_tiles(L);
+        it.nj = it.causal ? (it.pos0 + it.nt - 1) / kKeyTile + 1
+                          : min(prefix_chunk_tiles(L), ceil_div(L, kKeyTile) - it.kt0);
         it.end = 0;
         const int nbl = ceil_div(L, kBlockSize);
         const int32_t* bt = p.block_tables + (long long)r * p.max_blocks;
         // Block-table entries 32 blocks (four key tiles) per load, the next
         // group fetched while the current one is issued, checked at use.
         auto raw_entries = [&](int x0) {
-          const int x = x0 + lane;
+          const int x = it.kt0 * 8 + x0 + lane;
           return x < nbl ? __ldg(bt + x) : kPastEnd;
         };
         int ent_cur = raw_entries(0);
@@ -386,7 +395,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         // Pass 1: the row maximum of this tile (masked keys excluded).  S
         // stays in TMEM and is read in 32-column chunks, twice, so that the
         // loop bodies stay small.
-        const int kbase = j * kKeyTile;
+        const int kbase = (it.kt0 + j) * kKeyTile;
         const bool full_tile = kbase + kKeyTile - 1 <= prow;  // no key of this tile masked
         float mxp[8];
         #pragma unroll
@@ -500,9 +509,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const long long orow = (long long)(it.row0 + t_local) * p.num_q_heads + (long long)it.k * G + h;
       __nv_bfloat16* dst = p.out + orow * kHeadDim;
-      float* pdst = p.pre_o + orow * kHeadDim;  // prefix pass: partial state
+      // Prefix pass: the partial state of this key chunk.
+      const long long prow_slot = (long long)it.kc * p.num_q_tokens * p.num_q_heads + orow;
+      float* pdst = p.pre_o + prow_slot * kHeadDim;
       if (p.prefix_mode && valid && ok)
-        *reinterpret_cast<float2*>(p.pre_ml + orow * 2) = make_float2(m, l);
+        *reinterpret_cast<float2*>(p.pre_ml + prow_slot * 2) = make_float2(m, l);
       #pragma unroll
       for (int c = 0; c < 4; ++c) {
         float o[32];

@@ -39,6 +39,19 @@ def attention_bytes(seq_lens, q_lens, num_q_heads, num_kv_heads, head_dim=128,
     return {"kv": kv, "q_out": qo, "total": kv + qo}
 
 
+def unique_kv_bytes(seq_lens, q_lens, num_kv_heads, prefix_groups, block_size=16,
+                    head_dim=128, kv_dtype_bytes: int = BF16) -> int:
+    """KV bytes a step must read when each shared prefix (first request,
+    members, blocks) is read once for its group instead of once per member."""
+    seq_lens = np.asarray(seq_lens, np.int64)
+    q_lens = np.asarray(q_lens, np.int64)
+    tokens = int(seq_lens[q_lens > 0].sum())
+    for first, members, blocks in prefix_groups:
+        active = int((q_lens[first:first + members] > 0).sum())
+        tokens -= max(0, active - 1) * blocks * block_size
+    return tokens * kv_bytes_per_token(num_kv_heads, head_dim, kv_dtype_bytes)
+
+
 def append_bytes(num_tokens, num_kv_heads, head_dim=128, kv_dtype_bytes: int = BF16) -> int:
     """Read k_new/v_new (bf16) and write them into the pool (bf16 or e4m3)."""
     return 2 * num_tokens * num_kv_heads * head_dim * (BF16 + kv_dtype_bytes)

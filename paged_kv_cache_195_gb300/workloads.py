@@ -147,6 +147,14 @@ def qwen_shared_prefix(layers: int = 28) -> StepShape:
                      layers=layers, seed=195, prefix_groups=groups)
 
 
+def qwen_shared_long() -> StepShape:
+    """The Qwen long batch (128 x 2048) with shared prompts: eight groups of
+    16 requests share their first 1536 tokens (96 blocks)."""
+    groups = tuple((16 * i, 16, 96) for i in range(8))
+    return StepShape("qwen2.5-1.5b_decode_r128_L2048_shared8x1536", [2048] * 128, [1] * 128,
+                     12, 2, seed=195, prefix_groups=groups)
+
+
 CONFIGS = {
     "tiny": tiny_decode,
     "qwen_decode": qwen_decode,
@@ -154,6 +162,7 @@ CONFIGS = {
     "llama_mixed": llama_mixed,
     "llama_long": llama_long_context,
     "qwen_shared": qwen_shared_prefix,
+    "qwen_shared_long": qwen_shared_long,
 }
 
 
