@@ -590,6 +590,13 @@ int pkv_get_device_error(cudaStream_t stream) {
   return PKV_OK;
 }
 
+#if PKV_PF_TRACE
+// Debug builds only: copies the prefill kernel's per-tile timeline.
+int pkv_debug_pf_trace(void* host, size_t bytes) {
+  return pkv::prefill_trace(host, bytes) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+#endif
+
 #if PKV_TC_TRACE
 // Debug builds only: copies the tensor-core decode's per-tile timeline.
 int pkv_debug_tc_trace(void* host, size_t bytes) {

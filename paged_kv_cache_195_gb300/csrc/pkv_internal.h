@@ -212,6 +212,12 @@ cudaError_t decode_trace(void* host, size_t bytes);
 #if PKV_TC_TRACE
 cudaError_t decode_tc_trace(void* host, size_t bytes);
 #endif
+#ifndef PKV_PF_TRACE
+#define PKV_PF_TRACE 0
+#endif
+#if PKV_PF_TRACE
+cudaError_t prefill_trace(void* host, size_t bytes);
+#endif
 
 // Sets the thread's pkv_last_error() message.
 void set_error_message(const char* msg);

@@ -41,6 +41,22 @@ constexpr int kHalfBytes = kTileRows * 128;  // one 64-column half of a 128-row 
 constexpr uint32_t kTmemCols = 512;          // S0: cols 0..127, S1: 128..255, O: 256..383
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kNegBig = -1.0e30f;
+// Debug-only per-tile timeline of CTA 0 (build with -DPKV_PF_TRACE=1):
+// %globaltimer at load issue, keys seen by the MMA warp, scores seen by the
+// softmax, probabilities ready (PV issue), stage released to the producer.
+#ifndef PKV_PF_TRACE
+#define PKV_PF_TRACE 0
+#endif
+#if PKV_PF_TRACE
+constexpr int kPfTrTiles = 64;
+__device__ unsigned long long g_pf_trace[5][kPfTrTiles];
+#define PF_TR(ev, tile) do { if (blockIdx.x == 0 && (tile) < kPfTrTiles) g_pf_trace[ev][tile] = global_timer_ns(); } while (0)
+#else
+#define PF_TR(ev, tile) do { } while (0)
+#endif
+#ifndef PKV_PF_PV_FIRST
+#define PKV_PF_PV_FIRST 0  // issue the previous tile's PV before this tile's QK^T
+#endif
 constexpr int kPastEnd = INT_MIN;            // block-table slot past the request (not read)
 
 struct Item {
@@ -56,14 +72,15 @@ struct Item {
   int end;    // no more items
 };
 
+constexpr int kPfStages = 3;  // K/V tile stages (64 KiB each)
+
 struct __align__(1024) PfSmem {
-  uint8_t q[2][kHalfBytes];      // Q: d 0..63 | d 64..127
-  uint8_t k[2][2][kHalfBytes];   // [stage][d half]
-  uint8_t v[2][2][kHalfBytes];   // [stage][d half]
-  uint8_t p[2][2][kHalfBytes];   // [buffer][keys 0..63 | keys 64..127]
+  uint8_t q[2][kHalfBytes];              // Q: d 0..63 | d 64..127
+  uint8_t k[kPfStages][2][kHalfBytes];   // [stage][d half]
+  uint8_t v[kPfStages][2][kHalfBytes];   // [stage][d half]
   uint64_t q_full, q_empty;
-  uint64_t k_full[2], v_full[2], kv_empty[2];
-  uint64_t s_full[2], s_free[2], p_full[2], p_free[2];
+  uint64_t k_full[kPfStages], v_full[kPfStages], kv_empty[kPfStages];
+  uint64_t s_full[2], p_full[2], p_free[2];
   uint64_t o_full, o_empty;
   Item items[2];
   uint32_t tmem_base;
@@ -164,16 +181,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   if (tid == 0) {
     mbar_init(&sm.q_full, 1);
     mbar_init(&sm.q_empty, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kPfStages; ++s) {
       mbar_init(&sm.k_full[s], 1);
       mbar_init(&sm.v_full[s], 1);
       mbar_init(&sm.kv_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.s_full[b], 1);   // tcgen05.commit after S = QK^T into buffer b
-      mbar_init(&sm.s_free[b], 4);   // the four softmax warps have read S buffer b
-      mbar_init(&sm.p_full[b], 4);   // P buffer b written (and O rescaled) by all four
-      mbar_init(&sm.p_free[b], 1);   // tcgen05.commit after the PV that read P buffer b
+      mbar_init(&sm.p_full[b], 4);   // P written over S buffer b (and O rescaled) by all four
+      mbar_init(&sm.p_free[b], 1);   // tcgen05.commit after the PV that read P in buffer b
     }
     mbar_init(&sm.o_full, 1);
     mbar_init(&sm.o_empty, 4);
@@ -269,10 +285,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             ent_cur = ent_nxt;
             if (j + 4 < it.nj) ent_nxt = raw_entries((j + 4) * 8);
           }
-          const int st = tile_ctr & 1;
-          if (tile_ctr >= 2 &&
-              !mbar_wait(&sm.kv_empty[st], ((tile_ctr >> 1) - 1) & 1, p.err, abort_flag))
+          const int st = tile_ctr % kPfStages;
+          if (tile_ctr >= kPfStages &&
+              !mbar_wait(&sm.kv_empty[st], ((tile_ctr / kPfStages) - 1) & 1, p.err, abort_flag))
             break;
+          if (lane == 0 && tile_ctr >= kPfStages) PF_TR(4, tile_ctr - kPfStages);
+          if (lane == 0) PF_TR(0, tile_ctr);
           if (lane == 0) {
             mbar_arrive_expect_tx(&sm.k_full[st], 2u * kHalfBytes);
             mbar_arrive_expect_tx(&sm.v_full[st], 2u * kHalfBytes);
@@ -328,21 +346,24 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       int t = 0;  // tile counter, shared sequence with the producer and softmax
       bool ok = true;
       auto pv = [&](int tt, bool first, int n_item) {
-        const int b = tt & 1;
+        const int b = tt & 1, st = tt % kPfStages;
         ok = ok && mbar_wait(&sm.p_full[b], (tt >> 1) & 1, p.err, abort_flag);
-        ok = ok && mbar_wait(&sm.v_full[b], (tt >> 1) & 1, p.err, abort_flag);
+        ok = ok && mbar_wait(&sm.v_full[st], (tt / kPfStages) & 1, p.err, abort_flag);
         if (first && n_item > 0)
           ok = ok && mbar_wait(&sm.o_empty, (n_item - 1) & 1, p.err, abort_flag);
+        PF_TR(3, tt);
         tc_fence_after();
         #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t da = smem_desc_sw128(smem_u32(sm.p[b][kk >> 2]) + (kk & 3) * 32, 16, 1024);
+          // P (bf16) lies in the first 64 columns of S buffer b, two keys
+          // per column: keys 16kk .. 16kk+15 in columns 8kk .. 8kk+7.
+          const uint32_t ta = tmem + b * kKeyTile + kk * 8;
           // V is MN-major (d contiguous): atoms of 64 d x 8 keys; the two d
           // halves are kHalfBytes apart, 8-key groups 1024 bytes apart.
-          const uint64_t db = smem_desc_sw128(smem_u32(sm.v[b][0]) + kk * 2048, kHalfBytes, 1024);
-          tc_mma_f16_ss(tO, da, db, kIdescO, !first || kk > 0);
+          const uint64_t db = smem_desc_sw128(smem_u32(sm.v[st][0]) + kk * 2048, kHalfBytes, 1024);
+          tc_mma_f16_ts(tO, ta, db, kIdescO, !first || kk > 0);
         }
-        tc_commit(&sm.kv_empty[b]);
+        tc_commit(&sm.kv_empty[st]);
         tc_commit(&sm.p_free[b]);
       };
       for (int n_item = 0; ok; ++n_item) {
@@ -351,19 +372,22 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         if (it.end) break;
         tc_fence_after();
         for (int j = 0; j < it.nj && ok; ++j, ++t) {
-          const int b = t & 1;
-          ok = mbar_wait(&sm.k_full[b], (t >> 1) & 1, p.err, abort_flag);
-          if (t >= 2) ok = ok && mbar_wait(&sm.s_free[b], ((t >> 1) - 1) & 1, p.err, abort_flag);
+          const int b = t & 1, st = t % kPfStages;
+          if (PKV_PF_PV_FIRST && j >= 1) pv(t - 1, j == 1, n_item);
+          ok = ok && mbar_wait(&sm.k_full[st], (t / kPfStages) & 1, p.err, abort_flag);
+          PF_TR(1, t);
+          // S buffer b holds P(t - 2) until the PV of tile t - 2 has read it.
+          if (t >= 2) ok = ok && mbar_wait(&sm.p_free[b], ((t >> 1) - 1) & 1, p.err, abort_flag);
           tc_fence_after();
           const uint32_t tS = tmem + b * kKeyTile;
           #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint64_t da = smem_desc_sw128(smem_u32(sm.q[kk >> 2]) + (kk & 3) * 32, 16, 1024);
-            const uint64_t db = smem_desc_sw128(smem_u32(sm.k[b][kk >> 2]) + (kk & 3) * 32, 16, 1024);
+            const uint64_t db = smem_desc_sw128(smem_u32(sm.k[st][kk >> 2]) + (kk & 3) * 32, 16, 1024);
             tc_mma_f16_ss(tS, da, db, kIdescS, kk > 0);
           }
           tc_commit(&sm.s_full[b]);
-          if (j >= 1) pv(t - 1, j == 1, n_item);
+          if (!PKV_PF_PV_FIRST && j >= 1) pv(t - 1, j == 1, n_item);
         }
         if (ok) pv(t - 1, it.nj == 1, n_item);  // the item's last tile
         tc_commit(&sm.o_full);
@@ -391,29 +415,27 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const int sb = tile_ctr & 1;  // S / P / K / V buffer of this tile
         const uint32_t tS = tmem + lane_off + sb * kKeyTile;
         ok = ok && mbar_wait(&sm.s_full[sb], (tile_ctr >> 1) & 1, p.err, abort_flag);
+        if (row == 0) PF_TR(2, tile_ctr);
         tc_fence_after();
-        // Pass 1: the row maximum of this tile (masked keys excluded).  S
-        // stays in TMEM and is read in 32-column chunks, twice, so that the
-        // loop bodies stay small.
+        // The row's 128 scores of this tile, read from TMEM once (four loads
+        // in flight, one wait), then the maximum over the visible keys.
         const int kbase = (it.kt0 + j) * kKeyTile;
         const bool full_tile = kbase + kKeyTile - 1 <= prow;  // no key of this tile masked
+        float v[kKeyTile];
+        #pragma unroll
+        for (int c = 0; c < 4; ++c)
+          tmem_ld32(tS + c * 32, *reinterpret_cast<float(*)[32]>(v + c * 32));
+        tc_wait_ld();
+        if (!full_tile) {
+          #pragma unroll
+          for (int i = 0; i < kKeyTile; ++i)
+            if (kbase + i > prow) v[i] = -INFINITY;
+        }
         float mxp[8];
         #pragma unroll
         for (int i = 0; i < 8; ++i) mxp[i] = -INFINITY;
-        #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          float v[32];
-          tmem_ld32(tS + c * 32, v);
-          tc_wait_ld();
-          if (full_tile) {
-            #pragma unroll
-            for (int i = 0; i < 32; ++i) mxp[i & 7] = fmaxf(mxp[i & 7], v[i]);
-          } else {
-            #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (kbase + c * 32 + i <= prow) mxp[i & 7] = fmaxf(mxp[i & 7], v[i]);
-          }
-        }
+        #pragma unroll
+        for (int i = 0; i < kKeyTile; ++i) mxp[i & 7] = fmaxf(mxp[i & 7], v[i]);
         float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
                          fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
         mx = mx * p.scale_log2;  // scale > 0 keeps the arg max
@@ -443,54 +465,36 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           m_use = m_new;
         }
         m = m_use;
-        // P buffer sb was last read by the PV of tile - 2.
-        if (tile_ctr >= 2)
-          ok = ok && mbar_wait(&sm.p_free[sb], ((tile_ctr >> 1) - 1) & 1, p.err, abort_flag);
-        // Pass 2: P = exp2(s * scale_log2 - m) in bf16, keys contiguous per
-        // row, 128-byte swizzle; the normaliser sums the rounded values the
-        // MMA will use.
+        // P = exp2(s * scale_log2 - m) in bf16 (masked keys are -inf: p = 0),
+        // written over the first 64 columns of this row's S in TMEM, two keys
+        // per column, where the PV MMA reads it; the normaliser sums the
+        // rounded values the MMA will use.
         float sump[4] = {0.f, 0.f, 0.f, 0.f};
         const float neg_m = -m;
-        #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          float v[32];
-          tmem_ld32(tS + c * 32, v);
-          tc_wait_ld();
+        #pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t w[32];
           #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {  // 16-byte chunk: keys c*32 + q4*8 .. +8
-            uint32_t w[4];
-            #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int i0 = q4 * 8 + 2 * e;
-              float p0 = fast_exp2(fmaf(v[i0], p.scale_log2, neg_m));
-              float p1 = fast_exp2(fmaf(v[i0 + 1], p.scale_log2, neg_m));
-              if (!full_tile) {
-                if (kbase + c * 32 + i0 > prow) p0 = 0.f;
-                if (kbase + c * 32 + i0 + 1 > prow) p1 = 0.f;
-              }
-              w[e] = pack_bf16x2(p0, p1);
-              const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&w[e]);
-              sump[e] += __low2float(b2) + __high2float(b2);
-            }
-            const int chunk = c * 4 + q4, half = chunk >> 3, cc = chunk & 7;
-            uint8_t* rowp = sm.p[sb][half] + (row >> 3) * 1024 + (row & 7) * 128;
-            *reinterpret_cast<uint4*>(rowp + ((cc ^ (row & 7)) * 16)) =
-                make_uint4(w[0], w[1], w[2], w[3]);
+          for (int e = 0; e < 32; ++e) {
+            const int i0 = half * 64 + 2 * e;
+            const float p0 = fast_exp2(fmaf(v[i0], p.scale_log2, neg_m));
+            const float p1 = fast_exp2(fmaf(v[i0 + 1], p.scale_log2, neg_m));
+            w[e] = pack_bf16x2(p0, p1);
+            const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&w[e]);
+            sump[e & 3] += __low2float(b2) + __high2float(b2);
           }
+          tmem_st32(tS + half * 32, *reinterpret_cast<const float(*)[32]>(w));
         }
-        // S is no longer needed: the MMA may overwrite this buffer (tile + 2).
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.s_free[sb]);
+        tc_wait_st();
         const float sum = (sump[0] + sump[1]) + (sump[2] + sump[3]);
         l += sum;
         // Keys past the request's end inside its last block may hold anything
         // (even NaN); zero those V rows so that 0 * V stays 0 in the MMA.
-        const int st = sb;
+        const int st = tile_ctr % kPfStages;
         const int tail0 = it.L - kbase;                      // first key >= L in this tile
         const int tail1 = min(kKeyTile, ceil_div(it.L, kBlockSize) * kBlockSize - kbase);
         if (warp == 0 && tail0 < tail1 && tail0 >= 0) {
-          ok = ok && mbar_wait(&sm.v_full[st], (tile_ctr >> 1) & 1, p.err, abort_flag);
+          ok = ok && mbar_wait(&sm.v_full[st], (tile_ctr / kPfStages) & 1, p.err, abort_flag);
           const int nrows = tail1 - tail0;
           for (int i = lane; i < nrows * 16; i += 32) {
             const int rr = tail0 + i / 16, half = (i / 8) & 1, chunk = i & 7;
@@ -582,6 +586,12 @@ cudaError_t launch_prefill_g(const PrefillLaunch& L, cudaStream_t stream) {
 }  // namespace
 
 int prefill_tokens_per_tile(int group) { return kTileRows / group; }
+
+#if PKV_PF_TRACE
+cudaError_t prefill_trace(void* host, size_t bytes) {
+  return cudaMemcpyFromSymbol(host, g_pf_trace, bytes < sizeof(g_pf_trace) ? bytes : sizeof(g_pf_trace));
+}
+#endif
 
 cudaError_t launch_prefill(const PrefillLaunch& L, int group, cudaStream_t stream) {
   switch (group) {

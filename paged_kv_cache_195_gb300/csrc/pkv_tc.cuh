@@ -79,6 +79,18 @@ __device__ __forceinline__ void tc_mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, 
       : "memory");
 }
 
+// D[tmem] (+)= A[tmem] x B[smem]^T (kind::f16): A is read from Tensor Memory,
+// one row per lane, two 16-bit elements of K per 32-bit column.
+__device__ __forceinline__ void tc_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                              uint32_t idesc, bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
+      : "memory");
+}
+
 // Arrive on `bar` once every tcgen05 operation this thread issued so far has
 // completed.
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
