@@ -19,13 +19,17 @@
 // fills with zeros.  Q comes in with one 3-D TMA copy per half (d, head,
 // token).
 //
-// Roles (192 threads): warps 0-3 own one TMEM lane / MMA row each and run the
-// softmax and the epilogue; warp 4 issues TMA copies; one thread of warp 5
-// issues tcgen05.mma and commits.  Per key tile: S = Q K^T (8 MMAs of K=16)
-// into TMEM, softmax reads S, writes P (bf16, swizzled) to shared memory,
-// then O += P V (8 MMAs) accumulates in TMEM.  O is rescaled in TMEM only
-// when a row's maximum grows by more than 2^8 (the result is exact either
-// way: O and the normaliser always share the same reference maximum).
+// Roles (352 threads): eight softmax warps -- warps 0-3 and 6-9, two threads
+// per TMEM lane / MMA row, each taking half of the row's keys and output
+// dims -- run the softmax and the epilogue; warp 4 issues the Q and K copies,
+// warp 10 the V copies; one thread of warp 5 issues tcgen05.mma and commits.
+// Per key tile: S = Q K^T (8 MMAs of K=16) into TMEM, the softmax reads S and
+// writes P (bf16, two keys per column) over it, then O += P V (8 MMAs, A read
+// from TMEM) accumulates in TMEM.  K and V have rings of their own: a K stage
+// is free once its QK^T is done, a V stage once its PV is, so K runs ahead of
+// the tensor core by the whole ring.  O is rescaled in TMEM only when a row's
+// maximum grows by more than 2^8 (the result is exact either way: O and the
+// normaliser always share the same reference maximum).
 #include <climits>
 
 #include "pkv_internal.h"
@@ -34,7 +38,9 @@
 namespace pkv {
 namespace {
 
-constexpr int kPfThreads = 192;
+constexpr int kPfThreads = 352;          // 11 warps
+constexpr int kSoftThreads = 256;        // softmax warps 0-3 and 6-9
+constexpr int kBarSoftmax = 1;           // their named barrier
 constexpr int kTileRows = 128;               // MMA M
 constexpr int kKeyTile = 128;                // MMA N for S, K for PV
 constexpr int kHalfBytes = kTileRows * 128;  // one 64-column half of a 128-row tile
@@ -79,10 +85,11 @@ struct __align__(1024) PfSmem {
   uint8_t k[kPfStages][2][kHalfBytes];   // [stage][d half]
   uint8_t v[kPfStages][2][kHalfBytes];   // [stage][d half]
   uint64_t q_full, q_empty;
-  uint64_t k_full[kPfStages], v_full[kPfStages], kv_empty[kPfStages];
+  uint64_t k_full[kPfStages], v_full[kPfStages], k_empty[kPfStages], v_empty[kPfStages];
   uint64_t s_full[2], p_full[2], p_free[2];
   uint64_t o_full, o_empty;
   Item items[2];
+  float xrow[2][kTileRows];      // [key half][row]: half-row maxima, then normalisers
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -184,15 +191,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     for (int s = 0; s < kPfStages; ++s) {
       mbar_init(&sm.k_full[s], 1);
       mbar_init(&sm.v_full[s], 1);
-      mbar_init(&sm.kv_empty[s], 1);
+      mbar_init(&sm.k_empty[s], 1);
+      mbar_init(&sm.v_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.s_full[b], 1);   // tcgen05.commit after S = QK^T into buffer b
-      mbar_init(&sm.p_full[b], 4);   // P written over S buffer b (and O rescaled) by all four
+      mbar_init(&sm.p_full[b], 8);   // P written over S buffer b (and O rescaled) by all eight
       mbar_init(&sm.p_free[b], 1);   // tcgen05.commit after the PV that read P in buffer b
     }
     mbar_init(&sm.o_full, 1);
-    mbar_init(&sm.o_empty, 4);
+    mbar_init(&sm.o_empty, 8);
     sm.abort_flag = 0;
     fence_barrier_init();
   }
@@ -223,8 +231,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const uint32_t tmem = sm.tmem_base;
   allow_dependent_launch();
 
-  if (warp == 4) {
-    // ========================= TMA producer ===============================
+  if (warp == 4 || warp == 10) {
+    // ==================== TMA producers (K + Q | V) =======================
+    // Both warps walk the same item sequence; each feeds its own ring.
+    const bool vside = warp == 10;
+    uint64_t* const full = vside ? sm.v_full : sm.k_full;
+    uint64_t* const empty = vside ? sm.v_empty : sm.k_empty;
+    const CUtensorMap* const map = vside ? &vmap : &kmap;
     int n_item = 0, tile_ctr = 0;
     long long item = blockIdx.x;  // global item index handled next
     long long base = 0;           // items before the current request batch
@@ -287,28 +300,25 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           }
           const int st = tile_ctr % kPfStages;
           if (tile_ctr >= kPfStages &&
-              !mbar_wait(&sm.kv_empty[st], ((tile_ctr / kPfStages) - 1) & 1, p.err, abort_flag))
+              !mbar_wait(&empty[st], ((tile_ctr / kPfStages) - 1) & 1, p.err, abort_flag))
             break;
-          if (lane == 0 && tile_ctr >= kPfStages) PF_TR(4, tile_ctr - kPfStages);
-          if (lane == 0) PF_TR(0, tile_ctr);
-          if (lane == 0) {
-            mbar_arrive_expect_tx(&sm.k_full[st], 2u * kHalfBytes);
-            mbar_arrive_expect_tx(&sm.v_full[st], 2u * kHalfBytes);
-          }
+          if (lane == 0 && vside && tile_ctr >= kPfStages) PF_TR(4, tile_ctr - kPfStages);
+          if (lane == 0 && !vside) PF_TR(0, tile_ctr);
+          if (lane == 0) mbar_arrive_expect_tx(&full[st], 2u * kHalfBytes);
           __syncwarp();
-          // Lanes 0..15 each copy one (block, d half) of K and of V; blocks
-          // past the request are read at an out-of-range row (zero fill).
+          // Lanes 0..15 each copy one (block, d half); blocks past the
+          // request are read at an out-of-range row (zero fill).
           const int bsel = lane & 7, hsel = (lane >> 3) & 1;
           const int phys = __shfl_sync(0xffffffffu, ent_cur, (j & 3) * 8 + bsel);
           if (lane < 16) {
             int rowc = oob_row;
             if ((unsigned)phys < (unsigned)p.num_blocks) rowc = (phys * Hkv + k) * kBlockSize;
-            else if (phys != kPastEnd && hsel == 0) record_error(p.err, kErrBounds);
-            tma_load_2d(sm.k[st][hsel] + bsel * 2048, &kmap, hsel * 64, rowc, &sm.k_full[st]);
-            tma_load_2d(sm.v[st][hsel] + bsel * 2048, &vmap, hsel * 64, rowc, &sm.v_full[st]);
+            else if (phys != kPastEnd && hsel == 0 && !vside) record_error(p.err, kErrBounds);
+            uint8_t* dst = (vside ? sm.v[st][hsel] : sm.k[st][hsel]) + bsel * 2048;
+            tma_load_2d(dst, map, hsel * 64, rowc, &full[st]);
           }
           __syncwarp();
-          if (j == 0) {
+          if (j == 0 && !vside) {
             // Q of this item, once the previous item's MMAs are done with Q
             // (its first K/V tile is already on its way).
             if (n_item >= 1 && !mbar_wait(&sm.q_empty, (n_item - 1) & 1, p.err, abort_flag))
@@ -327,8 +337,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
       base += total;
     }
-    // end marker
-    if (n_item == 0 || mbar_wait(&sm.q_empty, (n_item - 1) & 1, p.err, abort_flag)) {
+    // end marker (the Q side owns the item slots)
+    if (!vside && (n_item == 0 || mbar_wait(&sm.q_empty, (n_item - 1) & 1, p.err, abort_flag))) {
       if (lane == 0) {
         sm.items[n_item & 1].end = 1;
         mbar_arrive(&sm.q_full);
@@ -363,7 +373,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           const uint64_t db = smem_desc_sw128(smem_u32(sm.v[st][0]) + kk * 2048, kHalfBytes, 1024);
           tc_mma_f16_ts(tO, ta, db, kIdescO, !first || kk > 0);
         }
-        tc_commit(&sm.kv_empty[st]);
+        tc_commit(&sm.v_empty[st]);
         tc_commit(&sm.p_free[b]);
       };
       for (int n_item = 0; ok; ++n_item) {
@@ -386,6 +396,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             const uint64_t db = smem_desc_sw128(smem_u32(sm.k[st][kk >> 2]) + (kk & 3) * 32, 16, 1024);
             tc_mma_f16_ss(tS, da, db, kIdescS, kk > 0);
           }
+          tc_commit(&sm.k_empty[st]);
           tc_commit(&sm.s_full[b]);
           if (!PKV_PF_PV_FIRST && j >= 1) pv(t - 1, j == 1, n_item);
         }
@@ -396,48 +407,64 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
     __syncwarp();
   } else {
-    // ===================== softmax + epilogue (warps 0-3) ==================
-    const int row = tid;  // MMA row == TMEM lane
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    const uint32_t tO = tmem + lane_off + 2 * kKeyTile;
+    // ============= softmax + epilogue (warps 0-3 and 6-9) ===================
+    // Two threads share each MMA row: warps 0-3 take keys 0..63 of a tile and
+    // output dims 0..63, warps 6-9 keys 64..127 and dims 64..127.  Warp w
+    // reaches TMEM lanes 32 (w % 4) .. +31, so warps with equal w % 4 hold the
+    // same 32 rows.  The two halves agree on the row maximum through shared
+    // memory once per tile.
+    const int quad = warp & 3;
+    const int half = warp < 4 ? 0 : 1;
+    const int row = quad * 32 + lane;  // MMA row == TMEM lane
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const uint32_t tO = tmem + lane_off + 2 * kKeyTile + half * 64;
     const int t_local = row / G, h = row % G;
     int tile_ctr = 0;
     for (int n_item = 0;; ++n_item) {
       const bool have = mbar_wait(&sm.q_full, n_item & 1, p.err, abort_flag);
       const Item it = sm.items[n_item & 1];
-      if (!have || it.end) break;
+      // Agree before any barrier: a wait that gave up (abort) stops everyone.
+      if (barrier_or(kBarSoftmax, kSoftThreads, !have || it.end)) break;
       const bool valid = row < ROWS && t_local < it.nt;
       // The last key this row sees (all keys in the prefix pass).
       const int prow = !valid ? -1 : it.causal ? it.pos0 + t_local : it.L - 1;
       float m = kNegBig, l = 0.f;
       bool ok = true;
       for (int j = 0; j < it.nj; ++j, ++tile_ctr) {
-        const int sb = tile_ctr & 1;  // S / P / K / V buffer of this tile
+        const int sb = tile_ctr & 1;  // S / P buffer of this tile
         const uint32_t tS = tmem + lane_off + sb * kKeyTile;
         ok = ok && mbar_wait(&sm.s_full[sb], (tile_ctr >> 1) & 1, p.err, abort_flag);
-        if (row == 0) PF_TR(2, tile_ctr);
+        if (row == 0 && half == 0) PF_TR(2, tile_ctr);
         tc_fence_after();
-        // The row's 128 scores of this tile, read from TMEM once (four loads
-        // in flight, one wait), then the maximum over the visible keys.
-        const int kbase = (it.kt0 + j) * kKeyTile;
-        const bool full_tile = kbase + kKeyTile - 1 <= prow;  // no key of this tile masked
-        float v[kKeyTile];
-        #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          tmem_ld32(tS + c * 32, *reinterpret_cast<float(*)[32]>(v + c * 32));
+        // This half's 64 scores, read from TMEM once, and their maximum over
+        // the visible keys.
+        const int kbase = (it.kt0 + j) * kKeyTile + half * 64;
+        const bool full_half = kbase + 63 <= prow;  // no key of this half masked
+        float v[64];
+        tmem_ld32(tS + half * 64, *reinterpret_cast<float(*)[32]>(v));
+        tmem_ld32(tS + half * 64 + 32, *reinterpret_cast<float(*)[32]>(v + 32));
         tc_wait_ld();
-        if (!full_tile) {
+        if (!full_half) {
           #pragma unroll
-          for (int i = 0; i < kKeyTile; ++i)
+          for (int i = 0; i < 64; ++i)
             if (kbase + i > prow) v[i] = -INFINITY;
         }
         float mxp[8];
         #pragma unroll
         for (int i = 0; i < 8; ++i) mxp[i] = -INFINITY;
         #pragma unroll
-        for (int i = 0; i < kKeyTile; ++i) mxp[i & 7] = fmaxf(mxp[i & 7], v[i]);
-        float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
-                         fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
+        for (int i = 0; i < 64; ++i) mxp[i & 7] = fmaxf(mxp[i & 7], v[i]);
+        const float mxh = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
+                                fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
+        // The row maximum over both halves.  The barrier also orders every
+        // thread's S reads before any P write (P of half 1 lands in TMEM
+        // columns that held half 0's scores).
+        sm.xrow[half][row] = mxh;
+        tc_fence_before();
+        named_barrier(kBarSoftmax, kSoftThreads);
+        tc_fence_after();
+        float mx = fmaxf(mxh, sm.xrow[half ^ 1][row]);
+        named_barrier(kBarSoftmax, kSoftThreads);  // sm.xrow is free again
         mx = mx * p.scale_log2;  // scale > 0 keeps the arg max
         float m_use = m;
         const bool grow = j == 0 ? true : (mx > m + kRescaleLog2);
@@ -452,7 +479,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           const float m_new = grow ? fmaxf(m, mx) : m;
           const float alpha = fast_exp2(m - m_new);
           #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < 2; ++c) {
             float o[32];
             tmem_ld32(tO + c * 32, o);
             tc_wait_ld();
@@ -466,39 +493,36 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         m = m_use;
         // P = exp2(s * scale_log2 - m) in bf16 (masked keys are -inf: p = 0),
-        // written over the first 64 columns of this row's S in TMEM, two keys
-        // per column, where the PV MMA reads it; the normaliser sums the
-        // rounded values the MMA will use.
+        // written over the row's S in TMEM two keys per column -- keys
+        // 64 half .. +63 in columns 32 half .. +31 -- where the PV MMA reads
+        // it; the normaliser sums the rounded values the MMA will use.
         float sump[4] = {0.f, 0.f, 0.f, 0.f};
         const float neg_m = -m;
+        uint32_t w[32];
         #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t w[32];
-          #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int i0 = half * 64 + 2 * e;
-            const float p0 = fast_exp2(fmaf(v[i0], p.scale_log2, neg_m));
-            const float p1 = fast_exp2(fmaf(v[i0 + 1], p.scale_log2, neg_m));
-            w[e] = pack_bf16x2(p0, p1);
-            const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&w[e]);
-            sump[e & 3] += __low2float(b2) + __high2float(b2);
-          }
-          tmem_st32(tS + half * 32, *reinterpret_cast<const float(*)[32]>(w));
+        for (int e = 0; e < 32; ++e) {
+          const float p0 = fast_exp2(fmaf(v[2 * e], p.scale_log2, neg_m));
+          const float p1 = fast_exp2(fmaf(v[2 * e + 1], p.scale_log2, neg_m));
+          w[e] = pack_bf16x2(p0, p1);
+          const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&w[e]);
+          sump[e & 3] += __low2float(b2) + __high2float(b2);
         }
+        tmem_st32(tS + half * 32, *reinterpret_cast<const float(*)[32]>(w));
         tc_wait_st();
         const float sum = (sump[0] + sump[1]) + (sump[2] + sump[3]);
         l += sum;
         // Keys past the request's end inside its last block may hold anything
         // (even NaN); zero those V rows so that 0 * V stays 0 in the MMA.
         const int st = tile_ctr % kPfStages;
-        const int tail0 = it.L - kbase;                      // first key >= L in this tile
-        const int tail1 = min(kKeyTile, ceil_div(it.L, kBlockSize) * kBlockSize - kbase);
+        const int tbase = (it.kt0 + j) * kKeyTile;
+        const int tail0 = it.L - tbase;                      // first key >= L in this tile
+        const int tail1 = min(kKeyTile, ceil_div(it.L, kBlockSize) * kBlockSize - tbase);
         if (warp == 0 && tail0 < tail1 && tail0 >= 0) {
           ok = ok && mbar_wait(&sm.v_full[st], (tile_ctr / kPfStages) & 1, p.err, abort_flag);
           const int nrows = tail1 - tail0;
           for (int i = lane; i < nrows * 16; i += 32) {
-            const int rr = tail0 + i / 16, half = (i / 8) & 1, chunk = i & 7;
-            *reinterpret_cast<uint4*>(sm.v[st][half] + (rr >> 3) * 1024 + (rr & 7) * 128 +
+            const int rr = tail0 + i / 16, hf = (i / 8) & 1, chunk = i & 7;
+            *reinterpret_cast<uint4*>(sm.v[st][hf] + (rr >> 3) * 1024 + (rr & 7) * 128 +
                                       chunk * 16) = make_uint4(0, 0, 0, 0);
           }
         }
@@ -507,19 +531,23 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.p_full[sb]);
       }
-      // ---- epilogue: O / l -> bf16 -> out ---------------------------------
+      // ---- epilogue: O / l -> bf16 -> out (this half's 64 dims) ----------
+      sm.xrow[half][row] = l;
+      named_barrier(kBarSoftmax, kSoftThreads);
+      const float lrow = l + sm.xrow[half ^ 1][row];
+      named_barrier(kBarSoftmax, kSoftThreads);  // sm.xrow is free again
       ok = ok && mbar_wait(&sm.o_full, n_item & 1, p.err, abort_flag);
       tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = lrow > 0.f ? 1.f / lrow : 0.f;
       const long long orow = (long long)(it.row0 + t_local) * p.num_q_heads + (long long)it.k * G + h;
-      __nv_bfloat16* dst = p.out + orow * kHeadDim;
+      __nv_bfloat16* dst = p.out + orow * kHeadDim + half * 64;
       // Prefix pass: the partial state of this key chunk.
       const long long prow_slot = (long long)it.kc * p.num_q_tokens * p.num_q_heads + orow;
-      float* pdst = p.pre_o + prow_slot * kHeadDim;
-      if (p.prefix_mode && valid && ok)
-        *reinterpret_cast<float2*>(p.pre_ml + prow_slot * 2) = make_float2(m, l);
+      float* pdst = p.pre_o + prow_slot * kHeadDim + half * 64;
+      if (p.prefix_mode && valid && ok && half == 0)
+        *reinterpret_cast<float2*>(p.pre_ml + prow_slot * 2) = make_float2(m, lrow);
       #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         float o[32];
         tmem_ld32(tO + c * 32, o);
         tc_wait_ld();
@@ -531,19 +559,18 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         } else if (valid && ok) {
           #pragma unroll
           for (int i = 0; i < 32; i += 8) {
-            uint4 v;
-            v.x = pack_bf16x2(o[i] * inv, o[i + 1] * inv);
-            v.y = pack_bf16x2(o[i + 2] * inv, o[i + 3] * inv);
-            v.z = pack_bf16x2(o[i + 4] * inv, o[i + 5] * inv);
-            v.w = pack_bf16x2(o[i + 6] * inv, o[i + 7] * inv);
-            *reinterpret_cast<uint4*>(dst + c * 32 + i) = v;
+            uint4 q4;
+            q4.x = pack_bf16x2(o[i] * inv, o[i + 1] * inv);
+            q4.y = pack_bf16x2(o[i + 2] * inv, o[i + 3] * inv);
+            q4.z = pack_bf16x2(o[i + 4] * inv, o[i + 5] * inv);
+            q4.w = pack_bf16x2(o[i + 6] * inv, o[i + 7] * inv);
+            *reinterpret_cast<uint4*>(dst + c * 32 + i) = q4;
           }
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.o_empty);
-      if (!ok) break;
     }
   }
   // Every warp reaches this point (aborts only shorten the loops), so the
