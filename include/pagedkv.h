@@ -167,6 +167,31 @@ int pkv_attention(const void *q, const void *k_pool, const void *v_pool,
                   cudaStream_t stream);
 
 /*
+ * One layer of an engine step: pkv_append of this step's dims->num_q_tokens
+ * new tokens, then pkv_attention over the updated pools -- the same results
+ * as the two calls in that order, with the same arguments, preconditions and
+ * errors.  Additional precondition: slot_mapping[t] for t = query_start_loc[r]
+ * + i is either negative (padding) or the slot of position L_r - q_r + i of
+ * request r through its block table, i.e. the append writes no pool slot that
+ * holds an earlier position.  Because of it the attention kernel does not
+ * wait for the append before streaming the K/V tiles that hold only earlier
+ * positions (nor before reading q and block_tables); it waits only before the
+ * first tile of a row that holds one of the new tokens, so the append's
+ * latency hides behind the gather (with PKV_PDL=0 or PKV_EARLY_KV=0 the two
+ * run back to back instead).
+ * Source: LLM 7 - Efficient LLM Serving, sec. 3 "What the Cache Stores" (the
+ * step appends each new token's K and V, then attends over the cache); The
+ * Serving Playbook, "The block table lives in the hottest kernel in the
+ * system".
+ */
+int pkv_append_attention(const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                         void *k_pool, void *v_pool, const void *q,
+                         const int32_t *block_tables, const int32_t *seq_lens,
+                         const int32_t *query_start_loc, float scale, void *out,
+                         const pkv_dims *dims, void *workspace, size_t workspace_bytes,
+                         cudaStream_t stream);
+
+/*
  * KV append into e4m3 pools (8-bit float: 1 sign, 4 exponent bits with bias
  * 7, 3 mantissa bits, largest finite magnitude 448).  Same slots, padding and
  * bounds rules as pkv_append; k_pool / v_pool are [num_blocks, Hkv, bs, 128]

@@ -178,12 +178,11 @@ namespace pkv {
 void set_error_message(const char* msg) { snprintf(g_last_error, sizeof g_last_error, "%s", msg); }
 }  // namespace pkv
 
-extern "C" {
+namespace {
 
-const char* pkv_last_error(void) { return g_last_error; }
-
-int pkv_append(const void* k_new, const void* v_new, const int64_t* slot_mapping, void* k_pool,
-               void* v_pool, int32_t num_new_tokens, const pkv_dims* dims, cudaStream_t stream) {
+int append_impl(const void* k_new, const void* v_new, const int64_t* slot_mapping, void* k_pool,
+                void* v_pool, int32_t num_new_tokens, const pkv_dims* dims, cudaStream_t stream,
+                bool early_trigger) {
   g_last_error[0] = '\0';
   int rc = check_dims(dims, false);
   if (rc != PKV_OK) return rc;
@@ -206,9 +205,22 @@ int pkv_append(const void* k_new, const void* v_new, const int64_t* slot_mapping
   p.num_kv_heads = dims->num_kv_heads;
   p.num_blocks = dims->num_blocks;
   p.pdl = env_int("PKV_PDL", 1) != 0;
+  p.early_trigger = early_trigger && p.pdl;
   cudaError_t e = pkv::launch_append(p, stream);
   if (e != cudaSuccess) return cuda_fail(e, "append launch");
   return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pkv_last_error(void) { return g_last_error; }
+
+int pkv_append(const void* k_new, const void* v_new, const int64_t* slot_mapping, void* k_pool,
+               void* v_pool, int32_t num_new_tokens, const pkv_dims* dims, cudaStream_t stream) {
+  return append_impl(k_new, v_new, slot_mapping, k_pool, v_pool, num_new_tokens, dims, stream,
+                     false);
 }
 
 int pkv_append_fp8(const void* k_new, const void* v_new, const int64_t* slot_mapping,
@@ -331,7 +343,8 @@ int attention_impl(const void* q, const void* k_pool, const void* v_pool, const 
                    const float* v_scale, const int32_t* block_tables, const int32_t* seq_lens,
                    const int32_t* query_start_loc, float scale, void* out, const pkv_dims* dims,
                    void* workspace, size_t workspace_bytes, cudaStream_t stream,
-                   const CascadeArgs* cas = nullptr) {
+                   const CascadeArgs* cas = nullptr, bool after_append = false,
+                   bool append_triggered_early = false) {
   g_last_error[0] = '\0';
   const bool fp8 = k_scale != nullptr;
   int rc = check_dims(dims, true);
@@ -393,6 +406,10 @@ int attention_impl(const void* q, const void* k_pool, const void* v_pool, const 
   p.qsl = query_start_loc;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.ws_cnt = reinterpret_cast<int*>(ws + w.cnt_off);
+  p.plan_cache = env_int("PKV_PLAN_CACHE", 1) != 0 && dims->num_reqs <= pkv::kPlanCacheReqs
+                     ? reinterpret_cast<int*>(ws + w.plan_off)
+                     : nullptr;
+  p.plan_entries = w.plan_entries;
   p.ws_ml = reinterpret_cast<float*>(ws + w.ml_off);
   p.ws_o = reinterpret_cast<float*>(ws + w.o_off);
   p.err = st->err;
@@ -487,6 +504,10 @@ int attention_impl(const void* q, const void* k_pool, const void* v_pool, const 
     p.prefill_min_q = 0x7fffffff;
     p.early_plan = 0;  // first_block comes from the set-up kernel, two launches back
   }
+  // Right after the append of this step's tokens (pkv_append_attention), the
+  // decode kernel streams every tile without a new token before waiting.
+  p.early_kv = after_append && !cascade && p.pdl;
+  p.early_q = !append_triggered_early;
   const bool do_prefill = run_prefill && !cascade;
   if (use_tc) {
     pkv::DecodeTcLaunch T{};
@@ -538,6 +559,29 @@ int pkv_attention(const void* q, const void* k_pool, const void* v_pool,
                   void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   return attention_impl(q, k_pool, v_pool, nullptr, nullptr, block_tables, seq_lens,
                         query_start_loc, scale, out, dims, workspace, workspace_bytes, stream);
+}
+
+int pkv_append_attention(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                         void* k_pool, void* v_pool, const void* q, const int32_t* block_tables,
+                         const int32_t* seq_lens, const int32_t* query_start_loc, float scale,
+                         void* out, const pkv_dims* dims, void* workspace,
+                         size_t workspace_bytes, cudaStream_t stream) {
+  g_last_error[0] = '\0';
+  int rc = check_dims(dims, true);
+  if (rc != PKV_OK) return rc;
+  // The attention kernel reads K/V tiles without this step's tokens (and the
+  // lengths and tables) before it waits for the append.  PKV_EARLY_TRIGGER=1
+  // also lets it launch as soon as the append starts, before the kernel
+  // ahead of the append has finished; q, out and the workspace then wait.
+  const bool pdl = env_int("PKV_PDL", 1) != 0;
+  const bool early = pdl && env_int("PKV_EARLY_KV", 1) != 0;
+  const bool trigger = early && env_int("PKV_EARLY_TRIGGER", 0) != 0;
+  rc = append_impl(k_new, v_new, slot_mapping, k_pool, v_pool, dims->num_q_tokens, dims, stream,
+                   trigger);
+  if (rc != PKV_OK) return rc;
+  return attention_impl(q, k_pool, v_pool, nullptr, nullptr, block_tables, seq_lens,
+                        query_start_loc, scale, out, dims, workspace, workspace_bytes, stream,
+                        nullptr, early, trigger);
 }
 
 size_t pkv_cascade_workspace_size(const pkv_dims* dims) {

@@ -10,9 +10,25 @@
 
 namespace pkv {
 
+// Debug-only per-block timeline (entry, past the grid-dependency wait, row
+// written by thread 0), read together with the decode kernel's.
+#if PKV_TC_TRACE >= 3
+constexpr int kApTrBlocks = 256, kApTrSlots = 32;
+__device__ unsigned long long g_ap_trace[kApTrSlots][kApTrBlocks][4];
+#define AP_TR(ev) do { if (threadIdx.x == 0 && blockIdx.x < kApTrBlocks) g_ap_trace[(uint32_t)((reinterpret_cast<uintptr_t>(p.k_new) >> 8) * 0x9E3779B1u) >> 27][blockIdx.x][ev] = global_timer_ns(); } while (0)
+cudaError_t append_trace(void* host, size_t bytes) {
+  return cudaMemcpyFromSymbol(host, g_ap_trace, bytes < sizeof(g_ap_trace) ? bytes : sizeof(g_ap_trace));
+}
+#else
+#define AP_TR(ev) do { } while (0)
+#endif
+
 __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
+  AP_TR(0);
+  if (p.early_trigger) allow_dependent_launch();
   grid_dependency_wait();  // inputs and pool may belong to the previous kernel
-  allow_dependent_launch();
+  if (!p.early_trigger) allow_dependent_launch();
+  AP_TR(1);
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= p.num_tokens * p.num_kv_heads) return;
@@ -33,6 +49,7 @@ __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
   uint4* dst = reinterpret_cast<uint4*>(half ? p.v_pool : p.k_pool) +
                ((blk * p.num_kv_heads + h) * kBlockSize + off) * (kHeadDim / 8) + c;
   *dst = __ldg(src);
+  AP_TR(2);
 }
 
 // Quantising append into e4m3 pools (The Serving Playbook, "Quantized

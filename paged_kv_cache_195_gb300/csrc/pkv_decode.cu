@@ -32,8 +32,11 @@ WorkspaceLayout decode_workspace_layout(int num_q_tokens, int num_kv_heads, int 
   WorkspaceLayout w;
   auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
   w.num_slots = 2 * sm_count * 2;  // two partial pieces per CTA, up to two CTAs per SM
+  w.plan_entries = w.num_slots / 2;  // one per CTA index of the largest grid
   w.cnt_off = 0;
-  w.ml_off = up((size_t)num_q_tokens * num_kv_heads * sizeof(int));
+  // The plan cache sits inside the zero-initialised head of the workspace.
+  w.plan_off = up((size_t)num_q_tokens * num_kv_heads * sizeof(int));
+  w.ml_off = w.plan_off + up((size_t)w.plan_entries * kPlanEntryWords * sizeof(int));
   w.o_off = w.ml_off + up((size_t)w.num_slots * group * 2 * sizeof(float));
   w.total = w.o_off + up((size_t)w.num_slots * group * kHeadDim * sizeof(float));
   return w;

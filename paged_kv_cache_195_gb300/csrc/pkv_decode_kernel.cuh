@@ -443,7 +443,14 @@ __global__ void __launch_bounds__(DecodeCfg<G>::kThreads) __maxnreg__(DecodeCfg<
   // its first read of q, the block table or the pools.  Every thread lets
   // the next kernel launch only after its own wait, so that kernel may rely
   // on everything before this one having completed.
-  if (warp != DecodeCfg<G>::kCW || !p.early_plan) {
+  // With early_kv the previous kernel is the append of this step's new
+  // tokens: before the wait the producer reads the lengths, the block table
+  // and blocks without a new token, and waits before the first block holding
+  // one (and before it blocks on the consumers).  If that append lets this
+  // grid launch as soon as the append starts (early_q unset), q, out and the
+  // workspace may still belong to the kernel before the append: Q copies are
+  // then issued after the wait and the consumers wait before anything else.
+  if (!p.early_kv && (warp != DecodeCfg<G>::kCW || !p.early_plan)) {
     grid_dependency_wait();
     allow_dependent_launch();
   }
@@ -452,30 +459,52 @@ __global__ void __launch_bounds__(DecodeCfg<G>::kThreads) __maxnreg__(DecodeCfg<
   if (warp == DecodeCfg<G>::kCW) {
     // ======================= producer warp =================================
     if (p.prefetch) plan::prefetch_block_table(p, lane);
-    const plan::Range rg = plan::cta_range(p, lane);
+    plan::Range rg;
+    plan::Walker wk;
+    plan::plan_cta(p, lane, rg, wk);
     if (lane == 0) TRACE(2);
 
     const uint64_t pol = l2_policy_evict_first();
     uint32_t n = 0;  // CTA-wide block sequence number
     int j = 0;       // CTA-local piece index
-    if (p.early_plan) {
+    bool waited = !p.early_kv;
+    if (p.early_plan && !p.early_kv) {
       grid_dependency_wait();
       allow_dependent_launch();
     }
-    plan::Walker wk;
-    wk.start(p, rg, lane);
+    // Q copies of pieces met before the wait (at most the two buffers'),
+    // issued once it has been taken.
+    int q_pend = 0;
+    const __nv_bfloat16 *q_src0 = nullptr, *q_src1 = nullptr;
+    auto take_wait = [&]() {
+      if (!waited) {
+        grid_dependency_wait();  // the append of this step's tokens is complete
+        allow_dependent_launch();
+        waited = true;
+      }
+      if (lane == 0 && (q_pend & 1)) bulk_copy_g2s(sm.qbuf[0], q_src0, G * kHeadDim * 2, &sm.qfull[0]);
+      if (lane == 0 && (q_pend & 2)) bulk_copy_g2s(sm.qbuf[1], q_src1, G * kHeadDim * 2, &sm.qfull[1]);
+      q_pend = 0;
+    };
     Piece pc;
     while (!*abort_flag && wk.next(p, pc)) {
       // ---- one piece: blocks [b0, b0 + nblk) of row-group (row, k) --------
       const int k = pc.k;
       const int ub = j & 1;
-      if (j >= 2 && !mbar_wait(&sm.qempty[ub], ((j >> 1) - 1) & 1, p.err, abort_flag)) break;
+      if (j >= 2) {
+        if (!waited || q_pend) take_wait();
+        if (!mbar_wait(&sm.qempty[ub], ((j >> 1) - 1) & 1, p.err, abort_flag)) break;
+      }
+      const __nv_bfloat16* qsrc =
+          p.q + ((long long)pc.row * p.num_q_heads + (long long)k * G) * kHeadDim;
       if (lane == 0) {
         sm.pinfo[ub] = pc;
         mbar_arrive_expect_tx(&sm.qfull[ub], G * kHeadDim * 2);
-        bulk_copy_g2s(sm.qbuf[ub],
-                      p.q + ((long long)pc.row * p.num_q_heads + (long long)k * G) * kHeadDim,
-                      G * kHeadDim * 2, &sm.qfull[ub]);
+        if (waited || p.early_q) bulk_copy_g2s(sm.qbuf[ub], qsrc, G * kHeadDim * 2, &sm.qfull[ub]);
+      }
+      if (!waited && !p.early_q) {
+        q_pend |= 1 << ub;
+        if (ub == 0) q_src0 = qsrc; else q_src1 = qsrc;
       }
       const int32_t* bt = p.block_tables + (long long)pc.r * p.max_blocks + pc.b0;
       for (int bb = 0; bb < pc.nblk && !*abort_flag; bb += 32) {
@@ -484,6 +513,10 @@ __global__ void __launch_bounds__(DecodeCfg<G>::kThreads) __maxnreg__(DecodeCfg<
         for (int xb = 0; xb < cnt; ++xb, ++n) {
           int phys = __shfl_sync(0xffffffffu, ent, xb);
           const int st = n % kStages;
+          // Before blocking on the consumers, or before a block with a new token.
+          if (n >= kStages || pc.b0 + bb + xb >= pc.fresh) {
+            if (!waited || q_pend) take_wait();
+          }
           [[maybe_unused]] const unsigned long long tw0 = TRACE_NOW();
           if (n >= kStages &&
               !mbar_wait(&sm.empty[st], ((n / kStages) - 1) & 1, p.err, abort_flag))
@@ -506,6 +539,10 @@ __global__ void __launch_bounds__(DecodeCfg<G>::kThreads) __maxnreg__(DecodeCfg<
       }
       ++j;
     }
+    // The CTA finishes after the previous kernel in any case; Q copies still
+    // pending are issued unless the CTA is giving up.
+    if (*abort_flag) q_pend = 0;
+    take_wait();
     // End marker: no more pieces for this CTA.
     const int ub = j & 1;
     if (j < 2 || mbar_wait(&sm.qempty[ub], ((j >> 1) - 1) & 1, p.err, abort_flag)) {
@@ -518,6 +555,7 @@ __global__ void __launch_bounds__(DecodeCfg<G>::kThreads) __maxnreg__(DecodeCfg<
   }
 
   // ========================= consumer warps ================================
+  if (p.early_kv && !p.early_q) grid_dependency_wait();  // out and the workspace are written below
   using Cfg = DecodeCfg<G>;
   constexpr int GH = Cfg::kGH;  // heads of this warp: ho .. ho + GH - 1
   using BM = BlockMath<GH, Smem::kPStride, KV>;

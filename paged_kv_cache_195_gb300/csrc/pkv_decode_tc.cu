@@ -40,6 +40,12 @@
 #include <climits>
 
 #include "pkv_internal.h"
+#if defined(PKV_TC_TRACE) && PKV_TC_TRACE >= 5
+namespace pkv {
+__device__ unsigned long long g_plan_ts[256][8];  // debug: steps of the plan
+}
+#define PKV_PLAN_TS(n) do { if (lane == 0 && blockIdx.x < 256) ::pkv::g_plan_ts[blockIdx.x][n] = ::pkv::global_timer_ns(); } while (0)
+#endif
 #include "pkv_plan.cuh"
 #include "pkv_tc.cuh"
 
@@ -82,6 +88,19 @@ __device__ unsigned long long g_tc_trace[7][kTrTiles];
 #define TC_TR(ev, tile) do { if (blockIdx.x == 0 && (tile) < kTrTiles) g_tc_trace[ev][tile] = global_timer_ns(); } while (0)
 #else
 #define TC_TR(ev, tile) do { } while (0)
+#endif
+// With PKV_TC_TRACE >= 3 also a per-CTA timeline of the whole kernel: entry,
+// set-up done, producer past the grid-dependency wait, first load issued,
+// first keys seen by the MMA warp, last PV issued, last piece written, exit.
+#if PKV_TC_TRACE >= 3
+// Slots by the out pointer, so that consecutive launches keep their own.
+constexpr int kTrCtas = 256, kTrSlots = 32;
+__device__ unsigned long long g_tc_cta[kTrSlots][kTrCtas][14];
+#define TC_CTA(ev) do { if (blockIdx.x < kTrCtas) g_tc_cta[(uint32_t)((reinterpret_cast<uintptr_t>(p.out) >> 8) * 0x9E3779B1u) >> 27][blockIdx.x][ev] = global_timer_ns(); } while (0)
+#define TC_CTA_VAL(ev, v) do { if (blockIdx.x < kTrCtas) g_tc_cta[(uint32_t)((reinterpret_cast<uintptr_t>(p.out) >> 8) * 0x9E3779B1u) >> 27][blockIdx.x][ev] = (v); } while (0)
+#else
+#define TC_CTA(ev) do { } while (0)
+#define TC_CTA_VAL(ev, v) do { } while (0)
 #endif
 
 struct __align__(1024) TcSmem {
@@ -129,6 +148,59 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   volatile int* abort_flag = &sm.abort_flag;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hkv = p.num_kv_heads;
+  if (tid == 0) TC_CTA(0);
+#if PKV_TC_TRACE >= 3
+  if (tid == 0) {
+    uint32_t smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    TC_CTA_VAL(8, smid + 1);
+  }
+#endif
+  // The producer plans before the CTA's set-up whenever the plan's inputs
+  // may be read before the grid-dependency wait: seq_lens and
+  // query_start_loc (early_plan), and with early_kv also the block table.
+  const bool early_plan = p.early_plan || p.early_kv;
+  plan::Range rg;
+  plan::Walker wk;
+  Piece pc, pn;
+  bool have = false, have_n = false;
+  int ent_first = kPastPiece, ent_first_n = kPastPiece;
+  // Block-table entries are loaded 32 blocks (four tiles) at a time and
+  // well before use -- the next group while a group is issued, the next
+  // piece's first group while a piece is issued -- and checked only when
+  // used, so the producer never waits on the table.
+  auto raw_entries = [&](const Piece& q, int x0) {
+    const int x = x0 + lane;
+    return x < q.nblk ? __ldg(p.block_tables + (long long)q.r * p.max_blocks + q.b0 + x)
+                      : kPastPiece;
+  };
+  auto plan_first = [&]() {
+    if (p.prefetch) plan::prefetch_block_table(p, lane);
+    plan::plan_cta(p, lane, rg, wk);
+    if (lane == 0) TC_CTA(10);
+#if PKV_TC_TRACE >= 4
+    {  // the same plan again (warm caches), for the timeline only
+      plan::Range rg2;
+      plan::Walker wk2;
+      plan::plan_cta(p, lane, rg2, wk2);
+      if (lane == 0) TC_CTA_VAL(12, global_timer_ns() + (rg2.lo == rg.lo ? 0 : 1));
+      const int x = __ldg(p.seq_lens + (lane * 7) % p.num_reqs);
+      if (lane == 0) TC_CTA_VAL(13, global_timer_ns() + (x == -12345 ? 1 : 0));
+    }
+#endif
+    have = wk.next(p, pc);
+    if (p.early_kv && have) ent_first = raw_entries(pc, 0);  // in flight during next()
+    have_n = have && wk.next(p, pn);
+    if (lane == 0) TC_CTA(11);
+  };
+  auto first_entries = [&]() {
+    if (!p.early_kv && have) ent_first = raw_entries(pc, 0);
+    if (have_n) ent_first_n = raw_entries(pn, 0);
+  };
+  if (warp == 4 && early_plan) {
+    plan_first();
+    if (p.early_kv) first_entries();
+  }
 
   if (tid == 0) {
     for (int b = 0; b < 2; ++b) {
@@ -173,40 +245,59 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
+  if (tid == 0) TC_CTA(1);
   // Consumers wait for the previous kernel on the stream here; the producer
   // builds its plan first (it reads only seq_lens / query_start_loc, which
   // with early_plan set the previous kernel does not write).  Each thread
   // lets the next kernel launch only after its own wait.
-  if (warp != 4 || !p.early_plan) {
+  //
+  // With early_kv the previous kernel is the append of this step's new
+  // tokens: before the wait this kernel reads the lengths, the block table
+  // and the K/V tiles without a new token, and the producer waits before the
+  // first tile that holds one (and before it blocks on a consumer); the
+  // softmax and MMA warps read only what it stages.  If that append lets this
+  // grid launch as soon as the append starts (early_q unset), q, out and the
+  // workspace may still belong to the kernel before the append: Q copies are
+  // then issued after the wait and the epilogue waits before its first write.
+  if (!p.early_kv && (warp != 4 || !p.early_plan)) {
     grid_dependency_wait();
     allow_dependent_launch();
   }
 
   if (warp == 4) {
     // ========================= plan + TMA producer ========================
-    if (p.prefetch) plan::prefetch_block_table(p, lane);
-    const plan::Range rg = plan::cta_range(p, lane);
-    if (p.early_plan) {
+    bool waited = !p.early_kv;
+    if (!early_plan) plan_first();  // after the wait above
+    if (p.early_plan && !p.early_kv) {
       grid_dependency_wait();
       allow_dependent_launch();
     }
+    if (!p.early_kv) first_entries();
+    if (lane == 0) TC_CTA(2);
     const int oob_row = p.num_blocks * Hkv * kBlockSize;  // zero-filled by TMA
-    plan::Walker wk;
-    wk.start(p, rg, lane);
-    // Block-table entries are loaded 32 blocks (four tiles) at a time and
-    // well before use -- the next group while a group is issued, the next
-    // piece's first group while a piece is issued -- and checked only when
-    // used, so the producer never waits on the table.
-    auto raw_entries = [&](const Piece& q, int x0) {
-      const int x = x0 + lane;
-      return x < q.nblk ? __ldg(p.block_tables + (long long)q.r * p.max_blocks + q.b0 + x)
-                        : kPastPiece;
+    // Every K/V tile is read once per call: evict it from L2 first, so that
+    // the small per-step arrays (lengths, tables, q) stay cached.
+    const uint64_t pol = l2_policy_evict_first();
+    // Q copies of pieces met before the wait (at most the two buffers'),
+    // issued once it has been taken.
+    int q_pend = 0, q_row0 = 0, q_row1 = 0, q_k0 = 0, q_k1 = 0;
+    auto issue_q = [&](int ub, int row, int kh) {
+      if (lane == 0) {
+        tma_load_3d(sm.q[ub][0], &qmap, 0, kh * G, row, &sm.q_full[ub]);
+        tma_load_3d(sm.q[ub][1], &qmap, 64, kh * G, row, &sm.q_full[ub]);
+      }
     };
-    Piece pc, pn;
-    bool have = wk.next(p, pc);
-    bool have_n = have && wk.next(p, pn);
-    int ent_first = have ? raw_entries(pc, 0) : kPastPiece;
-    int ent_first_n = have_n ? raw_entries(pn, 0) : kPastPiece;
+    auto take_wait = [&]() {
+      if (!waited) {
+        grid_dependency_wait();  // the append of this step's tokens is complete
+        allow_dependent_launch();
+        waited = true;
+        if (lane == 0) TC_CTA(9);
+      }
+      if (q_pend & 1) issue_q(0, q_row0, q_k0);
+      if (q_pend & 2) issue_q(1, q_row1, q_k1);
+      q_pend = 0;
+    };
     int j = 0, t = 0;  // piece and tile counters
     bool ok = true;
     while (ok && have && !*abort_flag) {
@@ -220,6 +311,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (tt + 4 < ntile) ent_nxt = raw_entries(pc, (tt + 4) * kBlkPerTile);
         }
         const int st = t % kStages;
+        // Before blocking on the consumers, or before a tile with a new token.
+        if (t >= kStages || pc.b0 + min(pc.nblk, (tt + 1) * kBlkPerTile) - 1 >= pc.fresh) {
+          if (!waited || q_pend) take_wait();
+        }
         if (t >= kStages &&
             !mbar_wait(&sm.kv_empty[st], ((t / kStages) - 1) & 1, p.err, abort_flag)) {
           ok = false;
@@ -227,6 +322,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         if (lane == 0 && t >= kStages) TC_TR(4, t - kStages);
         if (lane == 0) TC_TR(0, t);
+        if (lane == 0 && t == 0) TC_CTA(3);
         if (lane == 0) {
           mbar_arrive_expect_tx(&sm.k_full[st], 2u * kHalf);
           mbar_arrive_expect_tx(&sm.v_full[st], 2u * kHalf);
@@ -240,23 +336,36 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           int row = oob_row;
           if ((unsigned)phys < (unsigned)p.num_blocks) row = (phys * Hkv + k) * kBlockSize;
           else if (phys != kPastPiece && hsel == 0) record_error(p.err, kErrBounds);
-          tma_load_2d(sm.k[st][hsel] + bsel * 2048, &kmap, hsel * 64, row, &sm.k_full[st]);
-          tma_load_2d(sm.v[st][hsel] + bsel * 2048, &vmap, hsel * 64, row, &sm.v_full[st]);
+          tma_load_2d(sm.k[st][hsel] + bsel * 2048, &kmap, hsel * 64, row, &sm.k_full[st], pol);
+          tma_load_2d(sm.v[st][hsel] + bsel * 2048, &vmap, hsel * 64, row, &sm.v_full[st], pol);
         }
         __syncwarp();
         if (tt == 0) {
           // Q of this piece, once the MMAs of piece j-2 are done with its
           // buffer (the piece's first K/V tile is already on its way).
           const int ub = j & 1;
-          if (j >= 2 && !mbar_wait(&sm.q_empty[ub], ((j >> 1) - 1) & 1, p.err, abort_flag)) {
-            ok = false;
-            break;
+          if (j >= 2) {
+            if (!waited || q_pend) take_wait();
+            if (!mbar_wait(&sm.q_empty[ub], ((j >> 1) - 1) & 1, p.err, abort_flag)) {
+              ok = false;
+              break;
+            }
           }
           if (lane == 0) {
             sm.pinfo[ub] = pc;
             mbar_arrive_expect_tx(&sm.q_full[ub], 2u * 64u * G * 2u);
-            tma_load_3d(sm.q[ub][0], &qmap, 0, k * G, pc.row, &sm.q_full[ub]);
-            tma_load_3d(sm.q[ub][1], &qmap, 64, k * G, pc.row, &sm.q_full[ub]);
+          }
+          if (waited || p.early_q) {
+            issue_q(ub, pc.row, k);
+          } else {
+            q_pend |= 1 << ub;
+            if (ub == 0) {
+              q_row0 = pc.row;
+              q_k0 = k;
+            } else {
+              q_row1 = pc.row;
+              q_k1 = k;
+            }
           }
           if (pc.pre) {
             // The epilogue will fold the prefix pass's partial states of
@@ -283,6 +392,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       have_n = have && wk.next(p, pn);
       ent_first_n = have_n ? raw_entries(pn, 0) : kPastPiece;
     }
+    // The CTA finishes after the previous kernel in any case; Q copies still
+    // pending are issued unless the CTA is giving up.
+    if (*abort_flag) q_pend = 0;
+    take_wait();
     // End marker: no more pieces for this CTA.
     const int ub = j & 1;
     if (j < 2 || mbar_wait(&sm.q_empty[ub], ((j >> 1) - 1) & 1, p.err, abort_flag)) {
@@ -310,6 +423,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           ok = ok && mbar_wait(&sm.o_empty[ob], ((j >> 1) - 1) & 1, p.err, abort_flag);
         if (!ok) return;
         TC_TR(3, tt);
+        TC_CTA(5);
         tc_fence_after();
         #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
@@ -341,6 +455,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (PKV_TC_PV_FIRST && tt >= 1) pv(t - 1, tt == 1, j);
           ok = ok && mbar_wait(&sm.k_full[st], (t / kStages) & 1, p.err, abort_flag);
           TC_TR(1, t);
+          if (t == 0) TC_CTA(4);
           if (t >= 2) ok = ok && mbar_wait(&sm.s_free[b], ((t >> 1) - 1) & 1, p.err, abort_flag);
           if (!ok) break;
           tc_fence_after();
@@ -505,6 +620,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int d = (warp & 3) * 32 + lane;
       const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
       constexpr int kEpiThreads = 128;
+      if (p.early_kv && !p.early_q) grid_dependency_wait();  // before writing out or the workspace
       for (int j = 0;; ++j) {
         const int ob = j & 1;
         const bool got = mbar_wait(&sm.st_full[ob], (j >> 1) & 1, p.err, abort_flag);
@@ -624,6 +740,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           named_barrier(kBarEpi, kEpiThreads);  // sm.is_last is free again
         }
+        if (d == 0) TC_CTA(6);
       }
     }
   }
@@ -633,6 +750,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 5) tmem_dealloc(tmem, kTmemCols);
+  if (tid == 0) TC_CTA(7);
 }
 
 template <int G>
@@ -668,7 +786,25 @@ cudaError_t launch_decode_tc_g(const DecodeTcLaunch& L, cudaStream_t stream) {
 
 #if PKV_TC_TRACE
 cudaError_t decode_tc_trace(void* host, size_t bytes) {
-  return cudaMemcpyFromSymbol(host, g_tc_trace, bytes < sizeof(g_tc_trace) ? bytes : sizeof(g_tc_trace));
+  // [tile timeline of CTA 0][per-CTA timeline][append kernel's per-block timeline]
+  cudaError_t e =
+      cudaMemcpyFromSymbol(host, g_tc_trace, bytes < sizeof(g_tc_trace) ? bytes : sizeof(g_tc_trace));
+#if PKV_TC_TRACE >= 3
+  if (e == cudaSuccess && bytes > sizeof(g_tc_trace)) {
+    const size_t rest = bytes - sizeof(g_tc_trace);
+    uint8_t* h = static_cast<uint8_t*>(host) + sizeof(g_tc_trace);
+    e = cudaMemcpyFromSymbol(h, g_tc_cta, rest < sizeof(g_tc_cta) ? rest : sizeof(g_tc_cta));
+    if (e == cudaSuccess && rest > sizeof(g_tc_cta))
+      e = append_trace(h + sizeof(g_tc_cta), rest - sizeof(g_tc_cta));
+#if PKV_TC_TRACE >= 5
+    const size_t ap_bytes = 32 * 256 * 4 * 8;
+    if (e == cudaSuccess && rest > sizeof(g_tc_cta) + ap_bytes)
+      e = cudaMemcpyFromSymbol(h + sizeof(g_tc_cta) + ap_bytes, g_plan_ts,
+                               std::min(rest - sizeof(g_tc_cta) - ap_bytes, sizeof(g_plan_ts)));
+#endif
+  }
+#endif
+  return e;
 }
 #endif
 

@@ -23,6 +23,9 @@ struct AppendParams {
   int num_kv_heads;
   int num_blocks;
   int pdl;  // launch with programmatic stream serialization
+  // Let the next kernel (an attention kernel that reads only blocks without
+  // these tokens before its own wait) launch before this one's wait.
+  int early_trigger;
 };
 
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
@@ -75,6 +78,18 @@ struct DecodeParams {
   int align_slack;    // ... if that lengthens the per-CTA range by at most this many blocks
   int prefetch;       // warm L2 with the block-table rows this CTA will likely read
   int early_plan;     // plan from seq_lens / query_start_loc before the PDL wait
+  // The kernel before this one on the stream is the append of exactly this
+  // step's new tokens (positions L - q_r .. L - 1 of each request): q, the
+  // block table and every K/V tile holding none of those positions are read
+  // before the PDL wait, which is taken only before the first tile that does.
+  int early_kv;
+  // With early_kv: the append waited for its own predecessor before letting
+  // this kernel launch, so q, out and the workspace are free as well (else
+  // they wait for the append like the tiles with new tokens).
+  int early_q;
+  // Per-CTA plan cache in the workspace (see pkv_plan.cuh), or null.
+  int* plan_cache;
+  int plan_entries;
   // Shared-prefix (cascade) calls: the first table column each request reads
   // ([R], or null), and the prefix pass's partial states to merge
   // ([Tq, Hq, 128] normalised outputs and [Tq, Hq] (max, normaliser)).
@@ -85,9 +100,14 @@ struct DecodeParams {
 };
 
 // Workspace carve-up shared by the host code that sizes it and the launcher.
+// Decode plans are cached for steps of up to kPlanCacheReqs requests, one
+// entry of kPlanEntryWords int32 words per CTA index.
+constexpr int kPlanCacheReqs = 256;
+constexpr int kPlanEntryWords = 576;
+
 struct WorkspaceLayout {
-  size_t cnt_off, ml_off, o_off, total;
-  int num_slots;
+  size_t cnt_off, plan_off, ml_off, o_off, total;
+  int num_slots, plan_entries;
 };
 
 WorkspaceLayout decode_workspace_layout(int num_q_tokens, int num_kv_heads, int group,
@@ -211,6 +231,9 @@ cudaError_t decode_trace(void* host, size_t bytes);
 #endif
 #if PKV_TC_TRACE
 cudaError_t decode_tc_trace(void* host, size_t bytes);
+#if PKV_TC_TRACE >= 3
+cudaError_t append_trace(void* host, size_t bytes);
+#endif
 #endif
 #ifndef PKV_PF_TRACE
 #define PKV_PF_TRACE 0

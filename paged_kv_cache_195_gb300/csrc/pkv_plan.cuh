@@ -20,11 +20,22 @@
 
 #include "pkv_internal.h"
 
+// Debug-only timestamps inside the plan (an includer may define it).
+#ifndef PKV_PLAN_TS
+#define PKV_PLAN_TS(n) do { } while (0)
+#endif
+
 namespace pkv {
 namespace plan {
 
 __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
-__device__ __forceinline__ long long cdiv_ll(long long a, long long b) { return (a + b - 1) / b; }
+// a / b for a >= 0, b > 0: a 32-bit division whenever both fit (the usual
+// case; a 64-bit division is several times longer).
+__device__ __forceinline__ long long div_ll(long long a, long long b) {
+  if ((unsigned long long)(a | b) <= 0xffffffffull) return (unsigned)a / (unsigned)b;
+  return a / b;
+}
+__device__ __forceinline__ long long cdiv_ll(long long a, long long b) { return div_ll(a + b - 1, b); }
 
 // Sum over x = 1..n of ceil(x / 16): with n = 16m + t, 8m(m+1) + t(m+1).
 __device__ __forceinline__ long long ceil16_prefix(long long n) {
@@ -39,19 +50,26 @@ struct ReqInfo {
   bool decode;  // has rows the decode kernels serve
 };
 
-__device__ __forceinline__ ReqInfo load_request(const DecodeParams& p, int r) {
+// A request's record from its raw fields (query_start_loc[r], [r + 1],
+// seq_lens[r], first_block[r]).
+__device__ __forceinline__ ReqInfo make_request(const DecodeParams& p, int q0, int q1, int L,
+                                                int fb) {
   ReqInfo ri;
-  ri.q0 = __ldg(p.qsl + r);
-  const int q1 = __ldg(p.qsl + r + 1);
-  ri.L = __ldg(p.seq_lens + r);
-  ri.qr = q1 - ri.q0;
+  ri.q0 = q0;
+  ri.L = L;
+  ri.qr = q1 - q0;
   const bool ok = ri.q0 >= 0 && ri.qr >= 0 && q1 <= p.num_q_tokens && ri.qr <= ri.L &&
                   ri.L <= p.max_blocks * kBlockSize;
   ri.decode = ok && ri.qr > 0 && ri.qr < p.prefill_min_q;
   // A shared prefix (cascade) must end before the request's first query.
-  ri.fb = p.first_block ? __ldg(p.first_block + r) : 0;
+  ri.fb = fb;
   if (ri.fb < 0 || (long long)ri.fb * kBlockSize > (long long)ri.L - ri.qr) ri.fb = 0;
   return ri;
+}
+
+__device__ __forceinline__ ReqInfo load_request(const DecodeParams& p, int r) {
+  return make_request(p, __ldg(p.qsl + r), __ldg(p.qsl + r + 1), __ldg(p.seq_lens + r),
+                      p.first_block ? __ldg(p.first_block + r) : 0);
 }
 
 // Blocks row i reads: positions fb*16 .. L - qr + i (row i sees L - qr + i + 1 keys).
@@ -71,20 +89,25 @@ struct Range {
   long long lo, hi, chunk;
 };
 
-__device__ __forceinline__ Range cta_range(const DecodeParams& p, int lane) {
-  const int R = p.num_reqs, Hkv = p.num_kv_heads;
-  long long mine = 0;
-  int nb_min = INT_MAX, nb_max = 0;
-  for (int r = lane; r < R; r += 32) {
-    const ReqInfo ri = load_request(p, r);
-    if (ri.decode) {
-      mine += rows_blocks(ri, ri.qr) * Hkv;
-      nb_min = min(nb_min, row_blocks(ri, 0));
-      nb_max = max(nb_max, row_blocks(ri, ri.qr - 1));
-    } else if (blockIdx.x == 0 && ri.qr != 0 && ri.qr < p.prefill_min_q) {
-      record_error(p.err, kErrBounds);  // inconsistent lengths: request skipped
-    }
+// Adds request r's row-groups to this lane's running totals (its blocks over
+// all rows and KV heads, the extreme row-group lengths); returns its blocks.
+__device__ __forceinline__ long long tally_request(const DecodeParams& p, const ReqInfo& ri, int r,
+                                                   long long& mine, int& nb_min, int& nb_max) {
+  long long w = 0;
+  if (ri.decode) {
+    w = rows_blocks(ri, ri.qr) * p.num_kv_heads;
+    nb_min = min(nb_min, row_blocks(ri, 0));
+    nb_max = max(nb_max, row_blocks(ri, ri.qr - 1));
+  } else if (blockIdx.x == 0 && r < p.num_reqs && ri.qr != 0 && ri.qr < p.prefill_min_q) {
+    record_error(p.err, kErrBounds);  // inconsistent lengths: request skipped
   }
+  mine += w;
+  return w;
+}
+
+// The range from the lanes' totals.  Warp-collective.
+__device__ __forceinline__ Range finish_range(const DecodeParams& p, long long mine, int nb_min,
+                                              int nb_max) {
   #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     mine += __shfl_xor_sync(0xffffffffu, mine, o);
@@ -99,7 +122,7 @@ __device__ __forceinline__ Range cta_range(const DecodeParams& p, int lane) {
     // unless that lengthens every CTA's range by more than align_slack
     // blocks (then idle CTAs cost more than the extra pieces save).
     const long long nb = nb_max;
-    const long long snapped = chunk < nb ? cdiv_ll(nb, nb / chunk) : cdiv_ll(chunk, nb) * nb;
+    const long long snapped = chunk < nb ? cdiv_ll(nb, div_ll(nb, chunk)) : cdiv_ll(chunk, nb) * nb;
     if (snapped - chunk <= p.align_slack) chunk = snapped;
   }
   Range rg;
@@ -107,6 +130,14 @@ __device__ __forceinline__ Range cta_range(const DecodeParams& p, int lane) {
   rg.lo = (long long)blockIdx.x * chunk;
   rg.hi = min(W, rg.lo + chunk);
   return rg;
+}
+
+__device__ __forceinline__ Range cta_range(const DecodeParams& p, int lane) {
+  long long mine = 0;
+  int nb_min = INT_MAX, nb_max = 0;
+  for (int r = lane; r < p.num_reqs; r += 32)
+    tally_request(p, load_request(p, r), r, mine, nb_min, nb_max);
+  return finish_range(p, mine, nb_min, nb_max);
 }
 
 // One piece of a row-group: the blocks [b0, b0 + nblk) of row `row`, KV head k.
@@ -120,6 +151,7 @@ struct Piece {
   int nblk;    // blocks in the piece (>= 1)
   int limit;   // keys visible to this row: positions < limit
   int L;       // request length (positions >= L hold no key)
+  int fresh;   // first table column holding one of this step's new tokens
   int slot;    // workspace slot of this piece's partial state (partial pieces)
   int c0;      // first CTA whose range touches the row-group
   int S;       // pieces of the row-group (1: complete in this CTA)
@@ -173,7 +205,15 @@ struct Walker {
       done = true;
       return;
     }
-    ri = load_request(p, r);
+    finish_start(p, load_request(p, r), pos);
+  }
+
+  // Request r (record q, first global block pos) holds block lo: the row,
+  // KV head and row-group the range starts in.
+  __device__ __forceinline__ void finish_start(const DecodeParams& p, const ReqInfo& q,
+                                               long long pos) {
+    const int Hkv = p.num_kv_heads;
+    ri = q;
     {  // first row of request r whose groups reach lo (binary search)
       int a = 0, b = ri.qr - 1;
       while (a < b) {
@@ -184,7 +224,7 @@ struct Walker {
     }
     g = pos + rows_blocks(ri, i) * Hkv;  // start of row i, head 0
     nb = row_blocks(ri, i);
-    k = (int)((rg.lo - g) / nb);
+    k = (int)div_ll(rg.lo - g, nb);
     g += (long long)k * nb;
     done = g >= rg.hi;
   }
@@ -193,7 +233,7 @@ struct Walker {
   __device__ __forceinline__ bool next(const DecodeParams& p, Piece& pc) {
     if (done) return false;
     const long long s0 = max(g, rg.lo), s1 = min(g + nb, rg.hi);
-    const long long c0 = g / rg.chunk, c1 = (g + nb - 1) / rg.chunk;
+    const long long c0 = div_ll(g, rg.chunk), c1 = div_ll(g + nb - 1, rg.chunk);
     pc.row = ri.q0 + i;
     pc.r = r;
     pc.k = k;
@@ -203,6 +243,7 @@ struct Walker {
     pc.nblk = (int)(s1 - s0);
     pc.limit = ri.L - ri.qr + i + 1;
     pc.L = ri.L;
+    pc.fresh = (ri.L - ri.qr) / kBlockSize;
     pc.S = (int)(c1 - c0 + 1);
     pc.c0 = (int)c0;
     pc.odd0 = g != c0 * rg.chunk;
@@ -226,6 +267,221 @@ struct Walker {
     return true;
   }
 };
+
+// Requests per lane whose records plan_cta keeps in registers: steps of up to
+// 32 * kPlanRegReqs requests are planned from one batch of loads.
+constexpr int kPlanRegReqs = 8;
+static_assert(32 * kPlanRegReqs <= kPlanCacheReqs, "plan cache too small");
+
+// Plan cache entry (one per CTA index, int32 words): the inputs the plan was
+// computed from -- a header of sizes and tuning values, query_start_loc and
+// seq_lens -- and the resulting range and walker state.  Every layer of an
+// engine step has the same lengths, so a CTA computes its plan once per step
+// and later calls compare and reuse it; the comparison is exact, so a reused
+// plan is always the plan of the current lengths.
+constexpr int kPcHeader = 10, kPcQsl = 16, kPcLens = kPcQsl + kPlanCacheReqs + 4,
+              kPcState = kPcLens + kPlanCacheReqs, kPcStateWords = 18;
+static_assert(kPcState + kPcStateWords <= kPlanEntryWords, "plan cache entry layout");
+constexpr int kPcMagic = 0x504c414e;
+
+__device__ __forceinline__ int plan_header_word(const DecodeParams& p, int j) {
+  switch (j) {
+    case 0: return p.num_reqs;
+    case 1: return p.num_q_tokens;
+    case 2: return p.num_kv_heads;
+    case 3: return p.prefill_min_q;
+    case 4: return p.min_chunk;
+    case 5: return p.align;
+    case 6: return p.align_slack;
+    case 7: return (int)gridDim.x;
+    case 8: return p.max_blocks;
+    default: return kPcMagic;
+  }
+}
+
+// The CTA's range and a walker at its first row-group: the same result as
+// cta_range followed by Walker::start, but for steps of up to 32 *
+// kPlanRegReqs requests every record is loaded once, all loads are in flight
+// together, and each lane takes a contiguous run of requests so that one
+// warp-wide scan finds the request holding the range's first block.
+// Warp-collective.
+__device__ __forceinline__ void plan_cta(const DecodeParams& p, int lane, Range& rg,
+                                         Walker& wk) {
+  const int R = p.num_reqs;
+  if (R > 32 * kPlanRegReqs) {
+    rg = cta_range(p, lane);
+    wk.start(p, rg, lane);
+    return;
+  }
+  const int per = (R + 31) / 32;  // requests per lane: r0 .. r0 + per - 1
+  const int r0 = lane * per;
+  // The cached plan of this CTA index, if any (not for shared-prefix calls,
+  // whose first blocks change with every call).
+  int* const ce = p.plan_cache != nullptr && p.first_block == nullptr &&
+                          (int)blockIdx.x < p.plan_entries
+                      ? p.plan_cache + (long long)blockIdx.x * kPlanEntryWords
+                      : nullptr;
+  int a0[kPlanRegReqs], a1[kPlanRegReqs], aL[kPlanRegReqs], aF[kPlanRegReqs];
+  int c0[kPlanRegReqs], c1[kPlanRegReqs], cL[kPlanRegReqs];
+  int ch = 0, cs = 0;
+  if (ce != nullptr) {  // issued together with the request loads below
+    if (lane < kPcHeader) ch = __ldcg(ce + lane);
+    if (lane < kPcStateWords) cs = __ldcg(ce + kPcState + lane);
+  }
+  #pragma unroll
+  for (int i = 0; i < kPlanRegReqs; ++i) {
+    const int r = r0 + i;
+    const bool in = i < per && r < R;
+    a0[i] = in ? __ldg(p.qsl + r) : 0;
+    a1[i] = in ? __ldg(p.qsl + r + 1) : 0;
+    aL[i] = in ? __ldg(p.seq_lens + r) : 0;
+    aF[i] = in && p.first_block ? __ldg(p.first_block + r) : 0;
+    const bool cin = in && ce != nullptr;
+    c0[i] = cin ? __ldcg(ce + kPcQsl + r) : 0;
+    c1[i] = cin ? __ldcg(ce + kPcQsl + r + 1) : 0;
+    cL[i] = cin ? __ldcg(ce + kPcLens + r) : 0;
+  }
+  if (ce != nullptr) {
+    bool same = lane >= kPcHeader || ch == plan_header_word(p, lane);
+    #pragma unroll
+    for (int i = 0; i < kPlanRegReqs; ++i)
+      same = same && (i >= per || (a0[i] == c0[i] && a1[i] == c1[i] && aL[i] == cL[i]));
+    if (__all_sync(0xffffffffu, same)) {
+      auto word = [&](int j) { return __shfl_sync(0xffffffffu, cs, j); };
+      auto dword = [&](int j) {
+        return (long long)(((unsigned long long)(unsigned)word(j + 1) << 32) | (unsigned)word(j));
+      };
+      rg.lo = dword(0);
+      rg.hi = dword(2);
+      rg.chunk = dword(4);
+      wk.rg = rg;
+      wk.g = dword(6);
+      wk.r = word(8);
+      wk.i = word(9);
+      wk.k = word(10);
+      wk.nb = word(11);
+      wk.done = word(12) != 0;
+      wk.ri.q0 = word(13);
+      wk.ri.qr = word(14);
+      wk.ri.L = word(15);
+      wk.ri.fb = word(16);
+      wk.ri.decode = word(17) != 0;
+      return;
+    }
+  }
+  // After computing: record the plan in the cache (the next calls with these
+  // lengths reuse it).  Lanes that share a query_start_loc entry write the
+  // same value.
+  auto record = [&]() {
+    if (ce == nullptr) return;
+    #pragma unroll
+    for (int i = 0; i < kPlanRegReqs; ++i) {
+      const int r = r0 + i;
+      if (i < per && r < R) {
+        __stcg(ce + kPcQsl + r, a0[i]);
+        __stcg(ce + kPcQsl + r + 1, a1[i]);
+        __stcg(ce + kPcLens + r, aL[i]);
+      }
+    }
+    int sv = 0;
+    auto put = [&](int j, int v) { if (lane == j) sv = v; };
+    auto put2 = [&](int j, long long v) {
+      put(j, (int)(unsigned)(unsigned long long)v);
+      put(j + 1, (int)(unsigned)((unsigned long long)v >> 32));
+    };
+    put2(0, wk.rg.lo);
+    put2(2, wk.rg.hi);
+    put2(4, wk.rg.chunk);
+    put2(6, wk.g);
+    put(8, wk.r);
+    put(9, wk.i);
+    put(10, wk.k);
+    put(11, wk.nb);
+    put(12, wk.done ? 1 : 0);
+    put(13, wk.ri.q0);
+    put(14, wk.ri.qr);
+    put(15, wk.ri.L);
+    put(16, wk.ri.fb);
+    put(17, wk.ri.decode ? 1 : 0);
+    if (lane < kPcStateWords) __stcg(ce + kPcState + lane, sv);
+    if (lane < kPcHeader) __stcg(ce + lane, plan_header_word(p, lane));
+    __threadfence();
+  };
+  PKV_PLAN_TS(0);
+  long long w[kPlanRegReqs];
+  long long mine = 0;
+  int nb_min = INT_MAX, nb_max = 0;
+  #pragma unroll
+  for (int i = 0; i < kPlanRegReqs; ++i) {
+    w[i] = 0;
+    if (i < per) {  // warp-uniform: the iterations past the runs are skipped
+      const int r = r0 + i;
+      ReqInfo q = make_request(p, a0[i], a1[i], aL[i], aF[i]);
+      q.decode = q.decode && r < R;
+      w[i] = tally_request(p, q, r, mine, nb_min, nb_max);
+    }
+  }
+  const long long own_total = mine;
+  PKV_PLAN_TS(1);
+  rg = finish_range(p, mine, nb_min, nb_max);
+  PKV_PLAN_TS(2);
+  wk.rg = rg;
+  wk.done = rg.lo >= rg.hi;
+  if (wk.done) {
+    wk.g = 0;
+    wk.r = wk.i = wk.k = wk.nb = 0;
+    wk.ri = ReqInfo{0, 0, 0, 0, false};
+    record();
+    return;
+  }
+  // Blocks of the requests before this lane's run (exclusive scan).
+  long long incl = own_total;
+  #pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  const long long base = incl - own_total;
+  const unsigned own = __ballot_sync(0xffffffffu, own_total > 0 && base <= rg.lo && rg.lo < incl);
+  if (own == 0) {
+    record_error(p.err, kErrBounds);  // unreachable when the lengths are stable
+    wk.done = true;
+    return;
+  }
+  const int owner = __ffs(own) - 1;
+  PKV_PLAN_TS(3);
+  // The owner lane walks its run to the request that holds block lo.
+  int fr = 0, f0 = 0, f1 = 0, fL = 0, fF = 0;
+  long long pos = 0;
+  if (lane == owner) {
+    long long acc = base;
+    bool found = false;
+    #pragma unroll
+    for (int i = 0; i < kPlanRegReqs; ++i) {
+      if (i < per && !found && w[i] > 0 && rg.lo < acc + w[i]) {
+        found = true;
+        fr = r0 + i;
+        f0 = a0[i];
+        f1 = a1[i];
+        fL = aL[i];
+        fF = aF[i];
+        pos = acc;
+      }
+      acc += w[i];
+    }
+  }
+  fr = __shfl_sync(0xffffffffu, fr, owner);
+  f0 = __shfl_sync(0xffffffffu, f0, owner);
+  f1 = __shfl_sync(0xffffffffu, f1, owner);
+  fL = __shfl_sync(0xffffffffu, fL, owner);
+  fF = __shfl_sync(0xffffffffu, fF, owner);
+  pos = __shfl_sync(0xffffffffu, pos, owner);
+  wk.r = fr;
+  PKV_PLAN_TS(4);
+  wk.finish_start(p, make_request(p, f0, f1, fL, fF), pos);
+  PKV_PLAN_TS(5);
+  record();
+}
 
 // Warms L2 with the part of the block table this CTA will probably read (its
 // share of the step if every row were full).

@@ -421,3 +421,56 @@ def test_copy_blocks_out_of_range_is_reported():
     pkv.pkv_copy_blocks(inp.k_pool, inp.v_pool, inp.k_pool, inp.v_pool, pairs)
     assert pkv.pkv_get_device_error() == pkv._binding.PKV_ERR_DEVICE_BOUNDS
     assert np.array_equal(wl.bf16_bits(inp.k_pool), before)
+
+
+@pytest.mark.parametrize("R", [31, 32, 33, 100, 255, 256, 257, 600])
+@pytest.mark.parametrize("g", [2, 6])
+def test_plan_request_counts(R, g):
+    # the decode plan batches the request records of small steps (up to 256
+    # requests) and walks larger steps in rounds; both must cut the step the
+    # same way the oracle reads it
+    rng = np.random.default_rng(700 + R + g)
+    lens = rng.integers(1, 90, size=R)
+    shape = wl.StepShape(f"plan_r{R}_g{g}", lens, np.ones(R, np.int32), 2 * g, 2, seed=700 + R)
+    _full_parity(shape)
+
+
+def test_plan_cache_follows_lengths(monkeypatch):
+    # One workspace across calls whose lengths change and come back: the
+    # cached per-CTA plans are reused only for identical lengths, so every
+    # call matches the oracle, and equals a call with caching switched off.
+    R = 40
+    rng = np.random.default_rng(720)
+    shapes = []
+    for seed in (721, 722, 721):
+        lens = np.random.default_rng(seed).integers(5, 400, size=R)
+        shapes.append(wl.StepShape(f"plan_cache_{seed}", lens, np.ones(R, np.int32), 12, 2,
+                                   seed=seed))
+    d = None
+    ws = None
+    for shape in shapes:
+        inp = wl.make_step(shape, device="cuda")
+        h = host_copy(inp)
+        kp, vp = oracle_pools_after_append(h)
+        if ws is None:
+            d = pkv.make_dims(tuple(inp.q.shape), tuple(inp.k_pool.shape), R,
+                              max(s.max_blocks_per_req for s in shapes))
+            ws = pkv.Workspace(d)
+            pkv.pkv_workspace_init(ws, d)
+        bt = torch.full((R, d.max_blocks_per_req), -1, dtype=torch.int32, device="cuda")
+        bt[:, :inp.block_tables.shape[1]] = inp.block_tables
+        pkv.pkv_append(inp.k_new, inp.v_new, inp.slot_mapping, inp.k_pool, inp.v_pool)
+        outs = []
+        for _ in range(2):  # the second call reuses the plans of the first
+            outs.append(pkv.pkv_attention(inp.q, inp.k_pool, inp.v_pool, bt, inp.seq_lens,
+                                          inp.query_start_loc, inp.scale, workspace=ws))
+        monkeypatch.setenv("PKV_PLAN_CACHE", "0")
+        outs.append(pkv.pkv_attention(inp.q, inp.k_pool, inp.v_pool, bt, inp.seq_lens,
+                                      inp.query_start_loc, inp.scale, workspace=ws))
+        monkeypatch.delenv("PKV_PLAN_CACHE")
+        torch.cuda.synchronize()
+        assert pkv.pkv_get_device_error() == 0, pkv.pkv_last_error()
+        assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+        bt_h = bt.cpu().numpy()
+        h["block_tables"] = bt_h
+        assert_close(to_f64(outs[0]), oracle_full(h, kp, vp), shape.name)
