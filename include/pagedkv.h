@@ -149,11 +149,12 @@ int pkv_workspace_init(void *workspace, size_t workspace_bytes,
  * Launch overlap: unless the environment sets PKV_PDL=0, the kernels are
  * launched with programmatic dependent launch and may start while the
  * kernel before them on the stream is still running.  They wait for it
- * before touching q, the pools, block_tables, out or the workspace, but read
- * seq_lens and query_start_loc before that wait (PKV_EARLY_PLAN=0 moves
- * those reads after it).  So the kernel issued immediately before this call
- * must not write seq_lens or query_start_loc; pkv_append, which writes only
- * pool slots, and host-to-device copies may.
+ * before touching q, the pools, out or the workspace, but read seq_lens,
+ * query_start_loc and (in the tensor-core decode) block_tables before that
+ * wait (PKV_EARLY_PLAN=0 moves those reads after it).  So the kernel issued
+ * immediately before this call must not write seq_lens, query_start_loc or
+ * block_tables; pkv_append, which writes only pool slots, and host-to-device
+ * copies may.
  * Source: The Serving Playbook, "The block table lives in the hottest kernel
  * in the system" (gather through the table, partial softmax per piece of the
  * cache, rescaling pass), "Kernel fusion, briefly" (Flash-Decoding splits the

@@ -40,12 +40,6 @@
 #include <climits>
 
 #include "pkv_internal.h"
-#if defined(PKV_TC_TRACE) && PKV_TC_TRACE >= 5
-namespace pkv {
-__device__ unsigned long long g_plan_ts[256][8];  // debug: steps of the plan
-}
-#define PKV_PLAN_TS(n) do { if (lane == 0 && blockIdx.x < 256) ::pkv::g_plan_ts[blockIdx.x][n] = ::pkv::global_timer_ns(); } while (0)
-#endif
 #include "pkv_plan.cuh"
 #include "pkv_tc.cuh"
 
@@ -89,13 +83,17 @@ __device__ unsigned long long g_tc_trace[7][kTrTiles];
 #else
 #define TC_TR(ev, tile) do { } while (0)
 #endif
-// With PKV_TC_TRACE >= 3 also a per-CTA timeline of the whole kernel: entry,
-// set-up done, producer past the grid-dependency wait, first load issued,
-// first keys seen by the MMA warp, last PV issued, last piece written, exit.
+// With PKV_TC_TRACE >= 3 also a per-CTA timeline of the whole kernel, one
+// set of events per launch (slot chosen by the out pointer): 0 entry, 1
+// set-up done, 2 producer ready, 3 first load issued, 4 first keys seen by the
+// MMA warp, 5 last PV issued, 6 last piece written, 7 exit, 8 SM id + 1, 9
+// grid-dependency wait taken (early_kv), 10 plan done, 11 first pieces
+// known, 14 softmax statistics published, 15 seen by the epilogue, 16 O read
+// from TMEM, 17 last O commit issued.
 #if PKV_TC_TRACE >= 3
 // Slots by the out pointer, so that consecutive launches keep their own.
 constexpr int kTrCtas = 256, kTrSlots = 32;
-__device__ unsigned long long g_tc_cta[kTrSlots][kTrCtas][14];
+__device__ unsigned long long g_tc_cta[kTrSlots][kTrCtas][18];
 #define TC_CTA(ev) do { if (blockIdx.x < kTrCtas) g_tc_cta[(uint32_t)((reinterpret_cast<uintptr_t>(p.out) >> 8) * 0x9E3779B1u) >> 27][blockIdx.x][ev] = global_timer_ns(); } while (0)
 #define TC_CTA_VAL(ev, v) do { if (blockIdx.x < kTrCtas) g_tc_cta[(uint32_t)((reinterpret_cast<uintptr_t>(p.out) >> 8) * 0x9E3779B1u) >> 27][blockIdx.x][ev] = (v); } while (0)
 #else
@@ -157,8 +155,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 #endif
   // The producer plans before the CTA's set-up whenever the plan's inputs
-  // may be read before the grid-dependency wait: seq_lens and
-  // query_start_loc (early_plan), and with early_kv also the block table.
+  // may be read before the grid-dependency wait: seq_lens, query_start_loc
+  // and the block table (early_plan).
   const bool early_plan = p.early_plan || p.early_kv;
   plan::Range rg;
   plan::Walker wk;
@@ -178,28 +176,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (p.prefetch) plan::prefetch_block_table(p, lane);
     plan::plan_cta(p, lane, rg, wk);
     if (lane == 0) TC_CTA(10);
-#if PKV_TC_TRACE >= 4
-    {  // the same plan again (warm caches), for the timeline only
-      plan::Range rg2;
-      plan::Walker wk2;
-      plan::plan_cta(p, lane, rg2, wk2);
-      if (lane == 0) TC_CTA_VAL(12, global_timer_ns() + (rg2.lo == rg.lo ? 0 : 1));
-      const int x = __ldg(p.seq_lens + (lane * 7) % p.num_reqs);
-      if (lane == 0) TC_CTA_VAL(13, global_timer_ns() + (x == -12345 ? 1 : 0));
-    }
-#endif
     have = wk.next(p, pc);
-    if (p.early_kv && have) ent_first = raw_entries(pc, 0);  // in flight during next()
+    if (early_plan && have) ent_first = raw_entries(pc, 0);  // in flight during next()
     have_n = have && wk.next(p, pn);
     if (lane == 0) TC_CTA(11);
   };
   auto first_entries = [&]() {
-    if (!p.early_kv && have) ent_first = raw_entries(pc, 0);
+    if (!early_plan && have) ent_first = raw_entries(pc, 0);
     if (have_n) ent_first_n = raw_entries(pn, 0);
   };
   if (warp == 4 && early_plan) {
     plan_first();
-    if (p.early_kv) first_entries();
+    first_entries();
   }
 
   if (tid == 0) {
@@ -247,9 +235,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t tmem = sm.tmem_base;
   if (tid == 0) TC_CTA(1);
   // Consumers wait for the previous kernel on the stream here; the producer
-  // builds its plan first (it reads only seq_lens / query_start_loc, which
-  // with early_plan set the previous kernel does not write).  Each thread
-  // lets the next kernel launch only after its own wait.
+  // builds its plan and loads its first block-table entries first (it reads
+  // only seq_lens, query_start_loc and block_tables, which with early_plan
+  // set the previous kernel does not write).  Each thread lets the next
+  // kernel launch only after its own wait.
   //
   // With early_kv the previous kernel is the append of this step's new
   // tokens: before the wait this kernel reads the lengths, the block table
@@ -272,7 +261,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       grid_dependency_wait();
       allow_dependent_launch();
     }
-    if (!p.early_kv) first_entries();
+    if (!early_plan) first_entries();
     if (lane == 0) TC_CTA(2);
     const int oob_row = p.num_blocks * Hkv * kBlockSize;  // zero-filled by TMA
     // Every K/V tile is read once per call: evict it from L2 first, so that
@@ -477,6 +466,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         if (ok) pv(t - 1, ntile == 1, j);  // the piece's last tile
         tc_commit(&sm.o_full[ub]);
+        TC_CTA(17);
         tc_commit(&sm.q_empty[ub]);
       }
     }
@@ -605,6 +595,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.st_full[ub]);
+        if (warp == 0 && lane == 0) TC_CTA(14);
       }
       // End marker for the epilogue.
       {
@@ -626,6 +617,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const bool got = mbar_wait(&sm.st_full[ob], (j >> 1) & 1, p.err, abort_flag);
         const Piece pc = sm.st_pc[ob];
         if (barrier_or(kBarEpi, kEpiThreads, !got || pc.row == kEndRow)) break;
+        if (d == 0) TC_CTA(15);
         float m[8], lt[8];
         #pragma unroll
         for (int h = 0; h < G; ++h) {
@@ -637,6 +629,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         float o[8];
         tmem_ld8(tmem + lane_off + kColO + ob * kN, o);
         tc_wait_ld();
+        if (d == 0) TC_CTA(16);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
@@ -796,12 +789,6 @@ cudaError_t decode_tc_trace(void* host, size_t bytes) {
     e = cudaMemcpyFromSymbol(h, g_tc_cta, rest < sizeof(g_tc_cta) ? rest : sizeof(g_tc_cta));
     if (e == cudaSuccess && rest > sizeof(g_tc_cta))
       e = append_trace(h + sizeof(g_tc_cta), rest - sizeof(g_tc_cta));
-#if PKV_TC_TRACE >= 5
-    const size_t ap_bytes = 32 * 256 * 4 * 8;
-    if (e == cudaSuccess && rest > sizeof(g_tc_cta) + ap_bytes)
-      e = cudaMemcpyFromSymbol(h + sizeof(g_tc_cta) + ap_bytes, g_plan_ts,
-                               std::min(rest - sizeof(g_tc_cta) - ap_bytes, sizeof(g_plan_ts)));
-#endif
   }
 #endif
   return e;

@@ -20,11 +20,6 @@
 
 #include "pkv_internal.h"
 
-// Debug-only timestamps inside the plan (an includer may define it).
-#ifndef PKV_PLAN_TS
-#define PKV_PLAN_TS(n) do { } while (0)
-#endif
-
 namespace pkv {
 namespace plan {
 
@@ -407,7 +402,6 @@ __device__ __forceinline__ void plan_cta(const DecodeParams& p, int lane, Range&
     if (lane < kPcHeader) __stcg(ce + lane, plan_header_word(p, lane));
     __threadfence();
   };
-  PKV_PLAN_TS(0);
   long long w[kPlanRegReqs];
   long long mine = 0;
   int nb_min = INT_MAX, nb_max = 0;
@@ -422,9 +416,7 @@ __device__ __forceinline__ void plan_cta(const DecodeParams& p, int lane, Range&
     }
   }
   const long long own_total = mine;
-  PKV_PLAN_TS(1);
   rg = finish_range(p, mine, nb_min, nb_max);
-  PKV_PLAN_TS(2);
   wk.rg = rg;
   wk.done = rg.lo >= rg.hi;
   if (wk.done) {
@@ -449,7 +441,6 @@ __device__ __forceinline__ void plan_cta(const DecodeParams& p, int lane, Range&
     return;
   }
   const int owner = __ffs(own) - 1;
-  PKV_PLAN_TS(3);
   // The owner lane walks its run to the request that holds block lo.
   int fr = 0, f0 = 0, f1 = 0, fL = 0, fF = 0;
   long long pos = 0;
@@ -477,9 +468,7 @@ __device__ __forceinline__ void plan_cta(const DecodeParams& p, int lane, Range&
   fF = __shfl_sync(0xffffffffu, fF, owner);
   pos = __shfl_sync(0xffffffffu, pos, owner);
   wk.r = fr;
-  PKV_PLAN_TS(4);
   wk.finish_start(p, make_request(p, f0, f1, fL, fF), pos);
-  PKV_PLAN_TS(5);
   record();
 }
 

@@ -96,6 +96,7 @@ struct __align__(1024) PfSmem {
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
@@ -495,22 +496,22 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         // P = exp2(s * scale_log2 - m) in bf16 (masked keys are -inf: p = 0),
         // written over the row's S in TMEM two keys per column -- keys
         // 64 half .. +63 in columns 32 half .. +31 -- where the PV MMA reads
-        // it; the normaliser sums the rounded values the MMA will use.
-        float sump[4] = {0.f, 0.f, 0.f, 0.f};
-        const float neg_m = -m;
+        // it; the normaliser sums the rounded values the MMA will use.  Pairs
+        // of keys go through packed fp32 arithmetic (the softmax is bound by
+        // its instruction count).
+        const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+        const float2 nm2 = make_float2(-m, -m), one2 = make_float2(1.f, 1.f);
+        float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
         uint32_t w[32];
         #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          const float p0 = fast_exp2(fmaf(v[2 * e], p.scale_log2, neg_m));
-          const float p1 = fast_exp2(fmaf(v[2 * e + 1], p.scale_log2, neg_m));
-          w[e] = pack_bf16x2(p0, p1);
-          const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&w[e]);
-          sump[e & 3] += __low2float(b2) + __high2float(b2);
+          const float2 x = ffma2(make_float2(v[2 * e], v[2 * e + 1]), sc2, nm2);
+          w[e] = pack_bf16x2(fast_exp2(x.x), fast_exp2(x.y));
+          sum2[e & 1] = ffma2(bf16x2_to_float2(w[e]), one2, sum2[e & 1]);
         }
         tmem_st32(tS + half * 32, *reinterpret_cast<const float(*)[32]>(w));
         tc_wait_st();
-        const float sum = (sump[0] + sump[1]) + (sump[2] + sump[3]);
-        l += sum;
+        l += (sum2[0].x + sum2[0].y) + (sum2[1].x + sum2[1].y);
         // Keys past the request's end inside its last block may hold anything
         // (even NaN); zero those V rows so that 0 * V stays 0 in the MMA.
         const int st = tile_ctr % kPfStages;
