@@ -172,6 +172,25 @@ __device__ __forceinline__ bool barrier_or(int id, int threads, bool v) {
   return r != 0;
 }
 
+// s0 += low bf16 of w, s1 += high bf16 of w, each by one mixed-precision FMA
+// (bf16 times bf16 one, plus fp32): the same fp32 sums as widening first.
+__device__ __forceinline__ void add_bf16x2(float& s0, float& s1, uint32_t w) {
+  const unsigned short one = 0x3F80;  // bf16 1.0
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "mov.b32 {lo, hi}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, lo, %3, %0;\n\t"
+      "fma.rn.f32.bf16 %1, hi, %3, %1;\n\t}"
+      : "+f"(s0), "+f"(s1)
+      : "r"(w), "h"(one));
+}
+
+// max(a, b, c) in one instruction (the three-input form of max.f32).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -454,7 +454,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         #pragma unroll
         for (int i = 0; i < 8; ++i) mxp[i] = -INFINITY;
         #pragma unroll
-        for (int i = 0; i < 64; ++i) mxp[i & 7] = fmaxf(mxp[i & 7], v[i]);
+        for (int i = 0; i < 32; ++i) mxp[i & 7] = fmax3(mxp[i & 7], v[2 * i], v[2 * i + 1]);
         const float mxh = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
                                 fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
         // The row maximum over both halves.  The barrier also orders every
@@ -500,18 +500,18 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         // of keys go through packed fp32 arithmetic (the softmax is bound by
         // its instruction count).
         const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
-        const float2 nm2 = make_float2(-m, -m), one2 = make_float2(1.f, 1.f);
-        float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        const float2 nm2 = make_float2(-m, -m);
+        float sum_lo[2] = {0.f, 0.f}, sum_hi[2] = {0.f, 0.f};
         uint32_t w[32];
         #pragma unroll
         for (int e = 0; e < 32; ++e) {
           const float2 x = ffma2(make_float2(v[2 * e], v[2 * e + 1]), sc2, nm2);
           w[e] = pack_bf16x2(fast_exp2(x.x), fast_exp2(x.y));
-          sum2[e & 1] = ffma2(bf16x2_to_float2(w[e]), one2, sum2[e & 1]);
+          add_bf16x2(sum_lo[e & 1], sum_hi[e & 1], w[e]);
         }
         tmem_st32(tS + half * 32, *reinterpret_cast<const float(*)[32]>(w));
         tc_wait_st();
-        l += (sum2[0].x + sum2[0].y) + (sum2[1].x + sum2[1].y);
+        l += (sum_lo[0] + sum_hi[0]) + (sum_lo[1] + sum_hi[1]);
         // Keys past the request's end inside its last block may hold anything
         // (even NaN); zero those V rows so that 0 * V stays 0 in the MMA.
         const int st = tile_ctr % kPfStages;
