@@ -136,7 +136,9 @@ int pkv_workspace_init(void *workspace, size_t workspace_bytes,
  * over keys j = 0 .. L_r - q_r + i, where K_r[j] = k_pool[block_tables[r,
  * j/bs], :, j%bs, :].  Computed with fp32 accumulation and an online softmax;
  * long contexts are split across CTAs and merged by log-sum-exp (Flash-
- * Decoding); prefill chunks run on tcgen05 tensor cores.  out is written as
+ * Decoding); prefill chunks, and decode rows of groups of 4 or more query
+ * heads per KV head, run on tcgen05 tensor cores (their probabilities enter
+ * the PV product in bf16).  out is written as
  * bf16 (round to nearest even).  Requests with q_r = 0 produce nothing.
  * Preconditions: query_start_loc[0] = 0, non-decreasing, last entry =
  * num_q_tokens; 0 <= q_r <= L_r <= max_blocks_per_req * bs; table entries
