@@ -494,6 +494,7 @@ int attention_impl(const void* q, const void* k_pool, const void* v_pool, const 
     L.p.num_groups = cas->num_groups;
     L.p.pre_o = reinterpret_cast<float*>(ws + cl.pre_o);
     L.p.pre_ml = reinterpret_cast<float*>(ws + cl.pre_ml);
+    L.p.sched = reinterpret_cast<unsigned long long*>(ws + w.sched_off);
     L.grid = st->sm_count;
     e = pkv::launch_prefill(L, group, stream);
     if (e != cudaSuccess) return cuda_fail(e, "prefix pass launch");
@@ -542,6 +543,7 @@ int attention_impl(const void* q, const void* k_pool, const void* v_pool, const 
     L.p.scale_log2 = p.scale_log2;
     L.p.prefill_min_q = prefill_min_q;
     L.p.pdl = p.pdl;
+    L.p.sched = reinterpret_cast<unsigned long long*>(ws + w.sched_off);
     L.grid = st->sm_count;
     e = pkv::launch_prefill(L, group, stream);
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");

@@ -34,8 +34,10 @@ WorkspaceLayout decode_workspace_layout(int num_q_tokens, int num_kv_heads, int 
   w.num_slots = 2 * sm_count * 2;  // two partial pieces per CTA, up to two CTAs per SM
   w.plan_entries = w.num_slots / 2;  // one per CTA index of the largest grid
   w.cnt_off = 0;
-  // The plan cache sits inside the zero-initialised head of the workspace.
-  w.plan_off = up((size_t)num_q_tokens * num_kv_heads * sizeof(int));
+  // The prefill work queue and the plan cache sit inside the
+  // zero-initialised head of the workspace.
+  w.sched_off = up((size_t)num_q_tokens * num_kv_heads * sizeof(int));
+  w.plan_off = w.sched_off + 256;
   w.ml_off = w.plan_off + up((size_t)w.plan_entries * kPlanEntryWords * sizeof(int));
   w.o_off = w.ml_off + up((size_t)w.num_slots * group * 2 * sizeof(float));
   w.total = w.o_off + up((size_t)w.num_slots * group * kHeadDim * sizeof(float));

@@ -106,7 +106,7 @@ constexpr int kPlanCacheReqs = 256;
 constexpr int kPlanEntryWords = 576;
 
 struct WorkspaceLayout {
-  size_t cnt_off, plan_off, ml_off, o_off, total;
+  size_t cnt_off, sched_off, plan_off, ml_off, o_off, total;
   int num_slots, plan_entries;
 };
 
@@ -175,6 +175,9 @@ struct PrefillParams {
   int num_groups;
   float* pre_o;               // [Tq, Hq, 128] normalised partial outputs
   float* pre_ml;              // [Tq, Hq, 2] (max in log2 units, normaliser)
+  // Work queue: [0] next item, [1] CTAs done; zero between launches (the
+  // last CTA to finish resets both).
+  unsigned long long* sched;
 };
 
 // Shared-prefix (cascade) prefix pass: a group's shared keys (L of them) are

@@ -65,10 +65,16 @@ extern "C" int pkv_attention_noalloc(const void* q, const void* k_pool, const vo
     }
     scratch = g_noalloc_ptr[dev];
   }
-  // The array keeps the previous call's contents; the merge counters at its
-  // head must start at zero (their extent moves with the dims).
+  // The array keeps the previous call's contents; its head (merge counters,
+  // prefill work queue, plan cache) must start at zero: its extent moves with
+  // the dims.
+  int sm_count = 1;
+  if (cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    pkv::set_error_message("pkv_attention_noalloc: cudaDeviceGetAttribute failed");
+    return PKV_ERR_CUDA;
+  }
   const pkv::WorkspaceLayout w = pkv::decode_workspace_layout(
-      dims->num_q_tokens, dims->num_kv_heads, dims->num_q_heads / dims->num_kv_heads, 1);
+      dims->num_q_tokens, dims->num_kv_heads, dims->num_q_heads / dims->num_kv_heads, sm_count);
   if (w.ml_off > 0 && cudaMemsetAsync(scratch, 0, w.ml_off, stream) != cudaSuccess) {
     pkv::set_error_message("pkv_attention_noalloc: clearing the scratch counters failed");
     return PKV_ERR_CUDA;

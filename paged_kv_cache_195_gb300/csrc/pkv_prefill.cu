@@ -90,6 +90,8 @@ struct __align__(1024) PfSmem {
   uint64_t o_full, o_empty;
   Item items[2];
   float xrow[2][kTileRows];      // [key half][row]: half-row maxima, then normalisers
+  Item vitems[4];                // items handed from the K producer to the V producer
+  uint64_t vitem_full[4], vitem_empty[4];
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -176,7 +178,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
       total += cnt;
     }
-    if (lane == 0) sm.abort_flag = (long long)blockIdx.x >= total;  // reused as "idle"
+    if (lane == 0) {
+      sm.abort_flag = (long long)blockIdx.x >= total;  // reused as "idle"
+      sm.items[0].r = (int)min(total, (long long)gridDim.x);  // CTAs that take items
+    }
   }
   __syncthreads();
   if (sm.abort_flag) {
@@ -184,6 +189,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     grid_dependency_wait();
     return;
   }
+  const int n_active = sm.items[0].r;
   __syncthreads();
 
   if (tid == 0) {
@@ -202,6 +208,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
     mbar_init(&sm.o_full, 1);
     mbar_init(&sm.o_empty, 8);
+    for (int b = 0; b < 4; ++b) {
+      mbar_init(&sm.vitem_full[b], 1);
+      mbar_init(&sm.vitem_empty[b], 1);
+    }
     sm.abort_flag = 0;
     fence_barrier_init();
   }
@@ -234,115 +244,157 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
   if (warp == 4 || warp == 10) {
     // ==================== TMA producers (K + Q | V) =======================
-    // Both warps walk the same item sequence; each feeds its own ring.
+    // Warp 4 takes items from the work queue, streams their K tiles and Q,
+    // and hands each item to warp 10, which streams the V tiles.
     const bool vside = warp == 10;
     uint64_t* const full = vside ? sm.v_full : sm.k_full;
     uint64_t* const empty = vside ? sm.v_empty : sm.k_empty;
     const CUtensorMap* const map = vside ? &vmap : &kmap;
     int n_item = 0, tile_ctr = 0;
-    long long item = blockIdx.x;  // global item index handled next
-    long long base = 0;           // items before the current request batch
     const int oob_row = p.num_blocks * Hkv * kBlockSize;
-    const int nunits = num_units(p);
-    for (int b = 0; b < nunits && !*abort_flag; b += 32) {
-      const int rr = b + lane;
-      PfReq rq = {0, 0, 0, 0, 0, 1, false};
-      if (rr < nunits) rq = load_pf_request(p, rr, TQ);
-      const long long cnt = (long long)rq.ntiles * Hkv;
-      long long incl = cnt;
-      #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const long long t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += t;
-      }
-      const long long excl = incl - cnt;
-      const long long total = __shfl_sync(0xffffffffu, incl, 31);
-      while (item < base + total && !*abort_flag) {
-        const long long rel = item - base;
-        const unsigned own = __ballot_sync(0xffffffffu, cnt > 0 && excl <= rel && rel < incl);
-        const int src = __ffs(own) - 1;
-        const long long local = rel - __shfl_sync(0xffffffffu, excl, src);
-        const int r = __shfl_sync(0xffffffffu, rq.tab, src);
-        const int q0 = __shfl_sync(0xffffffffu, rq.q0, src);
-        const int qr = __shfl_sync(0xffffffffu, rq.qr, src);
-        const int L = __shfl_sync(0xffffffffu, rq.L, src);
-        const int ntiles = __shfl_sync(0xffffffffu, rq.ntiles, src);
-        const int nchunk = __shfl_sync(0xffffffffu, rq.nchunk, src);
-        // heavier (later) q-tiles first
-        const int qk = ntiles - 1 - (int)(local / Hkv);
-        const int qt = qk / nchunk, kc = qk % nchunk;
-        const int k = (int)(local % Hkv);
-        Item it;
-        it.r = r; it.k = k;
-        it.row0 = q0 + qt * TQ;
-        it.nt = min(TQ, qr - qt * TQ);
-        it.pos0 = L - qr + qt * TQ;
-        it.L = L;
-        it.causal = !p.prefix_mode;
-        it.kc = kc;
-        it.kt0 = it.causal ? 0 : kc * prefix_chunk_tiles(L);
-        it.nj = it.causal ? (it.pos0 + it.nt - 1) / kKeyTile + 1
-                          : min(prefix_chunk_tiles(L), ceil_div(L, kKeyTile) - it.kt0);
-        it.end = 0;
-        const int nbl = ceil_div(L, kBlockSize);
-        const int32_t* bt = p.block_tables + (long long)r * p.max_blocks;
-        // Block-table entries 32 blocks (four key tiles) per load, the next
-        // group fetched while the current one is issued, checked at use.
-        auto raw_entries = [&](int x0) {
-          const int x = it.kt0 * 8 + x0 + lane;
-          return x < nbl ? __ldg(bt + x) : kPastEnd;
-        };
-        int ent_cur = raw_entries(0);
-        int ent_nxt = it.nj > 4 ? raw_entries(32) : kPastEnd;
-        for (int j = 0; j < it.nj; ++j, ++tile_ctr) {
-          if (j > 0 && (j & 3) == 0) {
-            ent_cur = ent_nxt;
-            if (j + 4 < it.nj) ent_nxt = raw_entries((j + 4) * 8);
-          }
-          const int st = tile_ctr % kPfStages;
-          if (tile_ctr >= kPfStages &&
-              !mbar_wait(&empty[st], ((tile_ctr / kPfStages) - 1) & 1, p.err, abort_flag))
-            break;
-          if (lane == 0 && vside && tile_ctr >= kPfStages) PF_TR(4, tile_ctr - kPfStages);
-          if (lane == 0 && !vside) PF_TR(0, tile_ctr);
-          if (lane == 0) mbar_arrive_expect_tx(&full[st], 2u * kHalfBytes);
-          __syncwarp();
-          // Lanes 0..15 each copy one (block, d half); blocks past the
-          // request are read at an out-of-range row (zero fill).
-          const int bsel = lane & 7, hsel = (lane >> 3) & 1;
-          const int phys = __shfl_sync(0xffffffffu, ent_cur, (j & 3) * 8 + bsel);
-          if (lane < 16) {
-            int rowc = oob_row;
-            if ((unsigned)phys < (unsigned)p.num_blocks) rowc = (phys * Hkv + k) * kBlockSize;
-            else if (phys != kPastEnd && hsel == 0 && !vside) record_error(p.err, kErrBounds);
-            uint8_t* dst = (vside ? sm.v[st][hsel] : sm.k[st][hsel]) + bsel * 2048;
-            tma_load_2d(dst, map, hsel * 64, rowc, &full[st]);
-          }
-          __syncwarp();
-          if (j == 0 && !vside) {
-            // Q of this item, once the previous item's MMAs are done with Q
-            // (its first K/V tile is already on its way).
-            if (n_item >= 1 && !mbar_wait(&sm.q_empty, (n_item - 1) & 1, p.err, abort_flag))
-              break;
-            if (lane == 0) {
-              sm.items[n_item & 1] = it;
-              mbar_arrive_expect_tx(&sm.q_full, 2u * 64u * ROWS * 2u);
-              tma_load_3d(sm.q[0], &qmap, 0, k * G, it.row0, &sm.q_full);
-              tma_load_3d(sm.q[1], &qmap, 64, k * G, it.row0, &sm.q_full);
-            }
-            __syncwarp();
-          }
+    // The item's tiles (and, on the K side, its Q).  False if a wait gave up.
+    auto stream_item = [&](const Item& it) {
+      const int nbl = ceil_div(it.L, kBlockSize);
+      const int32_t* bt = p.block_tables + (long long)it.r * p.max_blocks;
+      // Block-table entries 32 blocks (four key tiles) per load, the next
+      // group fetched while the current one is issued, checked at use.
+      auto raw_entries = [&](int x0) {
+        const int x = it.kt0 * 8 + x0 + lane;
+        return x < nbl ? __ldg(bt + x) : kPastEnd;
+      };
+      int ent_cur = raw_entries(0);
+      int ent_nxt = it.nj > 4 ? raw_entries(32) : kPastEnd;
+      for (int j = 0; j < it.nj; ++j, ++tile_ctr) {
+        if (j > 0 && (j & 3) == 0) {
+          ent_cur = ent_nxt;
+          if (j + 4 < it.nj) ent_nxt = raw_entries((j + 4) * 8);
         }
-        ++n_item;
-        item += gridDim.x;
+        const int st = tile_ctr % kPfStages;
+        if (tile_ctr >= kPfStages &&
+            !mbar_wait(&empty[st], ((tile_ctr / kPfStages) - 1) & 1, p.err, abort_flag))
+          return false;
+        if (lane == 0 && vside && tile_ctr >= kPfStages) PF_TR(4, tile_ctr - kPfStages);
+        if (lane == 0 && !vside) PF_TR(0, tile_ctr);
+        if (lane == 0) mbar_arrive_expect_tx(&full[st], 2u * kHalfBytes);
+        __syncwarp();
+        // Lanes 0..15 each copy one (block, d half); blocks past the
+        // request are read at an out-of-range row (zero fill).
+        const int bsel = lane & 7, hsel = (lane >> 3) & 1;
+        const int phys = __shfl_sync(0xffffffffu, ent_cur, (j & 3) * 8 + bsel);
+        if (lane < 16) {
+          int rowc = oob_row;
+          if ((unsigned)phys < (unsigned)p.num_blocks) rowc = (phys * Hkv + it.k) * kBlockSize;
+          else if (phys != kPastEnd && hsel == 0 && !vside) record_error(p.err, kErrBounds);
+          uint8_t* dst = (vside ? sm.v[st][hsel] : sm.k[st][hsel]) + bsel * 2048;
+          tma_load_2d(dst, map, hsel * 64, rowc, &full[st]);
+        }
+        __syncwarp();
+        if (j == 0 && !vside) {
+          // Q of this item, once the previous item's MMAs are done with Q
+          // (its first K tile is already on its way).
+          if (n_item >= 1 && !mbar_wait(&sm.q_empty, (n_item - 1) & 1, p.err, abort_flag))
+            return false;
+          if (lane == 0) {
+            sm.items[n_item & 1] = it;
+            mbar_arrive_expect_tx(&sm.q_full, 2u * 64u * ROWS * 2u);
+            tma_load_3d(sm.q[0], &qmap, 0, it.k * G, it.row0, &sm.q_full);
+            tma_load_3d(sm.q[1], &qmap, 64, it.k * G, it.row0, &sm.q_full);
+          }
+          __syncwarp();
+        }
       }
-      base += total;
-    }
-    // end marker (the Q side owns the item slots)
-    if (!vside && (n_item == 0 || mbar_wait(&sm.q_empty, (n_item - 1) & 1, p.err, abort_flag))) {
-      if (lane == 0) {
-        sm.items[n_item & 1].end = 1;
-        mbar_arrive(&sm.q_full);
+      return true;
+    };
+    if (vside) {
+      for (;; ++n_item) {
+        const int mb = n_item & 3;
+        if (!mbar_wait(&sm.vitem_full[mb], (n_item >> 2) & 1, p.err, abort_flag)) break;
+        const Item it = sm.vitems[mb];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.vitem_empty[mb]);
+        if (it.end || !stream_item(it)) break;
+      }
+    } else {
+      // Items are numbered request by request (heavier q-tiles first within
+      // a request) and taken from the queue in that order, so each CTA's
+      // sequence increases and one forward scan over the requests serves it.
+      auto next_item = [&]() {
+        unsigned long long v = 0;
+        if (lane == 0) v = atomicAdd(p.sched, 1ull);
+        return (long long)__shfl_sync(0xffffffffu, v, 0);
+      };
+      auto hand_over = [&](const Item& it) {  // to the V producer
+        const int mb = n_item & 3;
+        if (n_item >= 4 &&
+            !mbar_wait(&sm.vitem_empty[mb], ((n_item >> 2) - 1) & 1, p.err, abort_flag))
+          return false;
+        if (lane == 0) {
+          sm.vitems[mb] = it;
+          mbar_arrive(&sm.vitem_full[mb]);
+        }
+        __syncwarp();
+        return true;
+      };
+      long long item = next_item();  // global item index handled next
+      long long base = 0;            // items before the current request batch
+      const int nunits = num_units(p);
+      bool ok = true;
+      for (int b = 0; b < nunits && ok && !*abort_flag; b += 32) {
+        const int rr = b + lane;
+        PfReq rq = {0, 0, 0, 0, 0, 1, false};
+        if (rr < nunits) rq = load_pf_request(p, rr, TQ);
+        const long long cnt = (long long)rq.ntiles * Hkv;
+        long long incl = cnt;
+        #pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const long long t = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += t;
+        }
+        const long long excl = incl - cnt;
+        const long long total = __shfl_sync(0xffffffffu, incl, 31);
+        while (item < base + total && ok && !*abort_flag) {
+          const long long rel = item - base;
+          const unsigned own = __ballot_sync(0xffffffffu, cnt > 0 && excl <= rel && rel < incl);
+          const int src = __ffs(own) - 1;
+          const long long local = rel - __shfl_sync(0xffffffffu, excl, src);
+          const int r = __shfl_sync(0xffffffffu, rq.tab, src);
+          const int q0 = __shfl_sync(0xffffffffu, rq.q0, src);
+          const int qr = __shfl_sync(0xffffffffu, rq.qr, src);
+          const int L = __shfl_sync(0xffffffffu, rq.L, src);
+          const int ntiles = __shfl_sync(0xffffffffu, rq.ntiles, src);
+          const int nchunk = __shfl_sync(0xffffffffu, rq.nchunk, src);
+          // heavier (later) q-tiles first
+          const int qk = ntiles - 1 - (int)(local / Hkv);
+          const int qt = qk / nchunk, kc = qk % nchunk;
+          Item it;
+          it.r = r;
+          it.k = (int)(local % Hkv);
+          it.row0 = q0 + qt * TQ;
+          it.nt = min(TQ, qr - qt * TQ);
+          it.pos0 = L - qr + qt * TQ;
+          it.L = L;
+          it.causal = !p.prefix_mode;
+          it.kc = kc;
+          it.kt0 = it.causal ? 0 : kc * prefix_chunk_tiles(L);
+          it.nj = it.causal ? (it.pos0 + it.nt - 1) / kKeyTile + 1
+                            : min(prefix_chunk_tiles(L), ceil_div(L, kKeyTile) - it.kt0);
+          it.end = 0;
+          ok = hand_over(it) && stream_item(it);
+          ++n_item;
+          item = next_item();
+        }
+        base += total;
+      }
+      // end markers: for the V producer, and for the MMA and softmax warps
+      // (the Q side owns the item slots)
+      Item fin = {};
+      fin.end = 1;
+      if (ok) hand_over(fin);
+      if (n_item == 0 || mbar_wait(&sm.q_empty, (n_item - 1) & 1, p.err, abort_flag)) {
+        if (lane == 0) {
+          sm.items[n_item & 1].end = 1;
+          mbar_arrive(&sm.q_full);
+        }
       }
     }
   } else if (warp == 5) {
@@ -581,6 +633,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   tc_fence_after();
   if (warp == 5) tmem_dealloc(tmem, kTmemCols);
   grid_dependency_wait();
+  // The last CTA to finish empties the work queue for the next launch (each
+  // CTA stops taking items before it gets here).
+  if (tid == 0) {
+    __threadfence();
+    if (atomicAdd(p.sched + 1, 1ull) == (unsigned long long)(n_active - 1)) {
+      p.sched[0] = 0;
+      p.sched[1] = 0;
+      __threadfence();
+    }
+  }
 }
 
 template <int G>
