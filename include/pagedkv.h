@@ -181,7 +181,11 @@ int pkv_attention(const void *q, const void *k_pool, const void *v_pool,
  * positions (nor before reading q and block_tables); it waits only before the
  * first tile of a row that holds one of the new tokens, so the append's
  * latency hides behind the gather (with PKV_PDL=0 or PKV_EARLY_KV=0 the two
- * run back to back instead).
+ * run back to back instead).  PKV_EARLY_TRIGGER=1 also lets the attention
+ * kernel launch as soon as the append starts; it then reads q and writes
+ * out and the workspace only after the append has finished, and the kernel
+ * issued before this call must not write seq_lens, query_start_loc,
+ * block_tables or pool slots of earlier positions either.
  * Source: LLM 7 - Efficient LLM Serving, sec. 3 "What the Cache Stores" (the
  * step appends each new token's K and V, then attends over the cache); The
  * Serving Playbook, "The block table lives in the hottest kernel in the
