@@ -72,10 +72,15 @@ def measured_peak():
 
 
 def decode_source_sha() -> str:
+    """Hash of the decode kernels' code: the sources with // comments and
+    blank lines removed, so that edits to comments keep a profile valid."""
     h = hashlib.sha256()
     for path in DECODE_SRCS:
-        with open(path, "rb") as f:
-            h.update(f.read())
+        with open(path, encoding="utf-8") as f:
+            for line in f:
+                code = re.sub(r"//.*", "", line).rstrip()
+                if code:
+                    h.update(code.encode() + b"\n")
     return h.hexdigest()[:16]
 
 

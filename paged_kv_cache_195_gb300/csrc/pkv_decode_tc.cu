@@ -29,9 +29,11 @@
 // both accumulating in fp32 in TMEM.  Thread t of the four softmax warps owns
 // TMEM lane t: key t of S^T, dim t of O^T.
 //
-// Roles (320 threads): warps 0-3 softmax, warp 4 plan and TMA producer, one
-// thread of warp 5 issues the MMAs, warps 6-9 the epilogue (normalise, write
-// the output or a partial piece, merge).  S, P and O^T are double buffered:
+// Roles (320 threads): warps 0-3 softmax, warp 4 plan and TMA producer (it
+// plans before the CTA's set-up, and K/V tiles are evict-first in L2: each is
+// read once), one thread of warp 5 issues the MMAs, warps 6-9 the epilogue
+// (normalise, write the output or a partial piece, merge, fold a shared
+// prefix's states).  S, P and O^T are double buffered:
 // the softmax moves on to the next piece while the epilogue finishes the
 // previous one, so piece boundaries do not stall the K/V stream.
 // The running maximum is raised only when a score exceeds it by more than

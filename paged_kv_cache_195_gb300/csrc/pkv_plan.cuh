@@ -13,7 +13,10 @@
 //
 // One warp of each CTA computes the plan from seq_lens / query_start_loc in
 // device memory (a warp-wide scan over the requests), so the launch shape
-// depends only on bounds and the call can be captured in a CUDA graph.
+// depends only on bounds and the call can be captured in a CUDA graph.  For
+// steps of up to 256 requests each CTA also keeps its plan in the workspace,
+// with the exact inputs it came from, and reuses it while they are unchanged
+// (every layer of an engine step has the same lengths).
 #pragma once
 
 #include <climits>
