@@ -140,6 +140,22 @@ EncodeTiledFn encode_tiled() {
 }
 
 // 2-D map of a pool as [num_blocks * Hkv * 16 rows][128] bf16, 64 x 16 boxes.
+// e4m3 pools: the same view in bytes, boxes of 16 rows x 128 codes.
+int encode_pool_map_e4m3(CUtensorMap* m, const void* pool, const pkv_dims* d) {
+  EncodeTiledFn enc = encode_tiled();
+  if (!enc) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  const cuuint64_t dims[2] = {(cuuint64_t)pkv::kHeadDim,
+                              (cuuint64_t)d->num_blocks * d->num_kv_heads * pkv::kBlockSize};
+  const cuuint64_t strides[1] = {(cuuint64_t)pkv::kHeadDim};
+  const cuuint32_t box[2] = {(cuuint32_t)pkv::kHeadDim, (cuuint32_t)pkv::kBlockSize};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(pool), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "encode e4m3 pool tensor map: CUresult %d", (int)r);
+  return PKV_OK;
+}
+
 int encode_pool_map(CUtensorMap* m, const void* pool, const pkv_dims* d) {
   EncodeTiledFn enc = encode_tiled();
   if (!enc) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
@@ -444,8 +460,12 @@ int attention_impl(const void* q, const void* k_pool, const void* v_pool, const 
   const int grid_env = env_int("PKV_DECODE_GRID", 0);  // tuning override, bounded by the slots
   if (grid_env > 0 && 2 * grid_env <= w.num_slots) grid = grid_env;
   // Groups of 4 or more query heads per KV head make the decode's FP32 FMA
-  // work comparable to its HBM time; those run on the tensor cores.
-  const bool use_tc = !fp8 && group >= 4 && env_int("PKV_DECODE_TC", 1) != 0;
+  // work comparable to its HBM time; those run on the tensor cores.  e4m3
+  // pools can too (PKV_DECODE_TC_FP8=1: tiles widened to bf16 in shared
+  // memory by two converter warps), but the widening, not HBM, then bounds
+  // the kernel, so by default they stay on the SIMT decode.
+  const bool use_tc = group >= 4 && env_int("PKV_DECODE_TC", 1) != 0 &&
+                      (!fp8 || env_int("PKV_DECODE_TC_FP8", 0) != 0);
   cudaError_t e;
   // Shared prefixes are read once by the prefix pass when the tensor-core
   // decode serves the step; otherwise every row reads its whole context (the
@@ -513,8 +533,10 @@ int attention_impl(const void* q, const void* k_pool, const void* v_pool, const 
   if (use_tc) {
     pkv::DecodeTcLaunch T{};
     rc = encode_q_map(&T.qmap, q, dims, group, 1);
-    if (rc == PKV_OK) rc = encode_pool_map(&T.kmap, k_pool, dims);
-    if (rc == PKV_OK) rc = encode_pool_map(&T.vmap, v_pool, dims);
+    if (rc == PKV_OK) rc = fp8 ? encode_pool_map_e4m3(&T.kmap, k_pool, dims)
+                               : encode_pool_map(&T.kmap, k_pool, dims);
+    if (rc == PKV_OK) rc = fp8 ? encode_pool_map_e4m3(&T.vmap, v_pool, dims)
+                               : encode_pool_map(&T.vmap, v_pool, dims);
     if (rc != PKV_OK) return rc;
     T.p = p;
     T.grid = st->sm_count;

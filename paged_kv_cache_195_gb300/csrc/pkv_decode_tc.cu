@@ -52,6 +52,11 @@ using plan::Piece;
 using plan::kEndRow;
 
 constexpr int kTcThreads = 320;
+// e4m3 pools: two more warps (10, 11) widen each K / V tile to bf16 in
+// shared memory before the tensor core reads it.
+constexpr int kTcThreadsF8 = 384;
+constexpr int kConvWarps = 2;
+constexpr int kRawTile = 128 * kHeadDim;   // one 128-key tile of e4m3 codes (bytes)
 constexpr int kTile = 128;                 // keys per tile (MMA M of S^T, K of PV)
 constexpr int kBlkPerTile = kTile / kBlockSize;
 constexpr int kN = 16;                     // MMA N: the group's heads, padded
@@ -115,12 +120,14 @@ struct __align__(1024) TcSmem {
   Piece pinfo[2];
   uint64_t q_full[2], q_empty[2];
   uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
+  uint64_t kraw_full[kStages], vraw_full[kStages];  // e4m3 codes landed (e4m3 pools)
   uint64_t s_full[2], s_free[2], p_full[2], p_free[2];
   uint64_t o_full[2], o_empty[2];  // O^T buffer complete / read by the epilogue
   uint64_t st_full[2], st_empty[2];  // piece statistics published / consumed
   uint32_t tmem_base;
   int abort_flag;
   int is_last;
+  int conv_end;                   // e4m3 pools: tiles issued in all (set at the end)
 };
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -135,12 +142,48 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-template <int G>
-__global__ void __launch_bounds__(kTcThreads, 1)
+// Key row `row` of a tile whose e4m3 codes TMA left in buf[1] (128 bytes per
+// row, 128-byte swizzle) becomes the bf16 operand row: d 0..63 in buf[0],
+// d 64..127 in buf[1], both 128-byte swizzled.  Every e4m3 value is a bf16
+// value, so the widening is exact.  The row's codes are read before any of
+// its bf16 chunks is written, and no other row's bytes are touched, so the
+// rows of a tile can be widened in any order and in place.
+__device__ __forceinline__ void widen_e4m3_row(uint8_t* half0, uint8_t* half1, int row) {
+  const int sw = row & 7;
+  uint4 raw[8];
+  #pragma unroll
+  for (int c8 = 0; c8 < 8; ++c8) raw[c8] = lds128(half1 + row * 128 + ((c8 ^ sw) * 16));
+  #pragma unroll
+  for (int c8 = 0; c8 < 8; ++c8) {
+    // codes of d = 16 c8 .. 16 c8 + 15 -> bf16 chunks 2 (c8 % 4) and +1 of half c8 / 4
+    const uint32_t w[4] = {raw[c8].x, raw[c8].y, raw[c8].z, raw[c8].w};
+    uint32_t b[8];
+    #pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 lo = e4m3x2_to_float2(w[j] & 0xffffu);
+      const float2 hi = e4m3x2_to_float2(w[j] >> 16);
+      const __nv_bfloat162 l2 = __floats2bfloat162_rn(lo.x, lo.y);
+      const __nv_bfloat162 h2 = __floats2bfloat162_rn(hi.x, hi.y);
+      b[2 * j] = *reinterpret_cast<const uint32_t*>(&l2);
+      b[2 * j + 1] = *reinterpret_cast<const uint32_t*>(&h2);
+    }
+    uint8_t* dst = (c8 < 4 ? half0 : half1) + row * 128;
+    const int c = (c8 & 3) * 2;
+    *reinterpret_cast<uint4*>(dst + ((c ^ sw) * 16)) = make_uint4(b[0], b[1], b[2], b[3]);
+    *reinterpret_cast<uint4*>(dst + (((c + 1) ^ sw) * 16)) = make_uint4(b[4], b[5], b[6], b[7]);
+  }
+}
+
+// F8: the pools hold e4m3 codes (kmap / vmap are maps of bytes); each tile is
+// widened to bf16 in shared memory, the key scale joins the softmax scale and
+// the value scale multiplies the output.
+template <int G, bool F8>
+__global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap qmap,
                      const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
   static_assert(G >= 1 && G <= 8, "group size");
+  constexpr int kThreads = F8 ? kTcThreadsF8 : kTcThreads;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 128-byte swizzled operands need 1024-byte aligned shared addresses.
   const uint32_t raw = smem_u32(smem_raw);
@@ -202,9 +245,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&sm.p_free[b], 1);    // tcgen05.commit after the PV that read P^T buffer b
     }
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&sm.k_full[s], 1);
-      mbar_init(&sm.v_full[s], 1);
+      // bf16 tiles: the TMA transaction count; e4m3: the converter warps
+      mbar_init(&sm.k_full[s], F8 ? kConvWarps : 1);
+      mbar_init(&sm.v_full[s], F8 ? kConvWarps : 1);
       mbar_init(&sm.kv_empty[s], 1);
+      mbar_init(&sm.kraw_full[s], 1);
+      mbar_init(&sm.vraw_full[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.o_full[b], 1);    // tcgen05.commit after the piece's last PV
@@ -213,10 +259,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&sm.st_empty[b], 4);  // the epilogue warps have read them
     }
     sm.abort_flag = 0;
+    sm.conv_end = INT_MAX;
     fence_barrier_init();
   }
   // Operand rows g..15 (padding heads) stay zero for the whole kernel.
-  for (int i = tid; i < (int)(sizeof(sm.q) + sizeof(sm.pt)) / 16; i += kTcThreads) {
+  for (int i = tid; i < (int)(sizeof(sm.q) + sizeof(sm.pt)) / 16; i += kThreads) {
     uint8_t* base = i < (int)sizeof(sm.q) / 16 ? &sm.q[0][0][0] + i * 16
                                                : &sm.pt[0][0][0] + (i - (int)sizeof(sm.q) / 16) * 16;
     *reinterpret_cast<uint4*>(base) = make_uint4(0, 0, 0, 0);
@@ -315,20 +362,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) TC_TR(0, t);
         if (lane == 0 && t == 0) TC_CTA(3);
         if (lane == 0) {
-          mbar_arrive_expect_tx(&sm.k_full[st], 2u * kHalf);
-          mbar_arrive_expect_tx(&sm.v_full[st], 2u * kHalf);
+          if (F8) {
+            mbar_arrive_expect_tx(&sm.kraw_full[st], (uint32_t)kRawTile);
+            mbar_arrive_expect_tx(&sm.vraw_full[st], (uint32_t)kRawTile);
+          } else {
+            mbar_arrive_expect_tx(&sm.k_full[st], 2u * kHalf);
+            mbar_arrive_expect_tx(&sm.v_full[st], 2u * kHalf);
+          }
         }
         __syncwarp();
-        // Lanes 0..15 each copy one (block, d half) of K and of V; blocks
-        // past the piece are read at an out-of-range row (zero fill).
+        // bf16: lanes 0..15 each copy one (block, d half) of K and of V.
+        // e4m3: lanes 0..7 each copy one block's 16 rows of 128 codes into
+        // the stage's second half, where the converter warps widen them.
+        // Blocks past the piece are read at an out-of-range row (zero fill).
         const int bsel = lane & 7, hsel = (lane >> 3) & 1;
         const int phys = __shfl_sync(0xffffffffu, ent_cur, (tt & 3) * kBlkPerTile + bsel);
-        if (lane < 16) {
+        if (lane < (F8 ? 8 : 16)) {
           int row = oob_row;
           if ((unsigned)phys < (unsigned)p.num_blocks) row = (phys * Hkv + k) * kBlockSize;
           else if (phys != kPastPiece && hsel == 0) record_error(p.err, kErrBounds);
-          tma_load_2d(sm.k[st][hsel] + bsel * 2048, &kmap, hsel * 64, row, &sm.k_full[st], pol);
-          tma_load_2d(sm.v[st][hsel] + bsel * 2048, &vmap, hsel * 64, row, &sm.v_full[st], pol);
+          if (F8) {
+            tma_load_2d(sm.k[st][1] + bsel * 2048, &kmap, 0, row, &sm.kraw_full[st], pol);
+            tma_load_2d(sm.v[st][1] + bsel * 2048, &vmap, 0, row, &sm.vraw_full[st], pol);
+          } else {
+            tma_load_2d(sm.k[st][hsel] + bsel * 2048, &kmap, hsel * 64, row, &sm.k_full[st], pol);
+            tma_load_2d(sm.v[st][hsel] + bsel * 2048, &vmap, hsel * 64, row, &sm.v_full[st], pol);
+          }
         }
         __syncwarp();
         if (tt == 0) {
@@ -387,6 +446,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // pending are issued unless the CTA is giving up.
     if (*abort_flag) q_pend = 0;
     take_wait();
+    if (F8 && ok && !*abort_flag) {
+      // Tell the converter warps that tile t does not exist: completing the
+      // phase they wait on for it, once its stage's previous tile is done.
+      const int st = t % kStages;
+      if (t < kStages || mbar_wait(&sm.kv_empty[st], ((t / kStages) - 1) & 1, p.err, abort_flag)) {
+        if (lane == 0) {
+          *reinterpret_cast<volatile int*>(&sm.conv_end) = t;
+          mbar_arrive(&sm.kraw_full[st]);
+        }
+      }
+      __syncwarp();
+    }
     // End marker: no more pieces for this CTA.
     const int ub = j & 1;
     if (j < 2 || mbar_wait(&sm.q_empty[ub], ((j >> 1) - 1) & 1, p.err, abort_flag)) {
@@ -473,6 +544,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     }
     __syncwarp();
+  } else if (F8 && warp >= 10) {
+    // ================= e4m3 converters (warps 10, 11) ====================
+    // Tile by tile, in the producer's order: widen K when its codes land,
+    // hand it to the MMA, then the same for V.  Each thread takes rows r and
+    // r + 64 of the 128-key tile.
+    const int r0 = tid - kTcThreads;  // 0 .. 63
+    for (int t = 0;; ++t) {
+      const int st = t % kStages;
+      if (!mbar_wait(&sm.kraw_full[st], (t / kStages) & 1, p.err, abort_flag)) break;
+      if (t >= *reinterpret_cast<volatile int*>(&sm.conv_end)) break;
+      widen_e4m3_row(sm.k[st][0], sm.k[st][1], r0);
+      widen_e4m3_row(sm.k[st][0], sm.k[st][1], r0 + 64);
+      fence_proxy_async_smem();  // generic-proxy writes, read by the tensor core
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.k_full[st]);
+      if (!mbar_wait(&sm.vraw_full[st], (t / kStages) & 1, p.err, abort_flag)) break;
+      widen_e4m3_row(sm.v[st][0], sm.v[st][1], r0);
+      widen_e4m3_row(sm.v[st][0], sm.v[st][1], r0 + 64);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.v_full[st]);
+    }
   } else {
     if (warp < 4) {
       // ========================= softmax (warps 0-3) ========================
@@ -490,6 +583,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         bool ok = true;
         const uint32_t tO = tmem + lane_off + kColO + ub * kN;
         const int ntile = plan::cdiv(pc.nblk, kBlkPerTile);
+        // e4m3: the key scale of this KV head joins the softmax scale
+        const float sl =
+            F8 && pc.k >= 0 && pc.k < Hkv ? p.scale_log2 * __ldg(p.k_scale + pc.k) : p.scale_log2;
         float m[G], l[G];
         #pragma unroll
         for (int h = 0; h < G; ++h) {
@@ -511,7 +607,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           bool over = false;
           #pragma unroll
           for (int h = 0; h < G; ++h) {
-            s[h] = valid ? s[h] * p.scale_log2 : -INFINITY;
+            s[h] = valid ? s[h] * sl : -INFINITY;
             over |= s[h] > m[h] + kLazyMargin;
           }
           // S buffer b has been read: the MMA may overwrite it (tile t + 2).
@@ -632,6 +728,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tmem_ld8(tmem + lane_off + kColO + ob * kN, o);
         tc_wait_ld();
         if (d == 0) TC_CTA(16);
+        if (F8) {  // the value scale of this KV head
+          const float vs = pc.k >= 0 && pc.k < Hkv ? __ldg(p.v_scale + pc.k) : 0.f;
+          #pragma unroll
+          for (int h = 0; h < G; ++h) o[h] *= vs;
+        }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
@@ -748,7 +849,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (tid == 0) TC_CTA(7);
 }
 
-template <int G>
+template <int G, bool F8>
 cudaError_t launch_decode_tc_g(const DecodeTcLaunch& L, cudaStream_t stream) {
   const size_t smem = sizeof(TcSmem) + 1024;  // + alignment slack
   static unsigned long long configured = 0;   // bit per device ordinal
@@ -757,14 +858,14 @@ cudaError_t launch_decode_tc_g(const DecodeTcLaunch& L, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const unsigned long long bit = 1ull << (dev & 63);
   if (!(__atomic_load_n(&configured, __ATOMIC_ACQUIRE) & bit)) {
-    e = cudaFuncSetAttribute(decode_tc_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(decode_tc_kernel<G, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
     if (e != cudaSuccess) return e;
     __atomic_fetch_or(&configured, bit, __ATOMIC_RELEASE);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(L.grid);
-  cfg.blockDim = dim3(kTcThreads);
+  cfg.blockDim = dim3(F8 ? kTcThreadsF8 : kTcThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -772,7 +873,7 @@ cudaError_t launch_decode_tc_g(const DecodeTcLaunch& L, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = L.p.pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, decode_tc_kernel<G>, L.qmap, L.kmap, L.vmap, L.p);
+  e = cudaLaunchKernelEx(&cfg, decode_tc_kernel<G, F8>, L.qmap, L.kmap, L.vmap, L.p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -798,12 +899,22 @@ cudaError_t decode_tc_trace(void* host, size_t bytes) {
 #endif
 
 cudaError_t launch_decode_tc(const DecodeTcLaunch& L, int group, cudaStream_t stream) {
+  if (L.p.kv_fp8) {
+    switch (group) {
+      case 4: return launch_decode_tc_g<4, true>(L, stream);
+      case 5: return launch_decode_tc_g<5, true>(L, stream);
+      case 6: return launch_decode_tc_g<6, true>(L, stream);
+      case 7: return launch_decode_tc_g<7, true>(L, stream);
+      case 8: return launch_decode_tc_g<8, true>(L, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (group) {
-    case 4: return launch_decode_tc_g<4>(L, stream);
-    case 5: return launch_decode_tc_g<5>(L, stream);
-    case 6: return launch_decode_tc_g<6>(L, stream);
-    case 7: return launch_decode_tc_g<7>(L, stream);
-    case 8: return launch_decode_tc_g<8>(L, stream);
+    case 4: return launch_decode_tc_g<4, false>(L, stream);
+    case 5: return launch_decode_tc_g<5, false>(L, stream);
+    case 6: return launch_decode_tc_g<6, false>(L, stream);
+    case 7: return launch_decode_tc_g<7, false>(L, stream);
+    case 8: return launch_decode_tc_g<8, false>(L, stream);
     default: return cudaErrorInvalidValue;
   }
 }
