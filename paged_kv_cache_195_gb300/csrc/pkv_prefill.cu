@@ -21,8 +21,10 @@
 //
 // Roles (352 threads): eight softmax warps -- warps 0-3 and 6-9, two threads
 // per TMEM lane / MMA row, each taking half of the row's keys and output
-// dims -- run the softmax and the epilogue; warp 4 issues the Q and K copies,
-// warp 10 the V copies; one thread of warp 5 issues tcgen05.mma and commits.
+// dims -- run the softmax and the epilogue; warp 4 takes items from a work
+// queue in the workspace and issues the Q and K copies, warp 10 the V copies
+// of the items warp 4 hands it; one thread of warp 5 issues tcgen05.mma and
+// commits.
 // Per key tile: S = Q K^T (8 MMAs of K=16) into TMEM, the softmax reads S and
 // writes P (bf16, two keys per column) over it, then O += P V (8 MMAs, A read
 // from TMEM) accumulates in TMEM.  K and V have rings of their own: a K stage
