@@ -51,7 +51,7 @@ def decode_kernel_name(group: int, fp8: bool) -> str:
     """The decode kernel the library routes this step to (4 or more query
     heads per KV head run on the tensor cores, e4m3 pools widened to bf16)."""
     tc = group >= 4 and os.environ.get("PKV_DECODE_TC", "1") != "0" and \
-        (not fp8 or os.environ.get("PKV_DECODE_TC_FP8", "0") != "0")
+        (not fp8 or os.environ.get("PKV_DECODE_TC_FP8", "1") != "0")
     if tc:
         return f"pkv::decode_tc_kernel<{group}, {'true' if fp8 else 'false'}>"
     return f"pkv::decode_kernel<{group}, {'KvE4m3' if fp8 else 'KvBf16'}>"

@@ -460,12 +460,11 @@ int attention_impl(const void* q, const void* k_pool, const void* v_pool, const 
   const int grid_env = env_int("PKV_DECODE_GRID", 0);  // tuning override, bounded by the slots
   if (grid_env > 0 && 2 * grid_env <= w.num_slots) grid = grid_env;
   // Groups of 4 or more query heads per KV head make the decode's FP32 FMA
-  // work comparable to its HBM time; those run on the tensor cores.  e4m3
-  // pools can too (PKV_DECODE_TC_FP8=1: tiles widened to bf16 in shared
-  // memory by two converter warps), but the widening, not HBM, then bounds
-  // the kernel, so by default they stay on the SIMT decode.
+  // work comparable to its HBM time; those run on the tensor cores, e4m3
+  // pools included (their tiles widened to f16 in shared memory by two
+  // converter warps; PKV_DECODE_TC_FP8=0 keeps them on the SIMT decode).
   const bool use_tc = group >= 4 && env_int("PKV_DECODE_TC", 1) != 0 &&
-                      (!fp8 || env_int("PKV_DECODE_TC_FP8", 0) != 0);
+                      (!fp8 || env_int("PKV_DECODE_TC_FP8", 1) != 0);
   cudaError_t e;
   // Shared prefixes are read once by the prefix pass when the tensor-core
   // decode serves the step; otherwise every row reads its whole context (the

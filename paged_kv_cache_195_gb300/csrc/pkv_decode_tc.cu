@@ -52,8 +52,10 @@ using plan::Piece;
 using plan::kEndRow;
 
 constexpr int kTcThreads = 320;
-// e4m3 pools: two more warps (10, 11) widen each K / V tile to bf16 in
-// shared memory before the tensor core reads it.
+// e4m3 pools: two more warps (10, 11) widen each K / V tile to f16 in
+// shared memory before the tensor core reads it (one hardware conversion per
+// pair of codes); Q and P are then f16 as well, since both operands of a
+// kind::f16 MMA must have the same type.
 constexpr int kTcThreadsF8 = 384;
 constexpr int kConvWarps = 2;
 constexpr int kRawTile = 128 * kHeadDim;   // one 128-key tile of e4m3 codes (bytes)
@@ -121,6 +123,7 @@ struct __align__(1024) TcSmem {
   uint64_t q_full[2], q_empty[2];
   uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
   uint64_t kraw_full[kStages], vraw_full[kStages];  // e4m3 codes landed (e4m3 pools)
+  uint64_t q_conv[2];             // e4m3 pools: Q buffer converted to f16 by the softmax warps
   uint64_t s_full[2], s_free[2], p_full[2], p_free[2];
   uint64_t o_full[2], o_empty[2];  // O^T buffer complete / read by the epilogue
   uint64_t st_full[2], st_empty[2];  // piece statistics published / consumed
@@ -143,11 +146,17 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // Key row `row` of a tile whose e4m3 codes TMA left in buf[1] (128 bytes per
-// row, 128-byte swizzle) becomes the bf16 operand row: d 0..63 in buf[0],
-// d 64..127 in buf[1], both 128-byte swizzled.  Every e4m3 value is a bf16
-// value, so the widening is exact.  The row's codes are read before any of
-// its bf16 chunks is written, and no other row's bytes are touched, so the
-// rows of a tile can be widened in any order and in place.
+// row, 128-byte swizzle) becomes the f16 operand row: d 0..63 in buf[0],
+// d 64..127 in buf[1], both 128-byte swizzled.  Every e4m3 value is an f16
+// value, so the widening (the hardware e4m3x2 -> f16x2 conversion) is exact.
+// The row's codes are read before any of its f16 chunks is written, and no
+// other row's bytes are touched, so the rows of a tile can be widened in any
+// order and in place.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2_bits(uint32_t two_codes) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two_codes, __NV_E4M3);
+  return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+
 __device__ __forceinline__ void widen_e4m3_row(uint8_t* half0, uint8_t* half1, int row) {
   const int sw = row & 7;
   uint4 raw[8];
@@ -155,17 +164,13 @@ __device__ __forceinline__ void widen_e4m3_row(uint8_t* half0, uint8_t* half1, i
   for (int c8 = 0; c8 < 8; ++c8) raw[c8] = lds128(half1 + row * 128 + ((c8 ^ sw) * 16));
   #pragma unroll
   for (int c8 = 0; c8 < 8; ++c8) {
-    // codes of d = 16 c8 .. 16 c8 + 15 -> bf16 chunks 2 (c8 % 4) and +1 of half c8 / 4
+    // codes of d = 16 c8 .. 16 c8 + 15 -> f16 chunks 2 (c8 % 4) and +1 of half c8 / 4
     const uint32_t w[4] = {raw[c8].x, raw[c8].y, raw[c8].z, raw[c8].w};
     uint32_t b[8];
     #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const float2 lo = e4m3x2_to_float2(w[j] & 0xffffu);
-      const float2 hi = e4m3x2_to_float2(w[j] >> 16);
-      const __nv_bfloat162 l2 = __floats2bfloat162_rn(lo.x, lo.y);
-      const __nv_bfloat162 h2 = __floats2bfloat162_rn(hi.x, hi.y);
-      b[2 * j] = *reinterpret_cast<const uint32_t*>(&l2);
-      b[2 * j + 1] = *reinterpret_cast<const uint32_t*>(&h2);
+      b[2 * j] = e4m3x2_to_f16x2_bits(w[j] & 0xffffu);
+      b[2 * j + 1] = e4m3x2_to_f16x2_bits(w[j] >> 16);
     }
     uint8_t* dst = (c8 < 4 ? half0 : half1) + row * 128;
     const int c = (c8 & 3) * 2;
@@ -253,6 +258,7 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 1)
       mbar_init(&sm.vraw_full[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.q_conv[b], 4);    // e4m3 pools: Q buffer b converted by the softmax warps
       mbar_init(&sm.o_full[b], 1);    // tcgen05.commit after the piece's last PV
       mbar_init(&sm.o_empty[b], 4);   // the epilogue warps have read O^T buffer b
       mbar_init(&sm.st_full[b], 4);   // the softmax warps have published the statistics
@@ -471,8 +477,10 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 1)
     // Tile n: S^T(n) = K(n) Q^T into S buffer n&1, then O^T += V^T(n-1)
     // P^T(n-1), so the QK^T of a tile overlaps the softmax of the previous.
     if (lane == 0) {
-      constexpr uint32_t kIdescS = idesc_bf16_f32(kTile, kN, 0, 0);
-      constexpr uint32_t kIdescO = idesc_bf16_f32(kHeadDim, kN, 1, 0);
+      constexpr uint32_t kIdescS =
+          F8 ? idesc_f16_f32(kTile, kN, 0, 0) : idesc_bf16_f32(kTile, kN, 0, 0);
+      constexpr uint32_t kIdescO =
+          F8 ? idesc_f16_f32(kHeadDim, kN, 1, 0) : idesc_bf16_f32(kHeadDim, kN, 1, 0);
       int t = 0;
       bool ok = true;
       auto pv = [&](int tt, bool first, int j) {
@@ -508,6 +516,8 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 1)
         if (!mbar_wait(&sm.q_full[ub], (j >> 1) & 1, p.err, abort_flag)) break;
         const Piece pc = sm.pinfo[ub];
         if (pc.row == kEndRow) break;
+        // e4m3 pools: Q in f16, like the widened K and V
+        if (F8 && !mbar_wait(&sm.q_conv[ub], (j >> 1) & 1, p.err, abort_flag)) break;
         const int ntile = plan::cdiv(pc.nblk, kBlkPerTile);
         tc_fence_after();
         for (int tt = 0; tt < ntile && ok; ++tt, ++t) {
@@ -580,6 +590,26 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 1)
         const Piece pc = sm.pinfo[ub];
         // Agree before any barrier: a wait that gave up (abort) stops everyone.
         if (barrier_or(kBarSoftmax, kSoftThreads, !got || pc.row == kEndRow)) break;
+        if (F8) {
+          // Q of this piece to f16 in place (2 x 16 rows x 64 dims: two
+          // 16-byte chunks per thread), for the MMA's same-type operands
+          #pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint4* qp = reinterpret_cast<uint4*>(&sm.q[ub][0][0]) + tid * 2 + c;
+            uint4 v = *qp;
+            uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+            #pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float2 f = bf16x2_to_float2(w[i]);
+              const __half2 h2 = __floats2half2_rn(f.x, f.y);
+              w[i] = *reinterpret_cast<const uint32_t*>(&h2);
+            }
+            *qp = v;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.q_conv[ub]);
+        }
         bool ok = true;
         const uint32_t tO = tmem + lane_off + kColO + ub * kN;
         const int ntile = plan::cdiv(pc.nblk, kBlkPerTile);
@@ -658,10 +688,17 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 1)
           const int kc = (row & 63) >> 3;
           #pragma unroll
           for (int h = 0; h < G; ++h) {
-            const __nv_bfloat16 pb = __float2bfloat16_rn(fast_exp2(s[h] - m[h]));
-            l[h] += __bfloat162float(pb);
-            *reinterpret_cast<__nv_bfloat16*>(prow + (h >> 3) * 1024 + (h & 7) * 128 +
-                                              ((kc ^ (h & 7)) * 16) + (row & 7) * 2) = pb;
+            uint16_t* dst = reinterpret_cast<uint16_t*>(prow + (h >> 3) * 1024 + (h & 7) * 128 +
+                                                        ((kc ^ (h & 7)) * 16) + (row & 7) * 2);
+            if (F8) {  // f16, the type of the widened V
+              const __half ph = __float2half_rn(fast_exp2(s[h] - m[h]));
+              l[h] += __half2float(ph);
+              *dst = *reinterpret_cast<const uint16_t*>(&ph);
+            } else {
+              const __nv_bfloat16 pb = __float2bfloat16_rn(fast_exp2(s[h] - m[h]));
+              l[h] += __bfloat162float(pb);
+              *dst = *reinterpret_cast<const uint16_t*>(&pb);
+            }
           }
           // Keys past the request's end inside its last block may hold anything
           // (even NaN): zero those V rows so that 0 * V stays 0 in the MMA.

@@ -195,4 +195,9 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, in
          | ((uint32_t)(M >> 4) << 24);  // M / 16
 }
 
+// The same with f16 A and B (both operands must have the same type).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, int a_mn, int b_mn) {
+  return idesc_bf16_f32(M, N, a_mn, b_mn) & ~((1u << 7) | (1u << 10));
+}
+
 }  // namespace pkv

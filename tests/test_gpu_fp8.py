@@ -115,20 +115,20 @@ def test_fp8_every_group_size(g):
 
 
 @pytest.mark.parametrize("g", [4, 6, 8])
-def test_fp8_tensor_core_decode(g, monkeypatch):
-    # the opt-in tensor-core path for e4m3 pools: tiles widened to bf16 in
-    # shared memory, key scale in the softmax, value scale on the output
-    monkeypatch.setenv("PKV_DECODE_TC_FP8", "1")
-    shape = wl.StepShape(f"fp8_tc_g{g}", [1, 31, 300, 129, 2000], [1, 1, 1, 3, 1], 2 * g, 2,
+def test_fp8_simt_decode_large_groups(g, monkeypatch):
+    # groups of 4 or more run on the tensor cores by default (tiles widened
+    # to f16); the SIMT decode serves them too when asked
+    monkeypatch.setenv("PKV_DECODE_TC_FP8", "0")
+    shape = wl.StepShape(f"fp8_simt_g{g}", [1, 31, 300, 129, 2000], [1, 1, 1, 3, 1], 2 * g, 2,
                          seed=190 + g)
     _full_parity(shape)
 
 
-def test_fp8_tensor_core_decode_split_and_chunks(monkeypatch):
-    monkeypatch.setenv("PKV_DECODE_TC_FP8", "1")
-    _full_parity(wl.StepShape("fp8_tc_long", [20000, 3000, 17], [1, 2, 1], 32, 8, seed=198),
+def test_fp8_simt_decode_split_and_chunks(monkeypatch):
+    monkeypatch.setenv("PKV_DECODE_TC_FP8", "0")
+    _full_parity(wl.StepShape("fp8_simt_long", [20000, 3000, 17], [1, 2, 1], 32, 8, seed=198),
                  poison=False)
-    _full_parity(wl.StepShape("fp8_tc_chunks", [700, 64, 230, 5], [64, 64, 200, 1], 32, 8,
+    _full_parity(wl.StepShape("fp8_simt_chunks", [700, 64, 230, 5], [64, 64, 200, 1], 32, 8,
                               seed=197))
 
 
