@@ -219,8 +219,10 @@ int pkv_append_fp8(const void *k_new, const void *v_new, const int64_t *slot_map
  * position j, KV head kh, is decode(code) * k_scale[kh], the value
  * decode(code) * v_scale[kh]; everything else (q, out, lengths, tables,
  * workspace, errors) as in pkv_attention.  All rows, prefill chunks
- * included, run in the split-context decode kernel (the tensor-core prefill
- * kernel takes bf16 pools only).
+ * included, run in the split-context decode kernels (the tensor-core prefill
+ * kernel takes bf16 pools only); with 4 or more query heads per KV head that
+ * is the tensor-core decode, which widens the codes to f16 in shared memory
+ * and takes q and the probabilities in f16 (q rounded from bf16 to f16).
  * Source: as pkv_attention; The Serving Playbook, "Quantized serving".
  */
 int pkv_attention_fp8kv(const void *q, const void *k_pool, const void *v_pool,
