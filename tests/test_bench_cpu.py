@@ -1,0 +1,91 @@
+"""bench.py's host-side helpers and its reference arm, on the CPU.
+
+The reference arm times the fp64 oracle on the host cores and must print the
+benchmark's JSON line; the ours arm reports `roofline.traffic` from a
+committed ncu summary only while the decode kernels' code still hashes to
+the value recorded there (comments may change freely).
+"""
+import importlib.util
+import json
+import os
+import shutil
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def bench():
+    spec = importlib.util.spec_from_file_location("bench_under_test", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def test_source_hash_ignores_comments_but_not_code(bench, tmp_path, monkeypatch):
+    srcs = []
+    for path in bench.DECODE_SRCS:
+        dst = tmp_path / os.path.basename(path)
+        shutil.copy(path, dst)
+        srcs.append(str(dst))
+    monkeypatch.setattr(bench, "DECODE_SRCS", srcs)
+    h0 = bench.decode_source_sha()
+    with open(srcs[1], "a") as f:
+        f.write("\n// a note about the code\n\n")
+    assert bench.decode_source_sha() == h0
+    with open(srcs[1], "a") as f:
+        f.write("static int an_extra_symbol = 1;\n")
+    assert bench.decode_source_sha() != h0
+
+
+def test_committed_traffic_matches_current_sources(bench):
+    # both committed decode summaries were taken on the current decode code
+    for kv in ("bf16", "fp8"):
+        t = bench.committed_traffic("qwen_decode", kv)
+        assert isinstance(t, int) and t > 0, kv
+    assert bench.committed_traffic("no_such_config", "bf16") is None
+
+
+def test_committed_traffic_is_dropped_when_code_changes(bench, tmp_path, monkeypatch):
+    srcs = []
+    for path in bench.DECODE_SRCS:
+        dst = tmp_path / os.path.basename(path)
+        shutil.copy(path, dst)
+        srcs.append(str(dst))
+    with open(srcs[0], "a") as f:
+        f.write("static int changed = 2;\n")
+    monkeypatch.setattr(bench, "DECODE_SRCS", srcs)
+    assert bench.committed_traffic("qwen_decode", "bf16") is None
+
+
+def test_decode_kernel_names_follow_the_routing(bench, monkeypatch):
+    monkeypatch.delenv("PKV_DECODE_TC", raising=False)
+    monkeypatch.delenv("PKV_DECODE_TC_FP8", raising=False)
+    assert bench.decode_kernel_name(6, False) == "pkv::decode_tc_kernel<6, false>"
+    assert bench.decode_kernel_name(4, True) == "pkv::decode_tc_kernel<4, true>"
+    assert bench.decode_kernel_name(2, False) == "pkv::decode_kernel<2, KvBf16>"
+    assert bench.decode_kernel_name(3, True) == "pkv::decode_kernel<3, KvE4m3>"
+    monkeypatch.setenv("PKV_DECODE_TC_FP8", "0")
+    assert bench.decode_kernel_name(6, True) == "pkv::decode_kernel<6, KvE4m3>"
+    assert bench.decode_kernel_name(6, False) == "pkv::decode_tc_kernel<6, false>"
+    monkeypatch.setenv("PKV_DECODE_TC", "0")
+    assert bench.decode_kernel_name(6, False) == "pkv::decode_kernel<6, KvBf16>"
+
+
+def test_reference_arm_prints_the_benchmark_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--config", "tiny", "--steps", "3", "--warmup", "3"],
+                       capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference"
+    assert line["value"] > 0 and line["unit"] == "GB/s" and line["higher_is_better"] is True
+    assert line["steps"] == 3 and line["warmup"] == 3
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+    assert line["config"]["workload"]
