@@ -371,14 +371,16 @@ int attention_impl(const void* q, const void* k_pool, const void* v_pool, const 
   if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
     return fail(PKV_ERR_INVALID, "q, out and the pools must be 16-byte aligned");
   if (!(scale == scale) || scale == 0.f) return fail(PKV_ERR_INVALID, "scale must be finite, non-zero");
+  if (cas) {
+    if (cas->num_groups < 0) return fail(PKV_ERR_INVALID, "num_groups < 0");
+    if (cas->num_groups > 0 && (!cas->grp_first || !cas->grp_count || !cas->grp_blocks))
+      return fail(PKV_ERR_INVALID, "NULL group array");
+  }
   DeviceState* st = device_state();
   if (!st) return PKV_ERR_CUDA;
   const pkv::WorkspaceLayout w = layout_for(dims, st->sm_count);
   const CascadeLayout cl = cascade_layout(w, dims);
   if (cas) {
-    if (cas->num_groups < 0) return fail(PKV_ERR_INVALID, "num_groups < 0");
-    if (cas->num_groups > 0 && (!cas->grp_first || !cas->grp_count || !cas->grp_blocks))
-      return fail(PKV_ERR_INVALID, "NULL group array");
     if (workspace == nullptr || workspace_bytes < cl.total)
       return fail(PKV_ERR_WORKSPACE, "cascade workspace %zu bytes, need %zu (caller-owned)",
                   workspace_bytes, cl.total);

@@ -103,3 +103,52 @@ def test_binding_refuses_cpu_tensors():
     pool = torch.zeros(4, 2, 16, 128, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         pkv.pkv_append(x, x, torch.zeros(1, dtype=torch.int64), pool, pool)
+
+
+def test_one_layer_call_validates_like_its_parts(lib):
+    fake = ctypes.c_void_p(0x1000)
+    args = lambda d, k_new=fake: (k_new, fake, fake, fake, fake, fake, fake, fake, fake,
+                                  ctypes.c_float(0.1), fake, ctypes.byref(d), None, 0, None)
+    assert lib.pkv_append_attention(*args(_dims(head_dim=64))) == b.PKV_ERR_UNSUPPORTED
+    assert lib.pkv_append_attention(*args(_dims(num_q_heads=13))) == b.PKV_ERR_INVALID
+    assert lib.pkv_append_attention(*args(_dims(), k_new=None)) == b.PKV_ERR_INVALID
+    assert lib.pkv_append_attention(*args(_dims(num_reqs=0, num_q_tokens=0))) == b.PKV_OK
+
+
+def test_cascade_call_rejects_bad_groups_before_the_device(lib):
+    fake = ctypes.c_void_p(0x1000)
+    d = _dims()
+
+    def call(first, count, blocks, n):
+        return lib.pkv_attention_cascade(fake, fake, fake, fake, fake, fake, first, count, blocks,
+                                         n, ctypes.c_float(0.1), fake, ctypes.byref(d), fake,
+                                         1 << 20, None)
+    assert call(fake, fake, fake, -1) == b.PKV_ERR_INVALID
+    assert call(None, fake, fake, 2) == b.PKV_ERR_INVALID
+    assert call(fake, fake, None, 1) == b.PKV_ERR_INVALID
+
+
+def test_fp8_calls_reject_bad_arguments(lib):
+    fake = ctypes.c_void_p(0x1000)
+    d = _dims()
+    # attention over e4m3 pools needs both scale arrays
+    assert lib.pkv_attention_fp8kv(fake, fake, fake, None, fake, fake, fake, fake,
+                                   ctypes.c_float(0.1), fake, ctypes.byref(d), None, 0,
+                                   None) == b.PKV_ERR_INVALID
+    assert lib.pkv_append_fp8(fake, fake, fake, fake, fake, fake, None, 3, ctypes.byref(d),
+                              None) == b.PKV_ERR_INVALID
+    assert lib.pkv_append_fp8(fake, fake, fake, fake, fake, fake, fake, -2, ctypes.byref(d),
+                              None) == b.PKV_ERR_INVALID
+    assert lib.pkv_append_fp8(fake, fake, fake, fake, fake, fake, fake, 0, ctypes.byref(d),
+                              None) == b.PKV_OK
+
+
+def test_copy_blocks_rejects_bad_arguments(lib):
+    fake = ctypes.c_void_p(0x1000)
+    d = _dims()
+    assert lib.pkv_copy_blocks(fake, fake, fake, fake, fake, -1, 8, 8, ctypes.byref(d),
+                               None) == b.PKV_ERR_INVALID
+    assert lib.pkv_copy_blocks(fake, fake, fake, fake, None, 2, 8, 8, ctypes.byref(d),
+                               None) == b.PKV_ERR_INVALID
+    assert lib.pkv_copy_blocks(fake, fake, fake, fake, fake, 0, 8, 8, ctypes.byref(d),
+                               None) == b.PKV_OK
