@@ -3,6 +3,12 @@
 The kernels live in ``libpagedkv.so`` (hand-written CUDA for sm_103a behind the
 C ABI of ``include/pagedkv.h``); this package is its thin Python binding plus
 the seeded workload generator.  Build with ``paged_kv_cache_195_gb300.build``.
+
+One layer of an engine step is ``pkv_append`` then ``pkv_attention`` (or the
+two as one call, ``pkv_append_attention``); ``pkv_append_fp8`` /
+``pkv_attention_fp8kv`` do the same over e4m3 pools, ``pkv_attention_cascade``
+reads prompts shared by groups of requests once per group, and
+``pkv_copy_blocks`` copies or swaps whole blocks.
 """
 from ._binding import (  # noqa: F401
     Dims, PagedKVError, Workspace, load_library, make_dims, paged_attention,
