@@ -41,11 +41,17 @@ def test_source_hash_ignores_comments_but_not_code(bench, tmp_path, monkeypatch)
     assert bench.decode_source_sha() != h0
 
 
-def test_committed_traffic_matches_current_sources(bench):
-    # both committed decode summaries were taken on the current decode code
-    for kv in ("bf16", "fp8"):
-        t = bench.committed_traffic("qwen_decode", kv)
-        assert isinstance(t, int) and t > 0, kv
+def test_committed_traffic_is_read_while_the_hash_matches(bench, tmp_path, monkeypatch):
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (prof / "decode_qwen_decode_bf16.md").write_text(
+        "# summary\n\nkernel_source_sha256_16: %s\ndram_bytes_per_launch: 123456\n"
+        % bench.decode_source_sha())
+    (prof / "decode_qwen_decode_fp8.md").write_text(
+        "kernel_source_sha256_16: 0000000000000000\ndram_bytes_per_launch: 777\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.committed_traffic("qwen_decode", "bf16") == 123456
+    assert bench.committed_traffic("qwen_decode", "fp8") is None   # other code
     assert bench.committed_traffic("no_such_config", "bf16") is None
 
 
