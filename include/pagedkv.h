@@ -17,7 +17,8 @@
  *
  * Conventions shared by every call
  * --------------------------------
- * - Element type: bf16 for q, K/V rows, pools and out.  head_dim = 128 and
+ * - Element type: bf16 for q, K/V rows, pools and out (pools hold e4m3 codes
+ *   for pkv_append_fp8 / pkv_attention_fp8kv).  head_dim = 128 and
  *   block_size = 16 are the supported shapes; num_q_heads must be a multiple
  *   of num_kv_heads with a group size g = num_q_heads / num_kv_heads of 1..8.
  * - Layouts (row-major, contiguous):
