@@ -33,7 +33,8 @@
 // plans before the CTA's set-up, and K/V tiles are evict-first in L2: each is
 // read once), one thread of warp 5 issues the MMAs, warps 6-9 the epilogue
 // (normalise, write the output or a partial piece, merge, fold a shared
-// prefix's states).  S, P and O^T are double buffered:
+// prefix's states).  e4m3 pools add warps 10-11 (384 threads), which widen
+// each tile's codes to f16 in shared memory; Q and P are then f16 too.  S, P and O^T are double buffered:
 // the softmax moves on to the next piece while the epilogue finishes the
 // previous one, so piece boundaries do not stall the K/V stream.
 // The running maximum is raised only when a score exceeds it by more than
