@@ -9,7 +9,11 @@ attention.  The 56 launches are captured once in a CUDA graph and replayed.
 
 Prints one JSON line (rank 0).  ``value`` is algorithmic HBM bytes (KV read +
 q read + out write + append traffic) per second over all ranks; the pools of
-one step (1.2 GB) exceed L2, so every step streams from HBM.
+one step (1.2 GB) exceed L2, so every step streams from HBM.  ``roofline``
+times the step's attention launches back to back for about a second
+(``--roofline-s``).  ``configs`` adds the same measurements for the other
+single-layer workloads (the long batch, the mixed continuous-batching step,
+the long-context step, and e4m3 caches), unless ``--no-extra``.
 
 ``--impl reference`` times the fp64 CPU oracle on bounded samples of the same
 workload on the host cores instead (the reference arm).
@@ -20,14 +24,12 @@ import argparse
 import ctypes
 import hashlib
 import json
-import math
 import os
 import re
 import statistics
 import subprocess
 import sys
 import tempfile
-import threading
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -47,11 +49,11 @@ DECODE_SRCS = [os.path.join(ROOT, "paged_kv_cache_195_gb300", "csrc", f)
                          "pkv_plan.cuh")]
 
 
-def decode_kernel_name(group: int, fp8: bool) -> str:
-    """The decode kernel the library routes this step to (4 or more query
-    heads per KV head run on the tensor cores, e4m3 pools widened to bf16)."""
-    tc = group >= 4 and os.environ.get("PKV_DECODE_TC", "1") != "0" and \
-        (not fp8 or os.environ.get("PKV_DECODE_TC_FP8", "1") != "0")
+def decode_kernel_name(group: int, fp8: bool, opts: dict) -> str:
+    """The decode kernel the library routes this step to under the options
+    `opts` (4 or more query heads per KV head run on the tensor cores, e4m3
+    pools widened to f16 there)."""
+    tc = group >= 4 and opts["decode_tc"] != 0 and (not fp8 or opts["decode_tc_fp8"] != 0)
     if tc:
         return f"pkv::decode_tc_kernel<{group}, {'true' if fp8 else 'false'}>"
     return f"pkv::decode_kernel<{group}, {'KvE4m3' if fp8 else 'KvBf16'}>"
@@ -196,13 +198,30 @@ class GraphEvents:
 # our arm
 # ---------------------------------------------------------------------------
 
+# Workloads timed after the headline one, each a single-layer call (attention
+# over shuffled pools, plus the append that feeds it): the long batch, the
+# mixed continuous-batching step, the long-context step, and the e4m3 cache on
+# the two Qwen-shaped decodes.
+EXTRA_CONFIGS = (("qwen_long", "bf16"), ("llama_mixed", "bf16"), ("llama_long", "bf16"),
+                 ("qwen_decode", "fp8"), ("qwen_long", "fp8"))
+
+
+def lengths_summary(values) -> dict | int:
+    """One number for uniform lengths, else their spread."""
+    v = np.asarray(values, np.int64)
+    if v.size and (v == v[0]).all():
+        return int(v[0])
+    return {"min": int(v.min()), "median": float(np.median(v)), "max": int(v.max()),
+            "sum": int(v.sum())}
+
+
 def workload_config(shape, ws_n, kv="bf16"):
     """The `config` object of the JSON line (both arms)."""
     kvb = 1 if kv == "fp8" else 2
     return {
         "workload": f"{shape.name} x{shape.layers} layers",
-        "num_reqs": shape.num_reqs, "context": int(shape.seq_lens[0]),
-        "q_tokens_per_req": int(shape.q_lens[0]), "layers": shape.layers,
+        "num_reqs": shape.num_reqs, "context": lengths_summary(shape.seq_lens),
+        "q_tokens_per_req": lengths_summary(shape.q_lens), "layers": shape.layers,
         "num_q_heads": shape.num_q_heads, "num_kv_heads": shape.num_kv_heads,
         "head_dim": shape.head_dim, "block_size": shape.block_size,
         "pool_blocks_per_layer": shape.num_blocks, "parallelism": f"replicas x{ws_n}",
@@ -230,9 +249,224 @@ def aggregate_over_ranks(ms_local: float, units_local: float, device=None):
     return float(t.item()), float(u.item())
 
 
-def build_layers(shape, device, rank, kv="bf16"):
+def build_layers(shape, device, rank, kv="bf16", count=None):
     make = wl.make_fp8_step if kv == "fp8" else wl.make_step
-    return [make(shape, device=device, layer=layer + 1000 * rank) for layer in range(shape.layers)]
+    n = shape.layers if count is None else count
+    return [make(shape, device=device, layer=layer + 1000 * rank) for layer in range(n)]
+
+
+def percentile(xs, q):
+    return float(np.percentile(np.asarray(xs, np.float64), q))
+
+
+class ConfigRun:
+    """One workload on this GPU: its layers' inputs, a workspace, and three
+    CUDA graphs -- the step (every layer's append + attention), the roofline
+    pass (attention launches back to back between two event nodes) and, for
+    the headline, the end-to-end step through pinned host buffers."""
+
+    def __init__(self, pkv, shape, kv, device, rank, with_e2e):
+        self.pkv, self.shape, self.kv, self.device = pkv, shape, kv, device
+        self.fp8 = kv == "fp8"
+        self.kvb = 1 if self.fp8 else 2
+        # single-layer workloads: two copies of the layer alternate in the
+        # roofline pass, so consecutive launches never share data in L2
+        n_pools = shape.layers if shape.layers > 1 else 2
+        self.layers = build_layers(shape, device, rank, kv, count=n_pools)
+        self.step_layers = self.layers[:shape.layers]
+        self.roof_seq = list(range(shape.layers)) if shape.layers > 1 else [0, 1] * 4
+        L0 = self.layers[0]
+        dims = pkv.make_dims(tuple(L0.q.shape), tuple(L0.k_pool.shape), shape.num_reqs,
+                             shape.max_blocks_per_req)
+        self.cascade = bool(shape.prefix_groups) and not self.fp8
+        self.ws = (pkv.CascadeWorkspace if self.cascade else pkv.Workspace)(dims, device=device)
+        pkv.pkv_workspace_init(self.ws, dims)
+        if self.cascade:
+            grp = np.array(shape.prefix_groups, dtype=np.int32).reshape(-1, 3)
+            self.grp_t = [torch.from_numpy(np.ascontiguousarray(grp[:, i])).to(device)
+                          for i in range(3)]
+        self.outs = [torch.empty_like(x.q) for x in self.layers]
+        self.stream = torch.cuda.Stream(device)
+        self.gev = GraphEvents(2)
+        with torch.cuda.stream(self.stream):
+            self.step()  # eager warm-up (module load, attribute set-up)
+        torch.cuda.synchronize(device)
+        assert pkv.pkv_get_device_error() == 0, pkv.pkv_last_error()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=self.stream):
+            self.step()
+        self.graph_roof = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph_roof, stream=self.stream):
+            self.attention_only()
+        self.graph_e2e = None
+        if with_e2e:
+            self._capture_e2e()
+
+    def attention(self, li):
+        pkv, x, out, ws = self.pkv, self.layers[li], self.outs[li], self.ws
+        if self.fp8:
+            pkv.pkv_attention_fp8kv(x.q, x.k_pool, x.v_pool, x.k_scale, x.v_scale,
+                                    x.block_tables, x.seq_lens, x.query_start_loc, x.scale,
+                                    out=out, workspace=ws)
+        elif self.cascade:
+            pkv.pkv_attention_cascade(x.q, x.k_pool, x.v_pool, x.block_tables, x.seq_lens,
+                                      x.query_start_loc, *self.grp_t, x.scale, out=out,
+                                      workspace=ws)
+        else:
+            pkv.pkv_attention(x.q, x.k_pool, x.v_pool, x.block_tables, x.seq_lens,
+                              x.query_start_loc, x.scale, out=out, workspace=ws)
+
+    def step(self):
+        pkv = self.pkv
+        for li, x in enumerate(self.step_layers):
+            if self.fp8:
+                pkv.pkv_append_fp8(x.k_new, x.v_new, x.slot_mapping, x.k_pool, x.v_pool,
+                                   x.k_scale, x.v_scale)
+                self.attention(li)
+            elif self.cascade:
+                pkv.pkv_append(x.k_new, x.v_new, x.slot_mapping, x.k_pool, x.v_pool)
+                self.attention(li)
+            else:
+                # one layer: the append, then the attention, which streams the
+                # tiles without this step's tokens while the append runs
+                pkv.pkv_append_attention(x.k_new, x.v_new, x.slot_mapping, x.k_pool, x.v_pool,
+                                         x.q, x.block_tables, x.seq_lens, x.query_start_loc,
+                                         x.scale, out=self.outs[li], workspace=self.ws)
+
+    def attention_only(self):
+        # the attention launches back to back (the pools already hold the
+        # step's tokens), bracketed by two event nodes; nothing between the
+        # launches, so they overlap as in the step
+        s = torch.cuda.current_stream(self.device)
+        self.gev.record(0, s)
+        for li in self.roof_seq:
+            self.attention(li)
+        self.gev.record(1, s)
+
+    def _capture_e2e(self):
+        # pinned host inputs -> device, the step, result -> pinned host
+        self.host_in = []
+        for x in self.step_layers:
+            self.host_in.append({k: getattr(x, k).cpu().pin_memory() for k in
+                                 ("q", "k_new", "v_new", "slot_mapping", "block_tables",
+                                  "seq_lens", "query_start_loc")})
+        self.host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+                         for o in self.outs[:len(self.step_layers)]]
+        self.h2d = sum(t.numel() * t.element_size() for d in self.host_in for t in d.values())
+        self.d2h = sum(t.numel() * t.element_size() for t in self.host_out)
+        self.graph_e2e = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph_e2e, stream=self.stream):
+            for x, hin in zip(self.step_layers, self.host_in):
+                for k, t in hin.items():
+                    getattr(x, k).copy_(t, non_blocking=True)
+            self.step()
+            for o, ho in zip(self.outs, self.host_out):
+                ho.copy_(o, non_blocking=True)
+
+    def timed(self, g, k, warmup, barrier=lambda: None):
+        for _ in range(warmup):
+            g.replay()
+        torch.cuda.synchronize(self.device)
+        barrier()
+        torch.cuda.synchronize(self.device)
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(self.stream)
+        with torch.cuda.stream(self.stream):
+            for _ in range(k):
+                g.replay()
+        t1.record(self.stream)
+        torch.cuda.synchronize(self.device)
+        barrier()
+        return t0.elapsed_time(t1)
+
+    def roofline_pass(self, warmup, min_s, clocks=None):
+        """Replays the back-to-back attention graph for at least min_s
+        seconds; per replay, the bracketed time over its launches."""
+        durs = []
+        with torch.cuda.stream(self.stream):
+            for _ in range(warmup):
+                self.graph_roof.replay()
+            torch.cuda.synchronize(self.device)
+            if clocks:
+                clocks.start()
+            t_end = time.perf_counter() + min_s
+            while len(durs) < 3 or (time.perf_counter() < t_end and len(durs) < 20000):
+                self.graph_roof.replay()
+                self.stream.synchronize()
+                durs.append(self.gev.elapsed_ms(0, 1) / len(self.roof_seq))
+        clock_info = clocks.stop() if clocks else None
+        return durs, clock_info
+
+    def unique_bytes(self):
+        shape = self.shape
+        att = rl.attention_bytes(shape.seq_lens, shape.q_lens, shape.num_q_heads,
+                                 shape.num_kv_heads, kv_dtype_bytes=self.kvb)
+        # The roofline counts the bytes the kernels must read: with shared
+        # prefixes, each group's prefix once.
+        if shape.prefix_groups and self.cascade:
+            return rl.unique_kv_bytes(shape.seq_lens, shape.q_lens, shape.num_kv_heads,
+                                      shape.prefix_groups, kv_dtype_bytes=self.kvb) + att["q_out"]
+        return att["total"]
+
+    def kernels_per_layer(self):
+        shape = self.shape
+        has_prefill = (not self.fp8 and not self.cascade and
+                       shape.num_q_tokens - shape.num_reqs + 1 >= 16)
+        return 2 + (1 if has_prefill else 0) + (2 if self.cascade else 0)
+
+    def roofline(self, durs_ms, config_name, clock_info):
+        peak, peak_src = measured_peak()
+        unique = self.unique_bytes()
+        mean_ms = statistics.mean(durs_ms)
+        achieved = unique / (mean_ms * 1e-3) / 1e9
+        shape = self.shape
+        return {
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": committed_traffic(config_name, self.kv),
+            "kernel": decode_kernel_name(shape.num_q_heads // shape.num_kv_heads, self.fp8,
+                                         self.pkv.get_options()),
+            "timing": (f"{len(self.roof_seq)} attention launches back to back "
+                       f"({'distinct layers' if shape.layers > 1 else 'two copies alternating'})"
+                       f", one event pair per replay, {len(durs_ms)} replays"),
+            "algorithmic_bytes_per_launch": unique,
+            "avg_launch_us": round(mean_ms * 1e3, 3),
+            "p10_us": round(percentile(durs_ms, 10) * 1e3, 3),
+            "p50_us": round(percentile(durs_ms, 50) * 1e3, 3),
+            "p90_us": round(percentile(durs_ms, 90) * 1e3, 3),
+            "peak_source": peak_src,
+            "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
+            "clocks": clock_info,
+        }
+
+
+def measure_extra(pkv, config, kv, device, rank, args, local):
+    """A single-layer workload: the per-layer step time and the roofline of
+    its attention launches."""
+    shape = wl.CONFIGS[config]()
+    run = ConfigRun(pkv, shape, kv, device, rank, with_e2e=False)
+    ms = run.timed(run.graph, max(3, args.steps), args.warmup) / max(3, args.steps)
+    durs, clk = run.roofline_pass(args.warmup, args.roofline_s, ClockSampler(nvsmi_id(local)))
+    assert pkv.pkv_get_device_error() == 0, pkv.pkv_last_error()
+    att = rl.attention_bytes(shape.seq_lens, shape.q_lens, shape.num_q_heads,
+                             shape.num_kv_heads, kv_dtype_bytes=run.kvb)
+    app = rl.append_bytes(shape.num_q_tokens, shape.num_kv_heads, kv_dtype_bytes=run.kvb)
+    rec = {
+        "workload": f"{shape.name}", "kv_cache_dtype": workload_config(shape, 1, kv)["kv_cache_dtype"],
+        "num_reqs": shape.num_reqs, "context": lengths_summary(shape.seq_lens),
+        "q_tokens_per_req": lengths_summary(shape.q_lens),
+        "us_per_layer": round(ms * 1e3 / shape.layers, 3),
+        "step_gb_per_s": round((att["total"] + app) * shape.layers / (ms * 1e-3) / 1e9, 1),
+        "attended_tokens_per_s": round(rl.attended_tokens(shape.seq_lens, shape.q_lens)
+                                       * shape.layers / (ms * 1e-3), 1),
+        "roofline": run.roofline(durs, config, clk),
+    }
+    flops = rl.attention_flops(shape.seq_lens, shape.q_lens, shape.num_q_heads)
+    if shape.num_q_tokens > shape.num_reqs:
+        rec["attention_tflops_per_layer_call"] = round(flops / 1e12, 4)
+    del run
+    torch.cuda.empty_cache()
+    return rec
 
 
 def run_ours(args):
@@ -252,161 +486,51 @@ def run_ours(args):
         pkv_build.build()
     pkv.load_library()
 
-    shape = wl.CONFIGS[args.config]()
-    fp8 = args.kv == "fp8"
-    kvb = 1 if fp8 else 2
-    layers = build_layers(shape, device, rank, args.kv)
-    L0 = layers[0]
-    dims = pkv.make_dims(tuple(L0.q.shape), tuple(L0.k_pool.shape), shape.num_reqs,
-                         shape.max_blocks_per_req)
-    cascade = bool(shape.prefix_groups) and not fp8
-    ws = (pkv.CascadeWorkspace if cascade else pkv.Workspace)(dims, device=device)
-    pkv.pkv_workspace_init(ws, dims)
-    if cascade:
-        grp = np.array(shape.prefix_groups, dtype=np.int32).reshape(-1, 3)
-        grp_t = [torch.from_numpy(np.ascontiguousarray(grp[:, i])).to(device) for i in range(3)]
-    outs = [torch.empty_like(x.q) for x in layers]
-
-    att = rl.attention_bytes(shape.seq_lens, shape.q_lens, shape.num_q_heads, shape.num_kv_heads,
-                             kv_dtype_bytes=kvb)
-    app = rl.append_bytes(shape.num_q_tokens, shape.num_kv_heads, kv_dtype_bytes=kvb)
-    bytes_per_layer = att["total"] + app
-    bytes_per_step = bytes_per_layer * shape.layers
-    tokens_per_step = rl.attended_tokens(shape.seq_lens, shape.q_lens) * shape.layers
-
-    stream = torch.cuda.Stream(device)
-    gev = GraphEvents(2)
-
-    def step():
-        for li, x in enumerate(layers):
-            if fp8:
-                pkv.pkv_append_fp8(x.k_new, x.v_new, x.slot_mapping, x.k_pool, x.v_pool,
-                                   x.k_scale, x.v_scale)
-                attention(li, x)
-            elif cascade:
-                pkv.pkv_append(x.k_new, x.v_new, x.slot_mapping, x.k_pool, x.v_pool)
-                attention(li, x)
-            else:
-                # one layer: the append, then the attention, which streams the
-                # tiles without this step's tokens while the append runs
-                pkv.pkv_append_attention(x.k_new, x.v_new, x.slot_mapping, x.k_pool, x.v_pool,
-                                         x.q, x.block_tables, x.seq_lens, x.query_start_loc,
-                                         x.scale, out=outs[li], workspace=ws)
-
-    def attention(li, x):
-        if fp8:
-            pkv.pkv_attention_fp8kv(x.q, x.k_pool, x.v_pool, x.k_scale, x.v_scale,
-                                    x.block_tables, x.seq_lens, x.query_start_loc, x.scale,
-                                    out=outs[li], workspace=ws)
-        elif cascade:
-            pkv.pkv_attention_cascade(x.q, x.k_pool, x.v_pool, x.block_tables, x.seq_lens,
-                                      x.query_start_loc, *grp_t, x.scale, out=outs[li],
-                                      workspace=ws)
-        else:
-            pkv.pkv_attention(x.q, x.k_pool, x.v_pool, x.block_tables, x.seq_lens,
-                              x.query_start_loc, x.scale, out=outs[li], workspace=ws)
-
-    def attention_only():
-        # the roofline pass: the attention launches of a step back to back
-        # (the pools already hold the step's tokens), bracketed by two event
-        # nodes; nothing between the launches, so they overlap as in the step
-        s = torch.cuda.current_stream(device)
-        gev.record(0, s)
-        for li, x in enumerate(layers):
-            attention(li, x)
-        gev.record(1, s)
-
-    # eager warm-up (module load, attribute set-up), then capture
-    with torch.cuda.stream(stream):
-        step()
-    torch.cuda.synchronize(device)
-    assert pkv.pkv_get_device_error() == 0, pkv.pkv_last_error()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        step()
-    graph_ev = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph_ev, stream=stream):
-        attention_only()
-
-    # e2e: pinned host inputs -> device, the step, result -> pinned host
-    host_in = []
-    for x in layers:
-        host_in.append({k: getattr(x, k).cpu().pin_memory() for k in
-                        ("q", "k_new", "v_new", "slot_mapping", "block_tables", "seq_lens",
-                         "query_start_loc")})
-    host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
-    h2d = sum(t.numel() * t.element_size() for d in host_in for t in d.values())
-    d2h = sum(t.numel() * t.element_size() for t in host_out)
-    graph_e2e = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph_e2e, stream=stream):
-        for x, hin in zip(layers, host_in):
-            for k, t in hin.items():
-                getattr(x, k).copy_(t, non_blocking=True)
-        step()
-        for o, ho in zip(outs, host_out):
-            ho.copy_(o, non_blocking=True)
-
     def barrier():
         if ws_n > 1:
             torch.distributed.barrier()
 
-    def timed(g, k):
-        for _ in range(args.warmup):
-            g.replay()
-        torch.cuda.synchronize(device)
-        barrier()
-        torch.cuda.synchronize(device)
-        t0 = torch.cuda.Event(enable_timing=True)
-        t1 = torch.cuda.Event(enable_timing=True)
-        t0.record(stream)
-        with torch.cuda.stream(stream):
-            for _ in range(k):
-                g.replay()
-        t1.record(stream)
-        torch.cuda.synchronize(device)
-        barrier()
-        ms, _ = aggregate_over_ranks(t0.elapsed_time(t1), 0.0, device)
-        return ms
+    shape = wl.CONFIGS[args.config]()
+    run = ConfigRun(pkv, shape, args.kv, device, rank, with_e2e=True)
+    fp8 = run.fp8
+    att = rl.attention_bytes(shape.seq_lens, shape.q_lens, shape.num_q_heads, shape.num_kv_heads,
+                             kv_dtype_bytes=run.kvb)
+    app = rl.append_bytes(shape.num_q_tokens, shape.num_kv_heads, kv_dtype_bytes=run.kvb)
+    bytes_per_step = (att["total"] + app) * shape.layers
+    tokens_per_step = rl.attended_tokens(shape.seq_lens, shape.q_lens) * shape.layers
 
+    # the timed steps, with clocks sampled from their start to the end of the
+    # roofline pass that follows (the steps alone can be shorter than one
+    # sampling period)
     clocks = ClockSampler(nvsmi_id(local))
     clocks.start()
-    ms_total = timed(graph, args.steps)
-    clock_info = clocks.stop()
+    ms_local = run.timed(run.graph, args.steps, args.warmup, barrier)
+    ms_total, _ = aggregate_over_ranks(ms_local, 0.0, device)
     ms_step = ms_total / args.steps
+    durs, _ = run.roofline_pass(args.warmup, args.roofline_s)
+    clock_info = clocks.stop()
 
-    # roofline pass: the attention launches alone, back to back; the average
-    # launch duration is the bracketed time over the launches, over the replays
-    durs = []
-    n_rep = max(3, min(args.steps, 200))
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            graph_ev.replay()
-        for _ in range(n_rep):
-            graph_ev.replay()
-            stream.synchronize()
-            durs.append(gev.elapsed_ms(0, 1) / shape.layers)
-    kernel_ms = statistics.mean(durs)
-
-    e2e_ms = timed(graph_e2e, max(1, args.steps // 4)) / max(1, args.steps // 4)
+    n_e2e = max(1, args.steps // 4)
+    e2e_ms = run.timed(run.graph_e2e, n_e2e, args.warmup, barrier) / n_e2e
+    e2e_ms, _ = aggregate_over_ranks(e2e_ms, 0.0, device)
     assert pkv.pkv_get_device_error() == 0, pkv.pkv_last_error()
-
-    # our kernels per layer: append, decode, the prefill kernel when some
-    # request can have 16 or more query tokens, the set-up and prefix pass of
-    # shared-prefix calls
-    has_prefill = (not fp8 and not cascade and
-                   shape.num_q_tokens - shape.num_reqs + 1 >= 16)
-    kernels_per_layer = 2 + (1 if has_prefill else 0) + (2 if cascade else 0)
-    peak, peak_src = measured_peak()
+    kernels_per_layer = run.kernels_per_layer()
     value = bytes_per_step * ws_n / (ms_step * 1e-3) / 1e9
-    # The roofline counts the bytes the kernels must read: with shared
-    # prefixes, each group's prefix once.
-    unique = (rl.unique_kv_bytes(shape.seq_lens, shape.q_lens, shape.num_kv_heads,
-                                 shape.prefix_groups, kv_dtype_bytes=kvb) + att["q_out"]
-              if shape.prefix_groups else att["total"])
+    roof = run.roofline(durs, args.config, None)
+    h2d, d2h = run.h2d, run.d2h
+    layers_cpu = run.layers[:2]
+    del run
+    torch.cuda.empty_cache()
 
-    achieved = unique / (kernel_ms * 1e-3) / 1e9
-    traffic = committed_traffic(args.config, args.kv)
-    cpu = cpu_baseline(shape, layers, args) if (rank == 0 and ws_n == 1 and not args.no_cpu) else None
+    extras = {}
+    if not args.no_extra and rank == 0 and ws_n == 1:
+        for config, kv in EXTRA_CONFIGS:
+            if (config, kv) == (args.config, args.kv):
+                continue
+            extras[f"{config}/{kv}"] = measure_extra(pkv, config, kv, device, rank, args, local)
+
+    cpu = (cpu_baseline(shape, layers_cpu, args.kv)
+           if (rank == 0 and ws_n == 1 and not args.no_cpu) else None)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws_n,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
@@ -419,21 +543,14 @@ def run_ours(args):
         "attended_tokens_per_s": round(tokens_per_step * ws_n / (ms_step * 1e-3), 1),
         "us_per_layer": round(ms_step * 1e3 / shape.layers, 3),
         "frac_of_nominal_8tbs": round(value / ws_n / NOMINAL_HBM_GBS, 4),
-        "roofline": {
-            "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-            "frac": round(achieved / peak, 4), "traffic": traffic,
-            "kernel": decode_kernel_name(shape.num_q_heads // shape.num_kv_heads, fp8),
-            "timing": f"{shape.layers} attention launches back to back, one event pair",
-            "algorithmic_bytes_per_launch": unique,
-            "avg_launch_us": round(kernel_ms * 1e3, 3), "peak_source": peak_src,
-            "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
-        },
+        "roofline": roof,
         "e2e": {"value": round(bytes_per_step * ws_n / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": kernels_per_layer * shape.layers * args.steps,
         "clocks": clock_info,
         "cpu_baseline": cpu,
+        "configs": extras,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -473,26 +590,72 @@ def _host_layer(inp):
     return h
 
 
-def cpu_baseline(shape, layers, args, budget_s=10.0):
-    import oracle
-    oracle.build()
-    host = [_host_layer(x) for x in layers[:4]]
-    done_bytes, t_total, n_calls = 0, 0.0, 0
-    per_req = rl.attention_bytes(shape.seq_lens[:1], shape.q_lens[:1], shape.num_q_heads,
-                                 shape.num_kv_heads,
-                                 kv_dtype_bytes=1 if args.kv == "fp8" else 2)["total"]
-    t0 = time.perf_counter()
-    while t_total < budget_s:
+def sample_bytes(shape, n_reqs, kv):
+    """Algorithmic bytes of the attention of the first n_reqs requests."""
+    return rl.attention_bytes(shape.seq_lens[:n_reqs], shape.q_lens[:n_reqs], shape.num_q_heads,
+                              shape.num_kv_heads,
+                              kv_dtype_bytes=1 if kv == "fp8" else 2)["total"]
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (x86 'model name', else lscpu's)."""
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def _time_oracle(shape, host, n_reqs, budget_s):
+    """Calls on the first n_reqs requests, cycling over the host layers,
+    until budget_s of oracle time; returns (calls, seconds)."""
+    n_calls, t_total = 0, 0.0
+    while t_total < budget_s or n_calls == 0:
         h = host[n_calls % len(host)]
         t1 = time.perf_counter()
-        _oracle_sample(shape, h, shape.num_reqs)
+        _oracle_sample(shape, h, n_reqs)
         t_total += time.perf_counter() - t1
-        done_bytes += per_req * shape.num_reqs
         n_calls += 1
-    return {"value": round(done_bytes / t_total / 1e9, 4), "unit": "GB/s",
-            "cores": oracle.max_threads(), "kind": "oracle",
+    return n_calls, t_total
+
+
+def cpu_baseline(shape, layers, kv, budget_s=10.0, budget_1t_s=4.0):
+    """The fp64 oracle on the host cores: whole layers with every thread,
+    then a sample of requests on one thread."""
+    import oracle
+    oracle.build()
+    host = [_host_layer(x) for x in layers]
+    t0 = time.perf_counter()
+    threads = oracle.max_threads()
+    n_calls, t_all = _time_oracle(shape, host, shape.num_reqs, budget_s)
+    value = sample_bytes(shape, shape.num_reqs, kv) * n_calls / t_all / 1e9
+    # one thread: as many requests as fit about a tenth of the budget per call
+    oracle.set_threads(1)
+    try:
+        t1 = time.perf_counter()
+        _oracle_sample(shape, host[0], 1)
+        one = max(1e-4, time.perf_counter() - t1)
+        n1 = int(max(1, min(shape.num_reqs, 0.1 * budget_1t_s / one)))
+        c1, t_1 = _time_oracle(shape, host, n1, budget_1t_s)
+    finally:
+        oracle.set_threads(threads)
+    value_1t = sample_bytes(shape, n1, kv) * c1 / t_1 / 1e9
+    return {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
             "sample": f"{n_calls} full layers ({shape.num_reqs} requests each) of {shape.name}, "
-                      f"fp64 C oracle, OpenMP, {t_total:.1f} s wall",
+                      f"fp64 C oracle, OpenMP, {t_all:.1f} s",
+            "one_thread": {"value": round(value_1t, 4), "unit": "GB/s", "cores": 1,
+                           "sample": f"{c1} calls on the first {n1} requests, {t_1:.1f} s"},
+            "nproc": os.cpu_count(), "cpu_model": cpu_model(),
             "wall_s": round(time.perf_counter() - t0, 2)}
 
 
@@ -507,9 +670,6 @@ def run_reference(args):
     n_layers = min(shape.layers, 2)
     make = wl.make_fp8_step if args.kv == "fp8" else wl.make_step
     host = [_host_layer(make(shape, device="cpu", layer=li)) for li in range(n_layers)]
-    per_req = rl.attention_bytes(shape.seq_lens[:1], shape.q_lens[:1], shape.num_q_heads,
-                                 shape.num_kv_heads,
-                                 kv_dtype_bytes=1 if args.kv == "fp8" else 2)["total"]
     # size each step so that warm-up + timed steps fit in about a minute
     t1 = time.perf_counter()
     _oracle_sample(shape, host[0], 1)
@@ -522,7 +682,7 @@ def run_reference(args):
     for i in range(args.steps):
         _oracle_sample(shape, host[i % n_layers], n_reqs)
     dt = time.perf_counter() - t0
-    value = per_req * n_reqs * args.steps / dt / 1e9
+    value = sample_bytes(shape, n_reqs, args.kv) * args.steps / dt / 1e9
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "n_gpus": ws_n, "steps": args.steps, "warmup": args.warmup,
@@ -531,8 +691,9 @@ def run_reference(args):
         "config": workload_config(shape, ws_n, args.kv),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.max_threads(),
                          "kind": "oracle",
-                         "sample": f"each step: attention of {n_reqs} of {shape.num_reqs} "
-                                   f"requests of one layer, fp64 C oracle"},
+                         "sample": f"each step: attention of the first {n_reqs} of "
+                                   f"{shape.num_reqs} requests of one layer, fp64 C oracle",
+                         "nproc": os.cpu_count(), "cpu_model": cpu_model()},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -549,6 +710,10 @@ def main():
     ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
                     help="KV-cache element type (fp8: e4m3 with per-KV-head scales)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="time only the chosen workload (not the other single-layer ones)")
+    ap.add_argument("--roofline-s", type=float, default=1.0,
+                    help="seconds of back-to-back attention replays per roofline pass")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -67,7 +67,7 @@ extern "C" {
 
 typedef struct pkv_dims {
     int32_t num_reqs;           /* R */
-    int32_t num_q_tokens;       /* Tq = query_start_loc[R] */
+    int32_t num_q_tokens;       /* Tq >= query_start_loc[R] (rows past it are padding) */
     int32_t num_q_heads;        /* Hq */
     int32_t num_kv_heads;       /* Hkv */
     int32_t head_dim;           /* D, must be 128 */
@@ -141,20 +141,26 @@ int pkv_workspace_init(void *workspace, size_t workspace_bytes,
  * heads per KV head, run on tcgen05 tensor cores (their probabilities enter
  * the PV product in bf16).  out is written as
  * bf16 (round to nearest even).  Requests with q_r = 0 produce nothing.
- * Preconditions: query_start_loc[0] = 0, non-decreasing, last entry =
+ * Preconditions: query_start_loc[0] = 0, non-decreasing, last entry <=
  * num_q_tokens; 0 <= q_r <= L_r <= max_blocks_per_req * bs; table entries
  * b < ceil(L_r / bs) are in [0, num_blocks).  Violations found on the device
  * skip the affected work and are reported by pkv_get_device_error.
+ * Padded (bucketed) steps: a CUDA graph captured for a bucket of R requests
+ * and Tq query rows serves any step that fits in it, its buffers rewritten in
+ * place between replays.  Pad the unused requests with q_r = 0 (their
+ * query_start_loc entries repeat the last live one) and L_r = 0; their table
+ * rows are not read.  Rows query_start_loc[R] .. num_q_tokens - 1 of out are
+ * padding: no call writes them.  Give padding rows slot -1 in a slot mapping.
  * workspace: at least pkv_attention_workspace_size(dims) bytes, initialised
  * once with pkv_workspace_init; NULL makes the library use an internal
  * per-device buffer (allocated on first use: not capturable in a CUDA graph,
  * and not safe for concurrent calls on different streams).
- * Launch overlap: unless the environment sets PKV_PDL=0, the kernels are
- * launched with programmatic dependent launch and may start while the
- * kernel before them on the stream is still running.  They wait for it
- * before touching q, the pools, out or the workspace, but read seq_lens,
- * query_start_loc and (in the tensor-core decode) block_tables before that
- * wait (PKV_EARLY_PLAN=0 moves those reads after it).  So the kernel issued
+ * Launch overlap: unless pkv_options.pdl is 0, the kernels are launched
+ * with programmatic dependent launch and may start while the kernel before
+ * them on the stream is still running.  They wait for it before touching q,
+ * the pools, out or the workspace, but read seq_lens, query_start_loc and
+ * (in the tensor-core decode) block_tables before that wait
+ * (pkv_options.early_plan = 0 moves those reads after it).  So the kernel issued
  * immediately before this call must not write seq_lens, query_start_loc or
  * block_tables; pkv_append, which writes only pool slots, and host-to-device
  * copies may.
@@ -181,9 +187,9 @@ int pkv_attention(const void *q, const void *k_pool, const void *v_pool,
  * wait for the append before streaming the K/V tiles that hold only earlier
  * positions (nor before reading q and block_tables); it waits only before the
  * first tile of a row that holds one of the new tokens, so the append's
- * latency hides behind the gather (with PKV_PDL=0 or PKV_EARLY_KV=0 the two
- * run back to back instead).  PKV_EARLY_TRIGGER=1 also lets the attention
- * kernel launch as soon as the append starts; it then reads q and writes
+ * latency hides behind the gather (with pkv_options.pdl or .early_kv = 0 the
+ * two run back to back instead).  pkv_options.early_trigger = 1 also lets the
+ * attention kernel launch as soon as the append starts; it then reads q and writes
  * out and the workspace only after the append has finished, and the kernel
  * issued before this call must not write seq_lens, query_start_loc,
  * block_tables or pool slots of earlier positions either.
@@ -283,26 +289,79 @@ int pkv_attention_cascade(const void *q, const void *k_pool, const void *v_pool,
  * pkv_attention without a workspace and without any allocation.  The paper
  * has no counterpart: this is a convenience of the library.
  *
- * For callers that cannot allocate device memory -- code running while a
- * CUDA graph is captured in global mode, plugins whose host framework owns
- * all device memory, serving loops that forbid allocation after start-up --
- * and so cannot pass pkv_attention a workspace.  Same arguments, results and
- * error codes as pkv_attention; the split-context scratch comes from a
- * PKV_NOALLOC_SCRATCH_BYTES array compiled into the library, which every GPU
- * that loads the library holds until the process exits.  Dims needing more
- * scratch than that (pkv_attention_workspace_size) return PKV_ERR_WORKSPACE.
+ * For callers that cannot allocate device memory -- plugins whose host
+ * framework owns all device memory through its own pool, serving loops that
+ * forbid allocation after start-up -- and so cannot pass pkv_attention a
+ * workspace.  Same arguments, results and error codes as pkv_attention; the
+ * split-context scratch comes from a PKV_NOALLOC_SCRATCH_BYTES array compiled
+ * into the library, which every GPU that loads the library holds until the
+ * process exits.  Dims needing more scratch than that
+ * (pkv_attention_workspace_size) return PKV_ERR_WORKSPACE.
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream
- * capture.  Each call clears the merge counters at the head of the array
- * (stream-ordered memset) and leaves other contents from earlier calls in
- * place.  All calls share the one array: calls that overlap on the GPU (two
- * streams, two host threads) race and must be serialised by the caller.
+ * capture.  Each call clears the head of the array (merge counters, prefill
+ * work queue, plan cache) with a stream-ordered memset and leaves other
+ * contents from earlier calls in place; so these calls make their plan
+ * afresh every time, and the memset keeps the attention kernel from
+ * overlapping the kernel before it.  All calls share the one array: calls
+ * that overlap on the GPU (two streams, two host threads) race and must be
+ * serialised by the caller.
  * Never calls cudaMalloc, cudaFree or any allocating routine.
  */
 int pkv_attention_noalloc(const void *q, const void *k_pool, const void *v_pool,
                           const int32_t *block_tables, const int32_t *seq_lens,
                           const int32_t *query_start_loc, float scale, void *out,
                           const pkv_dims *dims, cudaStream_t stream);
+
+/*
+ * Launch and routing options (process-wide).  The defaults are the measured
+ * best.  Each field can also be set by the environment variable named beside
+ * it, read once, when a call of this library first needs the options; after
+ * that, pkv_set_options is the only way to change them.  Every call takes a
+ * copy of the options when it starts; change them only while no other host
+ * thread is inside a call of this library.  None of them changes a result
+ * beyond rounding: they choose kernels, launch overlap and work splits.
+ */
+typedef struct pkv_options {
+    int32_t pdl;            /* PKV_PDL (1): programmatic dependent launch between the
+                               library's kernels (see pkv_attention) */
+    int32_t early_plan;     /* PKV_EARLY_PLAN (1): decode plans read seq_lens,
+                               query_start_loc (and block_tables) before the launch wait */
+    int32_t early_kv;       /* PKV_EARLY_KV (1): pkv_append_attention streams K/V tiles
+                               without this step's tokens before the append finishes */
+    int32_t early_trigger;  /* PKV_EARLY_TRIGGER (0): pkv_append_attention's append lets
+                               the attention launch at once */
+    int32_t plan_cache;     /* PKV_PLAN_CACHE (1): per-CTA plan cache in the workspace */
+    int32_t decode_tc;      /* PKV_DECODE_TC (1): tensor-core decode for 4..8 query heads
+                               per KV head (0: the SIMT decode for every group) */
+    int32_t decode_tc_fp8;  /* PKV_DECODE_TC_FP8 (1): the same for e4m3 pools */
+    int32_t prefill_min_q;  /* PKV_PREFILL_MIN_Q (16): requests with at least this many
+                               query tokens run in the tensor-core prefill kernel
+                               (0: none do); bf16 pools only */
+    int32_t align;          /* PKV_ALIGN (1): with uniform row-groups, snap decode ranges
+                               to row-group boundaries ... */
+    int32_t align_slack;    /* PKV_ALIGN_SLACK (64): ... when that lengthens every range
+                               by at most this many blocks */
+    int32_t min_chunk;      /* PKV_MIN_CHUNK (4): smallest decode range per CTA, in
+                               blocks (>= 1) */
+    int32_t prefetch;       /* PKV_PREFETCH (1): warm L2 with the block-table rows a
+                               decode CTA will read */
+    int32_t decode_grid;    /* PKV_DECODE_GRID (0): SIMT decode grid (0: by group size;
+                               tuning only, capped by the workspace) */
+    int32_t wait_limit_us;  /* PKV_WAIT_LIMIT_US (2000000): a bounded device wait gives
+                               up after this many microseconds and reports
+                               PKV_ERR_TIMEOUT (>= 1) */
+    int32_t debug_withhold_q; /* testing only (0): the tensor-core decode never loads q,
+                               so its waits run out after wait_limit_us; exercises
+                               the timeout path.  Results are not computed. */
+} pkv_options;
+
+/* Copies the current options into *opts. */
+void pkv_get_options(pkv_options *opts);
+
+/* Replaces the options; PKV_ERR_INVALID (nothing changed) if a field is out
+ * of range. */
+int pkv_set_options(const pkv_options *opts);
 
 /* Message of the last failing call on this thread ("" if none). */
 const char *pkv_last_error(void);

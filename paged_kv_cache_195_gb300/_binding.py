@@ -8,6 +8,7 @@ PyTorch supplies device memory and streams, nothing else.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
@@ -29,7 +30,12 @@ EXPORTED = ("pkv_append", "pkv_attention", "pkv_attention_workspace_size",
             "pkv_workspace_init", "pkv_last_error", "pkv_get_device_error",
             "pkv_attention_noalloc", "pkv_copy_blocks", "pkv_append_fp8",
             "pkv_attention_fp8kv", "pkv_cascade_workspace_size", "pkv_attention_cascade",
-            "pkv_append_attention")
+            "pkv_append_attention", "pkv_get_options", "pkv_set_options")
+
+# Fields of pkv_options, in declaration order (int32 each).
+OPTION_FIELDS = ("pdl", "early_plan", "early_kv", "early_trigger", "plan_cache", "decode_tc",
+                 "decode_tc_fp8", "prefill_min_q", "align", "align_slack", "min_chunk",
+                 "prefetch", "decode_grid", "wait_limit_us", "debug_withhold_q")
 
 
 class PagedKVError(RuntimeError):
@@ -43,6 +49,10 @@ class Dims(ctypes.Structure):
                 ("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32),
                 ("num_blocks", ctypes.c_int32), ("max_blocks_per_req", ctypes.c_int32)]
+
+
+class Options(ctypes.Structure):
+    _fields_ = [(name, ctypes.c_int32) for name in OPTION_FIELDS]
 
 
 _lock = threading.Lock()
@@ -91,8 +101,41 @@ def load_library(path: str = LIB_PATH):
         lib.pkv_append_attention.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float,
                                              vp, dp, vp, sz, vp]
         lib.pkv_append_attention.restype = ctypes.c_int
+        lib.pkv_get_options.argtypes = [ctypes.POINTER(Options)]
+        lib.pkv_get_options.restype = None
+        lib.pkv_set_options.argtypes = [ctypes.POINTER(Options)]
+        lib.pkv_set_options.restype = ctypes.c_int
         _lib = lib
         return lib
+
+
+def get_options() -> dict:
+    """The library's current launch and routing options (pkv_options)."""
+    o = Options()
+    load_library().pkv_get_options(ctypes.byref(o))
+    return {name: int(getattr(o, name)) for name in OPTION_FIELDS}
+
+
+def set_options(**changes) -> dict:
+    """Change some options (the rest keep their values); returns the old ones."""
+    old = get_options()
+    unknown = set(changes) - set(OPTION_FIELDS)
+    if unknown:
+        raise KeyError(f"unknown options: {sorted(unknown)}")
+    new = dict(old, **{k: int(v) for k, v in changes.items()})
+    o = Options(*(new[name] for name in OPTION_FIELDS))
+    _check(load_library().pkv_set_options(ctypes.byref(o)))
+    return old
+
+
+@contextlib.contextmanager
+def options(**changes):
+    """Run a block with some options changed, then put the old ones back."""
+    old = set_options(**changes)
+    try:
+        yield
+    finally:
+        set_options(**old)
 
 
 def pkv_last_error() -> str:
@@ -121,6 +164,24 @@ def _need(t: torch.Tensor, name: str, dtype, ndim: int):
         raise ValueError(f"{name} must have {ndim} dims, got shape {tuple(t.shape)}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
+
+
+def check_attention_shapes(q, k_pool, v_pool, block_tables, seq_lens, query_start_loc,
+                           out=None):
+    """Shape agreement of an attention call's tensors (any device): the
+    pools equal in shape with q's head_dim, one table row and length per
+    request, query_start_loc one longer, out shaped like q.  Raises
+    ValueError before anything reaches the library, whose kernels size every
+    pool access from k_pool's shape alone."""
+    R = seq_lens.shape[0]
+    if query_start_loc.shape[0] != R + 1 or block_tables.shape[0] != R:
+        raise ValueError("seq_lens, query_start_loc and block_tables disagree on num_reqs")
+    if tuple(v_pool.shape) != tuple(k_pool.shape) or k_pool.shape[3] != q.shape[2]:
+        raise ValueError("pool / q shape mismatch: v_pool must have k_pool's shape and "
+                         "head_dim must match q's")
+    if out is not None and tuple(out.shape) != tuple(q.shape):
+        raise ValueError("out must have q's shape")
+    return R
 
 
 def make_dims(q_shape, pool_shape, num_reqs: int, max_blocks_per_req: int) -> Dims:
@@ -187,11 +248,7 @@ def pkv_attention(q, k_pool, v_pool, block_tables, seq_lens, query_start_loc, sc
     _need(block_tables, "block_tables", torch.int32, 2)
     _need(seq_lens, "seq_lens", torch.int32, 1)
     _need(query_start_loc, "query_start_loc", torch.int32, 1)
-    R = seq_lens.shape[0]
-    if query_start_loc.shape[0] != R + 1 or block_tables.shape[0] != R:
-        raise ValueError("seq_lens, query_start_loc and block_tables disagree on num_reqs")
-    if v_pool.shape != k_pool.shape or k_pool.shape[3] != q.shape[2]:
-        raise ValueError("pool / q shape mismatch")
+    R = check_attention_shapes(q, k_pool, v_pool, block_tables, seq_lens, query_start_loc)
     if out is None:
         out = torch.empty_like(q)
     else:
@@ -232,9 +289,7 @@ def pkv_append_attention(k_new, v_new, slot_mapping, k_pool, v_pool, q, block_ta
     if v_pool.shape != k_pool.shape or k_pool.shape[1] != k_new.shape[1] or \
             k_pool.shape[3] != k_new.shape[2] or k_pool.shape[3] != q.shape[2]:
         raise ValueError("pool / new rows / q shape mismatch")
-    R = seq_lens.shape[0]
-    if query_start_loc.shape[0] != R + 1 or block_tables.shape[0] != R:
-        raise ValueError("seq_lens, query_start_loc and block_tables disagree on num_reqs")
+    R = check_attention_shapes(q, k_pool, v_pool, block_tables, seq_lens, query_start_loc)
     if out is None:
         out = torch.empty_like(q)
     else:
@@ -300,11 +355,7 @@ def pkv_attention_fp8kv(q, k_pool, v_pool, k_scale, v_scale, block_tables, seq_l
     _need(block_tables, "block_tables", torch.int32, 2)
     _need(seq_lens, "seq_lens", torch.int32, 1)
     _need(query_start_loc, "query_start_loc", torch.int32, 1)
-    R = seq_lens.shape[0]
-    if query_start_loc.shape[0] != R + 1 or block_tables.shape[0] != R:
-        raise ValueError("seq_lens, query_start_loc and block_tables disagree on num_reqs")
-    if v_pool.shape != k_pool.shape or k_pool.shape[3] != q.shape[2]:
-        raise ValueError("pool / q shape mismatch")
+    R = check_attention_shapes(q, k_pool, v_pool, block_tables, seq_lens, query_start_loc)
     _need_scales(k_scale, v_scale, k_pool.shape[1])
     if out is None:
         out = torch.empty_like(q)
@@ -358,11 +409,7 @@ def pkv_attention_cascade(q, k_pool, v_pool, block_tables, seq_lens, query_start
     G = group_first_req.shape[0]
     if group_num_reqs.shape[0] != G or group_prefix_blocks.shape[0] != G:
         raise ValueError("group arrays disagree on the group count")
-    R = seq_lens.shape[0]
-    if query_start_loc.shape[0] != R + 1 or block_tables.shape[0] != R:
-        raise ValueError("seq_lens, query_start_loc and block_tables disagree on num_reqs")
-    if v_pool.shape != k_pool.shape or k_pool.shape[3] != q.shape[2]:
-        raise ValueError("pool / q shape mismatch")
+    R = check_attention_shapes(q, k_pool, v_pool, block_tables, seq_lens, query_start_loc)
     if out is None:
         out = torch.empty_like(q)
     else:
@@ -397,9 +444,7 @@ def pkv_attention_noalloc(q, k_pool, v_pool, block_tables, seq_lens, query_start
                             (query_start_loc, "query_start_loc", torch.int32, 1),
                             (out, "out", torch.bfloat16, 3)):
         _need(t, name, dt, nd)
-    R = seq_lens.shape[0]
-    if query_start_loc.shape[0] != R + 1 or block_tables.shape[0] != R or out.shape != q.shape:
-        raise ValueError("inconsistent shapes")
+    R = check_attention_shapes(q, k_pool, v_pool, block_tables, seq_lens, query_start_loc, out)
     dims = make_dims(tuple(q.shape), tuple(k_pool.shape), R, block_tables.shape[1])
     _check(load_library().pkv_attention_noalloc(
         ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k_pool.data_ptr()),

@@ -34,7 +34,7 @@ int cuda_fail(cudaError_t e, const char* what) {
 // address as an argument.
 __device__ int g_device_error;
 
-constexpr int kMaxDevices = 64;
+using pkv::kMaxDevices;
 
 struct DeviceState {
   bool ready = false;
@@ -113,9 +113,57 @@ pkv::WorkspaceLayout layout_for(const pkv_dims* d, int sm_count) {
                                       d->num_q_heads / d->num_kv_heads, sm_count);
 }
 
+// ----------------------------------------------------------------- options
+// Process-wide launch and routing options: built-in defaults, overridden once
+// by the environment when first needed, then only by pkv_set_options.  Every
+// call works from one copy taken when it starts.
 int env_int(const char* name, int dflt) {
   const char* v = getenv(name);
   return (v && *v) ? atoi(v) : dflt;
+}
+
+bool options_valid(const pkv_options& o) {
+  return o.prefill_min_q >= 0 && o.align_slack >= 0 && o.min_chunk >= 1 && o.decode_grid >= 0 &&
+         o.wait_limit_us >= 1;
+}
+
+pkv_options options_from_env() {
+  pkv_options o{};
+  o.pdl = env_int("PKV_PDL", 1);
+  o.early_plan = env_int("PKV_EARLY_PLAN", 1);
+  o.early_kv = env_int("PKV_EARLY_KV", 1);
+  o.early_trigger = env_int("PKV_EARLY_TRIGGER", 0);
+  o.plan_cache = env_int("PKV_PLAN_CACHE", 1);
+  o.decode_tc = env_int("PKV_DECODE_TC", 1);
+  o.decode_tc_fp8 = env_int("PKV_DECODE_TC_FP8", 1);
+  o.prefill_min_q = env_int("PKV_PREFILL_MIN_Q", 16);
+  o.align = env_int("PKV_ALIGN", 1);
+  o.align_slack = env_int("PKV_ALIGN_SLACK", 64);
+  o.min_chunk = env_int("PKV_MIN_CHUNK", 4);
+  o.prefetch = env_int("PKV_PREFETCH", 1);
+  o.decode_grid = env_int("PKV_DECODE_GRID", 0);
+  o.wait_limit_us = env_int("PKV_WAIT_LIMIT_US", (int)(pkv::kDefaultWaitLimitNs / 1000));
+  o.debug_withhold_q = 0;  // never from the environment
+  // Out-of-range values from the environment fall back to the defaults.
+  if (o.prefill_min_q < 0) o.prefill_min_q = 16;
+  if (o.align_slack < 0) o.align_slack = 64;
+  if (o.min_chunk < 1) o.min_chunk = 4;
+  if (o.decode_grid < 0) o.decode_grid = 0;
+  if (o.wait_limit_us < 1) o.wait_limit_us = (int)(pkv::kDefaultWaitLimitNs / 1000);
+  return o;
+}
+
+std::mutex g_opts_mutex;
+bool g_opts_ready = false;
+pkv_options g_opts;
+
+pkv_options current_options() {
+  std::lock_guard<std::mutex> lock(g_opts_mutex);
+  if (!g_opts_ready) {
+    g_opts = options_from_env();
+    g_opts_ready = true;
+  }
+  return g_opts;
 }
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no link
@@ -192,6 +240,16 @@ int encode_q_map(CUtensorMap* m, const void* q, const pkv_dims* d, int group, in
 
 namespace pkv {
 void set_error_message(const char* msg) { snprintf(g_last_error, sizeof g_last_error, "%s", msg); }
+
+int attention_workspace_bytes(const pkv_dims* dims, size_t* bytes) {
+  *bytes = 0;
+  const int rc = check_dims(dims, true);
+  if (rc != PKV_OK) return rc;
+  DeviceState* st = device_state();
+  if (!st) return PKV_ERR_CUDA;
+  *bytes = layout_for(dims, st->sm_count).total;
+  return PKV_OK;
+}
 }  // namespace pkv
 
 namespace {
@@ -220,7 +278,7 @@ int append_impl(const void* k_new, const void* v_new, const int64_t* slot_mappin
   p.num_tokens = num_new_tokens;
   p.num_kv_heads = dims->num_kv_heads;
   p.num_blocks = dims->num_blocks;
-  p.pdl = env_int("PKV_PDL", 1) != 0;
+  p.pdl = current_options().pdl != 0;
   p.early_trigger = early_trigger && p.pdl;
   cudaError_t e = pkv::launch_append(p, stream);
   if (e != cudaSuccess) return cuda_fail(e, "append launch");
@@ -265,7 +323,7 @@ int pkv_append_fp8(const void* k_new, const void* v_new, const int64_t* slot_map
   p.num_tokens = num_new_tokens;
   p.num_kv_heads = dims->num_kv_heads;
   p.num_blocks = dims->num_blocks;
-  p.pdl = env_int("PKV_PDL", 1) != 0;
+  p.pdl = current_options().pdl != 0;
   cudaError_t e = pkv::launch_append_fp8(p, stream);
   if (e != cudaSuccess) return cuda_fail(e, "append_fp8 launch");
   return PKV_OK;
@@ -297,17 +355,15 @@ int pkv_copy_blocks(const void* k_src, const void* v_src, void* k_dst, void* v_d
   p.num_kv_heads = dims->num_kv_heads;
   p.src_blocks = src_num_blocks;
   p.dst_blocks = dst_num_blocks;
-  p.pdl = env_int("PKV_PDL", 1) != 0;
+  p.pdl = current_options().pdl != 0;
   cudaError_t e = pkv::launch_copy_blocks(p, st->sm_count, stream);
   if (e != cudaSuccess) return cuda_fail(e, "copy_blocks launch");
   return PKV_OK;
 }
 
 size_t pkv_attention_workspace_size(const pkv_dims* dims) {
-  if (check_dims(dims, true) != PKV_OK) return 0;
-  DeviceState* st = device_state();
-  if (!st) return 0;
-  return layout_for(dims, st->sm_count).total;
+  size_t bytes = 0;
+  return pkv::attention_workspace_bytes(dims, &bytes) == PKV_OK ? bytes : 0;
 }
 
 int pkv_workspace_init(void* workspace, size_t workspace_bytes, const pkv_dims* dims,
@@ -411,6 +467,7 @@ int attention_impl(const void* q, const void* k_pool, const void* v_pool, const 
   if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
     return fail(PKV_ERR_INVALID, "workspace must be 256-byte aligned");
 
+  const pkv_options opt = current_options();
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   pkv::DecodeParams p{};
   p.q = static_cast<const __nv_bfloat16*>(q);
@@ -424,7 +481,7 @@ int attention_impl(const void* q, const void* k_pool, const void* v_pool, const 
   p.qsl = query_start_loc;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.ws_cnt = reinterpret_cast<int*>(ws + w.cnt_off);
-  p.plan_cache = env_int("PKV_PLAN_CACHE", 1) != 0 && dims->num_reqs <= pkv::kPlanCacheReqs
+  p.plan_cache = opt.plan_cache != 0 && dims->num_reqs <= pkv::kPlanCacheReqs
                      ? reinterpret_cast<int*>(ws + w.plan_off)
                      : nullptr;
   p.plan_entries = w.plan_entries;
@@ -440,7 +497,7 @@ int attention_impl(const void* q, const void* k_pool, const void* v_pool, const 
   p.scale_log2 = scale * 1.4426950408889634f;
   // Requests with at least this many query tokens go to the tensor-core
   // prefill kernel (when the step has that many query tokens at all).
-  int prefill_min_q = env_int("PKV_PREFILL_MIN_Q", 16);
+  int prefill_min_q = opt.prefill_min_q;
   if (prefill_min_q < 1) prefill_min_q = 0x7fffffff;
   // Launch it only when the step can hold such a request next to one query
   // for every other request; otherwise the decode kernel serves every row
@@ -450,23 +507,23 @@ int attention_impl(const void* q, const void* k_pool, const void* v_pool, const 
       !fp8 && (long long)dims->num_q_tokens - dims->num_reqs + 1 >= (long long)prefill_min_q;
   p.prefill_min_q = run_prefill ? prefill_min_q : 0x7fffffff;
   p.num_slots = w.num_slots;
-  p.pdl = env_int("PKV_PDL", 1) != 0;
-  p.min_chunk = env_int("PKV_MIN_CHUNK", 4);
-  if (p.min_chunk < 1) p.min_chunk = 1;
-  p.align = env_int("PKV_ALIGN", 1) != 0;
-  p.align_slack = env_int("PKV_ALIGN_SLACK", 64);
-  p.prefetch = env_int("PKV_PREFETCH", 1) != 0;
-  p.early_plan = p.pdl && env_int("PKV_EARLY_PLAN", 1) != 0;
+  p.pdl = opt.pdl != 0;
+  p.min_chunk = opt.min_chunk;
+  p.align = opt.align != 0;
+  p.align_slack = opt.align_slack;
+  p.prefetch = opt.prefetch != 0;
+  p.early_plan = p.pdl && opt.early_plan != 0;
+  p.wait_limit_ns = (unsigned long long)opt.wait_limit_us * 1000ull;
+  p.debug_withhold_q = opt.debug_withhold_q != 0;
   const int group = dims->num_q_heads / dims->num_kv_heads;
   int grid = pkv::decode_grid(st->sm_count, group);
-  const int grid_env = env_int("PKV_DECODE_GRID", 0);  // tuning override, bounded by the slots
-  if (grid_env > 0 && 2 * grid_env <= w.num_slots) grid = grid_env;
+  // tuning override, bounded by the workspace's slots
+  if (opt.decode_grid > 0 && 2 * opt.decode_grid <= w.num_slots) grid = opt.decode_grid;
   // Groups of 4 or more query heads per KV head make the decode's FP32 FMA
   // work comparable to its HBM time; those run on the tensor cores, e4m3
   // pools included (their tiles widened to f16 in shared memory by two
-  // converter warps; PKV_DECODE_TC_FP8=0 keeps them on the SIMT decode).
-  const bool use_tc = group >= 4 && env_int("PKV_DECODE_TC", 1) != 0 &&
-                      (!fp8 || env_int("PKV_DECODE_TC_FP8", 1) != 0);
+  // converter warps; decode_tc_fp8 = 0 keeps them on the SIMT decode).
+  const bool use_tc = group >= 4 && opt.decode_tc != 0 && (!fp8 || opt.decode_tc_fp8 != 0);
   cudaError_t e;
   // Shared prefixes are read once by the prefix pass when the tensor-core
   // decode serves the step; otherwise every row reads its whole context (the
@@ -516,6 +573,7 @@ int attention_impl(const void* q, const void* k_pool, const void* v_pool, const 
     L.p.pre_o = reinterpret_cast<float*>(ws + cl.pre_o);
     L.p.pre_ml = reinterpret_cast<float*>(ws + cl.pre_ml);
     L.p.sched = reinterpret_cast<unsigned long long*>(ws + w.sched_off);
+    L.p.wait_limit_ns = p.wait_limit_ns;
     L.grid = st->sm_count;
     e = pkv::launch_prefill(L, group, stream);
     if (e != cudaSuccess) return cuda_fail(e, "prefix pass launch");
@@ -567,6 +625,7 @@ int attention_impl(const void* q, const void* k_pool, const void* v_pool, const 
     L.p.prefill_min_q = prefill_min_q;
     L.p.pdl = p.pdl;
     L.p.sched = reinterpret_cast<unsigned long long*>(ws + w.sched_off);
+    L.p.wait_limit_ns = p.wait_limit_ns;
     L.grid = st->sm_count;
     e = pkv::launch_prefill(L, group, stream);
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
@@ -598,9 +657,10 @@ int pkv_append_attention(const void* k_new, const void* v_new, const int64_t* sl
   // lengths and tables) before it waits for the append.  PKV_EARLY_TRIGGER=1
   // also lets it launch as soon as the append starts, before the kernel
   // ahead of the append has finished; q, out and the workspace then wait.
-  const bool pdl = env_int("PKV_PDL", 1) != 0;
-  const bool early = pdl && env_int("PKV_EARLY_KV", 1) != 0;
-  const bool trigger = early && env_int("PKV_EARLY_TRIGGER", 0) != 0;
+  const pkv_options opt = current_options();
+  const bool pdl = opt.pdl != 0;
+  const bool early = pdl && opt.early_kv != 0;
+  const bool trigger = early && opt.early_trigger != 0;
   rc = append_impl(k_new, v_new, slot_mapping, k_pool, v_pool, dims->num_q_tokens, dims, stream,
                    trigger);
   if (rc != PKV_OK) return rc;
@@ -639,6 +699,20 @@ int pkv_attention_fp8kv(const void* q, const void* k_pool, const void* v_pool,
   }
   return attention_impl(q, k_pool, v_pool, k_scale, v_scale, block_tables, seq_lens,
                         query_start_loc, scale, out, dims, workspace, workspace_bytes, stream);
+}
+
+void pkv_get_options(pkv_options* opts) {
+  if (opts) *opts = current_options();
+}
+
+int pkv_set_options(const pkv_options* opts) {
+  g_last_error[0] = '\0';
+  if (opts == nullptr) return fail(PKV_ERR_INVALID, "options is NULL");
+  if (!options_valid(*opts)) return fail(PKV_ERR_INVALID, "an option is out of range");
+  current_options();  // the environment is read once, before the first change
+  std::lock_guard<std::mutex> lock(g_opts_mutex);
+  g_opts = *opts;
+  return PKV_OK;
 }
 
 int pkv_get_device_error(cudaStream_t stream) {

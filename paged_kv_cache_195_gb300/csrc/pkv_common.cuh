@@ -23,8 +23,17 @@ constexpr int kErrBounds = 1;   // block id / slot / lengths out of range
 constexpr int kErrTimeout = 2;  // a bounded wait ran out
 constexpr int kErrCapacity = 4; // plan exceeded the workspace bound
 
-// A bounded wait gives up after this many nanoseconds of %globaltimer.
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+// Default of the bounded waits' limit (nanoseconds of %globaltimer); the
+// host passes the limit to every kernel (pkv_options.wait_limit_us).
+constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;  // 2 s
+
+// Per-CTA state of the bounded waits, in shared memory: the abort flag every
+// wait checks, and the limit after which a wait gives up.
+struct WaitCtl {
+  volatile int abort;
+  int pad;
+  unsigned long long limit_ns;
+};
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -61,25 +70,9 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
-// One potentially blocking probe of an mbarrier phase.  With
-// PKV_WAIT_HINT the warp may sleep until the phase completes or about
-// kSuspendHintNs pass; without it the probe returns at once.
-#ifndef PKV_WAIT_HINT
-#define PKV_WAIT_HINT 0
-#endif
-constexpr uint32_t kSuspendHintNs = 100000;
-
+// One probe of an mbarrier phase (returns at once).
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
-#if PKV_WAIT_HINT
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
-      : "memory");
-#else
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
@@ -87,26 +80,42 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "=r"(ok)
       : "r"(smem_u32(bar)), "r"(parity)
       : "memory");
-#endif
   return ok != 0;
 }
 
 // Waits for the phase with the given parity to complete.  Gives up and
-// returns false if the CTA's abort flag is set, or after kWaitLimitNs (then it
-// records kErrTimeout and sets the abort flag so that every other wait of the
-// CTA returns at once).
+// returns false if the CTA's abort flag is set, or after ctl->limit_ns (then
+// it records kErrTimeout and sets the abort flag so that every other wait of
+// the CTA returns at once).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err,
-                                          volatile int* abort_flag) {
+                                          WaitCtl* ctl) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
   while (true) {
-    if (*abort_flag) return false;
+    if (ctl->abort) return false;
     #pragma unroll 1
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
+    if (global_timer_ns() - t0 > ctl->limit_ns) {
       record_error(err, kErrTimeout);
-      *abort_flag = 1;
+      ctl->abort = 1;
+      return false;
+    }
+  }
+}
+
+// The same wait without the abort flag, for draining an aborted CTA: it
+// still gives up after ctl->limit_ns (recording kErrTimeout).
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, int* err,
+                                                WaitCtl* ctl) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  while (true) {
+    #pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (global_timer_ns() - t0 > ctl->limit_ns) {
+      record_error(err, kErrTimeout);
       return false;
     }
   }
@@ -197,19 +206,7 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// Packed fp32: d = a * b + c on both lanes of a float2 (one instruction;
-// PKV_SCALAR_FMA=1 builds two scalar FMAs instead, for comparison).
-#ifndef PKV_SCALAR_FMA
-#define PKV_SCALAR_FMA 0
-#endif
-#if PKV_SCALAR_FMA
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-  return make_float2(fmaf(a.x, b.x, c.x), fmaf(a.y, b.y, c.y));
-}
-__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
-  return make_float2(a.x * b.x, a.y * b.y);
-}
-#else
+// Packed fp32: d = a * b + c on both lanes of a float2 (one instruction).
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
   float2 d;
   asm("fma.rn.f32x2 %0, %1, %2, %3;"
@@ -228,7 +225,6 @@ __device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
         "l"(reinterpret_cast<unsigned long long&>(b)));
   return d;
 }
-#endif
 
 // Two packed bf16 -> two fp32 (exact: a bf16 is the top half of an fp32).
 __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {

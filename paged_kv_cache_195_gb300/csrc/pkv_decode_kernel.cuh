@@ -83,31 +83,14 @@ struct KvE4m3 {
   }
 };
 
-// Warp layout.  Blocks are consumed by four warp groups in turn; with an
-// even group size g the g query heads are split across the two warps of a
-// group (each warp owns g/2 heads: half the registers, twice the warps per
-// SM to hide latency), otherwise one warp holds all g heads.
-#ifndef PKV_HSPLIT
-#define PKV_HSPLIT 0
-#endif
-#ifndef PKV_GROUPS_SPLIT
-#define PKV_GROUPS_SPLIT 3
-#endif
-#ifndef PKV_DEC_GROUPS
-#define PKV_DEC_GROUPS 4  // warp groups (blocks in flight per round) without a head split
-#endif
-#ifndef PKV_DEC_CTAS
-#define PKV_DEC_CTAS 0    // CTAs per SM; 0: two when a warp holds at most 6 heads, else one
-#endif
+// Warp layout: blocks are consumed by four warp groups of one warp each, in
+// turn; a warp holds all g heads of the group.
 template <int G>
 struct DecodeCfg {
-  static constexpr int kHS = (PKV_HSPLIT && G % 2 == 0) ? 2 : 1;  // warps per group
-  static constexpr int kGH = G / kHS;                             // heads per warp
-  static constexpr int kMinCtas = PKV_DEC_CTAS > 0 ? PKV_DEC_CTAS : (kGH <= 6) ? 2 : 1;
-  static constexpr int kGroups = kHS == 2 ? PKV_GROUPS_SPLIT
-                                 : PKV_DEC_GROUPS > 0 ? PKV_DEC_GROUPS
-                                 : 4;
-  static constexpr int kCW = kGroups * kHS;                       // consumer warps
+  static constexpr int kGH = G;                                   // heads per warp
+  static constexpr int kMinCtas = (kGH <= 6) ? 2 : 1;             // CTAs per SM
+  static constexpr int kGroups = 4;                               // consumer warp groups
+  static constexpr int kCW = kGroups;                             // consumer warps
   static constexpr int kThreads = (kCW + 1) * 32;                 // + producer warp
   // Registers per thread that still let kMinCtas CTAs share an SM: each of
   // the four SM sub-partitions owns a quarter of the register file (16384)
@@ -126,31 +109,18 @@ struct DecodeCfg {
 // group, i.e. if the group count divides the ring depth.  Otherwise a warp
 // can run two phases ahead, pass a stale parity and read a stage that is
 // still being filled.
-#ifndef PKV_RING
-#define PKV_RING 8
-#endif
 template <int G, class KV>
 constexpr int stages_for() {
   constexpr int kWant =
-      (DecodeCfg<G>::kMinCtas == 2 ? PKV_RING : 20) * (KvBf16::kTileBytes / KV::kTileBytes);
+      (DecodeCfg<G>::kMinCtas == 2 ? 8 : 20) * (KvBf16::kTileBytes / KV::kTileBytes);
   constexpr int kGroups = DecodeCfg<G>::kGroups;
   return (kWant + kGroups - 1) / kGroups * kGroups;
 }
 constexpr float kNegBig = -1.0e30f;          // "no key seen yet" running max
-#ifndef PKV_LAZY_MAX
-#define PKV_LAZY_MAX 1
-#endif
-constexpr bool kLazyMax = PKV_LAZY_MAX != 0;  // raise the running max only when needed
 constexpr float kLazyMargin = 8.f;           // log2 of the largest probability allowed
 using plan::Piece;
 using plan::kEndRow;
 
-#ifndef PKV_P_DUP
-#define PKV_P_DUP 0
-#endif
-#ifndef PKV_PV_FAST
-#define PKV_PV_FAST 1
-#endif
 
 template <int G, class KV>
 struct __align__(128) DecodeSmem {
@@ -160,11 +130,7 @@ struct __align__(128) DecodeSmem {
   static constexpr int kStageBytes = 2 * KV::kTileBytes;  // K tile then V tile
   // Probabilities of one block, stored twice ({p, p}) so that the PV loop
   // feeds packed fp32 FMAs straight from 16-byte loads.
-#if PKV_P_DUP
-  static constexpr int kPStride = (Cfg::kGH + 1) & ~1;  // float2 entries per token
-#else
   static constexpr int kPStride = ((Cfg::kGH + 3) & ~3) / 2;  // float2 slots = 2 floats each
-#endif
   uint8_t ring[kStages][kStageBytes];
   __nv_bfloat16 qbuf[2][G * kHeadDim];
   float2 pbuf[Cfg::kCW][kBlockSize][kPStride];
@@ -177,7 +143,7 @@ struct __align__(128) DecodeSmem {
   uint64_t empty[kStages];
   uint64_t qfull[2];
   uint64_t qempty[2];
-  int abort_flag;
+  WaitCtl wait;                   // abort flag and wait limit of the bounded waits
   int is_last;
   int wait_ok[Cfg::kCW];
   int end_flag[Cfg::kCW];
@@ -227,15 +193,6 @@ struct BlockMath {  // G = query heads this warp holds
                                                   float2 (*pbuf)[kPStride]) {
     float2 vv[4];
     KV::load8(Vt + tok * KV::kRowBytes, c, vv);
-#if PKV_P_DUP
-    float2 pr[kPStride];
-    #pragma unroll
-    for (int i = 0; i < kPStride; i += 2) {
-      const float4 t4 = *reinterpret_cast<const float4*>(&pbuf[tok][i]);
-      pr[i] = make_float2(t4.x, t4.y);
-      pr[i + 1] = make_float2(t4.z, t4.w);
-    }
-#else
     float prs[2 * kPStride];
     #pragma unroll
     for (int i = 0; i < 2 * kPStride; i += 4) {
@@ -243,14 +200,9 @@ struct BlockMath {  // G = query heads this warp holds
           *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(pbuf[tok]) + i);
       prs[i] = t4.x; prs[i + 1] = t4.y; prs[i + 2] = t4.z; prs[i + 3] = t4.w;
     }
-#endif
     #pragma unroll
     for (int h = 0; h < G; ++h) {
-#if PKV_P_DUP
-      const float2 p2 = pr[h];
-#else
       const float2 p2 = make_float2(prs[h], prs[h]);
-#endif
       #pragma unroll
       for (int i = 0; i < 4; ++i) acc[h][i] = ffma2(p2, vv[i], acc[h][i]);
     }
@@ -326,7 +278,7 @@ struct BlockMath {  // G = query heads this warp holds
       else mo[j] = m[j];
       over |= sc[j] > mo[j] + kLazyMargin;
     }
-    if (!kLazyMax || __any_sync(0xffffffffu, over)) {
+    if (__any_sync(0xffffffffu, over)) {
       float bm[F];
       #pragma unroll
       for (int j = 0; j < F; ++j) bm[j] = sc[j];
@@ -383,17 +335,13 @@ struct BlockMath {  // G = query heads this warp holds
       const int h = head_of_slot(j, b0);
       const float pj = fast_exp2(sc[j] - mo[j]);
       lsum[j] += pj;
-#if PKV_P_DUP
-      if (kEven || b0 == 0) pbuf[tl][h] = make_float2(pj, pj);
-#else
       if (kEven || b0 == 0) reinterpret_cast<float*>(pbuf[tl])[h] = pj;
-#endif
     }
     __syncwarp();
     // ---- PV over this half's 8 tokens --------------------------------------
     // Full blocks (every block but a row's last) take a loop without
     // per-token checks.
-    if (PKV_PV_FAST && nvalid >= kBlockSize) {
+    if (nvalid >= kBlockSize) {
       #pragma unroll
       for (int tt = 0; tt < 8; ++tt) pv_token(Vt, half * 8 + tt, c, acc, pbuf);
     } else {
@@ -413,7 +361,7 @@ __global__ void __launch_bounds__(DecodeCfg<G>::kThreads) __maxnreg__(DecodeCfg<
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   using Smem = DecodeSmem<G, KV>;
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
-  volatile int* abort_flag = &sm.abort_flag;
+  WaitCtl* abort_flag = &sm.wait;
   constexpr int kStages = Smem::kStages;
   constexpr int kStageBytes = Smem::kStageBytes;
   constexpr int kTile = KV::kTileBytes;
@@ -426,13 +374,14 @@ __global__ void __launch_bounds__(DecodeCfg<G>::kThreads) __maxnreg__(DecodeCfg<
     #pragma unroll
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.full[s], 1);
-      mbar_init(&sm.empty[s], DecodeCfg<G>::kHS);
+      mbar_init(&sm.empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.qfull[b], 1);
       mbar_init(&sm.qempty[b], DecodeCfg<G>::kCW);
     }
-    sm.abort_flag = 0;
+    sm.wait.abort = 0;
+    sm.wait.limit_ns = p.wait_limit_ns;
     fence_barrier_init();
   }
   __syncthreads();
@@ -487,7 +436,7 @@ __global__ void __launch_bounds__(DecodeCfg<G>::kThreads) __maxnreg__(DecodeCfg<
       q_pend = 0;
     };
     Piece pc;
-    while (!*abort_flag && wk.next(p, pc)) {
+    while (!abort_flag->abort && wk.next(p, pc)) {
       // ---- one piece: blocks [b0, b0 + nblk) of row-group (row, k) --------
       const int k = pc.k;
       const int ub = j & 1;
@@ -507,7 +456,7 @@ __global__ void __launch_bounds__(DecodeCfg<G>::kThreads) __maxnreg__(DecodeCfg<
         if (ub == 0) q_src0 = qsrc; else q_src1 = qsrc;
       }
       const int32_t* bt = p.block_tables + (long long)pc.r * p.max_blocks + pc.b0;
-      for (int bb = 0; bb < pc.nblk && !*abort_flag; bb += 32) {
+      for (int bb = 0; bb < pc.nblk && !abort_flag->abort; bb += 32) {
         const int cnt = min(32, pc.nblk - bb);
         const int ent = lane < cnt ? __ldg(bt + bb + lane) : 0;
         for (int xb = 0; xb < cnt; ++xb, ++n) {
@@ -541,7 +490,7 @@ __global__ void __launch_bounds__(DecodeCfg<G>::kThreads) __maxnreg__(DecodeCfg<
     }
     // The CTA finishes after the previous kernel in any case; Q copies still
     // pending are issued unless the CTA is giving up.
-    if (*abort_flag) q_pend = 0;
+    if (abort_flag->abort) q_pend = 0;
     take_wait();
     // End marker: no more pieces for this CTA.
     const int ub = j & 1;
@@ -557,14 +506,13 @@ __global__ void __launch_bounds__(DecodeCfg<G>::kThreads) __maxnreg__(DecodeCfg<
   // ========================= consumer warps ================================
   if (p.early_kv && !p.early_q) grid_dependency_wait();  // out and the workspace are written below
   using Cfg = DecodeCfg<G>;
-  constexpr int GH = Cfg::kGH;  // heads of this warp: ho .. ho + GH - 1
+  constexpr int GH = Cfg::kGH;  // heads of this warp: all G of the group
   using BM = BlockMath<GH, Smem::kPStride, KV>;
   constexpr int F = BM::F;
   constexpr int kConsumerThreads = Cfg::kCW * 32;
   const int cw = warp;
   constexpr int kGroups = Cfg::kGroups;
-  const int grp = cw / Cfg::kHS;       // the warp group that takes a block
-  const int ho = (cw % Cfg::kHS) * GH;  // first head of this warp
+  const int grp = cw;  // the warp group (one warp) that takes a block
   const int ct = tid;  // 0..127: the output dim this thread writes in the epilogue
   const int c = lane & 15;
   const int b0bit = lane & 1;
@@ -593,7 +541,7 @@ __global__ void __launch_bounds__(DecodeCfg<G>::kThreads) __maxnreg__(DecodeCfg<
     float2 qf[GH][4];
     #pragma unroll
     for (int hs = 0; hs < GH; ++hs) {
-      const int hl = ho + BM::head_of_slot(hs, b0bit);
+      const int hl = BM::head_of_slot(hs, b0bit);
       const uint4 w = lds128(&sm.qbuf[ub][hl * kHeadDim + c * 8]);
       const float qs = p.scale_log2 * kscale;
       const float2 s2 = make_float2(qs, qs);
@@ -680,7 +628,7 @@ __global__ void __launch_bounds__(DecodeCfg<G>::kThreads) __maxnreg__(DecodeCfg<
     if (lane < 16) {
       #pragma unroll
       for (int h = 0; h < GH; ++h) {
-        float4* dst = reinterpret_cast<float4*>(&sm.comb[grp][ho + h][c * 8]);
+        float4* dst = reinterpret_cast<float4*>(&sm.comb[grp][h][c * 8]);
         dst[0] = make_float4(acc[h][0].x, acc[h][0].y, acc[h][1].x, acc[h][1].y);
         dst[1] = make_float4(acc[h][2].x, acc[h][2].y, acc[h][3].x, acc[h][3].y);
       }
@@ -688,8 +636,8 @@ __global__ void __launch_bounds__(DecodeCfg<G>::kThreads) __maxnreg__(DecodeCfg<
     if (lane == 0) {
       #pragma unroll
       for (int h = 0; h < GH; ++h) {
-        sm.comb_m[grp][ho + h] = m[h];
-        sm.comb_l[grp][ho + h] = lall[h];
+        sm.comb_m[grp][h] = m[h];
+        sm.comb_l[grp][h] = lall[h];
       }
       sm.wait_ok[cw] = in_range;
       sm.end_flag[cw] = is_end;
@@ -782,14 +730,6 @@ __global__ void __launch_bounds__(DecodeCfg<G>::kThreads) __maxnreg__(DecodeCfg<
 template <int G, class KV>
 cudaError_t launch_decode_g(const DecodeParams& p, int grid, cudaStream_t stream) {
   using Smem = DecodeSmem<G, KV>;
-  if (getenv("PKV_DEBUG")) {
-    int occ = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_kernel<G, KV>, DecodeCfg<G>::kThreads,
-                                                  sizeof(Smem));
-    fprintf(stderr, "decode_kernel<%d, %s>: smem %zu B, %d CTAs/SM resident, grid %d\n", G,
-            KV::kFp8 ? "e4m3" : "bf16",
-            sizeof(Smem), occ, grid);
-  }
   const size_t smem = sizeof(Smem);
   static unsigned long long configured = 0;  // bit per device ordinal
   int dev = 0;

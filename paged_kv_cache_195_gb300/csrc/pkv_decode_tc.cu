@@ -65,13 +65,7 @@ constexpr int kBlkPerTile = kTile / kBlockSize;
 constexpr int kN = 16;                     // MMA N: the group's heads, padded
 constexpr int kHalf = kTile * 128;         // one 64-dim half of a 128-key bf16 tile
 constexpr int kOpHalf = kN * 128;          // one 64-element half of a 16-row operand
-#ifndef PKV_TC_STAGES
-#define PKV_TC_STAGES 3
-#endif
-constexpr int kStages = PKV_TC_STAGES;     // K/V tile stages (64 KiB each)
-#ifndef PKV_TC_PV_FIRST
-#define PKV_TC_PV_FIRST 1
-#endif
+constexpr int kStages = 3;                 // K/V tile stages (64 KiB each)
 constexpr uint32_t kTmemCols = 64;         // S0: 0..15, S1: 16..31, O0: 32..47, O1: 48..63
 constexpr uint32_t kColO = 32;             // O^T of piece j in columns kColO + (j & 1) * kN
 constexpr float kNegBig = -1.0e30f;
@@ -128,8 +122,9 @@ struct __align__(1024) TcSmem {
   uint64_t s_full[2], s_free[2], p_full[2], p_free[2];
   uint64_t o_full[2], o_empty[2];  // O^T buffer complete / read by the epilogue
   uint64_t st_full[2], st_empty[2];  // piece statistics published / consumed
+  uint64_t mma_done;              // an aborted CTA's last tcgen05.commit
   uint32_t tmem_base;
-  int abort_flag;
+  WaitCtl wait;                   // abort flag and wait limit of the bounded waits
   int is_last;
   int conv_end;                   // e4m3 pools: tiles issued in all (set at the end)
 };
@@ -194,7 +189,7 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 1)
   // 128-byte swizzled operands need 1024-byte aligned shared addresses.
   const uint32_t raw = smem_u32(smem_raw);
   TcSmem& sm = *reinterpret_cast<TcSmem*>(smem_raw + (((raw + 1023u) & ~1023u) - raw));
-  volatile int* abort_flag = &sm.abort_flag;
+  WaitCtl* abort_flag = &sm.wait;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hkv = p.num_kv_heads;
   if (tid == 0) TC_CTA(0);
@@ -265,7 +260,9 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 1)
       mbar_init(&sm.st_full[b], 4);   // the softmax warps have published the statistics
       mbar_init(&sm.st_empty[b], 4);  // the epilogue warps have read them
     }
-    sm.abort_flag = 0;
+    mbar_init(&sm.mma_done, 1);
+    sm.wait.abort = 0;
+    sm.wait.limit_ns = p.wait_limit_ns;
     sm.conv_end = INT_MAX;
     fence_barrier_init();
   }
@@ -326,7 +323,16 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 1)
     // Q copies of pieces met before the wait (at most the two buffers'),
     // issued once it has been taken.
     int q_pend = 0, q_row0 = 0, q_row1 = 0, q_k0 = 0, q_k1 = 0;
+    // Per Q buffer: phases armed so far, and whether the last armed phase's
+    // copy was issued (an aborted CTA drains the copies in flight).
+    int q_armed[2] = {0, 0};
+    bool q_copy[2] = {false, false};
     auto issue_q = [&](int ub, int row, int kh) {
+      // Testing only: the first piece's q is never loaded, so the waits on
+      // it run out and the CTA takes the timeout path.
+      // (Piece 0 is buffer 0's first phase.)
+      if (p.debug_withhold_q && ub == 0 && q_armed[0] == 1) return;
+      q_copy[ub] = true;
       if (lane == 0) {
         tma_load_3d(sm.q[ub][0], &qmap, 0, kh * G, row, &sm.q_full[ub]);
         tma_load_3d(sm.q[ub][1], &qmap, 64, kh * G, row, &sm.q_full[ub]);
@@ -344,8 +350,9 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 1)
       q_pend = 0;
     };
     int j = 0, t = 0;  // piece and tile counters
+    int n_issued = 0;  // tiles whose copies have been issued
     bool ok = true;
-    while (ok && have && !*abort_flag) {
+    while (ok && have && !abort_flag->abort) {
       const int k = pc.k;
       const int ntile = plan::cdiv(pc.nblk, kBlkPerTile);
       int ent_cur = ent_first;
@@ -397,6 +404,7 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 1)
           }
         }
         __syncwarp();
+        n_issued = t + 1;
         if (tt == 0) {
           // Q of this piece, once the MMAs of piece j-2 are done with its
           // buffer (the piece's first K/V tile is already on its way).
@@ -412,6 +420,8 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 1)
             sm.pinfo[ub] = pc;
             mbar_arrive_expect_tx(&sm.q_full[ub], 2u * 64u * G * 2u);
           }
+          ++q_armed[ub];
+          q_copy[ub] = false;
           if (waited || p.early_q) {
             issue_q(ub, pc.row, k);
           } else {
@@ -451,9 +461,9 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 1)
     }
     // The CTA finishes after the previous kernel in any case; Q copies still
     // pending are issued unless the CTA is giving up.
-    if (*abort_flag) q_pend = 0;
+    if (abort_flag->abort) q_pend = 0;
     take_wait();
-    if (F8 && ok && !*abort_flag) {
+    if (F8 && ok && !abort_flag->abort) {
       // Tell the converter warps that tile t does not exist: completing the
       // phase they wait on for it, once its stage's previous tile is done.
       const int st = t % kStages;
@@ -465,13 +475,30 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 1)
       }
       __syncwarp();
     }
-    // End marker: no more pieces for this CTA.
-    const int ub = j & 1;
-    if (j < 2 || mbar_wait(&sm.q_empty[ub], ((j >> 1) - 1) & 1, p.err, abort_flag)) {
-      if (lane == 0) {
-        sm.pinfo[ub].row = kEndRow;
-        mbar_arrive(&sm.q_full[ub]);
+    if (!abort_flag->abort) {
+      // End marker: no more pieces for this CTA.  (An aborted CTA sends none:
+      // every wait returns at once, and the buffer's phase may already have
+      // its arrival.)
+      const int ub = j & 1;
+      if (j < 2 || mbar_wait(&sm.q_empty[ub], ((j >> 1) - 1) & 1, p.err, abort_flag)) {
+        if (lane == 0) {
+          sm.pinfo[ub].row = kEndRow;
+          mbar_arrive(&sm.q_full[ub]);
+        }
       }
+    }
+    if (abort_flag->abort) {
+      // Copies still in flight must land before the CTA's shared memory is
+      // released: the last tile of each stage and the last Q of each buffer.
+      for (int tp = max(0, n_issued - kStages); tp < n_issued; ++tp) {
+        const int st = tp % kStages;
+        const uint32_t par = (tp / kStages) & 1;
+        mbar_wait_drain(F8 ? &sm.kraw_full[st] : &sm.k_full[st], par, p.err, abort_flag);
+        mbar_wait_drain(F8 ? &sm.vraw_full[st] : &sm.v_full[st], par, p.err, abort_flag);
+      }
+      for (int ub = 0; ub < 2; ++ub)
+        if (q_armed[ub] > 0 && q_copy[ub])
+          mbar_wait_drain(&sm.q_full[ub], (q_armed[ub] - 1) & 1, p.err, abort_flag);
     }
   } else if (warp == 5) {
     // ============================ MMA issuer ==============================
@@ -525,7 +552,7 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 1)
           const int b = t & 1, st = t % kStages;
           // The previous tile's PV first: its stage is released as soon as
           // its probabilities are ready, not after this tile's keys arrive.
-          if (PKV_TC_PV_FIRST && tt >= 1) pv(t - 1, tt == 1, j);
+          if (tt >= 1) pv(t - 1, tt == 1, j);
           ok = ok && mbar_wait(&sm.k_full[st], (t / kStages) & 1, p.err, abort_flag);
           TC_TR(1, t);
           if (t == 0) TC_CTA(4);
@@ -546,12 +573,16 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 1)
           mbar_wait(&sm.s_full[b], (t >> 1) & 1, p.err, abort_flag);  // QK completion
           TC_TR(5, t);
 #endif
-          if (!PKV_TC_PV_FIRST && tt >= 1) pv(t - 1, tt == 1, j);
         }
         if (ok) pv(t - 1, ntile == 1, j);  // the piece's last tile
         tc_commit(&sm.o_full[ub]);
         TC_CTA(17);
         tc_commit(&sm.q_empty[ub]);
+      }
+      if (abort_flag->abort) {
+        // The MMAs already issued must finish before TMEM is freed.
+        tc_commit(&sm.mma_done);
+        mbar_wait_drain(&sm.mma_done, 0, p.err, abort_flag);
       }
     }
     __syncwarp();

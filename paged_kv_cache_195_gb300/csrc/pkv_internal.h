@@ -10,7 +10,12 @@
 
 #include "pkv_common.cuh"
 
+struct pkv_dims;  // include/pagedkv.h
+
 namespace pkv {
+
+// Device ordinals the library keeps per-device state for (0 .. kMaxDevices-1).
+constexpr int kMaxDevices = 64;
 
 struct AppendParams {
   const __nv_bfloat16* k_new;
@@ -97,6 +102,10 @@ struct DecodeParams {
   const float* pre_o;
   const float* pre_ml;
   int pdl;            // launch with programmatic stream serialization
+  unsigned long long wait_limit_ns;  // bounded device waits give up after this long
+  // Testing only: the tensor-core decode's producer arms the first piece's
+  // q barrier but never issues its copy, so the waits on it run out.
+  int debug_withhold_q;
 };
 
 // Workspace carve-up shared by the host code that sizes it and the launcher.
@@ -178,6 +187,7 @@ struct PrefillParams {
   // Work queue: [0] next item, [1] CTAs done; zero between launches (the
   // last CTA to finish resets both).
   unsigned long long* sched;
+  unsigned long long wait_limit_ns;  // bounded device waits give up after this long
 };
 
 // Shared-prefix (cascade) prefix pass: a group's shared keys (L of them) are
@@ -247,6 +257,9 @@ cudaError_t prefill_trace(void* host, size_t bytes);
 
 // Sets the thread's pkv_last_error() message.
 void set_error_message(const char* msg);
+
+// pkv_attention_workspace_size with its error code (message set on failure).
+int attention_workspace_bytes(const ::pkv_dims* dims, size_t* bytes);
 
 cudaError_t launch_prefill(const PrefillLaunch& L, int group, cudaStream_t stream);
 

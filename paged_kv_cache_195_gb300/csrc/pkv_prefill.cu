@@ -62,9 +62,6 @@ __device__ unsigned long long g_pf_trace[5][kPfTrTiles];
 #else
 #define PF_TR(ev, tile) do { } while (0)
 #endif
-#ifndef PKV_PF_PV_FIRST
-#define PKV_PF_PV_FIRST 0  // issue the previous tile's PV before this tile's QK^T
-#endif
 constexpr int kPastEnd = INT_MIN;            // block-table slot past the request (not read)
 
 struct Item {
@@ -95,7 +92,7 @@ struct __align__(1024) PfSmem {
   Item vitems[4];                // items handed from the K producer to the V producer
   uint64_t vitem_full[4], vitem_empty[4];
   uint32_t tmem_base;
-  int abort_flag;
+  WaitCtl wait;                   // abort flag and wait limit of the bounded waits
 };
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
@@ -157,7 +154,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   // 128-byte swizzled tiles need 1024-byte aligned shared addresses.
   const uint32_t raw = smem_u32(smem_raw);
   PfSmem& sm = *reinterpret_cast<PfSmem*>(smem_raw + (((raw + 1023u) & ~1023u) - raw));
-  volatile int* abort_flag = &sm.abort_flag;
+  WaitCtl* abort_flag = &sm.wait;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hkv = p.num_kv_heads;
 
@@ -181,12 +178,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       total += cnt;
     }
     if (lane == 0) {
-      sm.abort_flag = (long long)blockIdx.x >= total;  // reused as "idle"
+      sm.wait.abort = (long long)blockIdx.x >= total;  // reused as "idle"
       sm.items[0].r = (int)min(total, (long long)gridDim.x);  // CTAs that take items
     }
   }
   __syncthreads();
-  if (sm.abort_flag) {
+  if (sm.wait.abort) {
     allow_dependent_launch();
     grid_dependency_wait();
     return;
@@ -214,7 +211,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       mbar_init(&sm.vitem_full[b], 1);
       mbar_init(&sm.vitem_empty[b], 1);
     }
-    sm.abort_flag = 0;
+    sm.wait.abort = 0;
+    sm.wait.limit_ns = p.wait_limit_ns;
     fence_barrier_init();
   }
   if (warp == 4 && lane == 0) {
@@ -341,7 +339,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       long long base = 0;            // items before the current request batch
       const int nunits = num_units(p);
       bool ok = true;
-      for (int b = 0; b < nunits && ok && !*abort_flag; b += 32) {
+      for (int b = 0; b < nunits && ok && !abort_flag->abort; b += 32) {
         const int rr = b + lane;
         PfReq rq = {0, 0, 0, 0, 0, 1, false};
         if (rr < nunits) rq = load_pf_request(p, rr, TQ);
@@ -354,7 +352,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         const long long excl = incl - cnt;
         const long long total = __shfl_sync(0xffffffffu, incl, 31);
-        while (item < base + total && ok && !*abort_flag) {
+        while (item < base + total && ok && !abort_flag->abort) {
           const long long rel = item - base;
           const unsigned own = __ballot_sync(0xffffffffu, cnt > 0 && excl <= rel && rel < incl);
           const int src = __ffs(own) - 1;
@@ -438,7 +436,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         tc_fence_after();
         for (int j = 0; j < it.nj && ok; ++j, ++t) {
           const int b = t & 1, st = t % kPfStages;
-          if (PKV_PF_PV_FIRST && j >= 1) pv(t - 1, j == 1, n_item);
           ok = ok && mbar_wait(&sm.k_full[st], (t / kPfStages) & 1, p.err, abort_flag);
           PF_TR(1, t);
           // S buffer b holds P(t - 2) until the PV of tile t - 2 has read it.
@@ -453,7 +450,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           }
           tc_commit(&sm.k_empty[st]);
           tc_commit(&sm.s_full[b]);
-          if (!PKV_PF_PV_FIRST && j >= 1) pv(t - 1, j == 1, n_item);
+          if (j >= 1) pv(t - 1, j == 1, n_item);
         }
         if (ok) pv(t - 1, it.nj == 1, n_item);  // the item's last tile
         tc_commit(&sm.o_full);

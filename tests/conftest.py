@@ -11,3 +11,17 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line(
         "markers", "gpu: needs a CUDA GPU (sm_103a) and the built CUDA library")
+
+
+@pytest.fixture
+def pkv_opts():
+    """Setter of the library's options for one test; the options in force
+    before the test are put back afterwards."""
+    import paged_kv_cache_195_gb300 as pkv
+    saved = pkv.get_options()
+
+    def set_(**changes):
+        pkv.set_options(**changes)
+
+    yield set_
+    pkv.set_options(**saved)

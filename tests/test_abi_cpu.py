@@ -152,3 +152,92 @@ def test_copy_blocks_rejects_bad_arguments(lib):
                                None) == b.PKV_ERR_INVALID
     assert lib.pkv_copy_blocks(fake, fake, fake, fake, fake, 0, 8, 8, ctypes.byref(d),
                                None) == b.PKV_OK
+
+
+# ---------------------------------------------------------------------------
+# launch and routing options (pkv_options)
+# ---------------------------------------------------------------------------
+
+def test_options_struct_matches_header():
+    text = open(os.path.join(ROOT, "include", "pagedkv.h")).read()
+    body = re.search(r"typedef struct pkv_options \{(.*?)\} pkv_options;", text, re.S).group(1)
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    fields = re.findall(r"int32_t\s+(\w+);", body)
+    assert tuple(fields) == b.OPTION_FIELDS
+
+
+def test_options_defaults_and_round_trip(lib):
+    o = pkv.get_options()
+    assert o["pdl"] in (0, 1) and o["min_chunk"] >= 1 and o["wait_limit_us"] >= 1
+    assert o["debug_withhold_q"] == 0
+    with pkv.options(prefill_min_q=3, decode_tc=0):
+        now = pkv.get_options()
+        assert now["prefill_min_q"] == 3 and now["decode_tc"] == 0
+        assert {k: v for k, v in now.items() if k not in ("prefill_min_q", "decode_tc")} == \
+            {k: v for k, v in o.items() if k not in ("prefill_min_q", "decode_tc")}
+    assert pkv.get_options() == o
+
+
+@pytest.mark.parametrize("bad", [{"min_chunk": 0}, {"wait_limit_us": 0}, {"prefill_min_q": -1},
+                                 {"align_slack": -5}, {"decode_grid": -1}])
+def test_out_of_range_options_are_rejected(lib, bad):
+    o = pkv.get_options()
+    with pytest.raises(pkv.PagedKVError) as e:
+        pkv.set_options(**bad)
+    assert e.value.code == b.PKV_ERR_INVALID
+    assert pkv.get_options() == o
+
+
+def test_options_come_from_the_environment_once(tmp_path):
+    code = ("import paged_kv_cache_195_gb300 as pkv, os, json\n"
+            "a = pkv.get_options()\n"
+            "os.environ['PKV_PREFILL_MIN_Q'] = '9'\n"
+            "b = pkv.get_options()\n"
+            "print(json.dumps([a['prefill_min_q'], a['decode_tc'], a['wait_limit_us'],"
+            " b['prefill_min_q']]))\n")
+    env = dict(os.environ, PKV_PREFILL_MIN_Q="7", PKV_DECODE_TC="0", PKV_WAIT_LIMIT_US="1000")
+    import json
+    import subprocess
+    import sys
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                       cwd=ROOT, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    # read at first use; a later change of the environment is not seen
+    assert json.loads(r.stdout.strip().splitlines()[-1]) == [7, 0, 1000, 7]
+
+
+# ---------------------------------------------------------------------------
+# shape checks of the Python binding (before any launch)
+# ---------------------------------------------------------------------------
+
+def _attention_tensors(v_pool_shape=None, out_shape=None, R=3):
+    import torch
+    q = torch.zeros(4, 12, 128, dtype=torch.bfloat16)
+    kp = torch.zeros(10, 2, 16, 128, dtype=torch.bfloat16)
+    vp = torch.zeros(*(v_pool_shape or kp.shape), dtype=torch.bfloat16)
+    bt = torch.zeros(R, 5, dtype=torch.int32)
+    sl = torch.zeros(R, dtype=torch.int32)
+    qsl = torch.zeros(R + 1, dtype=torch.int32)
+    out = torch.zeros(*(out_shape or q.shape), dtype=torch.bfloat16)
+    return q, kp, vp, bt, sl, qsl, out
+
+
+def test_shape_check_accepts_consistent_tensors():
+    assert b.check_attention_shapes(*_attention_tensors()) == 3
+
+
+@pytest.mark.parametrize("vshape", [(8, 2, 16, 128), (10, 1, 16, 128), (10, 2, 16, 64)])
+def test_mismatched_v_pool_is_rejected_before_any_launch(vshape):
+    with pytest.raises(ValueError, match="v_pool"):
+        b.check_attention_shapes(*_attention_tensors(v_pool_shape=vshape))
+
+
+def test_head_dim_and_out_mismatch_are_rejected():
+    q, kp, vp, bt, sl, qsl, out = _attention_tensors()
+    import torch
+    with pytest.raises(ValueError):
+        b.check_attention_shapes(q[:, :, :64].contiguous(), kp, vp, bt, sl, qsl)
+    with pytest.raises(ValueError, match="out"):
+        b.check_attention_shapes(q, kp, vp, bt, sl, qsl, torch.zeros(3, 12, 128))
+    with pytest.raises(ValueError, match="num_reqs"):
+        b.check_attention_shapes(q, kp, vp, bt[:2], sl, qsl)

@@ -67,18 +67,17 @@ def test_committed_traffic_is_dropped_when_code_changes(bench, tmp_path, monkeyp
     assert bench.committed_traffic("qwen_decode", "bf16") is None
 
 
-def test_decode_kernel_names_follow_the_routing(bench, monkeypatch):
-    monkeypatch.delenv("PKV_DECODE_TC", raising=False)
-    monkeypatch.delenv("PKV_DECODE_TC_FP8", raising=False)
-    assert bench.decode_kernel_name(6, False) == "pkv::decode_tc_kernel<6, false>"
-    assert bench.decode_kernel_name(4, True) == "pkv::decode_tc_kernel<4, true>"
-    assert bench.decode_kernel_name(2, False) == "pkv::decode_kernel<2, KvBf16>"
-    assert bench.decode_kernel_name(3, True) == "pkv::decode_kernel<3, KvE4m3>"
-    monkeypatch.setenv("PKV_DECODE_TC_FP8", "0")
-    assert bench.decode_kernel_name(6, True) == "pkv::decode_kernel<6, KvE4m3>"
-    assert bench.decode_kernel_name(6, False) == "pkv::decode_tc_kernel<6, false>"
-    monkeypatch.setenv("PKV_DECODE_TC", "0")
-    assert bench.decode_kernel_name(6, False) == "pkv::decode_kernel<6, KvBf16>"
+def test_decode_kernel_names_follow_the_routing(bench):
+    on = {"decode_tc": 1, "decode_tc_fp8": 1}
+    assert bench.decode_kernel_name(6, False, on) == "pkv::decode_tc_kernel<6, false>"
+    assert bench.decode_kernel_name(4, True, on) == "pkv::decode_tc_kernel<4, true>"
+    assert bench.decode_kernel_name(2, False, on) == "pkv::decode_kernel<2, KvBf16>"
+    assert bench.decode_kernel_name(3, True, on) == "pkv::decode_kernel<3, KvE4m3>"
+    simt_fp8 = {"decode_tc": 1, "decode_tc_fp8": 0}
+    assert bench.decode_kernel_name(6, True, simt_fp8) == "pkv::decode_kernel<6, KvE4m3>"
+    assert bench.decode_kernel_name(6, False, simt_fp8) == "pkv::decode_tc_kernel<6, false>"
+    simt = {"decode_tc": 0, "decode_tc_fp8": 1}
+    assert bench.decode_kernel_name(6, False, simt) == "pkv::decode_kernel<6, KvBf16>"
 
 
 def test_reference_arm_prints_the_benchmark_line():
@@ -95,3 +94,29 @@ def test_reference_arm_prints_the_benchmark_line():
     assert line["e2e"] == {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
     assert line["config"]["workload"]
+
+
+def test_cpu_sample_bytes_follow_the_requests_run(bench):
+    # ragged lengths: the bytes of the first n requests, not n x request 0's
+    from paged_kv_cache_195_gb300 import roofline as rl
+    from paged_kv_cache_195_gb300 import workloads as wl
+    shape = wl.llama_mixed()
+    for n in (1, 7, 100, shape.num_reqs):
+        want = rl.attention_bytes(shape.seq_lens[:n], shape.q_lens[:n], 32, 8)["total"]
+        assert bench.sample_bytes(shape, n, "bf16") == want
+    per_req0 = rl.attention_bytes(shape.seq_lens[:1], shape.q_lens[:1], 32, 8)["total"]
+    assert bench.sample_bytes(shape, 100, "bf16") != 100 * per_req0
+    e4m3 = bench.sample_bytes(shape, 10, "fp8")
+    assert e4m3 == rl.attention_bytes(shape.seq_lens[:10], shape.q_lens[:10], 32, 8,
+                                      kv_dtype_bytes=1)["total"]
+
+
+def test_lengths_summary(bench):
+    assert bench.lengths_summary([512] * 64) == 512
+    s = bench.lengths_summary([16, 1000, 8192, 40])
+    assert s == {"min": 16, "median": 520.0, "max": 8192, "sum": 9248}
+
+
+def test_cpu_model_is_named(bench):
+    name = bench.cpu_model()
+    assert isinstance(name, str) and name

@@ -14,8 +14,7 @@ import paged_kv_cache_195_gb300 as pkv
 from paged_kv_cache_195_gb300 import build as pkv_build
 from paged_kv_cache_195_gb300 import workloads as wl
 
-from pkv_testutil import (assert_close, host_copy, oracle_full, oracle_pools_after_append,
-                          snapshot_oracle, snapshot_rows, to_f64)
+from pkv_testutil import (assert_close, host_copy, oracle_full, oracle_pools_after_append, to_f64)
 
 pytestmark = pytest.mark.gpu
 
@@ -120,16 +119,15 @@ def test_cascade_matches_plain_attention():
     assert float(diff.max()) <= 2e-2 and float(diff.mean()) <= 1e-3
 
 
-def test_cascade_qwen_shared_full_size_sampled():
+def test_cascade_qwen_shared_full_size_every_element():
     shape = wl.qwen_shared_prefix(layers=1)
     inp = wl.make_step(shape, device="cuda")
-    rows = [(r, 0) for r in (0, 5, 15, 16, 33, 47, 48, 63)]
-    snap = snapshot_rows(inp, rows)
+    h = host_copy(inp)
     out = _cascade(inp)
     torch.cuda.synchronize()
     assert pkv.pkv_get_device_error() == 0, pkv.pkv_last_error()
-    got = to_f64(out[torch.tensor(snap["qrows"], device="cuda")])
-    assert_close(got, snapshot_oracle(snap), "qwen_shared")
+    kp, vp = oracle_pools_after_append(h)
+    assert_close(to_f64(out), oracle_full(h, kp, vp), "qwen_shared")
 
 
 def test_cascade_bad_group_reported():

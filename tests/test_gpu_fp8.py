@@ -16,7 +16,7 @@ import paged_kv_cache_195_gb300 as pkv
 from paged_kv_cache_195_gb300 import build as pkv_build
 from paged_kv_cache_195_gb300 import workloads as wl
 
-from pkv_testutil import assert_close, pool_host, snapshot_oracle, snapshot_rows, to_f64
+from pkv_testutil import assert_close, pool_host, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -115,17 +115,17 @@ def test_fp8_every_group_size(g):
 
 
 @pytest.mark.parametrize("g", [4, 6, 8])
-def test_fp8_simt_decode_large_groups(g, monkeypatch):
+def test_fp8_simt_decode_large_groups(g, pkv_opts):
     # groups of 4 or more run on the tensor cores by default (tiles widened
     # to f16); the SIMT decode serves them too when asked
-    monkeypatch.setenv("PKV_DECODE_TC_FP8", "0")
+    pkv_opts(decode_tc_fp8=0)
     shape = wl.StepShape(f"fp8_simt_g{g}", [1, 31, 300, 129, 2000], [1, 1, 1, 3, 1], 2 * g, 2,
                          seed=190 + g)
     _full_parity(shape)
 
 
-def test_fp8_simt_decode_split_and_chunks(monkeypatch):
-    monkeypatch.setenv("PKV_DECODE_TC_FP8", "0")
+def test_fp8_simt_decode_split_and_chunks(pkv_opts):
+    pkv_opts(decode_tc_fp8=0)
     _full_parity(wl.StepShape("fp8_simt_long", [20000, 3000, 17], [1, 2, 1], 32, 8, seed=198),
                  poison=False)
     _full_parity(wl.StepShape("fp8_simt_chunks", [700, 64, 230, 5], [64, 64, 200, 1], 32, 8,
@@ -165,18 +165,22 @@ def test_fp8_relabelling_bit_identical():
     assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
 
 
-def test_fp8_qwen_decode_full_size_sampled():
-    shape = wl.qwen_decode()
-    inp = wl.make_fp8_step(shape, device="cuda", layer=3)
-    rng = np.random.default_rng(100)
-    rows = [(int(r), 0) for r in rng.choice(shape.num_reqs, 16, replace=False)]
-    snap = snapshot_rows(inp, rows)
+@pytest.mark.parametrize("factory,layer", [(wl.qwen_decode, 3), (wl.qwen_long_batch, 0)],
+                         ids=["qwen_decode", "qwen_long"])
+def test_fp8_full_size_every_element(factory, layer):
+    shape = factory()
+    inp = wl.make_fp8_step(shape, device="cuda", layer=layer)
+    h = _host(inp)
     out = _step(inp)
     torch.cuda.synchronize()
     assert pkv.pkv_get_device_error() == 0, pkv.pkv_last_error()
-    want = snapshot_oracle(snap)
-    got = to_f64(out[torch.tensor(snap["qrows"], device="cuda")])
-    assert_close(got, want, "fp8 qwen_decode")
+    got = to_f64(out)
+    del inp, out
+    kp, vp = oracle.append_fp8(h["k_new"], h["v_new"], h["slots"], h["k_pool"], h["v_pool"],
+                               h["k_scale"], h["v_scale"])
+    want = oracle.paged_attention_fp8(h["q"], kp, vp, h["k_scale"], h["v_scale"], h["bt"],
+                                      h["sl"], h["qsl"], h["scale"])
+    assert_close(got, want, f"fp8 {shape.name}")
 
 
 def test_fp8_bad_block_reported():

@@ -4,8 +4,6 @@ Small cases are compared element by element on every output; the full-size
 workloads (in the launch configuration the benchmark times) on sampled rows
 the oracle computes one by one, plus properties that hold at any size.
 """
-import math
-import os
 
 import numpy as np
 import pytest
@@ -134,16 +132,16 @@ def test_block_relabelling_is_bit_identical():
     assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
 
 
-def test_split_count_does_not_change_the_answer(monkeypatch):
+def test_split_count_does_not_change_the_answer(pkv_opts):
     """Online-softmax merging is exact: any split count gives the same result
     up to fp32 rounding (at most one bf16 ulp of the output).  This holds for
     the SIMT decode, whose probabilities stay in fp32."""
-    monkeypatch.setenv("PKV_DECODE_TC", "0")
+    pkv_opts(decode_tc=0)
     shape = wl.StepShape("splits", [3000, 1200, 17], [1, 3, 1], 32, 8, seed=5)
     inp = wl.make_step(shape, device="cuda")
     outs = []
-    for chunk in ("1", "3", "4096"):
-        monkeypatch.setenv("PKV_MIN_CHUNK", chunk)
+    for chunk in (1, 3, 4096):
+        pkv_opts(min_chunk=chunk)
         outs.append(gpu_step(inp, append=False).float().clone())
     ref = oracle_full(host_copy(inp))
     for o in outs:
@@ -152,18 +150,18 @@ def test_split_count_does_not_change_the_answer(monkeypatch):
         assert ((o - outs[-1]).abs() <= ulp + 1e-6).all()
 
 
-def test_split_count_tensor_core_decode(monkeypatch):
+def test_split_count_tensor_core_decode(pkv_opts):
     """The tensor-core decode feeds P to the MMA in bf16 (relative error at
     most 2^-9 per weight), and where a piece starts decides which 128-key
     tiles form; the merge itself is exact.  A softmax-weighted mean with every
     weight perturbed by at most 2^-9 moves by at most 2 * 2^-9 * max_j |v_j - o|,
     so two splits differ by at most twice that plus the output rounding."""
-    monkeypatch.setenv("PKV_DECODE_TC", "1")
+    pkv_opts(decode_tc=1)
     shape = wl.StepShape("splits_tc", [3000, 1200, 17], [1, 3, 1], 32, 8, seed=5)
     inp = wl.make_step(shape, device="cuda")
     outs = []
-    for chunk in ("1", "3", "4096"):
-        monkeypatch.setenv("PKV_MIN_CHUNK", chunk)
+    for chunk in (1, 3, 4096):
+        pkv_opts(min_chunk=chunk)
         outs.append(gpu_step(inp, append=False).float().clone())
     h = host_copy(inp)
     ref = oracle_full(h)
@@ -238,7 +236,8 @@ def test_inconsistent_lengths_are_reported():
 
 
 # ---------------------------------------------------------------------------
-# Full-size workloads: sampled rows against the oracle + size-free properties
+# Full-size workloads: every output element against the oracle (plus
+# determinism); the two stress shapes beyond them compare sampled rows
 # ---------------------------------------------------------------------------
 
 def _sample_rows(shape, n_rows, seed):
@@ -267,24 +266,39 @@ def _sampled(shape, n_rows, seed, layer=0, extra_rows=()):
     return assert_close(got, want, shape.name)
 
 
-def test_qwen_decode_full_size_layers():
-    shape = wl.qwen_decode()
-    for layer in (0, 27):
-        _sampled(shape, 24, 10 + layer, layer=layer)
+def _full_size(shape, layer=0):
+    """The whole step at full size: append + attention on the GPU, the
+    oracle's own append + attention on host copies taken before, compared on
+    every element (max and mean over the whole output); a second attention
+    call must give the same bits."""
+    inp = wl.make_step(shape, device="cuda", layer=layer)
+    h = host_copy(inp)
+    out = gpu_step(inp)
+    again = gpu_step(inp, append=False)
+    torch.cuda.synchronize()
+    assert pkv.pkv_get_device_error() == 0, pkv.pkv_last_error()
+    assert torch.equal(out.view(torch.int16), again.view(torch.int16)), "non-deterministic"
+    got = to_f64(out)
+    del inp, out, again
+    kp, vp = oracle_pools_after_append(h)
+    return assert_close(got, oracle_full(h, kp, vp), f"{shape.name} layer {layer}")
+
+
+@pytest.mark.parametrize("layer", [0, 27])
+def test_qwen_decode_full_size_layers(layer):
+    _full_size(wl.qwen_decode(), layer=layer)
 
 
 def test_qwen_long_batch_full_size():
-    _sampled(wl.qwen_long_batch(), 24, 11)
+    _full_size(wl.qwen_long_batch())
 
 
 def test_llama_mixed_full_size():
-    # sampled decode rows plus the first, middle and last rows of every prefill
-    rows = [(r, i) for r in range(248, 256) for i in (0, 255, 511)]
-    _sampled(wl.llama_mixed(), 20, 12, extra_rows=rows)
+    _full_size(wl.llama_mixed())
 
 
 def test_llama_long_context_full_size():
-    _sampled(wl.llama_long_context(), 8, 13)
+    _full_size(wl.llama_long_context())
 
 
 def test_maximum_request_count():
@@ -317,20 +331,20 @@ def _prefill_shape(g, seed, Hkv=2):
 
 
 @pytest.mark.parametrize("g", [1, 2, 3, 4, 5, 6, 7, 8])
-def test_prefill_tensor_core_path(g, monkeypatch):
-    monkeypatch.setenv("PKV_PREFILL_MIN_Q", "16")
+def test_prefill_tensor_core_path(g, pkv_opts):
+    pkv_opts(prefill_min_q=16)
     _full_parity(_prefill_shape(g, 700 + g), poison=True)
 
 
 @pytest.mark.parametrize("route", ["decode_only", "prefill_from_2"])
-def test_both_routes_agree_with_oracle(route, monkeypatch):
-    monkeypatch.setenv("PKV_PREFILL_MIN_Q", "0" if route == "decode_only" else "2")
+def test_both_routes_agree_with_oracle(route, pkv_opts):
+    pkv_opts(prefill_min_q=0 if route == "decode_only" else 2)
     shape = wl.StepShape("mix", [300, 40, 517, 129, 16], [1, 40, 200, 3, 16], 32, 8, seed=41)
     _full_parity(shape, poison=True)
 
 
-def test_prefill_long_prefix_many_key_tiles(monkeypatch):
-    monkeypatch.setenv("PKV_PREFILL_MIN_Q", "16")
+def test_prefill_long_prefix_many_key_tiles(pkv_opts):
+    pkv_opts(prefill_min_q=16)
     shape = wl.StepShape("longprefix", [4096 + 512, 1000 + 64], [512, 64], 32, 8, seed=42)
     rows = [(0, i) for i in (0, 1, 31, 32, 255, 511)] + [(1, i) for i in (0, 63)]
     inp = wl.make_step(shape, device="cuda", poison=True)
@@ -435,7 +449,7 @@ def test_plan_request_counts(R, g):
     _full_parity(shape)
 
 
-def test_plan_cache_follows_lengths(monkeypatch):
+def test_plan_cache_follows_lengths(pkv_opts):
     # One workspace across calls whose lengths change and come back: the
     # cached per-CTA plans are reused only for identical lengths, so every
     # call matches the oracle, and equals a call with caching switched off.
@@ -464,10 +478,10 @@ def test_plan_cache_follows_lengths(monkeypatch):
         for _ in range(2):  # the second call reuses the plans of the first
             outs.append(pkv.pkv_attention(inp.q, inp.k_pool, inp.v_pool, bt, inp.seq_lens,
                                           inp.query_start_loc, inp.scale, workspace=ws))
-        monkeypatch.setenv("PKV_PLAN_CACHE", "0")
+        pkv_opts(plan_cache=0)
         outs.append(pkv.pkv_attention(inp.q, inp.k_pool, inp.v_pool, bt, inp.seq_lens,
                                       inp.query_start_loc, inp.scale, workspace=ws))
-        monkeypatch.delenv("PKV_PLAN_CACHE")
+        pkv_opts(plan_cache=1)
         torch.cuda.synchronize()
         assert pkv.pkv_get_device_error() == 0, pkv.pkv_last_error()
         assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])

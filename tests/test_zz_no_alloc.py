@@ -1,9 +1,9 @@
 """pkv_attention_noalloc: attention for callers that cannot allocate.
 
-Callers that may not call cudaMalloc (graph capture in global mode, plugins
-whose host owns all device memory, loops that forbid allocation after
-start-up) use this entry point; its scratch is a fixed array inside the
-library.  Its output must match the regular entry point's, call after call,
+Callers that may not call cudaMalloc (plugins whose host framework owns all
+device memory, serving loops that forbid allocation after start-up) use this
+entry point; its scratch is a fixed array inside the library.  Its output
+must match the regular entry point's and the fp64 oracle's, call after call,
 even when the dims (and so the scratch layout) change between calls.
 
 This file is collected last on purpose: if it fails, a run that stops at the
@@ -17,7 +17,8 @@ import paged_kv_cache_195_gb300 as pkv
 from paged_kv_cache_195_gb300 import build as pkv_build
 from paged_kv_cache_195_gb300 import workloads as wl
 
-from pkv_testutil import MAX_ABS, MEAN_ABS
+from pkv_testutil import (MAX_ABS, MEAN_ABS, assert_close, host_copy, oracle_full,
+                          oracle_pools_after_append, to_f64)
 
 pytestmark = pytest.mark.gpu
 
@@ -32,6 +33,8 @@ def _built():
 
 def _both(shape):
     inp = wl.make_step(shape, device="cuda", poison=True)
+    h = host_copy(inp)
+    kp, vp = oracle_pools_after_append(h)
     pkv.pkv_append(inp.k_new, inp.v_new, inp.slot_mapping, inp.k_pool, inp.v_pool)
     ref = pkv.pkv_attention(inp.q, inp.k_pool, inp.v_pool, inp.block_tables, inp.seq_lens,
                             inp.query_start_loc, inp.scale)
@@ -44,6 +47,8 @@ def _both(shape):
     assert np.isfinite(got).all()
     err = np.abs(got - want)
     assert err.max() <= MAX_ABS and err.mean() <= MEAN_ABS, (err.max(), err.mean())
+    # and against the fp64 oracle on the same inputs (its own append)
+    assert_close(to_f64(out), oracle_full(h, kp, vp), shape.name)
 
 
 def test_noalloc_matches_pkv_attention_on_consecutive_calls():
