@@ -229,7 +229,9 @@ def workload_config(shape, ws_n, kv="bf16"):
         "l2": f"inputs exceed L2: {shape.layers} distinct pools, "
               f"{2 * shape.layers * shape.num_blocks * shape.num_kv_heads * 2048 * kvb / 1e9:.2f}"
               " GB per step",
-        "launch": f"CUDA graph of {shape.layers} x (append + attention)",
+        "launch": f"CUDA graph of {shape.layers} x (append + attention)"
+                  + ("" if kv == "fp8" or shape.prefix_groups else
+                     ", pkv_append_attention with early_trigger"),
         **({"shared_prefix": [{"first_request": int(f), "members": int(m), "blocks": int(b)}
                               for f, m, b in shape.prefix_groups],
             "attention_call": "pkv_attention_cascade"} if shape.prefix_groups else {}),
@@ -267,6 +269,11 @@ class ConfigRun:
 
     def __init__(self, pkv, shape, kv, device, rank, with_e2e):
         self.pkv, self.shape, self.kv, self.device = pkv, shape, kv, device
+        # The step's pkv_append_attention calls let the attention launch as
+        # soon as the append starts (its documented precondition holds: the
+        # kernel before each call is the previous layer's attention, which
+        # writes neither the tables, the lengths nor this layer's pool).
+        pkv.set_options(early_trigger=1)
         self.fp8 = kv == "fp8"
         self.kvb = 1 if self.fp8 else 2
         # single-layer workloads: two copies of the layer alternate in the

@@ -124,7 +124,7 @@ int env_int(const char* name, int dflt) {
 
 bool options_valid(const pkv_options& o) {
   return o.prefill_min_q >= 0 && o.align_slack >= 0 && o.min_chunk >= 1 && o.decode_grid >= 0 &&
-         o.wait_limit_us >= 1;
+         o.warm_kv >= 0 && o.warm_kv <= 2 && o.wait_limit_us >= 1;
 }
 
 pkv_options options_from_env() {
@@ -142,6 +142,7 @@ pkv_options options_from_env() {
   o.min_chunk = env_int("PKV_MIN_CHUNK", 4);
   o.prefetch = env_int("PKV_PREFETCH", 1);
   o.decode_grid = env_int("PKV_DECODE_GRID", 0);
+  o.warm_kv = env_int("PKV_WARM_KV", 0);
   o.wait_limit_us = env_int("PKV_WAIT_LIMIT_US", (int)(pkv::kDefaultWaitLimitNs / 1000));
   o.debug_withhold_q = 0;  // never from the environment
   // Out-of-range values from the environment fall back to the defaults.
@@ -149,6 +150,7 @@ pkv_options options_from_env() {
   if (o.align_slack < 0) o.align_slack = 64;
   if (o.min_chunk < 1) o.min_chunk = 4;
   if (o.decode_grid < 0) o.decode_grid = 0;
+  if (o.warm_kv < 0 || o.warm_kv > 2) o.warm_kv = 0;
   if (o.wait_limit_us < 1) o.wait_limit_us = (int)(pkv::kDefaultWaitLimitNs / 1000);
   return o;
 }
@@ -513,6 +515,7 @@ int attention_impl(const void* q, const void* k_pool, const void* v_pool, const 
   p.align_slack = opt.align_slack;
   p.prefetch = opt.prefetch != 0;
   p.early_plan = p.pdl && opt.early_plan != 0;
+  p.warm_kv = opt.warm_kv;
   p.wait_limit_ns = (unsigned long long)opt.wait_limit_us * 1000ull;
   p.debug_withhold_q = opt.debug_withhold_q != 0;
   const int group = dims->num_q_heads / dims->num_kv_heads;
@@ -598,7 +601,21 @@ int attention_impl(const void* q, const void* k_pool, const void* v_pool, const 
                                : encode_pool_map(&T.vmap, v_pool, dims);
     if (rc != PKV_OK) return rc;
     T.p = p;
-    T.grid = st->sm_count;
+    // Two CTAs per SM; steps with at most 8 tiles (64 blocks) per SM run on
+    // one CTA per SM, so that the next launch's CTAs can prepare beside them.
+    // When the dims alone bound the work that low (every decode row reads at
+    // most max_blocks_per_req blocks per KV head) the grid is one CTA per SM;
+    // otherwise the plan makes the choice on the device from the lengths.
+    constexpr long long kHalfGridBlocks = 64;
+    const long long bound = (long long)dims->num_q_tokens * dims->max_blocks_per_req * dims->num_kv_heads;
+    const bool small = bound <= kHalfGridBlocks * st->sm_count;
+    T.grid = small ? st->sm_count : 2 * st->sm_count;
+    T.p.half_grid_blocks = small ? 0 : (int)kHalfGridBlocks;
+    // tuning override, bounded by the workspace's slots
+    if (opt.decode_grid > 0 && 2 * opt.decode_grid <= w.num_slots) {
+      T.grid = opt.decode_grid;
+      T.p.half_grid_blocks = 0;
+    }
     e = pkv::launch_decode_tc(T, group, stream);
   } else {
     e = pkv::launch_decode(p, group, grid, stream);

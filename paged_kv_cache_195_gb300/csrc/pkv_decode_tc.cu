@@ -29,14 +29,25 @@
 // both accumulating in fp32 in TMEM.  Thread t of the four softmax warps owns
 // TMEM lane t: key t of S^T, dim t of O^T.
 //
-// Roles (320 threads): warps 0-3 softmax, warp 4 plan and TMA producer (it
-// plans before the CTA's set-up, and K/V tiles are evict-first in L2: each is
-// read once), one thread of warp 5 issues the MMAs, warps 6-9 the epilogue
-// (normalise, write the output or a partial piece, merge, fold a shared
-// prefix's states).  e4m3 pools add warps 10-11 (384 threads), which widen
-// each tile's codes to f16 in shared memory; Q and P are then f16 too.  S, P and O^T are double buffered:
-// the softmax moves on to the next piece while the epilogue finishes the
-// previous one, so piece boundaries do not stall the K/V stream.
+// Two CTAs per SM.  A CTA takes 111 KB of shared memory and 192 threads, so
+// the next launch's CTAs (the next layer of an engine step) become resident
+// beside this launch's as soon as it lets them launch: they plan, allocate
+// TMEM and warm L2 with their first K/V blocks while this launch streams,
+// and start copying the moment it completes.  K and V tiles share one ring
+// of three 32 KiB slots (K of tile t, then V of tile t), a K slot freed as
+// soon as its S^T is computed, a V slot when its PV is.  Optionally
+// (warm_kv) the producer also warms L2 with the K/V blocks of its first eight
+// tiles before the wait (prefetches: hints, with no effect on results).
+//
+// Roles (192 threads): warps 0-3 run the softmax and, at the end of each
+// piece, its epilogue (normalise, write the output or a partial piece, merge,
+// fold a shared prefix's states); warp 4 plans, warms L2 and issues the TMA
+// copies (it plans before the CTA's set-up, and K/V tiles are evict-first in
+// L2: each is read once); one thread of warp 5 issues the MMAs.  e4m3 pools
+// add warps 6-7 (256 threads), which widen each slot's codes to f16 in
+// shared memory; Q and P are then f16 too.  S and O^T are double buffered in
+// TMEM, so the MMAs of the next piece proceed while the softmax warps finish
+// the previous one.
 // The running maximum is raised only when a score exceeds it by more than
 // 2^8 (a CTA-wide vote), so the common tile needs no cross-thread reduction;
 // O^T is rescaled in TMEM on the rare raise.
@@ -52,31 +63,33 @@ namespace {
 using plan::Piece;
 using plan::kEndRow;
 
-constexpr int kTcThreads = 320;
-// e4m3 pools: two more warps (10, 11) widen each K / V tile to f16 in
-// shared memory before the tensor core reads it (one hardware conversion per
-// pair of codes); Q and P are then f16 as well, since both operands of a
-// kind::f16 MMA must have the same type.
-constexpr int kTcThreadsF8 = 384;
+constexpr int kTcWarps = 6;                 // 0-3 softmax + epilogue, 4 producer, 5 MMA
+constexpr int kTcThreads = 32 * kTcWarps;
+// e4m3 pools: two more warps (6, 7) widen each slot's codes to f16 in shared
+// memory before the tensor core reads them (one hardware conversion per pair
+// of codes); Q and P are then f16 as well, since both operands of a kind::f16
+// MMA must have the same type.
 constexpr int kConvWarps = 2;
+constexpr int kTcThreadsF8 = kTcThreads + 32 * kConvWarps;
 constexpr int kRawTile = 128 * kHeadDim;   // one 128-key tile of e4m3 codes (bytes)
 constexpr int kTile = 128;                 // keys per tile (MMA M of S^T, K of PV)
 constexpr int kBlkPerTile = kTile / kBlockSize;
 constexpr int kN = 16;                     // MMA N: the group's heads, padded
 constexpr int kHalf = kTile * 128;         // one 64-dim half of a 128-key bf16 tile
 constexpr int kOpHalf = kN * 128;          // one 64-element half of a 16-row operand
-constexpr int kStages = 3;                 // K/V tile stages (64 KiB each)
+constexpr int kSlots = 3;                  // ring slots (32 KiB): K or V of one tile
 constexpr uint32_t kTmemCols = 64;         // S0: 0..15, S1: 16..31, O0: 32..47, O1: 48..63
 constexpr uint32_t kColO = 32;             // O^T of piece j in columns kColO + (j & 1) * kN
 constexpr float kNegBig = -1.0e30f;
 constexpr float kLazyMargin = 8.f;         // log2 of the largest probability allowed
 constexpr int kBarSoftmax = 1;             // named barrier of the four softmax warps
-constexpr int kBarEpi = 2;                 // named barrier of the four epilogue warps
+constexpr int kSoftThreads = 128;
 constexpr int kPastPiece = INT_MIN;        // block-table slot past the piece (not read)
+constexpr int kWindow = 32;                // block-table entries loaded at a time (4 tiles)
 
 // Debug-only per-tile timeline of CTA 0 (build with -DPKV_TC_TRACE=1):
 // %globaltimer at load issue, keys seen by the MMA warp, scores seen by the
-// softmax, PV issue, and stage release seen by the producer.
+// softmax, PV issue, and slot release seen by the producer.
 #ifndef PKV_TC_TRACE
 #define PKV_TC_TRACE 0
 #endif
@@ -92,8 +105,8 @@ __device__ unsigned long long g_tc_trace[7][kTrTiles];
 // set-up done, 2 producer ready, 3 first load issued, 4 first keys seen by the
 // MMA warp, 5 last PV issued, 6 last piece written, 7 exit, 8 SM id + 1, 9
 // grid-dependency wait taken (early_kv), 10 plan done, 11 first pieces
-// known, 14 softmax statistics published, 15 seen by the epilogue, 16 O read
-// from TMEM, 17 last O commit issued.
+// known, 12 first blocks warmed in L2, 16 O read from TMEM, 17 last O commit
+// issued.
 #if PKV_TC_TRACE >= 3
 // Slots by the out pointer, so that consecutive launches keep their own.
 constexpr int kTrCtas = 256, kTrSlots = 32;
@@ -106,27 +119,28 @@ __device__ unsigned long long g_tc_cta[kTrSlots][kTrCtas][18];
 #endif
 
 struct __align__(1024) TcSmem {
-  uint8_t k[kStages][2][kHalf];   // [stage][d half]: 128 keys x 64 d, swizzled
-  uint8_t v[kStages][2][kHalf];
+  // Ring occupant n (n = 0, 1, 2, ...) lives in slot n % kSlots: the K tile of
+  // tile n / 2 when n is even, its V tile when n is odd; [d half] 128 keys x
+  // 64 d, 128-byte swizzled.
+  uint8_t slot[kSlots][2][kHalf];
   uint8_t q[2][2][kOpHalf];       // [piece buffer][d half]: Q rows (heads), rows >= g zero
-  uint8_t pt[2][2][kOpHalf];      // [buffer][key half]: P^T as 16 rows (heads) x 64 keys
+  uint8_t pt[2][kOpHalf];         // [key half]: P^T as 16 rows (heads) x 64 keys
   float red[4][kN];               // per-warp partial maxima (softmax warps)
-  float st_l[2][4][kN];           // [piece buffer][softmax warp]: normaliser partial sums
-  float st_m[2][kN];              // [piece buffer]: running maxima (log2 domain)
-  Piece st_pc[2];                 // [piece buffer]: the piece, for the epilogue
+  float st_l[4][kN];              // per-warp normaliser partial sums (epilogue)
   Piece pinfo[2];
   uint64_t q_full[2], q_empty[2];
-  uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
-  uint64_t kraw_full[kStages], vraw_full[kStages];  // e4m3 codes landed (e4m3 pools)
+  uint64_t full[kSlots], empty[kSlots];  // occupant landed (bf16) or widened (e4m3) / released
+  uint64_t raw_full[kSlots];      // e4m3 pools: the occupant's codes landed
   uint64_t q_conv[2];             // e4m3 pools: Q buffer converted to f16 by the softmax warps
-  uint64_t s_full[2], s_free[2], p_full[2], p_free[2];
+  uint64_t s_full[2], s_free[2];  // S^T buffer computed / read by the softmax
+  uint64_t p_full, p_free;        // P^T written by the softmax / read by the PV
   uint64_t o_full[2], o_empty[2];  // O^T buffer complete / read by the epilogue
-  uint64_t st_full[2], st_empty[2];  // piece statistics published / consumed
   uint64_t mma_done;              // an aborted CTA's last tcgen05.commit
   uint32_t tmem_base;
   WaitCtl wait;                   // abort flag and wait limit of the bounded waits
   int is_last;
-  int conv_end;                   // e4m3 pools: tiles issued in all (set at the end)
+  int idle;                       // the plan gave this CTA no work
+  int conv_end;                   // e4m3 pools: ring occupants issued in all (set at the end)
 };
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -175,11 +189,11 @@ __device__ __forceinline__ void widen_e4m3_row(uint8_t* half0, uint8_t* half1, i
   }
 }
 
-// F8: the pools hold e4m3 codes (kmap / vmap are maps of bytes); each tile is
-// widened to bf16 in shared memory, the key scale joins the softmax scale and
+// F8: the pools hold e4m3 codes (kmap / vmap are maps of bytes); each slot is
+// widened to f16 in shared memory, the key scale joins the softmax scale and
 // the value scale multiplies the output.
 template <int G, bool F8>
-__global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 1)
+__global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 2)
     decode_tc_kernel(const __grid_constant__ CUtensorMap qmap,
                      const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
@@ -208,32 +222,75 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 1)
   plan::Walker wk;
   Piece pc, pn;
   bool have = false, have_n = false;
-  int ent_first = kPastPiece, ent_first_n = kPastPiece;
-  // Block-table entries are loaded 32 blocks (four tiles) at a time and
-  // well before use -- the next group while a group is issued, the next
-  // piece's first group while a piece is issued -- and checked only when
-  // used, so the producer never waits on the table.
+  // Block-table entries, 32 blocks (four tiles, one "window") per load and
+  // one per lane: the current piece's first two windows (w0, w1) and the next
+  // piece's (n0, n1), loaded a piece ahead and checked only when used, so the
+  // producer never waits on the table.
+  int ent_w0 = kPastPiece, ent_w1 = kPastPiece, ent_n0 = kPastPiece, ent_n1 = kPastPiece;
   auto raw_entries = [&](const Piece& q, int x0) {
     const int x = x0 + lane;
     return x < q.nblk ? __ldg(p.block_tables + (long long)q.r * p.max_blocks + q.b0 + x)
                       : kPastPiece;
+  };
+  // Warms L2 with one window's K and V blocks of KV head kh (lane = block),
+  // before this kernel may read the pools (the prefetches are hints: L2 stays
+  // coherent with any write of the kernel before).  warm_kv 1: one bulk
+  // prefetch per block and tensor; 2: one prefetch instruction per 128-byte
+  // line, through the load path rather than the copy engine.  Blocks past the
+  // piece and ids outside the pool are skipped.
+  constexpr uint32_t kBlkBytes = F8 ? kBlockSize * kHeadDim : kBlockSize * kHeadDim * 2;
+  auto warm = [&](int ent, int kh) {
+    if (p.warm_kv && (unsigned)ent < (unsigned)p.num_blocks && kh >= 0 && kh < Hkv) {
+      const long long off = ((long long)ent * Hkv + kh) * kBlkBytes;
+      if (p.warm_kv == 1) {
+        prefetch_l2_bulk(p.k_pool + off, kBlkBytes);
+        prefetch_l2_bulk(p.v_pool + off, kBlkBytes);
+      } else {
+        #pragma unroll 4
+        for (uint32_t b = 0; b < kBlkBytes; b += 128) {
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(p.k_pool + off + b));
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(p.v_pool + off + b));
+        }
+      }
+    }
   };
   auto plan_first = [&]() {
     if (p.prefetch) plan::prefetch_block_table(p, lane);
     plan::plan_cta(p, lane, rg, wk);
     if (lane == 0) TC_CTA(10);
     have = wk.next(p, pc);
-    if (early_plan && have) ent_first = raw_entries(pc, 0);  // in flight during next()
+    if (have) ent_w0 = raw_entries(pc, 0);  // in flight during next()
+    if (have && pc.nblk > kWindow) ent_w1 = raw_entries(pc, kWindow);
     have_n = have && wk.next(p, pn);
+    if (have_n) ent_n0 = raw_entries(pn, 0);
+    if (have_n && pn.nblk > kWindow) ent_n1 = raw_entries(pn, kWindow);
     if (lane == 0) TC_CTA(11);
   };
-  auto first_entries = [&]() {
-    if (!early_plan && have) ent_first = raw_entries(pc, 0);
-    if (have_n) ent_first_n = raw_entries(pn, 0);
+  // The first eight tiles' blocks into L2: the first piece's two windows, or
+  // its window and the next piece's.
+  auto warm_first = [&]() {
+    if (!have) return;
+    warm(ent_w0, pc.k);
+    if (pc.nblk > kWindow) warm(ent_w1, pc.k);
+    else if (have_n) warm(ent_n0, pn.k);
+    if (lane == 0) TC_CTA(12);
   };
   if (warp == 4 && early_plan) {
     plan_first();
-    first_entries();
+    warm_first();
+    // The entries must be in registers before the wait below: a volatile
+    // use keeps the compiler from sinking their loads past it.
+    asm volatile("" ::"r"(ent_w0), "r"(ent_w1), "r"(ent_n0), "r"(ent_n1));
+  }
+  // A CTA the plan gives no work leaves at once (after the launch wait, so
+  // that this grid never completes before the kernel ahead of it): its SM
+  // slot goes to the next launch.
+  if (warp == 4 && lane == 0) sm.idle = early_plan && !have;
+  __syncthreads();
+  if (sm.idle) {
+    grid_dependency_wait();
+    allow_dependent_launch();
+    return;
   }
 
   if (tid == 0) {
@@ -242,23 +299,17 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 1)
       mbar_init(&sm.q_empty[b], 1);   // tcgen05.commit after the piece's last MMA
       mbar_init(&sm.s_full[b], 1);    // tcgen05.commit after S^T = K Q^T into buffer b
       mbar_init(&sm.s_free[b], 4);    // the softmax warps have read S buffer b
-      mbar_init(&sm.p_full[b], 4);    // P^T buffer b written by the softmax warps
-      mbar_init(&sm.p_free[b], 1);    // tcgen05.commit after the PV that read P^T buffer b
-    }
-    for (int s = 0; s < kStages; ++s) {
-      // bf16 tiles: the TMA transaction count; e4m3: the converter warps
-      mbar_init(&sm.k_full[s], F8 ? kConvWarps : 1);
-      mbar_init(&sm.v_full[s], F8 ? kConvWarps : 1);
-      mbar_init(&sm.kv_empty[s], 1);
-      mbar_init(&sm.kraw_full[s], 1);
-      mbar_init(&sm.vraw_full[s], 1);
-    }
-    for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.q_conv[b], 4);    // e4m3 pools: Q buffer b converted by the softmax warps
       mbar_init(&sm.o_full[b], 1);    // tcgen05.commit after the piece's last PV
-      mbar_init(&sm.o_empty[b], 4);   // the epilogue warps have read O^T buffer b
-      mbar_init(&sm.st_full[b], 4);   // the softmax warps have published the statistics
-      mbar_init(&sm.st_empty[b], 4);  // the epilogue warps have read them
+      mbar_init(&sm.o_empty[b], 4);   // the epilogue (softmax warps) has read O^T buffer b
+    }
+    mbar_init(&sm.p_full, 4);         // P^T written by the softmax warps
+    mbar_init(&sm.p_free, 1);         // tcgen05.commit after the PV that read P^T
+    for (int s = 0; s < kSlots; ++s) {
+      // bf16: the TMA transaction count; e4m3: the converter warps
+      mbar_init(&sm.full[s], F8 ? kConvWarps : 1);
+      mbar_init(&sm.empty[s], 1);     // tcgen05.commit after the MMAs that read the slot
+      mbar_init(&sm.raw_full[s], 1);
     }
     mbar_init(&sm.mma_done, 1);
     sm.wait.abort = 0;
@@ -269,7 +320,7 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 1)
   // Operand rows g..15 (padding heads) stay zero for the whole kernel.
   for (int i = tid; i < (int)(sizeof(sm.q) + sizeof(sm.pt)) / 16; i += kThreads) {
     uint8_t* base = i < (int)sizeof(sm.q) / 16 ? &sm.q[0][0][0] + i * 16
-                                               : &sm.pt[0][0][0] + (i - (int)sizeof(sm.q) / 16) * 16;
+                                               : &sm.pt[0][0] + (i - (int)sizeof(sm.q) / 16) * 16;
     *reinterpret_cast<uint4*>(base) = make_uint4(0, 0, 0, 0);
   }
   fence_proxy_async_smem();
@@ -288,10 +339,11 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 1)
   const uint32_t tmem = sm.tmem_base;
   if (tid == 0) TC_CTA(1);
   // Consumers wait for the previous kernel on the stream here; the producer
-  // builds its plan and loads its first block-table entries first (it reads
-  // only seq_lens, query_start_loc and block_tables, which with early_plan
-  // set the previous kernel does not write).  Each thread lets the next
-  // kernel launch only after its own wait.
+  // builds its plan, loads its first block-table entries and warms L2 with
+  // the first tiles first (it reads only seq_lens, query_start_loc and
+  // block_tables, which with early_plan set the previous kernel does not
+  // write; the L2 prefetches are hints).  Each thread lets the next kernel
+  // launch only after its own wait.
   //
   // With early_kv the previous kernel is the append of this step's new
   // tokens: before the wait this kernel reads the lengths, the block table
@@ -307,14 +359,13 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 1)
   }
 
   if (warp == 4) {
-    // ========================= plan + TMA producer ========================
+    // ===================== plan + L2 warming + TMA producer ==================
     bool waited = !p.early_kv;
     if (!early_plan) plan_first();  // after the wait above
     if (p.early_plan && !p.early_kv) {
       grid_dependency_wait();
       allow_dependent_launch();
     }
-    if (!early_plan) first_entries();
     if (lane == 0) TC_CTA(2);
     const int oob_row = p.num_blocks * Hkv * kBlockSize;  // zero-filled by TMA
     // Every K/V tile is read once per call: evict it from L2 first, so that
@@ -328,9 +379,8 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 1)
     int q_armed[2] = {0, 0};
     bool q_copy[2] = {false, false};
     auto issue_q = [&](int ub, int row, int kh) {
-      // Testing only: the first piece's q is never loaded, so the waits on
-      // it run out and the CTA takes the timeout path.
-      // (Piece 0 is buffer 0's first phase.)
+      // Testing only: the first piece's q (buffer 0's first phase) is never
+      // loaded, so the waits on it run out and the CTA takes the timeout path.
       if (p.debug_withhold_q && ub == 0 && q_armed[0] == 1) return;
       q_copy[ub] = true;
       if (lane == 0) {
@@ -350,61 +400,59 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 1)
       q_pend = 0;
     };
     int j = 0, t = 0;  // piece and tile counters
-    int n_issued = 0;  // tiles whose copies have been issued
+    int n_occ = 0;     // ring occupants whose copies have been issued
     bool ok = true;
     while (ok && have && !abort_flag->abort) {
       const int k = pc.k;
       const int ntile = plan::cdiv(pc.nblk, kBlkPerTile);
-      int ent_cur = ent_first;
-      int ent_nxt = ntile > 4 ? raw_entries(pc, 32) : kPastPiece;
+      int ent_cur = ent_w0, ent_nxt = ent_w1;
+      int ent_nn = ntile > 8 ? raw_entries(pc, 2 * kWindow) : kPastPiece;
       for (int tt = 0; tt < ntile; ++tt, ++t) {
         if (tt > 0 && (tt & 3) == 0) {
+          // next window; the one after it was loaded a window ago: warm it
           ent_cur = ent_nxt;
-          if (tt + 4 < ntile) ent_nxt = raw_entries(pc, (tt + 4) * kBlkPerTile);
+          ent_nxt = ent_nn;
+          ent_nn = tt + 8 < ntile ? raw_entries(pc, (tt + 8) * kBlkPerTile) : kPastPiece;
         }
-        const int st = t % kStages;
         // Before blocking on the consumers, or before a tile with a new token.
-        if (t >= kStages || pc.b0 + min(pc.nblk, (tt + 1) * kBlkPerTile) - 1 >= pc.fresh) {
+        if (2 * t + 1 >= kSlots || pc.b0 + min(pc.nblk, (tt + 1) * kBlkPerTile) - 1 >= pc.fresh) {
           if (!waited || q_pend) take_wait();
         }
-        if (t >= kStages &&
-            !mbar_wait(&sm.kv_empty[st], ((t / kStages) - 1) & 1, p.err, abort_flag)) {
-          ok = false;
-          break;
-        }
-        if (lane == 0 && t >= kStages) TC_TR(4, t - kStages);
-        if (lane == 0) TC_TR(0, t);
-        if (lane == 0 && t == 0) TC_CTA(3);
-        if (lane == 0) {
-          if (F8) {
-            mbar_arrive_expect_tx(&sm.kraw_full[st], (uint32_t)kRawTile);
-            mbar_arrive_expect_tx(&sm.vraw_full[st], (uint32_t)kRawTile);
-          } else {
-            mbar_arrive_expect_tx(&sm.k_full[st], 2u * kHalf);
-            mbar_arrive_expect_tx(&sm.v_full[st], 2u * kHalf);
-          }
-        }
-        __syncwarp();
-        // bf16: lanes 0..15 each copy one (block, d half) of K and of V.
-        // e4m3: lanes 0..7 each copy one block's 16 rows of 128 codes into
-        // the stage's second half, where the converter warps widen them.
-        // Blocks past the piece are read at an out-of-range row (zero fill).
+        // bf16: lanes 0..15 each copy one (block, d half) of the tile's K or V.
+        // e4m3: lanes 0..7 each copy one block's 16 rows of 128 codes into the
+        // slot's second half, where the converter warps widen them.  Blocks
+        // past the piece are read at an out-of-range row (zero fill).
         const int bsel = lane & 7, hsel = (lane >> 3) & 1;
         const int phys = __shfl_sync(0xffffffffu, ent_cur, (tt & 3) * kBlkPerTile + bsel);
-        if (lane < (F8 ? 8 : 16)) {
-          int row = oob_row;
-          if ((unsigned)phys < (unsigned)p.num_blocks) row = (phys * Hkv + k) * kBlockSize;
-          else if (phys != kPastPiece && hsel == 0) record_error(p.err, kErrBounds);
-          if (F8) {
-            tma_load_2d(sm.k[st][1] + bsel * 2048, &kmap, 0, row, &sm.kraw_full[st], pol);
-            tma_load_2d(sm.v[st][1] + bsel * 2048, &vmap, 0, row, &sm.vraw_full[st], pol);
-          } else {
-            tma_load_2d(sm.k[st][hsel] + bsel * 2048, &kmap, hsel * 64, row, &sm.k_full[st], pol);
-            tma_load_2d(sm.v[st][hsel] + bsel * 2048, &vmap, hsel * 64, row, &sm.v_full[st], pol);
+        int row = oob_row;
+        if ((unsigned)phys < (unsigned)p.num_blocks) row = (phys * Hkv + k) * kBlockSize;
+        else if (phys != kPastPiece && hsel == 0 && lane < 16) record_error(p.err, kErrBounds);
+        #pragma unroll 1
+        for (int kv = 0; kv < 2 && ok; ++kv) {
+          const int n = 2 * t + kv;  // ring occupant: K (kv = 0) or V (kv = 1) of tile t
+          const int s = n % kSlots;
+          if (n >= kSlots && !mbar_wait(&sm.empty[s], ((n / kSlots) - 1) & 1, p.err, abort_flag)) {
+            ok = false;
+            break;
           }
+          if (lane == 0 && kv == 0 && t >= 2) TC_TR(4, t - 2);
+          if (lane == 0 && kv == 0) TC_TR(0, t);
+          if (lane == 0 && t == 0 && kv == 0) TC_CTA(3);
+          if (lane == 0) {
+            if (F8) mbar_arrive_expect_tx(&sm.raw_full[s], (uint32_t)kRawTile);
+            else mbar_arrive_expect_tx(&sm.full[s], 2u * kHalf);
+          }
+          __syncwarp();
+          const CUtensorMap* map = kv == 0 ? &kmap : &vmap;
+          if (F8) {
+            if (lane < 8) tma_load_2d(sm.slot[s][1] + bsel * 2048, map, 0, row, &sm.raw_full[s], pol);
+          } else if (lane < 16) {
+            tma_load_2d(sm.slot[s][hsel] + bsel * 2048, map, hsel * 64, row, &sm.full[s], pol);
+          }
+          __syncwarp();
+          n_occ = n + 1;
         }
-        __syncwarp();
-        n_issued = t + 1;
+        if (!ok) break;
         if (tt == 0) {
           // Q of this piece, once the MMAs of piece j-2 are done with its
           // buffer (the piece's first K/V tile is already on its way).
@@ -455,22 +503,26 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 1)
       ++j;
       pc = pn;
       have = have_n;
-      ent_first = ent_first_n;
+      ent_w0 = ent_n0;
+      ent_w1 = ent_n1;
       have_n = have && wk.next(p, pn);
-      ent_first_n = have_n ? raw_entries(pn, 0) : kPastPiece;
+      ent_n0 = have_n ? raw_entries(pn, 0) : kPastPiece;
+      ent_n1 = have_n && pn.nblk > kWindow ? raw_entries(pn, kWindow) : kPastPiece;
     }
     // The CTA finishes after the previous kernel in any case; Q copies still
     // pending are issued unless the CTA is giving up.
     if (abort_flag->abort) q_pend = 0;
     take_wait();
     if (F8 && ok && !abort_flag->abort) {
-      // Tell the converter warps that tile t does not exist: completing the
-      // phase they wait on for it, once its stage's previous tile is done.
-      const int st = t % kStages;
-      if (t < kStages || mbar_wait(&sm.kv_empty[st], ((t / kStages) - 1) & 1, p.err, abort_flag)) {
+      // Tell the converter warps that occupant n_occ does not exist:
+      // completing the phase they wait on for it, once its slot's previous
+      // occupant is done.
+      const int s = n_occ % kSlots;
+      if (n_occ < kSlots ||
+          mbar_wait(&sm.empty[s], ((n_occ / kSlots) - 1) & 1, p.err, abort_flag)) {
         if (lane == 0) {
-          *reinterpret_cast<volatile int*>(&sm.conv_end) = t;
-          mbar_arrive(&sm.kraw_full[st]);
+          *reinterpret_cast<volatile int*>(&sm.conv_end) = n_occ;
+          mbar_arrive(&sm.raw_full[s]);
         }
       }
       __syncwarp();
@@ -489,12 +541,10 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 1)
     }
     if (abort_flag->abort) {
       // Copies still in flight must land before the CTA's shared memory is
-      // released: the last tile of each stage and the last Q of each buffer.
-      for (int tp = max(0, n_issued - kStages); tp < n_issued; ++tp) {
-        const int st = tp % kStages;
-        const uint32_t par = (tp / kStages) & 1;
-        mbar_wait_drain(F8 ? &sm.kraw_full[st] : &sm.k_full[st], par, p.err, abort_flag);
-        mbar_wait_drain(F8 ? &sm.vraw_full[st] : &sm.v_full[st], par, p.err, abort_flag);
+      // released: the last occupant of each slot and the last Q of each buffer.
+      for (int m = max(0, n_occ - kSlots); m < n_occ; ++m) {
+        const int s = m % kSlots;
+        mbar_wait_drain(F8 ? &sm.raw_full[s] : &sm.full[s], (m / kSlots) & 1, p.err, abort_flag);
       }
       for (int ub = 0; ub < 2; ++ub)
         if (q_armed[ub] > 0 && q_copy[ub])
@@ -502,8 +552,8 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 1)
     }
   } else if (warp == 5) {
     // ============================ MMA issuer ==============================
-    // Tile n: S^T(n) = K(n) Q^T into S buffer n&1, then O^T += V^T(n-1)
-    // P^T(n-1), so the QK^T of a tile overlaps the softmax of the previous.
+    // Tile n: O^T += V^T(n-1) P^T(n-1) first, then S^T(n) = K(n) Q^T into S
+    // buffer n&1, so the QK^T of a tile overlaps the softmax of the previous.
     if (lane == 0) {
       constexpr uint32_t kIdescS =
           F8 ? idesc_f16_f32(kTile, kN, 0, 0) : idesc_bf16_f32(kTile, kN, 0, 0);
@@ -512,10 +562,10 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 1)
       int t = 0;
       bool ok = true;
       auto pv = [&](int tt, bool first, int j) {
-        const int b = tt & 1, st = tt % kStages, ob = j & 1;
+        const int n = 2 * tt + 1, s = n % kSlots, ob = j & 1;
         const uint32_t tO = tmem + kColO + ob * kN;
-        ok = ok && mbar_wait(&sm.p_full[b], (tt >> 1) & 1, p.err, abort_flag);
-        ok = ok && mbar_wait(&sm.v_full[st], (tt / kStages) & 1, p.err, abort_flag);
+        ok = ok && mbar_wait(&sm.p_full, tt & 1, p.err, abort_flag);
+        ok = ok && mbar_wait(&sm.full[s], (n / kSlots) & 1, p.err, abort_flag);
         // O^T buffer ob was last read by the epilogue of piece j - 2.
         if (first && j >= 2)
           ok = ok && mbar_wait(&sm.o_empty[ob], ((j >> 1) - 1) & 1, p.err, abort_flag);
@@ -527,15 +577,14 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 1)
         for (int kk = 0; kk < 8; ++kk) {
           // V^T is MN-major (d contiguous): atoms of 64 d x 8 keys, the two d
           // halves kHalf apart, 8-key groups 1024 bytes apart.
-          const uint64_t da = smem_desc_sw128(smem_u32(sm.v[st][0]) + kk * 2048, kHalf, 1024);
-          const uint64_t db =
-              smem_desc_sw128(smem_u32(sm.pt[b][kk >> 2]) + (kk & 3) * 32, 16, 1024);
+          const uint64_t da = smem_desc_sw128(smem_u32(sm.slot[s][0]) + kk * 2048, kHalf, 1024);
+          const uint64_t db = smem_desc_sw128(smem_u32(sm.pt[kk >> 2]) + (kk & 3) * 32, 16, 1024);
           tc_mma_f16_ss(tO, da, db, kIdescO, !first || kk > 0);
         }
-        tc_commit(&sm.kv_empty[st]);
-        tc_commit(&sm.p_free[b]);
+        tc_commit(&sm.empty[s]);
+        tc_commit(&sm.p_free);
 #if PKV_TC_TRACE >= 2
-        mbar_wait(&sm.p_free[b], (tt >> 1) & 1, p.err, abort_flag);  // PV completion
+        mbar_wait(&sm.p_free, tt & 1, p.err, abort_flag);  // PV completion
         TC_TR(6, tt);
 #endif
       };
@@ -549,11 +598,11 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 1)
         const int ntile = plan::cdiv(pc.nblk, kBlkPerTile);
         tc_fence_after();
         for (int tt = 0; tt < ntile && ok; ++tt, ++t) {
-          const int b = t & 1, st = t % kStages;
-          // The previous tile's PV first: its stage is released as soon as
+          const int b = t & 1, n = 2 * t, s = n % kSlots;
+          // The previous tile's PV first: its V slot is released as soon as
           // its probabilities are ready, not after this tile's keys arrive.
           if (tt >= 1) pv(t - 1, tt == 1, j);
-          ok = ok && mbar_wait(&sm.k_full[st], (t / kStages) & 1, p.err, abort_flag);
+          ok = ok && mbar_wait(&sm.full[s], (n / kSlots) & 1, p.err, abort_flag);
           TC_TR(1, t);
           if (t == 0) TC_CTA(4);
           if (t >= 2) ok = ok && mbar_wait(&sm.s_free[b], ((t >> 1) - 1) & 1, p.err, abort_flag);
@@ -563,11 +612,12 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 1)
           #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint64_t da =
-                smem_desc_sw128(smem_u32(sm.k[st][kk >> 2]) + (kk & 3) * 32, 16, 1024);
+                smem_desc_sw128(smem_u32(sm.slot[s][kk >> 2]) + (kk & 3) * 32, 16, 1024);
             const uint64_t db =
                 smem_desc_sw128(smem_u32(sm.q[ub][kk >> 2]) + (kk & 3) * 32, 16, 1024);
             tc_mma_f16_ss(tS, da, db, kIdescS, kk > 0);
           }
+          tc_commit(&sm.empty[s]);  // the K slot is free once S^T is computed
           tc_commit(&sm.s_full[b]);
 #if PKV_TC_TRACE >= 2
           mbar_wait(&sm.s_full[b], (t >> 1) & 1, p.err, abort_flag);  // QK completion
@@ -586,327 +636,289 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 1)
       }
     }
     __syncwarp();
-  } else if (F8 && warp >= 10) {
-    // ================= e4m3 converters (warps 10, 11) ====================
-    // Tile by tile, in the producer's order: widen K when its codes land,
-    // hand it to the MMA, then the same for V.  Each thread takes rows r and
+  } else if (F8 && warp >= kTcWarps) {
+    // ================= e4m3 converters (warps 6, 7) ======================
+    // Occupant by occupant, in the producer's order: widen the codes when
+    // they land and hand the slot to the MMA.  Each thread takes rows r and
     // r + 64 of the 128-key tile.
     const int r0 = tid - kTcThreads;  // 0 .. 63
-    for (int t = 0;; ++t) {
-      const int st = t % kStages;
-      if (!mbar_wait(&sm.kraw_full[st], (t / kStages) & 1, p.err, abort_flag)) break;
-      if (t >= *reinterpret_cast<volatile int*>(&sm.conv_end)) break;
-      widen_e4m3_row(sm.k[st][0], sm.k[st][1], r0);
-      widen_e4m3_row(sm.k[st][0], sm.k[st][1], r0 + 64);
+    for (int n = 0;; ++n) {
+      const int s = n % kSlots;
+      if (!mbar_wait(&sm.raw_full[s], (n / kSlots) & 1, p.err, abort_flag)) break;
+      if (n >= *reinterpret_cast<volatile int*>(&sm.conv_end)) break;
+      widen_e4m3_row(sm.slot[s][0], sm.slot[s][1], r0);
+      widen_e4m3_row(sm.slot[s][0], sm.slot[s][1], r0 + 64);
       fence_proxy_async_smem();  // generic-proxy writes, read by the tensor core
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.k_full[st]);
-      if (!mbar_wait(&sm.vraw_full[st], (t / kStages) & 1, p.err, abort_flag)) break;
-      widen_e4m3_row(sm.v[st][0], sm.v[st][1], r0);
-      widen_e4m3_row(sm.v[st][0], sm.v[st][1], r0 + 64);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.v_full[st]);
+      if (lane == 0) mbar_arrive(&sm.full[s]);
     }
-  } else {
-    if (warp < 4) {
-      // ========================= softmax (warps 0-3) ========================
-      const int row = tid;  // TMEM lane: key `row` of a tile
-      const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-      constexpr int kSoftThreads = 128;
-      int t = 0;
-      int j = 0;
-      for (;; ++j) {
-        const int ub = j & 1;
-        const bool got = mbar_wait(&sm.q_full[ub], (j >> 1) & 1, p.err, abort_flag);
-        const Piece pc = sm.pinfo[ub];
-        // Agree before any barrier: a wait that gave up (abort) stops everyone.
-        if (barrier_or(kBarSoftmax, kSoftThreads, !got || pc.row == kEndRow)) break;
-        if (F8) {
-          // Q of this piece to f16 in place (2 x 16 rows x 64 dims: two
-          // 16-byte chunks per thread), for the MMA's same-type operands
-          #pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            uint4* qp = reinterpret_cast<uint4*>(&sm.q[ub][0][0]) + tid * 2 + c;
-            uint4 v = *qp;
-            uint32_t* w = reinterpret_cast<uint32_t*>(&v);
-            #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float2 f = bf16x2_to_float2(w[i]);
-              const __half2 h2 = __floats2half2_rn(f.x, f.y);
-              w[i] = *reinterpret_cast<const uint32_t*>(&h2);
-            }
-            *qp = v;
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sm.q_conv[ub]);
-        }
-        bool ok = true;
-        const uint32_t tO = tmem + lane_off + kColO + ub * kN;
-        const int ntile = plan::cdiv(pc.nblk, kBlkPerTile);
-        // e4m3: the key scale of this KV head joins the softmax scale
-        const float sl =
-            F8 && pc.k >= 0 && pc.k < Hkv ? p.scale_log2 * __ldg(p.k_scale + pc.k) : p.scale_log2;
-        float m[G], l[G];
+  } else if (warp < 4) {
+    // ================ softmax + epilogue (warps 0-3) ======================
+    const int row = tid;  // TMEM lane: key `row` of a tile, dim `row` of O^T
+    const int d = tid;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    bool out_ready = !(p.early_kv && !p.early_q);  // out and the workspace may be written
+    int t = 0;
+    for (int j = 0;; ++j) {
+      const int ub = j & 1;
+      const bool got = mbar_wait(&sm.q_full[ub], (j >> 1) & 1, p.err, abort_flag);
+      const Piece pc = sm.pinfo[ub];
+      // Agree before any barrier: a wait that gave up (abort) stops everyone.
+      if (barrier_or(kBarSoftmax, kSoftThreads, !got || pc.row == kEndRow)) break;
+      if (F8) {
+        // Q of this piece to f16 in place (2 x 16 rows x 64 dims: two
+        // 16-byte chunks per thread), for the MMA's same-type operands
         #pragma unroll
-        for (int h = 0; h < G; ++h) {
-          m[h] = kNegBig;
-          l[h] = 0.f;
-        }
-        for (int tt = 0; tt < ntile; ++tt, ++t) {
-          const int b = t & 1, st = t % kStages;
-          ok = ok && mbar_wait(&sm.s_full[b], (t >> 1) & 1, p.err, abort_flag);
-          if (row == 0) TC_TR(2, t);
-          tc_fence_after();
-          float s[8];
-          tmem_ld8(tmem + lane_off + b * kN, s);
-          tc_wait_ld();
-          // Key `row` of this tile: block x of the tile, offset row % 16.
-          const int x = tt * kBlkPerTile + (row >> 4);
-          const int pos = (pc.b0 + x) * kBlockSize + (row & 15);
-          const bool valid = ok && x < pc.nblk && pos < pc.limit;
-          bool over = false;
+        for (int c = 0; c < 2; ++c) {
+          uint4* qp = reinterpret_cast<uint4*>(&sm.q[ub][0][0]) + tid * 2 + c;
+          uint4 v = *qp;
+          uint32_t* w = reinterpret_cast<uint32_t*>(&v);
           #pragma unroll
-          for (int h = 0; h < G; ++h) {
-            s[h] = valid ? s[h] * sl : -INFINITY;
-            over |= s[h] > m[h] + kLazyMargin;
+          for (int i = 0; i < 4; ++i) {
+            const float2 f = bf16x2_to_float2(w[i]);
+            const __half2 h2 = __floats2half2_rn(f.x, f.y);
+            w[i] = *reinterpret_cast<const uint32_t*>(&h2);
           }
-          // S buffer b has been read: the MMA may overwrite it (tile t + 2).
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sm.s_free[b]);
-          if (barrier_or(kBarSoftmax, kSoftThreads, over)) {
-            // Raise the running maxima to this tile's; O^T and l move with them.
-            #pragma unroll
-            for (int h = 0; h < G; ++h) {
-              const float mx = warp_max(s[h]);
-              if (lane == 0) sm.red[warp][h] = mx;
-            }
-            named_barrier(kBarSoftmax, kSoftThreads);
-            float alpha[8];
-            bool grow = false;
-            #pragma unroll
-            for (int h = 0; h < G; ++h) {
-              const float mx = fmaxf(fmaxf(sm.red[0][h], sm.red[1][h]),
-                                     fmaxf(sm.red[2][h], sm.red[3][h]));
-              const float mn = fmaxf(m[h], mx);
-              alpha[h] = fast_exp2(m[h] - mn);
-              grow |= mn != m[h];
-              m[h] = mn;
-              l[h] *= alpha[h];
-            }
-            if (tt > 0 && grow) {
-              // O^T must hold the previous tile's PV before it is rescaled.
-              ok = ok && mbar_wait(&sm.p_free[(t - 1) & 1], ((t - 1) >> 1) & 1, p.err, abort_flag);
-              tc_fence_after();
-              float o[8];
-              tmem_ld8(tO, o);
-              tc_wait_ld();
-              #pragma unroll
-              for (int h = 0; h < G; ++h) o[h] *= alpha[h];
-              tmem_st8(tO, o);
-              tc_wait_st();
-            }
-            // sm.red is read by every softmax thread before its next write.
-            named_barrier(kBarSoftmax, kSoftThreads);
-          }
-          // P^T buffer b was last read by the PV of tile t - 2.
-          if (t >= 2) ok = ok && mbar_wait(&sm.p_free[b], ((t >> 1) - 1) & 1, p.err, abort_flag);
-          // p = exp2(s - m) in bf16; P^T row h holds head h, keys contiguous,
-          // 128-byte swizzle.  The normaliser sums the rounded values the MMA
-          // will use.
-          uint8_t* prow = sm.pt[b][row >> 6];
-          const int kc = (row & 63) >> 3;
-          #pragma unroll
-          for (int h = 0; h < G; ++h) {
-            uint16_t* dst = reinterpret_cast<uint16_t*>(prow + (h >> 3) * 1024 + (h & 7) * 128 +
-                                                        ((kc ^ (h & 7)) * 16) + (row & 7) * 2);
-            if (F8) {  // f16, the type of the widened V
-              const __half ph = __float2half_rn(fast_exp2(s[h] - m[h]));
-              l[h] += __half2float(ph);
-              *dst = *reinterpret_cast<const uint16_t*>(&ph);
-            } else {
-              const __nv_bfloat16 pb = __float2bfloat16_rn(fast_exp2(s[h] - m[h]));
-              l[h] += __bfloat162float(pb);
-              *dst = *reinterpret_cast<const uint16_t*>(&pb);
-            }
-          }
-          // Keys past the request's end inside its last block may hold anything
-          // (even NaN): zero those V rows so that 0 * V stays 0 in the MMA.
-          if (x < pc.nblk && pos >= pc.L) {
-            ok = ok && mbar_wait(&sm.v_full[st], (t / kStages) & 1, p.err, abort_flag);
-            #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-              uint4* vr = reinterpret_cast<uint4*>(sm.v[st][hf] + (row >> 3) * 1024 + (row & 7) * 128);
-              #pragma unroll
-              for (int c = 0; c < 8; ++c) vr[c] = make_uint4(0, 0, 0, 0);
-            }
-          }
-          fence_proxy_async_smem();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sm.p_full[b]);
+          *qp = v;
         }
-        // ---- hand the piece to the epilogue: maxima, normaliser partials ---
-        if (j >= 2) mbar_wait(&sm.st_empty[ub], ((j >> 1) - 1) & 1, p.err, abort_flag);
-        #pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float sw = warp_sum(l[h]);
-          if (lane == 0) sm.st_l[ub][warp][h] = sw;
-        }
-        if (warp == 0 && lane == 0) {
-          #pragma unroll
-          for (int h = 0; h < G; ++h) sm.st_m[ub][h] = m[h];
-          sm.st_pc[ub] = pc;
-        }
+        fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.st_full[ub]);
-        if (warp == 0 && lane == 0) TC_CTA(14);
+        if (lane == 0) mbar_arrive(&sm.q_conv[ub]);
       }
-      // End marker for the epilogue.
-      {
-        const int ub = j & 1;
-        if (j >= 2) mbar_wait(&sm.st_empty[ub], ((j >> 1) - 1) & 1, p.err, abort_flag);
-        if (warp == 0 && lane == 0) sm.st_pc[ub].row = kEndRow;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.st_full[ub]);
+      bool ok = true;
+      const uint32_t tO = tmem + lane_off + kColO + ub * kN;
+      const int ntile = plan::cdiv(pc.nblk, kBlkPerTile);
+      // e4m3: the key scale of this KV head joins the softmax scale
+      const float sl =
+          F8 && pc.k >= 0 && pc.k < Hkv ? p.scale_log2 * __ldg(p.k_scale + pc.k) : p.scale_log2;
+      float m[G], l[G];
+      #pragma unroll
+      for (int h = 0; h < G; ++h) {
+        m[h] = kNegBig;
+        l[h] = 0.f;
       }
-    } else {
-      // ======================== epilogue (warps 6-9) ========================
-      // Warp w reaches TMEM lanes 32 (w % 4) .. +31: dims d of O^T.
-      const int d = (warp & 3) * 32 + lane;
-      const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-      constexpr int kEpiThreads = 128;
-      if (p.early_kv && !p.early_q) grid_dependency_wait();  // before writing out or the workspace
-      for (int j = 0;; ++j) {
-        const int ob = j & 1;
-        const bool got = mbar_wait(&sm.st_full[ob], (j >> 1) & 1, p.err, abort_flag);
-        const Piece pc = sm.st_pc[ob];
-        if (barrier_or(kBarEpi, kEpiThreads, !got || pc.row == kEndRow)) break;
-        if (d == 0) TC_CTA(15);
-        float m[8], lt[8];
-        #pragma unroll
-        for (int h = 0; h < G; ++h) {
-          m[h] = sm.st_m[ob][h];
-          lt[h] = (sm.st_l[ob][0][h] + sm.st_l[ob][1][h]) + (sm.st_l[ob][2][h] + sm.st_l[ob][3][h]);
-        }
-        const bool ok = mbar_wait(&sm.o_full[ob], (j >> 1) & 1, p.err, abort_flag);
+      for (int tt = 0; tt < ntile; ++tt, ++t) {
+        const int b = t & 1;
+        ok = ok && mbar_wait(&sm.s_full[b], (t >> 1) & 1, p.err, abort_flag);
+        if (row == 0) TC_TR(2, t);
         tc_fence_after();
-        float o[8];
-        tmem_ld8(tmem + lane_off + kColO + ob * kN, o);
+        float s[8];
+        tmem_ld8(tmem + lane_off + b * kN, s);
         tc_wait_ld();
-        if (d == 0) TC_CTA(16);
-        if (F8) {  // the value scale of this KV head
-          const float vs = pc.k >= 0 && pc.k < Hkv ? __ldg(p.v_scale + pc.k) : 0.f;
-          #pragma unroll
-          for (int h = 0; h < G; ++h) o[h] *= vs;
+        // Key `row` of this tile: block x of the tile, offset row % 16.
+        const int x = tt * kBlkPerTile + (row >> 4);
+        const int pos = (pc.b0 + x) * kBlockSize + (row & 15);
+        const bool valid = ok && x < pc.nblk && pos < pc.limit;
+        bool over = false;
+        #pragma unroll
+        for (int h = 0; h < G; ++h) {
+          s[h] = valid ? s[h] * sl : -INFINITY;
+          over |= s[h] > m[h] + kLazyMargin;
         }
+        // S buffer b has been read: the MMA may overwrite it (tile t + 2).
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&sm.o_empty[ob]);
-          mbar_arrive(&sm.st_empty[ob]);
-        }
-        const bool in_range = pc.row >= 0 && pc.row < p.num_q_tokens && pc.k >= 0 &&
-                              pc.k < Hkv && pc.nblk >= 1 && pc.S >= 1 && pc.c0 >= 0 &&
-                              2 * (pc.c0 + pc.S) <= p.num_slots && pc.slot >= 0 &&
-                              pc.slot < p.num_slots;
-        const long long out_row = ((long long)pc.row * p.num_q_heads + (long long)pc.k * G) * kHeadDim;
-        // Shared-prefix (cascade) rows: fold in the prefix pass's partial
-        // state (max M, normaliser, normalised output) by log-sum-exp.
-        // The prefix pass left one partial per chunk of the shared keys
-        // (pc.b0 is at least the shared block count, and the row's first
-        // piece starts exactly there).
-        auto fold_prefix = [&](int h, float& M, float& num, float& den) {
-          const long long pr = (long long)pc.row * p.num_q_heads + (long long)pc.k * G + h;
-          const long long stride = (long long)p.num_q_tokens * p.num_q_heads;
-          const int nch = prefix_chunks(pc.fb * kBlockSize);
-          // all chunks' loads first (they were prefetched into L2), then fold
-          float2 ml[kPrefixSplits];
-          float ov[kPrefixSplits];
+        if (lane == 0) mbar_arrive(&sm.s_free[b]);
+        // P^T was last read (and O^T last updated) by the PV of tile t - 1.
+        if (t >= 1) ok = ok && mbar_wait(&sm.p_free, (t - 1) & 1, p.err, abort_flag);
+        if (barrier_or(kBarSoftmax, kSoftThreads, over)) {
+          // Raise the running maxima to this tile's; O^T and l move with them.
           #pragma unroll
-          for (int c = 0; c < kPrefixSplits; ++c) {
-            if (c < nch) {
-              const long long sl = c * stride + pr;
-              ml[c] = __ldcg(reinterpret_cast<const float2*>(p.pre_ml + sl * 2));
-              ov[c] = __ldcg(p.pre_o + sl * kHeadDim + d);
-            }
+          for (int h = 0; h < G; ++h) {
+            const float mx = warp_max(s[h]);
+            if (lane == 0) sm.red[warp][h] = mx;
           }
+          named_barrier(kBarSoftmax, kSoftThreads);
+          float alpha[8];
+          bool grow = false;
           #pragma unroll
-          for (int c = 0; c < kPrefixSplits; ++c) {
-            if (c < nch) {
-              const float Mn = fmaxf(M, ml[c].x);
-              const float a = fast_exp2(M - Mn), w = fast_exp2(ml[c].x - Mn) * ml[c].y;
-              num = num * a + w * ov[c];
+          for (int h = 0; h < G; ++h) {
+            const float mx = fmaxf(fmaxf(sm.red[0][h], sm.red[1][h]),
+                                   fmaxf(sm.red[2][h], sm.red[3][h]));
+            const float mn = fmaxf(m[h], mx);
+            alpha[h] = fast_exp2(m[h] - mn);
+            grow |= mn != m[h];
+            m[h] = mn;
+            l[h] *= alpha[h];
+          }
+          if (tt > 0 && grow) {
+            tc_fence_after();
+            float o[8];
+            tmem_ld8(tO, o);
+            tc_wait_ld();
+            #pragma unroll
+            for (int h = 0; h < G; ++h) o[h] *= alpha[h];
+            tmem_st8(tO, o);
+            tc_wait_st();
+          }
+          // sm.red is read by every softmax thread before its next write.
+          named_barrier(kBarSoftmax, kSoftThreads);
+        }
+        // p = exp2(s - m) in bf16; P^T row h holds head h, keys contiguous,
+        // 128-byte swizzle.  The normaliser sums the rounded values the MMA
+        // will use.
+        uint8_t* prow = sm.pt[row >> 6];
+        const int kc = (row & 63) >> 3;
+        #pragma unroll
+        for (int h = 0; h < G; ++h) {
+          uint16_t* dst = reinterpret_cast<uint16_t*>(prow + (h >> 3) * 1024 + (h & 7) * 128 +
+                                                      ((kc ^ (h & 7)) * 16) + (row & 7) * 2);
+          if (F8) {  // f16, the type of the widened V
+            const __half ph = __float2half_rn(fast_exp2(s[h] - m[h]));
+            l[h] += __half2float(ph);
+            *dst = *reinterpret_cast<const uint16_t*>(&ph);
+          } else {
+            const __nv_bfloat16 pb = __float2bfloat16_rn(fast_exp2(s[h] - m[h]));
+            l[h] += __bfloat162float(pb);
+            *dst = *reinterpret_cast<const uint16_t*>(&pb);
+          }
+        }
+        // Keys past the request's end inside its last block may hold anything
+        // (even NaN): zero those V rows so that 0 * V stays 0 in the MMA.
+        if (x < pc.nblk && pos >= pc.L) {
+          const int n = 2 * t + 1, sv = n % kSlots;
+          ok = ok && mbar_wait(&sm.full[sv], (n / kSlots) & 1, p.err, abort_flag);
+          #pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            uint4* vr = reinterpret_cast<uint4*>(sm.slot[sv][hf] + (row >> 3) * 1024 + (row & 7) * 128);
+            #pragma unroll
+            for (int c = 0; c < 8; ++c) vr[c] = make_uint4(0, 0, 0, 0);
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.p_full);
+      }
+      // ============ epilogue of the piece (same four warps) ================
+      // Thread d reads TMEM lane d: dim d of O^T for the g heads.
+      #pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float sw = warp_sum(l[h]);
+        if (lane == 0) sm.st_l[warp][h] = sw;
+      }
+      named_barrier(kBarSoftmax, kSoftThreads);
+      float lt[8];
+      #pragma unroll
+      for (int h = 0; h < G; ++h)
+        lt[h] = (sm.st_l[0][h] + sm.st_l[1][h]) + (sm.st_l[2][h] + sm.st_l[3][h]);
+      const bool okO = ok && mbar_wait(&sm.o_full[ub], (j >> 1) & 1, p.err, abort_flag);
+      tc_fence_after();
+      float o[8];
+      tmem_ld8(tO, o);
+      tc_wait_ld();
+      if (d == 0) TC_CTA(16);
+      if (F8) {  // the value scale of this KV head
+        const float vs = pc.k >= 0 && pc.k < Hkv ? __ldg(p.v_scale + pc.k) : 0.f;
+        #pragma unroll
+        for (int h = 0; h < G; ++h) o[h] *= vs;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.o_empty[ub]);
+      if (!out_ready) {
+        grid_dependency_wait();  // before writing out or the workspace
+        out_ready = true;
+      }
+      const bool in_range = pc.row >= 0 && pc.row < p.num_q_tokens && pc.k >= 0 &&
+                            pc.k < Hkv && pc.nblk >= 1 && pc.S >= 1 && pc.c0 >= 0 &&
+                            2 * (pc.c0 + pc.S) <= p.num_slots && pc.slot >= 0 &&
+                            pc.slot < p.num_slots;
+      const long long out_row = ((long long)pc.row * p.num_q_heads + (long long)pc.k * G) * kHeadDim;
+      // Shared-prefix (cascade) rows: fold in the prefix pass's partial
+      // state (max M, normaliser, normalised output) by log-sum-exp.  The
+      // prefix pass left one partial per chunk of the shared keys (pc.b0 is
+      // at least the shared block count, and the row's first piece starts
+      // exactly there).
+      auto fold_prefix = [&](int h, float& M, float& num, float& den) {
+        const long long pr = (long long)pc.row * p.num_q_heads + (long long)pc.k * G + h;
+        const long long stride = (long long)p.num_q_tokens * p.num_q_heads;
+        const int nch = prefix_chunks(pc.fb * kBlockSize);
+        // all chunks' loads first (they were prefetched into L2), then fold
+        float2 ml[kPrefixSplits];
+        float ov[kPrefixSplits];
+        #pragma unroll
+        for (int c = 0; c < kPrefixSplits; ++c) {
+          if (c < nch) {
+            const long long sl2 = c * stride + pr;
+            ml[c] = __ldcg(reinterpret_cast<const float2*>(p.pre_ml + sl2 * 2));
+            ov[c] = __ldcg(p.pre_o + sl2 * kHeadDim + d);
+          }
+        }
+        #pragma unroll
+        for (int c = 0; c < kPrefixSplits; ++c) {
+          if (c < nch) {
+            const float Mn = fmaxf(M, ml[c].x);
+            const float a = fast_exp2(M - Mn), w = fast_exp2(ml[c].x - Mn) * ml[c].y;
+            num = num * a + w * ov[c];
+            den = den * a + w;
+            M = Mn;
+          }
+        }
+      };
+      if (in_range && pc.S == 1) {
+        if (okO) {
+          #pragma unroll
+          for (int h = 0; h < G; ++h) {
+            float res = lt[h] > 0.f ? o[h] * __frcp_rn(lt[h]) : 0.f;
+            if (pc.pre) {
+              float M = m[h], num = lt[h] * res, den = lt[h];
+              fold_prefix(h, M, num, den);
+              res = den > 0.f ? num / den : 0.f;
+            }
+            p.out[out_row + h * kHeadDim + d] = __float2bfloat16_rn(res);
+          }
+        }
+      } else if (in_range) {
+        // Partial piece: normalised output and (max, normaliser), then the
+        // last piece of the row-group to arrive merges all of them.  Every
+        // softmax thread takes this branch (pc is shared), so the barriers
+        // below are uniform.
+        if (okO) {
+          #pragma unroll
+          for (int h = 0; h < G; ++h) {
+            const long long slot = (long long)pc.slot * G + h;
+            p.ws_o[slot * kHeadDim + d] = lt[h] > 0.f ? o[h] * __frcp_rn(lt[h]) : 0.f;
+            if (d == 0) *reinterpret_cast<float2*>(p.ws_ml + slot * 2) = make_float2(m[h], lt[h]);
+          }
+        }
+        named_barrier(kBarSoftmax, kSoftThreads);
+        if (d == 0) {
+          __threadfence();
+          int* cnt = p.ws_cnt + (long long)pc.row * Hkv + pc.k;
+          const int old = atomicAdd(cnt, 1);
+          const int last = (old == pc.S - 1);
+          if (last) {
+            *cnt = 0;  // every piece has arrived: leave the counter at zero
+            __threadfence();
+          }
+          sm.is_last = last;
+        }
+        named_barrier(kBarSoftmax, kSoftThreads);
+        if (sm.is_last) {
+          #pragma unroll
+          for (int h = 0; h < G; ++h) {
+            float M = kNegBig, num = 0.f, den = 0.f;
+            #pragma unroll 4
+            for (int s2 = 0; s2 < pc.S; ++s2) {
+              const int slot = 2 * (pc.c0 + s2) + ((s2 == 0 && pc.odd0) ? 1 : 0);
+              const long long sl2 = (long long)slot * G + h;
+              const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.ws_ml + sl2 * 2));
+              const float ov = __ldcg(p.ws_o + sl2 * kHeadDim + d);
+              const float Mn = fmaxf(M, ml.x);
+              const float a = fast_exp2(M - Mn), w = fast_exp2(ml.x - Mn) * ml.y;
+              num = num * a + w * ov;
               den = den * a + w;
               M = Mn;
             }
+            if (pc.pre) fold_prefix(h, M, num, den);
+            p.out[out_row + h * kHeadDim + d] = __float2bfloat16_rn(den > 0.f ? num / den : 0.f);
           }
-        };
-        if (in_range && pc.S == 1) {
-          if (ok) {
-            #pragma unroll
-            for (int h = 0; h < G; ++h) {
-              float res = lt[h] > 0.f ? o[h] / lt[h] : 0.f;
-              if (pc.pre) {
-                float M = m[h], num = lt[h] * res, den = lt[h];
-                fold_prefix(h, M, num, den);
-                res = den > 0.f ? num / den : 0.f;
-              }
-              p.out[out_row + h * kHeadDim + d] = __float2bfloat16_rn(res);
-            }
-          }
-        } else if (in_range) {
-          // Partial piece: normalised output and (max, normaliser), then the
-          // last piece of the row-group to arrive merges all of them.  Every
-          // epilogue thread takes this branch (pc is shared), so the barriers
-          // below are uniform.
-          if (ok) {
-            #pragma unroll
-            for (int h = 0; h < G; ++h) {
-              const long long slot = (long long)pc.slot * G + h;
-              p.ws_o[slot * kHeadDim + d] = lt[h] > 0.f ? o[h] / lt[h] : 0.f;
-              if (d == 0) *reinterpret_cast<float2*>(p.ws_ml + slot * 2) = make_float2(m[h], lt[h]);
-            }
-          }
-          named_barrier(kBarEpi, kEpiThreads);
-          if (d == 0) {
-            __threadfence();
-            int* cnt = p.ws_cnt + (long long)pc.row * Hkv + pc.k;
-            const int old = atomicAdd(cnt, 1);
-            const int last = (old == pc.S - 1);
-            if (last) {
-              *cnt = 0;  // every piece has arrived: leave the counter at zero
-              __threadfence();
-            }
-            sm.is_last = last;
-          }
-          named_barrier(kBarEpi, kEpiThreads);
-          if (sm.is_last) {
-            #pragma unroll
-            for (int h = 0; h < G; ++h) {
-              float M = kNegBig, num = 0.f, den = 0.f;
-              #pragma unroll 4
-              for (int s2 = 0; s2 < pc.S; ++s2) {
-                const int slot = 2 * (pc.c0 + s2) + ((s2 == 0 && pc.odd0) ? 1 : 0);
-                const long long sl = (long long)slot * G + h;
-                const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.ws_ml + sl * 2));
-                const float ov = __ldcg(p.ws_o + sl * kHeadDim + d);
-                const float Mn = fmaxf(M, ml.x);
-                const float a = fast_exp2(M - Mn), w = fast_exp2(ml.x - Mn) * ml.y;
-                num = num * a + w * ov;
-                den = den * a + w;
-                M = Mn;
-              }
-              if (pc.pre) fold_prefix(h, M, num, den);
-              p.out[out_row + h * kHeadDim + d] = __float2bfloat16_rn(den > 0.f ? num / den : 0.f);
-            }
-          }
-          named_barrier(kBarEpi, kEpiThreads);  // sm.is_last is free again
         }
-        if (d == 0) TC_CTA(6);
       }
+      // sm.st_l and sm.is_last are free again once every thread is here.
+      named_barrier(kBarSoftmax, kSoftThreads);
+      if (d == 0) TC_CTA(6);
     }
   }
   // Every warp reaches this point (aborts only shorten the loops), so the
@@ -917,6 +929,10 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 1)
   if (warp == 5) tmem_dealloc(tmem, kTmemCols);
   if (tid == 0) TC_CTA(7);
 }
+
+// Two CTAs per SM: each takes at most half of the SM's 228 KiB of shared
+// memory, less the 1 KiB the hardware reserves per CTA.
+static_assert(sizeof(TcSmem) + 1024 <= (228 * 1024) / 2 - 1024, "two CTAs per SM");
 
 template <int G, bool F8>
 cudaError_t launch_decode_tc_g(const DecodeTcLaunch& L, cudaStream_t stream) {
@@ -929,6 +945,10 @@ cudaError_t launch_decode_tc_g(const DecodeTcLaunch& L, cudaStream_t stream) {
   if (!(__atomic_load_n(&configured, __ATOMIC_ACQUIRE) & bit)) {
     e = cudaFuncSetAttribute(decode_tc_kernel<G, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
+    if (e != cudaSuccess) return e;
+    // Two CTAs per SM need the largest shared-memory carveout.
+    e = cudaFuncSetAttribute(decode_tc_kernel<G, F8>,
+                             cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
     __atomic_fetch_or(&configured, bit, __ATOMIC_RELEASE);
   }

@@ -83,6 +83,11 @@ struct DecodeParams {
   int align_slack;    // ... if that lengthens the per-CTA range by at most this many blocks
   int prefetch;       // warm L2 with the block-table rows this CTA will likely read
   int early_plan;     // plan from seq_lens / query_start_loc before the PDL wait
+  // If the step has at most this many blocks per CTA of half the grid, only
+  // the first half of the grid takes work (0: the whole grid always does).
+  int half_grid_blocks;
+  int warm_kv;        // tensor-core decode: warm L2 with the first K/V blocks before the
+                      // PDL wait (0 off, 1 bulk prefetches, 2 per-line prefetches)
   // The kernel before this one on the stream is the append of exactly this
   // step's new tokens (positions L - q_r .. L - 1 of each request): q, the
   // block table and every K/V tile holding none of those positions are read

@@ -113,7 +113,12 @@ __device__ __forceinline__ Range finish_range(const DecodeParams& p, long long m
     nb_max = max(nb_max, __shfl_xor_sync(0xffffffffu, nb_max, o));
   }
   const long long W = mine;
-  long long chunk = max((long long)p.min_chunk, cdiv_ll(W, gridDim.x));
+  // Steps with little work run on the first half of the grid (one CTA per
+  // SM when the grid is two per SM), leaving each SM's second slot to the
+  // next launch, which can then prepare while this one streams.
+  const int ctas = p.half_grid_blocks > 0 && W <= (long long)p.half_grid_blocks * (gridDim.x / 2)
+                       ? (int)(gridDim.x / 2) : (int)gridDim.x;
+  long long chunk = max((long long)p.min_chunk, cdiv_ll(W, ctas));
   if (p.align && nb_min == nb_max && W > 0) {
     // Uniform row-groups: cut each into equal pieces, or keep whole groups
     // together, so that piece boundaries coincide with CTA boundaries --
@@ -293,7 +298,7 @@ __device__ __forceinline__ int plan_header_word(const DecodeParams& p, int j) {
     case 6: return p.align_slack;
     case 7: return (int)gridDim.x;
     case 8: return p.max_blocks;
-    default: return kPcMagic;
+    default: return kPcMagic ^ p.half_grid_blocks;
   }
 }
 

@@ -488,3 +488,24 @@ def test_plan_cache_follows_lengths(pkv_opts):
         bt_h = bt.cpu().numpy()
         h["block_tables"] = bt_h
         assert_close(to_f64(outs[0]), oracle_full(h, kp, vp), shape.name)
+
+
+@pytest.mark.parametrize("width", [600, 5000])
+def test_wide_table_small_step_matches_narrow_table(width):
+    # A table far wider than the lengths need makes the host launch the
+    # tensor-core decode on two CTAs per SM; the plan then finds the work
+    # small and gives it to the first half of the grid only (the rest exit
+    # at once).  The split is the same as with the narrow table: same bits.
+    shape = wl.StepShape("wide_table", np.full(64, 512), np.ones(64), 12, 2, seed=81)
+    inp = wl.make_step(shape, device="cuda", poison=True)
+    h = host_copy(inp)
+    kp, vp = oracle_pools_after_append(h)
+    narrow = gpu_step(inp)
+    wide_bt = torch.full((shape.num_reqs, width), -1, dtype=torch.int32, device="cuda")
+    wide_bt[:, :inp.block_tables.shape[1]] = inp.block_tables
+    wide = pkv.pkv_attention(inp.q, inp.k_pool, inp.v_pool, wide_bt, inp.seq_lens,
+                             inp.query_start_loc, inp.scale)
+    torch.cuda.synchronize()
+    assert pkv.pkv_get_device_error() == 0, pkv.pkv_last_error()
+    assert torch.equal(narrow.view(torch.int16), wide.view(torch.int16))
+    assert_close(to_f64(wide), oracle_full(h, kp, vp), "wide table")
