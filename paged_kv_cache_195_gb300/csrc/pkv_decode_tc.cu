@@ -65,21 +65,26 @@ using plan::kEndRow;
 
 constexpr int kTcWarps = 6;                 // 0-3 softmax + epilogue, 4 producer, 5 MMA
 constexpr int kTcThreads = 32 * kTcWarps;
-// e4m3 pools: two more warps (6, 7) widen each slot's codes to f16 in shared
-// memory before the tensor core reads them (one hardware conversion per pair
-// of codes); Q and P are then f16 as well, since both operands of a kind::f16
-// MMA must have the same type.
-constexpr int kConvWarps = 2;
+// e4m3 pools: four more warps (6-9), one per TMEM lane quarter, widen the
+// codes to f16 (one hardware conversion per pair of codes): K rows straight
+// into TMEM, where the S^T MMA reads its A operand, V rows into a shared-
+// memory operand; Q and P are then f16 as well, since both operands of a
+// kind::f16 MMA must have the same type.
+constexpr int kConvWarps = 4;
 constexpr int kTcThreadsF8 = kTcThreads + 32 * kConvWarps;
 constexpr int kRawTile = 128 * kHeadDim;   // one 128-key tile of e4m3 codes (bytes)
+constexpr int kRawSlots = 4;               // e4m3 ring: K or V codes of one tile
 constexpr int kTile = 128;                 // keys per tile (MMA M of S^T, K of PV)
 constexpr int kBlkPerTile = kTile / kBlockSize;
 constexpr int kN = 16;                     // MMA N: the group's heads, padded
 constexpr int kHalf = kTile * 128;         // one 64-dim half of a 128-key bf16 tile
 constexpr int kOpHalf = kN * 128;          // one 64-element half of a 16-row operand
 constexpr int kSlots = 3;                  // ring slots (32 KiB): K or V of one tile
-constexpr uint32_t kTmemCols = 64;         // S0: 0..15, S1: 16..31, O0: 32..47, O1: 48..63
+// TMEM columns: S0 0..15, S1 16..31, O0 32..47, O1 48..63; e4m3 pools also
+// hold the widened K tiles there (two buffers of 64 columns: 128 keys x 128 d
+// f16, two d per column).
 constexpr uint32_t kColO = 32;             // O^T of piece j in columns kColO + (j & 1) * kN
+constexpr uint32_t kColK = 64;             // e4m3: K tile t in columns kColK + (t & 1) * 64
 constexpr float kNegBig = -1.0e30f;
 constexpr float kLazyMargin = 8.f;         // log2 of the largest probability allowed
 constexpr int kBarSoftmax = 1;             // named barrier of the four softmax warps
@@ -119,18 +124,28 @@ __device__ unsigned long long g_tc_cta[kTrSlots][kTrCtas][18];
 #endif
 
 struct __align__(1024) TcSmem {
-  // Ring occupant n (n = 0, 1, 2, ...) lives in slot n % kSlots: the K tile of
-  // tile n / 2 when n is even, its V tile when n is odd; [d half] 128 keys x
-  // 64 d, 128-byte swizzled.
-  uint8_t slot[kSlots][2][kHalf];
+  union {
+    // bf16: ring occupant n (n = 0, 1, 2, ...) lives in slot n % kSlots: the
+    // K tile of tile n / 2 when n is even, its V tile when n is odd; [d half]
+    // 128 keys x 64 d, 128-byte swizzled.
+    uint8_t slot[kSlots][2][kHalf];
+    struct {
+      // e4m3: occupant n's codes in raw slot n % kRawSlots (128 keys x 128
+      // codes, 128-byte swizzled), and the widened V operand of one tile.
+      uint8_t raw[kRawSlots][kRawTile];
+      uint8_t vbuf[2][kHalf];
+    } f8;
+  };
   uint8_t q[2][2][kOpHalf];       // [piece buffer][d half]: Q rows (heads), rows >= g zero
   uint8_t pt[2][kOpHalf];         // [key half]: P^T as 16 rows (heads) x 64 keys
   float red[4][kN];               // per-warp partial maxima (softmax warps)
   float st_l[4][kN];              // per-warp normaliser partial sums (epilogue)
   Piece pinfo[2];
   uint64_t q_full[2], q_empty[2];
-  uint64_t full[kSlots], empty[kSlots];  // occupant landed (bf16) or widened (e4m3) / released
-  uint64_t raw_full[kSlots];      // e4m3 pools: the occupant's codes landed
+  uint64_t full[kSlots], empty[kSlots];  // bf16: occupant landed / released
+  uint64_t raw_full[kRawSlots], raw_empty[kRawSlots];  // e4m3: codes landed / read
+  uint64_t kt_full[2], kt_free[2];  // e4m3: K tile widened into TMEM / read by S^T
+  uint64_t v_full, v_free;        // e4m3: V operand widened / read by the PV
   uint64_t q_conv[2];             // e4m3 pools: Q buffer converted to f16 by the softmax warps
   uint64_t s_full[2], s_free[2];  // S^T buffer computed / read by the softmax
   uint64_t p_full, p_free;        // P^T written by the softmax / read by the PV
@@ -141,6 +156,7 @@ struct __align__(1024) TcSmem {
   int is_last;
   int idle;                       // the plan gave this CTA no work
   int conv_end;                   // e4m3 pools: ring occupants issued in all (set at the end)
+  int raw_valid[kRawSlots];       // e4m3: leading rows of the occupant's tile that hold keys
 };
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -155,33 +171,34 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// Key row `row` of a tile whose e4m3 codes TMA left in buf[1] (128 bytes per
-// row, 128-byte swizzle) becomes the f16 operand row: d 0..63 in buf[0],
-// d 64..127 in buf[1], both 128-byte swizzled.  Every e4m3 value is an f16
-// value, so the widening (the hardware e4m3x2 -> f16x2 conversion) is exact.
-// The row's codes are read before any of its f16 chunks is written, and no
-// other row's bytes are touched, so the rows of a tile can be widened in any
-// order and in place.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2_bits(uint32_t two_codes) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two_codes, __NV_E4M3);
-  return (uint32_t)h.x | ((uint32_t)h.y << 16);
+// Two e4m3 codes (low byte first) to two f16 (low half first).  Every e4m3
+// value is an f16 value, so the widening (the hardware e4m3x2 -> f16x2
+// conversion) is exact.
+// Four codes (one 32-bit word, low byte first) become two f16 pairs: codes
+// 0, 1 in lo and 2, 3 in hi, one hardware conversion per pair.
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 a, b;\n\t"
+      "mov.b32 {a, b}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, a;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
 }
 
-__device__ __forceinline__ void widen_e4m3_row(uint8_t* half0, uint8_t* half1, int row) {
+// Row `row` of a raw e4m3 tile (128 codes, 128-byte swizzle) widened to f16
+// into the V operand: d 0..63 in half0, d 64..127 in half1, the same
+// swizzled row layout a bf16 tile has; rows past the request's end (which may
+// hold any code, NaN included) become zeros, so that 0 * V stays 0.
+__device__ __forceinline__ void widen_e4m3_row_to(const uint8_t* raw, uint8_t* half0,
+                                                  uint8_t* half1, int row, bool zero) {
   const int sw = row & 7;
-  uint4 raw[8];
-  #pragma unroll
-  for (int c8 = 0; c8 < 8; ++c8) raw[c8] = lds128(half1 + row * 128 + ((c8 ^ sw) * 16));
   #pragma unroll
   for (int c8 = 0; c8 < 8; ++c8) {
-    // codes of d = 16 c8 .. 16 c8 + 15 -> f16 chunks 2 (c8 % 4) and +1 of half c8 / 4
-    const uint32_t w[4] = {raw[c8].x, raw[c8].y, raw[c8].z, raw[c8].w};
+    const uint4 v = zero ? make_uint4(0, 0, 0, 0) : lds128(raw + row * 128 + ((c8 ^ sw) * 16));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t b[8];
     #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      b[2 * j] = e4m3x2_to_f16x2_bits(w[j] & 0xffffu);
-      b[2 * j + 1] = e4m3x2_to_f16x2_bits(w[j] >> 16);
-    }
+    for (int j = 0; j < 4; ++j) e4m3x4_to_f16x4(w[j], b[2 * j], b[2 * j + 1]);
     uint8_t* dst = (c8 < 4 ? half0 : half1) + row * 128;
     const int c = (c8 & 3) * 2;
     *reinterpret_cast<uint4*>(dst + ((c ^ sw) * 16)) = make_uint4(b[0], b[1], b[2], b[3]);
@@ -189,9 +206,9 @@ __device__ __forceinline__ void widen_e4m3_row(uint8_t* half0, uint8_t* half1, i
   }
 }
 
-// F8: the pools hold e4m3 codes (kmap / vmap are maps of bytes); each slot is
-// widened to f16 in shared memory, the key scale joins the softmax scale and
-// the value scale multiplies the output.
+// F8: the pools hold e4m3 codes (kmap / vmap are maps of bytes); K tiles are
+// widened into TMEM and V tiles into shared memory, the key scale joins the
+// softmax scale and the value scale multiplies the output.
 template <int G, bool F8>
 __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 2)
     decode_tc_kernel(const __grid_constant__ CUtensorMap qmap,
@@ -199,6 +216,8 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 2)
                      const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
   static_assert(G >= 1 && G <= 8, "group size");
   constexpr int kThreads = F8 ? kTcThreadsF8 : kTcThreads;
+  constexpr uint32_t kTmemCols = F8 ? 256 : 64;
+  constexpr int kRing = F8 ? kRawSlots : kSlots;  // ring slots (K or V of one tile each)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 128-byte swizzled operands need 1024-byte aligned shared addresses.
   const uint32_t raw = smem_u32(smem_raw);
@@ -306,11 +325,19 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 2)
     mbar_init(&sm.p_full, 4);         // P^T written by the softmax warps
     mbar_init(&sm.p_free, 1);         // tcgen05.commit after the PV that read P^T
     for (int s = 0; s < kSlots; ++s) {
-      // bf16: the TMA transaction count; e4m3: the converter warps
-      mbar_init(&sm.full[s], F8 ? kConvWarps : 1);
+      mbar_init(&sm.full[s], 1);      // bf16: the TMA transaction count
       mbar_init(&sm.empty[s], 1);     // tcgen05.commit after the MMAs that read the slot
-      mbar_init(&sm.raw_full[s], 1);
     }
+    for (int s = 0; s < kRawSlots; ++s) {
+      mbar_init(&sm.raw_full[s], 1);           // e4m3: the TMA transaction count
+      mbar_init(&sm.raw_empty[s], kConvWarps); // e4m3: the converter warps have read it
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.kt_full[b], kConvWarps);   // e4m3: K tile widened into TMEM buffer b
+      mbar_init(&sm.kt_free[b], 1);            // tcgen05.commit after the S^T that read it
+    }
+    mbar_init(&sm.v_full, kConvWarps);         // e4m3: V operand widened
+    mbar_init(&sm.v_free, 1);                  // tcgen05.commit after the PV that read it
     mbar_init(&sm.mma_done, 1);
     sm.wait.abort = 0;
     sm.wait.limit_ns = p.wait_limit_ns;
@@ -415,7 +442,7 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 2)
           ent_nn = tt + 8 < ntile ? raw_entries(pc, (tt + 8) * kBlkPerTile) : kPastPiece;
         }
         // Before blocking on the consumers, or before a tile with a new token.
-        if (2 * t + 1 >= kSlots || pc.b0 + min(pc.nblk, (tt + 1) * kBlkPerTile) - 1 >= pc.fresh) {
+        if (2 * t + 1 >= kRing || pc.b0 + min(pc.nblk, (tt + 1) * kBlkPerTile) - 1 >= pc.fresh) {
           if (!waited || q_pend) take_wait();
         }
         // bf16: lanes 0..15 each copy one (block, d half) of the tile's K or V.
@@ -430,8 +457,9 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 2)
         #pragma unroll 1
         for (int kv = 0; kv < 2 && ok; ++kv) {
           const int n = 2 * t + kv;  // ring occupant: K (kv = 0) or V (kv = 1) of tile t
-          const int s = n % kSlots;
-          if (n >= kSlots && !mbar_wait(&sm.empty[s], ((n / kSlots) - 1) & 1, p.err, abort_flag)) {
+          const int s = n % kRing;
+          uint64_t* rel = F8 ? &sm.raw_empty[s] : &sm.empty[s];
+          if (n >= kRing && !mbar_wait(rel, ((n / kRing) - 1) & 1, p.err, abort_flag)) {
             ok = false;
             break;
           }
@@ -439,13 +467,19 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 2)
           if (lane == 0 && kv == 0) TC_TR(0, t);
           if (lane == 0 && t == 0 && kv == 0) TC_CTA(3);
           if (lane == 0) {
-            if (F8) mbar_arrive_expect_tx(&sm.raw_full[s], (uint32_t)kRawTile);
-            else mbar_arrive_expect_tx(&sm.full[s], 2u * kHalf);
+            if (F8) {
+              // rows of this tile holding keys before the request's end
+              const int key0 = (pc.b0 + tt * kBlkPerTile) * kBlockSize;
+              sm.raw_valid[s] = max(0, min(kTile, pc.L - key0));
+              mbar_arrive_expect_tx(&sm.raw_full[s], (uint32_t)kRawTile);
+            } else {
+              mbar_arrive_expect_tx(&sm.full[s], 2u * kHalf);
+            }
           }
           __syncwarp();
           const CUtensorMap* map = kv == 0 ? &kmap : &vmap;
           if (F8) {
-            if (lane < 8) tma_load_2d(sm.slot[s][1] + bsel * 2048, map, 0, row, &sm.raw_full[s], pol);
+            if (lane < 8) tma_load_2d(sm.f8.raw[s] + bsel * 2048, map, 0, row, &sm.raw_full[s], pol);
           } else if (lane < 16) {
             tma_load_2d(sm.slot[s][hsel] + bsel * 2048, map, hsel * 64, row, &sm.full[s], pol);
           }
@@ -517,9 +551,9 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 2)
       // Tell the converter warps that occupant n_occ does not exist:
       // completing the phase they wait on for it, once its slot's previous
       // occupant is done.
-      const int s = n_occ % kSlots;
-      if (n_occ < kSlots ||
-          mbar_wait(&sm.empty[s], ((n_occ / kSlots) - 1) & 1, p.err, abort_flag)) {
+      const int s = n_occ % kRawSlots;
+      if (n_occ < kRawSlots ||
+          mbar_wait(&sm.raw_empty[s], ((n_occ / kRawSlots) - 1) & 1, p.err, abort_flag)) {
         if (lane == 0) {
           *reinterpret_cast<volatile int*>(&sm.conv_end) = n_occ;
           mbar_arrive(&sm.raw_full[s]);
@@ -542,9 +576,9 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 2)
     if (abort_flag->abort) {
       // Copies still in flight must land before the CTA's shared memory is
       // released: the last occupant of each slot and the last Q of each buffer.
-      for (int m = max(0, n_occ - kSlots); m < n_occ; ++m) {
-        const int s = m % kSlots;
-        mbar_wait_drain(F8 ? &sm.raw_full[s] : &sm.full[s], (m / kSlots) & 1, p.err, abort_flag);
+      for (int m = max(0, n_occ - kRing); m < n_occ; ++m) {
+        const int s = m % kRing;
+        mbar_wait_drain(F8 ? &sm.raw_full[s] : &sm.full[s], (m / kRing) & 1, p.err, abort_flag);
       }
       for (int ub = 0; ub < 2; ++ub)
         if (q_armed[ub] > 0 && q_copy[ub])
@@ -565,7 +599,8 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 2)
         const int n = 2 * tt + 1, s = n % kSlots, ob = j & 1;
         const uint32_t tO = tmem + kColO + ob * kN;
         ok = ok && mbar_wait(&sm.p_full, tt & 1, p.err, abort_flag);
-        ok = ok && mbar_wait(&sm.full[s], (n / kSlots) & 1, p.err, abort_flag);
+        ok = ok && (F8 ? mbar_wait(&sm.v_full, tt & 1, p.err, abort_flag)
+                       : mbar_wait(&sm.full[s], (n / kSlots) & 1, p.err, abort_flag));
         // O^T buffer ob was last read by the epilogue of piece j - 2.
         if (first && j >= 2)
           ok = ok && mbar_wait(&sm.o_empty[ob], ((j >> 1) - 1) & 1, p.err, abort_flag);
@@ -577,11 +612,12 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 2)
         for (int kk = 0; kk < 8; ++kk) {
           // V^T is MN-major (d contiguous): atoms of 64 d x 8 keys, the two d
           // halves kHalf apart, 8-key groups 1024 bytes apart.
-          const uint64_t da = smem_desc_sw128(smem_u32(sm.slot[s][0]) + kk * 2048, kHalf, 1024);
+          const uint32_t va = F8 ? smem_u32(sm.f8.vbuf[0]) : smem_u32(sm.slot[s][0]);
+          const uint64_t da = smem_desc_sw128(va + kk * 2048, kHalf, 1024);
           const uint64_t db = smem_desc_sw128(smem_u32(sm.pt[kk >> 2]) + (kk & 3) * 32, 16, 1024);
           tc_mma_f16_ss(tO, da, db, kIdescO, !first || kk > 0);
         }
-        tc_commit(&sm.empty[s]);
+        tc_commit(F8 ? &sm.v_free : &sm.empty[s]);
         tc_commit(&sm.p_free);
 #if PKV_TC_TRACE >= 2
         mbar_wait(&sm.p_free, tt & 1, p.err, abort_flag);  // PV completion
@@ -602,7 +638,8 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 2)
           // The previous tile's PV first: its V slot is released as soon as
           // its probabilities are ready, not after this tile's keys arrive.
           if (tt >= 1) pv(t - 1, tt == 1, j);
-          ok = ok && mbar_wait(&sm.full[s], (n / kSlots) & 1, p.err, abort_flag);
+          ok = ok && (F8 ? mbar_wait(&sm.kt_full[t & 1], (t >> 1) & 1, p.err, abort_flag)
+                         : mbar_wait(&sm.full[s], (n / kSlots) & 1, p.err, abort_flag));
           TC_TR(1, t);
           if (t == 0) TC_CTA(4);
           if (t >= 2) ok = ok && mbar_wait(&sm.s_free[b], ((t >> 1) - 1) & 1, p.err, abort_flag);
@@ -611,13 +648,19 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 2)
           const uint32_t tS = tmem + b * kN;
           #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t da =
-                smem_desc_sw128(smem_u32(sm.slot[s][kk >> 2]) + (kk & 3) * 32, 16, 1024);
             const uint64_t db =
                 smem_desc_sw128(smem_u32(sm.q[ub][kk >> 2]) + (kk & 3) * 32, 16, 1024);
-            tc_mma_f16_ss(tS, da, db, kIdescS, kk > 0);
+            if (F8) {
+              // A = the widened K tile in TMEM: d 16kk .. 16kk+15 in columns 8kk .. 8kk+7
+              tc_mma_f16_ts(tS, tmem + kColK + (t & 1) * 64 + kk * 8, db, kIdescS, kk > 0);
+            } else {
+              const uint64_t da =
+                  smem_desc_sw128(smem_u32(sm.slot[s][kk >> 2]) + (kk & 3) * 32, 16, 1024);
+              tc_mma_f16_ss(tS, da, db, kIdescS, kk > 0);
+            }
           }
-          tc_commit(&sm.empty[s]);  // the K slot is free once S^T is computed
+          // the K slot (K buffer) is free once S^T is computed
+          tc_commit(F8 ? &sm.kt_free[t & 1] : &sm.empty[s]);
           tc_commit(&sm.s_full[b]);
 #if PKV_TC_TRACE >= 2
           mbar_wait(&sm.s_full[b], (t >> 1) & 1, p.err, abort_flag);  // QK completion
@@ -637,20 +680,66 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 2)
     }
     __syncwarp();
   } else if (F8 && warp >= kTcWarps) {
-    // ================= e4m3 converters (warps 6, 7) ======================
-    // Occupant by occupant, in the producer's order: widen the codes when
-    // they land and hand the slot to the MMA.  Each thread takes rows r and
-    // r + 64 of the 128-key tile.
-    const int r0 = tid - kTcThreads;  // 0 .. 63
-    for (int n = 0;; ++n) {
-      const int s = n % kSlots;
-      if (!mbar_wait(&sm.raw_full[s], (n / kSlots) & 1, p.err, abort_flag)) break;
-      if (n >= *reinterpret_cast<volatile int*>(&sm.conv_end)) break;
-      widen_e4m3_row(sm.slot[s][0], sm.slot[s][1], r0);
-      widen_e4m3_row(sm.slot[s][0], sm.slot[s][1], r0 + 64);
+    // ================= e4m3 converters (warps 6-9) =======================
+    // Occupant by occupant, in the producer's order: thread r widens key row
+    // r of the tile (its warp reaches TMEM lanes 32 (warp % 4) .. +31).  A K
+    // tile goes into TMEM buffer t & 1 once the S^T of tile t - 2 has read
+    // it; a V tile into the shared-memory operand once the PV of tile t - 1
+    // has read it.  The raw slot is released as soon as its codes are read.
+    const int r = (warp & 3) * 32 + lane;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    // K runs one tile ahead: K(0), then K(t + 1) and V(t) for t = 0, 1, ...,
+    // so that the S^T of the next tile never waits behind the widening of a
+    // V tile, which itself waits for the PV of the tile before.
+    auto convert_k = [&](int t) -> bool {
+      const int n = 2 * t, s = n % kRawSlots;
+      if (!mbar_wait(&sm.raw_full[s], (n / kRawSlots) & 1, p.err, abort_flag)) return false;
+      if (n >= *reinterpret_cast<volatile int*>(&sm.conv_end)) return false;
+      if (t >= 2 && !mbar_wait(&sm.kt_free[t & 1], ((t >> 1) - 1) & 1, p.err, abort_flag)) return false;
+      tc_fence_after();
+      const uint8_t* src = sm.f8.raw[s];
+      const uint32_t tk = tmem + lane_off + kColK + (t & 1) * 64;
+      #pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {  // d 64 hh .. 64 hh + 63: columns 32 hh .. +31
+        uint32_t w[32];
+        #pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int c8 = hh * 4 + c;
+          const uint4 v = lds128(src + r * 128 + ((c8 ^ (r & 7)) * 16));
+          const uint32_t x[4] = {v.x, v.y, v.z, v.w};
+          #pragma unroll
+          for (int i = 0; i < 4; ++i) e4m3x4_to_f16x4(x[i], w[c * 8 + 2 * i], w[c * 8 + 2 * i + 1]);
+        }
+        tmem_st32(tk + hh * 32, *reinterpret_cast<const float(*)[32]>(w));
+      }
+      tc_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&sm.raw_empty[s]);
+        mbar_arrive(&sm.kt_full[t & 1]);
+      }
+      return true;
+    };
+    auto convert_v = [&](int t) -> bool {
+      const int n = 2 * t + 1, s = n % kRawSlots;
+      if (!mbar_wait(&sm.raw_full[s], (n / kRawSlots) & 1, p.err, abort_flag)) return false;
+      if (n >= *reinterpret_cast<volatile int*>(&sm.conv_end)) return false;
+      if (t >= 1 && !mbar_wait(&sm.v_free, (t - 1) & 1, p.err, abort_flag)) return false;
+      widen_e4m3_row_to(sm.f8.raw[s], sm.f8.vbuf[0], sm.f8.vbuf[1], r, r >= sm.raw_valid[s]);
       fence_proxy_async_smem();  // generic-proxy writes, read by the tensor core
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.full[s]);
+      if (lane == 0) {
+        mbar_arrive(&sm.raw_empty[s]);
+        mbar_arrive(&sm.v_full);
+      }
+      return true;
+    };
+    if (convert_k(0)) {
+      for (int t = 0;; ++t) {
+        const bool more = convert_k(t + 1);  // false past the last tile (or on abort)
+        if (!convert_v(t) || !more) break;
+      }
     }
   } else if (warp < 4) {
     // ================ softmax + epilogue (warps 0-3) ======================
@@ -775,7 +864,7 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 2)
         }
         // Keys past the request's end inside its last block may hold anything
         // (even NaN): zero those V rows so that 0 * V stays 0 in the MMA.
-        if (x < pc.nblk && pos >= pc.L) {
+        if (!F8 && x < pc.nblk && pos >= pc.L) {
           const int n = 2 * t + 1, sv = n % kSlots;
           ok = ok && mbar_wait(&sm.full[sv], (n / kSlots) & 1, p.err, abort_flag);
           #pragma unroll
