@@ -209,8 +209,12 @@ __device__ __forceinline__ void widen_e4m3_row_to(const uint8_t* raw, uint8_t* h
 // F8: the pools hold e4m3 codes (kmap / vmap are maps of bytes); K tiles are
 // widened into TMEM and V tiles into shared memory, the key scale joins the
 // softmax scale and the value scale multiplies the output.
+// Registers: bf16 pools cap them at 152 per thread, so that two CTAs (the
+// running launch's and the next's) and one CTA of the KV append (8 warps of
+// at most 24 registers) fit an SM's 65,536 together; e4m3 pools (320
+// threads) take the two-CTA share, 96.
 template <int G, bool F8>
-__global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 2)
+__global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 2) __maxnreg__(F8 ? 96 : 152)
     decode_tc_kernel(const __grid_constant__ CUtensorMap qmap,
                      const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
