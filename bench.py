@@ -75,6 +75,15 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def measured_tensor_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
 def decode_source_sha() -> str:
     """Hash of the decode kernels' code: the sources with // comments and
     blank lines removed, so that edits to comments keep a profile valid."""
@@ -471,6 +480,15 @@ def measure_extra(pkv, config, kv, device, rank, args, local):
     flops = rl.attention_flops(shape.seq_lens, shape.q_lens, shape.num_q_heads)
     if shape.num_q_tokens > shape.num_reqs:
         rec["attention_tflops_per_layer_call"] = round(flops / 1e12, 4)
+    if int((shape.q_lens > 1).sum()) == shape.num_reqs:
+        # every request is a prefill chunk: the tensor-core roofline (a
+        # contraction timed alone takes the burst bf16 peak)
+        tpk, tsrc = measured_tensor_peak()
+        ach = flops / (statistics.mean(durs) * 1e-3) / 1e12
+        rec["tensor_roofline"] = {"bound": "tensor", "achieved": round(ach, 1), "peak": tpk,
+                                  "unit": "TFLOP/s", "frac": round(ach / tpk, 4),
+                                  "peak_source": tsrc,
+                                  "flops_per_launch": flops}
     del run
     torch.cuda.empty_cache()
     return rec

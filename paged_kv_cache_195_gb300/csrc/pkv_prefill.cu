@@ -19,12 +19,14 @@
 // fills with zeros.  Q comes in with one 3-D TMA copy per half (d, head,
 // token).
 //
-// Roles (352 threads): eight softmax warps -- warps 0-3 and 6-9, two threads
-// per TMEM lane / MMA row, each taking half of the row's keys and output
-// dims -- run the softmax and the epilogue; warp 4 takes items from a work
-// queue in the workspace and issues the Q and K copies, warp 10 the V copies
-// of the items warp 4 hands it; one thread of warp 5 issues tcgen05.mma and
-// commits.
+// Roles (608 threads): sixteen softmax warps -- warps 0-15, four threads
+// per TMEM lane / MMA row, each taking a quarter of the row's keys and of
+// its output dims -- run the softmax and the epilogue; warp 16 takes items
+// from a work queue in the workspace and issues the Q and K copies, warp 18
+// the V copies of the items warp 16 hands it; one thread of warp 17 issues
+// tcgen05.mma and commits.  Four threads per row (rather than two) halve each
+// thread's serial chain of exponentials per tile and double the warps that
+// hide its latencies: the softmax, not the tensor core, sets the pace.
 // Per key tile: S = Q K^T (8 MMAs of K=16) into TMEM, the softmax reads S and
 // writes P (bf16, two keys per column) over it, then O += P V (8 MMAs, A read
 // from TMEM) accumulates in TMEM.  K and V have rings of their own: a K stage
@@ -40,9 +42,16 @@
 namespace pkv {
 namespace {
 
-constexpr int kPfThreads = 352;          // 11 warps
-constexpr int kSoftThreads = 256;        // softmax warps 0-3 and 6-9
-constexpr int kBarSoftmax = 1;           // their named barrier
+constexpr int kParts = 4;                // softmax threads per MMA row
+constexpr int kPartKeys = 128 / kParts;  // keys (and output dims) per softmax thread
+constexpr int kSoftWarps = 4 * kParts;   // warps 0 .. 15
+constexpr int kSoftThreads = 32 * kSoftWarps;
+constexpr int kWarpQK = kSoftWarps;      // Q + K producer (takes the items)
+constexpr int kWarpMma = kSoftWarps + 1; // MMA issuer
+constexpr int kWarpV = kSoftWarps + 2;   // V producer
+constexpr int kPfThreads = 32 * (kSoftWarps + 3);
+constexpr int kBarSoftmax = 1;           // the softmax warps' named barrier
+constexpr int kBarQuad = 2;              // + quad: the four warps holding the same 32 rows
 constexpr int kTileRows = 128;               // MMA M
 constexpr int kKeyTile = 128;                // MMA N for S, K for PV
 constexpr int kHalfBytes = kTileRows * 128;  // one 64-column half of a 128-row tile
@@ -51,13 +60,15 @@ constexpr float kRescaleLog2 = 8.0f;
 constexpr float kNegBig = -1.0e30f;
 // Debug-only per-tile timeline of CTA 0 (build with -DPKV_PF_TRACE=1):
 // %globaltimer at load issue, keys seen by the MMA warp, scores seen by the
-// softmax, probabilities ready (PV issue), stage released to the producer.
+// softmax, probabilities ready (PV issue), stage released to the producer;
+// then, for the softmax thread of row 0, key part 0: scores in registers,
+// vote done, exponentials done, P stored in TMEM, arrival.
 #ifndef PKV_PF_TRACE
 #define PKV_PF_TRACE 0
 #endif
 #if PKV_PF_TRACE
 constexpr int kPfTrTiles = 64;
-__device__ unsigned long long g_pf_trace[5][kPfTrTiles];
+__device__ unsigned long long g_pf_trace[10][kPfTrTiles];
 #define PF_TR(ev, tile) do { if (blockIdx.x == 0 && (tile) < kPfTrTiles) g_pf_trace[ev][tile] = global_timer_ns(); } while (0)
 #else
 #define PF_TR(ev, tile) do { } while (0)
@@ -77,18 +88,22 @@ struct Item {
   int end;    // no more items
 };
 
-constexpr int kPfStages = 3;  // K/V tile stages (64 KiB each)
+// K and V tile stages (32 KiB each).  A V tile is needed only after its
+// tile's softmax, so its ring can be one stage shorter than K's; the room
+// holds the softmax threads' row exchange.
+constexpr int kPfStagesK = 3;
+constexpr int kPfStagesV = 2;
 
 struct __align__(1024) PfSmem {
   uint8_t q[2][kHalfBytes];              // Q: d 0..63 | d 64..127
-  uint8_t k[kPfStages][2][kHalfBytes];   // [stage][d half]
-  uint8_t v[kPfStages][2][kHalfBytes];   // [stage][d half]
+  uint8_t k[kPfStagesK][2][kHalfBytes];  // [stage][d half]
+  uint8_t v[kPfStagesV][2][kHalfBytes];  // [stage][d half]
   uint64_t q_full, q_empty;
-  uint64_t k_full[kPfStages], v_full[kPfStages], k_empty[kPfStages], v_empty[kPfStages];
+  uint64_t k_full[kPfStagesK], v_full[kPfStagesV], k_empty[kPfStagesK], v_empty[kPfStagesV];
   uint64_t s_full[2], p_full[2], p_free[2];
   uint64_t o_full, o_empty;
   Item items[2];
-  float xrow[2][kTileRows];      // [key half][row]: half-row maxima, then normalisers
+  float xrow[kParts][kTileRows]; // [key part][row]: partial row maxima, then normalisers
   Item vitems[4];                // items handed from the K producer to the V producer
   uint64_t vitem_full[4], vitem_empty[4];
   uint32_t tmem_base;
@@ -194,19 +209,21 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   if (tid == 0) {
     mbar_init(&sm.q_full, 1);
     mbar_init(&sm.q_empty, 1);
-    for (int s = 0; s < kPfStages; ++s) {
+    for (int s = 0; s < kPfStagesK; ++s) {
       mbar_init(&sm.k_full[s], 1);
-      mbar_init(&sm.v_full[s], 1);
       mbar_init(&sm.k_empty[s], 1);
+    }
+    for (int s = 0; s < kPfStagesV; ++s) {
+      mbar_init(&sm.v_full[s], 1);
       mbar_init(&sm.v_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.s_full[b], 1);   // tcgen05.commit after S = QK^T into buffer b
-      mbar_init(&sm.p_full[b], 8);   // P written over S buffer b (and O rescaled) by all eight
+      mbar_init(&sm.p_full[b], kSoftWarps);  // P written over S buffer b (and O rescaled)
       mbar_init(&sm.p_free[b], 1);   // tcgen05.commit after the PV that read P in buffer b
     }
     mbar_init(&sm.o_full, 1);
-    mbar_init(&sm.o_empty, 8);
+    mbar_init(&sm.o_empty, kSoftWarps);
     for (int b = 0; b < 4; ++b) {
       mbar_init(&sm.vitem_full[b], 1);
       mbar_init(&sm.vitem_empty[b], 1);
@@ -215,7 +232,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     sm.wait.limit_ns = p.wait_limit_ns;
     fence_barrier_init();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == kWarpQK && lane == 0) {
     prefetch_tensormap(&qmap);
     prefetch_tensormap(&kmap);
     prefetch_tensormap(&vmap);
@@ -232,7 +249,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
     fence_proxy_async_smem();
   }
-  if (warp == 5) {
+  if (warp == kWarpMma) {
     tmem_alloc(&sm.tmem_base, kTmemCols);
     tmem_relinquish();
   }
@@ -242,11 +259,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const uint32_t tmem = sm.tmem_base;
   allow_dependent_launch();
 
-  if (warp == 4 || warp == 10) {
+  if (warp == kWarpQK || warp == kWarpV) {
     // ==================== TMA producers (K + Q | V) =======================
-    // Warp 4 takes items from the work queue, streams their K tiles and Q,
-    // and hands each item to warp 10, which streams the V tiles.
-    const bool vside = warp == 10;
+    // Warp 16 takes items from the work queue, streams their K tiles and Q,
+    // and hands each item to warp 18, which streams the V tiles.
+    const bool vside = warp == kWarpV;
     uint64_t* const full = vside ? sm.v_full : sm.k_full;
     uint64_t* const empty = vside ? sm.v_empty : sm.k_empty;
     const CUtensorMap* const map = vside ? &vmap : &kmap;
@@ -269,11 +286,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           ent_cur = ent_nxt;
           if (j + 4 < it.nj) ent_nxt = raw_entries((j + 4) * 8);
         }
-        const int st = tile_ctr % kPfStages;
-        if (tile_ctr >= kPfStages &&
-            !mbar_wait(&empty[st], ((tile_ctr / kPfStages) - 1) & 1, p.err, abort_flag))
+        const int stages = vside ? kPfStagesV : kPfStagesK;
+        const int st = tile_ctr % stages;
+        if (tile_ctr >= stages &&
+            !mbar_wait(&empty[st], ((tile_ctr / stages) - 1) & 1, p.err, abort_flag))
           return false;
-        if (lane == 0 && vside && tile_ctr >= kPfStages) PF_TR(4, tile_ctr - kPfStages);
+        if (lane == 0 && vside && tile_ctr >= stages) PF_TR(4, tile_ctr - stages);
         if (lane == 0 && !vside) PF_TR(0, tile_ctr);
         if (lane == 0) mbar_arrive_expect_tx(&full[st], 2u * kHalfBytes);
         __syncwarp();
@@ -397,7 +415,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kWarpMma) {
     // ========================= MMA issuer =================================
     // Tile t: S(t) = Q K(t)^T into S buffer t&1, then O += P(t-1) V(t-1).  S
     // of the next tile therefore runs on the tensor core while the softmax
@@ -409,9 +427,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       int t = 0;  // tile counter, shared sequence with the producer and softmax
       bool ok = true;
       auto pv = [&](int tt, bool first, int n_item) {
-        const int b = tt & 1, st = tt % kPfStages;
+        const int b = tt & 1, st = tt % kPfStagesV;
         ok = ok && mbar_wait(&sm.p_full[b], (tt >> 1) & 1, p.err, abort_flag);
-        ok = ok && mbar_wait(&sm.v_full[st], (tt / kPfStages) & 1, p.err, abort_flag);
+        ok = ok && mbar_wait(&sm.v_full[st], (tt / kPfStagesV) & 1, p.err, abort_flag);
         if (first && n_item > 0)
           ok = ok && mbar_wait(&sm.o_empty, (n_item - 1) & 1, p.err, abort_flag);
         PF_TR(3, tt);
@@ -435,8 +453,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         if (it.end) break;
         tc_fence_after();
         for (int j = 0; j < it.nj && ok; ++j, ++t) {
-          const int b = t & 1, st = t % kPfStages;
-          ok = ok && mbar_wait(&sm.k_full[st], (t / kPfStages) & 1, p.err, abort_flag);
+          const int b = t & 1, st = t % kPfStagesK;
+          ok = ok && mbar_wait(&sm.k_full[st], (t / kPfStagesK) & 1, p.err, abort_flag);
           PF_TR(1, t);
           // S buffer b holds P(t - 2) until the PV of tile t - 2 has read it.
           if (t >= 2) ok = ok && mbar_wait(&sm.p_free[b], ((t >> 1) - 1) & 1, p.err, abort_flag);
@@ -458,18 +476,18 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
     }
     __syncwarp();
-  } else {
-    // ============= softmax + epilogue (warps 0-3 and 6-9) ===================
-    // Two threads share each MMA row: warps 0-3 take keys 0..63 of a tile and
-    // output dims 0..63, warps 6-9 keys 64..127 and dims 64..127.  Warp w
-    // reaches TMEM lanes 32 (w % 4) .. +31, so warps with equal w % 4 hold the
-    // same 32 rows.  The two halves agree on the row maximum through shared
-    // memory once per tile.
+  } else if (warp < kSoftWarps) {
+    // =================== softmax + epilogue (warps 0-15) =====================
+    // Four threads share each MMA row: warps 4c .. 4c+3 take keys 32c .. 32c+31
+    // of a tile and output dims 32c .. 32c+31.  Warp w reaches TMEM lanes
+    // 32 (w % 4) .. +31, so the four warps with equal w % 4 hold the same 32
+    // rows.  The four parts agree on the row maximum through shared memory
+    // once per tile.
     const int quad = warp & 3;
-    const int half = warp < 4 ? 0 : 1;
+    const int part = warp >> 2;
     const int row = quad * 32 + lane;  // MMA row == TMEM lane
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    const uint32_t tO = tmem + lane_off + 2 * kKeyTile + half * 64;
+    const uint32_t tO = tmem + lane_off + 2 * kKeyTile + part * kPartKeys;
     const int t_local = row / G, h = row % G;
     int tile_ctr = 0;
     for (int n_item = 0;; ++n_item) {
@@ -486,40 +504,48 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const int sb = tile_ctr & 1;  // S / P buffer of this tile
         const uint32_t tS = tmem + lane_off + sb * kKeyTile;
         ok = ok && mbar_wait(&sm.s_full[sb], (tile_ctr >> 1) & 1, p.err, abort_flag);
-        if (row == 0 && half == 0) PF_TR(2, tile_ctr);
+        if (row == 0 && part == 0) PF_TR(2, tile_ctr);
         tc_fence_after();
-        // This half's 64 scores, read from TMEM once, and their maximum over
+        // This part's 32 scores, read from TMEM once, and their maximum over
         // the visible keys.
-        const int kbase = (it.kt0 + j) * kKeyTile + half * 64;
-        const bool full_half = kbase + 63 <= prow;  // no key of this half masked
-        float v[64];
-        tmem_ld32(tS + half * 64, *reinterpret_cast<float(*)[32]>(v));
-        tmem_ld32(tS + half * 64 + 32, *reinterpret_cast<float(*)[32]>(v + 32));
+        const int kbase = (it.kt0 + j) * kKeyTile + part * kPartKeys;
+        const bool full_part = kbase + kPartKeys - 1 <= prow;  // no key of this part masked
+        float v[kPartKeys];
+        tmem_ld32(tS + part * kPartKeys, v);
         tc_wait_ld();
-        if (!full_half) {
+        if (row == 0 && part == 0) PF_TR(5, tile_ctr);
+        if (!full_part) {
           #pragma unroll
-          for (int i = 0; i < 64; ++i)
+          for (int i = 0; i < kPartKeys; ++i)
             if (kbase + i > prow) v[i] = -INFINITY;
         }
-        float mxp[8];
+        float mxp[4];
         #pragma unroll
-        for (int i = 0; i < 8; ++i) mxp[i] = -INFINITY;
+        for (int i = 0; i < 4; ++i) mxp[i] = -INFINITY;
         #pragma unroll
-        for (int i = 0; i < 32; ++i) mxp[i & 7] = fmax3(mxp[i & 7], v[2 * i], v[2 * i + 1]);
-        const float mxh = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
-                                fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
-        // The row maximum over both halves.  The barrier also orders every
-        // thread's S reads before any P write (P of half 1 lands in TMEM
-        // columns that held half 0's scores).
-        sm.xrow[half][row] = mxh;
+        for (int i = 0; i < kPartKeys / 2; ++i) mxp[i & 3] = fmax3(mxp[i & 3], v[2 * i], v[2 * i + 1]);
+        const float mxh = fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])) * p.scale_log2;
+        // Past an item's first tile the row maximum is needed only when some
+        // part's scores exceed the reference by more than 2^8: a vote of the
+        // four warps that hold these rows decides, and only then do the parts
+        // exchange their maxima.  The vote (a barrier of those warps) also
+        // orders their S reads before any P write (P of part c lands in TMEM
+        // columns that held the scores of keys 16c .. 16c + 15, of the same
+        // rows).  Each group of rows keeps its own pace: the PV waits for all.
         tc_fence_before();
-        named_barrier(kBarSoftmax, kSoftThreads);
+        const bool exchange = barrier_or(kBarQuad + quad, 128, j == 0 || mxh > m + kRescaleLog2);
         tc_fence_after();
-        float mx = fmaxf(mxh, sm.xrow[half ^ 1][row]);
-        named_barrier(kBarSoftmax, kSoftThreads);  // sm.xrow is free again
-        mx = mx * p.scale_log2;  // scale > 0 keeps the arg max
+        if (row == 0 && part == 0) PF_TR(6, tile_ctr);
+        float mx = mxh;
+        if (exchange) {
+          sm.xrow[part][row] = mxh;
+          named_barrier(kBarQuad + quad, 128);
+          mx = fmaxf(fmaxf(sm.xrow[0][row], sm.xrow[1][row]),
+                     fmaxf(sm.xrow[2][row], sm.xrow[3][row]));
+          named_barrier(kBarQuad + quad, 128);  // sm.xrow is free again
+        }
         float m_use = m;
-        const bool grow = j == 0 ? true : (mx > m + kRescaleLog2);
+        const bool grow = exchange && (j == 0 || mx > m + kRescaleLog2);
         if (j == 0) {
           m_use = fmaxf(m, mx);
         } else if (__any_sync(0xffffffffu, grow)) {
@@ -530,15 +556,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           tc_fence_after();
           const float m_new = grow ? fmaxf(m, mx) : m;
           const float alpha = fast_exp2(m - m_new);
-          #pragma unroll 1
-          for (int c = 0; c < 2; ++c) {
-            float o[32];
-            tmem_ld32(tO + c * 32, o);
-            tc_wait_ld();
-            #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] *= alpha;
-            tmem_st32(tO + c * 32, o);
-          }
+          float o[32];
+          tmem_ld32(tO, o);
+          tc_wait_ld();
+          #pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] *= alpha;
+          tmem_st32(tO, o);
           tc_wait_st();
           l *= alpha;
           m_use = m_new;
@@ -546,67 +569,68 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         m = m_use;
         // P = exp2(s * scale_log2 - m) in bf16 (masked keys are -inf: p = 0),
         // written over the row's S in TMEM two keys per column -- keys
-        // 64 half .. +63 in columns 32 half .. +31 -- where the PV MMA reads
+        // 32 part .. +31 in columns 16 part .. +15 -- where the PV MMA reads
         // it; the normaliser sums the rounded values the MMA will use.  Pairs
-        // of keys go through packed fp32 arithmetic (the softmax is bound by
-        // its instruction count).
+        // of keys go through packed fp32 arithmetic.
         const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
         const float2 nm2 = make_float2(-m, -m);
         float sum_lo[2] = {0.f, 0.f}, sum_hi[2] = {0.f, 0.f};
-        uint32_t w[32];
+        uint32_t w[kPartKeys / 2];
         #pragma unroll
-        for (int e = 0; e < 32; ++e) {
+        for (int e = 0; e < kPartKeys / 2; ++e) {
           const float2 x = ffma2(make_float2(v[2 * e], v[2 * e + 1]), sc2, nm2);
           w[e] = pack_bf16x2(fast_exp2(x.x), fast_exp2(x.y));
           add_bf16x2(sum_lo[e & 1], sum_hi[e & 1], w[e]);
         }
-        tmem_st32(tS + half * 32, *reinterpret_cast<const float(*)[32]>(w));
+        if (row == 0 && part == 0) PF_TR(7, tile_ctr);
+        tmem_st16(tS + part * (kPartKeys / 2), w);
         tc_wait_st();
+        if (row == 0 && part == 0) PF_TR(8, tile_ctr);
         l += (sum_lo[0] + sum_hi[0]) + (sum_lo[1] + sum_hi[1]);
         // Keys past the request's end inside its last block may hold anything
         // (even NaN); zero those V rows so that 0 * V stays 0 in the MMA.
-        const int st = tile_ctr % kPfStages;
+        const int st = tile_ctr % kPfStagesV;
         const int tbase = (it.kt0 + j) * kKeyTile;
         const int tail0 = it.L - tbase;                      // first key >= L in this tile
         const int tail1 = min(kKeyTile, ceil_div(it.L, kBlockSize) * kBlockSize - tbase);
         if (warp == 0 && tail0 < tail1 && tail0 >= 0) {
-          ok = ok && mbar_wait(&sm.v_full[st], (tile_ctr / kPfStages) & 1, p.err, abort_flag);
+          ok = ok && mbar_wait(&sm.v_full[st], (tile_ctr / kPfStagesV) & 1, p.err, abort_flag);
           const int nrows = tail1 - tail0;
           for (int i = lane; i < nrows * 16; i += 32) {
             const int rr = tail0 + i / 16, hf = (i / 8) & 1, chunk = i & 7;
             *reinterpret_cast<uint4*>(sm.v[st][hf] + (rr >> 3) * 1024 + (rr & 7) * 128 +
                                       chunk * 16) = make_uint4(0, 0, 0, 0);
           }
+          fence_proxy_async_smem();  // the zeros, read by the tensor core
         }
-        fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.p_full[sb]);
+        if (row == 0 && part == 0) PF_TR(9, tile_ctr);
       }
-      // ---- epilogue: O / l -> bf16 -> out (this half's 64 dims) ----------
-      sm.xrow[half][row] = l;
-      named_barrier(kBarSoftmax, kSoftThreads);
-      const float lrow = l + sm.xrow[half ^ 1][row];
-      named_barrier(kBarSoftmax, kSoftThreads);  // sm.xrow is free again
+      // ---- epilogue: O / l -> bf16 -> out (this part's 32 dims) ----------
+      sm.xrow[part][row] = l;
+      named_barrier(kBarQuad + quad, 128);
+      const float lrow = (sm.xrow[0][row] + sm.xrow[1][row]) + (sm.xrow[2][row] + sm.xrow[3][row]);
+      named_barrier(kBarQuad + quad, 128);  // sm.xrow is free again
       ok = ok && mbar_wait(&sm.o_full, n_item & 1, p.err, abort_flag);
       tc_fence_after();
       const float inv = lrow > 0.f ? 1.f / lrow : 0.f;
       const long long orow = (long long)(it.row0 + t_local) * p.num_q_heads + (long long)it.k * G + h;
-      __nv_bfloat16* dst = p.out + orow * kHeadDim + half * 64;
+      __nv_bfloat16* dst = p.out + orow * kHeadDim + part * kPartKeys;
       // Prefix pass: the partial state of this key chunk.
       const long long prow_slot = (long long)it.kc * p.num_q_tokens * p.num_q_heads + orow;
-      float* pdst = p.pre_o + prow_slot * kHeadDim + half * 64;
-      if (p.prefix_mode && valid && ok && half == 0)
+      float* pdst = p.pre_o + prow_slot * kHeadDim + part * kPartKeys;
+      if (p.prefix_mode && valid && ok && part == 0)
         *reinterpret_cast<float2*>(p.pre_ml + prow_slot * 2) = make_float2(m, lrow);
-      #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      {
         float o[32];
-        tmem_ld32(tO + c * 32, o);
+        tmem_ld32(tO, o);
         tc_wait_ld();
         if (valid && ok && p.prefix_mode) {
           #pragma unroll
           for (int i = 0; i < 32; i += 4)
-            *reinterpret_cast<float4*>(pdst + c * 32 + i) =
+            *reinterpret_cast<float4*>(pdst + i) =
                 make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv);
         } else if (valid && ok) {
           #pragma unroll
@@ -616,7 +640,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             q4.y = pack_bf16x2(o[i + 2] * inv, o[i + 3] * inv);
             q4.z = pack_bf16x2(o[i + 4] * inv, o[i + 5] * inv);
             q4.w = pack_bf16x2(o[i + 6] * inv, o[i + 7] * inv);
-            *reinterpret_cast<uint4*>(dst + c * 32 + i) = q4;
+            *reinterpret_cast<uint4*>(dst + i) = q4;
           }
         }
       }
@@ -630,7 +654,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 5) tmem_dealloc(tmem, kTmemCols);
+  if (warp == kWarpMma) tmem_dealloc(tmem, kTmemCols);
   grid_dependency_wait();
   // The last CTA to finish empties the work queue for the next launch (each
   // CTA stops taking items before it gets here).
@@ -643,6 +667,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
   }
 }
+
+static_assert(sizeof(PfSmem) + 1024 <= 227 * 1024, "prefill shared memory");
 
 template <int G>
 cudaError_t launch_prefill_g(const PrefillLaunch& L, cudaStream_t stream) {

@@ -161,6 +161,7 @@ CONFIGS = {
     "qwen_long": qwen_long_batch,
     "llama_mixed": llama_mixed,
     "llama_long": llama_long_context,
+    "llama_prefill": lambda: llama_mixed(num_decode=0),
     "qwen_shared": qwen_shared_prefix,
     "qwen_shared_long": qwen_shared_long,
 }
