@@ -239,8 +239,9 @@ def workload_config(shape, ws_n, kv="bf16"):
               f"{2 * shape.layers * shape.num_blocks * shape.num_kv_heads * 2048 * kvb / 1e9:.2f}"
               " GB per step",
         "launch": f"CUDA graph of {shape.layers} x (append + attention)"
-                  + ("" if kv == "fp8" or shape.prefix_groups else
-                     ", pkv_append_attention with early_trigger"),
+                  + ("" if shape.prefix_groups else
+                     f", {'pkv_append_attention_fp8' if kv == 'fp8' else 'pkv_append_attention'}"
+                     " with early_trigger"),
         **({"shared_prefix": [{"first_request": int(f), "members": int(m), "blocks": int(b)}
                               for f, m, b in shape.prefix_groups],
             "attention_call": "pkv_attention_cascade"} if shape.prefix_groups else {}),
@@ -336,9 +337,10 @@ class ConfigRun:
         pkv = self.pkv
         for li, x in enumerate(self.step_layers):
             if self.fp8:
-                pkv.pkv_append_fp8(x.k_new, x.v_new, x.slot_mapping, x.k_pool, x.v_pool,
-                                   x.k_scale, x.v_scale)
-                self.attention(li)
+                pkv.pkv_append_attention_fp8(x.k_new, x.v_new, x.slot_mapping, x.k_pool,
+                                             x.v_pool, x.k_scale, x.v_scale, x.q,
+                                             x.block_tables, x.seq_lens, x.query_start_loc,
+                                             x.scale, out=self.outs[li], workspace=self.ws)
             elif self.cascade:
                 pkv.pkv_append(x.k_new, x.v_new, x.slot_mapping, x.k_pool, x.v_pool)
                 self.attention(li)

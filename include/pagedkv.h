@@ -240,6 +240,25 @@ int pkv_attention_fp8kv(const void *q, const void *k_pool, const void *v_pool,
                         cudaStream_t stream);
 
 /*
+ * One layer of an engine step over e4m3 pools: pkv_append_fp8 of this step's
+ * dims->num_q_tokens new tokens, then pkv_attention_fp8kv over the updated
+ * pools -- the same results as the two calls in that order, with the same
+ * arguments, preconditions and errors, and the slot-mapping precondition of
+ * pkv_append_attention (slot_mapping[t] for t = query_start_loc[r] + i is
+ * negative or the slot of position L_r - q_r + i of request r), under which
+ * the attention streams the tiles holding only earlier positions before the
+ * append finishes (pkv_options.early_kv, .early_trigger as there).
+ * Source: as pkv_append_attention; The Serving Playbook, "Quantized serving".
+ */
+int pkv_append_attention_fp8(const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                             void *k_pool, void *v_pool, const float *k_scale,
+                             const float *v_scale, const void *q,
+                             const int32_t *block_tables, const int32_t *seq_lens,
+                             const int32_t *query_start_loc, float scale, void *out,
+                             const pkv_dims *dims, void *workspace, size_t workspace_bytes,
+                             cudaStream_t stream);
+
+/*
  * Bytes of workspace pkv_attention_cascade needs for these dims: the
  * pkv_attention workspace (same head, initialised the same way with
  * pkv_workspace_init), plus partial states for up to 8 chunks of each shared

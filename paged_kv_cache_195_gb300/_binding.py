@@ -30,7 +30,8 @@ EXPORTED = ("pkv_append", "pkv_attention", "pkv_attention_workspace_size",
             "pkv_workspace_init", "pkv_last_error", "pkv_get_device_error",
             "pkv_attention_noalloc", "pkv_copy_blocks", "pkv_append_fp8",
             "pkv_attention_fp8kv", "pkv_cascade_workspace_size", "pkv_attention_cascade",
-            "pkv_append_attention", "pkv_get_options", "pkv_set_options")
+            "pkv_append_attention", "pkv_append_attention_fp8", "pkv_get_options",
+            "pkv_set_options")
 
 # Fields of pkv_options, in declaration order (int32 each).
 OPTION_FIELDS = ("pdl", "early_plan", "early_kv", "early_trigger", "plan_cache", "decode_tc",
@@ -101,6 +102,9 @@ def load_library(path: str = LIB_PATH):
         lib.pkv_append_attention.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float,
                                              vp, dp, vp, sz, vp]
         lib.pkv_append_attention.restype = ctypes.c_int
+        lib.pkv_append_attention_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                                 ctypes.c_float, vp, dp, vp, sz, vp]
+        lib.pkv_append_attention_fp8.restype = ctypes.c_int
         lib.pkv_get_options.argtypes = [ctypes.POINTER(Options)]
         lib.pkv_get_options.restype = None
         lib.pkv_set_options.argtypes = [ctypes.POINTER(Options)]
@@ -374,6 +378,50 @@ def pkv_attention_fp8kv(q, k_pool, v_pool, k_scale, v_scale, block_tables, seq_l
         ctypes.c_void_p(seq_lens.data_ptr()), ctypes.c_void_p(query_start_loc.data_ptr()),
         ctypes.c_float(scale), ctypes.c_void_p(out.data_ptr()), ctypes.byref(dims),
         ctypes.c_void_p(ws_ptr), ws_bytes, ctypes.c_void_p(_stream(stream, q.device))))
+    return out
+
+
+def pkv_append_attention_fp8(k_new, v_new, slot_mapping, k_pool, v_pool, k_scale, v_scale, q,
+                             block_tables, seq_lens, query_start_loc, scale, out=None,
+                             workspace: Workspace | None = None, stream=None):
+    """One layer of an engine step over e4m3 pools: quantise and append the
+    step's new K/V rows (one per query token), then attend; returns out
+    [Tq, Hq, D] bf16."""
+    _need(k_new, "k_new", torch.bfloat16, 3)
+    _need(v_new, "v_new", torch.bfloat16, 3)
+    _need(slot_mapping, "slot_mapping", torch.int64, 1)
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_pool, "k_pool", torch.uint8, 4)
+    _need(v_pool, "v_pool", torch.uint8, 4)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    _need(query_start_loc, "query_start_loc", torch.int32, 1)
+    T = q.shape[0]
+    if k_new.shape[0] != T or v_new.shape != k_new.shape or slot_mapping.shape[0] != T:
+        raise ValueError("k_new, v_new and slot_mapping need one row per query token")
+    if k_pool.shape[1] != k_new.shape[1] or k_pool.shape[3] != k_new.shape[2]:
+        raise ValueError("pool / new rows shape mismatch")
+    R = check_attention_shapes(q, k_pool, v_pool, block_tables, seq_lens, query_start_loc)
+    _need_scales(k_scale, v_scale, k_pool.shape[1])
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need(out, "out", torch.bfloat16, 3)
+        if out.shape != q.shape:
+            raise ValueError("out must have q's shape")
+    dims = make_dims(tuple(q.shape), tuple(k_pool.shape), R, block_tables.shape[1])
+    if workspace is not None and workspace.counter_dims != (dims.num_q_tokens, dims.num_kv_heads):
+        pkv_workspace_init(workspace, dims, stream)
+    ws_ptr, ws_bytes = (None, 0) if workspace is None else (workspace.ptr, workspace.nbytes)
+    _check(load_library().pkv_append_attention_fp8(
+        ctypes.c_void_p(k_new.data_ptr()), ctypes.c_void_p(v_new.data_ptr()),
+        ctypes.c_void_p(slot_mapping.data_ptr()), ctypes.c_void_p(k_pool.data_ptr()),
+        ctypes.c_void_p(v_pool.data_ptr()), ctypes.c_void_p(k_scale.data_ptr()),
+        ctypes.c_void_p(v_scale.data_ptr()), ctypes.c_void_p(q.data_ptr()),
+        ctypes.c_void_p(block_tables.data_ptr()), ctypes.c_void_p(seq_lens.data_ptr()),
+        ctypes.c_void_p(query_start_loc.data_ptr()), ctypes.c_float(scale),
+        ctypes.c_void_p(out.data_ptr()), ctypes.byref(dims), ctypes.c_void_p(ws_ptr), ws_bytes,
+        ctypes.c_void_p(_stream(stream, q.device))))
     return out
 
 

@@ -287,21 +287,10 @@ int append_impl(const void* k_new, const void* v_new, const int64_t* slot_mappin
   return PKV_OK;
 }
 
-}  // namespace
-
-extern "C" {
-
-const char* pkv_last_error(void) { return g_last_error; }
-
-int pkv_append(const void* k_new, const void* v_new, const int64_t* slot_mapping, void* k_pool,
-               void* v_pool, int32_t num_new_tokens, const pkv_dims* dims, cudaStream_t stream) {
-  return append_impl(k_new, v_new, slot_mapping, k_pool, v_pool, num_new_tokens, dims, stream,
-                     false);
-}
-
-int pkv_append_fp8(const void* k_new, const void* v_new, const int64_t* slot_mapping,
-                   void* k_pool, void* v_pool, const float* k_scale, const float* v_scale,
-                   int32_t num_new_tokens, const pkv_dims* dims, cudaStream_t stream) {
+int append_fp8_impl(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                    void* k_pool, void* v_pool, const float* k_scale, const float* v_scale,
+                    int32_t num_new_tokens, const pkv_dims* dims, cudaStream_t stream,
+                    bool early_trigger) {
   g_last_error[0] = '\0';
   int rc = check_dims(dims, false);
   if (rc != PKV_OK) return rc;
@@ -326,9 +315,29 @@ int pkv_append_fp8(const void* k_new, const void* v_new, const int64_t* slot_map
   p.num_kv_heads = dims->num_kv_heads;
   p.num_blocks = dims->num_blocks;
   p.pdl = current_options().pdl != 0;
+  p.early_trigger = early_trigger && p.pdl;
   cudaError_t e = pkv::launch_append_fp8(p, stream);
   if (e != cudaSuccess) return cuda_fail(e, "append_fp8 launch");
   return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pkv_last_error(void) { return g_last_error; }
+
+int pkv_append(const void* k_new, const void* v_new, const int64_t* slot_mapping, void* k_pool,
+               void* v_pool, int32_t num_new_tokens, const pkv_dims* dims, cudaStream_t stream) {
+  return append_impl(k_new, v_new, slot_mapping, k_pool, v_pool, num_new_tokens, dims, stream,
+                     false);
+}
+
+int pkv_append_fp8(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                   void* k_pool, void* v_pool, const float* k_scale, const float* v_scale,
+                   int32_t num_new_tokens, const pkv_dims* dims, cudaStream_t stream) {
+  return append_fp8_impl(k_new, v_new, slot_mapping, k_pool, v_pool, k_scale, v_scale,
+                         num_new_tokens, dims, stream, false);
 }
 
 int pkv_copy_blocks(const void* k_src, const void* v_src, void* k_dst, void* v_dst,
@@ -682,6 +691,31 @@ int pkv_append_attention(const void* k_new, const void* v_new, const int64_t* sl
                    trigger);
   if (rc != PKV_OK) return rc;
   return attention_impl(q, k_pool, v_pool, nullptr, nullptr, block_tables, seq_lens,
+                        query_start_loc, scale, out, dims, workspace, workspace_bytes, stream,
+                        nullptr, early, trigger);
+}
+
+int pkv_append_attention_fp8(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                             void* k_pool, void* v_pool, const float* k_scale,
+                             const float* v_scale, const void* q, const int32_t* block_tables,
+                             const int32_t* seq_lens, const int32_t* query_start_loc,
+                             float scale, void* out, const pkv_dims* dims, void* workspace,
+                             size_t workspace_bytes, cudaStream_t stream) {
+  g_last_error[0] = '\0';
+  int rc = check_dims(dims, true);
+  if (rc != PKV_OK) return rc;
+  if (!k_scale || !v_scale) return fail(PKV_ERR_INVALID, "k_scale / v_scale is NULL");
+  // As pkv_append_attention: tiles without this step's tokens are read
+  // before the append finishes (early_kv), and with early_trigger the
+  // attention launches as soon as the append starts.
+  const pkv_options opt = current_options();
+  const bool pdl = opt.pdl != 0;
+  const bool early = pdl && opt.early_kv != 0;
+  const bool trigger = early && opt.early_trigger != 0;
+  rc = append_fp8_impl(k_new, v_new, slot_mapping, k_pool, v_pool, k_scale, v_scale,
+                       dims->num_q_tokens, dims, stream, trigger);
+  if (rc != PKV_OK) return rc;
+  return attention_impl(q, k_pool, v_pool, k_scale, v_scale, block_tables, seq_lens,
                         query_start_loc, scale, out, dims, workspace, workspace_bytes, stream,
                         nullptr, early, trigger);
 }

@@ -57,8 +57,9 @@ __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
 // (round to nearest even on the fp32 quotient, saturated to +-448).  Same
 // warp layout as the bf16 append; a lane reads 16 bytes and writes 8.
 __global__ void __launch_bounds__(256) append_fp8_kernel(AppendFp8Params p) {
-  grid_dependency_wait();
-  allow_dependent_launch();
+  if (p.early_trigger) allow_dependent_launch();
+  grid_dependency_wait();  // inputs and pool may belong to the previous kernel
+  if (!p.early_trigger) allow_dependent_launch();
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= p.num_tokens * p.num_kv_heads) return;

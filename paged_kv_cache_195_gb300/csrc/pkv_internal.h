@@ -157,6 +157,7 @@ struct AppendFp8Params {
   int num_kv_heads;
   int num_blocks;
   int pdl;
+  int early_trigger;  // as AppendParams::early_trigger
 };
 
 cudaError_t launch_append_fp8(const AppendFp8Params& p, cudaStream_t stream);

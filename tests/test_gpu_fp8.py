@@ -204,3 +204,65 @@ def test_fp8_null_scales_rejected():
         ctypes.c_void_p(inp.query_start_loc.data_ptr()), ctypes.c_float(inp.scale),
         ctypes.c_void_p(inp.q.data_ptr()), ctypes.byref(d), None, 0, None)
     assert rc == pkv._binding.PKV_ERR_INVALID
+
+
+# ---------------------------------------------------------------------------
+# One layer in one call over e4m3 pools: pkv_append_attention_fp8
+# ---------------------------------------------------------------------------
+
+FUSED_MODES = {"early_kv": {}, "early_trigger": {"early_trigger": 1}, "ordered": {"early_kv": 0}}
+
+FUSED_SHAPES = [
+    wl.StepShape("fp8_fused_g6", [17, 64, 100, 128, 513, 1000, 33, 16], [1] * 8, 12, 2, seed=411),
+    wl.StepShape("fp8_fused_g4", [300, 47, 2049, 160, 161, 5], [1] * 6, 32, 8, seed=412),
+    wl.StepShape("fp8_fused_g2", [90, 700, 66, 1025], [1] * 4, 4, 2, seed=413),
+    wl.StepShape("fp8_fused_mq", [200, 18, 47, 129], [3, 5, 15, 2], 12, 2, seed=414),
+]
+
+
+def _nan_codes_at_new_slots(inp):
+    """The NaN code at the slots this step's append writes (their old contents)."""
+    s = inp.slot_mapping[inp.slot_mapping >= 0]
+    nb, hkv, bs, d = inp.k_pool.shape
+    for pool in (inp.k_pool, inp.v_pool):
+        flat = pool.view(nb, hkv, bs, d).permute(0, 2, 1, 3).reshape(nb * bs, hkv, d)
+        flat[s] = wl.E4M3_NAN
+        pool.copy_(flat.reshape(nb, bs, hkv, d).permute(0, 2, 1, 3))
+
+
+def _fused_fp8(inp, out=None, workspace=None):
+    return pkv.pkv_append_attention_fp8(inp.k_new, inp.v_new, inp.slot_mapping, inp.k_pool,
+                                        inp.v_pool, inp.k_scale, inp.v_scale, inp.q,
+                                        inp.block_tables, inp.seq_lens, inp.query_start_loc,
+                                        inp.scale, out=out, workspace=workspace)
+
+
+@pytest.mark.parametrize("mode", list(FUSED_MODES))
+@pytest.mark.parametrize("shape", FUSED_SHAPES, ids=lambda s: s.name)
+def test_fp8_fused_matches_oracle(shape, mode, pkv_opts):
+    pkv_opts(**FUSED_MODES[mode])
+    inp = wl.make_fp8_step(shape, device="cuda", poison=True)
+    h = _host(inp)
+    kp, vp = oracle.append_fp8(h["k_new"], h["v_new"], h["slots"], h["k_pool"], h["v_pool"],
+                               h["k_scale"], h["v_scale"])
+    _nan_codes_at_new_slots(inp)
+    out = _fused_fp8(inp)
+    torch.cuda.synchronize()
+    assert pkv.pkv_get_device_error() == 0, pkv.pkv_last_error()
+    assert np.array_equal(pool_host(inp.k_pool), kp), "K codes differ from the oracle's"
+    assert np.array_equal(pool_host(inp.v_pool), vp), "V codes differ from the oracle's"
+    want = oracle.paged_attention_fp8(h["q"], kp, vp, h["k_scale"], h["v_scale"], h["bt"],
+                                      h["sl"], h["qsl"], h["scale"])
+    assert_close(to_f64(out), want, shape.name)
+
+
+@pytest.mark.parametrize("shape", FUSED_SHAPES, ids=lambda s: s.name)
+def test_fp8_fused_equals_separate_calls(shape):
+    a = wl.make_fp8_step(shape, device="cuda")
+    b = wl.make_fp8_step(shape, device="cuda")
+    ref = _step(a)
+    _nan_codes_at_new_slots(b)
+    got = _fused_fp8(b)
+    torch.cuda.synchronize()
+    assert torch.equal(got, ref)
+    assert torch.equal(a.k_pool, b.k_pool) and torch.equal(a.v_pool, b.v_pool)
