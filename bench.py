@@ -84,11 +84,12 @@ def measured_tensor_peak():
         return 1900.0, "fallback"
 
 
-def decode_source_sha() -> str:
-    """Hash of the decode kernels' code: the sources with // comments and
-    blank lines removed, so that edits to comments keep a profile valid."""
+def decode_source_sha(paths=None) -> str:
+    """Hash of the kernels' code (the decode sources unless `paths` names
+    others): the sources with // comments and blank lines removed, so that
+    edits to comments keep a profile valid."""
     h = hashlib.sha256()
-    for path in DECODE_SRCS:
+    for path in (DECODE_SRCS if paths is None else paths):
         with open(path, encoding="utf-8") as f:
             for line in f:
                 code = re.sub(r"//.*", "", line).rstrip()
@@ -98,15 +99,30 @@ def decode_source_sha() -> str:
 
 
 def committed_traffic(config: str, kv: str):
-    """Per-launch DRAM bytes of the decode kernel from the committed ncu
-    summary of this workload, if it was taken on the current decode sources
-    (else None)."""
-    path = os.path.join(ROOT, "profiles", f"decode_{config}_{kv}.md")
+    """Per-launch DRAM bytes of the attention call from the committed ncu
+    summary of this workload (decode_<config>_<kv>.md for a call that runs
+    the decode kernel alone, attention_<config>_<kv>.md for one that also
+    runs the prefill kernel), if it was taken on the current sources of the
+    kernels it names (its kernel_sources line; the decode sources if it has
+    none), else None."""
+    text = None
+    for stem in ("decode", "attention"):
+        try:
+            text = open(os.path.join(ROOT, "profiles", f"{stem}_{config}_{kv}.md")).read()
+            break
+        except OSError:
+            continue
+    if text is None:
+        return None
+    m_src = re.search(r"kernel_sources:[ \t]*(\S.*)", text)
+    paths = None
+    if m_src:
+        csrc = os.path.join(ROOT, "paged_kv_cache_195_gb300", "csrc")
+        paths = [os.path.join(csrc, f) for f in m_src.group(1).split()]
     try:
-        text = open(path).read()
+        src_sha = decode_source_sha(paths)
     except OSError:
         return None
-    src_sha = decode_source_sha()
     m_sha = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
     m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
     if m_sha and m_tr and m_sha.group(1) == src_sha:
@@ -427,11 +443,25 @@ class ConfigRun:
                                       shape.prefix_groups, kv_dtype_bytes=self.kvb) + att["q_out"]
         return att["total"]
 
-    def kernels_per_layer(self):
+    def has_prefill(self):
+        """Whether the library's routing sends part of this step to the
+        tensor-core prefill kernel (bf16 pools, a request with at least
+        prefill_min_q query tokens possible)."""
         shape = self.shape
-        has_prefill = (not self.fp8 and not self.cascade and
-                       shape.num_q_tokens - shape.num_reqs + 1 >= 16)
-        return 2 + (1 if has_prefill else 0) + (2 if self.cascade else 0)
+        min_q = self.pkv.get_options()["prefill_min_q"]
+        return (not self.fp8 and not self.cascade and min_q >= 1 and
+                shape.num_q_tokens - shape.num_reqs + 1 >= min_q)
+
+    def kernels_per_layer(self):
+        return 2 + (1 if self.has_prefill() else 0) + (2 if self.cascade else 0)
+
+    def kernel_label(self):
+        """The kernels one attention call runs on this step."""
+        group = self.shape.num_q_heads // self.shape.num_kv_heads
+        name = decode_kernel_name(group, self.fp8, self.pkv.get_options())
+        if self.has_prefill():
+            name += f" + pkv::prefill_kernel<{group}>"
+        return name
 
     def roofline(self, durs_ms, config_name, clock_info):
         peak, peak_src = measured_peak()
@@ -442,8 +472,7 @@ class ConfigRun:
         return {
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "traffic": committed_traffic(config_name, self.kv),
-            "kernel": decode_kernel_name(shape.num_q_heads // shape.num_kv_heads, self.fp8,
-                                         self.pkv.get_options()),
+            "kernel": self.kernel_label(),
             "timing": (f"{len(self.roof_seq)} attention launches back to back "
                        f"({'distinct layers' if shape.layers > 1 else 'two copies alternating'})"
                        f", one event pair per replay, {len(durs_ms)} replays"),

@@ -120,3 +120,27 @@ def test_lengths_summary(bench):
 def test_cpu_model_is_named(bench):
     name = bench.cpu_model()
     assert isinstance(name, str) and name
+
+
+def test_committed_traffic_of_a_two_kernel_call_hashes_its_listed_sources(bench, tmp_path,
+                                                                           monkeypatch):
+    csrc = tmp_path / "paged_kv_cache_195_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    for name in ("a.cu", "b.cuh"):
+        (csrc / name).write_text("int %s_symbol = 1;\n" % name[0])
+    sha = bench.decode_source_sha([str(csrc / "a.cu"), str(csrc / "b.cuh")])
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (prof / "attention_mixed_bf16.md").write_text(
+        "kernel_sources: a.cu b.cuh\nkernel_source_sha256_16: %s\n"
+        "dram_bytes_per_launch: 4242\n" % sha)
+    (prof / "attention_gone_bf16.md").write_text(
+        "kernel_sources: a.cu missing.cu\nkernel_source_sha256_16: %s\n"
+        "dram_bytes_per_launch: 1\n" % sha)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.committed_traffic("mixed", "bf16") == 4242
+    assert bench.committed_traffic("gone", "bf16") is None     # a listed source is missing
+    with open(csrc / "b.cuh", "a") as f:
+        f.write("int another = 2;\n")
+    assert bench.committed_traffic("mixed", "bf16") is None    # the code changed
+
