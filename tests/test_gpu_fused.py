@@ -81,7 +81,7 @@ def test_fused_matches_oracle(shape, mode, pkv_opts):
     assert_close(to_f64(out), oracle_full(h, kp, vp), shape.name)
 
 
-@pytest.mark.parametrize("shape", SHAPES[:2] + SHAPES[3:4] + SHAPES[6:], ids=lambda s: s.name)
+@pytest.mark.parametrize("shape", SHAPES[:2] + SHAPES[3:4] + SHAPES[5:], ids=lambda s: s.name)
 def test_fused_equals_separate_calls(shape):
     a = wl.make_step(shape, device="cuda")
     b = wl.make_step(shape, device="cuda")
@@ -150,3 +150,57 @@ def test_fused_padding_tokens_skip_append():
     got = _fused(b)
     torch.cuda.synchronize()
     assert torch.equal(got, ref)
+
+
+def _bucket_step(live, pad_rows):
+    """A step of `live` plus `pad_rows` trailing token rows past
+    query_start_loc[R] (a padded bucket), with the padding tokens' slots
+    pointing at free pool slots (not read by any request)."""
+    inp = wl.make_step(live, device="cuda", poison=True)
+    T = live.num_q_tokens + pad_rows
+    nb = inp.k_pool.shape[0]
+    used = set(inp.block_tables[inp.block_tables >= 0].tolist())
+    free = [b for b in range(nb) if b not in used][:pad_rows]
+    assert len(free) == pad_rows
+
+    def grow(x, fill):
+        y = torch.full((T,) + tuple(x.shape[1:]), fill, dtype=x.dtype, device=x.device)
+        y[:x.shape[0]] = x
+        return y
+
+    g = torch.Generator(device="cpu").manual_seed(77)
+    inp.q = grow(inp.q, float("nan"))
+    inp.k_new = grow(inp.k_new, 0.0)
+    inp.v_new = grow(inp.v_new, 0.0)
+    inp.k_new[live.num_q_tokens:] = torch.randn(inp.k_new[live.num_q_tokens:].shape,
+                                                generator=g).to(inp.k_new)
+    inp.v_new[live.num_q_tokens:] = torch.randn(inp.v_new[live.num_q_tokens:].shape,
+                                                generator=g).to(inp.v_new)
+    inp.slot_mapping = grow(inp.slot_mapping, -1)
+    inp.slot_mapping[live.num_q_tokens:] = torch.tensor([b * 16 + 3 for b in free],
+                                                        dtype=torch.int64)
+    return inp
+
+
+@pytest.mark.parametrize("mode", list(MODES))
+def test_fused_writes_trailing_tokens(mode, pkv_opts):
+    # token rows past query_start_loc[R] with a slot: appended like the others
+    # (their attention rows are padding: never written)
+    pkv_opts(**MODES[mode])
+    live = wl.StepShape("fused_trailing", [300, 47, 129, 16], [1] * 4, 12, 2, seed=410)
+    a, b = _bucket_step(live, 5), _bucket_step(live, 5)
+    pkv.pkv_append(a.k_new, a.v_new, a.slot_mapping, a.k_pool, a.v_pool)
+    ref = torch.full_like(a.q, 7.0)
+    pkv.pkv_attention(a.q, a.k_pool, a.v_pool, a.block_tables, a.seq_lens, a.query_start_loc,
+                      a.scale, out=ref)
+    got = torch.full_like(b.q, 7.0)
+    pkv.pkv_append_attention(b.k_new, b.v_new, b.slot_mapping, b.k_pool, b.v_pool, b.q,
+                             b.block_tables, b.seq_lens, b.query_start_loc, b.scale, out=got)
+    torch.cuda.synchronize()
+    assert pkv.pkv_get_device_error() == 0, pkv.pkv_last_error()
+    # bit patterns: the free slots hold NaN
+    assert torch.equal(a.k_pool.view(torch.int16), b.k_pool.view(torch.int16))
+    assert torch.equal(a.v_pool.view(torch.int16), b.v_pool.view(torch.int16))
+    assert torch.equal(got, ref)
+    assert bool((got[live.num_q_tokens:].float() == 7.0).all())
+
