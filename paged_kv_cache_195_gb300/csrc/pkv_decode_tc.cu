@@ -202,6 +202,94 @@ __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, int* err
   }
 }
 
+// Shared-prefix (cascade) rows: folds the prefix pass's partial states of
+// output dim d of row-head `rh` (row * Hq + head) into (M, num, den) by
+// log-sum-exp.  The prefix pass left one partial per chunk of the `shared`
+// keys: a normalised output and its (max, normaliser), stride `stride` rows
+// apart.  Out of line: only cascade calls reach it, and one copy keeps the
+// kernel's instruction footprint small.
+struct PrefixFold {
+  float M, num, den;
+};
+static __device__ __noinline__ PrefixFold fold_prefix_states(const float* pre_o,
+                                                             const float* pre_ml,
+                                                             long long rh, long long stride,
+                                                             int shared, int d, PrefixFold f) {
+  const int nch = prefix_chunks(shared);
+  // all chunks' loads first (they were prefetched into L2), then fold
+  float2 ml[kPrefixSplits];
+  float ov[kPrefixSplits];
+  #pragma unroll
+  for (int c = 0; c < kPrefixSplits; ++c) {
+    if (c < nch) {
+      const long long sl2 = c * stride + rh;
+      ml[c] = __ldcg(reinterpret_cast<const float2*>(pre_ml + sl2 * 2));
+      ov[c] = __ldcg(pre_o + sl2 * kHeadDim + d);
+    }
+  }
+  #pragma unroll
+  for (int c = 0; c < kPrefixSplits; ++c) {
+    if (c < nch) {
+      const float Mn = fmaxf(f.M, ml[c].x);
+      const float a = fast_exp2(f.M - Mn), w = fast_exp2(ml[c].x - Mn) * ml[c].y;
+      f.num = f.num * a + w * ov[c];
+      f.den = f.den * a + w;
+      f.M = Mn;
+    }
+  }
+  return f;
+}
+
+// The last piece of a split row-group to arrive: merges the pieces' partial
+// states of output dim d (each a normalised output and its (max,
+// normaliser), in workspace slots 2 (c0 + s) (+1 for piece 0 when odd0)) by
+// log-sum-exp, folds the shared prefix's states when `shared` >= 0, and
+// writes the G heads' outputs (out: dim d of the row's first head).  Out of
+// line: once per row-group, and one copy keeps the instruction footprint
+// small.
+template <int G>
+static __device__ __noinline__ void merge_pieces(const float* ws_ml, const float* ws_o,
+                                                 const float* pre_o, const float* pre_ml,
+                                                 __nv_bfloat16* out, int c0, int S, int odd0,
+                                                 int shared, long long rh0, long long stride,
+                                                 int d) {
+  #pragma unroll
+  for (int h = 0; h < G; ++h) {
+    PrefixFold f{kNegBig, 0.f, 0.f};
+    #pragma unroll 4
+    for (int s2 = 0; s2 < S; ++s2) {
+      const int slot = 2 * (c0 + s2) + ((s2 == 0 && odd0) ? 1 : 0);
+      const long long sl2 = (long long)slot * G + h;
+      const float2 ml = __ldcg(reinterpret_cast<const float2*>(ws_ml + sl2 * 2));
+      const float ov = __ldcg(ws_o + sl2 * kHeadDim + d);
+      const float Mn = fmaxf(f.M, ml.x);
+      const float a = fast_exp2(f.M - Mn), w = fast_exp2(ml.x - Mn) * ml.y;
+      f.num = f.num * a + w * ov;
+      f.den = f.den * a + w;
+      f.M = Mn;
+    }
+    if (shared >= 0) f = fold_prefix_states(pre_o, pre_ml, rh0 + h, stride, shared, d, f);
+    out[h * kHeadDim] = __float2bfloat16_rn(f.den > 0.f ? f.num / f.den : 0.f);
+  }
+}
+
+// Brings the prefix pass's partial states of the G heads of row-head rh0
+// into L2 (G x 512 B of outputs and the (max, normaliser) pairs per chunk of
+// the `shared` keys); warp-collective, out of line (cascade calls only).
+template <int G>
+static __device__ __noinline__ void prefetch_prefix_states(const float* pre_o, const float* pre_ml,
+                                                           long long rh0, long long stride,
+                                                           int shared, int lane) {
+  const int nch = prefix_chunks(shared);
+  for (int i = lane; i < nch * (G * 4 + 1); i += 32) {
+    const int c = i / (G * 4 + 1), x = i % (G * 4 + 1);
+    const char* a = x < G * 4
+        ? reinterpret_cast<const char*>(pre_o + ((c * stride + rh0) * kHeadDim)) + x * 128
+        : reinterpret_cast<const char*>(pre_ml + (c * stride + rh0) * 2);
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+  }
+}
+
 // Two e4m3 codes (low byte first) to two f16 (low half first).  Every e4m3
 // value is an f16 value, so the widening (the hardware e4m3x2 -> f16x2
 // conversion) is exact.
@@ -551,21 +639,13 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 2) __maxnreg__
               q_k1 = k;
             }
           }
-          if (pc.pre) {
-            // The epilogue will fold the prefix pass's partial states of
-            // this row: bring them into L2 now (G x 512 B of outputs and the
-            // (max, normaliser) pairs per chunk).
-            const long long pr = (long long)pc.row * p.num_q_heads + (long long)k * G;
-            const long long stride = (long long)p.num_q_tokens * p.num_q_heads;
-            const int nch = prefix_chunks(pc.fb * kBlockSize);
-            for (int i = lane; i < nch * (G * 4 + 1); i += 32) {
-              const int c = i / (G * 4 + 1), x = i % (G * 4 + 1);
-              const char* a = x < G * 4
-                  ? reinterpret_cast<const char*>(p.pre_o + ((c * stride + pr) * kHeadDim)) + x * 128
-                  : reinterpret_cast<const char*>(p.pre_ml + (c * stride + pr) * 2);
-              asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
-            }
-          }
+          // The epilogue will fold the prefix pass's partial states of this
+          // row: bring them into L2 now.
+          if (pc.pre)
+            prefetch_prefix_states<G>(p.pre_o, p.pre_ml,
+                                      (long long)pc.row * p.num_q_heads + (long long)k * G,
+                                      (long long)p.num_q_tokens * p.num_q_heads,
+                                      pc.fb * kBlockSize, lane);
           __syncwarp();
         }
       }
@@ -950,35 +1030,16 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 2) __maxnreg__
                             pc.slot < p.num_slots;
       const long long out_row = ((long long)pc.row * p.num_q_heads + (long long)pc.k * G) * kHeadDim;
       // Shared-prefix (cascade) rows: fold in the prefix pass's partial
-      // state (max M, normaliser, normalised output) by log-sum-exp.  The
-      // prefix pass left one partial per chunk of the shared keys (pc.b0 is
-      // at least the shared block count, and the row's first piece starts
-      // exactly there).
+      // states (pc.b0 is at least the shared block count, and the row's
+      // first piece starts exactly there).
       auto fold_prefix = [&](int h, float& M, float& num, float& den) {
-        const long long pr = (long long)pc.row * p.num_q_heads + (long long)pc.k * G + h;
-        const long long stride = (long long)p.num_q_tokens * p.num_q_heads;
-        const int nch = prefix_chunks(pc.fb * kBlockSize);
-        // all chunks' loads first (they were prefetched into L2), then fold
-        float2 ml[kPrefixSplits];
-        float ov[kPrefixSplits];
-        #pragma unroll
-        for (int c = 0; c < kPrefixSplits; ++c) {
-          if (c < nch) {
-            const long long sl2 = c * stride + pr;
-            ml[c] = __ldcg(reinterpret_cast<const float2*>(p.pre_ml + sl2 * 2));
-            ov[c] = __ldcg(p.pre_o + sl2 * kHeadDim + d);
-          }
-        }
-        #pragma unroll
-        for (int c = 0; c < kPrefixSplits; ++c) {
-          if (c < nch) {
-            const float Mn = fmaxf(M, ml[c].x);
-            const float a = fast_exp2(M - Mn), w = fast_exp2(ml[c].x - Mn) * ml[c].y;
-            num = num * a + w * ov[c];
-            den = den * a + w;
-            M = Mn;
-          }
-        }
+        const PrefixFold f = fold_prefix_states(
+            p.pre_o, p.pre_ml, (long long)pc.row * p.num_q_heads + (long long)pc.k * G + h,
+            (long long)p.num_q_tokens * p.num_q_heads, pc.fb * kBlockSize, d,
+            PrefixFold{M, num, den});
+        M = f.M;
+        num = f.num;
+        den = f.den;
       };
       if (in_range && pc.S == 1) {
         if (okO) {
@@ -1019,26 +1080,11 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 2) __maxnreg__
           sm.is_last = last;
         }
         named_barrier(kBarSoftmax, kSoftThreads);
-        if (sm.is_last) {
-          #pragma unroll
-          for (int h = 0; h < G; ++h) {
-            float M = kNegBig, num = 0.f, den = 0.f;
-            #pragma unroll 4
-            for (int s2 = 0; s2 < pc.S; ++s2) {
-              const int slot = 2 * (pc.c0 + s2) + ((s2 == 0 && pc.odd0) ? 1 : 0);
-              const long long sl2 = (long long)slot * G + h;
-              const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.ws_ml + sl2 * 2));
-              const float ov = __ldcg(p.ws_o + sl2 * kHeadDim + d);
-              const float Mn = fmaxf(M, ml.x);
-              const float a = fast_exp2(M - Mn), w = fast_exp2(ml.x - Mn) * ml.y;
-              num = num * a + w * ov;
-              den = den * a + w;
-              M = Mn;
-            }
-            if (pc.pre) fold_prefix(h, M, num, den);
-            p.out[out_row + h * kHeadDim + d] = __float2bfloat16_rn(den > 0.f ? num / den : 0.f);
-          }
-        }
+        if (sm.is_last)
+          merge_pieces<G>(p.ws_ml, p.ws_o, p.pre_o, p.pre_ml, p.out + out_row + d, pc.c0, pc.S,
+                          pc.odd0, pc.pre ? pc.fb * kBlockSize : -1,
+                          (long long)pc.row * p.num_q_heads + (long long)pc.k * G,
+                          (long long)p.num_q_tokens * p.num_q_heads, d);
       }
       // sm.st_l and sm.is_last are free again once every thread is here.
       named_barrier(kBarSoftmax, kSoftThreads);
