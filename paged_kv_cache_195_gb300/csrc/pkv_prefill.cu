@@ -159,6 +159,30 @@ __device__ __forceinline__ PfReq load_pf_request(const PrefillParams& p, int u, 
   return a;
 }
 
+// Rarely run parts of the softmax warps, out of line: one copy each keeps
+// the kernel's instruction footprint small.
+// O (this thread's 32 output columns at TMEM address tO) times alpha.
+static __device__ __noinline__ void rescale_o32(uint32_t tO, float alpha) {
+  float o[32];
+  tmem_ld32(tO, o);
+  tc_wait_ld();
+  #pragma unroll
+  for (int i = 0; i < 32; ++i) o[i] *= alpha;
+  tmem_st32(tO, o);
+  tc_wait_st();
+}
+
+// Zeroes rows tail0 .. tail0 + nrows - 1 of a staged V tile (two 64-column
+// halves `half_bytes` apart, 128-byte swizzled); warp-collective.
+static __device__ __noinline__ void zero_v_rows(uint8_t* v, int half_bytes, int tail0, int nrows,
+                                                int lane) {
+  for (int i = lane; i < nrows * 16; i += 32) {
+    const int rr = tail0 + i / 16, hf = (i / 8) & 1, chunk = i & 7;
+    *reinterpret_cast<uint4*>(v + hf * half_bytes + (rr >> 3) * 1024 + (rr & 7) * 128 +
+                              chunk * 16) = make_uint4(0, 0, 0, 0);
+  }
+}
+
 template <int G>
 __global__ void __launch_bounds__(kPfThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
@@ -556,13 +580,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           tc_fence_after();
           const float m_new = grow ? fmaxf(m, mx) : m;
           const float alpha = fast_exp2(m - m_new);
-          float o[32];
-          tmem_ld32(tO, o);
-          tc_wait_ld();
-          #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] *= alpha;
-          tmem_st32(tO, o);
-          tc_wait_st();
+          rescale_o32(tO, alpha);
           l *= alpha;
           m_use = m_new;
         }
@@ -595,12 +613,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const int tail1 = min(kKeyTile, ceil_div(it.L, kBlockSize) * kBlockSize - tbase);
         if (warp == 0 && tail0 < tail1 && tail0 >= 0) {
           ok = ok && mbar_wait(&sm.v_full[st], (tile_ctr / kPfStagesV) & 1, p.err, abort_flag);
-          const int nrows = tail1 - tail0;
-          for (int i = lane; i < nrows * 16; i += 32) {
-            const int rr = tail0 + i / 16, hf = (i / 8) & 1, chunk = i & 7;
-            *reinterpret_cast<uint4*>(sm.v[st][hf] + (rr >> 3) * 1024 + (rr & 7) * 128 +
-                                      chunk * 16) = make_uint4(0, 0, 0, 0);
-          }
+          zero_v_rows(sm.v[st][0], (int)(sm.v[st][1] - sm.v[st][0]), tail0, tail1 - tail0, lane);
           fence_proxy_async_smem();  // the zeros, read by the tensor core
         }
         tc_fence_before();
