@@ -290,6 +290,34 @@ static __device__ __noinline__ void prefetch_prefix_states(const float* pre_o, c
   }
 }
 
+// O^T's G columns of this thread's TMEM lane (tO) times alpha[h]: the rare
+// rescale after a tile raised a running maximum.  Out of line in the e4m3
+// kernel (4% faster there; the bf16 kernel was 3% slower with it).
+struct Alpha8 {
+  float v[8];
+};
+template <int G>
+static __device__ __noinline__ void rescale_ot(uint32_t tO, Alpha8 alpha) {
+  tc_fence_after();
+  float o[8];
+  tmem_ld8(tO, o);
+  tc_wait_ld();
+  #pragma unroll
+  for (int h = 0; h < G; ++h) o[h] *= alpha.v[h];
+  tmem_st8(tO, o);
+  tc_wait_st();
+}
+
+// An aborted CTA's producer: waits (bounded) for the copies still in flight
+// -- ring occupants n_occ - ring .. n_occ - 1 (barriers full[n % ring]) --
+// before the CTA's shared memory is released.  Out of line in the e4m3
+// kernel.
+static __device__ __noinline__ void drain_ring(uint64_t* full, int ring, int n_occ, int* err,
+                                               WaitCtl* ctl) {
+  for (int m = max(0, n_occ - ring); m < n_occ; ++m)
+    mbar_wait_drain(full + m % ring, (m / ring) & 1, err, ctl);
+}
+
 // Two e4m3 codes (low byte first) to two f16 (low half first).  Every e4m3
 // value is an f16 value, so the widening (the hardware e4m3x2 -> f16x2
 // conversion) is exact.
@@ -691,9 +719,11 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 2) __maxnreg__
     if (abort_flag->abort) {
       // Copies still in flight must land before the CTA's shared memory is
       // released: the last occupant of each slot and the last Q of each buffer.
-      for (int m = max(0, n_occ - kRing); m < n_occ; ++m) {
-        const int s = m % kRing;
-        mbar_wait_drain(F8 ? &sm.raw_full[s] : &sm.full[s], (m / kRing) & 1, p.err, abort_flag);
+      if constexpr (F8) {
+        drain_ring(sm.raw_full, kRing, n_occ, p.err, abort_flag);
+      } else {
+        for (int m = max(0, n_occ - kRing); m < n_occ; ++m)
+          mbar_wait_drain(&sm.full[m % kRing], (m / kRing) & 1, p.err, abort_flag);
       }
       for (int ub = 0; ub < 2; ++ub)
         if (q_armed[ub] > 0 && q_copy[ub])
@@ -946,14 +976,21 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 2) __maxnreg__
             l[h] *= alpha[h];
           }
           if (tt > 0 && grow) {
-            tc_fence_after();
-            float o[8];
-            tmem_ld8(tO, o);
-            tc_wait_ld();
-            #pragma unroll
-            for (int h = 0; h < G; ++h) o[h] *= alpha[h];
-            tmem_st8(tO, o);
-            tc_wait_st();
+            if constexpr (F8) {
+              Alpha8 a;
+              #pragma unroll
+              for (int h = 0; h < 8; ++h) a.v[h] = h < G ? alpha[h] : 1.f;
+              rescale_ot<G>(tO, a);
+            } else {
+              tc_fence_after();
+              float o[8];
+              tmem_ld8(tO, o);
+              tc_wait_ld();
+              #pragma unroll
+              for (int h = 0; h < G; ++h) o[h] *= alpha[h];
+              tmem_st8(tO, o);
+              tc_wait_st();
+            }
           }
           // sm.red is read by every softmax thread before its next write.
           named_barrier(kBarSoftmax, kSoftThreads);
