@@ -445,9 +445,15 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 2) __maxnreg__
     else if (have_n) warm(ent_n0, pn.k);
     if (lane == 0) TC_CTA(12);
   };
-  if (warp == 4 && early_plan) {
+  // One call site for the plan (its code is large): without early_plan its
+  // inputs may belong to the kernel before, so the producer waits first.
+  if (warp == 4) {
+    if (!early_plan) {
+      grid_dependency_wait();
+      allow_dependent_launch();
+    }
     plan_first();
-    warm_first();
+    if (early_plan) warm_first();
     // The entries must be in registers before the wait below: a volatile
     // use keeps the compiler from sinking their loads past it.
     asm volatile("" ::"r"(ent_w0), "r"(ent_w1), "r"(ent_n0), "r"(ent_n1));
@@ -455,7 +461,7 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 2) __maxnreg__
   // A CTA the plan gives no work leaves at once (after the launch wait, so
   // that this grid never completes before the kernel ahead of it): its SM
   // slot goes to the next launch.
-  if (warp == 4 && lane == 0) sm.idle = early_plan && !have;
+  if (warp == 4 && lane == 0) sm.idle = !have;
   __syncthreads();
   if (sm.idle) {
     grid_dependency_wait();
@@ -539,7 +545,6 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 2) __maxnreg__
   if (warp == 4) {
     // ===================== plan + L2 warming + TMA producer ==================
     bool waited = !p.early_kv;
-    if (!early_plan) plan_first();  // after the wait above
     if (p.early_plan && !p.early_kv) {
       grid_dependency_wait();
       allow_dependent_launch();
