@@ -424,16 +424,26 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 2) __maxnreg__
       }
     }
   };
+  // The next piece becomes the current one and the one after it is fetched
+  // (with its first block-table entries, in flight during the next call).
+  auto advance = [&]() {
+    pc = pn;
+    have = have_n;
+    ent_w0 = ent_n0;
+    ent_w1 = ent_n1;
+    have_n = have && wk.next(p, pn);
+    ent_n0 = have_n ? raw_entries(pn, 0) : kPastPiece;
+    ent_n1 = have_n && pn.nblk > kWindow ? raw_entries(pn, kWindow) : kPastPiece;
+  };
   auto plan_first = [&]() {
     if (p.prefetch) plan::prefetch_block_table(p, lane);
     plan::plan_cta(p, lane, rg, wk);
     if (lane == 0) TC_CTA(10);
-    have = wk.next(p, pc);
-    if (have) ent_w0 = raw_entries(pc, 0);  // in flight during next()
-    if (have && pc.nblk > kWindow) ent_w1 = raw_entries(pc, kWindow);
-    have_n = have && wk.next(p, pn);
-    if (have_n) ent_n0 = raw_entries(pn, 0);
-    if (have_n && pn.nblk > kWindow) ent_n1 = raw_entries(pn, kWindow);
+    // the first piece into pn, then into pc with the second into pn (one
+    // copy of the walker's code: the loop is not unrolled)
+    have_n = true;
+    #pragma unroll 1
+    for (int i = 0; i < 2; ++i) advance();
     if (lane == 0) TC_CTA(11);
   };
   // The first eight tiles' blocks into L2: the first piece's two windows, or
@@ -648,7 +658,8 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 2) __maxnreg__
           // buffer (the piece's first K/V tile is already on its way).
           const int ub = j & 1;
           if (j >= 2) {
-            if (!waited || q_pend) take_wait();
+            // (the launch wait is taken: from the third tile on, 2t + 1 >=
+            // kRing holds and the producer took it above)
             if (!tc_wait<F8>(&sm.q_empty[ub], ((j >> 1) - 1) & 1, p.err, abort_flag)) {
               ok = false;
               break;
@@ -683,13 +694,7 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 2) __maxnreg__
         }
       }
       ++j;
-      pc = pn;
-      have = have_n;
-      ent_w0 = ent_n0;
-      ent_w1 = ent_n1;
-      have_n = have && wk.next(p, pn);
-      ent_n0 = have_n ? raw_entries(pn, 0) : kPastPiece;
-      ent_n1 = have_n && pn.nblk > kWindow ? raw_entries(pn, kWindow) : kPastPiece;
+      advance();
     }
     // The CTA finishes after the previous kernel in any case; Q copies still
     // pending are issued unless the CTA is giving up.
