@@ -1116,14 +1116,13 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 2) __maxnreg__
         }
         named_barrier(kBarSoftmax, kSoftThreads);
         if (d == 0) {
-          __threadfence();
+          // The ticket: release publishes this piece's state (every softmax
+          // thread's writes, ordered before this one by the barrier above);
+          // acquire makes the other pieces' visible to the merge below.
           int* cnt = p.ws_cnt + (long long)pc.row * Hkv + pc.k;
-          const int old = atomicAdd(cnt, 1);
+          const int old = atom_add_acq_rel_gpu(cnt, 1);
           const int last = (old == pc.S - 1);
-          if (last) {
-            *cnt = 0;  // every piece has arrived: leave the counter at zero
-            __threadfence();
-          }
+          if (last) *cnt = 0;  // every piece has arrived: leave the counter at zero
           sm.is_last = last;
         }
         named_barrier(kBarSoftmax, kSoftThreads);
