@@ -253,23 +253,35 @@ static __device__ __noinline__ void merge_pieces(const float* ws_ml, const float
                                                  __nv_bfloat16* out, int c0, int S, int odd0,
                                                  int shared, long long rh0, long long stride,
                                                  int d) {
+  PrefixFold f[G];
+  #pragma unroll
+  for (int h = 0; h < G; ++h) f[h] = PrefixFold{kNegBig, 0.f, 0.f};
+  // Piece by piece, the G heads' states loaded together (2G loads in
+  // flight: one L2 round trip per piece rather than one per head and piece).
+  #pragma unroll 1
+  for (int s2 = 0; s2 < S; ++s2) {
+    const int slot = 2 * (c0 + s2) + ((s2 == 0 && odd0) ? 1 : 0);
+    float2 ml[G];
+    float ov[G];
+    #pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const long long sl2 = (long long)slot * G + h;
+      ml[h] = __ldcg(reinterpret_cast<const float2*>(ws_ml + sl2 * 2));
+      ov[h] = __ldcg(ws_o + sl2 * kHeadDim + d);
+    }
+    #pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float Mn = fmaxf(f[h].M, ml[h].x);
+      const float a = fast_exp2(f[h].M - Mn), w = fast_exp2(ml[h].x - Mn) * ml[h].y;
+      f[h].num = f[h].num * a + w * ov[h];
+      f[h].den = f[h].den * a + w;
+      f[h].M = Mn;
+    }
+  }
   #pragma unroll
   for (int h = 0; h < G; ++h) {
-    PrefixFold f{kNegBig, 0.f, 0.f};
-    #pragma unroll 4
-    for (int s2 = 0; s2 < S; ++s2) {
-      const int slot = 2 * (c0 + s2) + ((s2 == 0 && odd0) ? 1 : 0);
-      const long long sl2 = (long long)slot * G + h;
-      const float2 ml = __ldcg(reinterpret_cast<const float2*>(ws_ml + sl2 * 2));
-      const float ov = __ldcg(ws_o + sl2 * kHeadDim + d);
-      const float Mn = fmaxf(f.M, ml.x);
-      const float a = fast_exp2(f.M - Mn), w = fast_exp2(ml.x - Mn) * ml.y;
-      f.num = f.num * a + w * ov;
-      f.den = f.den * a + w;
-      f.M = Mn;
-    }
-    if (shared >= 0) f = fold_prefix_states(pre_o, pre_ml, rh0 + h, stride, shared, d, f);
-    out[h * kHeadDim] = __float2bfloat16_rn(f.den > 0.f ? f.num / f.den : 0.f);
+    if (shared >= 0) f[h] = fold_prefix_states(pre_o, pre_ml, rh0 + h, stride, shared, d, f[h]);
+    out[h * kHeadDim] = __float2bfloat16_rn(f[h].den > 0.f ? f[h].num / f[h].den : 0.f);
   }
 }
 
