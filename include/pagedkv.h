@@ -378,6 +378,10 @@ typedef struct pkv_options {
     int32_t debug_withhold_q; /* testing only (0): the tensor-core decode never loads q,
                                so its waits run out after wait_limit_us; exercises
                                the timeout path.  Results are not computed. */
+    int32_t rowgroup_cost;  /* PKV_ROWGROUP_COST (16): when the decode plan cuts the
+                               step into equal per-CTA ranges, every (query row, KV
+                               head) counts as its 16-token blocks plus this many,
+                               the fixed cost of a piece (0..1024) */
 } pkv_options;
 
 /* Copies the current options into *opts. */

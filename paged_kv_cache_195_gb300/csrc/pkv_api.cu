@@ -124,7 +124,8 @@ int env_int(const char* name, int dflt) {
 
 bool options_valid(const pkv_options& o) {
   return o.prefill_min_q >= 0 && o.align_slack >= 0 && o.min_chunk >= 1 && o.decode_grid >= 0 &&
-         o.warm_kv >= 0 && o.warm_kv <= 2 && o.wait_limit_us >= 1;
+         o.warm_kv >= 0 && o.warm_kv <= 2 && o.wait_limit_us >= 1 && o.rowgroup_cost >= 0 &&
+         o.rowgroup_cost <= 1024;
 }
 
 pkv_options options_from_env() {
@@ -145,6 +146,7 @@ pkv_options options_from_env() {
   o.warm_kv = env_int("PKV_WARM_KV", 0);
   o.wait_limit_us = env_int("PKV_WAIT_LIMIT_US", (int)(pkv::kDefaultWaitLimitNs / 1000));
   o.debug_withhold_q = 0;  // never from the environment
+  o.rowgroup_cost = env_int("PKV_ROWGROUP_COST", 16);
   // Out-of-range values from the environment fall back to the defaults.
   if (o.prefill_min_q < 0) o.prefill_min_q = 16;
   if (o.align_slack < 0) o.align_slack = 64;
@@ -152,6 +154,7 @@ pkv_options options_from_env() {
   if (o.decode_grid < 0) o.decode_grid = 0;
   if (o.warm_kv < 0 || o.warm_kv > 2) o.warm_kv = 0;
   if (o.wait_limit_us < 1) o.wait_limit_us = (int)(pkv::kDefaultWaitLimitNs / 1000);
+  if (o.rowgroup_cost < 0 || o.rowgroup_cost > 1024) o.rowgroup_cost = 16;
   return o;
 }
 
@@ -527,6 +530,7 @@ int attention_impl(const void* q, const void* k_pool, const void* v_pool, const 
   p.warm_kv = opt.warm_kv;
   p.wait_limit_ns = (unsigned long long)opt.wait_limit_us * 1000ull;
   p.debug_withhold_q = opt.debug_withhold_q != 0;
+  p.rowgroup_cost = opt.rowgroup_cost;
   const int group = dims->num_q_heads / dims->num_kv_heads;
   int grid = pkv::decode_grid(st->sm_count, group);
   // tuning override, bounded by the workspace's slots

@@ -111,6 +111,10 @@ struct DecodeParams {
   // Testing only: the tensor-core decode's producer arms the first piece's
   // q barrier but never issues its copy, so the waits on it run out.
   int debug_withhold_q;
+  // Blocks' worth of work a piece costs beyond its blocks (its epilogue and
+  // partial last tile): added to every row-group's length when the plan
+  // cuts the CTAs' ranges.
+  int rowgroup_cost;
 };
 
 // Workspace carve-up shared by the host code that sizes it and the launcher.

@@ -5,11 +5,12 @@
 // in request order, each a run of 16-token blocks: row i of request r (q_r
 // query tokens, length L) sees positions < L - q_r + i + 1 (the chunk sits at
 // the end of the sequence: The Serving Playbook, "Chunked prefill").  The
-// grid cuts that block sequence into equal contiguous ranges, one per CTA,
-// so every CTA streams the same number of tiles whatever the length mix; a
-// row-group cut by a range boundary is computed in pieces that are merged by
-// log-sum-exp (The Serving Playbook, "Kernel fusion, briefly": Flash-Decoding
-// splits the KV axis).
+// grid cuts that block sequence into equal contiguous ranges, one per CTA --
+// over weighted lengths, each row-group counting a few blocks more for the
+// fixed cost of a piece -- so every CTA has about the same work whatever the
+// length mix; a row-group cut by a range boundary is computed in pieces that
+// are merged by log-sum-exp (The Serving Playbook, "Kernel fusion, briefly":
+// Flash-Decoding splits the KV axis).
 //
 // One warp of each CTA computes the plan from seq_lens / query_start_loc in
 // device memory (a warp-wide scan over the requests), so the launch shape
@@ -81,8 +82,22 @@ __device__ __forceinline__ long long rows_blocks(const ReqInfo& ri, int i) {
   return ceil16_prefix(a + i - 1) - ceil16_prefix(a - 1) - (long long)i * ri.fb;
 }
 
-// This CTA's share [lo, hi) of the step's block sequence, and the range
-// length (chunk) every CTA uses.  Warp-collective.
+// The ranges are cut over weighted lengths: each row-group counts as its
+// blocks plus p.rowgroup_cost, the fixed cost of a piece (its epilogue, its
+// last partial tile) in blocks' worth of streaming, so that a CTA whose range
+// holds many short row-groups gets fewer blocks.  The weight's extra units
+// sit after the row-group's real blocks and hold no work.
+__device__ __forceinline__ int row_weight(const DecodeParams& p, const ReqInfo& ri, int i) {
+  return row_blocks(ri, i) + p.rowgroup_cost;
+}
+
+// Weighted length of rows 0..i-1 of a request (one KV head).
+__device__ __forceinline__ long long rows_weight(const DecodeParams& p, const ReqInfo& ri, int i) {
+  return rows_blocks(ri, i) + (long long)i * p.rowgroup_cost;
+}
+
+// This CTA's share [lo, hi) of the step's weighted block sequence, and the
+// range length (chunk) every CTA uses.  Warp-collective.
 struct Range {
   long long lo, hi, chunk;
 };
@@ -93,9 +108,9 @@ __device__ __forceinline__ long long tally_request(const DecodeParams& p, const 
                                                    long long& mine, int& nb_min, int& nb_max) {
   long long w = 0;
   if (ri.decode) {
-    w = rows_blocks(ri, ri.qr) * p.num_kv_heads;
-    nb_min = min(nb_min, row_blocks(ri, 0));
-    nb_max = max(nb_max, row_blocks(ri, ri.qr - 1));
+    w = rows_weight(p, ri, ri.qr) * p.num_kv_heads;
+    nb_min = min(nb_min, row_weight(p, ri, 0));
+    nb_max = max(nb_max, row_weight(p, ri, ri.qr - 1));
   } else if (blockIdx.x == 0 && r < p.num_reqs && ri.qr != 0 && ri.qr < p.prefill_min_q) {
     record_error(p.err, kErrBounds);  // inconsistent lengths: request skipped
   }
@@ -184,7 +199,7 @@ struct Walker {
       long long w = 0;
       if (rr < R) {
         const ReqInfo q = load_request(p, rr);
-        if (q.decode) w = rows_blocks(q, q.qr) * Hkv;
+        if (q.decode) w = rows_weight(p, q, q.qr) * Hkv;
       }
       long long incl = w;
       #pragma unroll
@@ -221,53 +236,62 @@ struct Walker {
       int a = 0, b = ri.qr - 1;
       while (a < b) {
         const int mid = (a + b + 1) / 2;
-        if (pos + rows_blocks(ri, mid) * Hkv <= rg.lo) a = mid; else b = mid - 1;
+        if (pos + rows_weight(p, ri, mid) * Hkv <= rg.lo) a = mid; else b = mid - 1;
       }
       i = a;
     }
-    g = pos + rows_blocks(ri, i) * Hkv;  // start of row i, head 0
-    nb = row_blocks(ri, i);
+    g = pos + rows_weight(p, ri, i) * Hkv;  // start of row i, head 0
+    nb = row_weight(p, ri, i);
     k = (int)div_ll(rg.lo - g, nb);
     g += (long long)k * nb;
     done = g >= rg.hi;
   }
 
-  // The current piece, then advance.  False when the range is exhausted.
+  // The next piece of the range, then advance.  False when the range is
+  // exhausted.  A row-group's real blocks are [g, g + nb - rowgroup_cost) of
+  // its weighted extent [g, g + nb); a range that meets only the rest of it
+  // has no piece of that row-group.
   __device__ __forceinline__ bool next(const DecodeParams& p, Piece& pc) {
-    if (done) return false;
-    const long long s0 = max(g, rg.lo), s1 = min(g + nb, rg.hi);
-    const long long c0 = div_ll(g, rg.chunk), c1 = div_ll(g + nb - 1, rg.chunk);
-    pc.row = ri.q0 + i;
-    pc.r = r;
-    pc.k = k;
-    pc.b0 = ri.fb + (int)(s0 - g);
-    pc.pre = ri.fb > 0;
-    pc.fb = ri.fb;
-    pc.nblk = (int)(s1 - s0);
-    pc.limit = ri.L - ri.qr + i + 1;
-    pc.L = ri.L;
-    pc.fresh = (ri.L - ri.qr) / kBlockSize;
-    pc.S = (int)(c1 - c0 + 1);
-    pc.c0 = (int)c0;
-    pc.odd0 = g != c0 * rg.chunk;
-    pc.slot = 2 * (int)blockIdx.x + (s0 == rg.lo ? 0 : 1);
-    // advance to the next row-group
-    g += nb;
-    if (++k == p.num_kv_heads) {
-      k = 0;
-      if (++i == ri.qr) {
-        i = 0;
-        do {
-          ++r;
-          if (r >= p.num_reqs) break;
-          ri = load_request(p, r);
-        } while (!ri.decode);
-        if (r >= p.num_reqs) done = true;
+    while (!done) {
+      const long long nbr = nb - p.rowgroup_cost;  // real blocks
+      const long long s0 = max(g, rg.lo), s1 = min(g + nbr, rg.hi);
+      const bool emit = s0 < s1;
+      if (emit) {
+        const long long c0 = div_ll(g, rg.chunk), c1 = div_ll(g + nbr - 1, rg.chunk);
+        pc.row = ri.q0 + i;
+        pc.r = r;
+        pc.k = k;
+        pc.b0 = ri.fb + (int)(s0 - g);
+        pc.pre = ri.fb > 0;
+        pc.fb = ri.fb;
+        pc.nblk = (int)(s1 - s0);
+        pc.limit = ri.L - ri.qr + i + 1;
+        pc.L = ri.L;
+        pc.fresh = (ri.L - ri.qr) / kBlockSize;
+        pc.S = (int)(c1 - c0 + 1);
+        pc.c0 = (int)c0;
+        pc.odd0 = g != c0 * rg.chunk;
+        pc.slot = 2 * (int)blockIdx.x + (s0 == rg.lo ? 0 : 1);
       }
-      if (!done) nb = row_blocks(ri, i);
+      // advance to the next row-group
+      g += nb;
+      if (++k == p.num_kv_heads) {
+        k = 0;
+        if (++i == ri.qr) {
+          i = 0;
+          do {
+            ++r;
+            if (r >= p.num_reqs) break;
+            ri = load_request(p, r);
+          } while (!ri.decode);
+          if (r >= p.num_reqs) done = true;
+        }
+        if (!done) nb = row_weight(p, ri, i);
+      }
+      if (g >= rg.hi) done = true;
+      if (emit) return true;
     }
-    if (g >= rg.hi) done = true;
-    return true;
+    return false;
   }
 };
 
@@ -282,7 +306,7 @@ static_assert(32 * kPlanRegReqs <= kPlanCacheReqs, "plan cache too small");
 // engine step has the same lengths, so a CTA computes its plan once per step
 // and later calls compare and reuse it; the comparison is exact, so a reused
 // plan is always the plan of the current lengths.
-constexpr int kPcHeader = 10, kPcQsl = 16, kPcLens = kPcQsl + kPlanCacheReqs + 4,
+constexpr int kPcHeader = 11, kPcQsl = 16, kPcLens = kPcQsl + kPlanCacheReqs + 4,
               kPcState = kPcLens + kPlanCacheReqs, kPcStateWords = 18;
 static_assert(kPcState + kPcStateWords <= kPlanEntryWords, "plan cache entry layout");
 constexpr int kPcMagic = 0x504c414e;
@@ -298,6 +322,7 @@ __device__ __forceinline__ int plan_header_word(const DecodeParams& p, int j) {
     case 6: return p.align_slack;
     case 7: return (int)gridDim.x;
     case 8: return p.max_blocks;
+    case 9: return p.rowgroup_cost;
     default: return kPcMagic ^ p.half_grid_blocks;
   }
 }

@@ -169,7 +169,7 @@ def test_options_struct_matches_header():
 def test_options_defaults_and_round_trip(lib):
     o = pkv.get_options()
     assert o["pdl"] in (0, 1) and o["min_chunk"] >= 1 and o["wait_limit_us"] >= 1
-    assert o["debug_withhold_q"] == 0
+    assert o["debug_withhold_q"] == 0 and 0 <= o["rowgroup_cost"] <= 1024
     with pkv.options(prefill_min_q=3, decode_tc=0):
         now = pkv.get_options()
         assert now["prefill_min_q"] == 3 and now["decode_tc"] == 0
@@ -179,7 +179,8 @@ def test_options_defaults_and_round_trip(lib):
 
 
 @pytest.mark.parametrize("bad", [{"min_chunk": 0}, {"wait_limit_us": 0}, {"prefill_min_q": -1},
-                                 {"align_slack": -5}, {"decode_grid": -1}])
+                                 {"align_slack": -5}, {"decode_grid": -1},
+                                 {"rowgroup_cost": -1}, {"rowgroup_cost": 1025}])
 def test_out_of_range_options_are_rejected(lib, bad):
     o = pkv.get_options()
     with pytest.raises(pkv.PagedKVError) as e:

@@ -95,6 +95,22 @@ def test_random_ragged_steps(seed):
     _full_parity(shape, poison=bool(seed % 2))
 
 
+@pytest.mark.parametrize("g", [6, 2])
+@pytest.mark.parametrize("cost", [0, 8, 64, 1024])
+def test_rowgroup_cost_does_not_change_the_answer(cost, g, pkv_opts):
+    """The plan cuts the CTAs' ranges over weighted row-group lengths (blocks
+    plus rowgroup_cost); ranges that meet only a row-group's weight hold no
+    piece of it.  Every weight gives the oracle's answer, on the tensor-core
+    (g = 6) and SIMT (g = 2) decodes, with short, long and multi-query rows."""
+    pkv_opts(rowgroup_cost=cost)
+    rng = np.random.default_rng(600 + g)
+    lens = rng.integers(1, 900, size=40)
+    ql = np.where(rng.random(40) < 0.2, rng.integers(2, 12, size=40), 1)
+    lens = np.maximum(lens, ql)
+    shape = wl.StepShape(f"cost{cost}_g{g}", lens, ql, 2 * g, 2, seed=610 + g)
+    _full_parity(shape, poison=True)
+
+
 @pytest.mark.parametrize("g", [1, 2, 3, 4, 5, 6, 7, 8])
 def test_every_group_size(g):
     shape = wl.StepShape(f"g{g}", [1, 15, 16, 17, 200, 777], [1, 1, 2, 17, 1, 5], 2 * g, 2,
