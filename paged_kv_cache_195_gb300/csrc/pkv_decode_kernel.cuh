@@ -680,18 +680,14 @@ __global__ void __launch_bounds__(DecodeCfg<G>::kThreads) __maxnreg__(DecodeCfg<
     }
     if (ok && pc.S > 1) {
       // Ticket: the barrier orders every thread's partial stores before
-      // thread 0's fence, whose release is cumulative, then the atomic.  The
-      // piece that draws the last ticket fences again (acquire) and merges.
+      // thread 0's acquire-release atomic, whose release is cumulative; the
+      // piece that draws the last ticket has acquired the others' and merges.
       named_barrier(1, kConsumerThreads);
       if (ct == 0) {
-        __threadfence();
         int* cnt = p.ws_cnt + (long long)pc.row * Hkv + pc.k;
-        const int old = atomicAdd(cnt, 1);
+        const int old = atom_add_acq_rel_gpu(cnt, 1);
         const int last = (old == pc.S - 1);
-        if (last) {
-          *cnt = 0;  // every piece has arrived: leave the counter at zero
-          __threadfence();
-        }
+        if (last) *cnt = 0;  // every piece has arrived: leave the counter at zero
         sm.is_last = last;
       }
       named_barrier(1, kConsumerThreads);
