@@ -130,7 +130,9 @@ def test_cascade_qwen_shared_full_size_every_element():
     assert_close(to_f64(out), oracle_full(h, kp, vp), "qwen_shared")
 
 
-def test_cascade_bad_group_reported():
+def test_cascade_bad_group_reported(pkv_opts):
+    # the groups are checked by the set-up kernel of the tensor-core route
+    pkv_opts(decode_tc=1)
     shape = wl.StepShape("cascade_bad", [64, 64], [1, 1], 8, 2, seed=316,
                          prefix_groups=((0, 2, 2),))
     inp = wl.make_step(shape, device="cuda")

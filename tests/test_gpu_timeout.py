@@ -56,7 +56,8 @@ def test_withheld_q_times_out_and_the_next_call_is_correct(pkv_opts):
     torch.cuda.synchronize()
     assert pkv.pkv_get_device_error() == 0
 
-    pkv_opts(wait_limit_us=1000, debug_withhold_q=1)
+    # the withheld q is a feature of the tensor-core decode
+    pkv_opts(wait_limit_us=1000, debug_withhold_q=1, decode_tc=1)
     out = torch.full_like(inp.q, float("nan"))
     t0 = time.perf_counter()
     pkv.pkv_attention(inp.q, inp.k_pool, inp.v_pool, inp.block_tables, inp.seq_lens,
@@ -88,7 +89,7 @@ def test_withheld_q_times_out_on_e4m3_pools(pkv_opts):
     ws = pkv.Workspace(d)
     pkv.pkv_workspace_init(ws, d)
 
-    pkv_opts(wait_limit_us=1000, debug_withhold_q=1)
+    pkv_opts(wait_limit_us=1000, debug_withhold_q=1, decode_tc=1, decode_tc_fp8=1)
     out = torch.full_like(inp.q, float("nan"))
     pkv.pkv_attention_fp8kv(inp.q, inp.k_pool, inp.v_pool, inp.k_scale, inp.v_scale,
                             inp.block_tables, inp.seq_lens, inp.query_start_loc, inp.scale,
