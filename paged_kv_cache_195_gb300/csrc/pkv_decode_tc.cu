@@ -94,13 +94,14 @@ constexpr int kWindow = 32;                // block-table entries loaded at a ti
 
 // Debug-only per-tile timeline of CTA 0 (build with -DPKV_TC_TRACE=1):
 // %globaltimer at load issue, keys seen by the MMA warp, scores seen by the
-// softmax, PV issue, and slot release seen by the producer.
+// softmax, PV issue, and slot release seen by the producer; e4m3 pools also
+// K (7) and V (8) widened by the converters.
 #ifndef PKV_TC_TRACE
 #define PKV_TC_TRACE 0
 #endif
 #if PKV_TC_TRACE
 constexpr int kTrTiles = 64;
-__device__ unsigned long long g_tc_trace[7][kTrTiles];
+__device__ unsigned long long g_tc_trace[9][kTrTiles];
 #define TC_TR(ev, tile) do { if (blockIdx.x == 0 && (tile) < kTrTiles) g_tc_trace[ev][tile] = global_timer_ns(); } while (0)
 #else
 #define TC_TR(ev, tile) do { } while (0)
@@ -886,6 +887,7 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 2) __maxnreg__
         mbar_arrive(&sm.raw_empty[s]);
         mbar_arrive(&sm.kt_full[t & 1]);
       }
+      if (r == 0) TC_TR(7, t);
       return true;
     };
     auto convert_v = [&](int t) -> bool {
@@ -900,6 +902,7 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 2) __maxnreg__
         mbar_arrive(&sm.raw_empty[s]);
         mbar_arrive(&sm.v_full);
       }
+      if (r == 0) TC_TR(8, t);
       return true;
     };
     if (convert_k(0)) {
