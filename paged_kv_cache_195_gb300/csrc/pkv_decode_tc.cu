@@ -346,21 +346,31 @@ __device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32
 }
 
 // Row `row` of a raw e4m3 tile (128 codes, 128-byte swizzle) widened to f16
-// into the V operand: d 0..63 in half0, d 64..127 in half1, the same
-// swizzled row layout a bf16 tile has; rows past the request's end (which may
-// hold any code, NaN included) become zeros, so that 0 * V stays 0.
-__device__ __forceinline__ void widen_e4m3_row_to(const uint8_t* raw, uint8_t* half0,
-                                                  uint8_t* half1, int row, bool zero) {
+// in registers: h[8 c8 + i] holds d 16 c8 + 2i, +1 (low half first); a row
+// past the request's end (which may hold any code, NaN included) becomes
+// zeros, so that 0 * V stays 0.
+__device__ __forceinline__ void widen_e4m3_row(const uint8_t* raw, int row, bool zero,
+                                               uint32_t (&h)[64]) {
   const int sw = row & 7;
   #pragma unroll
   for (int c8 = 0; c8 < 8; ++c8) {
     const uint4 v = zero ? make_uint4(0, 0, 0, 0) : lds128(raw + row * 128 + ((c8 ^ sw) * 16));
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t b[8];
     #pragma unroll
-    for (int j = 0; j < 4; ++j) e4m3x4_to_f16x4(w[j], b[2 * j], b[2 * j + 1]);
+    for (int j = 0; j < 4; ++j) e4m3x4_to_f16x4(w[j], h[c8 * 8 + 2 * j], h[c8 * 8 + 2 * j + 1]);
+  }
+}
+
+// The widened row into the V operand: d 0..63 in half0, d 64..127 in half1,
+// the same swizzled row layout a bf16 tile has.
+__device__ __forceinline__ void store_f16_row(const uint32_t (&h)[64], uint8_t* half0,
+                                              uint8_t* half1, int row) {
+  const int sw = row & 7;
+  #pragma unroll
+  for (int c8 = 0; c8 < 8; ++c8) {
     uint8_t* dst = (c8 < 4 ? half0 : half1) + row * 128;
     const int c = (c8 & 3) * 2;
+    const uint32_t* b = &h[c8 * 8];
     *reinterpret_cast<uint4*>(dst + ((c ^ sw) * 16)) = make_uint4(b[0], b[1], b[2], b[3]);
     *reinterpret_cast<uint4*>(dst + (((c + 1) ^ sw) * 16)) = make_uint4(b[4], b[5], b[6], b[7]);
   }
@@ -894,14 +904,18 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 2) __maxnreg__
       const int n = 2 * t + 1, s = n % kRawSlots;
       if (!tc_wait<F8>(&sm.raw_full[s], (n / kRawSlots) & 1, p.err, abort_flag)) return false;
       if (n >= *reinterpret_cast<volatile int*>(&sm.conv_end)) return false;
+      // The row is widened into registers while the previous tile's PV may
+      // still be reading the V operand, and its raw slot goes back at once;
+      // only the stores wait for that PV.
+      uint32_t hv[64];
+      widen_e4m3_row(sm.f8.raw[s], r, r >= sm.raw_valid[s], hv);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.raw_empty[s]);
       if (t >= 1 && !tc_wait<F8>(&sm.v_free, (t - 1) & 1, p.err, abort_flag)) return false;
-      widen_e4m3_row_to(sm.f8.raw[s], sm.f8.vbuf[0], sm.f8.vbuf[1], r, r >= sm.raw_valid[s]);
+      store_f16_row(hv, sm.f8.vbuf[0], sm.f8.vbuf[1], r);
       fence_proxy_async_smem();  // generic-proxy writes, read by the tensor core
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&sm.raw_empty[s]);
-        mbar_arrive(&sm.v_full);
-      }
+      if (lane == 0) mbar_arrive(&sm.v_full);
       if (r == 0) TC_TR(8, t);
       return true;
     };
