@@ -693,26 +693,39 @@ __global__ void __launch_bounds__(DecodeCfg<G>::kThreads) __maxnreg__(DecodeCfg<
       named_barrier(1, kConsumerThreads);
       if (sm.is_last) {
         // Log-sum-exp merge of the row-group's pieces, in piece order, one
-        // pass with a running maximum; loads of four pieces are in flight at
-        // once.
-        #pragma unroll 1
-        for (int idx = ct; idx < G * kHeadDim; idx += kConsumerThreads) {
-          const int h = idx / kHeadDim, d = idx % kHeadDim;
-          float M = kNegBig, num = 0.f, den = 0.f;
-          #pragma unroll 4
-          for (int s = 0; s < pc.S; ++s) {
-            const int slot = 2 * (pc.c0 + s) + ((s == 0 && pc.odd0) ? 1 : 0);
-            const long long sl = (long long)slot * G + h;
-            const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.ws_ml + sl * 2));
-            const float o = __ldcg(p.ws_o + sl * kHeadDim + d);
-            const float Mn = fmaxf(M, ml.x);
-            const float a = fast_exp2(M - Mn), w = fast_exp2(ml.x - Mn) * ml.y;
-            num = num * a + w * o;
-            den = den * a + w;
-            M = Mn;
-          }
-          p.out[out_row + h * kHeadDim + d] = __float2bfloat16_rn(num / den * vscale);
+        // pass with a running maximum; each piece's states of every head this
+        // thread merges are loaded together (one L2 round trip per piece).
+        static_assert(kConsumerThreads == kHeadDim, "one output dim per consumer thread");
+        const int d = ct;
+        float M[G], num[G], den[G];
+        #pragma unroll
+        for (int h = 0; h < G; ++h) {
+          M[h] = kNegBig;
+          num[h] = den[h] = 0.f;
         }
+        #pragma unroll 1
+        for (int s = 0; s < pc.S; ++s) {
+          const int slot = 2 * (pc.c0 + s) + ((s == 0 && pc.odd0) ? 1 : 0);
+          float2 ml[G];
+          float o[G];
+          #pragma unroll
+          for (int h = 0; h < G; ++h) {
+            const long long sl = (long long)slot * G + h;
+            ml[h] = __ldcg(reinterpret_cast<const float2*>(p.ws_ml + sl * 2));
+            o[h] = __ldcg(p.ws_o + sl * kHeadDim + d);
+          }
+          #pragma unroll
+          for (int h = 0; h < G; ++h) {
+            const float Mn = fmaxf(M[h], ml[h].x);
+            const float a = fast_exp2(M[h] - Mn), w = fast_exp2(ml[h].x - Mn) * ml[h].y;
+            num[h] = num[h] * a + w * o[h];
+            den[h] = den[h] * a + w;
+            M[h] = Mn;
+          }
+        }
+        #pragma unroll
+        for (int h = 0; h < G; ++h)
+          p.out[out_row + h * kHeadDim + d] = __float2bfloat16_rn(num[h] / den[h] * vscale);
       }
     }
     // Close the piece: nobody rewrites comb/is_last before everyone is done.
