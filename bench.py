@@ -570,18 +570,25 @@ def measure_extra(pkv, config, kv, device, rank, args, local):
     flops = rl.attention_flops(shape.seq_lens, shape.q_lens, shape.num_q_heads)
     if shape.num_q_tokens > shape.num_reqs:
         rec["attention_tflops_per_layer_call"] = round(flops / 1e12, 4)
-    if int((shape.q_lens > 1).sum()) == shape.num_reqs:
-        # every request is a prefill chunk: the tensor-core roofline (a
-        # contraction timed alone takes the burst bf16 peak)
-        tpk, tsrc = measured_tensor_peak()
-        ach = flops / (statistics.mean(durs) * 1e-3) / 1e12
-        rec["tensor_roofline"] = {"bound": "tensor", "achieved": round(ach, 1), "peak": tpk,
-                                  "unit": "TFLOP/s", "frac": round(ach / tpk, 4),
-                                  "peak_source": tsrc,
-                                  "flops_per_launch": flops}
+    troof = tensor_roofline(shape, durs)
+    if troof is not None:
+        rec["tensor_roofline"] = troof
     del run
     torch.cuda.empty_cache()
     return rec
+
+
+def tensor_roofline(shape, durs):
+    """The tensor-core roofline of a step whose every request is a prefill
+    chunk (a contraction timed alone takes the burst bf16 peak); None for a
+    step with decode requests, which HBM bounds."""
+    if int((shape.q_lens > 1).sum()) != shape.num_reqs:
+        return None
+    flops = rl.attention_flops(shape.seq_lens, shape.q_lens, shape.num_q_heads)
+    tpk, tsrc = measured_tensor_peak()
+    ach = flops / (statistics.mean(durs) * 1e-3) / 1e12
+    return {"bound": "tensor", "achieved": round(ach, 1), "peak": tpk, "unit": "TFLOP/s",
+            "frac": round(ach / tpk, 4), "peak_source": tsrc, "flops_per_launch": flops}
 
 
 def run_ours(args):
@@ -632,6 +639,7 @@ def run_ours(args):
     kernels_per_layer = run.kernels_per_layer()
     value = bytes_per_step * ws_n / (ms_step * 1e-3) / 1e9
     roof = run.roofline(durs, args.config, None)
+    troof = tensor_roofline(shape, durs)
     h2d, d2h = run.h2d, run.d2h
     layers_cpu = run.layers[:2]
     del run
@@ -673,6 +681,8 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "configs": extras,
     }
+    if troof is not None:
+        line["tensor_roofline"] = troof
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws_n > 1:

@@ -357,9 +357,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         if (it.end || !stream_item(it)) break;
       }
     } else {
-      // Items are numbered request by request (heavier q-tiles first within
-      // a request) and taken from the queue in that order, so each CTA's
-      // sequence increases and one forward scan over the requests serves it.
+      // Items are numbered batch of 32 requests by batch, request by request
+      // within a batch (longest first; heavier q-tiles first within a
+      // request), and taken from the queue in that order, so each CTA's
+      // sequence increases and one forward scan over the batches serves it.
       auto next_item = [&]() {
         unsigned long long v = 0;
         if (lane == 0) v = atomicAdd(p.sched, 1ull);
@@ -386,14 +387,26 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         PfReq rq = {0, 0, 0, 0, 0, 1, false};
         if (rr < nunits) rq = load_pf_request(p, rr, TQ);
         const long long cnt = (long long)rq.ntiles * Hkv;
-        long long incl = cnt;
+        long long total = cnt;
         #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const long long t = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += t;
+        for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
+        if (item >= base + total) {  // no item of this batch left for this CTA
+          base += total;
+          continue;
         }
-        const long long excl = incl - cnt;
-        const long long total = __shfl_sync(0xffffffffu, incl, 31);
+        // Within a batch of 32 requests the longest go first (then by index):
+        // a request's items cost about L / 128 key tiles each, and taking
+        // the longest first leaves short items for the queue's end, where
+        // the CTAs run out of work at different times.
+        const int key = cnt > 0 ? rq.L : -1;
+        long long excl = 0;
+        #pragma unroll 4
+        for (int s = 0; s < 32; ++s) {
+          const int ks = __shfl_sync(0xffffffffu, key, s);
+          const long long cs = __shfl_sync(0xffffffffu, cnt, s);
+          if (ks > key || (ks == key && s < lane)) excl += cs;
+        }
+        const long long incl = excl + cnt;
         while (item < base + total && ok && !abort_flag->abort) {
           const long long rel = item - base;
           const unsigned own = __ballot_sync(0xffffffffu, cnt > 0 && excl <= rel && rel < incl);
