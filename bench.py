@@ -227,7 +227,8 @@ class GraphEvents:
 # over shuffled pools, plus the append that feeds it): the long batch, the
 # mixed continuous-batching step, the long-context step, and the e4m3 cache on
 # the two Qwen-shaped decodes.
-EXTRA_CONFIGS = (("qwen_long", "bf16"), ("llama_mixed", "bf16"), ("llama_long", "bf16"),
+EXTRA_CONFIGS = (("qwen_long", "bf16"), ("llama_mixed", "bf16"), ("llama_decode", "bf16"),
+                 ("llama_long", "bf16"),
                  ("qwen_decode", "fp8"), ("qwen_long", "fp8"))
 
 

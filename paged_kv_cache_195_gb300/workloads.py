@@ -130,7 +130,8 @@ def llama_mixed(num_decode: int = 248, num_prefill: int = 8,
     seq = np.concatenate([dec, prefix + chunk]).astype(np.int32)
     ql = np.concatenate([np.ones(num_decode, np.int32),
                          np.full(num_prefill, chunk, np.int32)])
-    return StepShape("llama3-8b_mixed_d248_p8x512", seq, ql, 32, 8, seed=195)
+    return StepShape(f"llama3-8b_mixed_d{num_decode}_p{num_prefill}x{chunk}", seq, ql, 32, 8,
+                     seed=195)
 
 
 def llama_long_context() -> StepShape:
@@ -162,6 +163,7 @@ CONFIGS = {
     "llama_mixed": llama_mixed,
     "llama_long": llama_long_context,
     "llama_prefill": lambda: llama_mixed(num_decode=0),
+    "llama_decode": lambda: llama_mixed(num_prefill=0),
     "qwen_shared": qwen_shared_prefix,
     "qwen_shared_long": qwen_shared_long,
 }
