@@ -643,42 +643,10 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 2) __maxnreg__
         int row = oob_row;
         if ((unsigned)phys < (unsigned)p.num_blocks) row = (phys * Hkv + k) * kBlockSize;
         else if (phys != kPastPiece && hsel == 0 && lane < 16) record_error(p.err, kErrBounds);
-        #pragma unroll 1
-        for (int kv = 0; kv < 2 && ok; ++kv) {
-          const int n = 2 * t + kv;  // ring occupant: K (kv = 0) or V (kv = 1) of tile t
-          const int s = n % kRing;
-          uint64_t* rel = F8 ? &sm.raw_empty[s] : &sm.empty[s];
-          if (n >= kRing && !tc_wait<F8>(rel, ((n / kRing) - 1) & 1, p.err, abort_flag)) {
-            ok = false;
-            break;
-          }
-          if (lane == 0 && kv == 0 && t >= 2) TC_TR(4, t - 2);
-          if (lane == 0 && kv == 0) TC_TR(0, t);
-          if (lane == 0 && t == 0 && kv == 0) TC_CTA(3);
-          if (lane == 0) {
-            if (F8) {
-              // rows of this tile holding keys before the request's end
-              const int key0 = (pc.b0 + tt * kBlkPerTile) * kBlockSize;
-              sm.raw_valid[s] = max(0, min(kTile, pc.L - key0));
-              mbar_arrive_expect_tx(&sm.raw_full[s], (uint32_t)kRawTile);
-            } else {
-              mbar_arrive_expect_tx(&sm.full[s], 2u * kHalf);
-            }
-          }
-          __syncwarp();
-          const CUtensorMap* map = kv == 0 ? &kmap : &vmap;
-          if (F8) {
-            if (lane < 8) tma_load_2d(sm.f8.raw[s] + bsel * 2048, map, 0, row, &sm.raw_full[s], pol);
-          } else if (lane < 16) {
-            tma_load_2d(sm.slot[s][hsel] + bsel * 2048, map, hsel * 64, row, &sm.full[s], pol);
-          }
-          __syncwarp();
-          n_occ = n + 1;
-        }
-        if (!ok) break;
         if (tt == 0) {
-          // Q of this piece, once the MMAs of piece j-2 are done with its
-          // buffer (the piece's first K/V tile is already on its way).
+          // Q of this piece ahead of its first K/V tile (its copy is the
+          // smallest and the first MMA needs it), once the MMAs of piece j-2
+          // are done with its buffer.
           const int ub = j & 1;
           if (j >= 2) {
             // (the launch wait is taken: from the third tile on, 2t + 1 >=
@@ -715,6 +683,39 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 2) __maxnreg__
                                       pc.fb * kBlockSize, lane);
           __syncwarp();
         }
+        #pragma unroll 1
+        for (int kv = 0; kv < 2 && ok; ++kv) {
+          const int n = 2 * t + kv;  // ring occupant: K (kv = 0) or V (kv = 1) of tile t
+          const int s = n % kRing;
+          uint64_t* rel = F8 ? &sm.raw_empty[s] : &sm.empty[s];
+          if (n >= kRing && !tc_wait<F8>(rel, ((n / kRing) - 1) & 1, p.err, abort_flag)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0 && kv == 0 && t >= 2) TC_TR(4, t - 2);
+          if (lane == 0 && kv == 0) TC_TR(0, t);
+          if (lane == 0 && t == 0 && kv == 0) TC_CTA(3);
+          if (lane == 0) {
+            if (F8) {
+              // rows of this tile holding keys before the request's end
+              const int key0 = (pc.b0 + tt * kBlkPerTile) * kBlockSize;
+              sm.raw_valid[s] = max(0, min(kTile, pc.L - key0));
+              mbar_arrive_expect_tx(&sm.raw_full[s], (uint32_t)kRawTile);
+            } else {
+              mbar_arrive_expect_tx(&sm.full[s], 2u * kHalf);
+            }
+          }
+          __syncwarp();
+          const CUtensorMap* map = kv == 0 ? &kmap : &vmap;
+          if (F8) {
+            if (lane < 8) tma_load_2d(sm.f8.raw[s] + bsel * 2048, map, 0, row, &sm.raw_full[s], pol);
+          } else if (lane < 16) {
+            tma_load_2d(sm.slot[s][hsel] + bsel * 2048, map, hsel * 64, row, &sm.full[s], pol);
+          }
+          __syncwarp();
+          n_occ = n + 1;
+        }
+        if (!ok) break;
       }
       ++j;
       advance();
@@ -1121,7 +1122,7 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 2) __maxnreg__
         if (okO) {
           #pragma unroll
           for (int h = 0; h < G; ++h) {
-            float res = lt[h] > 0.f ? o[h] * __frcp_rn(lt[h]) : 0.f;
+            float res = lt[h] > 0.f ? __fdividef(o[h], lt[h]) : 0.f;
             if (pc.pre) {
               float M = m[h], num = lt[h] * res, den = lt[h];
               fold_prefix(h, M, num, den);
