@@ -368,10 +368,6 @@ typedef struct pkv_options {
     int32_t decode_grid;    /* PKV_DECODE_GRID (0): decode grid in CTAs (0: the
                                default for the kernel and group size; tuning only,
                                at most twice the SM count) */
-    int32_t warm_kv;        /* PKV_WARM_KV (0): tensor-core decode: before its launch
-                               wait, warm L2 with the K/V blocks of each CTA's first
-                               eight tiles (1: bulk prefetches, 2: per-line
-                               prefetches; hints, results do not change) */
     int32_t wait_limit_us;  /* PKV_WAIT_LIMIT_US (2000000): a bounded device wait gives
                                up after this many microseconds and reports
                                PKV_ERR_TIMEOUT (>= 1) */

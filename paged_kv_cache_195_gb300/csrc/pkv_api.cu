@@ -124,7 +124,7 @@ int env_int(const char* name, int dflt) {
 
 bool options_valid(const pkv_options& o) {
   return o.prefill_min_q >= 0 && o.align_slack >= 0 && o.min_chunk >= 1 && o.decode_grid >= 0 &&
-         o.warm_kv >= 0 && o.warm_kv <= 2 && o.wait_limit_us >= 1 && o.rowgroup_cost >= 0 &&
+         o.wait_limit_us >= 1 && o.rowgroup_cost >= 0 &&
          o.rowgroup_cost <= 1024;
 }
 
@@ -143,7 +143,6 @@ pkv_options options_from_env() {
   o.min_chunk = env_int("PKV_MIN_CHUNK", 4);
   o.prefetch = env_int("PKV_PREFETCH", 1);
   o.decode_grid = env_int("PKV_DECODE_GRID", 0);
-  o.warm_kv = env_int("PKV_WARM_KV", 0);
   o.wait_limit_us = env_int("PKV_WAIT_LIMIT_US", (int)(pkv::kDefaultWaitLimitNs / 1000));
   o.debug_withhold_q = 0;  // never from the environment
   o.rowgroup_cost = env_int("PKV_ROWGROUP_COST", 16);
@@ -152,7 +151,6 @@ pkv_options options_from_env() {
   if (o.align_slack < 0) o.align_slack = 64;
   if (o.min_chunk < 1) o.min_chunk = 4;
   if (o.decode_grid < 0) o.decode_grid = 0;
-  if (o.warm_kv < 0 || o.warm_kv > 2) o.warm_kv = 0;
   if (o.wait_limit_us < 1) o.wait_limit_us = (int)(pkv::kDefaultWaitLimitNs / 1000);
   if (o.rowgroup_cost < 0 || o.rowgroup_cost > 1024) o.rowgroup_cost = 16;
   return o;
@@ -527,7 +525,6 @@ int attention_impl(const void* q, const void* k_pool, const void* v_pool, const 
   p.align_slack = opt.align_slack;
   p.prefetch = opt.prefetch != 0;
   p.early_plan = p.pdl && opt.early_plan != 0;
-  p.warm_kv = opt.warm_kv;
   p.wait_limit_ns = (unsigned long long)opt.wait_limit_us * 1000ull;
   p.debug_withhold_q = opt.debug_withhold_q != 0;
   p.rowgroup_cost = opt.rowgroup_cost;

@@ -32,20 +32,18 @@
 // Two CTAs per SM.  A CTA takes 111 KB of shared memory and 192 threads, so
 // the next launch's CTAs (the next layer of an engine step) become resident
 // beside this launch's as soon as it lets them launch: they plan, allocate
-// TMEM and warm L2 with their first K/V blocks while this launch streams,
+// TMEM and load their first block-table entries while this launch streams,
 // and start copying the moment it completes.  K and V tiles share one ring
 // of three 32 KiB slots (K of tile t, then V of tile t), a K slot freed as
-// soon as its S^T is computed, a V slot when its PV is.  Optionally
-// (warm_kv) the producer also warms L2 with the K/V blocks of its first eight
-// tiles before the wait (prefetches: hints, with no effect on results).
+// soon as its S^T is computed, a V slot when its PV is.
 //
 // Roles (192 threads): warps 0-3 run the softmax and, at the end of each
 // piece, its epilogue (normalise, write the output or a partial piece, merge,
-// fold a shared prefix's states); warp 4 plans, warms L2 and issues the TMA
-// copies (it plans before the CTA's set-up, and K/V tiles are evict-first in
-// L2: each is read once); one thread of warp 5 issues the MMAs.  e4m3 pools
-// add warps 6-7 (256 threads), which widen each slot's codes to f16 in
-// shared memory; Q and P are then f16 too.  S and O^T are double buffered in
+// fold a shared prefix's states); warp 4 plans and issues the TMA copies (it
+// plans before the CTA's set-up, and K/V tiles are evict-first in L2: each
+// is read once); one thread of warp 5 issues the MMAs.  e4m3 pools add warps
+// 6-9 (320 threads), which widen the codes to f16: K tiles into TMEM, V tiles
+// into a shared-memory operand; Q and P are then f16 too.  S and O^T are double buffered in
 // TMEM, so the MMAs of the next piece proceed while the softmax warps finish
 // the previous one.
 // The running maximum is raised only when a score exceeds it by more than
@@ -111,8 +109,7 @@ __device__ unsigned long long g_tc_trace[9][kTrTiles];
 // set-up done, 2 producer ready, 3 first load issued, 4 first keys seen by the
 // MMA warp, 5 last PV issued, 6 last piece written, 7 exit, 8 SM id + 1, 9
 // grid-dependency wait taken (early_kv), 10 plan done, 11 first pieces
-// known, 12 first blocks warmed in L2, 16 O read from TMEM, 17 last O commit
-// issued.
+// known, 16 O read from TMEM, 17 last O commit issued.
 #if PKV_TC_TRACE >= 3
 // Slots by the out pointer, so that consecutive launches keep their own.
 constexpr int kTrCtas = 256, kTrSlots = 32;
@@ -425,28 +422,6 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 2) __maxnreg__
     return x < q.nblk ? __ldg(p.block_tables + (long long)q.r * p.max_blocks + q.b0 + x)
                       : kPastPiece;
   };
-  // Warms L2 with one window's K and V blocks of KV head kh (lane = block),
-  // before this kernel may read the pools (the prefetches are hints: L2 stays
-  // coherent with any write of the kernel before).  warm_kv 1: one bulk
-  // prefetch per block and tensor; 2: one prefetch instruction per 128-byte
-  // line, through the load path rather than the copy engine.  Blocks past the
-  // piece and ids outside the pool are skipped.
-  constexpr uint32_t kBlkBytes = F8 ? kBlockSize * kHeadDim : kBlockSize * kHeadDim * 2;
-  auto warm = [&](int ent, int kh) {
-    if (p.warm_kv && (unsigned)ent < (unsigned)p.num_blocks && kh >= 0 && kh < Hkv) {
-      const long long off = ((long long)ent * Hkv + kh) * kBlkBytes;
-      if (p.warm_kv == 1) {
-        prefetch_l2_bulk(p.k_pool + off, kBlkBytes);
-        prefetch_l2_bulk(p.v_pool + off, kBlkBytes);
-      } else {
-        #pragma unroll 4
-        for (uint32_t b = 0; b < kBlkBytes; b += 128) {
-          asm volatile("prefetch.global.L2 [%0];" ::"l"(p.k_pool + off + b));
-          asm volatile("prefetch.global.L2 [%0];" ::"l"(p.v_pool + off + b));
-        }
-      }
-    }
-  };
   // The next piece becomes the current one and the one after it is fetched
   // (with its first block-table entries, in flight during the next call).
   auto advance = [&]() {
@@ -469,15 +444,6 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 2) __maxnreg__
     for (int i = 0; i < 2; ++i) advance();
     if (lane == 0) TC_CTA(11);
   };
-  // The first eight tiles' blocks into L2: the first piece's two windows, or
-  // its window and the next piece's.
-  auto warm_first = [&]() {
-    if (!have) return;
-    warm(ent_w0, pc.k);
-    if (pc.nblk > kWindow) warm(ent_w1, pc.k);
-    else if (have_n) warm(ent_n0, pn.k);
-    if (lane == 0) TC_CTA(12);
-  };
   // One call site for the plan (its code is large): without early_plan its
   // inputs may belong to the kernel before, so the producer waits first.
   if (warp == 4) {
@@ -486,7 +452,6 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 2) __maxnreg__
       allow_dependent_launch();
     }
     plan_first();
-    if (early_plan) warm_first();
     // The entries must be in registers before the wait below: a volatile
     // use keeps the compiler from sinking their loads past it.
     asm volatile("" ::"r"(ent_w0), "r"(ent_w1), "r"(ent_n0), "r"(ent_n1));
@@ -556,11 +521,11 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 2) __maxnreg__
   const uint32_t tmem = sm.tmem_base;
   if (tid == 0) TC_CTA(1);
   // Consumers wait for the previous kernel on the stream here; the producer
-  // builds its plan, loads its first block-table entries and warms L2 with
-  // the first tiles first (it reads only seq_lens, query_start_loc and
-  // block_tables, which with early_plan set the previous kernel does not
-  // write; the L2 prefetches are hints).  Each thread lets the next kernel
-  // launch only after its own wait.
+  // builds its plan and loads its first block-table entries first (it reads
+  // only seq_lens, query_start_loc and block_tables, which with early_plan
+  // set the previous kernel does not write; the block-table prefetches are
+  // hints).  Each thread lets the next kernel launch only after its own
+  // wait.
   //
   // With early_kv the previous kernel is the append of this step's new
   // tokens: before the wait this kernel reads the lengths, the block table
@@ -576,7 +541,7 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 2) __maxnreg__
   }
 
   if (warp == 4) {
-    // ===================== plan + L2 warming + TMA producer ==================
+    // ========================= plan + TMA producer =========================
     bool waited = !p.early_kv;
     if (p.early_plan && !p.early_kv) {
       grid_dependency_wait();

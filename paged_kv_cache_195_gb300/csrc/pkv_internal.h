@@ -86,8 +86,6 @@ struct DecodeParams {
   // If the step has at most this many blocks per CTA of half the grid, only
   // the first half of the grid takes work (0: the whole grid always does).
   int half_grid_blocks;
-  int warm_kv;        // tensor-core decode: warm L2 with the first K/V blocks before the
-                      // PDL wait (0 off, 1 bulk prefetches, 2 per-line prefetches)
   // The kernel before this one on the stream is the append of exactly this
   // step's new tokens (positions L - q_r .. L - 1 of each request): q, the
   // block table and every K/V tile holding none of those positions are read
