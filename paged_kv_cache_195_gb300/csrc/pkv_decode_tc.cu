@@ -318,6 +318,18 @@ static __device__ __noinline__ void rescale_ot(uint32_t tO, Alpha8 alpha) {
   tc_wait_st();
 }
 
+// Key row `row` of a staged bf16 V tile (both 64-dim halves, 128-byte
+// swizzled rows) set to zero.  Out of line: it runs only in a request's last
+// tile, and only when the request ends inside a block.
+static __device__ __noinline__ void zero_v_row(uint8_t* half0, uint8_t* half1, int row) {
+  #pragma unroll
+  for (int hf = 0; hf < 2; ++hf) {
+    uint4* vr = reinterpret_cast<uint4*>((hf ? half1 : half0) + (row >> 3) * 1024 + (row & 7) * 128);
+    #pragma unroll
+    for (int c = 0; c < 8; ++c) vr[c] = make_uint4(0, 0, 0, 0);
+  }
+}
+
 // An aborted CTA's producer: waits (bounded) for the copies still in flight
 // -- ring occupants n_occ - ring .. n_occ - 1 (barriers full[n % ring]) --
 // before the CTA's shared memory is released.  Out of line in the e4m3
@@ -1024,12 +1036,7 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 2) __maxnreg__
         if (!F8 && x < pc.nblk && pos >= pc.L) {
           const int n = 2 * t + 1, sv = n % kSlots;
           ok = ok && tc_wait<F8>(&sm.full[sv], (n / kSlots) & 1, p.err, abort_flag);
-          #pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            uint4* vr = reinterpret_cast<uint4*>(sm.slot[sv][hf] + (row >> 3) * 1024 + (row & 7) * 128);
-            #pragma unroll
-            for (int c = 0; c < 8; ++c) vr[c] = make_uint4(0, 0, 0, 0);
-          }
+          zero_v_row(sm.slot[sv][0], sm.slot[sv][1], row);
         }
         fence_proxy_async_smem();
         tc_fence_before();
