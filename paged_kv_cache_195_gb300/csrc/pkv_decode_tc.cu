@@ -238,6 +238,28 @@ static __device__ __noinline__ PrefixFold fold_prefix_states(const float* pre_o,
   return f;
 }
 
+// The G heads' states of one output dim: running max, normaliser, output.
+struct HeadStates8 {
+  float m[8], l[8], o[8];
+};
+
+// A shared-prefix row's output (dim d of its G heads; out: the first head's):
+// this piece's states folded with the prefix pass's partial states of the
+// `shared` keys.  Out of line: cascade calls only.
+template <int G>
+static __device__ __noinline__ void write_prefixed(const float* pre_o, const float* pre_ml,
+                                                   __nv_bfloat16* out, long long rh0,
+                                                   long long stride, int shared, int d,
+                                                   HeadStates8 st) {
+  #pragma unroll
+  for (int h = 0; h < G; ++h) {
+    const float res = st.l[h] > 0.f ? __fdividef(st.o[h], st.l[h]) : 0.f;
+    const PrefixFold f = fold_prefix_states(pre_o, pre_ml, rh0 + h, stride, shared, d,
+                                            PrefixFold{st.m[h], st.l[h] * res, st.l[h]});
+    out[h * kHeadDim] = __float2bfloat16_rn(f.den > 0.f ? f.num / f.den : 0.f);
+  }
+}
+
 // The last piece of a split row-group to arrive: merges the pieces' partial
 // states of output dim d (each a normalised output and its (max,
 // normaliser), in workspace slots 2 (c0 + s) (+1 for piece 0 when odd0)) by
@@ -1078,30 +1100,27 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 2) __maxnreg__
                             2 * (pc.c0 + pc.S) <= p.num_slots && pc.slot >= 0 &&
                             pc.slot < p.num_slots;
       const long long out_row = ((long long)pc.row * p.num_q_heads + (long long)pc.k * G) * kHeadDim;
-      // Shared-prefix (cascade) rows: fold in the prefix pass's partial
-      // states (pc.b0 is at least the shared block count, and the row's
-      // first piece starts exactly there).
-      auto fold_prefix = [&](int h, float& M, float& num, float& den) {
-        const PrefixFold f = fold_prefix_states(
-            p.pre_o, p.pre_ml, (long long)pc.row * p.num_q_heads + (long long)pc.k * G + h,
-            (long long)p.num_q_tokens * p.num_q_heads, pc.fb * kBlockSize, d,
-            PrefixFold{M, num, den});
-        M = f.M;
-        num = f.num;
-        den = f.den;
-      };
       if (in_range && pc.S == 1) {
-        if (okO) {
+        if (!okO) {
+        } else if (pc.pre) {
+          // Shared-prefix (cascade) row: fold in the prefix pass's partial
+          // states (pc.b0 is at least the shared block count, and the row's
+          // first piece starts exactly there).
+          HeadStates8 st;
           #pragma unroll
-          for (int h = 0; h < G; ++h) {
-            float res = lt[h] > 0.f ? __fdividef(o[h], lt[h]) : 0.f;
-            if (pc.pre) {
-              float M = m[h], num = lt[h] * res, den = lt[h];
-              fold_prefix(h, M, num, den);
-              res = den > 0.f ? num / den : 0.f;
-            }
-            p.out[out_row + h * kHeadDim + d] = __float2bfloat16_rn(res);
+          for (int h = 0; h < 8; ++h) {
+            st.m[h] = h < G ? m[h] : 0.f;
+            st.l[h] = h < G ? lt[h] : 0.f;
+            st.o[h] = h < G ? o[h] : 0.f;
           }
+          write_prefixed<G>(p.pre_o, p.pre_ml, p.out + out_row + d,
+                            (long long)pc.row * p.num_q_heads + (long long)pc.k * G,
+                            (long long)p.num_q_tokens * p.num_q_heads, pc.fb * kBlockSize, d, st);
+        } else {
+          #pragma unroll
+          for (int h = 0; h < G; ++h)
+            p.out[out_row + h * kHeadDim + d] =
+                __float2bfloat16_rn(lt[h] > 0.f ? __fdividef(o[h], lt[h]) : 0.f);
         }
       } else if (in_range) {
         // Partial piece: normalised output and (max, normaliser), then the
