@@ -78,6 +78,21 @@ def test_cascade_long_prefix_split_suffix():
     _parity(shape, poison=False)
 
 
+def test_cascade_groups_across_batches():
+    """40 sharing groups of two (the prefix pass takes its groups in batches of
+    32, longest shared prefix first within a batch), against plain attention
+    in the oracle."""
+    rng = np.random.default_rng(320)
+    shared = rng.integers(1, 12, size=40)
+    lens, groups = [], []
+    for i, sb in enumerate(shared):
+        lens += [int(sb) * 16 + int(rng.integers(1, 60)) for _ in range(2)]
+        groups.append((2 * i, 2, int(sb)))
+    shape = wl.StepShape("cascade_batches", lens, [1] * len(lens), 16, 2, seed=321,
+                         prefix_groups=tuple(groups))
+    _parity(shape)
+
+
 def test_cascade_member_without_room_falls_back():
     # Requests 0-2 share 5 blocks (80 tokens); request 2's query sits at
     # position 80, right after them.

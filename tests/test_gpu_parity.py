@@ -359,6 +359,23 @@ def test_both_routes_agree_with_oracle(route, pkv_opts):
     _full_parity(shape, poison=True)
 
 
+@pytest.mark.parametrize("g", [4, 2])
+def test_prefill_chunks_across_request_batches(g, pkv_opts):
+    """Prefill chunks in three batches of 32 requests, mixed with decodes and
+    empty rows: the work queue numbers items batch by batch, longest request
+    first within a batch, and every item must still land once."""
+    pkv_opts(prefill_min_q=16)
+    rng = np.random.default_rng(900 + g)
+    R = 80
+    q = rng.integers(16, 70, size=R)
+    q[rng.random(R) < 0.3] = 1                    # decode rows between the chunks
+    q[5] = 0                                      # a row with nothing this step
+    prefix = rng.integers(0, 350, size=R)
+    seq = np.maximum(q + prefix, 1).astype(np.int32)
+    shape = wl.StepShape(f"prefill_batches_g{g}", seq, q.astype(np.int32), g * 2, 2, seed=901 + g)
+    _full_parity(shape, poison=True)
+
+
 def test_prefill_long_prefix_many_key_tiles(pkv_opts):
     pkv_opts(prefill_min_q=16)
     shape = wl.StepShape("longprefix", [4096 + 512, 1000 + 64], [512, 64], 32, 8, seed=42)
