@@ -149,14 +149,6 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
       : "memory");
 }
 
-// Brings `bytes` (a multiple of 16, 16-byte aligned address) of global memory
-// into L2 without waiting for it: a hint only -- L2 stays coherent with every
-// write, so data prefetched before another kernel writes it is never seen
-// stale.
-__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
 // Programmatic dependent launch: wait until the preceding kernel in the
 // stream has completed and its writes are visible (a no-op when the launch
 // had no programmatic dependency), and allow the next kernel to be scheduled.

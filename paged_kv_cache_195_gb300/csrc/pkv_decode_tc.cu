@@ -43,9 +43,9 @@
 // plans before the CTA's set-up, and K/V tiles are evict-first in L2: each
 // is read once); one thread of warp 5 issues the MMAs.  e4m3 pools add warps
 // 6-9 (320 threads), which widen the codes to f16: K tiles into TMEM, V tiles
-// into a shared-memory operand; Q and P are then f16 too.  S and O^T are double buffered in
-// TMEM, so the MMAs of the next piece proceed while the softmax warps finish
-// the previous one.
+// into a shared-memory operand; Q and P are then f16 too.  S and O^T are
+// double buffered in TMEM, so the MMAs of the next piece proceed while the
+// softmax warps finish the previous one.
 // The running maximum is raised only when a score exceeds it by more than
 // 2^8 (a CTA-wide vote), so the common tile needs no cross-thread reduction;
 // O^T is rescaled in TMEM on the rare raise.
