@@ -363,8 +363,6 @@ typedef struct pkv_options {
                                by at most this many blocks */
     int32_t min_chunk;      /* PKV_MIN_CHUNK (4): smallest decode range per CTA, in
                                blocks (>= 1) */
-    int32_t prefetch;       /* PKV_PREFETCH (1): warm L2 with the block-table rows a
-                               decode CTA will read (hints: results do not change) */
     int32_t decode_grid;    /* PKV_DECODE_GRID (0): decode grid in CTAs (0: the
                                default for the kernel and group size; tuning only,
                                at most twice the SM count) */

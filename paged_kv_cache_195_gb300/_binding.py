@@ -36,7 +36,7 @@ EXPORTED = ("pkv_append", "pkv_attention", "pkv_attention_workspace_size",
 # Fields of pkv_options, in declaration order (int32 each).
 OPTION_FIELDS = ("pdl", "early_plan", "early_kv", "early_trigger", "plan_cache", "decode_tc",
                  "decode_tc_fp8", "prefill_min_q", "align", "align_slack", "min_chunk",
-                 "prefetch", "decode_grid", "wait_limit_us", "debug_withhold_q",
+                 "decode_grid", "wait_limit_us", "debug_withhold_q",
                  "rowgroup_cost")
 
 

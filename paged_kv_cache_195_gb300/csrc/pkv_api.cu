@@ -141,7 +141,6 @@ pkv_options options_from_env() {
   o.align = env_int("PKV_ALIGN", 1);
   o.align_slack = env_int("PKV_ALIGN_SLACK", 64);
   o.min_chunk = env_int("PKV_MIN_CHUNK", 4);
-  o.prefetch = env_int("PKV_PREFETCH", 1);
   o.decode_grid = env_int("PKV_DECODE_GRID", 0);
   o.wait_limit_us = env_int("PKV_WAIT_LIMIT_US", (int)(pkv::kDefaultWaitLimitNs / 1000));
   o.debug_withhold_q = 0;  // never from the environment
@@ -523,7 +522,6 @@ int attention_impl(const void* q, const void* k_pool, const void* v_pool, const 
   p.min_chunk = opt.min_chunk;
   p.align = opt.align != 0;
   p.align_slack = opt.align_slack;
-  p.prefetch = opt.prefetch != 0;
   p.early_plan = p.pdl && opt.early_plan != 0;
   p.wait_limit_ns = (unsigned long long)opt.wait_limit_us * 1000ull;
   p.debug_withhold_q = opt.debug_withhold_q != 0;

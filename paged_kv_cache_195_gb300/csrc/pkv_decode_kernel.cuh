@@ -407,7 +407,6 @@ __global__ void __launch_bounds__(DecodeCfg<G>::kThreads) __maxnreg__(DecodeCfg<
 
   if (warp == DecodeCfg<G>::kCW) {
     // ======================= producer warp =================================
-    if (p.prefetch) plan::prefetch_block_table(p, lane);
     plan::Range rg;
     plan::Walker wk;
     plan::plan_cta(p, lane, rg, wk);

@@ -468,7 +468,6 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 2) __maxnreg__
     ent_n1 = have_n && pn.nblk > kWindow ? raw_entries(pn, kWindow) : kPastPiece;
   };
   auto plan_first = [&]() {
-    if (p.prefetch) plan::prefetch_block_table(p, lane);
     plan::plan_cta(p, lane, rg, wk);
     if (lane == 0) TC_CTA(10);
     // the first piece into pn, then into pc with the second into pn (one
@@ -557,9 +556,8 @@ __global__ void __launch_bounds__(F8 ? kTcThreadsF8 : kTcThreads, 2) __maxnreg__
   // Consumers wait for the previous kernel on the stream here; the producer
   // builds its plan and loads its first block-table entries first (it reads
   // only seq_lens, query_start_loc and block_tables, which with early_plan
-  // set the previous kernel does not write; the block-table prefetches are
-  // hints).  Each thread lets the next kernel launch only after its own
-  // wait.
+  // set the previous kernel does not write).  Each thread lets the next
+  // kernel launch only after its own wait.
   //
   // With early_kv the previous kernel is the append of this step's new
   // tokens: before the wait this kernel reads the lengths, the block table

@@ -81,7 +81,6 @@ struct DecodeParams {
   int min_chunk;      // smallest per-CTA range, in blocks
   int align;          // snap ranges to row-group boundaries when lengths are uniform
   int align_slack;    // ... if that lengthens the per-CTA range by at most this many blocks
-  int prefetch;       // warm L2 with the block-table rows this CTA will likely read
   int early_plan;     // plan from seq_lens / query_start_loc before the PDL wait
   // If the step has at most this many blocks per CTA of half the grid, only
   // the first half of the grid takes work (0: the whole grid always does).

@@ -505,18 +505,5 @@ __device__ __forceinline__ void plan_cta(const DecodeParams& p, int lane, Range&
   record();
 }
 
-// Warms L2 with the part of the block table this CTA will probably read (its
-// share of the step if every row were full).
-__device__ __forceinline__ void prefetch_block_table(const DecodeParams& p, int lane) {
-  const long long entries = (long long)p.num_reqs * p.max_blocks;
-  const long long est = entries * blockIdx.x / gridDim.x;
-  const long long line0 = (est * 4) / 128 - 2;
-  const long long lines = (entries * 4 + 127) / 128;
-  const long long line = line0 + lane;
-  if (line >= 0 && line < lines)
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(p.block_tables) +
-                                                 line * 128));
-}
-
 }  // namespace plan
 }  // namespace pkv
