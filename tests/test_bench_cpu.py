@@ -144,3 +144,18 @@ def test_committed_traffic_of_a_two_kernel_call_hashes_its_listed_sources(bench,
         f.write("int another = 2;\n")
     assert bench.committed_traffic("mixed", "bf16") is None    # the code changed
 
+
+
+def test_tensor_roofline_only_for_prefill_only_steps(bench):
+    import paged_kv_cache_195_gb300.roofline as rl
+    from paged_kv_cache_195_gb300 import workloads as wl
+    # a step with decode rows is bounded by HBM: no tensor-core line
+    assert bench.tensor_roofline(wl.llama_mixed(), [0.4]) is None
+    # the eight prefill chunks alone: flops over the mean launch time
+    shape = wl.llama_mixed(num_decode=0)
+    t = bench.tensor_roofline(shape, [0.15, 0.17])
+    flops = rl.attention_flops(shape.seq_lens, shape.q_lens, shape.num_q_heads)
+    assert t["bound"] == "tensor" and t["unit"] == "TFLOP/s"
+    assert t["flops_per_launch"] == flops
+    assert abs(t["achieved"] - flops / 0.16e-3 / 1e12) < 0.1
+    assert abs(t["frac"] - t["achieved"] / t["peak"]) < 1e-3
